@@ -1,0 +1,278 @@
+/*
+ * Oracle for the Ulysses DistributedAttention forward -- TEST INFRASTRUCTURE ONLY.
+ *
+ * Plain, single-threaded, deliberately slow C (fp64 arithmetic, no BLAS, no OpenMP,
+ * no -ffast-math).  It shares no code, header, table or constant with the CUDA library;
+ * only the test suite, the smoke check and the benchmark's CPU-baseline leg call it.
+ *
+ * What it computes, and the passages it follows:
+ *
+ *  - AllToAll, by its definition: every rank cuts its input into P chunks, sends chunk i
+ *    to rank i, and lays the chunks it receives out in the order of the sending rank
+ *    ("大模型分布式训练通信原语及其应用", section 5 "AllToAll（全交换）", definition and
+ *    the two-rank example).
+ *  - All-to-all #1 (seq -> head): each rank splits its [b, s/P, h, d] tensor along the
+ *    head axis into P parts, part j goes to rank j, and each rank concatenates the parts
+ *    it receives along the sequence axis in source-rank order
+ *    ("02 · DeepSpeed-Ulysses", section 2 "all-to-all 的转置与重分布", send/receive
+ *    listing; the batch axis is carried through unchanged).
+ *  - All-to-all #2 (head -> seq): the inverse -- split along the sequence axis, concat
+ *    along the head axis (same page, same section; section 1 figure caption: the two
+ *    exchanges are inverses).
+ *  - Local attention: for every local head, softmax(Q K^T / sqrt(d)) V over the full
+ *    sequence ("DeepSpeed-Ulysses 深度解析", section "核心设计：沿序列切分 + 两次
+ *    All-to-All", step 4), with the causal mask taken on global query/key positions
+ *    ("长上下文训练中的 SP 与 CP", section "Ring Attention：Q 留在本地，KV 沿环传递",
+ *    causal paragraph) and grouped K/V heads: local query head hh reads local K/V head
+ *    hh / (h_q / h_kv).
+ *
+ * Element types for attention inputs: 0 = binary32, 1 = bfloat16 (the upper 16 bits of a
+ * binary32), 2 = binary64.  Decoding is exact; all arithmetic is in double.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORC_OK 0
+#define ORC_BAD_ARG 1
+#define ORC_NO_MEMORY 2
+
+typedef unsigned char u8;
+
+/* ------------------------------------------------------------------ AllToAll */
+
+/* send[i*P + j] is rank i's chunk j; after the call recv[j*P + i] holds it. */
+void orc_all_to_all(int P, size_t chunk_bytes, const void* const* send, void* const* recv) {
+    for (int i = 0; i < P; ++i)
+        for (int j = 0; j < P; ++j)
+            memcpy(recv[(size_t)j * P + i], send[(size_t)i * P + j], chunk_bytes);
+}
+
+/* View x as [outer][n][inner] bytes and cut the middle axis into P equal parts. */
+static void split_middle(const u8* x, size_t outer, size_t n, size_t inner, int P, u8* const* parts) {
+    size_t np = n / (size_t)P;
+    for (int p = 0; p < P; ++p)
+        for (size_t o = 0; o < outer; ++o)
+            memcpy(parts[p] + o * np * inner, x + (o * n + (size_t)p * np) * inner, np * inner);
+}
+
+/* Inverse of split_middle: P parts [outer][np][inner] -> [outer][P*np][inner]. */
+static void concat_middle(const u8* const* parts, int P, size_t outer, size_t np, size_t inner, u8* y) {
+    size_t n = np * (size_t)P;
+    for (int p = 0; p < P; ++p)
+        for (size_t o = 0; o < outer; ++o)
+            memcpy(y + (o * n + (size_t)p * np) * inner, parts[p] + o * np * inner, np * inner);
+}
+
+static u8** alloc_chunks(int P, size_t chunk_bytes) {
+    u8** c = (u8**)calloc((size_t)P * P, sizeof(u8*));
+    if (!c) return NULL;
+    for (size_t i = 0; i < (size_t)P * P; ++i) {
+        c[i] = (u8*)malloc(chunk_bytes ? chunk_bytes : 1);
+        if (!c[i]) {
+            for (size_t k = 0; k < i; ++k) free(c[k]);
+            free(c);
+            return NULL;
+        }
+    }
+    return c;
+}
+
+static void free_chunks(u8** c, int P) {
+    if (!c) return;
+    for (size_t i = 0; i < (size_t)P * P; ++i) free(c[i]);
+    free(c);
+}
+
+static int shape_ok(int P, int b, int s, int h, int d, int e) {
+    return P >= 1 && b >= 0 && s >= 0 && h >= 1 && d >= 1 && e >= 1 && s % P == 0 && h % P == 0;
+}
+
+/*
+ * All-to-all #1: in_seq[j] is rank j's [b][s/P][h][d] tensor (element size e bytes);
+ * out_head[r] receives rank r's [b][s][h/P][d] tensor.
+ */
+int orc_seq2head(int P, int b, int s, int h, int d, int e, const void* const* in_seq, void* const* out_head) {
+    if (!shape_ok(P, b, s, h, d, e)) return ORC_BAD_ARG;
+    size_t S = (size_t)s / P, H = (size_t)h / P;
+    size_t chunk = (size_t)b * S * H * d * e;
+    u8** send = alloc_chunks(P, chunk);
+    u8** recv = alloc_chunks(P, chunk);
+    if (!send || !recv) { free_chunks(send, P); free_chunks(recv, P); return ORC_NO_MEMORY; }
+    /* each rank j: split [b*S][h][d] along heads into P parts [b*S][H][d] */
+    for (int j = 0; j < P; ++j)
+        split_middle((const u8*)in_seq[j], (size_t)b * S, (size_t)h, (size_t)d * e, P, send + (size_t)j * P);
+    orc_all_to_all(P, chunk, (const void* const*)send, (void* const*)recv);
+    /* each rank r: concat the parts from ranks 0..P-1 ([b][S][H*d] each) along seq */
+    for (int r = 0; r < P; ++r)
+        concat_middle((const u8* const*)(recv + (size_t)r * P), P, (size_t)b, S, H * d * e, (u8*)out_head[r]);
+    free_chunks(send, P);
+    free_chunks(recv, P);
+    return ORC_OK;
+}
+
+/*
+ * All-to-all #2: in_head[r] is rank r's [b][s][h/P][d] tensor; out_seq[j] receives rank
+ * j's [b][s/P][h][d] tensor.
+ */
+int orc_head2seq(int P, int b, int s, int h, int d, int e, const void* const* in_head, void* const* out_seq) {
+    if (!shape_ok(P, b, s, h, d, e)) return ORC_BAD_ARG;
+    size_t S = (size_t)s / P, H = (size_t)h / P;
+    size_t chunk = (size_t)b * S * H * d * e;
+    u8** send = alloc_chunks(P, chunk);
+    u8** recv = alloc_chunks(P, chunk);
+    if (!send || !recv) { free_chunks(send, P); free_chunks(recv, P); return ORC_NO_MEMORY; }
+    /* each rank r: split [b][s][H*d] along seq into P parts [b][S][H*d] */
+    for (int r = 0; r < P; ++r)
+        split_middle((const u8*)in_head[r], (size_t)b, (size_t)s, H * d * e, P, send + (size_t)r * P);
+    orc_all_to_all(P, chunk, (const void* const*)send, (void* const*)recv);
+    /* each rank j: concat the parts from ranks 0..P-1 ([b*S][H][d] each) along heads */
+    for (int j = 0; j < P; ++j)
+        concat_middle((const u8* const*)(recv + (size_t)j * P), P, (size_t)b * S, H, (size_t)d * e, (u8*)out_seq[j]);
+    free_chunks(send, P);
+    free_chunks(recv, P);
+    return ORC_OK;
+}
+
+/* ---------------------------------------------------------------- attention */
+
+static double load_elem(const void* base, size_t idx, int dtype) {
+    if (dtype == 0) {
+        float f;
+        memcpy(&f, (const u8*)base + idx * 4, 4);
+        return (double)f;
+    }
+    if (dtype == 1) {
+        uint16_t hbits;
+        memcpy(&hbits, (const u8*)base + idx * 2, 2);
+        uint32_t w = (uint32_t)hbits << 16;
+        float f;
+        memcpy(&f, &w, 4);
+        return (double)f;
+    }
+    double x;
+    memcpy(&x, (const u8*)base + idx * 8, 8);
+    return x;
+}
+
+/*
+ * One query row of softmax(q K^T / sqrt(d)) V.  q_at(c) is element c of the query;
+ * key/value rows j are read through the supplied index of their first element.
+ * Keys j > i are masked when causal.  Writes d doubles to out.  If no key is visible the
+ * row is defined as zero (unreachable for self-attention: the diagonal is visible).
+ */
+static void attend_row(int s, int d, int causal, int i,
+                       const void* qb, size_t q_off, int qdt,
+                       const void* kb, const size_t* k_off, const void* vb, const size_t* v_off, int kvdt,
+                       double* scores, double* out) {
+    double scale = 1.0 / sqrt((double)d);
+    int n = causal ? (i + 1 < s ? i + 1 : s) : s;
+    double m = -INFINITY;
+    for (int j = 0; j < n; ++j) {
+        double acc = 0.0;
+        for (int c = 0; c < d; ++c)
+            acc += load_elem(qb, q_off + (size_t)c, qdt) * load_elem(kb, k_off[j] + (size_t)c, kvdt);
+        scores[j] = acc * scale;
+        if (scores[j] > m) m = scores[j];
+    }
+    for (int c = 0; c < d; ++c) out[c] = 0.0;
+    if (n == 0) return;
+    double l = 0.0;
+    for (int j = 0; j < n; ++j) {
+        double p = exp(scores[j] - m);
+        scores[j] = p;
+        l += p;
+    }
+    for (int j = 0; j < n; ++j) {
+        double w = scores[j] / l;
+        for (int c = 0; c < d; ++c) out[c] += w * load_elem(vb, v_off[j] + (size_t)c, kvdt);
+    }
+}
+
+/*
+ * Local attention of one rank in head layout: q [b][s][hq][d], k/v [b][s][hkv][d],
+ * out [b][s][hq][d] in double.  hq % hkv == 0.
+ */
+int orc_attention(int b, int s, int hq, int hkv, int d, int causal, int dtype,
+                  const void* q, const void* k, const void* v, double* out) {
+    if (b < 0 || s < 0 || hq < 1 || hkv < 1 || d < 1 || hq % hkv) return ORC_BAD_ARG;
+    int g = hq / hkv;
+    double* scores = (double*)malloc(sizeof(double) * (s ? s : 1));
+    size_t* koff = (size_t*)malloc(sizeof(size_t) * (s ? s : 1));
+    size_t* voff = (size_t*)malloc(sizeof(size_t) * (s ? s : 1));
+    if (!scores || !koff || !voff) { free(scores); free(koff); free(voff); return ORC_NO_MEMORY; }
+    for (int bb = 0; bb < b; ++bb)
+        for (int hh = 0; hh < hq; ++hh) {
+            int kh = hh / g;
+            for (int j = 0; j < s; ++j) {
+                koff[j] = (((size_t)bb * s + j) * hkv + kh) * d;
+                voff[j] = koff[j];
+            }
+            for (int i = 0; i < s; ++i) {
+                size_t qo = (((size_t)bb * s + i) * hq + hh) * d;
+                attend_row(s, d, causal, i, q, qo, dtype, k, koff, v, voff, dtype, scores, out + qo);
+            }
+        }
+    free(scores);
+    free(koff);
+    free(voff);
+    return ORC_OK;
+}
+
+/*
+ * Sampled rows of the whole forward, read straight from the seq-partitioned inputs.
+ * Output row n is rank j's O_seq[b][t][gh][:] with (j, b, t, gh) = sample[4n..4n+3].
+ * By all-to-all #2 that row is head-layout rank r = gh / (hq/P), local head gh % (hq/P),
+ * token i = j*s/P + t; by all-to-all #1 its query is Q_seq[j][b][t][gh] and its keys and
+ * values at token i' are rank (i' / (s/P))'s rows i' % (s/P) at kv head
+ * r*(hkv/P) + (gh % (hq/P)) / g.  This is the same pipeline written per element, for
+ * problem sizes whose full fp64 evaluation is out of reach.
+ */
+int orc_dist_attn_rows(int P, int b, int s, int hq, int hkv, int d, int causal, int dtype,
+                       const void* const* q_seq, const void* const* k_seq, const void* const* v_seq,
+                       int n_samples, const int* sample, double* out) {
+    if (P < 1 || s % P || hq % P || hkv % P || hq % hkv || d < 1) return ORC_BAD_ARG;
+    int S = s / P, Hq = hq / P, Hk = hkv / P, g = hq / hkv;
+    double* scores = (double*)malloc(sizeof(double) * (s ? s : 1));
+    if (!scores) return ORC_NO_MEMORY;
+    for (int n = 0; n < n_samples; ++n) {
+        int j = sample[4 * n], bb = sample[4 * n + 1], t = sample[4 * n + 2], gh = sample[4 * n + 3];
+        if (j < 0 || j >= P || bb < 0 || bb >= b || t < 0 || t >= S || gh < 0 || gh >= hq) {
+            free(scores);
+            return ORC_BAD_ARG;
+        }
+        int r = gh / Hq, hh = gh % Hq;
+        int kv_head = r * Hk + hh / g;
+        int i = j * S + t;
+        int nvis = causal ? i + 1 : s;
+        const void* qb = q_seq[j];
+        size_t qo = (((size_t)bb * S + t) * hq + gh) * d;
+        double scale = 1.0 / sqrt((double)d);
+        double m = -INFINITY;
+        for (int jj = 0; jj < nvis; ++jj) {
+            int src = jj / S, tt = jj % S;
+            size_t ko = (((size_t)bb * S + tt) * hkv + kv_head) * d;
+            double acc = 0.0;
+            for (int c = 0; c < d; ++c)
+                acc += load_elem(qb, qo + (size_t)c, dtype) * load_elem(k_seq[src], ko + (size_t)c, dtype);
+            scores[jj] = acc * scale;
+            if (scores[jj] > m) m = scores[jj];
+        }
+        double l = 0.0;
+        for (int jj = 0; jj < nvis; ++jj) {
+            scores[jj] = exp(scores[jj] - m);
+            l += scores[jj];
+        }
+        double* o = out + (size_t)n * d;
+        for (int c = 0; c < d; ++c) o[c] = 0.0;
+        for (int jj = 0; jj < nvis; ++jj) {
+            int src = jj / S, tt = jj % S;
+            size_t vo = (((size_t)bb * S + tt) * hkv + kv_head) * d;
+            double w = scores[jj] / l;
+            for (int c = 0; c < d; ++c) o[c] += w * load_elem(v_seq[src], vo + (size_t)c, dtype);
+        }
+    }
+    free(scores);
+    return ORC_OK;
+}
