@@ -1,0 +1,142 @@
+/*
+ * ulysses.h -- C ABI of the GB300 (sm_103a) Ulysses DistributedAttention forward.
+ *
+ * The method ("DeepSpeed-Ulysses 深度解析：用 All-to-All 序列并行撑起百万 Token 超长序列训练",
+ * section "核心设计：沿序列切分 + 两次 All-to-All", steps 1-5): each of P sequence-parallel
+ * ranks holds a contiguous block of s/P tokens of Q, K and V with all heads; all-to-all #1
+ * turns that into all s tokens of h/P heads; every rank runs ordinary attention
+ * softmax(Q K^T / sqrt(d)) V on its heads; all-to-all #2 restores the sequence split.
+ *
+ * On one GPU the P ranks are P disjoint device buffers, so each all-to-all is a transpose
+ * in device memory.  Layouts (row-major, batch first, element type `uly_dtype`):
+ *     seq layout  (rank j):  [b][s/P][h][d]   tokens j*s/P .. (j+1)*s/P-1, all heads
+ *     head layout (rank r):  [b][s][h/P][d]   all tokens, heads r*h/P .. (r+1)*h/P-1
+ * Token blocks and head groups are contiguous and ordered by rank ("02 · DeepSpeed-Ulysses",
+ * section 2 "all-to-all 的转置与重分布": split the head axis, part j to rank j, concatenate
+ * what arrives along the sequence axis).
+ *
+ * Common rules for every entry point:
+ *  - Pointer arrays (`const void* const* x`) are HOST arrays of P DEVICE pointers, one per
+ *    rank, read only during the call.  Every device pointer must be 16-byte aligned.
+ *  - The caller owns all device memory and the stream.  The library allocates no device
+ *    memory, keeps no per-call state, and may be called from several host threads.
+ *  - Calls only enqueue work on `stream` and return; a kernel fault surfaces through the
+ *    usual CUDA error checks on that stream.  Argument errors are reported before any
+ *    work is enqueued, and nothing is written in that case.
+ *  - Outputs must not overlap inputs (out-of-place only); this is checked.
+ *  - Return value: ULY_OK, or the first error found (see uly_status).
+ */
+#ifndef ULYSSES_GB300_H
+#define ULYSSES_GB300_H
+
+#include <stddef.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    ULY_OK = 0,
+    ULY_ERR_INVALID_ARG = 1, /* bad sizes or divisibility, null/misaligned/overlapping pointers, small workspace */
+    ULY_ERR_UNSUPPORTED = 2, /* valid arguments for which no kernel exists (dtype/d combination, fused shape) */
+    ULY_ERR_CUDA = 3,        /* a CUDA runtime/driver call or a kernel launch failed */
+    ULY_ERR_TIMEOUT = 4      /* a bounded device-side wait gave up (reported by ulysses_device_status) */
+} uly_status;
+
+typedef enum {
+    ULY_FP32 = 0, /* IEEE binary32 inputs and outputs, fp32 arithmetic throughout (no TF32) */
+    ULY_BF16 = 1  /* bfloat16 inputs and outputs, fp32 accumulation and softmax */
+} uly_dtype;
+
+/*
+ * All-to-all #1, sequence -> head ("02 · DeepSpeed-Ulysses", section 2, send/receive
+ * listing; "DeepSpeed-Ulysses 深度解析", step 3).
+ *   out_head[r][bb][j*s/P + t][hh][:] = in_seq[j][bb][t][r*h/P + hh][:]
+ * for every rank r, source rank j, batch bb < b, token t < s/P, head hh < h/P.
+ * Sizes: 1 <= P <= 64, b >= 1, s >= 1, h >= 1, d >= 1, s % P == 0, h % P == 0.
+ * in_seq: P pointers to [b][s/P][h][d]; out_head: P pointers to [b][s][h/P][d].
+ * A pure bit copy (dtype only fixes the element size), so the result is bit-exact.
+ */
+uly_status ulysses_a2a_seq2head(int P, int b, int s, int h, int d, uly_dtype dtype,
+                                const void* const* in_seq, void* const* out_head,
+                                cudaStream_t stream);
+
+/*
+ * All-to-all #2, head -> sequence: the inverse of ulysses_a2a_seq2head ("02 ·
+ * DeepSpeed-Ulysses", section 2, last paragraph; section 1 figure caption).
+ *   out_seq[j][bb][t][r*h/P + hh][:] = in_head[r][bb][j*s/P + t][hh][:]
+ * in_head: P pointers to [b][s][h/P][d]; out_seq: P pointers to [b][s/P][h][d].
+ * Same size rules as ulysses_a2a_seq2head; bit-exact.
+ */
+uly_status ulysses_a2a_head2seq(int P, int b, int s, int h, int d, uly_dtype dtype,
+                                const void* const* in_head, void* const* out_seq,
+                                cudaStream_t stream);
+
+/*
+ * Local attention of every rank, head layout in and out ("DeepSpeed-Ulysses 深度解析",
+ * step 4: softmax(Q K^T / sqrt(d)) V per local head over the full sequence).
+ *   o_head[r][bb][i][hh][:] = sum_j softmax_j(q.k_j / sqrt(d)) v_j
+ * with q = q_head[r][bb][i][hh], k_j / v_j = k_head / v_head[r][bb][j][hh / (h_q/h_kv)].
+ * causal != 0 masks keys j > i (global positions: after all-to-all #1 the local token
+ * index is the global one -- "长上下文训练中的 SP 与 CP", section on Ring Attention,
+ * causal paragraph).  The scale is fixed at 1/sqrt(d).
+ * Sizes: P, b, s >= 1; h_q % P == 0, h_kv % P == 0, h_q % h_kv == 0 (grouped K/V heads:
+ * rank r's query heads read only its own K/V heads -- "02 · DeepSpeed-Ulysses", section 3).
+ * q_head / o_head: P pointers to [b][s][h_q/P][d]; k_head / v_head: P pointers to
+ * [b][s][h_kv/P][d].
+ * Kernels: ULY_BF16 with d in {64, 128} (tcgen05 tensor cores, fp32 accumulation, the
+ * softmax weights rounded to bf16 before the P.V product, output rounded to nearest even);
+ * ULY_FP32 with d % 4 == 0 and d <= 256 (fp32 FMA, no tensor cores).  Other combinations
+ * return ULY_ERR_UNSUPPORTED.  Any s is accepted (ragged tiles are masked).
+ */
+uly_status ulysses_local_attention(int P, int b, int s, int h_q, int h_kv, int d, uly_dtype dtype,
+                                   int causal,
+                                   const void* const* q_head, const void* const* k_head,
+                                   const void* const* v_head, void* const* o_head,
+                                   cudaStream_t stream);
+
+/*
+ * Bytes of device workspace ulysses_dist_attn_fwd needs for these arguments: the
+ * head-layout copies of Q, K, V and O of every rank (each 256-byte aligned) when
+ * fused == 0, and 0 when fused != 0.  Returns 0 for arguments that are invalid.
+ */
+size_t ulysses_dist_attn_workspace_bytes(int P, int b, int s, int h_q, int h_kv, int d,
+                                         uly_dtype dtype, int fused);
+
+/*
+ * The whole DistributedAttention forward ("DeepSpeed-Ulysses 深度解析", steps 3-5):
+ * all-to-all #1 on Q, K and V, local attention on every rank, all-to-all #2 on the output.
+ *   q_seq / o_seq: P pointers to [b][s/P][h_q][d]; k_seq / v_seq: P pointers to
+ *   [b][s/P][h_kv][d].  Size rules as ulysses_local_attention.
+ * fused == 0: three launches (one for the Q, K and V exchanges, one attention, one
+ *   output exchange) through `workspace` (device memory, 256-byte aligned, at least
+ *   ulysses_dist_attn_workspace_bytes(...) bytes, owned by the caller).
+ * fused != 0: one launch; the attention kernel reads its Q/K/V tiles straight from the
+ *   seq-layout buffers and stores its output tiles straight into o_seq, so no
+ *   head-layout copy exists.  Needs ULY_BF16, d in {64, 128}, P <= 16 and
+ *   (s/P) % 128 == 0, else ULY_ERR_UNSUPPORTED.  workspace may be NULL.
+ * Both paths give the same bits for the same inputs.
+ */
+uly_status ulysses_dist_attn_fwd(int P, int b, int s, int h_q, int h_kv, int d, uly_dtype dtype,
+                                 int causal,
+                                 const void* const* q_seq, const void* const* k_seq,
+                                 const void* const* v_seq, void* const* o_seq,
+                                 void* workspace, size_t workspace_bytes, int fused,
+                                 cudaStream_t stream);
+
+/*
+ * Reads (and, if clear != 0, resets) the library's device-side error word after
+ * synchronising the current device.  Returns ULY_ERR_TIMEOUT if a kernel's bounded wait
+ * gave up since the last reset (that kernel then wrote no output), ULY_ERR_CUDA if the
+ * device could not be queried, ULY_OK otherwise.
+ */
+uly_status ulysses_device_status(int clear);
+
+/* Static, human-readable name of a status code. */
+const char* ulysses_status_string(uly_status status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* ULYSSES_GB300_H */

@@ -1,0 +1,204 @@
+"""GB300 (sm_103a) Ulysses DistributedAttention forward: Python binding of the C ABI.
+
+The binding only marshals arguments: it reads shapes from the tensors, allocates outputs
+and workspace with PyTorch, and calls the functions of ``libulysses_gb300.so`` (declared
+in ``include/ulysses.h``) on the current CUDA stream.  Every step of the computation runs
+in the library's kernels; there is no fallback.  If the library is missing or cannot be
+loaded, every call raises.
+
+Layouts (per rank, row-major): seq layout ``[b, s/P, h, d]``, head layout
+``[b, s, h/P, d]``.  A list of P tensors stands for the P sequence-parallel ranks.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+__all__ = [
+    "UlyssesError", "library_path", "load_library",
+    "ulysses_a2a_seq2head", "ulysses_a2a_head2seq", "ulysses_local_attention",
+    "ulysses_dist_attn_workspace_bytes", "ulysses_dist_attn_fwd", "ulysses_device_status",
+    "ulysses_status_string", "EXPORTED_SYMBOLS",
+]
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_NAME = "libulysses_gb300.so"
+
+ULY_OK, ULY_ERR_INVALID_ARG, ULY_ERR_UNSUPPORTED, ULY_ERR_CUDA, ULY_ERR_TIMEOUT = range(5)
+_DTYPES = {torch.float32: 0, torch.bfloat16: 1}
+
+# every function include/ulysses.h declares
+EXPORTED_SYMBOLS = (
+    "ulysses_a2a_seq2head", "ulysses_a2a_head2seq", "ulysses_local_attention",
+    "ulysses_dist_attn_workspace_bytes", "ulysses_dist_attn_fwd", "ulysses_device_status",
+    "ulysses_status_string",
+)
+
+_lock = threading.Lock()
+_lib = None
+
+
+class UlyssesError(RuntimeError):
+    def __init__(self, status, what):
+        self.status = status
+        super().__init__(f"{what}: {_status_name(status)}")
+
+
+def library_path():
+    return os.path.join(_PKG, _LIB_NAME)
+
+
+def load_library():
+    """Load the C-ABI library (built by ``build.py``); raises if it is absent."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError(f"{_LIB_NAME} is not built (run sequence_attention_seq_gb300/build.py); "
+                               "this package has no CPU fallback")
+        lib = ctypes.CDLL(path)
+        vp, sz, i = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int
+        pp = ctypes.POINTER(ctypes.c_void_p)
+        for name in ("ulysses_a2a_seq2head", "ulysses_a2a_head2seq"):
+            f = getattr(lib, name)
+            f.argtypes = [i, i, i, i, i, i, pp, pp, vp]
+            f.restype = i
+        lib.ulysses_local_attention.argtypes = [i, i, i, i, i, i, i, i, pp, pp, pp, pp, vp]
+        lib.ulysses_local_attention.restype = i
+        lib.ulysses_dist_attn_workspace_bytes.argtypes = [i, i, i, i, i, i, i, i]
+        lib.ulysses_dist_attn_workspace_bytes.restype = sz
+        lib.ulysses_dist_attn_fwd.argtypes = [i, i, i, i, i, i, i, i, pp, pp, pp, pp, vp, sz, i, vp]
+        lib.ulysses_dist_attn_fwd.restype = i
+        lib.ulysses_device_status.argtypes = [i]
+        lib.ulysses_device_status.restype = i
+        lib.ulysses_status_string.argtypes = [i]
+        lib.ulysses_status_string.restype = ctypes.c_char_p
+        _lib = lib
+        return lib
+
+
+def _status_name(status):
+    try:
+        return load_library().ulysses_status_string(int(status)).decode()
+    except Exception:  # noqa: BLE001 - naming an error must not raise another
+        return f"status {status}"
+
+
+def ulysses_status_string(status):
+    return load_library().ulysses_status_string(int(status)).decode()
+
+
+def _check(status, what):
+    if status != ULY_OK:
+        raise UlyssesError(status, what)
+
+
+def _ptr_array(tensors):
+    arr = (ctypes.c_void_p * len(tensors))()
+    for n, t in enumerate(tensors):
+        arr[n] = t.data_ptr()
+    return arr
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dtype_code(t):
+    if t.dtype not in _DTYPES:
+        raise TypeError(f"unsupported dtype {t.dtype}")
+    return _DTYPES[t.dtype]
+
+
+def _same(tensors, what):
+    t0 = tensors[0]
+    for t in tensors:
+        if t.shape != t0.shape or t.dtype != t0.dtype or t.device != t0.device or not t.is_contiguous():
+            raise ValueError(f"{what}: every rank needs a contiguous tensor of one shape, dtype and device")
+        if t.device.type != "cuda":
+            raise ValueError(f"{what}: tensors must live on a CUDA device")
+    return t0
+
+
+def ulysses_a2a_seq2head(in_seq, out_head=None, stream=None):
+    """All-to-all #1: P tensors [b, s/P, h, d] -> P tensors [b, s, h/P, d]."""
+    t0 = _same(in_seq, "in_seq")
+    P = len(in_seq)
+    b, S, h, d = t0.shape
+    if out_head is None:
+        out_head = [torch.empty((b, S * P, h // P, d), dtype=t0.dtype, device=t0.device) for _ in range(P)]
+    _same(out_head, "out_head")
+    _check(load_library().ulysses_a2a_seq2head(P, b, S * P, h, d, _dtype_code(t0), _ptr_array(in_seq),
+                                               _ptr_array(out_head), _stream(stream)), "ulysses_a2a_seq2head")
+    return out_head
+
+
+def ulysses_a2a_head2seq(in_head, out_seq=None, stream=None):
+    """All-to-all #2: P tensors [b, s, h/P, d] -> P tensors [b, s/P, h, d]."""
+    t0 = _same(in_head, "in_head")
+    P = len(in_head)
+    b, s, H, d = t0.shape
+    if out_seq is None:
+        out_seq = [torch.empty((b, s // P, H * P, d), dtype=t0.dtype, device=t0.device) for _ in range(P)]
+    _same(out_seq, "out_seq")
+    _check(load_library().ulysses_a2a_head2seq(P, b, s, H * P, d, _dtype_code(t0), _ptr_array(in_head),
+                                               _ptr_array(out_seq), _stream(stream)), "ulysses_a2a_head2seq")
+    return out_seq
+
+
+def ulysses_local_attention(q_head, k_head, v_head, causal, out_head=None, stream=None):
+    """Attention of every rank in head layout: softmax(Q K^T / sqrt(d)) V per local head."""
+    q0 = _same(q_head, "q_head")
+    k0 = _same(k_head, "k_head")
+    _same(v_head, "v_head")
+    P = len(q_head)
+    b, s, Hq, d = q0.shape
+    Hk = k0.shape[2]
+    if out_head is None:
+        out_head = [torch.empty_like(q) for q in q_head]
+    _check(load_library().ulysses_local_attention(
+        P, b, s, Hq * P, Hk * P, d, _dtype_code(q0), int(bool(causal)), _ptr_array(q_head), _ptr_array(k_head),
+        _ptr_array(v_head), _ptr_array(out_head), _stream(stream)), "ulysses_local_attention")
+    return out_head
+
+
+def ulysses_dist_attn_workspace_bytes(P, b, s, h_q, h_kv, d, dtype, fused):
+    return int(load_library().ulysses_dist_attn_workspace_bytes(P, b, s, h_q, h_kv, d, _DTYPES[dtype], int(bool(fused))))
+
+
+def ulysses_dist_attn_fwd(q_seq, k_seq, v_seq, causal, fused=False, out_seq=None, workspace=None, stream=None):
+    """The whole forward: all-to-all #1 (Q, K, V), attention, all-to-all #2.
+
+    q_seq / k_seq / v_seq: P tensors [b, s/P, heads, d]; returns P tensors [b, s/P, h_q, d].
+    ``workspace`` (a uint8 CUDA tensor) is allocated when not given and fused is False.
+    """
+    q0 = _same(q_seq, "q_seq")
+    k0 = _same(k_seq, "k_seq")
+    _same(v_seq, "v_seq")
+    P = len(q_seq)
+    b, S, hq, d = q0.shape
+    hkv = k0.shape[2]
+    s = S * P
+    if out_seq is None:
+        out_seq = [torch.empty_like(q) for q in q_seq]
+    need = ulysses_dist_attn_workspace_bytes(P, b, s, hq, hkv, d, q0.dtype, fused)
+    if workspace is None and need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q0.device)
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_len = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(load_library().ulysses_dist_attn_fwd(
+        P, b, s, hq, hkv, d, _dtype_code(q0), int(bool(causal)), _ptr_array(q_seq), _ptr_array(k_seq),
+        _ptr_array(v_seq), _ptr_array(out_seq), ws_ptr, ws_len, int(bool(fused)), _stream(stream)),
+        "ulysses_dist_attn_fwd")
+    return out_seq
+
+
+def ulysses_device_status(clear=True):
+    """Synchronise and report (and by default clear) the device-side error word."""
+    return int(load_library().ulysses_device_status(int(bool(clear))))

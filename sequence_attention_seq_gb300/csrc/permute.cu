@@ -1,0 +1,162 @@
+// All-to-all #1 (seq -> head) and #2 (head -> seq) of the Ulysses forward as transposes
+// between P per-rank buffers in one device's memory.
+//
+// "02 · DeepSpeed-Ulysses", section 2 "all-to-all 的转置与重分布": rank j splits its
+// [s/P, h, d] block along heads, part r goes to rank r, and rank r concatenates the parts
+// along the sequence axis in source-rank order.  With batch first:
+//     head[r][bb][j*S + t][hh][:] == seq[j][bb][t][r*H + hh][:]     (S = s/P, H = h/P)
+// For every (rank r, source rank j, batch bb) the head-layout side is one contiguous slab
+// of S rows of H*d elements, and the seq-layout side is S runs of H*d elements with a
+// pitch of h*d elements.  The kernel streams those slabs with 16-byte (or narrower)
+// vector loads and stores: the contiguous side is fully coalesced, the strided side moves
+// whole runs (>= 128 bytes for every supported bf16/fp32 shape with d >= 64).
+#include "device_common.cuh"
+#include "internal.h"
+
+namespace uly {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kUnroll = 4;
+
+struct PermuteJob {
+    const uint8_t* src[kMaxRanks];
+    uint8_t* dst[kMaxRanks];
+    uint64_t run_bytes;   // H*d*e: one contiguous run on the seq-layout side
+    uint64_t row_pitch;   // h*d*e: seq-layout row pitch
+    uint32_t slab_vecs;   // S*run_bytes / VEC
+    FastDiv run_vecs;     // run_bytes / VEC
+};
+
+struct PermuteParams {
+    PermuteJob job[3];
+    uint32_t ntensors;
+    uint32_t units;  // P*P*b slabs per tensor
+    uint32_t P, S, s;
+};
+
+template <int VEC>
+struct VecT;
+template <>
+struct VecT<16> { using T = uint4; };
+template <>
+struct VecT<8> { using T = uint2; };
+template <>
+struct VecT<4> { using T = uint32_t; };
+template <>
+struct VecT<2> { using T = uint16_t; };
+template <>
+struct VecT<1> { using T = uint8_t; };
+
+template <typename T>
+__device__ __forceinline__ T load_stream(const uint8_t* p) {
+    return __ldcs(reinterpret_cast<const T*>(p));
+}
+template <>
+__device__ __forceinline__ uint8_t load_stream<uint8_t>(const uint8_t* p) {
+    return *reinterpret_cast<const volatile uint8_t*>(p);
+}
+
+// DIR 0: seq -> head (read strided, write contiguous); DIR 1: head -> seq (the reverse).
+template <int VEC, int DIR>
+__global__ void __launch_bounds__(kThreads) permute_kernel(const __grid_constant__ PermuteParams p) {
+    using V = typename VecT<VEC>::T;
+    const uint32_t P = p.P;
+    for (uint32_t yu = blockIdx.y; yu < p.ntensors * p.units; yu += gridDim.y) {
+        const uint32_t t = yu / p.units;
+        const uint32_t u = yu - t * p.units;
+        const uint32_t j = u % P;  // seq-layout rank (token block j)
+        const uint32_t rest = u / P;
+        const uint32_t r = rest % P;  // head-layout rank (head group r)
+        const uint32_t bb = rest / P;
+        const PermuteJob& J = p.job[t];
+        const uint64_t off_contig = ((uint64_t)bb * p.s + (uint64_t)j * p.S) * J.run_bytes;
+        const uint64_t off_strided = (uint64_t)bb * p.S * J.row_pitch + (uint64_t)r * J.run_bytes;
+        const uint8_t* src = DIR == 0 ? J.src[j] + off_strided : J.src[r] + off_contig;
+        uint8_t* dst = DIR == 0 ? J.dst[r] + off_contig : J.dst[j] + off_strided;
+        const uint32_t n = J.slab_vecs;
+        for (uint32_t i0 = blockIdx.x * (kThreads * kUnroll) + threadIdx.x; i0 < n;
+             i0 += gridDim.x * (kThreads * kUnroll)) {
+            V val[kUnroll];
+            uint64_t so[kUnroll], co[kUnroll];
+#pragma unroll
+            for (int k = 0; k < kUnroll; ++k) {
+                const uint32_t i = i0 + k * kThreads;
+                const uint32_t row = fdiv(i, J.run_vecs);
+                const uint32_t col = i - row * J.run_vecs.d;
+                so[k] = (uint64_t)row * J.row_pitch + (uint64_t)col * VEC;
+                co[k] = (uint64_t)i * VEC;
+                if (i < n) val[k] = load_stream<V>(DIR == 0 ? src + so[k] : src + co[k]);
+            }
+#pragma unroll
+            for (int k = 0; k < kUnroll; ++k) {
+                const uint32_t i = i0 + k * kThreads;
+                if (i < n) *reinterpret_cast<V*>(DIR == 0 ? dst + co[k] : dst + so[k]) = val[k];
+            }
+        }
+    }
+}
+
+template <int VEC>
+cudaError_t launch_vec(int direction, const PermuteParams& prm, uint32_t max_slab, cudaStream_t stream) {
+    const uint32_t ys = prm.ntensors * prm.units;
+    const uint32_t grid_y = ys < 65535u ? ys : 65535u;
+    const uint64_t per_unit = (max_slab + (uint64_t)kThreads * kUnroll - 1) / ((uint64_t)kThreads * kUnroll);
+    int dev = 0, sms = 152;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    // one full wave of 8 resident 256-thread blocks per SM, spread over the slabs
+    const uint64_t target = (uint64_t)sms * 8;
+    uint64_t gx = (target + grid_y - 1) / grid_y;
+    if (gx > per_unit) gx = per_unit;
+    if (gx < 1) gx = 1;
+    if (gx > 65535) gx = 65535;
+    dim3 grid((unsigned)gx, grid_y, 1);
+    if (direction == 0)
+        permute_kernel<VEC, 0><<<grid, kThreads, 0, stream>>>(prm);
+    else
+        permute_kernel<VEC, 1><<<grid, kThreads, 0, stream>>>(prm);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_permute(int direction, int P, int b, int s, int d, int elem_bytes, const PermuteTensor* tensors,
+                           int ntensors, cudaStream_t stream) {
+    PermuteParams prm;
+    memset(&prm, 0, sizeof(prm));
+    prm.ntensors = (uint32_t)ntensors;
+    prm.P = (uint32_t)P;
+    prm.S = (uint32_t)(s / P);
+    prm.s = (uint32_t)s;
+    prm.units = (uint32_t)P * (uint32_t)P * (uint32_t)b;
+    // widest vector that divides every run (all pointers are 16-byte aligned by contract)
+    int vec = 16;
+    for (int t = 0; t < ntensors; ++t) {
+        const uint64_t run = (uint64_t)(tensors[t].h / P) * d * elem_bytes;
+        while (vec > 1 && run % vec) vec >>= 1;
+    }
+    uint32_t max_slab = 0;
+    for (int t = 0; t < ntensors; ++t) {
+        PermuteJob& J = prm.job[t];
+        for (int r = 0; r < P; ++r) {
+            J.src[r] = static_cast<const uint8_t*>(tensors[t].src[r]);
+            J.dst[r] = static_cast<uint8_t*>(tensors[t].dst[r]);
+        }
+        J.run_bytes = (uint64_t)(tensors[t].h / P) * d * elem_bytes;
+        J.row_pitch = (uint64_t)tensors[t].h * d * elem_bytes;
+        J.slab_vecs = (uint32_t)((uint64_t)prm.S * J.run_bytes / vec);
+        J.run_vecs = make_fastdiv((uint32_t)(J.run_bytes / vec));
+        if (J.slab_vecs > max_slab) max_slab = J.slab_vecs;
+    }
+    if (max_slab == 0) return cudaSuccess;
+    switch (vec) {
+        case 16: return launch_vec<16>(direction, prm, max_slab, stream);
+        case 8: return launch_vec<8>(direction, prm, max_slab, stream);
+        case 4: return launch_vec<4>(direction, prm, max_slab, stream);
+        case 2: return launch_vec<2>(direction, prm, max_slab, stream);
+        default: return launch_vec<1>(direction, prm, max_slab, stream);
+    }
+}
+
+}  // namespace uly

@@ -1,0 +1,104 @@
+"""Host-side checks of the C ABI (no GPU needed): the library loads, exports every function
+include/ulysses.h declares, and rejects bad arguments before it touches the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import sequence_attention_seq_gb300 as uly
+from sequence_attention_seq_gb300 import build as uly_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ulysses.h")
+
+INVALID, UNSUPPORTED = 1, 2
+FP32, BF16 = 0, 1
+
+
+@pytest.fixture(scope="module")
+def lib():
+    uly_build.build()
+    return uly.load_library()
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(ulysses_\w+)\s*\(", text)))
+
+
+def test_header_declares_and_library_exports(lib):
+    names = _declared()
+    assert sorted(uly.EXPORTED_SYMBOLS) == names
+    for n in names:
+        assert hasattr(lib, n), f"{n} not exported"
+
+
+def _arr(*vals):
+    a = (ctypes.c_void_p * len(vals))()
+    for i, v in enumerate(vals):
+        a[i] = v
+    return a
+
+
+# fake, never dereferenced device addresses: validation fails before any CUDA call
+A, B, C, D = 0x10000000, 0x20000000, 0x30000000, 0x40000000
+
+
+def test_exchange_argument_errors(lib):
+    f = lib.ulysses_a2a_seq2head
+    ok_in, ok_out = _arr(A, B), _arr(C, D)
+    assert f(0, 1, 64, 4, 16, FP32, ok_in, ok_out, None) == INVALID           # P < 1
+    assert f(65, 1, 65 * 2, 65, 16, FP32, ok_in, ok_out, None) == INVALID     # P > 64
+    assert f(2, 1, 63, 4, 16, FP32, ok_in, ok_out, None) == INVALID           # s % P
+    assert f(2, 1, 64, 3, 16, FP32, ok_in, ok_out, None) == INVALID           # h % P
+    assert f(2, 1, 64, 4, 16, 7, ok_in, ok_out, None) == INVALID              # dtype
+    assert f(2, 1, 64, 4, 16, FP32, _arr(A, 0), ok_out, None) == INVALID      # null
+    assert f(2, 1, 64, 4, 16, FP32, _arr(A, B + 4), ok_out, None) == INVALID  # misaligned
+    assert f(2, 1, 64, 4, 16, FP32, ok_in, _arr(C, A + 64), None) == INVALID  # out overlaps in
+    assert f(2, 1, 64, 4, 16, FP32, ok_in, _arr(C, C + 64), None) == INVALID  # outputs overlap
+    g = lib.ulysses_a2a_head2seq
+    assert g(2, 1, 64, 4, 16, FP32, ok_in, _arr(C, A), None) == INVALID
+
+
+def test_attention_argument_errors(lib):
+    f = lib.ulysses_local_attention
+    q, k, v, o = _arr(A), _arr(B), _arr(C), _arr(D)
+    assert f(1, 1, 64, 4, 3, 16, FP32, 0, q, k, v, o, None) == INVALID        # h_q % h_kv
+    assert f(2, 1, 64, 4, 1, 16, FP32, 0, _arr(A, A + 0x1000000), _arr(B, B + 0x1000000),
+             _arr(C, C + 0x1000000), _arr(D, D + 0x1000000), None) == INVALID  # h_kv % P
+    assert f(1, 1, 64, 4, 4, 96, BF16, 0, q, k, v, o, None) == UNSUPPORTED    # bf16 needs d in {64,128}
+    assert f(1, 1, 64, 4, 4, 6, FP32, 0, q, k, v, o, None) == UNSUPPORTED     # fp32 needs d % 4 == 0
+    assert f(1, 1, 64, 4, 4, 260, FP32, 0, q, k, v, o, None) == UNSUPPORTED   # fp32 needs d <= 256
+    assert f(1, 1, 64, 4, 4, 16, FP32, 0, q, k, v, _arr(A + 256), None) == INVALID  # o overlaps q
+
+
+def test_dist_attn_errors_and_workspace(lib):
+    ws = lib.ulysses_dist_attn_workspace_bytes
+    e = 2
+    P, b, s, hq, hkv, d = 4, 2, 4096, 32, 8, 128
+    qh = b * s * (hq // P) * d * e
+    kh = b * s * (hkv // P) * d * e
+    assert ws(P, b, s, hq, hkv, d, BF16, 0) == P * (2 * qh + 2 * kh)
+    assert ws(P, b, s, hq, hkv, d, BF16, 1) == 0
+    assert ws(3, b, s, hq, hkv, d, BF16, 0) == 0  # invalid: h_q % P
+    f = lib.ulysses_dist_attn_fwd
+    qs = _arr(*[A + i * 0x1000000 for i in range(4)])
+    ks = _arr(*[B + i * 0x1000000 for i in range(4)])
+    vs = _arr(*[C + i * 0x1000000 for i in range(4)])
+    os_ = _arr(*[D + i * 0x1000000 for i in range(4)])
+    need = ws(P, b, s, hq, hkv, d, BF16, 0)
+    wsp = 0x100000000
+    assert f(P, b, s, hq, hkv, d, BF16, 0, qs, ks, vs, os_, None, need, 0, None) == INVALID   # no workspace
+    assert f(P, b, s, hq, hkv, d, BF16, 0, qs, ks, vs, os_, wsp, need - 1, 0, None) == INVALID  # too small
+    assert f(P, b, s, hq, hkv, d, BF16, 0, qs, ks, vs, os_, wsp + 16, need, 0, None) == INVALID  # 256-B align
+    assert f(P, b, 4 * 96, hq, hkv, d, BF16, 1, qs, ks, vs, os_, None, 0, 1, None) == UNSUPPORTED  # (s/P)%128
+    assert f(P, b, s, hq, hkv, 64, FP32, 1, qs, ks, vs, os_, None, 0, 1, None) == UNSUPPORTED     # fused fp32
+    assert f(P, b, s, hq, hkv, 96, BF16, 1, qs, ks, vs, os_, None, 0, 1, None) == UNSUPPORTED     # d
+
+
+def test_status_strings(lib):
+    for code, name in enumerate(["ULY_OK", "ULY_ERR_INVALID_ARG", "ULY_ERR_UNSUPPORTED", "ULY_ERR_CUDA",
+                                 "ULY_ERR_TIMEOUT"]):
+        assert uly.ulysses_status_string(code) == name
