@@ -1,0 +1,370 @@
+"""Benchmark of the Ulysses DistributedAttention forward on GB300.
+
+One step = one pass of the whole hot path over the DiT-like workload (P=4 virtual ranks,
+b=2, s=4096, h=32, d=128, bf16 N(0,1)), for both the non-causal and the causal mask:
+    all-to-all #1 on Q, K, V  ->  local attention  ->  all-to-all #2 on O   (unfused)
+    the fused kernel (exchanges folded into the attention tiles)             (fused)
+Every kernel launch is bracketed by CUDA events on the launching stream.
+
+value   = algorithmic attention FLOP of the step / step time (TFLOP/s), whole job.
+roofline = the attention kernel against the measured bf16 tensor peak.
+e2e     = the same metric with host buffers: per step the pinned-host Q/K/V go to the
+          device, the forward runs through the public API, the outputs come back.
+cpu_baseline / --impl reference = the fp64 CPU oracle on a bounded sample of the workload.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+Multi-GPU (torchrun): every rank runs an independent replica (the path needs no exchange
+between GPUs on this single-GPU emulation); value sums ranks over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "Ulysses attn fwd TFLOP/s + a2a permute GB/s, as fraction of GB300 roofline"
+WORKLOAD = dict(P=4, b=2, s=4096, h_q=32, h_kv=32, d=128)
+WORKLOAD_NAME = "DiT-like MHA: P=4 b=2 s=4096 h=32 d=128 bf16, non-causal + causal, unfused + fused forward"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def attn_flops(b, s, hq, d, causal):
+    """Algorithmic FLOP of attention: 4*b*h*d per visible (query, key) pair."""
+    pairs = s * (s + 1) // 2 if causal else s * s
+    return 4 * b * hq * d * pairs
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {k: float(p[k]) for k in FALLBACK_PEAKS}, "measured"
+    except Exception:  # noqa: BLE001
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.tmp = None
+
+    def start(self):
+        try:
+            self.tmp = tempfile.NamedTemporaryFile(mode="w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=self.tmp, stderr=subprocess.DEVNULL)
+        except Exception:  # noqa: BLE001
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:  # noqa: BLE001
+            self.proc.kill()
+        self.tmp.flush()
+        rows = []
+        with open(self.tmp.name) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.tmp.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for r in rows for k in range(4) if r[5 + k].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------------------- GPU arm
+def run_gpu(args, rank, world):
+    import torch
+
+    import sequence_attention_seq_gb300 as uly
+    from sequence_attention_seq_gb300 import build as uly_build
+    from sequence_attention_seq_gb300.inputs import seq_shards_qkv
+
+    if rank == 0 or not os.path.exists(uly.library_path()):
+        uly_build.build()
+    if world > 1:
+        torch.distributed.barrier()
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    w = WORKLOAD
+    P, b, s, hq, hkv, d = w["P"], w["b"], w["s"], w["h_q"], w["h_kv"], w["d"]
+    S = s // P
+    qs, ks, vs = seq_shards_qkv(P, b, s, hq, hkv, d, torch.bfloat16, seed=rank, device=str(dev))
+    q_head = [torch.empty((b, s, hq // P, d), dtype=torch.bfloat16, device=dev) for _ in range(P)]
+    k_head = [torch.empty((b, s, hkv // P, d), dtype=torch.bfloat16, device=dev) for _ in range(P)]
+    v_head = [torch.empty((b, s, hkv // P, d), dtype=torch.bfloat16, device=dev) for _ in range(P)]
+    o_head = [torch.empty((b, s, hq // P, d), dtype=torch.bfloat16, device=dev) for _ in range(P)]
+    o_seq = [torch.empty((b, S, hq, d), dtype=torch.bfloat16, device=dev) for _ in range(P)]
+    o_fused = [torch.empty((b, S, hq, d), dtype=torch.bfloat16, device=dev) for _ in range(P)]
+    stream = torch.cuda.current_stream(dev)
+
+    # (label, kind, bytes moved, flops, callable); one kernel launch each
+    tensor_bytes = b * s * hq * d * 2
+    kv_bytes = b * s * hkv * d * 2
+    ops = []
+    for causal in (False, True):
+        fl = attn_flops(b, s, hq, d, causal)
+        tag = "causal" if causal else "noncausal"
+        ops += [
+            (f"a2a_seq2head_q", "permute", 2 * tensor_bytes, 0, lambda: uly.ulysses_a2a_seq2head(qs, q_head)),
+            (f"a2a_seq2head_k", "permute", 2 * kv_bytes, 0, lambda: uly.ulysses_a2a_seq2head(ks, k_head)),
+            (f"a2a_seq2head_v", "permute", 2 * kv_bytes, 0, lambda: uly.ulysses_a2a_seq2head(vs, v_head)),
+            (f"attn_{tag}", "attention", 0, fl,
+             (lambda c=causal: uly.ulysses_local_attention(q_head, k_head, v_head, c, o_head))),
+            (f"a2a_head2seq_o", "permute", 2 * tensor_bytes, 0, lambda: uly.ulysses_a2a_head2seq(o_head, o_seq)),
+            (f"fused_{tag}", "fused", 0, fl,
+             (lambda c=causal: uly.ulysses_dist_attn_fwd(qs, ks, vs, c, fused=True, out_seq=o_fused))),
+        ]
+    step_flops = 2 * (attn_flops(b, s, hq, d, False) + attn_flops(b, s, hq, d, True))
+
+    def step(events=None):
+        for n, op in enumerate(ops):
+            if events is not None:
+                events[n][0].record(stream)
+            op[4]()
+            if events is not None:
+                events[n][1].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    if uly.ulysses_device_status(clear=True) != 0:
+        raise RuntimeError("a kernel's bounded wait gave up during warm-up")
+
+    ev = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)] for _ in ops]
+          for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(dev.index if dev.index is not None else 0)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    time.sleep(0.3)  # let the sampler come up before the timed region
+    t_start.record(stream)
+    for k in range(args.steps):
+        step(ev[k])
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    if world > 1:
+        torch.distributed.barrier()
+    total_ms = t_start.elapsed_time(t_end)
+    if uly.ulysses_device_status(clear=True) != 0:
+        raise RuntimeError("a kernel's bounded wait gave up during the timed steps")
+
+    per_op = {}
+    for n, op in enumerate(ops):
+        per_op.setdefault(op[0], []).extend(ev[k][n][0].elapsed_time(ev[k][n][1]) for k in range(args.steps))
+
+    # attention kernel (fused launches carry the whole forward in one launch)
+    attn_launch_ms, attn_launch_flops = [], []
+    for n, op in enumerate(ops):
+        if op[1] in ("attention", "fused"):
+            for k in range(args.steps):
+                attn_launch_ms.append(ev[k][n][0].elapsed_time(ev[k][n][1]))
+                attn_launch_flops.append(op[3])
+    attn_tflops = sum(attn_launch_flops) / (sum(attn_launch_ms) * 1e-3) / 1e12
+    perm_ms = [ev[k][n][0].elapsed_time(ev[k][n][1]) for n, op in enumerate(ops) if op[1] == "permute"
+               for k in range(args.steps)]
+    perm_bytes = [op[2] for op in ops if op[1] == "permute"] * args.steps
+    perm_gbs = sum(perm_bytes) / (sum(perm_ms) * 1e-3) / 1e9
+
+    # end to end through the public API with pinned host buffers
+    host_q = [t.cpu().pin_memory() for t in qs]
+    host_k = [t.cpu().pin_memory() for t in ks]
+    host_v = [t.cpu().pin_memory() for t in vs]
+    host_o = [torch.empty((b, S, hq, d), dtype=torch.bfloat16).pin_memory() for _ in range(P)]
+    dq = [torch.empty_like(t) for t in qs]
+    dk = [torch.empty_like(t) for t in ks]
+    dv = [torch.empty_like(t) for t in vs]
+    h2d = sum(t.numel() * 2 for t in host_q + host_k + host_v)
+    d2h = 4 * sum(t.numel() * 2 for t in host_o)
+    ws = torch.empty(uly.ulysses_dist_attn_workspace_bytes(P, b, s, hq, hkv, d, torch.bfloat16, False),
+                     dtype=torch.uint8, device=dev)
+
+    def e2e_step():
+        for src, dst in zip(host_q + host_k + host_v, dq + dk + dv):
+            dst.copy_(src, non_blocking=True)
+        for causal in (False, True):
+            for fused in (False, True):
+                out = uly.ulysses_dist_attn_fwd(dq, dk, dv, causal, fused=fused, workspace=None if fused else ws)
+                for o, ho in zip(out, host_o):
+                    ho.copy_(o, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1)
+
+    res = dict(total_ms=total_ms, e2e_ms=e2e_ms, attn_tflops=attn_tflops, perm_gbs=perm_gbs, clocks=clk,
+               per_op={k: statistics.mean(v) for k, v in per_op.items()}, step_flops=step_flops,
+               attn_launch_ms=statistics.mean(attn_launch_ms), h2d=h2d, d2h=d2h,
+               n_launches=len(ops) * args.steps)
+    return res
+
+
+# -------------------------------------------------------------------- CPU oracle
+def oracle_sample(budget_s=12.0, seed=0):
+    """Times the fp64 oracle on a bounded sample of the workload: the exchanges at full size
+    and sampled attention rows (each row exact), until the time budget is spent."""
+    import random
+
+    import torch
+
+    import oracle
+    from sequence_attention_seq_gb300.inputs import seq_shards_qkv
+
+    w = WORKLOAD
+    P, b, s, hq, hkv, d = w["P"], w["b"], w["s"], w["h_q"], w["h_kv"], w["d"]
+    qs, ks, vs = seq_shards_qkv(P, b, s, hq, hkv, d, torch.bfloat16, seed=seed)
+    t0 = time.perf_counter()
+    q_head = oracle.seq2head(qs)
+    oracle.seq2head(ks)
+    oracle.seq2head(vs)
+    oracle.head2seq(q_head)
+    t_perm = time.perf_counter() - t0
+    perm_bytes = 2 * 4 * b * s * hq * d * 2
+    rng = random.Random(seed)
+    flops, rows, t_attn = 0, 0, 0.0
+    S = s // P
+    while t_attn < budget_s:
+        causal = rows % 2 == 1
+        smp = [(rng.randrange(P), rng.randrange(b), rng.randrange(S), rng.randrange(hq)) for _ in range(8)]
+        t1 = time.perf_counter()
+        oracle.dist_attn_rows(qs, ks, vs, causal, smp)
+        t_attn += time.perf_counter() - t1
+        for (j, _, t, _) in smp:
+            keys = (j * S + t + 1) if causal else s
+            flops += 4 * d * keys
+        rows += len(smp)
+    return dict(tflops=flops / t_attn / 1e12, rows=rows, t_attn=t_attn, perm_gbs=perm_bytes / t_perm / 1e9,
+                t_perm=t_perm)
+
+
+def cpu_baseline_obj(smp):
+    return {"value": smp["tflops"], "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+            "sample": (f"{smp['rows']} attention rows (exact fp64, mixed causal/non-causal) of the DiT workload in "
+                       f"{smp['t_attn']:.1f} s, plus the four exchanges at full size "
+                       f"({smp['perm_gbs']:.2f} GB/s); single thread of {os.cpu_count()} host cores")}
+
+
+# -------------------------------------------------------------------------- main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    w = WORKLOAD
+    config = {"workload": WORKLOAD_NAME, "P": w["P"], "b": w["b"], "s": w["s"], "h_q": w["h_q"], "h_kv": w["h_kv"],
+              "d": w["d"], "l2": "inputs larger than L2 (Q+K+V+O = 256 MiB > 129 MB); no flush"}
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        steps = []
+        for k in range(args.warmup + args.steps):
+            smp = oracle_sample(budget_s=2.0, seed=k)
+            if k >= args.warmup:
+                steps.append(smp)
+        v = sum(x["tflops"] for x in steps) / len(steps)
+        line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "TFLOP/s", "n_gpus": args.gpus,
+                "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "dtype": "f64",
+                "data": "synthetic", "config": config,
+                "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+                                 "sample": "per step: the four exchanges at full size and ~2 s of exact fp64 "
+                                           "attention rows of the DiT workload, single thread"},
+                "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    import torch
+
+    if world > 1:
+        torch.distributed.init_process_group("nccl")
+    res = run_gpu(args, rank, world)
+    total_ms, e2e_ms = res["total_ms"], res["e2e_ms"]
+    if world > 1:
+        t = torch.tensor([total_ms, e2e_ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms, e2e_ms = t.tolist()
+    if rank != 0:
+        torch.distributed.destroy_process_group()
+        return
+    peaks, peak_src = load_peaks()
+    value = world * res["step_flops"] * args.steps / (total_ms * 1e-3) / 1e12
+    e2e_value = world * res["step_flops"] * args.steps / (e2e_ms * 1e-3) / 1e12
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        cpu = cpu_baseline_obj(oracle_sample(budget_s=12.0))
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16)", "config": config,
+        "roofline": {"kernel": "attn_tc_kernel<128> (all attention launches of the step)", "bound": "tensor",
+                     "achieved": res["attn_tflops"], "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": res["attn_tflops"] / peaks["bf16_tflops"],
+                     "frac_of_sustained": res["attn_tflops"] / peaks["bf16_tflops_sustained"],
+                     "peak_source": f"{peak_src} (bf16 dense, burst)", "traffic": None},
+        "permute": {"achieved": res["perm_gbs"], "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                    "frac": res["perm_gbs"] / peaks["hbm_gbs"], "bytes": "read+write of all ranks' data"},
+        "per_launch_ms": res["per_op"],
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": res["h2d"],
+                "d2h_bytes_per_step": res["d2h"]},
+        "gpu_launches": res["n_launches"] * world,
+        "clocks": res["clocks"],
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

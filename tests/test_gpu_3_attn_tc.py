@@ -20,7 +20,7 @@ CASES = [
     (2, 1, 384, 4, 4, 128, True),
     (2, 2, 320, 4, 2, 64, True),     # ragged tail, grouped K/V
     (2, 2, 320, 4, 2, 64, False),
-    (4, 1, 512, 8, 2, 128, True),    # 4 query heads per K/V head
+    (4, 1, 512, 16, 4, 128, True),   # 4 query heads per K/V head
     (1, 1, 1, 1, 1, 64, False),      # one token
     (2, 1, 1000, 2, 2, 128, True),   # ragged, several tiles
     (3, 1, 771, 3, 3, 64, False),
