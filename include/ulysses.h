@@ -126,6 +126,28 @@ uly_status ulysses_dist_attn_fwd(int P, int b, int s, int h_q, int h_kv, int d, 
                                  cudaStream_t stream);
 
 /*
+ * The unfused forward without any allocation by the caller or the library.  The paper has
+ * no counterpart: this exists for callers that cannot call cudaMalloc -- for example an
+ * application whose memory pool already holds all the device memory it may use, or a
+ * plugin whose host runtime gives it no allocator on its hot path.
+ * Same arguments, layouts, results and errors as ulysses_dist_attn_fwd with fused == 0,
+ * except that the workspace is a fixed array of ULYSSES_NOALLOC_SCRATCH_BYTES bytes of
+ * device memory inside the library, which every GPU that loads the library holds until
+ * the process exits.  Calls needing more scratch than that
+ * (ulysses_dist_attn_workspace_bytes(..., fused = 0) > ULYSSES_NOALLOC_SCRATCH_BYTES)
+ * return ULY_ERR_INVALID_ARG without enqueuing work.  The first call on a device looks up
+ * the array's device address (make it before any stream capture begins).  Every call
+ * shares the array: calls whose work overlaps on the GPU (e.g. on two streams) race and
+ * must be serialised by the caller.  Nothing is allocated, on the host or the device.
+ */
+#define ULYSSES_NOALLOC_SCRATCH_BYTES (64ull << 20)
+uly_status ulysses_dist_attn_fwd_noalloc(int P, int b, int s, int h_q, int h_kv, int d, uly_dtype dtype,
+                                         int causal,
+                                         const void* const* q_seq, const void* const* k_seq,
+                                         const void* const* v_seq, void* const* o_seq,
+                                         cudaStream_t stream);
+
+/*
  * Reads (and, if clear != 0, resets) the library's device-side error word after
  * synchronising the current device.  Returns ULY_ERR_TIMEOUT if a kernel's bounded wait
  * gave up since the last reset (that kernel then wrote no output), ULY_ERR_CUDA if the

@@ -21,7 +21,7 @@ __all__ = [
     "UlyssesError", "library_path", "load_library",
     "ulysses_a2a_seq2head", "ulysses_a2a_head2seq", "ulysses_local_attention",
     "ulysses_dist_attn_workspace_bytes", "ulysses_dist_attn_fwd", "ulysses_device_status",
-    "ulysses_status_string", "EXPORTED_SYMBOLS",
+    "ulysses_status_string", "EXPORTED_SYMBOLS", "ulysses_dist_attn_fwd_noalloc", "NOALLOC_SCRATCH_BYTES",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -34,7 +34,7 @@ _DTYPES = {torch.float32: 0, torch.bfloat16: 1}
 EXPORTED_SYMBOLS = (
     "ulysses_a2a_seq2head", "ulysses_a2a_head2seq", "ulysses_local_attention",
     "ulysses_dist_attn_workspace_bytes", "ulysses_dist_attn_fwd", "ulysses_device_status",
-    "ulysses_status_string",
+    "ulysses_status_string", "ulysses_dist_attn_fwd_noalloc",
 )
 
 _lock = threading.Lock()
@@ -74,6 +74,8 @@ def load_library():
         lib.ulysses_dist_attn_workspace_bytes.restype = sz
         lib.ulysses_dist_attn_fwd.argtypes = [i, i, i, i, i, i, i, i, pp, pp, pp, pp, vp, sz, i, vp]
         lib.ulysses_dist_attn_fwd.restype = i
+        lib.ulysses_dist_attn_fwd_noalloc.argtypes = [i, i, i, i, i, i, i, i, pp, pp, pp, pp, vp]
+        lib.ulysses_dist_attn_fwd_noalloc.restype = i
         lib.ulysses_device_status.argtypes = [i]
         lib.ulysses_device_status.restype = i
         lib.ulysses_status_string.argtypes = [i]
@@ -202,3 +204,27 @@ def ulysses_dist_attn_fwd(q_seq, k_seq, v_seq, causal, fused=False, out_seq=None
 def ulysses_device_status(clear=True):
     """Synchronise and report (and by default clear) the device-side error word."""
     return int(load_library().ulysses_device_status(int(bool(clear))))
+
+
+# size of the library's fixed scratch array used by ulysses_dist_attn_fwd_noalloc
+NOALLOC_SCRATCH_BYTES = 64 << 20
+
+
+def ulysses_dist_attn_fwd_noalloc(q_seq, k_seq, v_seq, causal, out_seq, stream=None):
+    """The unfused forward with the library's fixed scratch array as its workspace.
+
+    For callers that cannot allocate device memory: ``out_seq`` (P tensors
+    [b, s/P, h_q, d]) must be supplied, and nothing is allocated here or in the library.
+    Calls that would need more than NOALLOC_SCRATCH_BYTES of scratch raise.  Calls that
+    overlap on the GPU share the scratch and race; serialise them.
+    """
+    q0 = _same(q_seq, "q_seq")
+    k0 = _same(k_seq, "k_seq")
+    _same(v_seq, "v_seq")
+    _same(out_seq, "out_seq")
+    P = len(q_seq)
+    b, S, hq, d = q0.shape
+    _check(load_library().ulysses_dist_attn_fwd_noalloc(
+        P, b, S * P, hq, k0.shape[2], d, _dtype_code(q0), int(bool(causal)), _ptr_array(q_seq), _ptr_array(k_seq),
+        _ptr_array(v_seq), _ptr_array(out_seq), _stream(stream)), "ulysses_dist_attn_fwd_noalloc")
+    return out_seq
