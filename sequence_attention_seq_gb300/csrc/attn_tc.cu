@@ -10,23 +10,27 @@
 // accumulator recurrence of the same page's online-softmax paragraph, in base 2: scores
 // are scaled by log2(e)/sqrt(d) and exponentiated with the hardware ex2.
 //
-// Tiles: 128 query rows x 128 keys; head dim d in {64, 128}.  One CTA per (rank, batch,
-// head, query tile), 6 warps with fixed roles:
-//   warp 0      TMA producer: Q once, then K_j and V_j into 2-stage rings
-//   warp 1      allocates tensor memory and issues tcgen05.mma from one thread:
-//                 S_j = Q K_j^T into one of two S buffers (tensor memory),
-//                 O  += P_j V_j  into the O accumulator (tensor memory)
-//   warps 2..5  softmax: one thread per query row reads its S row from tensor memory,
-//               masks, updates (m, l), writes P_j = exp2(S - m) as bf16 into shared
-//               memory, rescales O when the reference maximum moved; finally O / l is
-//               written through shared memory with TMA stores.
-// The MMA for S_{j+1} runs while the softmax works on S_j.  The reference maximum is
-// only raised when a row maximum exceeds it by more than 8 (a factor 256), so O is
-// rarely rescaled; P entries stay below 256, exact enough in bf16, and the final O / l
-// is unchanged mathematically.
+// Work unit: one CTA owns two consecutive 128-row query tiles (Q0, Q1) of one (rank,
+// batch, head) and streams 128-key K/V tiles through a 4-slot shared-memory ring; each
+// K/V tile serves both query tiles.  Head dim d in {64, 128}.  10 warps:
+//   warps 0-3   softmax for Q0, warps 4-7 softmax for Q1: one thread per query row
+//               (warp w may access tensor-memory lanes 32*(w%4)..+31)
+//   warp 8      TMA producer: Q0, Q1 once, then K_j, V_j into the ring
+//   warp 9      allocates tensor memory; one thread issues every tcgen05.mma
+// Tensor memory (512 columns): S0 | S1 | O0 | O1, 128 columns each.  The softmax writes
+// P_k = exp2(S_k*c - m) as bf16 pairs back over the first 64 columns of S_k, and
+// O_k += P_k V_j reads P_k straight from tensor memory.
+// MMA order per key tile j: PV0(j), S0(j+1), PV1(j), S1(j+1).  The tensor pipe executes
+// MMAs in issue order, and a commit covers every earlier MMA, so when the softmax sees
+// S_k(j+1) complete, PV_k(j) is complete too: O_k can be rescaled right away and
+// S_k(j+1) cannot overwrite P_k(j) before PV_k(j) has read it.  While one softmax group
+// works on its tile, the tensor pipe runs the other group's PV and S.
+// The reference maximum m is only raised when a row maximum exceeds it by more than 8
+// (a factor 256), so O is rarely rescaled; P entries stay below 256, exact enough in
+// bf16, and the final O / l is unchanged mathematically.
 //
-// Fused mode ("DeepSpeed-Ulysses 深度解析", steps 3 and 5; the all-to-alls of "02 ·
-// DeepSpeed-Ulysses" section 3 "可合并"): the Q/K/V tiles of tokens [t0, t0+128) come
+// Fused mode ("DeepSpeed-Ulysses 深度解析", steps 3 and 5; "02 · DeepSpeed-Ulysses",
+// section 3, where the exchanges "can be merged"): the tiles of tokens [t0, t0+128) come
 // straight from source rank t0 / (s/P)'s seq-layout buffer at head column gh, and the
 // output tile goes straight to that rank's seq-layout output, so the head-layout copies
 // never exist.  Requires (s/P) % 128 == 0 so no tile straddles two ranks.
@@ -46,9 +50,12 @@ __device__ unsigned int g_uly_error_word = 0;
 
 namespace {
 
-constexpr int BM = 128;
-constexpr int BN = 128;
-constexpr int kThreads = 192;
+constexpr int BM = 128;   // query rows per tile
+constexpr int BN = 128;   // keys per tile
+constexpr int kSlots = 4; // K/V ring slots
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kThreads = 320;
 constexpr int kMaxMaps = 16;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far beyond any legitimate wait
@@ -62,6 +69,7 @@ struct TcParams {
     int s;             // sequence length
     int rows_per_map;  // tokens held by one map: s/P when fused, s otherwise
     int n_qtiles;      // ceil(s / BM)
+    int n_pairs;       // ceil(n_qtiles / 2)
     int heads;         // query heads per map group: h_q (fused) or h_q/P (per rank)
     int g;             // query heads per K/V head
     int b;
@@ -72,33 +80,26 @@ struct TcParams {
 
 template <int D>
 struct Smem {
-    static constexpr uint32_t kTileQ = BM * D * 2;  // bytes of a Q (or K, V) tile
-    static constexpr uint32_t kTileKV = BN * D * 2;
-    static constexpr uint32_t kTileP = BM * BN * 2;
-    static constexpr uint32_t offQ = 0;
-    static constexpr uint32_t offK = offQ + kTileQ;
-    static constexpr uint32_t offV = offK + 2 * kTileKV;
-    static constexpr uint32_t offP = offV + 2 * kTileKV;
-    static constexpr uint32_t offBar = offP + kTileP;
+    static constexpr uint32_t kTile = BM * D * 2;  // bytes of one Q, K or V tile
+    static constexpr uint32_t offQ = 0;            // Q0, Q1
+    static constexpr uint32_t offKV = 2 * kTile;   // ring of kSlots tiles
+    static constexpr uint32_t offBar = offKV + kSlots * kTile;
     static constexpr uint32_t kBarBytes = 256;
     static constexpr uint32_t kUsed = offBar + kBarBytes;
-    // 1 KB slack to align the base to 1024 bytes; d=64 pads to keep one CTA per SM
-    // (each CTA takes all 512 tensor-memory columns).
+    // 1 KB slack to align the base to 1024 bytes; d=64 pads so that one CTA (which takes
+    // all 512 tensor-memory columns) fills an SM.
     static constexpr uint32_t kAlloc = (kUsed + 1024) > 120u * 1024u ? (kUsed + 1024) : 120u * 1024u;
 };
 
 enum BarIdx {
-    B_Q_FULL = 0,
-    B_K_FULL = 1,   // +stage
-    B_K_EMPTY = 3,  // +stage
-    B_V_FULL = 5,   // +stage
-    B_V_EMPTY = 7,  // +stage
-    B_S_FULL = 9,   // +buffer
-    B_S_EMPTY = 11, // +buffer
-    B_P_FULL = 13,
-    B_O_DONE = 14,
-    B_MMA_DONE = 15,
-    B_COUNT = 16
+    B_Q_FULL = 0,                       // +tile (2)
+    B_KV_FULL = 2,                      // +slot (4)
+    B_KV_EMPTY = B_KV_FULL + kSlots,    // +slot (4)
+    B_S_FULL = B_KV_EMPTY + kSlots,     // +tile (2)
+    B_P_FULL = B_S_FULL + 2,            // +tile (2), 4 arrivals each
+    B_O_FINAL = B_P_FULL + 2,           // +tile (2)
+    B_MMA_DONE = B_O_FINAL + 2,
+    B_COUNT = B_MMA_DONE + 1
 };
 
 struct Shared {
@@ -138,6 +139,13 @@ __device__ __forceinline__ bool wait_phase_warp(uint64_t* bar, uint32_t parity, 
     return __all_sync(0xffffffffu, ok);
 }
 
+// Bounded drain wait used on the way out (no abort check: the copies/MMAs must land).
+__device__ __forceinline__ void drain_phase(uint64_t* bar, uint32_t parity) {
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait(bar, parity) && global_timer_ns() - t0 < kWaitLimitNs) {
+    }
+}
+
 struct TileCoord {
     int map;  // index into the map arrays
     int row;  // token coordinate inside that map
@@ -155,6 +163,49 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// Row maximum of 32 score columns; columns >= lim are masked when MASK.
+template <bool MASK>
+__device__ __forceinline__ float chunk_max(const uint32_t (&r)[32], int base, int lim, float m) {
+    float a = m, b = -INFINITY, c = -INFINITY, d = -INFINITY;
+#pragma unroll
+    for (int e = 0; e < 32; e += 4) {
+        float x0 = __uint_as_float(r[e]), x1 = __uint_as_float(r[e + 1]);
+        float x2 = __uint_as_float(r[e + 2]), x3 = __uint_as_float(r[e + 3]);
+        if (MASK) {
+            x0 = base + e < lim ? x0 : -INFINITY;
+            x1 = base + e + 1 < lim ? x1 : -INFINITY;
+            x2 = base + e + 2 < lim ? x2 : -INFINITY;
+            x3 = base + e + 3 < lim ? x3 : -INFINITY;
+        }
+        a = fmaxf(a, x0);
+        b = fmaxf(b, x1);
+        c = fmaxf(c, x2);
+        d = fmaxf(d, x3);
+    }
+    return fmaxf(fmaxf(a, b), fmaxf(c, d));
+}
+
+// P = exp2(S*scale - m) for 32 columns, packed into 16 bf16 pairs; returns the row sum.
+template <bool MASK>
+__device__ __forceinline__ float chunk_exp(const uint32_t (&r)[32], int base, int lim, float scale, float neg_m,
+                                           uint32_t (&pk)[16]) {
+    float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+    for (int e = 0; e < 32; e += 2) {
+        float x0 = __uint_as_float(r[e]), x1 = __uint_as_float(r[e + 1]);
+        if (MASK) {
+            x0 = base + e < lim ? x0 : -INFINITY;
+            x1 = base + e + 1 < lim ? x1 : -INFINITY;
+        }
+        const float e0 = ex2_approx(fmaf(x0, scale, neg_m));
+        const float e1 = ex2_approx(fmaf(x1, scale, neg_m));
+        s0 += e0;
+        s1 += e1;
+        pk[e >> 1] = pack_bf16x2(e0, e1);
+    }
+    return s0 + s1;
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_constant__ TcParams p) {
     using L = Smem<D>;
@@ -162,8 +213,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     constexpr int KSTEPS_PV = BN / 16; // MMA K-steps for O += P V
     constexpr uint32_t kIdescQK = idesc_bf16_f32(BM, BN, false);
     constexpr uint32_t kIdescPV = idesc_bf16_f32(BM, D, true);
-    constexpr uint32_t kHalfQ = BM * 128;  // bytes of one 64-column slab of a 128-row tile
-    constexpr uint32_t kHalfKV = BN * 128;
+    constexpr uint32_t kSlab = BM * 128;  // bytes of one 64-column slab of a 128-row tile
 
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -174,239 +224,222 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    // ---- block -> (rank, batch, kv head, query tile, head within group); heavy tiles first
+    // ---- block -> (rank, batch, kv head, query-tile pair, head within group); heavy pairs first
     int bid = blockIdx.x;
     const int hg = bid % p.g;
     bid /= p.g;
-    const int qt = p.n_qtiles - 1 - (bid % p.n_qtiles);
-    bid /= p.n_qtiles;
+    const int pair = p.n_pairs - 1 - (bid % p.n_pairs);
+    bid /= p.n_pairs;
     const int kv_heads = p.heads / p.g;
     const int kvh = bid % kv_heads;
     bid /= kv_heads;
     const int bb = bid % p.b;
     const int rank = bid / p.b;
     const int head = kvh * p.g + hg;
-    const int q0 = qt * BM;
-    const int n_kv = p.causal ? (qt + 1) : (p.s + BN - 1) / BN;
+    const int qt0 = 2 * pair;
+    const bool has_q1 = qt0 + 1 < p.n_qtiles;
+    const int n_kv_all = (p.s + BN - 1) / BN;
+    // key tiles each query tile needs
+    const int n0 = p.causal ? qt0 + 1 : n_kv_all;
+    const int n1 = has_q1 ? (p.causal ? qt0 + 2 : n_kv_all) : 0;
+    const int n_max = n0 > n1 ? n0 : n1;
 
     if (threadIdx.x == 0) {
         sh->abort = error_word_set() ? 1 : 0;
-        for (int i = 0; i < B_COUNT; ++i) {
-            // the four softmax warps arrive once each on S_EMPTY and P_FULL
-            const bool per_warp = i == B_S_EMPTY || i == B_S_EMPTY + 1 || i == B_P_FULL;
-            mbar_init(&bars[i], per_warp ? 4u : 1u);
-        }
+        for (int i = 0; i < B_COUNT; ++i) mbar_init(&bars[i], (i == B_P_FULL || i == B_P_FULL + 1) ? 4u : 1u);
         fence_mbarrier_init();
     }
     __syncthreads();
     if (sh->abort) return;  // an earlier CTA failed: nothing allocated yet, leave at once
 
-    if (warp == 1) {
-        tmem_alloc(&sh->tmem_base, kTmemCols);
-    }
+    if (warp == kMmaWarp) tmem_alloc(&sh->tmem_base, kTmemCols);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = sh->tmem_base;
-    const uint32_t tS[2] = {tmem, tmem + 128u};
-    const uint32_t tO = tmem + 256u;
 
-    if (warp == 0) {
+    if (warp == kProducerWarp) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
-            const TileCoord qc = tile_coord(p, rank, q0);
-            tma_prefetch_desc(&p.mq[qc.map]);
-            mbar_arrive_expect_tx(&bars[B_Q_FULL], L::kTileQ);
-#pragma unroll
-            for (int c = 0; c < D / 64; ++c)
-                tma_load_4d(sbase + L::offQ + c * kHalfQ, &p.mq[qc.map], &bars[B_Q_FULL], c * 64, head, qc.row, bb);
-            int issued_k[2] = {0, 0}, issued_v[2] = {0, 0};
-            bool ok = true;
-            for (int j = 0; j < n_kv && ok; ++j) {
-                const int st = j & 1;
-                const uint32_t ph = ((j >> 1) & 1) ^ 1;
-                const TileCoord kc = tile_coord(p, rank, j * BN);
-                ok = wait_phase(&bars[B_K_EMPTY + st], ph, sh);
-                if (!ok) break;
-                mbar_arrive_expect_tx(&bars[B_K_FULL + st], L::kTileKV);
+            int issued[kSlots] = {0, 0, 0, 0};
+            for (int t = 0; t < (has_q1 ? 2 : 1); ++t) {
+                const TileCoord qc = tile_coord(p, rank, (qt0 + t) * BM);
+                mbar_arrive_expect_tx(&bars[B_Q_FULL + t], L::kTile);
 #pragma unroll
                 for (int c = 0; c < D / 64; ++c)
-                    tma_load_4d(sbase + L::offK + st * L::kTileKV + c * kHalfKV, &p.mk[kc.map], &bars[B_K_FULL + st],
-                                c * 64, kvh, kc.row, bb);
-                ++issued_k[st];
-                ok = wait_phase(&bars[B_V_EMPTY + st], ph, sh);
-                if (!ok) break;
-                mbar_arrive_expect_tx(&bars[B_V_FULL + st], L::kTileKV);
-#pragma unroll
-                for (int c = 0; c < D / 64; ++c)
-                    tma_load_4d(sbase + L::offV + st * L::kTileKV + c * kHalfKV, &p.mv[kc.map], &bars[B_V_FULL + st],
-                                c * 64, kvh, kc.row, bb);
-                ++issued_v[st];
+                    tma_load_4d(sbase + L::offQ + t * L::kTile + c * kSlab, &p.mq[qc.map], &bars[B_Q_FULL + t], c * 64,
+                                head, qc.row, bb);
             }
-            if (!ok) {
-                // drain: every copy issued must land before shared memory goes away
-                const uint64_t t0 = global_timer_ns();
-                for (int st = 0; st < 2; ++st) {
-                    if (issued_k[st])
-                        while (!mbar_try_wait(&bars[B_K_FULL + st], ((issued_k[st] - 1) & 1)) &&
-                               global_timer_ns() - t0 < kWaitLimitNs) {
-                        }
-                    if (issued_v[st])
-                        while (!mbar_try_wait(&bars[B_V_FULL + st], ((issued_v[st] - 1) & 1)) &&
-                               global_timer_ns() - t0 < kWaitLimitNs) {
-                        }
-                }
-                const uint64_t t1 = global_timer_ns();
-                while (!mbar_try_wait(&bars[B_Q_FULL], 0) && global_timer_ns() - t1 < kWaitLimitNs) {
-                }
+            bool ok = true;
+            for (int n = 0; n < 2 * n_max && ok; ++n) {
+                const int j = n >> 1, slot = n % kSlots;
+                const TileCoord kc = tile_coord(p, rank, j * BN);
+                ok = wait_phase(&bars[B_KV_EMPTY + slot], ((n / kSlots) & 1) ^ 1, sh);
+                if (!ok) break;
+                const CUtensorMap* map = (n & 1) ? &p.mv[kc.map] : &p.mk[kc.map];
+                mbar_arrive_expect_tx(&bars[B_KV_FULL + slot], L::kTile);
+#pragma unroll
+                for (int c = 0; c < D / 64; ++c)
+                    tma_load_4d(sbase + L::offKV + slot * L::kTile + c * kSlab, map, &bars[B_KV_FULL + slot], c * 64,
+                                kvh, kc.row, bb);
+                ++issued[slot];
+            }
+            if (!ok) {  // every copy issued must land before shared memory goes away
+                for (int slot = 0; slot < kSlots; ++slot)
+                    if (issued[slot]) drain_phase(&bars[B_KV_FULL + slot], (issued[slot] - 1) & 1);
+                drain_phase(&bars[B_Q_FULL], 0);
+                if (has_q1) drain_phase(&bars[B_Q_FULL + 1], 0);
             }
         }
-    } else if (warp == 1) {
+    } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
+            const uint32_t tS[2] = {tmem, tmem + 128u};
+            const uint32_t tO[2] = {tmem + 256u, tmem + 384u};
+            const int nt[2] = {n0, n1};
+            auto kv_slot = [](int n) { return n % kSlots; };
+            auto kv_par = [](int n) { return (uint32_t)((n / kSlots) & 1); };
+            auto issue_s = [&](int t, int j) {  // S_t = Q_t K_j^T
+                const uint32_t kaddr = sbase + L::offKV + kv_slot(2 * j) * L::kTile;
+                const uint32_t qaddr = sbase + L::offQ + t * L::kTile;
+#pragma unroll
+                for (int kk = 0; kk < KSTEPS_QK; ++kk) {
+                    const uint64_t da = smem_desc_sw128(qaddr + (kk >> 2) * kSlab + (kk & 3) * 32, 16, 1024);
+                    const uint64_t db = smem_desc_sw128(kaddr + (kk >> 2) * kSlab + (kk & 3) * 32, 16, 1024);
+                    mma_bf16_ss(tS[t], da, db, kIdescQK, kk > 0 ? 1u : 0u);
+                }
+            };
+            auto issue_pv = [&](int t, int j) {  // O_t += P_t V_j, P_t from tensor memory
+                const uint32_t vaddr = sbase + L::offKV + kv_slot(2 * j + 1) * L::kTile;
+#pragma unroll
+                for (int kk = 0; kk < KSTEPS_PV; ++kk) {
+                    // V is [keys][d], d contiguous: MN-major B; 64-column slabs kSlab apart
+                    // (leading offset), 8-key groups 1024 bytes apart (stride offset)
+                    const uint64_t db = smem_desc_sw128(vaddr + kk * 16 * 128, kSlab, 1024);
+                    mma_bf16_ts(tO[t], tS[t] + kk * 8, db, kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+                }
+            };
             bool ok = wait_phase(&bars[B_Q_FULL], 0, sh);
-            tc_fence_after();
-            for (int j = 0; j <= n_kv && ok; ++j) {
-                if (j < n_kv) {
-                    const int st = j & 1;
-                    ok = wait_phase(&bars[B_K_FULL + st], (j >> 1) & 1, sh);
-                    if (ok) ok = wait_phase(&bars[B_S_EMPTY + st], ((j >> 1) & 1) ^ 1, sh);
+            if (ok && has_q1) ok = wait_phase(&bars[B_Q_FULL + 1], 0, sh);
+            if (ok) ok = wait_phase(&bars[B_KV_FULL + kv_slot(0)], kv_par(0), sh);
+            if (ok) {
+                tc_fence_after();
+                for (int t = 0; t < 2; ++t)
+                    if (nt[t] > 0) {
+                        issue_s(t, 0);
+                        mma_commit(&bars[B_S_FULL + t]);
+                    }
+                mma_commit(&bars[B_KV_EMPTY + kv_slot(0)]);
+            }
+            for (int j = 0; j < n_max && ok; ++j) {
+                ok = wait_phase(&bars[B_KV_FULL + kv_slot(2 * j + 1)], kv_par(2 * j + 1), sh);
+                const bool next = j + 1 < n_max;
+                bool k_next_ready = false;
+                for (int t = 0; t < 2 && ok; ++t) {
+                    if (j >= nt[t]) continue;
+                    ok = wait_phase(&bars[B_P_FULL + t], j & 1, sh);
                     if (!ok) break;
                     tc_fence_after();
-#pragma unroll
-                    for (int kk = 0; kk < KSTEPS_QK; ++kk) {
-                        const uint64_t da = smem_desc_sw128(sbase + L::offQ + (kk >> 2) * kHalfQ + (kk & 3) * 32, 16, 1024);
-                        const uint64_t db = smem_desc_sw128(
-                            sbase + L::offK + st * L::kTileKV + (kk >> 2) * kHalfKV + (kk & 3) * 32, 16, 1024);
-                        mma_bf16_ss(tS[st], da, db, kIdescQK, kk > 0 ? 1u : 0u);
+                    issue_pv(t, j);
+                    if (j + 1 < nt[t]) {
+                        if (!k_next_ready) {  // K_{j+1} is only needed from here on
+                            ok = wait_phase(&bars[B_KV_FULL + kv_slot(2 * j + 2)], kv_par(2 * j + 2), sh);
+                            if (!ok) break;
+                            tc_fence_after();
+                            k_next_ready = true;
+                        }
+                        issue_s(t, j + 1);
+                        mma_commit(&bars[B_S_FULL + t]);
+                    } else {
+                        mma_commit(&bars[B_O_FINAL + t]);
                     }
-                    mma_commit(&bars[B_S_FULL + st]);
-                    mma_commit(&bars[B_K_EMPTY + st]);
                 }
-                if (j >= 1) {
-                    const int jp = j - 1;
-                    const int st = jp & 1;
-                    ok = wait_phase(&bars[B_P_FULL], jp & 1, sh);
-                    if (ok) ok = wait_phase(&bars[B_V_FULL + st], (jp >> 1) & 1, sh);
-                    if (!ok) break;
-                    tc_fence_after();
-#pragma unroll
-                    for (int kk = 0; kk < KSTEPS_PV; ++kk) {
-                        const uint64_t da = smem_desc_sw128(sbase + L::offP + (kk >> 2) * kHalfQ + (kk & 3) * 32, 16, 1024);
-                        // V is [keys][d] with d contiguous: MN-major B operand; 64-column slabs
-                        // kHalfKV apart (leading offset), 8-key groups 1024 bytes apart (stride).
-                        const uint64_t db = smem_desc_sw128(sbase + L::offV + st * L::kTileKV + kk * 16 * 128, kHalfKV, 1024);
-                        mma_bf16_ss(tO, da, db, kIdescPV, (jp > 0 || kk > 0) ? 1u : 0u);
-                    }
-                    mma_commit(&bars[B_O_DONE]);
-                    mma_commit(&bars[B_V_EMPTY + st]);
-                }
+                if (!ok) break;
+                mma_commit(&bars[B_KV_EMPTY + kv_slot(2 * j + 1)]);
+                if (next) mma_commit(&bars[B_KV_EMPTY + kv_slot(2 * j + 2)]);
             }
             // every MMA issued above completes before tensor memory is released
             mma_commit(&bars[B_MMA_DONE]);
-            const uint64_t t0 = global_timer_ns();
-            while (!mbar_try_wait(&bars[B_MMA_DONE], 0) && global_timer_ns() - t0 < kWaitLimitNs) {
-            }
+            drain_phase(&bars[B_MMA_DONE], 0);
         }
     } else {
         // ------------------------------------------------------------ softmax warps
+        const int t = warp >> 2;           // query tile of this group
         const int sub = warp & 3;          // tensor-memory lane quarter this warp may access
         const int row = sub * 32 + lane;   // query row within the tile
+        const int q0 = (qt0 + t) * BM;
         const int qrow = q0 + row;         // global query position
+        const int nkv = t == 0 ? n0 : n1;
         const uint32_t lane_off = (uint32_t)(sub * 32) << 16;
-        uint8_t* sP = smem + L::offP;
+        const uint32_t tS = tmem + 128u * t + lane_off;
+        const uint32_t tO = tmem + 256u + 128u * t + lane_off;
+        const float scale = p.scale_log2;
         float m_ref = -INFINITY, l_sum = 0.f;
         bool ok = true;
-        for (int j = 0; j < n_kv; ++j) {
-            const int sb = j & 1;
-            ok = wait_phase_warp(&bars[B_S_FULL + sb], (j >> 1) & 1, sh);
+        for (int j = 0; j < nkv; ++j) {
+            ok = wait_phase_warp(&bars[B_S_FULL + t], j & 1, sh);
             if (!ok) break;
             tc_fence_after();
-            // pass 1: row maximum of the (masked) scores, 32 columns at a time
             const int k0 = j * BN;
             const bool need_mask = (p.causal && k0 + BN - 1 > q0) || k0 + BN > p.s;
-            const int lim = need_mask ? min(p.s - k0, p.causal ? qrow - k0 + 1 : BN) : BN;  // visible columns
+            const int lim = min(p.s - k0, p.causal ? qrow - k0 + 1 : BN);  // visible columns of this row
+            // pass 1: row maximum
             float mx = -INFINITY;
 #pragma unroll
             for (int c = 0; c < BN / 32; ++c) {
                 uint32_t r[32];
-                tmem_ld32(tS[sb] + lane_off + c * 32, r);
+                tmem_ld32(tS + c * 32, r);
                 tmem_wait_ld();
-#pragma unroll
-                for (int e = 0; e < 32; ++e)
-                    if (c * 32 + e < lim) mx = fmaxf(mx, __uint_as_float(r[e]));
+                mx = need_mask ? chunk_max<true>(r, c * 32, lim, mx) : chunk_max<false>(r, c * 32, lim, mx);
             }
-            const float mx2 = mx * p.scale_log2;
+            const float mx2 = mx * scale;
             float m_new = m_ref;
             if (j == 0 || mx2 > m_ref + 8.0f) m_new = mx2;
-            if (m_new == -INFINITY) m_new = 0.f;  // row with nothing visible yet (padding rows only)
+            if (m_new == -INFINITY) m_new = 0.f;  // a row with nothing visible yet (padding rows only)
             const float alpha = (j == 0) ? 0.f : ex2_approx(m_ref - m_new);
-            // pass 2: P = exp2(S * log2(e)/sqrt(d) - m), row sum, packed to bf16 pairs
+            // O_t already holds P_t(j-1) V_{j-1} (S_t(j) was issued after it): rescale in place
+            if (j > 0 && __any_sync(0xffffffffu, m_new != m_ref)) {
+                const float f = m_new != m_ref ? alpha : 1.0f;
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t r[32];
+                    tmem_ld32(tO + c * 32, r);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * f);
+                    tmem_st32(tO + c * 32, r);
+                }
+            }
+            // pass 2: P = exp2(S*scale - m) as bf16 pairs over the first 64 columns of S_t
+            const float neg_m = -m_new;
             float rsum = 0.f;
-            uint32_t pk[BN / 2];
 #pragma unroll
             for (int c = 0; c < BN / 32; ++c) {
-                uint32_t r[32];
-                tmem_ld32(tS[sb] + lane_off + c * 32, r);
+                uint32_t r[32], pk[16];
+                tmem_ld32(tS + c * 32, r);
                 tmem_wait_ld();
-#pragma unroll
-                for (int e = 0; e < 32; e += 2) {
-                    const float x0 = (c * 32 + e < lim) ? __uint_as_float(r[e]) : -INFINITY;
-                    const float x1 = (c * 32 + e + 1 < lim) ? __uint_as_float(r[e + 1]) : -INFINITY;
-                    const float e0 = ex2_approx(fmaf(x0, p.scale_log2, -m_new));
-                    const float e1 = ex2_approx(fmaf(x1, p.scale_log2, -m_new));
-                    rsum += e0 + e1;
-                    pk[(c * 32 + e) / 2] = pack_bf16x2(e0, e1);
-                }
+                rsum += need_mask ? chunk_exp<true>(r, c * 32, lim, scale, neg_m, pk)
+                                  : chunk_exp<false>(r, c * 32, lim, scale, neg_m, pk);
+                tmem_st16(tS + c * 16, pk);  // columns already read
             }
+            tmem_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bars[B_S_EMPTY + sb]);
-            if (j >= 1) {
-                // P_{j-1} V_{j-1} done: the P buffer is free and O holds the sum through j-1
-                ok = wait_phase_warp(&bars[B_O_DONE], (j - 1) & 1, sh);
-                if (!ok) break;
-                tc_fence_after();
-                const bool rescale = m_new != m_ref;
-                if (__any_sync(0xffffffffu, rescale)) {
-                    const float f = rescale ? alpha : 1.0f;
-#pragma unroll
-                    for (int c = 0; c < D / 32; ++c) {
-                        uint32_t r[32];
-                        tmem_ld32(tO + lane_off + c * 32, r);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * f);
-                        tmem_st32(tO + lane_off + c * 32, r);
-                    }
-                    tmem_wait_st();
-                }
-            }
-            // P row -> shared memory, K-major 128B-swizzled layout (two 64-key slabs)
-#pragma unroll
-            for (int c16 = 0; c16 < BN / 8; ++c16) {
-                const uint4 w = make_uint4(pk[c16 * 4 + 0], pk[c16 * 4 + 1], pk[c16 * 4 + 2], pk[c16 * 4 + 3]);
-                const uint32_t off = (c16 >> 3) * kHalfQ + row * 128 + (((c16 & 7) ^ (row & 7)) << 4);
-                *reinterpret_cast<uint4*>(sP + off) = w;
-            }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars[B_P_FULL]);
+            if (lane == 0) mbar_arrive(&bars[B_P_FULL + t]);
             l_sum = (j == 0) ? rsum : l_sum * alpha + rsum;
             m_ref = m_new;
         }
-        if (ok) ok = wait_phase_warp(&bars[B_O_DONE], (n_kv - 1) & 1, sh);
-        if (ok) {
+        if (ok && nkv > 0) ok = wait_phase_warp(&bars[B_O_FINAL + t], 0, sh);
+        if (ok && nkv > 0) {
             tc_fence_after();
-            // epilogue: O / l -> bf16 -> this warp's 32 rows of the staging tile (Q's slot,
-            // free since the last S MMA completed) -> TMA store of a 32-row box per slab
+            // epilogue: O / l -> bf16 -> this warp's 32 rows of the staging tile (Q_t's slot,
+            // free since S_t's last MMA completed) -> TMA store of a 32-row box per slab
             const float inv = l_sum > 0.f ? 1.0f / l_sum : 0.f;
-            uint8_t* stage = smem + L::offQ;
+            uint8_t* stage = smem + L::offQ + t * L::kTile;
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t r[32];
-                tmem_ld32(tO + lane_off + c * 32, r);
+                tmem_ld32(tO + c * 32, r);
                 tmem_wait_ld();
 #pragma unroll
                 for (int q4 = 0; q4 < 4; ++q4) {
@@ -416,7 +449,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
                     w.z = pack_bf16x2(__uint_as_float(r[q4 * 8 + 4]) * inv, __uint_as_float(r[q4 * 8 + 5]) * inv);
                     w.w = pack_bf16x2(__uint_as_float(r[q4 * 8 + 6]) * inv, __uint_as_float(r[q4 * 8 + 7]) * inv);
                     const int col = c * 32 + q4 * 8;  // first of 8 output columns
-                    const uint32_t off = (col >> 6) * kHalfQ + row * 128 + ((((col & 63) >> 3) ^ (row & 7)) << 4);
+                    const uint32_t off = (col >> 6) * kSlab + row * 128 + ((((col & 63) >> 3) ^ (row & 7)) << 4);
                     *reinterpret_cast<uint4*>(stage + off) = w;
                 }
             }
@@ -426,8 +459,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
                 const TileCoord oc = tile_coord(p, rank, q0);
 #pragma unroll
                 for (int c = 0; c < D / 64; ++c)
-                    tma_store_4d(&p.mo[oc.map], sbase + L::offQ + c * kHalfQ + sub * 32 * 128, c * 64, head,
-                                 oc.row + sub * 32, bb);
+                    tma_store_4d(&p.mo[oc.map], sbase + L::offQ + t * L::kTile + c * kSlab + sub * 32 * 128, c * 64,
+                                 head, oc.row + sub * 32, bb);
                 tma_store_commit_and_drain();
             }
         }
@@ -435,7 +468,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 1) {
+    if (warp == kMmaWarp) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
@@ -497,6 +530,7 @@ cudaError_t launch_attention_tc(int P, int b, int s, int h_q, int h_kv, int d, i
     memset(prm, 0, sizeof(TcParams));
     prm->s = s;
     prm->n_qtiles = (s + BM - 1) / BM;
+    prm->n_pairs = (prm->n_qtiles + 1) / 2;
     prm->g = h_q / h_kv;
     prm->b = b;
     prm->causal = causal ? 1 : 0;
@@ -515,7 +549,7 @@ cudaError_t launch_attention_tc(int P, int b, int s, int h_q, int h_kv, int d, i
                 err = cudaErrorInvalidValue;
         }
         if (err == cudaSuccess) {
-            const long long nblocks = (long long)b * h_q * prm->n_qtiles;
+            const long long nblocks = (long long)b * h_q * prm->n_pairs;
             err = d == 64 ? launch_d<64>(*prm, nblocks, stream) : launch_d<128>(*prm, nblocks, stream);
         }
     } else {
@@ -534,7 +568,7 @@ cudaError_t launch_attention_tc(int P, int b, int s, int h_q, int h_kv, int d, i
                     err = cudaErrorInvalidValue;
             }
             if (err != cudaSuccess) break;
-            const long long nblocks = (long long)nr * b * Hq * prm->n_qtiles;
+            const long long nblocks = (long long)nr * b * Hq * prm->n_pairs;
             err = d == 64 ? launch_d<64>(*prm, nblocks, stream) : launch_d<128>(*prm, nblocks, stream);
         }
     }
