@@ -21,10 +21,11 @@
 // P_k = exp2(S_k*c - m) as bf16 pairs back over the first 64 columns of S_k, and
 // O_k += P_k V_j reads P_k straight from tensor memory.
 // MMA order per key tile j: PV0(j), S0(j+1), PV1(j), S1(j+1).  The tensor pipe executes
-// MMAs in issue order, and a commit covers every earlier MMA, so when the softmax sees
-// S_k(j+1) complete, PV_k(j) is complete too: O_k can be rescaled right away and
-// S_k(j+1) cannot overwrite P_k(j) before PV_k(j) has read it.  While one softmax group
-// works on its tile, the tensor pipe runs the other group's PV and S.
+// MMAs in issue order and a commit covers every earlier MMA, so when a softmax group sees
+// S_k(j+1) complete, PV_k(j) is complete too: O_k can be rescaled right away, and S_k(j+1)
+// never overwrites P_k(j) early.  While one softmax group works on its tile, the tensor
+// pipe runs the other group's PV and S (measured faster than PV0 PV1 S0 S1, whose shorter
+// overlap window costs more than the pipe drain between PV_k(j) and S_k(j+1) it avoids).
 // The reference maximum m is only raised when a row maximum exceeds it by more than 8
 // (a factor 256), so O is rarely rescaled; P entries stay below 256, exact enough in
 // bf16, and the final O / l is unchanged mathematically.
@@ -113,7 +114,7 @@ __device__ __forceinline__ bool error_word_set() {
 
 // Bounded wait on an mbarrier phase.  Returns false (and raises the CTA abort flag) when
 // the time limit passes, the CTA is aborting, or another CTA reported an error.
-__device__ __noinline__ bool wait_phase(uint64_t* bar, uint32_t parity, Shared* sh) {
+__device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, Shared* sh) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     for (uint32_t it = 1;; ++it) {
@@ -163,39 +164,35 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&v);
 }
 
-// Row maximum of 32 score columns; columns >= lim are masked when MASK.
+// Row maximum of the 128 score columns; columns >= lim are masked when MASK.
 template <bool MASK>
-__device__ __forceinline__ float chunk_max(const uint32_t (&r)[32], int base, int lim, float m) {
-    float a = m, b = -INFINITY, c = -INFINITY, d = -INFINITY;
+__device__ __forceinline__ float row_max(const uint32_t (&r)[BN], int lim, float m) {
+    float acc[4] = {m, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-    for (int e = 0; e < 32; e += 4) {
-        float x0 = __uint_as_float(r[e]), x1 = __uint_as_float(r[e + 1]);
-        float x2 = __uint_as_float(r[e + 2]), x3 = __uint_as_float(r[e + 3]);
-        if (MASK) {
-            x0 = base + e < lim ? x0 : -INFINITY;
-            x1 = base + e + 1 < lim ? x1 : -INFINITY;
-            x2 = base + e + 2 < lim ? x2 : -INFINITY;
-            x3 = base + e + 3 < lim ? x3 : -INFINITY;
+    for (int e = 0; e < BN; e += 8) {
+        float x[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            x[u] = __uint_as_float(r[e + u]);
+            if (MASK) x[u] = e + u < lim ? x[u] : -INFINITY;
         }
-        a = fmaxf(a, x0);
-        b = fmaxf(b, x1);
-        c = fmaxf(c, x2);
-        d = fmaxf(d, x3);
+        acc[(e >> 3) & 3] = fmax3(acc[(e >> 3) & 3], fmax3(x[0], x[1], x[2]), fmax3(x[3], x[4], fmax3(x[5], x[6], x[7])));
     }
-    return fmaxf(fmaxf(a, b), fmaxf(c, d));
+    return fmax3(acc[0], acc[1], fmax3(acc[2], acc[3], -INFINITY));
 }
 
-// P = exp2(S*scale - m) for 32 columns, packed into 16 bf16 pairs; returns the row sum.
+// P = exp2(S*scale - m) for columns [32c, 32c+32), packed into 16 bf16 pairs; returns their sum.
 template <bool MASK>
-__device__ __forceinline__ float chunk_exp(const uint32_t (&r)[32], int base, int lim, float scale, float neg_m,
+__device__ __forceinline__ float chunk_exp(const uint32_t (&r)[BN], int c, int lim, float scale, float neg_m,
                                            uint32_t (&pk)[16]) {
     float s0 = 0.f, s1 = 0.f;
 #pragma unroll
     for (int e = 0; e < 32; e += 2) {
-        float x0 = __uint_as_float(r[e]), x1 = __uint_as_float(r[e + 1]);
+        const int col = c * 32 + e;
+        float x0 = __uint_as_float(r[col]), x1 = __uint_as_float(r[col + 1]);
         if (MASK) {
-            x0 = base + e < lim ? x0 : -INFINITY;
-            x1 = base + e + 1 < lim ? x1 : -INFINITY;
+            x0 = col < lim ? x0 : -INFINITY;
+            x1 = col + 1 < lim ? x1 : -INFINITY;
         }
         const float e0 = ex2_approx(fmaf(x0, scale, neg_m));
         const float e1 = ex2_approx(fmaf(x1, scale, neg_m));
@@ -260,8 +257,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
 
     if (warp == kProducerWarp) {
         // ------------------------------------------------------------ TMA producer
+        // The whole warp runs the loop (so it never diverges against a block barrier);
+        // lane 0 issues the copies.
+        int issued[kSlots] = {0, 0, 0, 0};
         if (lane == 0) {
-            int issued[kSlots] = {0, 0, 0, 0};
             for (int t = 0; t < (has_q1 ? 2 : 1); ++t) {
                 const TileCoord qc = tile_coord(p, rank, (qt0 + t) * BM);
                 mbar_arrive_expect_tx(&bars[B_Q_FULL + t], L::kTile);
@@ -270,98 +269,113 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
                     tma_load_4d(sbase + L::offQ + t * L::kTile + c * kSlab, &p.mq[qc.map], &bars[B_Q_FULL + t], c * 64,
                                 head, qc.row, bb);
             }
-            bool ok = true;
-            for (int n = 0; n < 2 * n_max && ok; ++n) {
-                const int j = n >> 1, slot = n % kSlots;
+        }
+        __syncwarp();
+        bool ok = true;
+        for (int n = 0; n < 2 * n_max; ++n) {
+            const int j = n >> 1, slot = n % kSlots;
+            ok = wait_phase_warp(&bars[B_KV_EMPTY + slot], ((n / kSlots) & 1) ^ 1, sh);
+            if (!ok) break;
+            if (lane == 0) {
                 const TileCoord kc = tile_coord(p, rank, j * BN);
-                ok = wait_phase(&bars[B_KV_EMPTY + slot], ((n / kSlots) & 1) ^ 1, sh);
-                if (!ok) break;
                 const CUtensorMap* map = (n & 1) ? &p.mv[kc.map] : &p.mk[kc.map];
                 mbar_arrive_expect_tx(&bars[B_KV_FULL + slot], L::kTile);
 #pragma unroll
                 for (int c = 0; c < D / 64; ++c)
                     tma_load_4d(sbase + L::offKV + slot * L::kTile + c * kSlab, map, &bars[B_KV_FULL + slot], c * 64,
                                 kvh, kc.row, bb);
-                ++issued[slot];
             }
-            if (!ok) {  // every copy issued must land before shared memory goes away
-                for (int slot = 0; slot < kSlots; ++slot)
-                    if (issued[slot]) drain_phase(&bars[B_KV_FULL + slot], (issued[slot] - 1) & 1);
-                drain_phase(&bars[B_Q_FULL], 0);
-                if (has_q1) drain_phase(&bars[B_Q_FULL + 1], 0);
-            }
+            ++issued[slot];
+            __syncwarp();
+        }
+        if (!ok) {  // every copy issued must land before shared memory goes away
+            for (int slot = 0; slot < kSlots; ++slot)
+                if (issued[slot]) drain_phase(&bars[B_KV_FULL + slot], (issued[slot] - 1) & 1);
+            drain_phase(&bars[B_Q_FULL], 0);
+            if (has_q1) drain_phase(&bars[B_Q_FULL + 1], 0);
         }
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            const uint32_t tS[2] = {tmem, tmem + 128u};
-            const uint32_t tO[2] = {tmem + 256u, tmem + 384u};
-            const int nt[2] = {n0, n1};
-            auto kv_slot = [](int n) { return n % kSlots; };
-            auto kv_par = [](int n) { return (uint32_t)((n / kSlots) & 1); };
-            auto issue_s = [&](int t, int j) {  // S_t = Q_t K_j^T
-                const uint32_t kaddr = sbase + L::offKV + kv_slot(2 * j) * L::kTile;
-                const uint32_t qaddr = sbase + L::offQ + t * L::kTile;
+        // The whole warp runs the loop and waits; lane 0 issues every tcgen05.mma/commit.
+        const uint32_t tS[2] = {tmem, tmem + 128u};
+        const uint32_t tO[2] = {tmem + 256u, tmem + 384u};
+        const int nt[2] = {n0, n1};
+        const bool leader = lane == 0;
+        auto kv_slot = [](int n) { return n % kSlots; };
+        auto kv_par = [](int n) { return (uint32_t)((n / kSlots) & 1); };
+        // descriptor bases; K-steps advance the start address field (bytes >> 4)
+        const uint64_t dq0 = smem_desc_sw128(sbase + L::offQ, 16, 1024);
+        const uint64_t dkv0 = smem_desc_sw128(sbase + L::offKV, 16, 1024);
+        const uint64_t dv0 = smem_desc_sw128(sbase + L::offKV, kSlab, 1024);
+        auto issue_s = [&](int t, int j) {  // S_t = Q_t K_j^T
+            const uint64_t qd = dq0 + ((t * L::kTile) >> 4);
+            const uint64_t kd = dkv0 + ((kv_slot(2 * j) * L::kTile) >> 4);
 #pragma unroll
-                for (int kk = 0; kk < KSTEPS_QK; ++kk) {
-                    const uint64_t da = smem_desc_sw128(qaddr + (kk >> 2) * kSlab + (kk & 3) * 32, 16, 1024);
-                    const uint64_t db = smem_desc_sw128(kaddr + (kk >> 2) * kSlab + (kk & 3) * 32, 16, 1024);
-                    mma_bf16_ss(tS[t], da, db, kIdescQK, kk > 0 ? 1u : 0u);
-                }
-            };
-            auto issue_pv = [&](int t, int j) {  // O_t += P_t V_j, P_t from tensor memory
-                const uint32_t vaddr = sbase + L::offKV + kv_slot(2 * j + 1) * L::kTile;
-#pragma unroll
-                for (int kk = 0; kk < KSTEPS_PV; ++kk) {
-                    // V is [keys][d], d contiguous: MN-major B; 64-column slabs kSlab apart
-                    // (leading offset), 8-key groups 1024 bytes apart (stride offset)
-                    const uint64_t db = smem_desc_sw128(vaddr + kk * 16 * 128, kSlab, 1024);
-                    mma_bf16_ts(tO[t], tS[t] + kk * 8, db, kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
-                }
-            };
-            bool ok = wait_phase(&bars[B_Q_FULL], 0, sh);
-            if (ok && has_q1) ok = wait_phase(&bars[B_Q_FULL + 1], 0, sh);
-            if (ok) ok = wait_phase(&bars[B_KV_FULL + kv_slot(0)], kv_par(0), sh);
-            if (ok) {
-                tc_fence_after();
-                for (int t = 0; t < 2; ++t)
-                    if (nt[t] > 0) {
-                        issue_s(t, 0);
-                        mma_commit(&bars[B_S_FULL + t]);
-                    }
-                mma_commit(&bars[B_KV_EMPTY + kv_slot(0)]);
+            for (int kk = 0; kk < KSTEPS_QK; ++kk) {
+                const uint32_t off = ((kk >> 2) * kSlab + (kk & 3) * 32) >> 4;
+                mma_bf16_ss(tS[t], qd + off, kd + off, kIdescQK, kk > 0 ? 1u : 0u);
             }
-            for (int j = 0; j < n_max && ok; ++j) {
-                ok = wait_phase(&bars[B_KV_FULL + kv_slot(2 * j + 1)], kv_par(2 * j + 1), sh);
-                const bool next = j + 1 < n_max;
-                bool k_next_ready = false;
-                for (int t = 0; t < 2 && ok; ++t) {
-                    if (j >= nt[t]) continue;
-                    ok = wait_phase(&bars[B_P_FULL + t], j & 1, sh);
-                    if (!ok) break;
+        };
+        auto issue_pv = [&](int t, int j) {  // O_t += P_t V_j, P_t from tensor memory
+            // V is [keys][d], d contiguous: MN-major B; 64-column slabs kSlab apart (leading
+            // offset), 8-key groups 1024 bytes apart (stride offset)
+            const uint64_t vd = dv0 + ((kv_slot(2 * j + 1) * L::kTile) >> 4);
+#pragma unroll
+            for (int kk = 0; kk < KSTEPS_PV; ++kk)
+                mma_bf16_ts(tO[t], tS[t] + kk * 8, vd + ((kk * 16 * 128) >> 4), kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+        };
+        bool ok = wait_phase_warp(&bars[B_Q_FULL], 0, sh);
+        if (ok && has_q1) ok = wait_phase_warp(&bars[B_Q_FULL + 1], 0, sh);
+        if (ok) ok = wait_phase_warp(&bars[B_KV_FULL + kv_slot(0)], kv_par(0), sh);
+        if (ok && leader) {
+            tc_fence_after();
+            for (int t = 0; t < 2; ++t)
+                if (nt[t] > 0) {
+                    issue_s(t, 0);
+                    mma_commit(&bars[B_S_FULL + t]);
+                }
+            mma_commit(&bars[B_KV_EMPTY + kv_slot(0)]);
+        }
+        __syncwarp();
+        for (int j = 0; j < n_max && ok; ++j) {
+            ok = wait_phase_warp(&bars[B_KV_FULL + kv_slot(2 * j + 1)], kv_par(2 * j + 1), sh);
+            const bool next = j + 1 < n_max;
+            bool k_next_ready = false;
+            for (int t = 0; t < 2 && ok; ++t) {
+                if (j >= nt[t]) continue;
+                ok = wait_phase_warp(&bars[B_P_FULL + t], j & 1, sh);
+                if (!ok) break;
+                if (leader) {
                     tc_fence_after();
                     issue_pv(t, j);
-                    if (j + 1 < nt[t]) {
-                        if (!k_next_ready) {  // K_{j+1} is only needed from here on
-                            ok = wait_phase(&bars[B_KV_FULL + kv_slot(2 * j + 2)], kv_par(2 * j + 2), sh);
-                            if (!ok) break;
-                            tc_fence_after();
-                            k_next_ready = true;
-                        }
+                }
+                if (j + 1 < nt[t]) {
+                    if (!k_next_ready) {  // K_{j+1} is only needed from here on
+                        ok = wait_phase_warp(&bars[B_KV_FULL + kv_slot(2 * j + 2)], kv_par(2 * j + 2), sh);
+                        if (!ok) break;
+                        k_next_ready = true;
+                    }
+                    if (leader) {
+                        tc_fence_after();
                         issue_s(t, j + 1);
                         mma_commit(&bars[B_S_FULL + t]);
-                    } else {
-                        mma_commit(&bars[B_O_FINAL + t]);
                     }
+                } else if (leader) {
+                    mma_commit(&bars[B_O_FINAL + t]);
                 }
-                if (!ok) break;
+                __syncwarp();
+            }
+            if (!ok) break;
+            if (leader) {
                 mma_commit(&bars[B_KV_EMPTY + kv_slot(2 * j + 1)]);
                 if (next) mma_commit(&bars[B_KV_EMPTY + kv_slot(2 * j + 2)]);
             }
-            // every MMA issued above completes before tensor memory is released
-            mma_commit(&bars[B_MMA_DONE]);
-            drain_phase(&bars[B_MMA_DONE], 0);
+            __syncwarp();
         }
+        // every MMA issued above completes before tensor memory is released
+        if (leader) mma_commit(&bars[B_MMA_DONE]);
+        __syncwarp();
+        drain_phase(&bars[B_MMA_DONE], 0);
     } else {
         // ------------------------------------------------------------ softmax warps
         const int t = warp >> 2;           // query tile of this group
@@ -383,19 +397,22 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
             const int k0 = j * BN;
             const bool need_mask = (p.causal && k0 + BN - 1 > q0) || k0 + BN > p.s;
             const int lim = min(p.s - k0, p.causal ? qrow - k0 + 1 : BN);  // visible columns of this row
-            // pass 1: row maximum
-            float mx = -INFINITY;
+            // the whole S row in one tensor-memory load, its maximum, then the exponentials
+            uint32_t sr[BN];
+            tmem_ld128(tS, sr);
+            tmem_wait_ld();
+            const float mx = need_mask ? row_max<true>(sr, lim, -INFINITY) : row_max<false>(sr, lim, -INFINITY);
+            const float mx2 = mx * scale;
+            float m_new = (j == 0 || mx2 > m_ref + 8.0f) ? mx2 : m_ref;
+            if (m_new == -INFINITY) m_new = 0.f;  // a row with nothing visible yet (padding rows only)
+            float rsum = 0.f;
 #pragma unroll
             for (int c = 0; c < BN / 32; ++c) {
-                uint32_t r[32];
-                tmem_ld32(tS + c * 32, r);
-                tmem_wait_ld();
-                mx = need_mask ? chunk_max<true>(r, c * 32, lim, mx) : chunk_max<false>(r, c * 32, lim, mx);
+                uint32_t pk[16];
+                rsum += need_mask ? chunk_exp<true>(sr, c, lim, scale, -m_new, pk)
+                                  : chunk_exp<false>(sr, c, lim, scale, -m_new, pk);
+                tmem_st16(tS + c * 16, pk);
             }
-            const float mx2 = mx * scale;
-            float m_new = m_ref;
-            if (j == 0 || mx2 > m_ref + 8.0f) m_new = mx2;
-            if (m_new == -INFINITY) m_new = 0.f;  // a row with nothing visible yet (padding rows only)
             const float alpha = (j == 0) ? 0.f : ex2_approx(m_ref - m_new);
             // O_t already holds P_t(j-1) V_{j-1} (S_t(j) was issued after it): rescale in place
             if (j > 0 && __any_sync(0xffffffffu, m_new != m_ref)) {
@@ -409,18 +426,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
                     for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * f);
                     tmem_st32(tO + c * 32, r);
                 }
-            }
-            // pass 2: P = exp2(S*scale - m) as bf16 pairs over the first 64 columns of S_t
-            const float neg_m = -m_new;
-            float rsum = 0.f;
-#pragma unroll
-            for (int c = 0; c < BN / 32; ++c) {
-                uint32_t r[32], pk[16];
-                tmem_ld32(tS + c * 32, r);
-                tmem_wait_ld();
-                rsum += need_mask ? chunk_exp<true>(r, c * 32, lim, scale, neg_m, pk)
-                                  : chunk_exp<false>(r, c * 32, lim, scale, neg_m, pk);
-                tmem_st16(tS + c * 16, pk);  // columns already read
             }
             tmem_wait_st();
             tc_fence_before();
