@@ -37,6 +37,23 @@ WORKLOAD_NAME = "DiT-like MHA: P=4 b=2 s=4096 h=32 d=128 bf16, non-causal + caus
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
+def reduce_max_over_ranks(values, device="cpu"):
+    """Element-wise maximum over all ranks of the job (identity when not distributed)."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return list(values)
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def job_throughput(units_per_rank, world, slowest_ms):
+    """Whole-job rate: every rank processed units_per_rank; the job took the slowest rank's time."""
+    return world * units_per_rank / (slowest_ms * 1e-3)
+
+
 def attn_flops(b, s, hq, d, causal):
     """Algorithmic FLOP of attention: 4*b*h*d per visible (query, key) pair."""
     pairs = s * (s + 1) // 2 if causal else s * s
@@ -329,17 +346,13 @@ def main():
     if world > 1:
         torch.distributed.init_process_group("nccl")
     res = run_gpu(args, rank, world)
-    total_ms, e2e_ms = res["total_ms"], res["e2e_ms"]
-    if world > 1:
-        t = torch.tensor([total_ms, e2e_ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms, e2e_ms = t.tolist()
+    total_ms, e2e_ms = reduce_max_over_ranks([res["total_ms"], res["e2e_ms"]], device="cuda")
     if rank != 0:
         torch.distributed.destroy_process_group()
         return
     peaks, peak_src = load_peaks()
-    value = world * res["step_flops"] * args.steps / (total_ms * 1e-3) / 1e12
-    e2e_value = world * res["step_flops"] * args.steps / (e2e_ms * 1e-3) / 1e12
+    value = job_throughput(res["step_flops"] * args.steps, world, total_ms) / 1e12
+    e2e_value = job_throughput(res["step_flops"] * args.steps, world, e2e_ms) / 1e12
     cpu = None
     if not args.no_cpu_baseline and world == 1:
         cpu = cpu_baseline_obj(oracle_sample(budget_s=12.0))
