@@ -296,11 +296,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         }
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
-        // The whole warp runs the loop and waits; lane 0 issues every tcgen05.mma/commit.
+        // The whole warp runs the loop with warp-uniform operands; one elected lane issues
+        // every tcgen05.mma and tcgen05.commit.
         const uint32_t tS[2] = {tmem, tmem + 128u};
         const uint32_t tO[2] = {tmem + 256u, tmem + 384u};
         const int nt[2] = {n0, n1};
-        const bool leader = lane == 0;
         auto kv_slot = [](int n) { return n % kSlots; };
         auto kv_par = [](int n) { return (uint32_t)((n / kSlots) & 1); };
         // descriptor bases; K-steps advance the start address field (bytes >> 4)
@@ -313,7 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
 #pragma unroll
             for (int kk = 0; kk < KSTEPS_QK; ++kk) {
                 const uint32_t off = ((kk >> 2) * kSlab + (kk & 3) * 32) >> 4;
-                mma_bf16_ss(tS[t], qd + off, kd + off, kIdescQK, kk > 0 ? 1u : 0u);
+                mma_bf16_ss_warp(tS[t], qd + off, kd + off, kIdescQK, kk > 0 ? 1u : 0u);
             }
         };
         auto issue_pv = [&](int t, int j) {  // O_t += P_t V_j, P_t from tensor memory
@@ -322,19 +322,19 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
             const uint64_t vd = dv0 + ((kv_slot(2 * j + 1) * L::kTile) >> 4);
 #pragma unroll
             for (int kk = 0; kk < KSTEPS_PV; ++kk)
-                mma_bf16_ts(tO[t], tS[t] + kk * 8, vd + ((kk * 16 * 128) >> 4), kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+                mma_bf16_ts_warp(tO[t], tS[t] + kk * 8, vd + ((kk * 16 * 128) >> 4), kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
         };
         bool ok = wait_phase_warp(&bars[B_Q_FULL], 0, sh);
         if (ok && has_q1) ok = wait_phase_warp(&bars[B_Q_FULL + 1], 0, sh);
         if (ok) ok = wait_phase_warp(&bars[B_KV_FULL + kv_slot(0)], kv_par(0), sh);
-        if (ok && leader) {
+        if (ok) {
             tc_fence_after();
             for (int t = 0; t < 2; ++t)
                 if (nt[t] > 0) {
                     issue_s(t, 0);
-                    mma_commit(&bars[B_S_FULL + t]);
+                    mma_commit_warp(&bars[B_S_FULL + t]);
                 }
-            mma_commit(&bars[B_KV_EMPTY + kv_slot(0)]);
+            mma_commit_warp(&bars[B_KV_EMPTY + kv_slot(0)]);
         }
         __syncwarp();
         for (int j = 0; j < n_max && ok; ++j) {
@@ -345,35 +345,29 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
                 if (j >= nt[t]) continue;
                 ok = wait_phase_warp(&bars[B_P_FULL + t], j & 1, sh);
                 if (!ok) break;
-                if (leader) {
-                    tc_fence_after();
-                    issue_pv(t, j);
-                }
+                tc_fence_after();
+                issue_pv(t, j);
                 if (j + 1 < nt[t]) {
                     if (!k_next_ready) {  // K_{j+1} is only needed from here on
                         ok = wait_phase_warp(&bars[B_KV_FULL + kv_slot(2 * j + 2)], kv_par(2 * j + 2), sh);
                         if (!ok) break;
                         k_next_ready = true;
                     }
-                    if (leader) {
-                        tc_fence_after();
-                        issue_s(t, j + 1);
-                        mma_commit(&bars[B_S_FULL + t]);
-                    }
-                } else if (leader) {
-                    mma_commit(&bars[B_O_FINAL + t]);
+                    tc_fence_after();
+                    issue_s(t, j + 1);
+                    mma_commit_warp(&bars[B_S_FULL + t]);
+                } else {
+                    mma_commit_warp(&bars[B_O_FINAL + t]);
                 }
                 __syncwarp();
             }
             if (!ok) break;
-            if (leader) {
-                mma_commit(&bars[B_KV_EMPTY + kv_slot(2 * j + 1)]);
-                if (next) mma_commit(&bars[B_KV_EMPTY + kv_slot(2 * j + 2)]);
-            }
+            mma_commit_warp(&bars[B_KV_EMPTY + kv_slot(2 * j + 1)]);
+            if (next) mma_commit_warp(&bars[B_KV_EMPTY + kv_slot(2 * j + 2)]);
             __syncwarp();
         }
         // every MMA issued above completes before tensor memory is released
-        if (leader) mma_commit(&bars[B_MMA_DONE]);
+        mma_commit_warp(&bars[B_MMA_DONE]);
         __syncwarp();
         drain_phase(&bars[B_MMA_DONE], 0);
     } else {
