@@ -194,10 +194,11 @@ __device__ __forceinline__ float chunk_exp(const uint32_t (&r)[BN], int c, int l
             x0 = col < lim ? x0 : -INFINITY;
             x1 = col + 1 < lim ? x1 : -INFINITY;
         }
-        const float e0 = ex2_approx(fmaf(x0, scale, neg_m));
-        const float e1 = ex2_approx(fmaf(x1, scale, neg_m));
-        s0 += e0;
-        s1 += e1;
+        float a0, a1;
+        ffma2(a0, a1, x0, x1, scale, scale, neg_m, neg_m);  // S*scale - m for two columns at once
+        const float e0 = ex2_approx(a0);
+        const float e1 = ex2_approx(a1);
+        fadd2(s0, s1, s0, s1, e0, e1);
         pk[e >> 1] = pack_bf16x2(e0, e1);
     }
     return s0 + s1;
@@ -257,36 +258,29 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
 
     if (warp == kProducerWarp) {
         // ------------------------------------------------------------ TMA producer
-        // The whole warp runs the loop (so it never diverges against a block barrier);
-        // lane 0 issues the copies.
+        // The whole warp runs the loop with warp-uniform operands; one elected lane issues.
         int issued[kSlots] = {0, 0, 0, 0};
-        if (lane == 0) {
-            for (int t = 0; t < (has_q1 ? 2 : 1); ++t) {
-                const TileCoord qc = tile_coord(p, rank, (qt0 + t) * BM);
-                mbar_arrive_expect_tx(&bars[B_Q_FULL + t], L::kTile);
+        for (int t = 0; t < (has_q1 ? 2 : 1); ++t) {
+            const TileCoord qc = tile_coord(p, rank, (qt0 + t) * BM);
+            mbar_arrive_expect_tx_warp(&bars[B_Q_FULL + t], L::kTile);
 #pragma unroll
-                for (int c = 0; c < D / 64; ++c)
-                    tma_load_4d(sbase + L::offQ + t * L::kTile + c * kSlab, &p.mq[qc.map], &bars[B_Q_FULL + t], c * 64,
-                                head, qc.row, bb);
-            }
+            for (int c = 0; c < D / 64; ++c)
+                tma_load_4d_warp(sbase + L::offQ + t * L::kTile + c * kSlab, &p.mq[qc.map], &bars[B_Q_FULL + t],
+                                 c * 64, head, qc.row, bb);
         }
-        __syncwarp();
         bool ok = true;
         for (int n = 0; n < 2 * n_max; ++n) {
             const int j = n >> 1, slot = n % kSlots;
             ok = wait_phase_warp(&bars[B_KV_EMPTY + slot], ((n / kSlots) & 1) ^ 1, sh);
             if (!ok) break;
-            if (lane == 0) {
-                const TileCoord kc = tile_coord(p, rank, j * BN);
-                const CUtensorMap* map = (n & 1) ? &p.mv[kc.map] : &p.mk[kc.map];
-                mbar_arrive_expect_tx(&bars[B_KV_FULL + slot], L::kTile);
+            const TileCoord kc = tile_coord(p, rank, j * BN);
+            const CUtensorMap* map = (n & 1) ? &p.mv[kc.map] : &p.mk[kc.map];
+            mbar_arrive_expect_tx_warp(&bars[B_KV_FULL + slot], L::kTile);
 #pragma unroll
-                for (int c = 0; c < D / 64; ++c)
-                    tma_load_4d(sbase + L::offKV + slot * L::kTile + c * kSlab, map, &bars[B_KV_FULL + slot], c * 64,
-                                kvh, kc.row, bb);
-            }
+            for (int c = 0; c < D / 64; ++c)
+                tma_load_4d_warp(sbase + L::offKV + slot * L::kTile + c * kSlab, map, &bars[B_KV_FULL + slot], c * 64,
+                                 kvh, kc.row, bb);
             ++issued[slot];
-            __syncwarp();
         }
         if (!ok) {  // every copy issued must land before shared memory goes away
             for (int slot = 0; slot < kSlots; ++slot)
