@@ -32,8 +32,20 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "Ulysses attn fwd TFLOP/s + a2a permute GB/s, as fraction of GB300 roofline"
-WORKLOAD = dict(P=4, b=2, s=4096, h_q=32, h_kv=32, d=128)
-WORKLOAD_NAME = "DiT-like MHA: P=4 b=2 s=4096 h=32 d=128 bf16, non-causal + causal, unfused + fused forward"
+# The default line is the DiT-like workload; the others are the named configurations,
+# measured on request (--workload).
+WORKLOADS = {
+    "dit": dict(P=4, b=2, s=4096, h_q=32, h_kv=32, d=128, dtype="bf16", masks=(False, True),
+                name="DiT-like MHA: P=4 b=2 s=4096 h=32 d=128 bf16, non-causal + causal, unfused + fused forward"),
+    "gqa": dict(P=8, b=1, s=32768, h_q=32, h_kv=8, d=128, dtype="bf16", masks=(True,),
+                name="GQA causal: P=8 b=1 s=32768 h_q=32 h_kv=8 d=128 bf16, unfused + fused forward"),
+    "long": dict(P=8, b=1, s=131072, h_q=64, h_kv=64, d=128, dtype="bf16", masks=(True,),
+                 name="Long-sequence causal: P=8 b=1 s=131072 h=64 d=128 bf16, unfused + fused forward"),
+    "tiny": dict(P=2, b=1, s=64, h_q=4, h_kv=4, d=16, dtype="fp32", masks=(False,),
+                 name="Tiny exactness case: P=2 b=1 s=64 h=4 d=16 fp32, non-causal, unfused forward"),
+}
+WORKLOAD = WORKLOADS["dit"]
+WORKLOAD_NAME = WORKLOAD["name"]
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -138,23 +150,26 @@ def run_gpu(args, rank, world):
         torch.distributed.barrier()
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
     torch.cuda.set_device(dev)
-    w = WORKLOAD
+    w = WORKLOADS[args.workload]
     P, b, s, hq, hkv, d = w["P"], w["b"], w["s"], w["h_q"], w["h_kv"], w["d"]
     S = s // P
-    qs, ks, vs = seq_shards_qkv(P, b, s, hq, hkv, d, torch.bfloat16, seed=rank, device=str(dev))
-    q_head = [torch.empty((b, s, hq // P, d), dtype=torch.bfloat16, device=dev) for _ in range(P)]
-    k_head = [torch.empty((b, s, hkv // P, d), dtype=torch.bfloat16, device=dev) for _ in range(P)]
-    v_head = [torch.empty((b, s, hkv // P, d), dtype=torch.bfloat16, device=dev) for _ in range(P)]
-    o_head = [torch.empty((b, s, hq // P, d), dtype=torch.bfloat16, device=dev) for _ in range(P)]
-    o_seq = [torch.empty((b, S, hq, d), dtype=torch.bfloat16, device=dev) for _ in range(P)]
-    o_fused = [torch.empty((b, S, hq, d), dtype=torch.bfloat16, device=dev) for _ in range(P)]
+    dt = torch.bfloat16 if w["dtype"] == "bf16" else torch.float32
+    esz = 2 if dt == torch.bfloat16 else 4
+    fused_ok = dt == torch.bfloat16 and S % 128 == 0 and P <= 16
+    qs, ks, vs = seq_shards_qkv(P, b, s, hq, hkv, d, dt, seed=rank, device=str(dev))
+    q_head = [torch.empty((b, s, hq // P, d), dtype=dt, device=dev) for _ in range(P)]
+    k_head = [torch.empty((b, s, hkv // P, d), dtype=dt, device=dev) for _ in range(P)]
+    v_head = [torch.empty((b, s, hkv // P, d), dtype=dt, device=dev) for _ in range(P)]
+    o_head = [torch.empty((b, s, hq // P, d), dtype=dt, device=dev) for _ in range(P)]
+    o_seq = [torch.empty((b, S, hq, d), dtype=dt, device=dev) for _ in range(P)]
+    o_fused = [torch.empty((b, S, hq, d), dtype=dt, device=dev) for _ in range(P)]
     stream = torch.cuda.current_stream(dev)
 
     # (label, kind, bytes moved, flops, callable); one kernel launch each
-    tensor_bytes = b * s * hq * d * 2
-    kv_bytes = b * s * hkv * d * 2
+    tensor_bytes = b * s * hq * d * esz
+    kv_bytes = b * s * hkv * d * esz
     ops = []
-    for causal in (False, True):
+    for causal in w["masks"]:
         fl = attn_flops(b, s, hq, d, causal)
         tag = "causal" if causal else "noncausal"
         ops += [
@@ -164,10 +179,11 @@ def run_gpu(args, rank, world):
             (f"attn_{tag}", "attention", 0, fl,
              (lambda c=causal: uly.ulysses_local_attention(q_head, k_head, v_head, c, o_head))),
             (f"a2a_head2seq_o", "permute", 2 * tensor_bytes, 0, lambda: uly.ulysses_a2a_head2seq(o_head, o_seq)),
-            (f"fused_{tag}", "fused", 0, fl,
-             (lambda c=causal: uly.ulysses_dist_attn_fwd(qs, ks, vs, c, fused=True, out_seq=o_fused))),
         ]
-    step_flops = 2 * (attn_flops(b, s, hq, d, False) + attn_flops(b, s, hq, d, True))
+        if fused_ok:
+            ops.append((f"fused_{tag}", "fused", 0, fl,
+                        (lambda c=causal: uly.ulysses_dist_attn_fwd(qs, ks, vs, c, fused=True, out_seq=o_fused))))
+    step_flops = sum(op[3] for op in ops)
 
     def step(events=None):
         for n, op in enumerate(ops):
@@ -225,20 +241,21 @@ def run_gpu(args, rank, world):
     host_q = [t.cpu().pin_memory() for t in qs]
     host_k = [t.cpu().pin_memory() for t in ks]
     host_v = [t.cpu().pin_memory() for t in vs]
-    host_o = [torch.empty((b, S, hq, d), dtype=torch.bfloat16).pin_memory() for _ in range(P)]
+    host_o = [torch.empty((b, S, hq, d), dtype=dt).pin_memory() for _ in range(P)]
     dq = [torch.empty_like(t) for t in qs]
     dk = [torch.empty_like(t) for t in ks]
     dv = [torch.empty_like(t) for t in vs]
-    h2d = sum(t.numel() * 2 for t in host_q + host_k + host_v)
-    d2h = 4 * sum(t.numel() * 2 for t in host_o)
-    ws = torch.empty(uly.ulysses_dist_attn_workspace_bytes(P, b, s, hq, hkv, d, torch.bfloat16, False),
+    fused_modes = (False, True) if fused_ok else (False,)
+    h2d = sum(t.numel() * esz for t in host_q + host_k + host_v)
+    d2h = len(w["masks"]) * len(fused_modes) * sum(t.numel() * esz for t in host_o)
+    ws = torch.empty(uly.ulysses_dist_attn_workspace_bytes(P, b, s, hq, hkv, d, dt, False),
                      dtype=torch.uint8, device=dev)
 
     def e2e_step():
         for src, dst in zip(host_q + host_k + host_v, dq + dk + dv):
             dst.copy_(src, non_blocking=True)
-        for causal in (False, True):
-            for fused in (False, True):
+        for causal in w["masks"]:
+            for fused in fused_modes:
                 out = uly.ulysses_dist_attn_fwd(dq, dk, dv, causal, fused=fused, workspace=None if fused else ws)
                 for o, ho in zip(out, host_o):
                     ho.copy_(o, non_blocking=True)
@@ -306,6 +323,78 @@ def cpu_baseline_obj(smp):
                        f"({smp['perm_gbs']:.2f} GB/s); single thread of {os.cpu_count()} host cores")}
 
 
+def kernel_source_digest():
+    """Digest of the attention kernel's sources (the traffic figure belongs to one version)."""
+    import hashlib
+
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "sequence_attention_seq_gb300", "csrc")
+    for name in ("attn_tc.cu", "device_common.cuh"):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def measured_traffic(workload):
+    """DRAM bytes per attention launch from the committed ncu capture, if it was taken on
+    this exact kernel source and workload; else None."""
+    path = os.path.join(ROOT, "profiles", "attn_tc_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except Exception:  # noqa: BLE001
+        return None
+    if rec.get("source_sha256") != kernel_source_digest() or rec.get("workload") != workload:
+        return None
+    return rec.get("dram_bytes_per_launch_mean")
+
+
+def run_permute_sweep(args):
+    """Exchange bandwidth over bf16 [P][1, s/P, 64, 128] with uniform random bits."""
+    import torch
+
+    import sequence_attention_seq_gb300 as uly
+    from sequence_attention_seq_gb300 import build as uly_build
+    from sequence_attention_seq_gb300.inputs import random_bits
+
+    uly_build.build()
+    peaks, _ = load_peaks()
+    h, d = 64, 128
+    rows = []
+    for s in (8192, 32768, 131072, 262144):
+        for P in (2, 4, 8, 16, 32, 64):
+            xs = [random_bits((1, s // P, h, d), torch.bfloat16, seed=j, device="cuda") for j in range(P)]
+            hd = [torch.empty((1, s, h // P, d), dtype=torch.bfloat16, device="cuda") for _ in range(P)]
+            back = [torch.empty_like(x) for x in xs]
+            nbytes = 2 * s * h * d * 2
+            res = {}
+            for name, fn in (("seq2head", lambda: uly.ulysses_a2a_seq2head(xs, hd)),
+                             ("head2seq", lambda: uly.ulysses_a2a_head2seq(hd, back))):
+                for _ in range(max(3, args.warmup)):
+                    fn()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                reps = 20
+                torch.cuda.synchronize()
+                e0.record()
+                for _ in range(reps):
+                    fn()
+                e1.record()
+                torch.cuda.synchronize()
+                res[name] = nbytes / (e0.elapsed_time(e1) / reps * 1e-3) / 1e9
+            exact = all(torch.equal(a.view(torch.int16), c.view(torch.int16)) for a, c in zip(xs, back))
+            row = {"s": s, "P": P, "run_bytes": h // P * d * 2, "seq2head_gbs": res["seq2head"],
+                   "head2seq_gbs": res["head2seq"], "round_trip_bit_exact": exact}
+            rows.append(row)
+            print(json.dumps(row))
+            del xs, hd, back
+            torch.cuda.empty_cache()
+    allv = [r[k] for r in rows for k in ("seq2head_gbs", "head2seq_gbs")]
+    print(json.dumps({"metric": "a2a permute GB/s (read+write), bf16 [P][1,s/P,64,128] sweep", "unit": "GB/s",
+                      "min": min(allv), "median": statistics.median(allv), "max": max(allv),
+                      "peak": peaks["hbm_gbs"], "median_frac": statistics.median(allv) / peaks["hbm_gbs"],
+                      "all_bit_exact": all(r["round_trip_bit_exact"] for r in rows)}))
+
+
 # -------------------------------------------------------------------------- main
 def main():
     ap = argparse.ArgumentParser()
@@ -314,13 +403,23 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default="dit", choices=sorted(WORKLOADS))
+    ap.add_argument("--permute-sweep", action="store_true",
+                    help="measure the exchanges over the permute-only sweep instead of the forward")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
-    w = WORKLOAD
-    config = {"workload": WORKLOAD_NAME, "P": w["P"], "b": w["b"], "s": w["s"], "h_q": w["h_q"], "h_kv": w["h_kv"],
-              "d": w["d"], "l2": "inputs larger than L2 (Q+K+V+O = 256 MiB > 129 MB); no flush"}
+    if args.permute_sweep:
+        if rank == 0:
+            run_permute_sweep(args)
+        return
+    w = WORKLOADS[args.workload]
+    esz = 2 if w["dtype"] == "bf16" else 4
+    io_bytes = (2 * w["h_q"] + 2 * w["h_kv"]) * w["b"] * w["s"] * w["d"] * esz
+    config = {"workload": w["name"], "P": w["P"], "b": w["b"], "s": w["s"], "h_q": w["h_q"], "h_kv": w["h_kv"],
+              "d": w["d"], "l2": (f"inputs larger than L2 (Q+K+V+O = {io_bytes / 2**20:.0f} MiB > 129 MB); no flush"
+                                  if io_bytes > 129e6 else "inputs smaller than L2: latency-bound exactness case")}
 
     if args.impl == "reference":
         if rank != 0:
@@ -351,20 +450,30 @@ def main():
         torch.distributed.destroy_process_group()
         return
     peaks, peak_src = load_peaks()
+    if w["dtype"] == "bf16":
+        kernel, bound, peak, peak_note = "attn_tc_kernel<%d> (all attention launches of the step)" % w["d"], \
+            "tensor", peaks["bf16_tflops"], f"{peak_src} (bf16 dense, burst)"
+    else:  # fp32 FMA attention: plain ALU peak, 152 SMs x 128 FMA lanes x 2 flop x max SM clock
+        kernel, bound = "attn_fp32_kernel (all attention launches of the step)", "alu"
+        peak = 152 * 128 * 2 * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
+        peak_note = "derived: 152 SMs x 128 fp32 FMA/clk x 2 flop x 2070 MHz"
+    traffic = measured_traffic(args.workload)
     value = job_throughput(res["step_flops"] * args.steps, world, total_ms) / 1e12
     e2e_value = job_throughput(res["step_flops"] * args.steps, world, e2e_ms) / 1e12
     cpu = None
-    if not args.no_cpu_baseline and world == 1:
+    if not args.no_cpu_baseline and world == 1 and args.workload == "dit":
         cpu = cpu_baseline_obj(oracle_sample(budget_s=12.0))
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16)", "config": config,
-        "roofline": {"kernel": "attn_tc_kernel<128> (all attention launches of the step)", "bound": "tensor",
-                     "achieved": res["attn_tflops"], "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                     "frac": res["attn_tflops"] / peaks["bf16_tflops"],
-                     "frac_of_sustained": res["attn_tflops"] / peaks["bf16_tflops_sustained"],
-                     "peak_source": f"{peak_src} (bf16 dense, burst)", "traffic": None},
+        "vs_baseline": None, "dtype": w["dtype"], "data": f"synthetic (seeded N(0,1) {w['dtype']})",
+        "config": config,
+        "roofline": {"kernel": kernel, "bound": bound,
+                     "achieved": res["attn_tflops"], "peak": peak, "unit": "TFLOP/s",
+                     "frac": res["attn_tflops"] / peak,
+                     "frac_of_sustained": (res["attn_tflops"] / peaks["bf16_tflops_sustained"]
+                                           if bound == "tensor" else None),
+                     "peak_source": peak_note, "traffic": traffic},
         "permute": {"achieved": res["perm_gbs"], "peak": peaks["hbm_gbs"], "unit": "GB/s",
                     "frac": res["perm_gbs"] / peaks["hbm_gbs"], "bytes": "read+write of all ranks' data"},
         "per_launch_ms": res["per_op"],
