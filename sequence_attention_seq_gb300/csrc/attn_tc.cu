@@ -66,7 +66,7 @@ struct TcParams {
     CUtensorMap mq[kMaxMaps];
     CUtensorMap mk[kMaxMaps];
     CUtensorMap mv[kMaxMaps];
-    CUtensorMap mo[kMaxMaps];
+    uint8_t* optr[kMaxMaps];  // output buffers (same indexing as the maps): [b][rows][heads][d] bf16
     int s;             // sequence length
     int rows_per_map;  // tokens held by one map: s/P when fused, s otherwise
     int n_qtiles;      // ceil(s / BM)
@@ -75,6 +75,7 @@ struct TcParams {
     int g;             // query heads per K/V head
     int b;
     int nranks;        // rank groups in this launch (fused: 1)
+    int n_items;       // query-tile pairs in this launch: nranks * b * heads * n_pairs
     int causal;
     float scale_log2;  // log2(e) / sqrt(d)
 };
@@ -99,7 +100,9 @@ enum BarIdx {
     B_S_FULL = B_KV_EMPTY + kSlots,     // +tile (2)
     B_P_FULL = B_S_FULL + 2,            // +tile (2), 4 arrivals each
     B_O_FINAL = B_P_FULL + 2,           // +tile (2)
-    B_MMA_DONE = B_O_FINAL + 2,
+    B_Q_EMPTY = B_O_FINAL + 2,          // +tile (2): the last S MMA of an item has read Q_t
+    B_O_EMPTY = B_Q_EMPTY + 2,          // +tile (2), 4 arrivals each: the epilogue has read O_t
+    B_MMA_DONE = B_O_EMPTY + 2,
     B_COUNT = B_MMA_DONE + 1
 };
 
@@ -157,6 +160,53 @@ __device__ __forceinline__ TileCoord tile_coord(const TcParams& p, int rank, int
     c.map = rank + t0 / p.rows_per_map;
     c.row = t0 % p.rows_per_map;
     return c;
+}
+
+// Work item w (a query-tile pair) -> coordinates.  Every role of a CTA walks the same
+// sequence.  Causal: the pair index is slowest and descending, so items are globally
+// sorted heaviest first and the snake assignment balances the CTAs.  Non-causal (all items
+// equal): the pairs of one head are adjacent, so concurrent CTAs share K/V in L2.  In both,
+// the query heads that share a K/V head are adjacent.
+struct Item {
+    int rank, bb, kvh, head, qt0, n0, n1;
+};
+
+__device__ __forceinline__ Item decode_item(const TcParams& p, int w) {
+    Item it;
+    const int kv_heads = p.heads / p.g;
+    const int hg = w % p.g;
+    w /= p.g;
+    int pair;
+    if (p.causal) {
+        it.kvh = w % kv_heads;
+        w /= kv_heads;
+        it.bb = w % p.b;
+        w /= p.b;
+        it.rank = w % p.nranks;
+        pair = p.n_pairs - 1 - w / p.nranks;
+    } else {
+        pair = w % p.n_pairs;
+        w /= p.n_pairs;
+        it.kvh = w % kv_heads;
+        w /= kv_heads;
+        it.bb = w % p.b;
+        it.rank = w / p.b;
+    }
+    it.head = it.kvh * p.g + hg;
+    it.qt0 = 2 * pair;
+    const bool has_q1 = it.qt0 + 1 < p.n_qtiles;
+    const int n_kv_all = (p.s + BN - 1) / BN;
+    it.n0 = p.causal ? it.qt0 + 1 : n_kv_all;  // key tiles query tile 0 needs
+    it.n1 = has_q1 ? (p.causal ? it.qt0 + 2 : n_kv_all) : 0;
+    return it;
+}
+
+// The k-th item of CTA c: rounds of gridDim.x items, alternating direction (snake), so
+// the heavy-first order spreads evenly; -1 when the CTA has no k-th item.
+__device__ __forceinline__ int item_index(const TcParams& p, int k) {
+    const int G = gridDim.x, c = blockIdx.x;
+    const int w = k * G + ((k & 1) ? G - 1 - c : c);
+    return w < p.n_items ? w : -1;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -222,29 +272,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    // ---- block -> (rank, batch, kv head, query-tile pair, head within group); heavy pairs first
-    int bid = blockIdx.x;
-    const int hg = bid % p.g;
-    bid /= p.g;
-    const int pair = p.n_pairs - 1 - (bid % p.n_pairs);
-    bid /= p.n_pairs;
-    const int kv_heads = p.heads / p.g;
-    const int kvh = bid % kv_heads;
-    bid /= kv_heads;
-    const int bb = bid % p.b;
-    const int rank = bid / p.b;
-    const int head = kvh * p.g + hg;
-    const int qt0 = 2 * pair;
-    const bool has_q1 = qt0 + 1 < p.n_qtiles;
-    const int n_kv_all = (p.s + BN - 1) / BN;
-    // key tiles each query tile needs
-    const int n0 = p.causal ? qt0 + 1 : n_kv_all;
-    const int n1 = has_q1 ? (p.causal ? qt0 + 2 : n_kv_all) : 0;
-    const int n_max = n0 > n1 ? n0 : n1;
-
     if (threadIdx.x == 0) {
         sh->abort = error_word_set() ? 1 : 0;
-        for (int i = 0; i < B_COUNT; ++i) mbar_init(&bars[i], (i == B_P_FULL || i == B_P_FULL + 1) ? 4u : 1u);
+        for (int i = 0; i < B_COUNT; ++i) {
+            const bool per_warp = i == B_P_FULL || i == B_P_FULL + 1 || i == B_O_EMPTY || i == B_O_EMPTY + 1;
+            mbar_init(&bars[i], per_warp ? 4u : 1u);
+        }
         fence_mbarrier_init();
     }
     __syncthreads();
@@ -258,177 +291,214 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
 
     if (warp == kProducerWarp) {
         // ------------------------------------------------------------ TMA producer
-        // The whole warp runs the loop with warp-uniform operands; one elected lane issues.
-        int issued[kSlots] = {0, 0, 0, 0};
-        for (int t = 0; t < (has_q1 ? 2 : 1); ++t) {
-            const TileCoord qc = tile_coord(p, rank, (qt0 + t) * BM);
-            mbar_arrive_expect_tx_warp(&bars[B_Q_FULL + t], L::kTile);
-#pragma unroll
-            for (int c = 0; c < D / 64; ++c)
-                tma_load_4d_warp(sbase + L::offQ + t * L::kTile + c * kSlab, &p.mq[qc.map], &bars[B_Q_FULL + t],
-                                 c * 64, head, qc.row, bb);
-        }
+        // Whole warp, warp-uniform operands, one elected lane issues.  Q_t of the next item
+        // is loaded as soon as the last S MMA of the current item has read Q_t.
+        int n = 0;                   // ring loads issued so far (slot n % kSlots)
+        int quse[2] = {0, 0};        // Q_t loads issued so far
         bool ok = true;
-        for (int n = 0; n < 2 * n_max; ++n) {
-            const int j = n >> 1, slot = n % kSlots;
-            ok = wait_phase_warp(&bars[B_KV_EMPTY + slot], ((n / kSlots) & 1) ^ 1, sh);
-            if (!ok) break;
-            const TileCoord kc = tile_coord(p, rank, j * BN);
-            const CUtensorMap* map = (n & 1) ? &p.mv[kc.map] : &p.mk[kc.map];
-            mbar_arrive_expect_tx_warp(&bars[B_KV_FULL + slot], L::kTile);
+        for (int k = 0; ok; ++k) {
+            const int w = item_index(p, k);
+            if (w < 0) break;
+            const Item it = decode_item(p, w);
+            for (int t = 0; t < 2 && ok; ++t) {
+                if ((t ? it.n1 : it.n0) == 0) continue;
+                if (quse[t] > 0) ok = wait_phase_warp(&bars[B_Q_EMPTY + t], (quse[t] - 1) & 1, sh);
+                if (!ok) break;
+                const TileCoord qc = tile_coord(p, it.rank, (it.qt0 + t) * BM);
+                mbar_arrive_expect_tx_warp(&bars[B_Q_FULL + t], L::kTile);
 #pragma unroll
-            for (int c = 0; c < D / 64; ++c)
-                tma_load_4d_warp(sbase + L::offKV + slot * L::kTile + c * kSlab, map, &bars[B_KV_FULL + slot], c * 64,
-                                 kvh, kc.row, bb);
-            ++issued[slot];
+                for (int c = 0; c < D / 64; ++c)
+                    tma_load_4d_warp(sbase + L::offQ + t * L::kTile + c * kSlab, &p.mq[qc.map], &bars[B_Q_FULL + t],
+                                     c * 64, it.head, qc.row, it.bb);
+                ++quse[t];
+            }
+            const int n_max = it.n0 > it.n1 ? it.n0 : it.n1;
+            for (int e = 0; e < 2 * n_max && ok; ++e, ++n) {
+                const int j = e >> 1, slot = n % kSlots;
+                ok = wait_phase_warp(&bars[B_KV_EMPTY + slot], ((n / kSlots) & 1) ^ 1, sh);
+                if (!ok) break;
+                const TileCoord kc = tile_coord(p, it.rank, j * BN);
+                const CUtensorMap* map = (e & 1) ? &p.mv[kc.map] : &p.mk[kc.map];
+                mbar_arrive_expect_tx_warp(&bars[B_KV_FULL + slot], L::kTile);
+#pragma unroll
+                for (int c = 0; c < D / 64; ++c)
+                    tma_load_4d_warp(sbase + L::offKV + slot * L::kTile + c * kSlab, map, &bars[B_KV_FULL + slot],
+                                     c * 64, it.kvh, kc.row, it.bb);
+            }
         }
         if (!ok) {  // every copy issued must land before shared memory goes away
-            for (int slot = 0; slot < kSlots; ++slot)
-                if (issued[slot]) drain_phase(&bars[B_KV_FULL + slot], (issued[slot] - 1) & 1);
-            drain_phase(&bars[B_Q_FULL], 0);
-            if (has_q1) drain_phase(&bars[B_Q_FULL + 1], 0);
+            for (int slot = 0; slot < kSlots; ++slot) {
+                const int cnt = (n - slot + kSlots - 1) / kSlots;  // loads that went to this slot
+                if (cnt > 0) drain_phase(&bars[B_KV_FULL + slot], (cnt - 1) & 1);
+            }
+            for (int t = 0; t < 2; ++t)
+                if (quse[t] > 0) drain_phase(&bars[B_Q_FULL + t], (quse[t] - 1) & 1);
         }
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
-        // The whole warp runs the loop with warp-uniform operands; one elected lane issues
-        // every tcgen05.mma and tcgen05.commit.
-        const uint32_t tS[2] = {tmem, tmem + 128u};
-        const uint32_t tO[2] = {tmem + 256u, tmem + 384u};
-        const int nt[2] = {n0, n1};
+        // Whole warp, warp-uniform operands; one elected lane issues every tcgen05.mma and
+        // tcgen05.commit (so all commits track that lane's MMAs).
         auto kv_slot = [](int n) { return n % kSlots; };
         auto kv_par = [](int n) { return (uint32_t)((n / kSlots) & 1); };
-        // descriptor bases; K-steps advance the start address field (bytes >> 4)
         const uint64_t dq0 = smem_desc_sw128(sbase + L::offQ, 16, 1024);
         const uint64_t dkv0 = smem_desc_sw128(sbase + L::offKV, 16, 1024);
         const uint64_t dv0 = smem_desc_sw128(sbase + L::offKV, kSlab, 1024);
-        auto issue_s = [&](int t, int j) {  // S_t = Q_t K_j^T
-            const uint64_t qd = dq0 + ((t * L::kTile) >> 4);
-            const uint64_t kd = dkv0 + ((kv_slot(2 * j) * L::kTile) >> 4);
+        int n = 0;                 // ring position of the current item's K_0
+        int use[2] = {0, 0};       // items so far in which query tile t took part
+        int sn[2] = {0, 0};        // S_t tiles computed so far (S_FULL / P_FULL phases)
+        bool ok = true;
+        for (int k = 0; ok; ++k) {
+            const int w = item_index(p, k);
+            if (w < 0) break;
+            const Item it = decode_item(p, w);
+            const int nt0 = it.n0, nt1 = it.n1;
+            const int n_max = nt0 > nt1 ? nt0 : nt1;
+            auto nt = [&](int t) { return t ? nt1 : nt0; };
+            auto issue_s = [&](int t, int j) {  // S_t = Q_t K_j^T
+                const uint64_t qd = dq0 + ((t * L::kTile) >> 4);
+                const uint64_t kd = dkv0 + ((kv_slot(n + 2 * j) * L::kTile) >> 4);
 #pragma unroll
-            for (int kk = 0; kk < KSTEPS_QK; ++kk) {
-                const uint32_t off = ((kk >> 2) * kSlab + (kk & 3) * 32) >> 4;
-                mma_bf16_ss_warp(tS[t], qd + off, kd + off, kIdescQK, kk > 0 ? 1u : 0u);
-            }
-        };
-        auto issue_pv = [&](int t, int j) {  // O_t += P_t V_j, P_t from tensor memory
-            // V is [keys][d], d contiguous: MN-major B; 64-column slabs kSlab apart (leading
-            // offset), 8-key groups 1024 bytes apart (stride offset)
-            const uint64_t vd = dv0 + ((kv_slot(2 * j + 1) * L::kTile) >> 4);
+                for (int kk = 0; kk < KSTEPS_QK; ++kk) {
+                    const uint32_t off = ((kk >> 2) * kSlab + (kk & 3) * 32) >> 4;
+                    mma_bf16_ss_warp(tmem + 128u * t, qd + off, kd + off, kIdescQK, kk > 0 ? 1u : 0u);
+                }
+            };
+            auto issue_pv = [&](int t, int j) {  // O_t += P_t V_j, P_t from tensor memory
+                // V is [keys][d], d contiguous: MN-major B; 64-column slabs kSlab apart (leading
+                // offset), 8-key groups 1024 bytes apart (stride offset)
+                const uint64_t vd = dv0 + ((kv_slot(n + 2 * j + 1) * L::kTile) >> 4);
 #pragma unroll
-            for (int kk = 0; kk < KSTEPS_PV; ++kk)
-                mma_bf16_ts_warp(tO[t], tS[t] + kk * 8, vd + ((kk * 16 * 128) >> 4), kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
-        };
-        bool ok = wait_phase_warp(&bars[B_Q_FULL], 0, sh);
-        if (ok && has_q1) ok = wait_phase_warp(&bars[B_Q_FULL + 1], 0, sh);
-        if (ok) ok = wait_phase_warp(&bars[B_KV_FULL + kv_slot(0)], kv_par(0), sh);
-        if (ok) {
+                for (int kk = 0; kk < KSTEPS_PV; ++kk)
+                    mma_bf16_ts_warp(tmem + 256u + 128u * t, tmem + 128u * t + kk * 8, vd + ((kk * 16 * 128) >> 4),
+                                     kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+            };
+            for (int t = 0; t < 2 && ok; ++t)
+                if (nt(t) > 0) ok = wait_phase_warp(&bars[B_Q_FULL + t], use[t] & 1, sh);
+            if (ok) ok = wait_phase_warp(&bars[B_KV_FULL + kv_slot(n)], kv_par(n), sh);
+            if (!ok) break;
             tc_fence_after();
             for (int t = 0; t < 2; ++t)
-                if (nt[t] > 0) {
+                if (nt(t) > 0) {
                     issue_s(t, 0);
                     mma_commit_warp(&bars[B_S_FULL + t]);
+                    if (nt(t) == 1) mma_commit_warp(&bars[B_Q_EMPTY + t]);
                 }
-            mma_commit_warp(&bars[B_KV_EMPTY + kv_slot(0)]);
-        }
-        __syncwarp();
-        for (int j = 0; j < n_max && ok; ++j) {
-            ok = wait_phase_warp(&bars[B_KV_FULL + kv_slot(2 * j + 1)], kv_par(2 * j + 1), sh);
-            const bool next = j + 1 < n_max;
-            bool k_next_ready = false;
-            for (int t = 0; t < 2 && ok; ++t) {
-                if (j >= nt[t]) continue;
-                ok = wait_phase_warp(&bars[B_P_FULL + t], j & 1, sh);
-                if (!ok) break;
-                tc_fence_after();
-                issue_pv(t, j);
-                if (j + 1 < nt[t]) {
-                    if (!k_next_ready) {  // K_{j+1} is only needed from here on
-                        ok = wait_phase_warp(&bars[B_KV_FULL + kv_slot(2 * j + 2)], kv_par(2 * j + 2), sh);
-                        if (!ok) break;
-                        k_next_ready = true;
-                    }
+            mma_commit_warp(&bars[B_KV_EMPTY + kv_slot(n)]);
+            for (int j = 0; j < n_max && ok; ++j) {
+                ok = wait_phase_warp(&bars[B_KV_FULL + kv_slot(n + 2 * j + 1)], kv_par(n + 2 * j + 1), sh);
+                const bool next = j + 1 < n_max;
+                bool k_next_ready = false;
+                for (int t = 0; t < 2 && ok; ++t) {
+                    if (j >= nt(t)) continue;
+                    // PV_t(0) overwrites O_t: the previous item's epilogue must have read it
+                    if (j == 0 && use[t] > 0) ok = wait_phase_warp(&bars[B_O_EMPTY + t], (use[t] - 1) & 1, sh);
+                    if (ok) ok = wait_phase_warp(&bars[B_P_FULL + t], (sn[t] + j) & 1, sh);
+                    if (!ok) break;
                     tc_fence_after();
-                    issue_s(t, j + 1);
-                    mma_commit_warp(&bars[B_S_FULL + t]);
-                } else {
-                    mma_commit_warp(&bars[B_O_FINAL + t]);
+                    issue_pv(t, j);
+                    if (j + 1 < nt(t)) {
+                        if (!k_next_ready) {  // K_{j+1} is only needed from here on
+                            ok = wait_phase_warp(&bars[B_KV_FULL + kv_slot(n + 2 * j + 2)], kv_par(n + 2 * j + 2), sh);
+                            if (!ok) break;
+                            k_next_ready = true;
+                        }
+                        tc_fence_after();
+                        issue_s(t, j + 1);
+                        mma_commit_warp(&bars[B_S_FULL + t]);
+                        if (j + 2 == nt(t)) mma_commit_warp(&bars[B_Q_EMPTY + t]);  // last read of Q_t
+                    } else {
+                        mma_commit_warp(&bars[B_O_FINAL + t]);
+                    }
                 }
-                __syncwarp();
+                if (!ok) break;
+                mma_commit_warp(&bars[B_KV_EMPTY + kv_slot(n + 2 * j + 1)]);
+                if (next) mma_commit_warp(&bars[B_KV_EMPTY + kv_slot(n + 2 * j + 2)]);
             }
-            if (!ok) break;
-            mma_commit_warp(&bars[B_KV_EMPTY + kv_slot(2 * j + 1)]);
-            if (next) mma_commit_warp(&bars[B_KV_EMPTY + kv_slot(2 * j + 2)]);
-            __syncwarp();
+            for (int t = 0; t < 2; ++t)
+                if (nt(t) > 0) {
+                    sn[t] += nt(t);
+                    ++use[t];
+                }
+            n += 2 * n_max;
         }
         // every MMA issued above completes before tensor memory is released
         mma_commit_warp(&bars[B_MMA_DONE]);
-        __syncwarp();
         drain_phase(&bars[B_MMA_DONE], 0);
     } else {
         // ------------------------------------------------------------ softmax warps
         const int t = warp >> 2;           // query tile of this group
         const int sub = warp & 3;          // tensor-memory lane quarter this warp may access
         const int row = sub * 32 + lane;   // query row within the tile
-        const int q0 = (qt0 + t) * BM;
-        const int qrow = q0 + row;         // global query position
-        const int nkv = t == 0 ? n0 : n1;
         const uint32_t lane_off = (uint32_t)(sub * 32) << 16;
         const uint32_t tS = tmem + 128u * t + lane_off;
         const uint32_t tO = tmem + 256u + 128u * t + lane_off;
         const float scale = p.scale_log2;
-        float m_ref = -INFINITY, l_sum = 0.f;
+        int use = 0, sn = 0;               // items and S tiles this group has processed
         bool ok = true;
-        for (int j = 0; j < nkv; ++j) {
-            ok = wait_phase_warp(&bars[B_S_FULL + t], j & 1, sh);
+        for (int k = 0; ok; ++k) {
+            const int w = item_index(p, k);
+            if (w < 0) break;
+            const Item it = decode_item(p, w);
+            const int nkv = t == 0 ? it.n0 : it.n1;
+            if (nkv == 0) continue;        // this item has no second query tile
+            const int q0 = (it.qt0 + t) * BM;
+            const int qrow = q0 + row;     // global query position
+            float m_ref = -INFINITY, l_sum = 0.f;
+            for (int j = 0; j < nkv; ++j) {
+                ok = wait_phase_warp(&bars[B_S_FULL + t], (sn + j) & 1, sh);
+                if (!ok) break;
+                tc_fence_after();
+                const int k0 = j * BN;
+                const bool need_mask = (p.causal && k0 + BN - 1 > q0) || k0 + BN > p.s;
+                const int lim = min(p.s - k0, p.causal ? qrow - k0 + 1 : BN);  // visible columns of this row
+                // the whole S row in one tensor-memory load, its maximum, then the exponentials
+                uint32_t sr[BN];
+                tmem_ld128(tS, sr);
+                tmem_wait_ld();
+                const float mx =
+                    need_mask ? row_max<true>(sr, lim, -INFINITY) : row_max<false>(sr, lim, -INFINITY);
+                const float mx2 = mx * scale;
+                float m_new = (j == 0 || mx2 > m_ref + 8.0f) ? mx2 : m_ref;
+                if (m_new == -INFINITY) m_new = 0.f;  // a row with nothing visible yet (padding rows only)
+                float rsum = 0.f;
+#pragma unroll
+                for (int c = 0; c < BN / 32; ++c) {
+                    uint32_t pk[16];
+                    rsum += need_mask ? chunk_exp<true>(sr, c, lim, scale, -m_new, pk)
+                                      : chunk_exp<false>(sr, c, lim, scale, -m_new, pk);
+                    tmem_st16(tS + c * 16, pk);
+                }
+                const float alpha = (j == 0) ? 0.f : ex2_approx(m_ref - m_new);
+                // O_t already holds P_t(j-1) V_{j-1} (S_t(j) was issued after it): rescale in place
+                if (j > 0 && __any_sync(0xffffffffu, m_new != m_ref)) {
+                    const float f = m_new != m_ref ? alpha : 1.0f;
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t r[32];
+                        tmem_ld32(tO + c * 32, r);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * f);
+                        tmem_st32(tO + c * 32, r);
+                    }
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars[B_P_FULL + t]);
+                l_sum = (j == 0) ? rsum : l_sum * alpha + rsum;
+                m_ref = m_new;
+            }
+            if (ok) ok = wait_phase_warp(&bars[B_O_FINAL + t], use & 1, sh);
             if (!ok) break;
             tc_fence_after();
-            const int k0 = j * BN;
-            const bool need_mask = (p.causal && k0 + BN - 1 > q0) || k0 + BN > p.s;
-            const int lim = min(p.s - k0, p.causal ? qrow - k0 + 1 : BN);  // visible columns of this row
-            // the whole S row in one tensor-memory load, its maximum, then the exponentials
-            uint32_t sr[BN];
-            tmem_ld128(tS, sr);
-            tmem_wait_ld();
-            const float mx = need_mask ? row_max<true>(sr, lim, -INFINITY) : row_max<false>(sr, lim, -INFINITY);
-            const float mx2 = mx * scale;
-            float m_new = (j == 0 || mx2 > m_ref + 8.0f) ? mx2 : m_ref;
-            if (m_new == -INFINITY) m_new = 0.f;  // a row with nothing visible yet (padding rows only)
-            float rsum = 0.f;
-#pragma unroll
-            for (int c = 0; c < BN / 32; ++c) {
-                uint32_t pk[16];
-                rsum += need_mask ? chunk_exp<true>(sr, c, lim, scale, -m_new, pk)
-                                  : chunk_exp<false>(sr, c, lim, scale, -m_new, pk);
-                tmem_st16(tS + c * 16, pk);
-            }
-            const float alpha = (j == 0) ? 0.f : ex2_approx(m_ref - m_new);
-            // O_t already holds P_t(j-1) V_{j-1} (S_t(j) was issued after it): rescale in place
-            if (j > 0 && __any_sync(0xffffffffu, m_new != m_ref)) {
-                const float f = m_new != m_ref ? alpha : 1.0f;
-#pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t r[32];
-                    tmem_ld32(tO + c * 32, r);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * f);
-                    tmem_st32(tO + c * 32, r);
-                }
-            }
-            tmem_wait_st();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars[B_P_FULL + t]);
-            l_sum = (j == 0) ? rsum : l_sum * alpha + rsum;
-            m_ref = m_new;
-        }
-        if (ok && nkv > 0) ok = wait_phase_warp(&bars[B_O_FINAL + t], 0, sh);
-        if (ok && nkv > 0) {
-            tc_fence_after();
-            // epilogue: O / l -> bf16 -> this warp's 32 rows of the staging tile (Q_t's slot,
-            // free since S_t's last MMA completed) -> TMA store of a 32-row box per slab
+            // epilogue: O / l -> bf16, each thread stores its own row (16-byte stores), then
+            // O_t is handed back to the MMA warp for the next item
             const float inv = l_sum > 0.f ? 1.0f / l_sum : 0.f;
-            uint8_t* stage = smem + L::offQ + t * L::kTile;
+            const TileCoord oc = tile_coord(p, it.rank, q0);
+            const bool row_ok = qrow < p.s;
+            uint8_t* orow = p.optr[oc.map] +
+                            ((((size_t)it.bb * p.rows_per_map + oc.row + row) * p.heads + it.head) * D) * 2;
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t r[32];
@@ -436,26 +506,19 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
                 tmem_wait_ld();
 #pragma unroll
                 for (int q4 = 0; q4 < 4; ++q4) {
-                    uint4 w;
-                    w.x = pack_bf16x2(__uint_as_float(r[q4 * 8 + 0]) * inv, __uint_as_float(r[q4 * 8 + 1]) * inv);
-                    w.y = pack_bf16x2(__uint_as_float(r[q4 * 8 + 2]) * inv, __uint_as_float(r[q4 * 8 + 3]) * inv);
-                    w.z = pack_bf16x2(__uint_as_float(r[q4 * 8 + 4]) * inv, __uint_as_float(r[q4 * 8 + 5]) * inv);
-                    w.w = pack_bf16x2(__uint_as_float(r[q4 * 8 + 6]) * inv, __uint_as_float(r[q4 * 8 + 7]) * inv);
-                    const int col = c * 32 + q4 * 8;  // first of 8 output columns
-                    const uint32_t off = (col >> 6) * kSlab + row * 128 + ((((col & 63) >> 3) ^ (row & 7)) << 4);
-                    *reinterpret_cast<uint4*>(stage + off) = w;
+                    uint4 v;
+                    v.x = pack_bf16x2(__uint_as_float(r[q4 * 8 + 0]) * inv, __uint_as_float(r[q4 * 8 + 1]) * inv);
+                    v.y = pack_bf16x2(__uint_as_float(r[q4 * 8 + 2]) * inv, __uint_as_float(r[q4 * 8 + 3]) * inv);
+                    v.z = pack_bf16x2(__uint_as_float(r[q4 * 8 + 4]) * inv, __uint_as_float(r[q4 * 8 + 5]) * inv);
+                    v.w = pack_bf16x2(__uint_as_float(r[q4 * 8 + 6]) * inv, __uint_as_float(r[q4 * 8 + 7]) * inv);
+                    if (row_ok) *reinterpret_cast<uint4*>(orow + (c * 32 + q4 * 8) * 2) = v;
                 }
             }
-            fence_proxy_async_smem();
+            tc_fence_before();
             __syncwarp();
-            if (lane == 0 && q0 + sub * 32 < p.s) {  // boxes wholly past the end are skipped
-                const TileCoord oc = tile_coord(p, rank, q0);
-#pragma unroll
-                for (int c = 0; c < D / 64; ++c)
-                    tma_store_4d(&p.mo[oc.map], sbase + L::offQ + t * L::kTile + c * kSlab + sub * 32 * 128, c * 64,
-                                 head, oc.row + sub * 32, bb);
-                tma_store_commit_and_drain();
-            }
+            if (lane == 0) mbar_arrive(&bars[B_O_EMPTY + t]);
+            sn += nkv;
+            ++use;
         }
     }
 
@@ -500,11 +563,18 @@ bool make_map(CUtensorMap* m, const void* base, int b, int rows, int heads, int 
 }
 
 template <int D>
-cudaError_t launch_d(const TcParams& prm, long long nblocks, cudaStream_t stream) {
+cudaError_t launch_d(TcParams& prm, long long n_items, cudaStream_t stream) {
     const uint32_t smem = Smem<D>::kAlloc;
     cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    attn_tc_kernel<D><<<(unsigned)nblocks, kThreads, smem, stream>>>(prm);
+    int dev = 0, sms = 0;
+    e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    // persistent: one CTA per SM walks the items (each CTA fills an SM: smem and all TMEM)
+    prm.n_items = (int)n_items;
+    const long long grid = n_items < sms ? n_items : sms;
+    attn_tc_kernel<D><<<(unsigned)grid, kThreads, smem, stream>>>(prm);
     return cudaGetLastError();
 }
 
@@ -537,13 +607,13 @@ cudaError_t launch_attention_tc(int P, int b, int s, int h_q, int h_kv, int d, i
         for (int j = 0; j < P && err == cudaSuccess; ++j) {
             if (!make_map(&prm->mq[j], ptrs.q[j], b, S, h_q, d, BM) ||
                 !make_map(&prm->mk[j], ptrs.k[j], b, S, h_kv, d, BN) ||
-                !make_map(&prm->mv[j], ptrs.v[j], b, S, h_kv, d, BN) ||
-                !make_map(&prm->mo[j], ptrs.o[j], b, S, h_q, d, 32))
+                !make_map(&prm->mv[j], ptrs.v[j], b, S, h_kv, d, BN))
                 err = cudaErrorInvalidValue;
+            prm->optr[j] = static_cast<uint8_t*>(ptrs.o[j]);
         }
         if (err == cudaSuccess) {
-            const long long nblocks = (long long)b * h_q * prm->n_pairs;
-            err = d == 64 ? launch_d<64>(*prm, nblocks, stream) : launch_d<128>(*prm, nblocks, stream);
+            const long long n_items = (long long)b * h_q * prm->n_pairs;
+            err = d == 64 ? launch_d<64>(*prm, n_items, stream) : launch_d<128>(*prm, n_items, stream);
         }
     } else {
         const int Hq = h_q / P, Hk = h_kv / P;
@@ -556,13 +626,13 @@ cudaError_t launch_attention_tc(int P, int b, int s, int h_q, int h_kv, int d, i
                 const int r = r0 + i;
                 if (!make_map(&prm->mq[i], ptrs.q[r], b, s, Hq, d, BM) ||
                     !make_map(&prm->mk[i], ptrs.k[r], b, s, Hk, d, BN) ||
-                    !make_map(&prm->mv[i], ptrs.v[r], b, s, Hk, d, BN) ||
-                    !make_map(&prm->mo[i], ptrs.o[r], b, s, Hq, d, 32))
+                    !make_map(&prm->mv[i], ptrs.v[r], b, s, Hk, d, BN))
                     err = cudaErrorInvalidValue;
+                prm->optr[i] = static_cast<uint8_t*>(ptrs.o[r]);
             }
             if (err != cudaSuccess) break;
-            const long long nblocks = (long long)nr * b * Hq * prm->n_pairs;
-            err = d == 64 ? launch_d<64>(*prm, nblocks, stream) : launch_d<128>(*prm, nblocks, stream);
+            const long long n_items = (long long)nr * b * Hq * prm->n_pairs;
+            err = d == 64 ? launch_d<64>(*prm, n_items, stream) : launch_d<128>(*prm, n_items, stream);
         }
     }
     delete prm;
