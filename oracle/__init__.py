@@ -1,4 +1,4 @@
-"""CPU oracle for the Ulysses DistributedAttention forward -- TEST INFRASTRUCTURE ONLY.
+"""CPU oracle for the Ulysses DistributedAttention forward and backward -- TEST INFRASTRUCTURE ONLY.
 
 Only ``tests/``, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline leg import
 this package.  The product path (``sequence_attention_seq_gb300``) never does, and this
@@ -56,6 +56,10 @@ def _load():
             lib.orc_dist_attn_rows.argtypes = [i, i, i, i, i, i, i, i, ctypes.POINTER(vp),
                                                ctypes.POINTER(vp), ctypes.POINTER(vp), i, vp, vp]
             lib.orc_dist_attn_rows.restype = i
+            lib.orc_attention_lse.argtypes = [i, i, i, i, i, i, i, vp, vp, vp]
+            lib.orc_attention_lse.restype = i
+            lib.orc_attention_bwd.argtypes = [i, i, i, i, i, i, i, vp, vp, vp, vp, vp, vp, vp]
+            lib.orc_attention_bwd.restype = i
             _lib = lib
     return _lib
 
@@ -145,3 +149,39 @@ def dist_attn_rows(q_seq, k_seq, v_seq, causal, samples):
                                       _ptrs(qs), _ptrs(ks), _ptrs(vs), smp.shape[0],
                                       smp.ctypes.data, out.ctypes.data), "dist_attn_rows")
     return torch.from_numpy(out)
+
+
+def attention_lse(q, k, causal):
+    """Per-row log-sum-exp (natural log) of one rank's scaled scores: float64 [b, h_q, s]."""
+    q, k = _cpu(q), _cpu(k)
+    b, s, hq, d = q.shape
+    out = torch.empty((b, hq, s), dtype=torch.float64)
+    _check(_load().orc_attention_lse(b, s, hq, k.shape[2], d, int(bool(causal)), DTYPE_CODE[q.dtype],
+                                     q.data_ptr(), k.data_ptr(), out.data_ptr()), "attention_lse")
+    return out
+
+
+def attention_bwd(q, k, v, dout, causal):
+    """Gradients (dq, dk, dv) of one rank's local attention in head layout, float64."""
+    q, k, v, dout = _cpu(q), _cpu(k), _cpu(v), _cpu(dout)
+    if not (q.dtype == k.dtype == v.dtype == dout.dtype):
+        raise ValueError("q, k, v, dout must share a dtype")
+    b, s, hq, d = q.shape
+    hkv = k.shape[2]
+    dq = torch.empty((b, s, hq, d), dtype=torch.float64)
+    dk = torch.empty((b, s, hkv, d), dtype=torch.float64)
+    dv = torch.empty((b, s, hkv, d), dtype=torch.float64)
+    _check(_load().orc_attention_bwd(b, s, hq, hkv, d, int(bool(causal)), DTYPE_CODE[q.dtype], q.data_ptr(),
+                                     k.data_ptr(), v.data_ptr(), dout.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                                     dv.data_ptr()), "attention_bwd")
+    return dq, dk, dv
+
+
+def dist_attn_bwd(q_seq, k_seq, v_seq, do_seq, causal):
+    """The Ulysses backward: all-to-all #1 on dO (the backward of all-to-all #2), per-rank
+    attention backward, all-to-all #2 on dQ, dK, dV (the backward of all-to-all #1)
+    ("02 · DeepSpeed-Ulysses", section 5).  Returns per-rank float64 seq-layout gradients."""
+    q_head, k_head, v_head = seq2head(q_seq), seq2head(k_seq), seq2head(v_seq)
+    do_head = seq2head(do_seq)
+    grads = [attention_bwd(q, k, v, g, causal) for q, k, v, g in zip(q_head, k_head, v_head, do_head)]
+    return (head2seq([x[0] for x in grads]), head2seq([x[1] for x in grads]), head2seq([x[2] for x in grads]))

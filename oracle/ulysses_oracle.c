@@ -276,3 +276,105 @@ int orc_dist_attn_rows(int P, int b, int s, int hq, int hkv, int d, int causal, 
     free(scores);
     return ORC_OK;
 }
+
+/* ----------------------------------------------------------------- backward */
+
+/*
+ * Per-row log-sum-exp of the scaled, masked scores of one rank's local attention, in
+ * natural-log units: lse[bb][hh][i] = log sum_j exp(q_i . k_j / sqrt(d)).  The training
+ * forward saves it so the backward can rebuild the softmax weights.
+ */
+int orc_attention_lse(int b, int s, int hq, int hkv, int d, int causal, int dtype,
+                      const void* q, const void* k, double* lse) {
+    if (b < 0 || s < 0 || hq < 1 || hkv < 1 || d < 1 || hq % hkv) return ORC_BAD_ARG;
+    int g = hq / hkv;
+    double scale = 1.0 / sqrt((double)d);
+    double* sc = (double*)malloc(sizeof(double) * (s ? s : 1));
+    if (!sc) return ORC_NO_MEMORY;
+    for (int bb = 0; bb < b; ++bb)
+        for (int hh = 0; hh < hq; ++hh) {
+            int kh = hh / g;
+            for (int i = 0; i < s; ++i) {
+                int n = causal ? i + 1 : s;
+                double m = -INFINITY;
+                for (int j = 0; j < n; ++j) {
+                    double acc = 0.0;
+                    for (int c = 0; c < d; ++c)
+                        acc += load_elem(q, (((size_t)bb * s + i) * hq + hh) * d + c, dtype) *
+                               load_elem(k, (((size_t)bb * s + j) * hkv + kh) * d + c, dtype);
+                    sc[j] = acc * scale;
+                    if (sc[j] > m) m = sc[j];
+                }
+                double l = 0.0;
+                for (int j = 0; j < n; ++j) l += exp(sc[j] - m);
+                lse[((size_t)bb * hq + hh) * s + i] = m + log(l);
+            }
+        }
+    free(sc);
+    return ORC_OK;
+}
+
+/*
+ * Gradient of one rank's local attention O = softmax(Q K^T / sqrt(d)) V (head layout),
+ * given dO: with P the softmax weights of a row, D_i = sum_c dO_ic O_ic,
+ *   dV_j += sum_i P_ij dO_i,   dP_ij = dO_i . v_j,   dS_ij = P_ij (dP_ij - D_i),
+ *   dQ_i = sum_j dS_ij k_j / sqrt(d),   dK_j += sum_i dS_ij q_i / sqrt(d).
+ * This is the derivative of the plain definition (the "ordinary attention backward" of
+ * "02 · DeepSpeed-Ulysses", section 5).  Grouped K/V heads sum the contributions of their
+ * g query heads.  dq [b][s][hq][d], dk/dv [b][s][hkv][d], all double, overwritten.
+ */
+int orc_attention_bwd(int b, int s, int hq, int hkv, int d, int causal, int dtype,
+                      const void* q, const void* k, const void* v, const void* dout,
+                      double* dq, double* dk, double* dv) {
+    if (b < 0 || s < 0 || hq < 1 || hkv < 1 || d < 1 || hq % hkv) return ORC_BAD_ARG;
+    int g = hq / hkv;
+    double scale = 1.0 / sqrt((double)d);
+    size_t nq = (size_t)b * s * hq * d, nk = (size_t)b * s * hkv * d;
+    for (size_t x = 0; x < nq; ++x) dq[x] = 0.0;
+    for (size_t x = 0; x < nk; ++x) { dk[x] = 0.0; dv[x] = 0.0; }
+    double* p = (double*)malloc(sizeof(double) * (s ? s : 1));
+    double* o = (double*)malloc(sizeof(double) * (d ? d : 1));
+    if (!p || !o) { free(p); free(o); return ORC_NO_MEMORY; }
+    for (int bb = 0; bb < b; ++bb)
+        for (int hh = 0; hh < hq; ++hh) {
+            int kh = hh / g;
+            for (int i = 0; i < s; ++i) {
+                int n = causal ? i + 1 : s;
+                size_t qo = (((size_t)bb * s + i) * hq + hh) * d;
+                /* softmax weights of row i */
+                double m = -INFINITY;
+                for (int j = 0; j < n; ++j) {
+                    size_t ko = (((size_t)bb * s + j) * hkv + kh) * d;
+                    double acc = 0.0;
+                    for (int c = 0; c < d; ++c) acc += load_elem(q, qo + c, dtype) * load_elem(k, ko + c, dtype);
+                    p[j] = acc * scale;
+                    if (p[j] > m) m = p[j];
+                }
+                double l = 0.0;
+                for (int j = 0; j < n; ++j) { p[j] = exp(p[j] - m); l += p[j]; }
+                for (int j = 0; j < n; ++j) p[j] /= l;
+                /* output row and D_i */
+                for (int c = 0; c < d; ++c) o[c] = 0.0;
+                for (int j = 0; j < n; ++j) {
+                    size_t vo = (((size_t)bb * s + j) * hkv + kh) * d;
+                    for (int c = 0; c < d; ++c) o[c] += p[j] * load_elem(v, vo + c, dtype);
+                }
+                double Di = 0.0;
+                for (int c = 0; c < d; ++c) Di += load_elem(dout, qo + c, dtype) * o[c];
+                for (int j = 0; j < n; ++j) {
+                    size_t ko = (((size_t)bb * s + j) * hkv + kh) * d;
+                    double dp = 0.0;
+                    for (int c = 0; c < d; ++c) dp += load_elem(dout, qo + c, dtype) * load_elem(v, ko + c, dtype);
+                    double ds = p[j] * (dp - Di);
+                    for (int c = 0; c < d; ++c) {
+                        dv[ko + c] += p[j] * load_elem(dout, qo + c, dtype);
+                        dq[qo + c] += ds * load_elem(k, ko + c, dtype) * scale;
+                        dk[ko + c] += ds * load_elem(q, qo + c, dtype) * scale;
+                    }
+                }
+            }
+        }
+    free(p);
+    free(o);
+    return ORC_OK;
+}
