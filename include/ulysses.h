@@ -1,5 +1,5 @@
 /*
- * ulysses.h -- C ABI of the GB300 (sm_103a) Ulysses DistributedAttention forward.
+ * ulysses.h -- C ABI of the GB300 (sm_103a) Ulysses DistributedAttention forward and backward.
  *
  * The method ("DeepSpeed-Ulysses 深度解析：用 All-to-All 序列并行撑起百万 Token 超长序列训练",
  * section "核心设计：沿序列切分 + 两次 All-to-All", steps 1-5): each of P sequence-parallel
@@ -146,6 +146,94 @@ uly_status ulysses_dist_attn_fwd_noalloc(int P, int b, int s, int h_q, int h_kv,
                                          const void* const* q_seq, const void* const* k_seq,
                                          const void* const* v_seq, void* const* o_seq,
                                          cudaStream_t stream);
+
+/*
+ * ------------------------------------------------------------------------------------
+ * Training: forward with the saved softmax statistics, and the backward.
+ *
+ * "02 · DeepSpeed-Ulysses", section 5 (backward): the gradient of all-to-all #2 is
+ * all-to-all #1 applied to dO, the local attention's gradient is the ordinary attention
+ * backward, and the gradient of all-to-all #1 is all-to-all #2 applied to dQ, dK and dV.
+ * The attention backward uses, for every query row i of every local head,
+ *   L_i = log sum_{visible j} exp(q_i.k_j / sqrt(d))        (natural log, fp32)
+ *   P_ij = exp(q_i.k_j / sqrt(d) - L_i),  D_i = sum_c dO_ic O_ic,
+ *   dV_j = sum_i P_ij dO_i,  dS_ij = P_ij (dO_i.v_j - D_i),
+ *   dQ_i = sum_j dS_ij k_j / sqrt(d),  dK_j = sum_i dS_ij q_i / sqrt(d)
+ * (grouped heads: dK/dV of a K/V head sum over all query heads that read it).
+ * lse arrays: P pointers, rank r's is [b][h_q/P][s] fp32 (row (bb, hh, i) = L_i of local
+ * head hh, i.e. global head r*h_q/P + hh), 16-byte aligned like every device pointer.
+ * Only ULY_BF16 with d in {64, 128} has these kernels (else ULY_ERR_UNSUPPORTED).
+ * dP, P and dS are formed in fp32; P and dS are rounded to bf16 before their tile
+ * products (as P is in the forward); gradients are accumulated in fp32 and rounded to
+ * nearest even at the end.  Each gradient element is written exactly once (no atomics),
+ * so repeated calls give the same bits.
+ * ------------------------------------------------------------------------------------
+ */
+
+/*
+ * ulysses_local_attention plus the per-row log-sum-exp: same arguments, layouts and
+ * output, and lse[r][bb][hh][i] = L_i as defined above.  lse must not overlap any other
+ * argument.
+ */
+uly_status ulysses_local_attention_fwd_lse(int P, int b, int s, int h_q, int h_kv, int d, uly_dtype dtype,
+                                           int causal,
+                                           const void* const* q_head, const void* const* k_head,
+                                           const void* const* v_head, void* const* o_head,
+                                           float* const* lse, cudaStream_t stream);
+
+/*
+ * ulysses_dist_attn_fwd (fused == 0, same workspace) plus the log-sum-exp of every head
+ * rank's rows: lse[r] is indexed in head layout ([b][h_q/P][s], all s tokens of rank r's
+ * heads), which is what ulysses_dist_attn_bwd takes back.
+ */
+uly_status ulysses_dist_attn_fwd_lse(int P, int b, int s, int h_q, int h_kv, int d, uly_dtype dtype,
+                                     int causal,
+                                     const void* const* q_seq, const void* const* k_seq,
+                                     const void* const* v_seq, void* const* o_seq, float* const* lse,
+                                     void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * Bytes of workspace the backward needs: for every rank two fp32 row arrays
+ * [b][h_q/P][ceil(s/128)*128] (L in base 2 and D), and, when dist != 0, the head-layout
+ * copies of Q, K, V, dO, dQ, dK and dV; each array 256-byte aligned.  0 for arguments
+ * that are invalid or unsupported.
+ */
+size_t ulysses_attn_bwd_workspace_bytes(int P, int b, int s, int h_q, int h_kv, int d, uly_dtype dtype,
+                                        int dist);
+
+/*
+ * Backward of ulysses_local_attention, head layout in and out.
+ *   q_head, o_head, do_head, dq_head: P pointers to [b][s][h_q/P][d];
+ *   k_head, v_head, dk_head, dv_head: P pointers to [b][s][h_kv/P][d];
+ *   lse: from ulysses_local_attention_fwd_lse on the same q, k (and causal flag).
+ * Four launches: row statistics, dK/dV, dQ (one pair per 16 ranks).  Outputs must not
+ * overlap each other, any input or the workspace (256-byte aligned, at least
+ * ulysses_attn_bwd_workspace_bytes(..., dist = 0) bytes, owned by the caller).
+ */
+uly_status ulysses_local_attention_bwd(int P, int b, int s, int h_q, int h_kv, int d, uly_dtype dtype,
+                                       int causal,
+                                       const void* const* q_head, const void* const* k_head,
+                                       const void* const* v_head, const void* const* o_head,
+                                       const void* const* do_head, const float* const* lse,
+                                       void* const* dq_head, void* const* dk_head, void* const* dv_head,
+                                       void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * The whole DistributedAttention backward, seq layout in and out:
+ *   all-to-all #1 on Q, K, V and dO (one launch), D from the seq-layout O and dO, the
+ *   local backward of every rank, all-to-all #2 on dQ, dK and dV (one launch).
+ *   q_seq, o_seq, do_seq, dq_seq: P pointers to [b][s/P][h_q][d];
+ *   k_seq, v_seq, dk_seq, dv_seq: P pointers to [b][s/P][h_kv][d];
+ *   lse: from ulysses_dist_attn_fwd_lse (head-layout indexed).
+ * workspace: 256-byte aligned, at least ulysses_attn_bwd_workspace_bytes(..., dist = 1)
+ * bytes.  Size and overlap rules as ulysses_local_attention_bwd plus the exchange rules.
+ */
+uly_status ulysses_dist_attn_bwd(int P, int b, int s, int h_q, int h_kv, int d, uly_dtype dtype, int causal,
+                                 const void* const* q_seq, const void* const* k_seq,
+                                 const void* const* v_seq, const void* const* o_seq,
+                                 const void* const* do_seq, const float* const* lse,
+                                 void* const* dq_seq, void* const* dk_seq, void* const* dv_seq,
+                                 void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
  * Reads (and, if clear != 0, resets) the library's device-side error word after

@@ -22,6 +22,8 @@ __all__ = [
     "ulysses_a2a_seq2head", "ulysses_a2a_head2seq", "ulysses_local_attention",
     "ulysses_dist_attn_workspace_bytes", "ulysses_dist_attn_fwd", "ulysses_device_status",
     "ulysses_status_string", "EXPORTED_SYMBOLS", "ulysses_dist_attn_fwd_noalloc", "NOALLOC_SCRATCH_BYTES",
+    "ulysses_local_attention_fwd_lse", "ulysses_dist_attn_fwd_lse", "ulysses_attn_bwd_workspace_bytes",
+    "ulysses_local_attention_bwd", "ulysses_dist_attn_bwd",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -34,7 +36,9 @@ _DTYPES = {torch.float32: 0, torch.bfloat16: 1}
 EXPORTED_SYMBOLS = (
     "ulysses_a2a_seq2head", "ulysses_a2a_head2seq", "ulysses_local_attention",
     "ulysses_dist_attn_workspace_bytes", "ulysses_dist_attn_fwd", "ulysses_device_status",
-    "ulysses_status_string", "ulysses_dist_attn_fwd_noalloc",
+    "ulysses_status_string", "ulysses_dist_attn_fwd_noalloc", "ulysses_local_attention_fwd_lse",
+    "ulysses_dist_attn_fwd_lse", "ulysses_attn_bwd_workspace_bytes", "ulysses_local_attention_bwd",
+    "ulysses_dist_attn_bwd",
 )
 
 _lock = threading.Lock()
@@ -76,6 +80,16 @@ def load_library():
         lib.ulysses_dist_attn_fwd.restype = i
         lib.ulysses_dist_attn_fwd_noalloc.argtypes = [i, i, i, i, i, i, i, i, pp, pp, pp, pp, vp]
         lib.ulysses_dist_attn_fwd_noalloc.restype = i
+        lib.ulysses_local_attention_fwd_lse.argtypes = [i, i, i, i, i, i, i, i, pp, pp, pp, pp, pp, vp]
+        lib.ulysses_local_attention_fwd_lse.restype = i
+        lib.ulysses_dist_attn_fwd_lse.argtypes = [i, i, i, i, i, i, i, i, pp, pp, pp, pp, pp, vp, sz, vp]
+        lib.ulysses_dist_attn_fwd_lse.restype = i
+        lib.ulysses_attn_bwd_workspace_bytes.argtypes = [i, i, i, i, i, i, i, i]
+        lib.ulysses_attn_bwd_workspace_bytes.restype = sz
+        for name in ("ulysses_local_attention_bwd", "ulysses_dist_attn_bwd"):
+            f = getattr(lib, name)
+            f.argtypes = [i, i, i, i, i, i, i, i, pp, pp, pp, pp, pp, pp, pp, pp, pp, vp, sz, vp]
+            f.restype = i
         lib.ulysses_device_status.argtypes = [i]
         lib.ulysses_device_status.restype = i
         lib.ulysses_status_string.argtypes = [i]
@@ -228,3 +242,97 @@ def ulysses_dist_attn_fwd_noalloc(q_seq, k_seq, v_seq, causal, out_seq, stream=N
         P, b, S * P, hq, k0.shape[2], d, _dtype_code(q0), int(bool(causal)), _ptr_array(q_seq), _ptr_array(k_seq),
         _ptr_array(v_seq), _ptr_array(out_seq), _stream(stream)), "ulysses_dist_attn_fwd_noalloc")
     return out_seq
+
+
+# ------------------------------------------------------------------------------ training
+def _rows_like(q_head_shape, device):
+    b, s, Hq, _ = q_head_shape
+    return torch.empty((b, Hq, s), dtype=torch.float32, device=device)
+
+
+def ulysses_local_attention_fwd_lse(q_head, k_head, v_head, causal, out_head=None, lse=None, stream=None):
+    """ulysses_local_attention plus the per-row log-sum-exp: returns (o_head, lse), lse being
+    P fp32 tensors [b, h_q/P, s] (natural log of the sum of exp of the scaled scores)."""
+    q0 = _same(q_head, "q_head")
+    k0 = _same(k_head, "k_head")
+    _same(v_head, "v_head")
+    P = len(q_head)
+    b, s, Hq, d = q0.shape
+    if out_head is None:
+        out_head = [torch.empty_like(q) for q in q_head]
+    if lse is None:
+        lse = [_rows_like(q0.shape, q0.device) for _ in range(P)]
+    _check(load_library().ulysses_local_attention_fwd_lse(
+        P, b, s, Hq * P, k0.shape[2] * P, d, _dtype_code(q0), int(bool(causal)), _ptr_array(q_head),
+        _ptr_array(k_head), _ptr_array(v_head), _ptr_array(out_head), _ptr_array(lse), _stream(stream)),
+        "ulysses_local_attention_fwd_lse")
+    return out_head, lse
+
+
+def ulysses_dist_attn_fwd_lse(q_seq, k_seq, v_seq, causal, out_seq=None, lse=None, workspace=None, stream=None):
+    """The unfused forward plus the log-sum-exp of every head rank's rows: returns (o_seq, lse)
+    with lse P fp32 tensors [b, h_q/P, s] indexed like the head layout."""
+    q0 = _same(q_seq, "q_seq")
+    k0 = _same(k_seq, "k_seq")
+    _same(v_seq, "v_seq")
+    P = len(q_seq)
+    b, S, hq, d = q0.shape
+    hkv = k0.shape[2]
+    s = S * P
+    if out_seq is None:
+        out_seq = [torch.empty_like(q) for q in q_seq]
+    if lse is None:
+        lse = [torch.empty((b, hq // P, s), dtype=torch.float32, device=q0.device) for _ in range(P)]
+    need = ulysses_dist_attn_workspace_bytes(P, b, s, hq, hkv, d, q0.dtype, False)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q0.device)
+    _check(load_library().ulysses_dist_attn_fwd_lse(
+        P, b, s, hq, hkv, d, _dtype_code(q0), int(bool(causal)), _ptr_array(q_seq), _ptr_array(k_seq),
+        _ptr_array(v_seq), _ptr_array(out_seq), _ptr_array(lse), workspace.data_ptr(),
+        workspace.numel() * workspace.element_size(), _stream(stream)), "ulysses_dist_attn_fwd_lse")
+    return out_seq, lse
+
+
+def ulysses_attn_bwd_workspace_bytes(P, b, s, h_q, h_kv, d, dtype, dist):
+    return int(load_library().ulysses_attn_bwd_workspace_bytes(P, b, s, h_q, h_kv, d, _DTYPES[dtype],
+                                                               int(bool(dist))))
+
+
+def _bwd_call(name, dist, q, k, v, o, do, lse, causal, grads, workspace, stream):
+    q0 = _same(q, "q")
+    k0 = _same(k, "k")
+    _same(v, "v")
+    _same(o, "o")
+    _same(do, "do")
+    _same(lse, "lse")
+    P = len(q)
+    if dist:
+        b, S, hq, d = q0.shape
+        s, hkv = S * P, k0.shape[2]
+    else:
+        b, s, Hq, d = q0.shape
+        hq, hkv = Hq * P, k0.shape[2] * P
+    if grads is None:
+        grads = ([torch.empty_like(x) for x in q], [torch.empty_like(x) for x in k], [torch.empty_like(x) for x in v])
+    need = ulysses_attn_bwd_workspace_bytes(P, b, s, hq, hkv, d, q0.dtype, dist)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q0.device)
+    dq, dk, dv = grads
+    _check(getattr(load_library(), name)(
+        P, b, s, hq, hkv, d, _dtype_code(q0), int(bool(causal)), _ptr_array(q), _ptr_array(k), _ptr_array(v),
+        _ptr_array(o), _ptr_array(do), _ptr_array(lse), _ptr_array(dq), _ptr_array(dk), _ptr_array(dv),
+        workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream(stream)), name)
+    return dq, dk, dv
+
+
+def ulysses_local_attention_bwd(q_head, k_head, v_head, o_head, do_head, lse, causal, grads=None, workspace=None,
+                                stream=None):
+    """Backward of the head-layout attention of every rank: returns (dq, dk, dv) head layout."""
+    return _bwd_call("ulysses_local_attention_bwd", False, q_head, k_head, v_head, o_head, do_head, lse, causal,
+                     grads, workspace, stream)
+
+
+def ulysses_dist_attn_bwd(q_seq, k_seq, v_seq, o_seq, do_seq, lse, causal, grads=None, workspace=None, stream=None):
+    """The DistributedAttention backward, seq layout in and out: returns (dq, dk, dv) seq layout."""
+    return _bwd_call("ulysses_dist_attn_bwd", True, q_seq, k_seq, v_seq, o_seq, do_seq, lse, causal, grads,
+                     workspace, stream)

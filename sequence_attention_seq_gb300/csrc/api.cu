@@ -75,6 +75,27 @@ uly_status check_attention_shape(int P, int b, int s, int hq, int hkv, int d, ul
 
 uint64_t round256(uint64_t x) { return (x + 255) & ~uint64_t(255); }
 
+// The backward and the log-sum-exp forward exist for the bf16 tensor-core path only.
+uly_status check_train_shape(int P, int b, int s, int hq, int hkv, int d, uly_dtype dt) {
+    uly_status st = check_attention_shape(P, b, s, hq, hkv, d, dt);
+    if (st != ULY_OK) return st;
+    if (dt != ULY_BF16) return ULY_ERR_UNSUPPORTED;
+    return ULY_OK;
+}
+
+// Per-rank bytes of one [b][h_q/P][s_pad] fp32 row array (s_pad = s rounded up to 128).
+uint64_t row_array_bytes(int P, int b, int s, int hq) {
+    return round256((uint64_t)b * (hq / P) * (((uint64_t)s + 127) / 128 * 128) * 4);
+}
+
+bool collect_f(const float* const* ptrs, int P, uint64_t bytes, std::vector<Range>& out) {
+    return collect(reinterpret_cast<const void* const*>(ptrs), P, bytes, out);
+}
+
+bool workspace_ok(const void* ws, size_t have, size_t need) {
+    return ws && !(reinterpret_cast<uintptr_t>(ws) & 255u) && have >= need;
+}
+
 uly_status exchange(int direction, int P, int b, int s, int h, int d, uly_dtype dt, const void* const* in,
                     void* const* out, cudaStream_t stream) {
     uly_status st = check_exchange_shape(P, b, s, h, d, dt);
@@ -98,7 +119,7 @@ uly_status exchange(int direction, int P, int b, int s, int h, int d, uly_dtype 
 uly_status run_attention(int P, int b, int s, int hq, int hkv, int d, uly_dtype dt, int causal, int fused,
                          const uly::AttnPtrs& ptrs, cudaStream_t stream) {
     if (dt == ULY_FP32) {
-        if (fused) return ULY_ERR_UNSUPPORTED;
+        if (fused || ptrs.lse[0]) return ULY_ERR_UNSUPPORTED;
         return uly::launch_attention_fp32(P, b, s, hq, hkv, d, causal, ptrs, stream) == cudaSuccess ? ULY_OK
                                                                                                     : ULY_ERR_CUDA;
     }
@@ -108,32 +129,25 @@ uly_status run_attention(int P, int b, int s, int hq, int hkv, int d, uly_dtype 
     return e == cudaSuccess ? ULY_OK : ULY_ERR_CUDA;
 }
 
-}  // namespace
-
-extern "C" {
-
-uly_status ulysses_a2a_seq2head(int P, int b, int s, int h, int d, uly_dtype dtype, const void* const* in_seq,
-                                void* const* out_head, cudaStream_t stream) {
-    return exchange(0, P, b, s, h, d, dtype, in_seq, out_head, stream);
-}
-
-uly_status ulysses_a2a_head2seq(int P, int b, int s, int h, int d, uly_dtype dtype, const void* const* in_head,
-                                void* const* out_seq, cudaStream_t stream) {
-    return exchange(1, P, b, s, h, d, dtype, in_head, out_seq, stream);
-}
-
-uly_status ulysses_local_attention(int P, int b, int s, int h_q, int h_kv, int d, uly_dtype dtype, int causal,
-                                   const void* const* q_head, const void* const* k_head, const void* const* v_head,
-                                   void* const* o_head, cudaStream_t stream) {
+// Head-layout attention of every rank; lse (optional, bf16 path only) receives the
+// per-row log-sum-exp.
+uly_status local_attention(int P, int b, int s, int h_q, int h_kv, int d, uly_dtype dtype, int causal,
+                           const void* const* q_head, const void* const* k_head, const void* const* v_head,
+                           void* const* o_head, float* const* lse, cudaStream_t stream) {
     uly_status st = check_attention_shape(P, b, s, h_q, h_kv, d, dtype);
     if (st != ULY_OK) return st;
     const int e = elem_bytes(dtype);
     const uint64_t qb = (uint64_t)b * s * (h_q / P) * d * e, kb = (uint64_t)b * s * (h_kv / P) * d * e;
-    std::vector<Range> rq, rk, rv, ro;
+    std::vector<Range> rq, rk, rv, ro, rl;
     if (!collect(q_head, P, qb, rq) || !collect(k_head, P, kb, rk) || !collect(v_head, P, kb, rv) ||
         !collect(reinterpret_cast<const void* const*>(o_head), P, qb, ro))
         return ULY_ERR_INVALID_ARG;
     if (overlaps(ro, rq) || overlaps(ro, rk) || overlaps(ro, rv) || self_overlap(ro)) return ULY_ERR_INVALID_ARG;
+    if (lse) {
+        if (!collect_f(lse, P, (uint64_t)b * (h_q / P) * s * 4, rl)) return ULY_ERR_INVALID_ARG;
+        if (self_overlap(rl) || overlaps(rl, rq) || overlaps(rl, rk) || overlaps(rl, rv) || overlaps(rl, ro))
+            return ULY_ERR_INVALID_ARG;
+    }
     uly::AttnPtrs ptrs;
     memset(&ptrs, 0, sizeof(ptrs));
     for (int r = 0; r < P; ++r) {
@@ -141,11 +155,47 @@ uly_status ulysses_local_attention(int P, int b, int s, int h_q, int h_kv, int d
         ptrs.k[r] = k_head[r];
         ptrs.v[r] = v_head[r];
         ptrs.o[r] = o_head[r];
+        ptrs.lse[r] = lse ? lse[r] : nullptr;
     }
     return run_attention(P, b, s, h_q, h_kv, d, dtype, causal, 0, ptrs, stream);
 }
 
-size_t ulysses_dist_attn_workspace_bytes(int P, int b, int s, int h_q, int h_kv, int d, uly_dtype dtype, int fused) {
+// Pointers of one head-layout scratch set inside a workspace: per rank, in this order,
+// the arrays whose per-rank sizes are listed in `sizes` (each 256-byte aligned).
+struct Carve {
+    uint8_t* base;
+    uint64_t per_rank;
+    std::vector<uint64_t> offs;
+    Carve(void* ws, const std::vector<uint64_t>& sizes) : base(static_cast<uint8_t*>(ws)), per_rank(0) {
+        for (uint64_t x : sizes) {
+            offs.push_back(per_rank);
+            per_rank += round256(x);
+        }
+    }
+    void* at(int r, int k) const { return base + (uint64_t)r * per_rank + offs[k]; }
+};
+
+// Workspace of the backward: per rank the two fp32 row arrays (lse2, D), and for the
+// distributed backward the head-layout Q, K, V, dO, dQ, dK, dV.
+std::vector<uint64_t> bwd_sizes(int P, int b, int s, int hq, int hkv, int d, int dist) {
+    const uint64_t ra = row_array_bytes(P, b, s, hq);
+    std::vector<uint64_t> v{ra, ra};
+    if (dist) {
+        const uint64_t qb = (uint64_t)b * s * (hq / P) * d * 2, kb = (uint64_t)b * s * (hkv / P) * d * 2;
+        for (uint64_t x : {qb, kb, kb, qb, qb, kb, kb}) v.push_back(x);
+    }
+    return v;
+}
+
+uly_status run_backward(int P, int b, int s, int hq, int hkv, int d, int causal, int od_seq,
+                        const uly::BwdPtrs& ptrs, cudaStream_t stream) {
+    int unsupported = 0;
+    cudaError_t e = uly::launch_attention_bwd_tc(P, b, s, hq, hkv, d, causal, od_seq, ptrs, stream, &unsupported);
+    if (unsupported) return ULY_ERR_UNSUPPORTED;
+    return e == cudaSuccess ? ULY_OK : ULY_ERR_CUDA;
+}
+
+size_t dist_workspace_bytes(int P, int b, int s, int h_q, int h_kv, int d, uly_dtype dtype, int fused) {
     if (check_attention_shape(P, b, s, h_q, h_kv, d, dtype) == ULY_ERR_INVALID_ARG) return 0;
     if (s % P) return 0;
     if (fused) return 0;
@@ -155,10 +205,11 @@ size_t ulysses_dist_attn_workspace_bytes(int P, int b, int s, int h_q, int h_kv,
     return (size_t)((uint64_t)P * (2 * qb + 2 * kb));
 }
 
-uly_status ulysses_dist_attn_fwd(int P, int b, int s, int h_q, int h_kv, int d, uly_dtype dtype, int causal,
-                                 const void* const* q_seq, const void* const* k_seq, const void* const* v_seq,
-                                 void* const* o_seq, void* workspace, size_t workspace_bytes, int fused,
-                                 cudaStream_t stream) {
+// The forward pipeline; lse (optional) receives the per-row log-sum-exp of every rank.
+uly_status dist_attn_fwd(int P, int b, int s, int h_q, int h_kv, int d, uly_dtype dtype, int causal,
+                         const void* const* q_seq, const void* const* k_seq, const void* const* v_seq,
+                         void* const* o_seq, float* const* lse, void* workspace, size_t workspace_bytes, int fused,
+                         cudaStream_t stream) {
     uly_status st = check_attention_shape(P, b, s, h_q, h_kv, d, dtype);
     if (st != ULY_OK) return st;
     st = check_exchange_shape(P, b, s, h_q, d, dtype);
@@ -173,6 +224,12 @@ uly_status ulysses_dist_attn_fwd(int P, int b, int s, int h_q, int h_kv, int d, 
         !collect(reinterpret_cast<const void* const*>(o_seq), P, qsb, ro))
         return ULY_ERR_INVALID_ARG;
     if (overlaps(ro, rq) || overlaps(ro, rk) || overlaps(ro, rv) || self_overlap(ro)) return ULY_ERR_INVALID_ARG;
+    std::vector<Range> rl;
+    if (lse) {
+        if (fused || !collect_f(lse, P, (uint64_t)b * (h_q / P) * s * 4, rl)) return ULY_ERR_INVALID_ARG;
+        if (self_overlap(rl) || overlaps(rl, rq) || overlaps(rl, rk) || overlaps(rl, rv) || overlaps(rl, ro))
+            return ULY_ERR_INVALID_ARG;
+    }
 
     if (fused) {
         if (dtype != ULY_BF16) return ULY_ERR_UNSUPPORTED;
@@ -187,11 +244,12 @@ uly_status ulysses_dist_attn_fwd(int P, int b, int s, int h_q, int h_kv, int d, 
         return run_attention(P, b, s, h_q, h_kv, d, dtype, causal, 1, ptrs, stream);
     }
 
-    const size_t need = ulysses_dist_attn_workspace_bytes(P, b, s, h_q, h_kv, d, dtype, 0);
+    const size_t need = dist_workspace_bytes(P, b, s, h_q, h_kv, d, dtype, 0);
     if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < need)
         return ULY_ERR_INVALID_ARG;
     std::vector<Range> rw{{reinterpret_cast<uintptr_t>(workspace), reinterpret_cast<uintptr_t>(workspace) + need}};
-    if (overlaps(rw, rq) || overlaps(rw, rk) || overlaps(rw, rv) || overlaps(rw, ro)) return ULY_ERR_INVALID_ARG;
+    if (overlaps(rw, rq) || overlaps(rw, rk) || overlaps(rw, rv) || overlaps(rw, ro) || overlaps(rw, rl))
+        return ULY_ERR_INVALID_ARG;
 
     // workspace: per rank [Q_head | K_head | V_head | O_head], each 256-byte aligned
     const uint64_t qhb = round256((uint64_t)b * s * (h_q / P) * d * e);
@@ -205,6 +263,7 @@ uly_status ulysses_dist_attn_fwd(int P, int b, int s, int h_q, int h_kv, int d, 
         head.k[r] = base + qhb;
         head.v[r] = base + qhb + khb;
         head.o[r] = base + qhb + 2 * khb;
+        head.lse[r] = lse ? lse[r] : nullptr;
     }
     // (1) all-to-all #1 for Q, K and V in one launch
     uly::PermuteTensor t[3];
@@ -233,6 +292,199 @@ uly_status ulysses_dist_attn_fwd(int P, int b, int s, int h_q, int h_kv, int d, 
     }
     to.h = h_q;
     return uly::launch_permute(1, P, b, s, d, e, &to, 1, stream) == cudaSuccess ? ULY_OK : ULY_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+uly_status ulysses_a2a_seq2head(int P, int b, int s, int h, int d, uly_dtype dtype, const void* const* in_seq,
+                                void* const* out_head, cudaStream_t stream) {
+    return exchange(0, P, b, s, h, d, dtype, in_seq, out_head, stream);
+}
+
+uly_status ulysses_a2a_head2seq(int P, int b, int s, int h, int d, uly_dtype dtype, const void* const* in_head,
+                                void* const* out_seq, cudaStream_t stream) {
+    return exchange(1, P, b, s, h, d, dtype, in_head, out_seq, stream);
+}
+
+uly_status ulysses_local_attention(int P, int b, int s, int h_q, int h_kv, int d, uly_dtype dtype, int causal,
+                                   const void* const* q_head, const void* const* k_head, const void* const* v_head,
+                                   void* const* o_head, cudaStream_t stream) {
+    return local_attention(P, b, s, h_q, h_kv, d, dtype, causal, q_head, k_head, v_head, o_head, nullptr, stream);
+}
+
+uly_status ulysses_local_attention_fwd_lse(int P, int b, int s, int h_q, int h_kv, int d, uly_dtype dtype,
+                                           int causal, const void* const* q_head, const void* const* k_head,
+                                           const void* const* v_head, void* const* o_head, float* const* lse,
+                                           cudaStream_t stream) {
+    uly_status st = check_train_shape(P, b, s, h_q, h_kv, d, dtype);
+    if (st != ULY_OK) return st;
+    if (!lse) return ULY_ERR_INVALID_ARG;
+    return local_attention(P, b, s, h_q, h_kv, d, dtype, causal, q_head, k_head, v_head, o_head, lse, stream);
+}
+
+size_t ulysses_dist_attn_workspace_bytes(int P, int b, int s, int h_q, int h_kv, int d, uly_dtype dtype, int fused) {
+    return dist_workspace_bytes(P, b, s, h_q, h_kv, d, dtype, fused);
+}
+
+uly_status ulysses_dist_attn_fwd(int P, int b, int s, int h_q, int h_kv, int d, uly_dtype dtype, int causal,
+                                 const void* const* q_seq, const void* const* k_seq, const void* const* v_seq,
+                                 void* const* o_seq, void* workspace, size_t workspace_bytes, int fused,
+                                 cudaStream_t stream) {
+    return dist_attn_fwd(P, b, s, h_q, h_kv, d, dtype, causal, q_seq, k_seq, v_seq, o_seq, nullptr, workspace,
+                         workspace_bytes, fused, stream);
+}
+
+uly_status ulysses_dist_attn_fwd_lse(int P, int b, int s, int h_q, int h_kv, int d, uly_dtype dtype, int causal,
+                                     const void* const* q_seq, const void* const* k_seq, const void* const* v_seq,
+                                     void* const* o_seq, float* const* lse, void* workspace, size_t workspace_bytes,
+                                     cudaStream_t stream) {
+    uly_status st = check_train_shape(P, b, s, h_q, h_kv, d, dtype);
+    if (st != ULY_OK) return st;
+    if (!lse) return ULY_ERR_INVALID_ARG;
+    return dist_attn_fwd(P, b, s, h_q, h_kv, d, dtype, causal, q_seq, k_seq, v_seq, o_seq, lse, workspace,
+                         workspace_bytes, 0, stream);
+}
+
+size_t ulysses_attn_bwd_workspace_bytes(int P, int b, int s, int h_q, int h_kv, int d, uly_dtype dtype, int dist) {
+    if (check_train_shape(P, b, s, h_q, h_kv, d, dtype) != ULY_OK) return 0;
+    if (dist && (check_exchange_shape(P, b, s, h_q, d, dtype) != ULY_OK ||
+                 check_exchange_shape(P, b, s, h_kv, d, dtype) != ULY_OK))
+        return 0;
+    uint64_t per_rank = 0;
+    for (uint64_t x : bwd_sizes(P, b, s, h_q, h_kv, d, dist)) per_rank += round256(x);
+    return (size_t)(per_rank * P);
+}
+
+uly_status ulysses_local_attention_bwd(int P, int b, int s, int h_q, int h_kv, int d, uly_dtype dtype, int causal,
+                                       const void* const* q_head, const void* const* k_head,
+                                       const void* const* v_head, const void* const* o_head,
+                                       const void* const* do_head, const float* const* lse, void* const* dq_head,
+                                       void* const* dk_head, void* const* dv_head, void* workspace,
+                                       size_t workspace_bytes, cudaStream_t stream) {
+    uly_status st = check_train_shape(P, b, s, h_q, h_kv, d, dtype);
+    if (st != ULY_OK) return st;
+    const uint64_t qb = (uint64_t)b * s * (h_q / P) * d * 2, kb = (uint64_t)b * s * (h_kv / P) * d * 2;
+    std::vector<Range> in, rdq, rdk, rdv;
+    if (!collect(q_head, P, qb, in) || !collect(k_head, P, kb, in) || !collect(v_head, P, kb, in) ||
+        !collect(o_head, P, qb, in) || !collect(do_head, P, qb, in) ||
+        !collect_f(lse, P, (uint64_t)b * (h_q / P) * s * 4, in) ||
+        !collect(reinterpret_cast<const void* const*>(dq_head), P, qb, rdq) ||
+        !collect(reinterpret_cast<const void* const*>(dk_head), P, kb, rdk) ||
+        !collect(reinterpret_cast<const void* const*>(dv_head), P, kb, rdv))
+        return ULY_ERR_INVALID_ARG;
+    std::vector<Range> outs(rdq);
+    outs.insert(outs.end(), rdk.begin(), rdk.end());
+    outs.insert(outs.end(), rdv.begin(), rdv.end());
+    if (self_overlap(outs) || overlaps(outs, in)) return ULY_ERR_INVALID_ARG;
+    const size_t need = ulysses_attn_bwd_workspace_bytes(P, b, s, h_q, h_kv, d, dtype, 0);
+    if (!workspace_ok(workspace, workspace_bytes, need)) return ULY_ERR_INVALID_ARG;
+    std::vector<Range> rw{{reinterpret_cast<uintptr_t>(workspace), reinterpret_cast<uintptr_t>(workspace) + need}};
+    if (overlaps(rw, in) || overlaps(rw, outs)) return ULY_ERR_INVALID_ARG;
+    const Carve ws(workspace, bwd_sizes(P, b, s, h_q, h_kv, d, 0));
+    uly::BwdPtrs* p = new uly::BwdPtrs;
+    memset(p, 0, sizeof(uly::BwdPtrs));
+    for (int r = 0; r < P; ++r) {
+        p->q[r] = q_head[r];
+        p->k[r] = k_head[r];
+        p->v[r] = v_head[r];
+        p->dout[r] = do_head[r];
+        p->o_rows[r] = o_head[r];
+        p->do_rows[r] = do_head[r];
+        p->lse[r] = lse[r];
+        p->dq[r] = dq_head[r];
+        p->dk[r] = dk_head[r];
+        p->dv[r] = dv_head[r];
+        p->lse2[r] = static_cast<float*>(ws.at(r, 0));
+        p->dsum[r] = static_cast<float*>(ws.at(r, 1));
+    }
+    st = run_backward(P, b, s, h_q, h_kv, d, causal, 0, *p, stream);
+    delete p;
+    return st;
+}
+
+uly_status ulysses_dist_attn_bwd(int P, int b, int s, int h_q, int h_kv, int d, uly_dtype dtype, int causal,
+                                 const void* const* q_seq, const void* const* k_seq, const void* const* v_seq,
+                                 const void* const* o_seq, const void* const* do_seq, const float* const* lse,
+                                 void* const* dq_seq, void* const* dk_seq, void* const* dv_seq, void* workspace,
+                                 size_t workspace_bytes, cudaStream_t stream) {
+    uly_status st = check_train_shape(P, b, s, h_q, h_kv, d, dtype);
+    if (st != ULY_OK) return st;
+    st = check_exchange_shape(P, b, s, h_q, d, dtype);
+    if (st != ULY_OK) return st;
+    st = check_exchange_shape(P, b, s, h_kv, d, dtype);
+    if (st != ULY_OK) return st;
+    const int S = s / P;
+    const uint64_t qsb = (uint64_t)b * S * h_q * d * 2, ksb = (uint64_t)b * S * h_kv * d * 2;
+    std::vector<Range> in, rdq, rdk, rdv;
+    if (!collect(q_seq, P, qsb, in) || !collect(k_seq, P, ksb, in) || !collect(v_seq, P, ksb, in) ||
+        !collect(o_seq, P, qsb, in) || !collect(do_seq, P, qsb, in) ||
+        !collect_f(lse, P, (uint64_t)b * (h_q / P) * s * 4, in) ||
+        !collect(reinterpret_cast<const void* const*>(dq_seq), P, qsb, rdq) ||
+        !collect(reinterpret_cast<const void* const*>(dk_seq), P, ksb, rdk) ||
+        !collect(reinterpret_cast<const void* const*>(dv_seq), P, ksb, rdv))
+        return ULY_ERR_INVALID_ARG;
+    std::vector<Range> outs(rdq);
+    outs.insert(outs.end(), rdk.begin(), rdk.end());
+    outs.insert(outs.end(), rdv.begin(), rdv.end());
+    if (self_overlap(outs) || overlaps(outs, in)) return ULY_ERR_INVALID_ARG;
+    const size_t need = ulysses_attn_bwd_workspace_bytes(P, b, s, h_q, h_kv, d, dtype, 1);
+    if (!workspace_ok(workspace, workspace_bytes, need)) return ULY_ERR_INVALID_ARG;
+    std::vector<Range> rw{{reinterpret_cast<uintptr_t>(workspace), reinterpret_cast<uintptr_t>(workspace) + need}};
+    if (overlaps(rw, in) || overlaps(rw, outs)) return ULY_ERR_INVALID_ARG;
+    const Carve ws(workspace, bwd_sizes(P, b, s, h_q, h_kv, d, 1));
+    enum { LSE2, DSUM, QH, KH, VH, DOH, DQH, DKH, DVH };
+    // (1) all-to-all #1 on Q, K, V and dO (the backward of all-to-all #2 is all-to-all #1)
+    uly::PermuteTensor* t = new uly::PermuteTensor[4];
+    memset(t, 0, 4 * sizeof(uly::PermuteTensor));
+    const void* const* srcs[4] = {q_seq, k_seq, v_seq, do_seq};
+    const int dsts[4] = {QH, KH, VH, DOH};
+    for (int k = 0; k < 4; ++k) {
+        for (int r = 0; r < P; ++r) {
+            t[k].src[r] = srcs[k][r];
+            t[k].dst[r] = ws.at(r, dsts[k]);
+        }
+        t[k].h = (k == 1 || k == 2) ? h_kv : h_q;
+    }
+    cudaError_t ce = uly::launch_permute(0, P, b, s, d, 2, t, 4, stream);
+    delete[] t;
+    if (ce != cudaSuccess) return ULY_ERR_CUDA;
+    // (2) local backward of every rank; D straight from the seq-layout O and dO
+    uly::BwdPtrs* p = new uly::BwdPtrs;
+    memset(p, 0, sizeof(uly::BwdPtrs));
+    for (int r = 0; r < P; ++r) {
+        p->q[r] = ws.at(r, QH);
+        p->k[r] = ws.at(r, KH);
+        p->v[r] = ws.at(r, VH);
+        p->dout[r] = ws.at(r, DOH);
+        p->o_rows[r] = o_seq[r];
+        p->do_rows[r] = do_seq[r];
+        p->lse[r] = lse[r];
+        p->dq[r] = ws.at(r, DQH);
+        p->dk[r] = ws.at(r, DKH);
+        p->dv[r] = ws.at(r, DVH);
+        p->lse2[r] = static_cast<float*>(ws.at(r, LSE2));
+        p->dsum[r] = static_cast<float*>(ws.at(r, DSUM));
+    }
+    st = run_backward(P, b, s, h_q, h_kv, d, causal, 1, *p, stream);
+    delete p;
+    if (st != ULY_OK) return st;
+    // (3) all-to-all #2 on dQ, dK, dV (the backward of all-to-all #1)
+    t = new uly::PermuteTensor[3];
+    memset(t, 0, 3 * sizeof(uly::PermuteTensor));
+    void* const* dsts2[3] = {dq_seq, dk_seq, dv_seq};
+    const int srcs2[3] = {DQH, DKH, DVH};
+    for (int k = 0; k < 3; ++k) {
+        for (int r = 0; r < P; ++r) {
+            t[k].src[r] = ws.at(r, srcs2[k]);
+            t[k].dst[r] = dsts2[k][r];
+        }
+        t[k].h = k == 0 ? h_q : h_kv;
+    }
+    ce = uly::launch_permute(1, P, b, s, d, 2, t, 3, stream);
+    delete[] t;
+    return ce == cudaSuccess ? ULY_OK : ULY_ERR_CUDA;
 }
 
 uly_status ulysses_device_status(int clear) {

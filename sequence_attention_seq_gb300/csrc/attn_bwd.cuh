@@ -1,0 +1,649 @@
+// Backward of the bf16 local attention on the sm_103a tensor cores.  Included by attn_tc.cu
+// inside its anonymous namespace: it shares the bounded waits, the device error word, the
+// bf16 packing and the tensor-map encoder.
+//
+// What it computes ("02 · DeepSpeed-Ulysses", section 5: the local attention's backward is
+// the ordinary one).  With the per-row log-sum-exp L_i of the scaled scores saved by the
+// forward, P_ij = exp(q_i.k_j/sqrt(d) - L_i) (0 for masked keys) and D_i = sum_c dO_ic O_ic:
+//   dV_j = sum_i P_ij dO_i          dP_ij = dO_i . v_j         dS_ij = P_ij (dP_ij - D_i)
+//   dK_j = sum_i dS_ij q_i / sqrt(d)                           dQ_i = sum_j dS_ij k_j / sqrt(d)
+// Three launches, no atomics, every output element written once:
+//   bwd_prep_kernel  D_i from O and dO, and L_i in base-2 units, into padded per-row arrays
+//   bwd_dkdv_kernel  one CTA per (rank, batch, K/V head, 128-key tile).  S^T = K Q^T and
+//                    dP^T = V dO^T land in tensor memory; eight row warps (two per tensor
+//                    memory lane quarter, each owning 64 of the 128 query columns) form P^T
+//                    (bf16, written back over S^T) and dS^T (bf16, into shared memory in the
+//                    operand layout); dV += P^T dO takes P^T straight from tensor memory and
+//                    dK += dS^T Q reads dS^T from shared memory.  The loop runs over every
+//                    query head of the K/V head's group and every query tile that sees the
+//                    key tile.
+//   bwd_dq_kernel    one CTA per (rank, batch, query head, 128-query tile).  S = Q K^T (two
+//                    tensor-memory buffers, so S of tile n+2 can be computed while tile n+1
+//                    is being worked on) and dP = dO V^T; the row warps write dS as bf16 over
+//                    S and dQ += dS K takes it from tensor memory.
+// Recomputing S and dP in both kernels costs 7 tile products instead of 5 but needs neither
+// atomics nor a second pass over dQ, and gives the same bits on every run.
+//
+// Tile orders.  All CTAs of one head stream the same sequence of Q/dO (or K/V) tiles at
+// the same time, so each tile is read from DRAM about once and served from L2 after that:
+// the dK/dV kernel walks query tiles from the last one down (causal: down to the diagonal
+// tile, which comes last and is the only masked one), the dQ kernel walks key tiles from 0
+// up (causal: up to the diagonal).  Within a head, the CTAs with the most tiles come first.
+// Rows past the sequence end read zeros (TMA fill) and get L = +inf, so their P is 0.
+//
+// Every wait is bounded like the forward's: a wait that gives up sets the device error
+// word, and the CTA drains its copies and MMAs, frees tensor memory and returns.
+
+constexpr int kBwdRowWarps = 8;
+constexpr int kBwdProducer = 8;
+constexpr int kBwdMma = 9;
+constexpr int kBwdThreads = 320;
+constexpr int kRingKV = 4;   // dK/dV kernel: Q/dO ring slots (two query tiles in flight)
+constexpr int kRingQ = 5;    // dQ kernel: K/V ring slots
+
+struct BwdParams {
+    CUtensorMap mq[kMaxMaps], mk[kMaxMaps], mv[kMaxMaps], mdo[kMaxMaps];
+    uint8_t* dq[kMaxMaps];        // [b][s][hq][d] bf16 (head layout of the rank)
+    uint8_t* dk[kMaxMaps];        // [b][s][hkv][d] bf16
+    uint8_t* dv[kMaxMaps];
+    const float* lse2[kMaxMaps];  // [b][hq][s_pad]: log-sum-exp in base-2 units (+inf on padding)
+    const float* dsum[kMaxMaps];  // [b][hq][s_pad]: D (0 on padding)
+    int s, s_pad, n_tiles, hq, hkv, g, b, causal;
+    float scale_log2;             // log2(e)/sqrt(d)
+    float scale;                  // 1/sqrt(d)
+};
+
+// ------------------------------------------------------------------------- prep
+struct PrepParams {
+    const uint8_t* o[kMaxRanks];
+    const uint8_t* dout[kMaxRanks];
+    const float* lse[kMaxRanks];  // [b][Hq][s], natural log
+    float* lse2[kMaxRanks];
+    float* dsum[kMaxRanks];
+    long long rows;               // P * b * Hq * s_pad
+    int b, s, s_pad, Hq, d, S, hq_total, seq_layout;
+    int lanes_log2;               // log2(d / 8): lanes per row
+};
+
+// d/8 lanes per (rank, batch, head, token) row, 16 bytes each.  O and dO are read in the
+// layout the caller holds them in: head layout of rank r, or (seq_layout) the seq layout,
+// where head-layout row (r, hh, t) is row t % S of rank t / S at head r*Hq + hh.
+__global__ void __launch_bounds__(256) bwd_prep_kernel(const __grid_constant__ PrepParams p) {
+    const long long gt = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    const long long row = gt >> p.lanes_log2;
+    const int sub = (int)(gt & ((1 << p.lanes_log2) - 1));
+    const bool valid = row < p.rows;
+    const long long rr = valid ? row : 0;
+    const int t = (int)(rr % p.s_pad);
+    long long r1 = rr / p.s_pad;
+    const int hh = (int)(r1 % p.Hq);
+    r1 /= p.Hq;
+    const int bb = (int)(r1 % p.b);
+    const int r = (int)(r1 / p.b);
+    float acc = 0.f;
+    if (valid && t < p.s) {
+        size_t off;
+        const uint8_t *o, *g;
+        if (p.seq_layout) {
+            const int j = t / p.S;
+            off = (((size_t)bb * p.S + (t - j * p.S)) * p.hq_total + (size_t)r * p.Hq + hh) * (size_t)p.d * 2;
+            o = p.o[j];
+            g = p.dout[j];
+        } else {
+            off = (((size_t)bb * p.s + t) * p.Hq + hh) * (size_t)p.d * 2;
+            o = p.o[r];
+            g = p.dout[r];
+        }
+        const uint4 a = *reinterpret_cast<const uint4*>(o + off + sub * 16);
+        const uint4 c = *reinterpret_cast<const uint4*>(g + off + sub * 16);
+        const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
+        const __nv_bfloat162* c2 = reinterpret_cast<const __nv_bfloat162*>(&c);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float2 fa = __bfloat1622float2(a2[e]), fc = __bfloat1622float2(c2[e]);
+            acc = fmaf(fa.x, fc.x, fmaf(fa.y, fc.y, acc));
+        }
+    }
+    for (int o = 1 << (p.lanes_log2 - 1); o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (valid && sub == 0) {
+        const size_t vi = ((size_t)bb * p.Hq + hh) * p.s_pad + t;
+        if (t < p.s) {
+            p.dsum[r][vi] = acc;
+            p.lse2[r][vi] = p.lse[r][((size_t)bb * p.Hq + hh) * p.s + t] * 1.4426950408889634f;
+        } else {
+            p.dsum[r][vi] = 0.f;
+            p.lse2[r][vi] = INFINITY;
+        }
+    }
+}
+
+// --------------------------------------------------------------- shared pieces
+template <int D, int RING, bool DS_SMEM>
+struct BwdSmem {
+    static constexpr uint32_t kTile = 128 * D * 2;
+    static constexpr uint32_t offFixA = 0;          // K (dK/dV kernel) or Q (dQ kernel)
+    static constexpr uint32_t offFixB = kTile;      // V or dO
+    static constexpr uint32_t offRing = 2 * kTile;  // RING streamed tiles
+    static constexpr uint32_t offDS = offRing + RING * kTile;  // dS^T, 128 x 128 bf16 (dK/dV kernel)
+    static constexpr uint32_t offBar = offDS + (DS_SMEM ? 128u * 128u * 2u : 0u);
+    static constexpr uint32_t kBarSlots = 24;
+    static constexpr uint32_t kUsed = offBar + kBarSlots * 8 + 64;
+    static constexpr uint32_t kAlloc = kUsed + 1024;  // slack to align the base to 1024 bytes
+};
+
+// Stores NC accumulator columns of this thread's tensor-memory lane as bf16 (times mul).
+template <int NC>
+__device__ __forceinline__ void store_row_bf16(uint32_t taddr, uint8_t* dst, float mul, bool ok) {
+#pragma unroll
+    for (int c = 0; c < NC / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld32(taddr + c * 32, r);
+        tmem_wait_ld();
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+            uint4 v;
+            v.x = pack_bf16x2(__uint_as_float(r[q4 * 8 + 0]) * mul, __uint_as_float(r[q4 * 8 + 1]) * mul);
+            v.y = pack_bf16x2(__uint_as_float(r[q4 * 8 + 2]) * mul, __uint_as_float(r[q4 * 8 + 3]) * mul);
+            v.z = pack_bf16x2(__uint_as_float(r[q4 * 8 + 4]) * mul, __uint_as_float(r[q4 * 8 + 5]) * mul);
+            v.w = pack_bf16x2(__uint_as_float(r[q4 * 8 + 6]) * mul, __uint_as_float(r[q4 * 8 + 7]) * mul);
+            if (ok) *reinterpret_cast<uint4*>(dst + (c * 32 + q4 * 8) * 2) = v;
+        }
+    }
+}
+
+// Initialises the barriers (those in [rows_from, rows_to) count one arrival per row warp)
+// and allocates tensor memory; false when the CTA must leave at once.
+__device__ __forceinline__ bool bwd_setup(uint64_t* bars, int nbars, int rows_from, int rows_to, Shared* sh) {
+    if (threadIdx.x == 0) {
+        sh->abort = error_word_set() ? 1 : 0;
+        for (int i = 0; i < nbars; ++i)
+            mbar_init(&bars[i], (i >= rows_from && i < rows_to) ? (uint32_t)kBwdRowWarps : 1u);
+        fence_mbarrier_init();
+    }
+    __syncthreads();
+    if (sh->abort) return false;
+    if ((threadIdx.x >> 5) == kBwdMma) tmem_alloc(&sh->tmem_base, kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    return true;
+}
+
+// d (128 x 128, fp32 in tensor memory) = A B^T, A and B 128 x D K-major tiles in shared memory.
+template <int D>
+__device__ __forceinline__ void mma_kmajor(uint32_t d, uint64_t a, uint64_t b) {
+    constexpr uint32_t kIdesc = idesc_bf16_f32(128, 128, false);
+    constexpr uint32_t kSlab = 128 * 128;
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = ((kk >> 2) * kSlab + (kk & 3) * 32) >> 4;
+        mma_bf16_ss_warp(d, a + off, b + off, kIdesc, kk > 0 ? 1u : 0u);
+    }
+}
+
+// acc (128 x D) += A (128 x 128 bf16 pairs in tensor memory at a_tmem) * B (128 x D tile in
+// shared memory, D contiguous: MN-major).  The row warps lay A out in two 64-column halves:
+// columns 16k..16k+15 of A sit at a_tmem + 64*(k/4) + 8*(k%4).
+template <int D>
+__device__ __forceinline__ void mma_acc_tmemA(uint32_t acc, uint32_t a_tmem, uint64_t b_mn, bool accumulate) {
+    constexpr uint32_t kIdesc = idesc_bf16_f32(128, D, true);
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk)
+        mma_bf16_ts_warp(acc, a_tmem + (kk >> 2) * 64 + (kk & 3) * 8, b_mn + ((kk * 16 * 128) >> 4), kIdesc,
+                         (accumulate || kk > 0) ? 1u : 0u);
+}
+
+// acc (128 x D) += A (128 x 128 K-major bf16 tile in shared memory) * B (MN-major tile).
+template <int D>
+__device__ __forceinline__ void mma_acc_smemA(uint32_t acc, uint64_t a_k, uint64_t b_mn, bool accumulate) {
+    constexpr uint32_t kIdesc = idesc_bf16_f32(128, D, true);
+    constexpr uint32_t kSlab = 128 * 128;
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk)
+        mma_bf16_ss_warp(acc, a_k + (((kk >> 2) * kSlab + (kk & 3) * 32) >> 4), b_mn + ((kk * 16 * 128) >> 4),
+                         kIdesc, (accumulate || kk > 0) ? 1u : 0u);
+}
+
+// ------------------------------------------------------------------ dK / dV
+// Block -> (rank, batch, K/V head, key tile), key tile fastest and ascending.
+// Tensor memory: S^T (then P^T) 0..127 | dP^T 128..255 | dK 256.. | dV 384..
+template <int D>
+__global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_constant__ BwdParams p) {
+    using L = BwdSmem<D, kRingKV, true>;
+    constexpr uint32_t kSlab = 128 * 128;
+    enum {
+        FIX = 0, FULL = 1, EMPTY = FULL + kRingKV, S_FULL = EMPTY + kRingKV, DP_FULL, P_READY, DS_READY, DS_EMPTY,
+        FINAL, NBARS
+    };
+    static_assert(NBARS <= (int)L::kBarSlots, "barrier slots");
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::offBar);
+    Shared* sh = reinterpret_cast<Shared*>(smem + L::offBar + L::kBarSlots * 8);
+    const uint32_t sbase = smem_addr(smem);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    int bid = blockIdx.x;
+    const int kt = bid % p.n_tiles;
+    bid /= p.n_tiles;
+    const int kvh = bid % p.hkv;
+    bid /= p.hkv;
+    const int bb = bid % p.b;
+    const int rank = bid / p.b;
+    const int k0 = kt * 128;
+    const int n_steps = p.g * (p.n_tiles - (p.causal ? kt : 0));  // (query tile, head) pairs
+    // step n: query tile n_tiles-1 - n/g of query head kvh*g + n%g
+    const int g = p.g, n_tiles = p.n_tiles;
+    auto step_head = [kvh, g](int n) { return kvh * g + n % g; };
+    auto step_qt = [n_tiles, g](int n) { return n_tiles - 1 - n / g; };
+
+    if (!bwd_setup(bars, NBARS, P_READY, DS_READY + 1, sh)) return;
+    const uint32_t tmem = sh->tmem_base;
+
+    if (warp == kBwdProducer) {
+        const CUtensorMap* mq = &p.mq[rank];
+        const CUtensorMap* mdo = &p.mdo[rank];
+        // the fixed tiles: K (A) and V (B) of this key tile; map_of gives Q then dO per step
+        mbar_arrive_expect_tx_warp(&bars[FIX], 2 * L::kTile);
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c) {
+            tma_load_4d_warp(sbase + L::offFixA + c * kSlab, &p.mk[rank], &bars[FIX], c * 64, kvh, k0, bb);
+            tma_load_4d_warp(sbase + L::offFixB + c * kSlab, &p.mv[rank], &bars[FIX], c * 64, kvh, k0, bb);
+        }
+        int issued = 0;
+        bool ok = true;
+        for (int m = 0; m < 2 * n_steps; ++m) {
+            const int slot = m % kRingKV;
+            ok = wait_phase_warp(&bars[EMPTY + slot], ((m / kRingKV) & 1) ^ 1, sh);
+            if (!ok) break;
+            const int n = m >> 1;
+            mbar_arrive_expect_tx_warp(&bars[FULL + slot], L::kTile);
+#pragma unroll
+            for (int c = 0; c < D / 64; ++c)
+                tma_load_4d_warp(sbase + L::offRing + slot * L::kTile + c * kSlab, (m & 1) ? mdo : mq,
+                                 &bars[FULL + slot], c * 64, step_head(n), step_qt(n) * 128, bb);
+            ++issued;
+        }
+        if (!ok) {
+            for (int slot = 0; slot < kRingKV; ++slot) {
+                const int cnt = (issued - slot + kRingKV - 1) / kRingKV;
+                if (cnt > 0) drain_phase(&bars[FULL + slot], (cnt - 1) & 1);
+            }
+            drain_phase(&bars[FIX], 0);
+        }
+    } else if (warp == kBwdMma) {
+        const uint64_t dk_a = smem_desc_sw128(sbase + L::offFixA, 16, 1024);        // K
+        const uint64_t dv_a = smem_desc_sw128(sbase + L::offFixB, 16, 1024);        // V
+        const uint64_t ring_k = smem_desc_sw128(sbase + L::offRing, 16, 1024);      // Q / dO, K-major
+        const uint64_t ring_mn = smem_desc_sw128(sbase + L::offRing, kSlab, 1024);  // Q / dO, MN-major
+        const uint64_t ds_a = smem_desc_sw128(sbase + L::offDS, 16, 1024);         // dS^T, K-major
+        auto so = [](int m) { return (uint64_t)(((m % kRingKV) * L::kTile) >> 4); };
+        auto full = [&](int m) { return wait_phase_warp(&bars[FULL + m % kRingKV], (m / kRingKV) & 1, sh); };
+        bool ok = wait_phase_warp(&bars[FIX], 0, sh) && full(0);
+        if (ok) {
+            tc_fence_after();
+            mma_kmajor<D>(tmem, dk_a, ring_k + so(0));  // S^T(0)
+            mma_commit_warp(&bars[S_FULL]);
+            ok = full(1);
+        }
+        if (ok) {
+            tc_fence_after();
+            mma_kmajor<D>(tmem + 128u, dv_a, ring_k + so(1));  // dP^T(0)
+            mma_commit_warp(&bars[DP_FULL]);
+        }
+        for (int n = 0; n < n_steps && ok; ++n) {
+            const int mq = 2 * n, mo = 2 * n + 1;
+            ok = wait_phase_warp(&bars[P_READY], n & 1, sh);
+            if (!ok) break;
+            tc_fence_after();
+            mma_acc_tmemA<D>(tmem + 384u, tmem, ring_mn + so(mo), n > 0);  // dV += P^T dO
+            mma_commit_warp(&bars[EMPTY + mo % kRingKV]);
+            if (n + 1 < n_steps) {  // S^T(n+1) over P^T(n): issued after the product that reads it
+                ok = full(mq + 2);
+                if (!ok) break;
+                tc_fence_after();
+                mma_kmajor<D>(tmem, dk_a, ring_k + so(mq + 2));
+                mma_commit_warp(&bars[S_FULL]);
+            }
+            ok = wait_phase_warp(&bars[DS_READY], n & 1, sh);
+            if (!ok) break;
+            tc_fence_after();
+            mma_acc_smemA<D>(tmem + 256u, ds_a, ring_mn + so(mq), n > 0);  // dK += dS^T Q
+            mma_commit_warp(&bars[DS_EMPTY]);
+            mma_commit_warp(&bars[EMPTY + mq % kRingKV]);
+            if (n + 1 < n_steps) {  // dP^T(n+1): the row warps have read dP^T(n)
+                ok = full(mo + 2);
+                if (!ok) break;
+                tc_fence_after();
+                mma_kmajor<D>(tmem + 128u, dv_a, ring_k + so(mo + 2));
+                mma_commit_warp(&bars[DP_FULL]);
+            }
+        }
+        mma_commit_warp(&bars[FINAL]);
+        drain_phase(&bars[FINAL], 0);
+    } else {
+        // row warps: thread = key row, warp half = 64 query columns
+        const int sub = warp & 3, half = warp >> 2;
+        const int row = sub * 32 + lane, key = k0 + row;
+        const uint32_t lane_off = (uint32_t)(sub * 32) << 16;
+        const uint32_t tS = tmem + lane_off + half * 64, tdP = tmem + 128u + lane_off + half * 64;
+        uint8_t* ds_row = smem + L::offDS + half * kSlab + row * 128;
+        const float sc = p.scale_log2;
+        bool ok = true;
+        for (int n = 0; n < n_steps; ++n) {
+            const int hh = step_head(n), qt = step_qt(n);
+            const int qb = qt * 128 + half * 64;  // first query column of this warp
+            const size_t vbase = ((size_t)bb * p.hq + hh) * p.s_pad + qb;
+            const float4* l4 = reinterpret_cast<const float4*>(p.lse2[rank] + vbase);
+            const float4* d4 = reinterpret_cast<const float4*>(p.dsum[rank] + vbase);
+            const bool diag = p.causal && qt == kt;
+            float pf[64];
+            ok = wait_phase_warp(&bars[S_FULL], n & 1, sh);
+            if (!ok) break;
+            tc_fence_after();
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                uint32_t sv[32];
+                float lv[32];
+                tmem_ld32(tS + c * 32, sv);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float4 x = __ldg(l4 + c * 8 + i);
+                    lv[4 * i] = x.x;
+                    lv[4 * i + 1] = x.y;
+                    lv[4 * i + 2] = x.z;
+                    lv[4 * i + 3] = x.w;
+                }
+                tmem_wait_ld();
+                uint32_t pk[16];
+#pragma unroll
+                for (int e = 0; e < 32; e += 2) {
+                    float a0, a1;
+                    ffma2(a0, a1, __uint_as_float(sv[e]), __uint_as_float(sv[e + 1]), sc, sc, -lv[e], -lv[e + 1]);
+                    float p0 = ex2_approx(a0), p1 = ex2_approx(a1);
+                    if (diag) {
+                        const int q = qb + c * 32 + e;
+                        p0 = key <= q ? p0 : 0.f;
+                        p1 = key <= q + 1 ? p1 : 0.f;
+                    }
+                    pf[c * 32 + e] = p0;
+                    pf[c * 32 + e + 1] = p1;
+                    pk[e >> 1] = pack_bf16x2(p0, p1);
+                }
+                tmem_st16(tS + c * 16, pk);  // P^T over S^T columns this warp has already read
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[P_READY]);
+
+            ok = wait_phase_warp(&bars[DP_FULL], n & 1, sh);
+            if (ok && n > 0) ok = wait_phase_warp(&bars[DS_EMPTY], (n - 1) & 1, sh);
+            if (!ok) break;
+            tc_fence_after();
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                uint32_t dv[32];
+                float dl[32];
+                tmem_ld32(tdP + c * 32, dv);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float4 x = __ldg(d4 + c * 8 + i);
+                    dl[4 * i] = x.x;
+                    dl[4 * i + 1] = x.y;
+                    dl[4 * i + 2] = x.z;
+                    dl[4 * i + 3] = x.w;
+                }
+                tmem_wait_ld();
+                uint32_t pk[16];
+#pragma unroll
+                for (int e = 0; e < 32; e += 2) {
+                    float t0, t1;
+                    fadd2(t0, t1, __uint_as_float(dv[e]), __uint_as_float(dv[e + 1]), -dl[e], -dl[e + 1]);
+                    pk[e >> 1] = pack_bf16x2(pf[c * 32 + e] * t0, pf[c * 32 + e + 1] * t1);
+                }
+                // dS^T row into the K-major 128-byte-swizzled operand tile (slab = this half)
+#pragma unroll
+                for (int q8 = 0; q8 < 4; ++q8) {
+                    const int chunk = c * 4 + q8;  // 16-byte chunk (8 queries) within the 64-query row
+                    *reinterpret_cast<uint4*>(ds_row + ((chunk ^ (row & 7)) << 4)) =
+                        make_uint4(pk[q8 * 4 + 0], pk[q8 * 4 + 1], pk[q8 * 4 + 2], pk[q8 * 4 + 3]);
+                }
+            }
+            fence_proxy_async_smem();  // generic-proxy stores -> visible to the tensor pipe
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[DS_READY]);
+        }
+        if (ok) ok = wait_phase_warp(&bars[FINAL], 0, sh);
+        if (ok) {
+            tc_fence_after();
+            const bool kok = key < p.s;
+            const size_t off = (((size_t)bb * p.s + (kok ? key : 0)) * p.hkv + kvh) * (size_t)D * 2 + half * D;
+            store_row_bf16<D / 2>(tmem + 256u + lane_off + half * (D / 2), p.dk[rank] + off, p.scale, kok);
+            store_row_bf16<D / 2>(tmem + 384u + lane_off + half * (D / 2), p.dv[rank] + off, 1.0f, kok);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kBwdMma) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// ----------------------------------------------------------------------- dQ
+// Block -> (rank, batch, query head, query tile), query tile fastest, last tile first;
+// query heads sharing a K/V head are adjacent.  Tensor memory: S/dS buffer 0 0..127 |
+// dP 128..255 | dQ 256.. | S/dS buffer 1 384..511.
+template <int D>
+__global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_constant__ BwdParams p) {
+    using L = BwdSmem<D, kRingQ, false>;
+    constexpr uint32_t kSlab = 128 * 128;
+    enum {
+        FIX = 0, FULL = 1, EMPTY = FULL + kRingQ, S_FULL = EMPTY + kRingQ, DP_FULL = S_FULL + 2, DS_READY, FINAL,
+        NBARS
+    };
+    static_assert(NBARS <= (int)L::kBarSlots, "barrier slots");
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::offBar);
+    Shared* sh = reinterpret_cast<Shared*>(smem + L::offBar + L::kBarSlots * 8);
+    const uint32_t sbase = smem_addr(smem);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    int bid = blockIdx.x;
+    const int qt = p.n_tiles - 1 - bid % p.n_tiles;
+    bid /= p.n_tiles;
+    const int hh = bid % p.hq;
+    bid /= p.hq;
+    const int bb = bid % p.b;
+    const int rank = bid / p.b;
+    const int kvh = hh / p.g;
+    const int q0 = qt * 128;
+    const int n_steps = p.causal ? qt + 1 : p.n_tiles;  // key tiles 0 .. n_steps-1
+
+    if (!bwd_setup(bars, NBARS, DS_READY, DS_READY + 1, sh)) return;
+    const uint32_t tmem = sh->tmem_base;
+    auto sbuf = [tmem](int n) { return tmem + ((n & 1) ? 384u : 0u); };
+
+    if (warp == kBwdProducer) {
+        const CUtensorMap* mk = &p.mk[rank];
+        const CUtensorMap* mv = &p.mv[rank];
+        mbar_arrive_expect_tx_warp(&bars[FIX], 2 * L::kTile);
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c) {
+            tma_load_4d_warp(sbase + L::offFixA + c * kSlab, &p.mq[rank], &bars[FIX], c * 64, hh, q0, bb);
+            tma_load_4d_warp(sbase + L::offFixB + c * kSlab, &p.mdo[rank], &bars[FIX], c * 64, hh, q0, bb);
+        }
+        int issued = 0;
+        bool ok = true;
+        for (int m = 0; m < 2 * n_steps; ++m) {  // K_n, then V_n
+            const int slot = m % kRingQ;
+            ok = wait_phase_warp(&bars[EMPTY + slot], ((m / kRingQ) & 1) ^ 1, sh);
+            if (!ok) break;
+            mbar_arrive_expect_tx_warp(&bars[FULL + slot], L::kTile);
+#pragma unroll
+            for (int c = 0; c < D / 64; ++c)
+                tma_load_4d_warp(sbase + L::offRing + slot * L::kTile + c * kSlab, (m & 1) ? mv : mk,
+                                 &bars[FULL + slot], c * 64, kvh, (m >> 1) * 128, bb);
+            ++issued;
+        }
+        if (!ok) {
+            for (int slot = 0; slot < kRingQ; ++slot) {
+                const int cnt = (issued - slot + kRingQ - 1) / kRingQ;
+                if (cnt > 0) drain_phase(&bars[FULL + slot], (cnt - 1) & 1);
+            }
+            drain_phase(&bars[FIX], 0);
+        }
+    } else if (warp == kBwdMma) {
+        const uint64_t q_a = smem_desc_sw128(sbase + L::offFixA, 16, 1024);         // Q
+        const uint64_t do_a = smem_desc_sw128(sbase + L::offFixB, 16, 1024);        // dO
+        const uint64_t ring_k = smem_desc_sw128(sbase + L::offRing, 16, 1024);      // K / V, K-major
+        const uint64_t ring_mn = smem_desc_sw128(sbase + L::offRing, kSlab, 1024);  // K, MN-major
+        auto so = [](int m) { return (uint64_t)(((m % kRingQ) * L::kTile) >> 4); };
+        auto full = [&](int m) { return wait_phase_warp(&bars[FULL + m % kRingQ], (m / kRingQ) & 1, sh); };
+        auto issue_s = [&](int n) {  // S(n) = Q K_n^T into buffer n % 2
+            mma_kmajor<D>(sbuf(n), q_a, ring_k + so(2 * n));
+            mma_commit_warp(&bars[S_FULL + (n & 1)]);
+        };
+        auto issue_dp = [&](int n) {  // dP(n) = dO V_n^T; V_n is not read after this
+            mma_kmajor<D>(tmem + 128u, do_a, ring_k + so(2 * n + 1));
+            mma_commit_warp(&bars[DP_FULL]);
+            mma_commit_warp(&bars[EMPTY + (2 * n + 1) % kRingQ]);
+        };
+        bool ok = wait_phase_warp(&bars[FIX], 0, sh) && full(0);
+        if (ok) {
+            tc_fence_after();
+            issue_s(0);
+            ok = full(1);
+        }
+        if (ok) {
+            tc_fence_after();
+            issue_dp(0);
+            if (n_steps > 1) {
+                ok = full(2);
+                if (ok) {
+                    tc_fence_after();
+                    issue_s(1);
+                }
+            }
+        }
+        for (int n = 0; n < n_steps && ok; ++n) {
+            ok = wait_phase_warp(&bars[DS_READY], n & 1, sh);
+            if (!ok) break;
+            tc_fence_after();
+            mma_acc_tmemA<D>(tmem + 256u, sbuf(n), ring_mn + so(2 * n), n > 0);  // dQ += dS K
+            mma_commit_warp(&bars[EMPTY + (2 * n) % kRingQ]);
+            if (n + 1 < n_steps) {  // the row warps have read dP(n)
+                ok = full(2 * n + 3);
+                if (!ok) break;
+                tc_fence_after();
+                issue_dp(n + 1);
+            }
+            if (n + 2 < n_steps) {  // buffer n % 2: dS(n) is read by the product issued above
+                ok = full(2 * n + 4);
+                if (!ok) break;
+                tc_fence_after();
+                issue_s(n + 2);
+            }
+        }
+        mma_commit_warp(&bars[FINAL]);
+        drain_phase(&bars[FINAL], 0);
+    } else {
+        // row warps: thread = query row, warp half = 64 key columns
+        const int sub = warp & 3, half = warp >> 2;
+        const int row = sub * 32 + lane, qrow = q0 + row;
+        const uint32_t lane_off = (uint32_t)(sub * 32) << 16;
+        const size_t vi = ((size_t)bb * p.hq + hh) * p.s_pad + qrow;  // qrow < s_pad always
+        const float neg_l = -p.lse2[rank][vi];
+        const float neg_d = -p.dsum[rank][vi];
+        const float sc = p.scale_log2;
+        const int lim = p.causal ? min(p.s, qrow + 1) : p.s;  // keys < lim are visible
+        bool ok = true;
+        for (int n = 0; n < n_steps; ++n) {
+            const uint32_t tS = sbuf(n) + lane_off + half * 64;
+            const uint32_t tdP = tmem + 128u + lane_off + half * 64;
+            const int kb = n * 128 + half * 64;  // first key column of this warp
+            // masked: the causal diagonal tile, and keys past the end (zero rows; kept out of
+            // the product so that no inf/nan can reach it)
+            const bool mask = (p.causal && n == qt) || kb + 64 > p.s;
+            float pf[64];
+            ok = wait_phase_warp(&bars[S_FULL + (n & 1)], (n >> 1) & 1, sh);
+            if (!ok) break;
+            tc_fence_after();
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                uint32_t sv[32];
+                tmem_ld32(tS + c * 32, sv);
+                tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 32; e += 2) {
+                    float a0, a1;
+                    ffma2(a0, a1, __uint_as_float(sv[e]), __uint_as_float(sv[e + 1]), sc, sc, neg_l, neg_l);
+                    float p0 = ex2_approx(a0), p1 = ex2_approx(a1);
+                    if (mask) {
+                        const int key = kb + c * 32 + e;
+                        p0 = key < lim ? p0 : 0.f;
+                        p1 = key + 1 < lim ? p1 : 0.f;
+                    }
+                    pf[c * 32 + e] = p0;
+                    pf[c * 32 + e + 1] = p1;
+                }
+            }
+            ok = wait_phase_warp(&bars[DP_FULL], n & 1, sh);
+            if (!ok) break;
+            tc_fence_after();
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                uint32_t dv[32];
+                tmem_ld32(tdP + c * 32, dv);
+                tmem_wait_ld();
+                uint32_t pk[16];
+#pragma unroll
+                for (int e = 0; e < 32; e += 2) {
+                    float t0, t1;
+                    fadd2(t0, t1, __uint_as_float(dv[e]), __uint_as_float(dv[e + 1]), neg_d, neg_d);
+                    pk[e >> 1] = pack_bf16x2(pf[c * 32 + e] * t0, pf[c * 32 + e + 1] * t1);
+                }
+                tmem_st16(tS + c * 16, pk);  // dS over S columns this warp has already read
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[DS_READY]);
+        }
+        if (ok) ok = wait_phase_warp(&bars[FINAL], 0, sh);
+        if (ok) {
+            tc_fence_after();
+            const bool qok = qrow < p.s;
+            const size_t off = (((size_t)bb * p.s + (qok ? qrow : 0)) * p.hq + hh) * (size_t)D * 2 + half * D;
+            store_row_bf16<D / 2>(tmem + 256u + lane_off + half * (D / 2), p.dq[rank] + off, p.scale, qok);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kBwdMma) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// ------------------------------------------------------------------ host side
+template <int D>
+cudaError_t launch_bwd_d(const BwdParams& prm, int nranks, cudaStream_t stream) {
+    using LK = BwdSmem<D, kRingKV, true>;
+    using LQ = BwdSmem<D, kRingQ, false>;
+    cudaError_t e =
+        cudaFuncSetAttribute(bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)LK::kAlloc);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)LQ::kAlloc);
+    if (e != cudaSuccess) return e;
+    const long long gk = (long long)nranks * prm.b * prm.hkv * prm.n_tiles;
+    const long long gq = (long long)nranks * prm.b * prm.hq * prm.n_tiles;
+    bwd_dkdv_kernel<D><<<(unsigned)gk, kBwdThreads, LK::kAlloc, stream>>>(prm);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    bwd_dq_kernel<D><<<(unsigned)gq, kBwdThreads, LQ::kAlloc, stream>>>(prm);
+    return cudaGetLastError();
+}

@@ -67,6 +67,7 @@ struct TcParams {
     CUtensorMap mk[kMaxMaps];
     CUtensorMap mv[kMaxMaps];
     uint8_t* optr[kMaxMaps];  // output buffers (same indexing as the maps): [b][rows][heads][d] bf16
+    float* lse[kMaxMaps];     // optional per-row log-sum-exp (natural log), [b][heads][rows]; unfused only
     int s;             // sequence length
     int rows_per_map;  // tokens held by one map: s/P when fused, s otherwise
     int n_qtiles;      // ceil(s / BM)
@@ -514,6 +515,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
                     if (row_ok) *reinterpret_cast<uint4*>(orow + (c * 32 + q4 * 8) * 2) = v;
                 }
             }
+            if (p.lse[oc.map] && row_ok)  // log-sum-exp of the scaled scores, natural log
+                p.lse[oc.map][((size_t)it.bb * p.heads + it.head) * p.rows_per_map + oc.row + row] =
+                    (m_ref + log2f(l_sum)) * 0.6931471805599453f;
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars[B_O_EMPTY + t]);
@@ -578,6 +582,8 @@ cudaError_t launch_d(TcParams& prm, long long n_items, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
+#include "attn_bwd.cuh"
+
 }  // namespace
 
 int tc_attention_supported(int d) { return d == 64 || d == 128; }
@@ -585,7 +591,8 @@ int tc_attention_supported(int d) { return d == 64 || d == 128; }
 cudaError_t launch_attention_tc(int P, int b, int s, int h_q, int h_kv, int d, int causal, int fused,
                                 const AttnPtrs& ptrs, cudaStream_t stream, int* unsupported) {
     *unsupported = 0;
-    if (!tc_attention_supported(d) || (fused && (P > kMaxMaps || (s / P) % BM != 0))) {
+    const bool want_lse = ptrs.lse[0] != nullptr;
+    if (!tc_attention_supported(d) || (fused && (P > kMaxMaps || (s / P) % BM != 0 || want_lse))) {
         *unsupported = 1;
         return cudaSuccess;
     }
@@ -629,11 +636,81 @@ cudaError_t launch_attention_tc(int P, int b, int s, int h_q, int h_kv, int d, i
                     !make_map(&prm->mv[i], ptrs.v[r], b, s, Hk, d, BN))
                     err = cudaErrorInvalidValue;
                 prm->optr[i] = static_cast<uint8_t*>(ptrs.o[r]);
+                prm->lse[i] = want_lse ? ptrs.lse[r] : nullptr;
             }
             if (err != cudaSuccess) break;
             const long long n_items = (long long)nr * b * Hq * prm->n_pairs;
             err = d == 64 ? launch_d<64>(*prm, n_items, stream) : launch_d<128>(*prm, n_items, stream);
         }
+    }
+    delete prm;
+    return err;
+}
+
+cudaError_t launch_attention_bwd_tc(int P, int b, int s, int h_q, int h_kv, int d, int causal, int od_seq_layout,
+                                    const BwdPtrs& ptrs, cudaStream_t stream, int* unsupported) {
+    *unsupported = 0;
+    if (!tc_attention_supported(d)) {
+        *unsupported = 1;
+        return cudaSuccess;
+    }
+    const int Hq = h_q / P, Hk = h_kv / P;
+    const int n_tiles = (s + 127) / 128;
+    // (1) row sums D and base-2 log-sum-exp, all ranks in one grid
+    PrepParams* pp = new PrepParams;
+    memset(pp, 0, sizeof(PrepParams));
+    for (int r = 0; r < P; ++r) {
+        pp->o[r] = static_cast<const uint8_t*>(ptrs.o_rows[r]);
+        pp->dout[r] = static_cast<const uint8_t*>(ptrs.do_rows[r]);
+        pp->lse[r] = ptrs.lse[r];
+        pp->lse2[r] = ptrs.lse2[r];
+        pp->dsum[r] = ptrs.dsum[r];
+    }
+    pp->b = b;
+    pp->s = s;
+    pp->s_pad = n_tiles * 128;
+    pp->Hq = Hq;
+    pp->d = d;
+    pp->S = s / P;
+    pp->hq_total = h_q;
+    pp->seq_layout = od_seq_layout ? 1 : 0;
+    pp->lanes_log2 = d == 64 ? 3 : 4;
+    pp->rows = (long long)P * b * Hq * pp->s_pad;
+    const long long threads = pp->rows << pp->lanes_log2;
+    bwd_prep_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, stream>>>(*pp);
+    delete pp;
+    cudaError_t err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+    // (2) dK/dV and dQ, up to kMaxMaps ranks per launch pair
+    BwdParams* prm = new BwdParams;
+    memset(prm, 0, sizeof(BwdParams));
+    prm->s = s;
+    prm->s_pad = n_tiles * 128;
+    prm->n_tiles = n_tiles;
+    prm->hq = Hq;
+    prm->hkv = Hk;
+    prm->g = Hq / Hk;
+    prm->b = b;
+    prm->causal = causal ? 1 : 0;
+    prm->scale = (float)(1.0 / std::sqrt((double)d));
+    prm->scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)d));
+    for (int r0 = 0; r0 < P && err == cudaSuccess; r0 += kMaxMaps) {
+        const int nr = (P - r0) < kMaxMaps ? (P - r0) : kMaxMaps;
+        for (int i = 0; i < nr && err == cudaSuccess; ++i) {
+            const int r = r0 + i;
+            if (!make_map(&prm->mq[i], ptrs.q[r], b, s, Hq, d, 128) ||
+                !make_map(&prm->mk[i], ptrs.k[r], b, s, Hk, d, 128) ||
+                !make_map(&prm->mv[i], ptrs.v[r], b, s, Hk, d, 128) ||
+                !make_map(&prm->mdo[i], ptrs.dout[r], b, s, Hq, d, 128))
+                err = cudaErrorInvalidValue;
+            prm->dq[i] = static_cast<uint8_t*>(ptrs.dq[r]);
+            prm->dk[i] = static_cast<uint8_t*>(ptrs.dk[r]);
+            prm->dv[i] = static_cast<uint8_t*>(ptrs.dv[r]);
+            prm->lse2[i] = ptrs.lse2[r];
+            prm->dsum[i] = ptrs.dsum[r];
+        }
+        if (err != cudaSuccess) break;
+        err = d == 64 ? launch_bwd_d<64>(*prm, nr, stream) : launch_bwd_d<128>(*prm, nr, stream);
     }
     delete prm;
     return err;

@@ -19,7 +19,7 @@ struct PermuteTensor {
     int h;  // heads of this tensor in seq layout (h_q for Q/O, h_kv for K/V)
 };
 
-// direction: 0 = seq -> head (all-to-all #1), 1 = head -> seq (all-to-all #2).
+// direction: 0 = seq -> head (all-to-all #1), 1 = head -> seq (all-to-all #2); 1 to 4 tensors.
 cudaError_t launch_permute(int direction, int P, int b, int s, int d, int elem_bytes, const PermuteTensor* tensors,
                            int ntensors, cudaStream_t stream);
 
@@ -29,6 +29,7 @@ struct AttnPtrs {
     const void* k[kMaxRanks];
     const void* v[kMaxRanks];
     void* o[kMaxRanks];
+    float* lse[kMaxRanks];  // optional (all null = none): per-row log-sum-exp, [b][h_q/P][s] fp32
 };
 
 // Head-layout local attention, fp32 in/out, all P ranks in one grid.
@@ -41,6 +42,26 @@ cudaError_t launch_attention_fp32(int P, int b, int s, int h_q, int h_kv, int d,
 int tc_attention_supported(int d);
 cudaError_t launch_attention_tc(int P, int b, int s, int h_q, int h_kv, int d, int causal, int fused,
                                 const AttnPtrs& ptrs, cudaStream_t stream, int* unsupported);
+
+// Backward of the bf16 tensor-core attention (head layout per rank).  O and dO for the
+// row sums D are read from `o_rows` / `do_rows` in head layout, or in seq layout when
+// od_seq_layout != 0 (then indexed by seq rank j, not by head rank r).
+struct BwdPtrs {
+    const void* q[kMaxRanks];
+    const void* k[kMaxRanks];
+    const void* v[kMaxRanks];
+    const void* dout[kMaxRanks];
+    const void* o_rows[kMaxRanks];
+    const void* do_rows[kMaxRanks];
+    const float* lse[kMaxRanks];  // [b][h_q/P][s], natural log, from the forward
+    void* dq[kMaxRanks];
+    void* dk[kMaxRanks];
+    void* dv[kMaxRanks];
+    float* lse2[kMaxRanks];       // scratch [b][h_q/P][s_pad], s_pad = ceil(s/128)*128
+    float* dsum[kMaxRanks];       // scratch, same shape
+};
+cudaError_t launch_attention_bwd_tc(int P, int b, int s, int h_q, int h_kv, int d, int causal, int od_seq_layout,
+                                    const BwdPtrs& ptrs, cudaStream_t stream, int* unsupported);
 
 // Device error word of the tensor-core kernels (bounded waits that gave up).
 cudaError_t read_device_error(unsigned int* value, int clear);

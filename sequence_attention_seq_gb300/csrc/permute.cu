@@ -29,7 +29,7 @@ struct PermuteJob {
 };
 
 struct PermuteParams {
-    PermuteJob job[3];
+    PermuteJob job[4];
     uint32_t ntensors;
     uint32_t units;  // P*P*b slabs per tensor
     uint32_t P, S, s;
@@ -123,6 +123,14 @@ cudaError_t launch_vec(int direction, const PermuteParams& prm, uint32_t max_sla
 
 cudaError_t launch_permute(int direction, int P, int b, int s, int d, int elem_bytes, const PermuteTensor* tensors,
                            int ntensors, cudaStream_t stream) {
+    if (ntensors < 1 || ntensors > 4) return cudaErrorInvalidValue;
+    if ((uint64_t)ntensors * P * P * b > 0xffffffffull) {  // one launch per tensor keeps the slab index in 32 bits
+        for (int t = 0; t < ntensors; ++t) {
+            const cudaError_t e = launch_permute(direction, P, b, s, d, elem_bytes, tensors + t, 1, stream);
+            if (e != cudaSuccess) return e;
+        }
+        return cudaSuccess;
+    }
     PermuteParams prm;
     memset(&prm, 0, sizeof(prm));
     prm.ntensors = (uint32_t)ntensors;

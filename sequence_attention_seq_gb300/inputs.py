@@ -14,6 +14,8 @@ Conventions (the pages fix no generator, so these are this library's choice):
   RNG speed.
 * Uniform random bits (permute-only workloads): ``torch.randint`` over the full
   16-bit (or 32-bit) range, reinterpreted as the element type.
+* Output gradients (backward): ``torch.randn`` in float32 for the global dO
+  ``[b, s, h_q, d]`` from a generator of its own, then the same cast.
 * Sequence sharding (the input layout of DistributedAttention): rank ``j`` holds the
   contiguous token block ``[j*s/P, (j+1)*s/P)`` of every batch row, all heads.
 """
@@ -21,7 +23,7 @@ from __future__ import annotations
 
 import torch
 
-__all__ = ["global_qkv", "shard_seq", "random_bits", "seq_shards_qkv", "empty_like_shards"]
+__all__ = ["global_qkv", "global_grad", "shard_seq", "random_bits", "seq_shards_qkv", "empty_like_shards"]
 
 
 def global_qkv(b, s, h_q, h_kv, d, dtype=torch.bfloat16, seed=0, device="cpu"):
@@ -32,6 +34,14 @@ def global_qkv(b, s, h_q, h_kv, d, dtype=torch.bfloat16, seed=0, device="cpu"):
     k = torch.randn((b, s, h_kv, d), generator=g, dtype=torch.float32, device=device)
     v = torch.randn((b, s, h_kv, d), generator=g, dtype=torch.float32, device=device)
     return q.to(dtype), k.to(dtype), v.to(dtype)
+
+
+def global_grad(b, s, h_q, d, dtype=torch.bfloat16, seed=0, device="cpu"):
+    """Return a global output gradient dO [b,s,h_q,d] drawn N(0,1) (its own generator and
+    seed, so it does not disturb the Q/K/V stream)."""
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    return torch.randn((b, s, h_q, d), generator=g, dtype=torch.float32, device=device).to(dtype)
 
 
 def shard_seq(x, P):

@@ -28,6 +28,26 @@ def assert_close(got, ref, dtype, what=""):
     return err.max().item(), err.mean().item()
 
 
+# Gradients (bf16 I/O): every element within 1.5e-2 + 2^-7 |ref|, mean-abs <= 2e-3.  The
+# absolute part is the output tolerance; the relative part covers the final rounding to
+# bf16 (at most 2^-8 |ref|) plus the bf16 rounding of the P and dS operands of the tile
+# products (at most 2^-8 of each term), which matter once gradients exceed 1 in magnitude.
+GRAD_ATOL, GRAD_RTOL, GRAD_MEAN = 1.5e-2, 2.0 ** -7, 2e-3
+
+
+def assert_close_grad(got, ref, what=""):
+    g = got.detach().to("cpu", torch.float64)
+    r = ref.to(torch.float64)
+    assert g.shape == r.shape, (g.shape, r.shape)
+    assert torch.isfinite(g).all(), f"{what}: non-finite gradient"
+    err = (g - r).abs()
+    bound = GRAD_ATOL + GRAD_RTOL * r.abs()
+    worst = (err / bound).max().item()
+    assert worst <= 1.0, f"{what}: error {err.max().item():.3e} exceeds the bound (ratio {worst:.2f})"
+    assert err.mean().item() <= GRAD_MEAN, f"{what}: mean-abs {err.mean().item():.3e} > {GRAD_MEAN}"
+    return err.max().item(), err.mean().item()
+
+
 def bits_equal(a, b):
     return torch.equal(a.contiguous().view(torch.uint8), b.contiguous().view(torch.uint8))
 

@@ -1,0 +1,198 @@
+"""Training path on the GPU: the forward's log-sum-exp, the local attention backward and
+the whole Ulysses backward against the fp64 oracle ("02 · DeepSpeed-Ulysses", section 5),
+plus bit-for-bit agreements that need no oracle (repeat calls, the seq-layout and
+head-layout routes to the same gradients)."""
+import pytest
+import torch
+
+import oracle
+import sequence_attention_seq_gb300 as uly
+from gpu_util import assert_close_grad, bits_equal, device_ok, need_gpu
+from sequence_attention_seq_gb300.inputs import global_grad, global_qkv, shard_seq
+
+pytestmark = pytest.mark.gpu
+
+LOCAL_CASES = [
+    # P, b, s, hq, hkv, d, causal
+    (1, 1, 128, 1, 1, 128, False),   # one tile
+    (1, 1, 128, 1, 1, 128, True),
+    (1, 1, 256, 2, 2, 64, True),
+    (2, 1, 384, 4, 4, 128, False),   # several tiles
+    (2, 1, 384, 4, 4, 128, True),
+    (2, 2, 320, 4, 2, 64, True),     # ragged tail, grouped K/V
+    (2, 2, 320, 4, 2, 64, False),
+    (4, 1, 512, 16, 4, 128, True),   # 4 query heads per K/V head
+    (1, 1, 1, 1, 1, 64, False),      # one token
+    (1, 1, 77, 2, 1, 128, True),     # one ragged tile
+    (2, 1, 1000, 2, 2, 128, True),   # ragged, several tiles
+    (3, 1, 771, 3, 3, 64, False),
+]
+
+
+def _head_inputs(P, b, s, hq, hkv, d, seed):
+    q, k, v = global_qkv(b, s, hq, hkv, d, torch.bfloat16, seed=seed)
+    do = global_grad(b, s, hq, d, torch.bfloat16, seed=seed + 1)
+    sh = [oracle.seq2head(shard_seq(x, P)) for x in (q, k, v, do)]
+    return sh  # [q_head, k_head, v_head, do_head], each P CPU tensors
+
+
+def _cuda(xs):
+    return [x.cuda() for x in xs]
+
+
+@pytest.mark.parametrize("P,b,s,hq,hkv,d,causal", LOCAL_CASES[:8])
+def test_forward_lse(P, b, s, hq, hkv, d, causal):
+    """The forward with statistics gives the plain forward's output bits, and L within
+    2e-4 of the oracle's (fp32 sum of ex2 values, then one log)."""
+    need_gpu()
+    qh, kh, vh, _ = _head_inputs(P, b, s, hq, hkv, d, seed=s + d)
+    o_plain = uly.ulysses_local_attention(_cuda(qh), _cuda(kh), _cuda(vh), causal)
+    o, lse = uly.ulysses_local_attention_fwd_lse(_cuda(qh), _cuda(kh), _cuda(vh), causal)
+    torch.cuda.synchronize()
+    device_ok()
+    for r in range(P):
+        assert bits_equal(o[r], o_plain[r]), f"rank {r}: output changed by the statistics store"
+        want = oracle.attention_lse(qh[r], kh[r], causal)
+        err = (lse[r].cpu().double() - want).abs().max().item()
+        assert err <= 2e-4, f"rank {r}: lse max-abs {err:.3e}"
+
+
+@pytest.mark.parametrize("P,b,s,hq,hkv,d,causal", LOCAL_CASES)
+def test_local_backward(P, b, s, hq, hkv, d, causal):
+    need_gpu()
+    qh, kh, vh, doh = _head_inputs(P, b, s, hq, hkv, d, seed=3 * s + d)
+    q, k, v, do = _cuda(qh), _cuda(kh), _cuda(vh), _cuda(doh)
+    o, lse = uly.ulysses_local_attention_fwd_lse(q, k, v, causal)
+    dq, dk, dv = uly.ulysses_local_attention_bwd(q, k, v, o, do, lse, causal)
+    torch.cuda.synchronize()
+    device_ok()
+    for r in range(P):
+        wq, wk, wv = oracle.attention_bwd(qh[r], kh[r], vh[r], doh[r], causal)
+        assert_close_grad(dq[r], wq, f"dq rank {r}")
+        assert_close_grad(dk[r], wk, f"dk rank {r}")
+        assert_close_grad(dv[r], wv, f"dv rank {r}")
+
+
+def _assert_normwise(got, ref, what):
+    """Norm-wise bound for the stress inputs below: max error <= 2^-6 max|ref| and mean error
+    <= 2^-8 mean|ref|.  With keys up to 4x a unit normal, the softmax saturates and dS = P (dP - D)
+    is a small difference of large terms, so its bf16 rounding and the bf16 rounding of the
+    output O that D is formed from show up relative to the size of the terms (of the order of
+    the largest gradient), not to each element."""
+    g = got.detach().to("cpu", torch.float64)
+    r = ref.to(torch.float64)
+    assert torch.isfinite(g).all(), f"{what}: non-finite gradient"
+    err = (g - r).abs()
+    assert err.max().item() <= 2.0 ** -6 * r.abs().max().item(), f"{what}: max-abs {err.max().item():.3e}"
+    assert err.mean().item() <= 2.0 ** -8 * r.abs().mean().item(), f"{what}: mean-abs {err.mean().item():.3e}"
+
+
+def test_backward_score_spike():
+    """Scores that grow along the key axis (and a saturated softmax) keep P = exp(S - L) <= 1."""
+    need_gpu()
+    s, d = 640, 128
+    g = torch.Generator().manual_seed(5)
+    q = torch.randn(1, s, 1, d, generator=g)
+    k = torch.randn(1, s, 1, d, generator=g) * torch.linspace(0.2, 4.0, s).view(1, s, 1, 1)
+    v = torch.randn(1, s, 1, d, generator=g)
+    do = torch.randn(1, s, 1, d, generator=g)
+    q, k, v, do = q.bfloat16(), k.bfloat16(), v.bfloat16(), do.bfloat16()
+    for causal in (False, True):
+        o, lse = uly.ulysses_local_attention_fwd_lse([q.cuda()], [k.cuda()], [v.cuda()], causal)
+        dq, dk, dv = uly.ulysses_local_attention_bwd([q.cuda()], [k.cuda()], [v.cuda()], o, [do.cuda()], lse, causal)
+        torch.cuda.synchronize()
+        wq, wk, wv = oracle.attention_bwd(q, k, v, do, causal)
+        _assert_normwise(dq[0], wq, f"dq causal={causal}")
+        _assert_normwise(dk[0], wk, f"dk causal={causal}")
+        _assert_normwise(dv[0], wv, f"dv causal={causal}")
+    device_ok()
+
+
+DIST_CASES = [
+    (2, 1, 256, 4, 2, 64, True),
+    (4, 2, 512, 8, 8, 128, False),
+    (4, 1, 512, 8, 8, 128, True),
+    (8, 1, 1024, 16, 8, 128, True),
+    (2, 1, 200, 4, 4, 128, True),     # ragged: s/P not a tile multiple
+    (1, 1, 384, 2, 1, 128, True),     # P = 1
+]
+
+
+@pytest.mark.parametrize("P,b,s,hq,hkv,d,causal", DIST_CASES)
+def test_dist_backward(P, b, s, hq, hkv, d, causal):
+    need_gpu()
+    q, k, v = global_qkv(b, s, hq, hkv, d, torch.bfloat16, seed=P * 7 + s)
+    do = global_grad(b, s, hq, d, torch.bfloat16, seed=P * 7 + s + 1)
+    qs, ks, vs, dos = (shard_seq(x, P) for x in (q, k, v, do))
+    qd, kd, vd, dod = _cuda(qs), _cuda(ks), _cuda(vs), _cuda(dos)
+    o, lse = uly.ulysses_dist_attn_fwd_lse(qd, kd, vd, causal)
+    o_plain = uly.ulysses_dist_attn_fwd(qd, kd, vd, causal, fused=False)
+    dq, dk, dv = uly.ulysses_dist_attn_bwd(qd, kd, vd, o, dod, lse, causal)
+    torch.cuda.synchronize()
+    device_ok()
+    wq, wk, wv = oracle.dist_attn_bwd(qs, ks, vs, dos, causal)
+    for j in range(P):
+        assert bits_equal(o[j], o_plain[j]), f"rank {j}: forward output changed by the statistics store"
+        assert_close_grad(dq[j], wq[j], f"dq rank {j}")
+        assert_close_grad(dk[j], wk[j], f"dk rank {j}")
+        assert_close_grad(dv[j], wv[j], f"dv rank {j}")
+
+
+def test_dist_backward_equals_head_layout_route():
+    """The distributed backward (D from the seq-layout O and dO) gives the same bits as the
+    exchanges done one by one around the head-layout backward (D from head layout)."""
+    need_gpu()
+    P, b, s, hq, hkv, d, causal = 4, 1, 640, 8, 4, 128, True
+    q, k, v = global_qkv(b, s, hq, hkv, d, torch.bfloat16, seed=99)
+    do = global_grad(b, s, hq, d, torch.bfloat16, seed=100)
+    qd, kd, vd, dod = (_cuda(shard_seq(x, P)) for x in (q, k, v, do))
+    o, lse = uly.ulysses_dist_attn_fwd_lse(qd, kd, vd, causal)
+    dq, dk, dv = uly.ulysses_dist_attn_bwd(qd, kd, vd, o, dod, lse, causal)
+    qh, kh, vh, oh, doh = (uly.ulysses_a2a_seq2head(x) for x in (qd, kd, vd, o, dod))
+    gq, gk, gv = uly.ulysses_local_attention_bwd(qh, kh, vh, oh, doh, lse, causal)
+    rq, rk, rv = (uly.ulysses_a2a_head2seq(x) for x in (gq, gk, gv))
+    torch.cuda.synchronize()
+    device_ok()
+    for j in range(P):
+        assert bits_equal(dq[j], rq[j]) and bits_equal(dk[j], rk[j]) and bits_equal(dv[j], rv[j]), f"rank {j}"
+
+
+def test_backward_repeat_calls_are_deterministic():
+    need_gpu()
+    P, b, s, hq, hkv, d, causal = 2, 1, 1024, 8, 2, 128, True
+    q, k, v = global_qkv(b, s, hq, hkv, d, torch.bfloat16, seed=7)
+    do = global_grad(b, s, hq, d, torch.bfloat16, seed=8)
+    qd, kd, vd, dod = (_cuda(shard_seq(x, P)) for x in (q, k, v, do))
+    o, lse = uly.ulysses_dist_attn_fwd_lse(qd, kd, vd, causal)
+    a = uly.ulysses_dist_attn_bwd(qd, kd, vd, o, dod, lse, causal)
+    b2 = uly.ulysses_dist_attn_bwd(qd, kd, vd, o, dod, lse, causal)
+    torch.cuda.synchronize()
+    device_ok()
+    for x, y in zip(a, b2):
+        for j in range(P):
+            assert bits_equal(x[j], y[j])
+
+
+def test_backward_argument_errors():
+    need_gpu()
+    P, b, s, hq, hkv, d = 2, 1, 256, 4, 2, 128
+    q, k, v = global_qkv(b, s, hq, hkv, d, torch.bfloat16, seed=1)
+    qd, kd, vd = (_cuda(shard_seq(x, P)) for x in (q, k, v))
+    o, lse = uly.ulysses_dist_attn_fwd_lse(qd, kd, vd, True)
+    # fp32 has no backward kernel
+    with pytest.raises(uly.UlyssesError) as e:
+        uly.ulysses_dist_attn_bwd([x.float() for x in qd], [x.float() for x in kd], [x.float() for x in vd],
+                                  [x.float() for x in o], [x.float() for x in o], lse, True)
+    assert e.value.status == 2
+    # output aliasing an input
+    with pytest.raises(uly.UlyssesError) as e:
+        uly.ulysses_dist_attn_bwd(qd, kd, vd, o, o, lse, True, grads=(qd, [torch.empty_like(x) for x in kd],
+                                                                        [torch.empty_like(x) for x in vd]))
+    assert e.value.status == 1
+    # workspace too small
+    with pytest.raises(uly.UlyssesError) as e:
+        uly.ulysses_dist_attn_bwd(qd, kd, vd, o, o, lse, True,
+                                  workspace=torch.empty(256, dtype=torch.uint8, device="cuda"))
+    assert e.value.status == 1
+    torch.cuda.synchronize()
+    device_ok()
