@@ -395,6 +395,126 @@ def run_permute_sweep(args):
                       "all_bit_exact": all(r["round_trip_bit_exact"] for r in rows)}))
 
 
+def run_backward(args):
+    """Backward of the Ulysses attention (not part of the default line): per mask, the local
+    backward alone (row statistics + dK/dV + dQ kernels, head layout) and the whole
+    distributed backward (exchange of Q, K, V, dO; local backward; exchange of dQ, dK, dV),
+    each call bracketed by CUDA events.  FLOP/s count the algorithmic 2.5x forward FLOPs
+    (the five tile products S, dP, dV, dK, dQ); the kernels execute 3.5x (S and dP twice)."""
+    import torch
+
+    import sequence_attention_seq_gb300 as uly
+    from sequence_attention_seq_gb300 import build as uly_build
+    from sequence_attention_seq_gb300.inputs import global_grad, seq_shards_qkv, shard_seq
+
+    uly_build.build()
+    w = WORKLOADS[args.workload]
+    P, b, s, hq, hkv, d = w["P"], w["b"], w["s"], w["h_q"], w["h_kv"], w["d"]
+    if w["dtype"] != "bf16":
+        raise SystemExit("the backward kernels are bf16 only")
+    dev = torch.device("cuda", 0)
+    qs, ks, vs = seq_shards_qkv(P, b, s, hq, hkv, d, torch.bfloat16, seed=0, device="cuda")
+    dos = shard_seq(global_grad(b, s, hq, d, torch.bfloat16, seed=1, device="cuda"), P)
+    qh, kh, vh, doh = (uly.ulysses_a2a_seq2head(x) for x in (qs, ks, vs, dos))
+    peaks, peak_src = load_peaks()
+    clocks = ClockSampler(0)
+    rows = {}
+    clocks.start()
+    time.sleep(0.3)
+    for causal in w["masks"]:
+        tag = "causal" if causal else "noncausal"
+        o, lse = uly.ulysses_dist_attn_fwd_lse(qs, ks, vs, causal)
+        oh = uly.ulysses_a2a_seq2head(o)
+        grads_h = ([torch.empty_like(x) for x in qh], [torch.empty_like(x) for x in kh],
+                   [torch.empty_like(x) for x in vh])
+        grads_s = ([torch.empty_like(x) for x in qs], [torch.empty_like(x) for x in ks],
+                   [torch.empty_like(x) for x in vs])
+        ws_l = torch.empty(uly.ulysses_attn_bwd_workspace_bytes(P, b, s, hq, hkv, d, torch.bfloat16, False),
+                           dtype=torch.uint8, device=dev)
+        ws_d = torch.empty(uly.ulysses_attn_bwd_workspace_bytes(P, b, s, hq, hkv, d, torch.bfloat16, True),
+                           dtype=torch.uint8, device=dev)
+        calls = {
+            "local_bwd": lambda: uly.ulysses_local_attention_bwd(qh, kh, vh, oh, doh, lse, causal, grads=grads_h,
+                                                                 workspace=ws_l),
+            "dist_bwd": lambda: uly.ulysses_dist_attn_bwd(qs, ks, vs, o, dos, lse, causal, grads=grads_s,
+                                                          workspace=ws_d),
+        }
+        fl = 2.5 * attn_flops(b, s, hq, d, causal)
+        for name, fn in calls.items():
+            for _ in range(max(3, args.warmup)):
+                fn()
+            torch.cuda.synchronize()
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(args.steps)]
+            for e0, e1 in evs:
+                e0.record()
+                fn()
+                e1.record()
+            torch.cuda.synchronize()
+            ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in evs)
+            rows[f"{name}_{tag}"] = {"ms": ms, "tflops": fl / (ms * 1e-3) / 1e12,
+                                     "frac": fl / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"]}
+        if uly.ulysses_device_status(clear=True) != 0:
+            raise RuntimeError("a kernel's bounded wait gave up")
+    clk = clocks.stop()
+    print(json.dumps({"metric": "Ulysses attn bwd TFLOP/s (algorithmic: 2.5x forward FLOPs)", "unit": "TFLOP/s",
+                      "workload": w["name"], "steps": args.steps, "peak": peaks["bf16_tflops"],
+                      "peak_source": f"{peak_src} (bf16 dense, burst)", "results": rows, "clocks": clk}))
+
+
+def run_overlap(args):
+    """The unfused forward against the overlapped one (n_chunks head groups, exchanges on a
+    side stream), per mask, each call bracketed by CUDA events on the main stream."""
+    import torch
+
+    import sequence_attention_seq_gb300 as uly
+    from sequence_attention_seq_gb300 import build as uly_build
+    from sequence_attention_seq_gb300.inputs import seq_shards_qkv
+
+    uly_build.build()
+    w = WORKLOADS[args.workload]
+    P, b, s, hq, hkv, d = w["P"], w["b"], w["s"], w["h_q"], w["h_kv"], w["d"]
+    dt = torch.bfloat16 if w["dtype"] == "bf16" else torch.float32
+    qs, ks, vs = seq_shards_qkv(P, b, s, hq, hkv, d, dt, seed=0, device="cuda")
+    out = [torch.empty_like(q) for q in qs]
+    ws = torch.empty(max(1, uly.ulysses_dist_attn_workspace_bytes(P, b, s, hq, hkv, d, dt, False)),
+                     dtype=torch.uint8, device="cuda")
+    chunks = [c for c in (2, 4, 8) if (hkv // P) % c == 0]
+    wso = {c: torch.empty(uly.ulysses_dist_attn_overlap_workspace_bytes(P, b, s, hq, hkv, d, dt, c),
+                          dtype=torch.uint8, device="cuda") for c in chunks}
+    rows = {}
+    clocks = ClockSampler(0)
+    clocks.start()
+    time.sleep(0.3)
+    for causal in w["masks"]:
+        tag = "causal" if causal else "noncausal"
+        fl = attn_flops(b, s, hq, d, causal)
+        calls = {"unfused": lambda: uly.ulysses_dist_attn_fwd(qs, ks, vs, causal, fused=False, out_seq=out,
+                                                              workspace=ws)}
+        for c in chunks:
+            calls[f"overlap_{c}"] = (lambda c=c: uly.ulysses_dist_attn_fwd_overlap(qs, ks, vs, causal, n_chunks=c,
+                                                                                  out_seq=out, workspace=wso[c]))
+        for name, fn in calls.items():
+            for _ in range(max(3, args.warmup)):
+                fn()
+            torch.cuda.synchronize()
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(args.steps)]
+            for e0, e1 in evs:
+                e0.record()
+                fn()
+                e1.record()
+            torch.cuda.synchronize()
+            ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in evs)
+            rows[f"{name}_{tag}"] = {"ms": ms, "tflops": fl / (ms * 1e-3) / 1e12}
+    if uly.ulysses_device_status(clear=True) != 0:
+        raise RuntimeError("a kernel's bounded wait gave up")
+    clk = clocks.stop()
+    print(json.dumps({"metric": "Ulysses unfused forward, plain vs exchanges overlapped by head group",
+                      "unit": "TFLOP/s (algorithmic attention flops / whole forward time)", "workload": w["name"],
+                      "steps": args.steps, "results": rows, "clocks": clk}))
+
+
 # -------------------------------------------------------------------------- main
 def main():
     ap = argparse.ArgumentParser()
@@ -406,10 +526,22 @@ def main():
     ap.add_argument("--workload", default="dit", choices=sorted(WORKLOADS))
     ap.add_argument("--permute-sweep", action="store_true",
                     help="measure the exchanges over the permute-only sweep instead of the forward")
+    ap.add_argument("--backward", action="store_true",
+                    help="measure the attention backward (local and distributed) instead of the forward")
+    ap.add_argument("--overlap", action="store_true",
+                    help="measure the unfused forward against the overlapped (chunked) forward")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
+    if args.overlap:
+        if rank == 0:
+            run_overlap(args)
+        return
+    if args.backward:
+        if rank == 0:
+            run_backward(args)
+        return
     if args.permute_sweep:
         if rank == 0:
             run_permute_sweep(args)

@@ -126,6 +126,33 @@ uly_status ulysses_dist_attn_fwd(int P, int b, int s, int h_q, int h_kv, int d, 
                                  cudaStream_t stream);
 
 /*
+ * The unfused forward with its exchanges overlapped with attention ("DeepSpeed-Ulysses
+ * 深度解析", section "怎么用：极简接入与通信组初始化", subsection "两行代码替换注意力":
+ * passing `sp_stream` to DistributedAttention overlaps the Q/K/V all-to-all with the
+ * computation).  The local heads of every rank are split into n_chunks equal groups
+ * (chunk c = local query heads [c*h_q/P/n, (c+1)*h_q/P/n) and the matching K/V heads).
+ * On `side_stream` run, in order: all-to-all #1 of chunks 0 and 1, then for every chunk c
+ * all-to-all #2 of c (after c's attention) and all-to-all #1 of c+2; on `stream` the
+ * attention of chunk c runs once c's inputs are there.  So while chunk c is computed the
+ * side stream moves chunk c-1's output and chunk c+1's inputs.  `stream` waits for
+ * everything before the call returns control of the results to it; `side_stream` first
+ * waits for the work already on `stream`.  side_stream may equal stream (no overlap).
+ * Arguments and results as ulysses_dist_attn_fwd with fused == 0 -- the same bits --
+ * plus: 1 <= n_chunks <= 64 and (h_kv/P) % n_chunks == 0, else ULY_ERR_INVALID_ARG;
+ * workspace: 256-byte aligned, at least ulysses_dist_attn_overlap_workspace_bytes(...)
+ * bytes (the chunks' head-layout Q, K, V, O).  The call creates and destroys CUDA events
+ * (host objects) for the cross-stream ordering; it allocates no device memory.
+ */
+size_t ulysses_dist_attn_overlap_workspace_bytes(int P, int b, int s, int h_q, int h_kv, int d,
+                                                 uly_dtype dtype, int n_chunks);
+uly_status ulysses_dist_attn_fwd_overlap(int P, int b, int s, int h_q, int h_kv, int d, uly_dtype dtype,
+                                         int causal,
+                                         const void* const* q_seq, const void* const* k_seq,
+                                         const void* const* v_seq, void* const* o_seq,
+                                         void* workspace, size_t workspace_bytes, int n_chunks,
+                                         cudaStream_t stream, cudaStream_t side_stream);
+
+/*
  * The unfused forward without any allocation by the caller or the library.  The paper has
  * no counterpart: this exists for callers that cannot call cudaMalloc -- for example an
  * application whose memory pool already holds all the device memory it may use, or a

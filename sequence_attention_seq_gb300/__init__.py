@@ -23,7 +23,8 @@ __all__ = [
     "ulysses_dist_attn_workspace_bytes", "ulysses_dist_attn_fwd", "ulysses_device_status",
     "ulysses_status_string", "EXPORTED_SYMBOLS", "ulysses_dist_attn_fwd_noalloc", "NOALLOC_SCRATCH_BYTES",
     "ulysses_local_attention_fwd_lse", "ulysses_dist_attn_fwd_lse", "ulysses_attn_bwd_workspace_bytes",
-    "ulysses_local_attention_bwd", "ulysses_dist_attn_bwd",
+    "ulysses_local_attention_bwd", "ulysses_dist_attn_bwd", "ulysses_dist_attn_overlap_workspace_bytes",
+    "ulysses_dist_attn_fwd_overlap",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -38,7 +39,7 @@ EXPORTED_SYMBOLS = (
     "ulysses_dist_attn_workspace_bytes", "ulysses_dist_attn_fwd", "ulysses_device_status",
     "ulysses_status_string", "ulysses_dist_attn_fwd_noalloc", "ulysses_local_attention_fwd_lse",
     "ulysses_dist_attn_fwd_lse", "ulysses_attn_bwd_workspace_bytes", "ulysses_local_attention_bwd",
-    "ulysses_dist_attn_bwd",
+    "ulysses_dist_attn_bwd", "ulysses_dist_attn_overlap_workspace_bytes", "ulysses_dist_attn_fwd_overlap",
 )
 
 _lock = threading.Lock()
@@ -90,6 +91,10 @@ def load_library():
             f = getattr(lib, name)
             f.argtypes = [i, i, i, i, i, i, i, i, pp, pp, pp, pp, pp, pp, pp, pp, pp, vp, sz, vp]
             f.restype = i
+        lib.ulysses_dist_attn_overlap_workspace_bytes.argtypes = [i, i, i, i, i, i, i, i]
+        lib.ulysses_dist_attn_overlap_workspace_bytes.restype = sz
+        lib.ulysses_dist_attn_fwd_overlap.argtypes = [i, i, i, i, i, i, i, i, pp, pp, pp, pp, vp, sz, i, vp, vp]
+        lib.ulysses_dist_attn_fwd_overlap.restype = i
         lib.ulysses_device_status.argtypes = [i]
         lib.ulysses_device_status.restype = i
         lib.ulysses_status_string.argtypes = [i]
@@ -336,3 +341,44 @@ def ulysses_dist_attn_bwd(q_seq, k_seq, v_seq, o_seq, do_seq, lse, causal, grads
     """The DistributedAttention backward, seq layout in and out: returns (dq, dk, dv) seq layout."""
     return _bwd_call("ulysses_dist_attn_bwd", True, q_seq, k_seq, v_seq, o_seq, do_seq, lse, causal, grads,
                      workspace, stream)
+
+
+# ------------------------------------------------------------------------- overlapped forward
+_side_streams = {}
+
+
+def _side_stream(device):
+    """One cached side stream per device for the overlapped forward's exchanges."""
+    key = torch.device(device).index
+    if key not in _side_streams:
+        _side_streams[key] = torch.cuda.Stream(device=device)
+    return _side_streams[key]
+
+
+def ulysses_dist_attn_overlap_workspace_bytes(P, b, s, h_q, h_kv, d, dtype, n_chunks):
+    return int(load_library().ulysses_dist_attn_overlap_workspace_bytes(P, b, s, h_q, h_kv, d, _DTYPES[dtype],
+                                                                       int(n_chunks)))
+
+
+def ulysses_dist_attn_fwd_overlap(q_seq, k_seq, v_seq, causal, n_chunks=2, out_seq=None, workspace=None,
+                                  stream=None, side_stream=None):
+    """The unfused forward with the exchanges of one head group overlapped with the attention
+    of the next (n_chunks head groups); same results, bit for bit, as ulysses_dist_attn_fwd."""
+    q0 = _same(q_seq, "q_seq")
+    k0 = _same(k_seq, "k_seq")
+    _same(v_seq, "v_seq")
+    P = len(q_seq)
+    b, S, hq, d = q0.shape
+    hkv = k0.shape[2]
+    s = S * P
+    if out_seq is None:
+        out_seq = [torch.empty_like(q) for q in q_seq]
+    if workspace is None:
+        need = ulysses_dist_attn_overlap_workspace_bytes(P, b, s, hq, hkv, d, q0.dtype, n_chunks)
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q0.device)
+    side = side_stream if side_stream is not None else _side_stream(q0.device)
+    _check(load_library().ulysses_dist_attn_fwd_overlap(
+        P, b, s, hq, hkv, d, _dtype_code(q0), int(bool(causal)), _ptr_array(q_seq), _ptr_array(k_seq),
+        _ptr_array(v_seq), _ptr_array(out_seq), workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+        int(n_chunks), _stream(stream), ctypes.c_void_p(side.cuda_stream)), "ulysses_dist_attn_fwd_overlap")
+    return out_seq

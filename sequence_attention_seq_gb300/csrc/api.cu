@@ -15,6 +15,7 @@ namespace {
 using uly::kMaxRanks;
 
 constexpr uint64_t kMaxSlabVecs = (1ull << 31) - 1;  // 32-bit index space of the permute kernel
+constexpr int kMaxChunks = 64;                        // head groups of the overlapped forward
 
 int elem_bytes(uly_dtype dt) { return dt == ULY_FP32 ? 4 : (dt == ULY_BF16 ? 2 : 0); }
 
@@ -485,6 +486,124 @@ uly_status ulysses_dist_attn_bwd(int P, int b, int s, int h_q, int h_kv, int d, 
     ce = uly::launch_permute(1, P, b, s, d, 2, t, 3, stream);
     delete[] t;
     return ce == cudaSuccess ? ULY_OK : ULY_ERR_CUDA;
+}
+
+size_t ulysses_dist_attn_overlap_workspace_bytes(int P, int b, int s, int h_q, int h_kv, int d, uly_dtype dtype,
+                                                 int n_chunks) {
+    if (check_attention_shape(P, b, s, h_q, h_kv, d, dtype) == ULY_ERR_INVALID_ARG) return 0;
+    if (s % P || n_chunks < 1 || n_chunks > kMaxChunks || (h_kv / P) % n_chunks) return 0;
+    const int e = elem_bytes(dtype);
+    const uint64_t qb = round256((uint64_t)b * s * (h_q / P / n_chunks) * d * e);
+    const uint64_t kb = round256((uint64_t)b * s * (h_kv / P / n_chunks) * d * e);
+    return (size_t)((uint64_t)n_chunks * P * (2 * qb + 2 * kb));
+}
+
+uly_status ulysses_dist_attn_fwd_overlap(int P, int b, int s, int h_q, int h_kv, int d, uly_dtype dtype, int causal,
+                                         const void* const* q_seq, const void* const* k_seq,
+                                         const void* const* v_seq, void* const* o_seq, void* workspace,
+                                         size_t workspace_bytes, int n_chunks, cudaStream_t stream,
+                                         cudaStream_t side_stream) {
+    uly_status st = check_attention_shape(P, b, s, h_q, h_kv, d, dtype);
+    if (st != ULY_OK) return st;
+    st = check_exchange_shape(P, b, s, h_q, d, dtype);
+    if (st != ULY_OK) return st;
+    st = check_exchange_shape(P, b, s, h_kv, d, dtype);
+    if (st != ULY_OK) return st;
+    if (n_chunks < 1 || n_chunks > kMaxChunks || (h_kv / P) % n_chunks) return ULY_ERR_INVALID_ARG;
+    const int e = elem_bytes(dtype);
+    const int S = s / P;
+    const uint64_t qsb = (uint64_t)b * S * h_q * d * e, ksb = (uint64_t)b * S * h_kv * d * e;
+    std::vector<Range> rq, rk, rv, ro;
+    if (!collect(q_seq, P, qsb, rq) || !collect(k_seq, P, ksb, rk) || !collect(v_seq, P, ksb, rv) ||
+        !collect(reinterpret_cast<const void* const*>(o_seq), P, qsb, ro))
+        return ULY_ERR_INVALID_ARG;
+    if (overlaps(ro, rq) || overlaps(ro, rk) || overlaps(ro, rv) || self_overlap(ro)) return ULY_ERR_INVALID_ARG;
+    const size_t need = ulysses_dist_attn_overlap_workspace_bytes(P, b, s, h_q, h_kv, d, dtype, n_chunks);
+    if (!workspace_ok(workspace, workspace_bytes, need)) return ULY_ERR_INVALID_ARG;
+    std::vector<Range> rw{{reinterpret_cast<uintptr_t>(workspace), reinterpret_cast<uintptr_t>(workspace) + need}};
+    if (overlaps(rw, rq) || overlaps(rw, rk) || overlaps(rw, rv) || overlaps(rw, ro)) return ULY_ERR_INVALID_ARG;
+
+    // workspace: chunk-major, then per rank [Q | K | V | O] of the chunk's heads in head layout
+    const int nc = n_chunks, Hc = h_q / P / nc, Hkc = h_kv / P / nc;
+    const Carve ws(workspace, {(uint64_t)b * s * Hc * d * e, (uint64_t)b * s * Hkc * d * e,
+                               (uint64_t)b * s * Hkc * d * e, (uint64_t)b * s * Hc * d * e});
+    auto buf = [&](int c, int r, int k) { return ws.at(c * P + r, k); };
+
+    std::vector<cudaEvent_t> ev;
+    auto cleanup = [&]() {
+        for (cudaEvent_t x : ev) cudaEventDestroy(x);
+    };
+    for (int i = 0; i < 2 * nc + 2; ++i) {
+        cudaEvent_t x;
+        if (cudaEventCreateWithFlags(&x, cudaEventDisableTiming) != cudaSuccess) {
+            cleanup();
+            return ULY_ERR_CUDA;
+        }
+        ev.push_back(x);
+    }
+    cudaEvent_t ev_start = ev[0], ev_done = ev[1];
+    auto ev_in = [&](int c) { return ev[2 + c]; };
+    auto ev_attn = [&](int c) { return ev[2 + nc + c]; };
+
+    uly::PermuteTensor* t = new uly::PermuteTensor[3];
+    auto exchange_in = [&](int c) {  // all-to-all #1 for chunk c's heads of Q, K and V (side stream)
+        memset(t, 0, 3 * sizeof(uly::PermuteTensor));
+        const void* const* src[3] = {q_seq, k_seq, v_seq};
+        for (int k = 0; k < 3; ++k) {
+            for (int r = 0; r < P; ++r) {
+                t[k].src[r] = src[k][r];
+                t[k].dst[r] = buf(c, r, k);
+            }
+            t[k].h = k == 0 ? h_q : h_kv;
+            t[k].hsub = k == 0 ? Hc : Hkc;
+            t[k].hoff = c * t[k].hsub;
+        }
+        return uly::launch_permute(0, P, b, s, d, e, t, 3, side_stream);
+    };
+    auto exchange_out = [&](int c) {  // all-to-all #2 for chunk c's output heads (side stream)
+        memset(t, 0, sizeof(uly::PermuteTensor));
+        for (int r = 0; r < P; ++r) {
+            t[0].src[r] = buf(c, r, 3);
+            t[0].dst[r] = o_seq[r];
+        }
+        t[0].h = h_q;
+        t[0].hsub = Hc;
+        t[0].hoff = c * Hc;
+        return uly::launch_permute(1, P, b, s, d, e, t, 1, side_stream);
+    };
+    uly::AttnPtrs* head = new uly::AttnPtrs;
+    bool ok = cudaEventRecord(ev_start, stream) == cudaSuccess &&
+              cudaStreamWaitEvent(side_stream, ev_start, 0) == cudaSuccess;
+    for (int c = 0; c < 2 && c < nc && ok; ++c)
+        ok = exchange_in(c) == cudaSuccess && cudaEventRecord(ev_in(c), side_stream) == cudaSuccess;
+    for (int c = 0; c < nc && ok; ++c) {
+        // main stream: attention of chunk c once its inputs are exchanged
+        memset(head, 0, sizeof(uly::AttnPtrs));
+        for (int r = 0; r < P; ++r) {
+            head->q[r] = buf(c, r, 0);
+            head->k[r] = buf(c, r, 1);
+            head->v[r] = buf(c, r, 2);
+            head->o[r] = buf(c, r, 3);
+        }
+        ok = cudaStreamWaitEvent(stream, ev_in(c), 0) == cudaSuccess;
+        if (ok) {
+            st = run_attention(P, b, s, Hc * P, Hkc * P, d, dtype, causal, 0, *head, stream);
+            ok = st == ULY_OK;
+        }
+        ok = ok && cudaEventRecord(ev_attn(c), stream) == cudaSuccess;
+        // side stream: chunk c's output exchange, then chunk c+2's input exchange, both
+        // running while the main stream computes chunk c+1
+        ok = ok && cudaStreamWaitEvent(side_stream, ev_attn(c), 0) == cudaSuccess && exchange_out(c) == cudaSuccess;
+        if (ok && c + 2 < nc)
+            ok = exchange_in(c + 2) == cudaSuccess && cudaEventRecord(ev_in(c + 2), side_stream) == cudaSuccess;
+    }
+    ok = ok && cudaEventRecord(ev_done, side_stream) == cudaSuccess &&
+         cudaStreamWaitEvent(stream, ev_done, 0) == cudaSuccess;
+    delete head;
+    delete[] t;
+    cleanup();  // destroying a recorded event is legal: its resources go once the work completes
+    if (!ok) return st != ULY_OK ? st : ULY_ERR_CUDA;
+    return ULY_OK;
 }
 
 uly_status ulysses_device_status(int clear) {

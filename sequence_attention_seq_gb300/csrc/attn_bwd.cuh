@@ -10,13 +10,14 @@
 // Three launches, no atomics, every output element written once:
 //   bwd_prep_kernel  D_i from O and dO, and L_i in base-2 units, into padded per-row arrays
 //   bwd_dkdv_kernel  one CTA per (rank, batch, K/V head, 128-key tile).  S^T = K Q^T and
-//                    dP^T = V dO^T land in tensor memory; eight row warps (two per tensor
-//                    memory lane quarter, each owning 64 of the 128 query columns) form P^T
-//                    (bf16, written back over S^T) and dS^T (bf16, into shared memory in the
-//                    operand layout); dV += P^T dO takes P^T straight from tensor memory and
-//                    dK += dS^T Q reads dS^T from shared memory.  The loop runs over every
-//                    query head of the K/V head's group and every query tile that sees the
-//                    key tile.
+//                    dP^T = V dO^T land in tensor memory; sixteen row warps (four per tensor
+//                    memory lane quarter, each owning 32 of the 128 query columns; the dQ
+//                    kernel uses eight, two per quarter, 64 columns each) form P^T
+//                    (bf16, written back over S^T) and dS^T (bf16, written back over dP^T);
+//                    dV += P^T dO and dK += dS^T Q both take their A operand straight from
+//                    tensor memory, so shared memory holds only K, V and the Q/dO stream.
+//                    The loop runs over every query head of the K/V head's group and every
+//                    query tile that sees the key tile.
 //   bwd_dq_kernel    one CTA per (rank, batch, query head, 128-query tile).  S = Q K^T (two
 //                    tensor-memory buffers, so S of tile n+2 can be computed while tile n+1
 //                    is being worked on) and dP = dO V^T; the row warps write dS as bf16 over
@@ -34,11 +35,21 @@
 // Every wait is bounded like the forward's: a wait that gives up sets the device error
 // word, and the CTA drains its copies and MMAs, frees tensor memory and returns.
 
-constexpr int kBwdRowWarps = 8;
-constexpr int kBwdProducer = 8;
-constexpr int kBwdMma = 9;
-constexpr int kBwdThreads = 320;
-constexpr int kRingKV = 4;   // dK/dV kernel: Q/dO ring slots (two query tiles in flight)
+// Warp roles of both kernels: RW row warps (RW/4 per tensor-memory lane quarter, each
+// owning 128/(RW/4) tile columns), then the TMA producer warp, then the MMA warp.
+template <int RW>
+struct RowCfg {
+    static constexpr int kRows = RW;
+    static constexpr int kProducer = RW;
+    static constexpr int kMma = RW + 1;
+    static constexpr int kThreads = (RW + 2) * 32;
+    static constexpr int kColGroups = RW / 4;       // row warps sharing one lane quarter
+    static constexpr int kColW = 128 / kColGroups;  // tile columns each row warp owns
+    static constexpr int kChunks = kColW / 32;      // 32-column tensor-memory loads per warp
+};
+constexpr int kRowsKV = 16;  // dK/dV kernel: faster than 8 on the DiT workload
+constexpr int kRowsQ = 8;    // dQ kernel: 8 and 16 measure the same; 8 needs fewer threads
+constexpr int kRingKV = 5;   // dK/dV kernel: Q/dO ring slots
 constexpr int kRingQ = 5;    // dQ kernel: K/V ring slots
 
 struct BwdParams {
@@ -118,14 +129,13 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __grid_constant__ P
 }
 
 // --------------------------------------------------------------- shared pieces
-template <int D, int RING, bool DS_SMEM>
+template <int D, int RING>
 struct BwdSmem {
     static constexpr uint32_t kTile = 128 * D * 2;
     static constexpr uint32_t offFixA = 0;          // K (dK/dV kernel) or Q (dQ kernel)
     static constexpr uint32_t offFixB = kTile;      // V or dO
     static constexpr uint32_t offRing = 2 * kTile;  // RING streamed tiles
-    static constexpr uint32_t offDS = offRing + RING * kTile;  // dS^T, 128 x 128 bf16 (dK/dV kernel)
-    static constexpr uint32_t offBar = offDS + (DS_SMEM ? 128u * 128u * 2u : 0u);
+    static constexpr uint32_t offBar = offRing + RING * kTile;
     static constexpr uint32_t kBarSlots = 24;
     static constexpr uint32_t kUsed = offBar + kBarSlots * 8 + 64;
     static constexpr uint32_t kAlloc = kUsed + 1024;  // slack to align the base to 1024 bytes
@@ -153,16 +163,17 @@ __device__ __forceinline__ void store_row_bf16(uint32_t taddr, uint8_t* dst, flo
 
 // Initialises the barriers (those in [rows_from, rows_to) count one arrival per row warp)
 // and allocates tensor memory; false when the CTA must leave at once.
-__device__ __forceinline__ bool bwd_setup(uint64_t* bars, int nbars, int rows_from, int rows_to, Shared* sh) {
+__device__ __forceinline__ bool bwd_setup(uint64_t* bars, int nbars, int rows_from, int rows_to, int row_warps,
+                                          int mma_warp, Shared* sh) {
     if (threadIdx.x == 0) {
         sh->abort = error_word_set() ? 1 : 0;
         for (int i = 0; i < nbars; ++i)
-            mbar_init(&bars[i], (i >= rows_from && i < rows_to) ? (uint32_t)kBwdRowWarps : 1u);
+            mbar_init(&bars[i], (i >= rows_from && i < rows_to) ? (uint32_t)row_warps : 1u);
         fence_mbarrier_init();
     }
     __syncthreads();
     if (sh->abort) return false;
-    if ((threadIdx.x >> 5) == kBwdMma) tmem_alloc(&sh->tmem_base, kTmemCols);
+    if ((threadIdx.x >> 5) == mma_warp) tmem_alloc(&sh->tmem_base, kTmemCols);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -182,38 +193,31 @@ __device__ __forceinline__ void mma_kmajor(uint32_t d, uint64_t a, uint64_t b) {
 }
 
 // acc (128 x D) += A (128 x 128 bf16 pairs in tensor memory at a_tmem) * B (128 x D tile in
-// shared memory, D contiguous: MN-major).  The row warps lay A out in two 64-column halves:
-// columns 16k..16k+15 of A sit at a_tmem + 64*(k/4) + 8*(k%4).
-template <int D>
+// shared memory, D contiguous: MN-major).  Each row warp packs its kColW columns of A into
+// the first kColW/2 tensor-memory columns of its own kColW-column group, so columns
+// 16k..16k+15 of A sit at a_tmem + kColW*(16k / kColW) + (16k % kColW)/2.
+template <int D, int kColW>
 __device__ __forceinline__ void mma_acc_tmemA(uint32_t acc, uint32_t a_tmem, uint64_t b_mn, bool accumulate) {
     constexpr uint32_t kIdesc = idesc_bf16_f32(128, D, true);
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk)
-        mma_bf16_ts_warp(acc, a_tmem + (kk >> 2) * 64 + (kk & 3) * 8, b_mn + ((kk * 16 * 128) >> 4), kIdesc,
-                         (accumulate || kk > 0) ? 1u : 0u);
-}
-
-// acc (128 x D) += A (128 x 128 K-major bf16 tile in shared memory) * B (MN-major tile).
-template <int D>
-__device__ __forceinline__ void mma_acc_smemA(uint32_t acc, uint64_t a_k, uint64_t b_mn, bool accumulate) {
-    constexpr uint32_t kIdesc = idesc_bf16_f32(128, D, true);
-    constexpr uint32_t kSlab = 128 * 128;
-#pragma unroll
-    for (int kk = 0; kk < 8; ++kk)
-        mma_bf16_ss_warp(acc, a_k + (((kk >> 2) * kSlab + (kk & 3) * 32) >> 4), b_mn + ((kk * 16 * 128) >> 4),
-                         kIdesc, (accumulate || kk > 0) ? 1u : 0u);
+        mma_bf16_ts_warp(acc, a_tmem + (kk * 16 / kColW) * kColW + ((kk * 16) % kColW) / 2,
+                         b_mn + ((kk * 16 * 128) >> 4), kIdesc, (accumulate || kk > 0) ? 1u : 0u);
 }
 
 // ------------------------------------------------------------------ dK / dV
 // Block -> (rank, batch, K/V head, key tile), key tile fastest and ascending.
-// Tensor memory: S^T (then P^T) 0..127 | dP^T 128..255 | dK 256.. | dV 384..
-template <int D>
-__global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_constant__ BwdParams p) {
-    using L = BwdSmem<D, kRingKV, true>;
+// Tensor memory: S^T (then P^T) 0..127 | dP^T (then dS^T) 128..255 | dK 256.. | dV 384..
+template <int D, int RW>
+__global__ void __launch_bounds__(RowCfg<RW>::kThreads, 1) bwd_dkdv_kernel(const __grid_constant__ BwdParams p) {
+    using C = RowCfg<RW>;
+    constexpr int kBwdRowWarps = C::kRows, kBwdProducer = C::kProducer, kBwdMma = C::kMma;
+    constexpr int kColGroups = C::kColGroups, kColW = C::kColW, kChunks = C::kChunks;
+    using L = BwdSmem<D, kRingKV>;
     constexpr uint32_t kSlab = 128 * 128;
     enum {
-        FIX = 0, FULL = 1, EMPTY = FULL + kRingKV, S_FULL = EMPTY + kRingKV, DP_FULL, P_READY, DS_READY, DS_EMPTY,
-        FINAL, NBARS
+        FIX = 0, FULL = 1, EMPTY = FULL + kRingKV, S_FULL = EMPTY + kRingKV, DP_FULL, P_READY, DS_READY, FINAL,
+        NBARS
     };
     static_assert(NBARS <= (int)L::kBarSlots, "barrier slots");
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -237,7 +241,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
     auto step_head = [kvh, g](int n) { return kvh * g + n % g; };
     auto step_qt = [n_tiles, g](int n) { return n_tiles - 1 - n / g; };
 
-    if (!bwd_setup(bars, NBARS, P_READY, DS_READY + 1, sh)) return;
+    if (!bwd_setup(bars, NBARS, P_READY, DS_READY + 1, kBwdRowWarps, kBwdMma, sh)) return;
     const uint32_t tmem = sh->tmem_base;
 
     if (warp == kBwdProducer) {
@@ -276,7 +280,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
         const uint64_t dv_a = smem_desc_sw128(sbase + L::offFixB, 16, 1024);        // V
         const uint64_t ring_k = smem_desc_sw128(sbase + L::offRing, 16, 1024);      // Q / dO, K-major
         const uint64_t ring_mn = smem_desc_sw128(sbase + L::offRing, kSlab, 1024);  // Q / dO, MN-major
-        const uint64_t ds_a = smem_desc_sw128(sbase + L::offDS, 16, 1024);         // dS^T, K-major
         auto so = [](int m) { return (uint64_t)(((m % kRingKV) * L::kTile) >> 4); };
         auto full = [&](int m) { return wait_phase_warp(&bars[FULL + m % kRingKV], (m / kRingKV) & 1, sh); };
         bool ok = wait_phase_warp(&bars[FIX], 0, sh) && full(0);
@@ -296,7 +299,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
             ok = wait_phase_warp(&bars[P_READY], n & 1, sh);
             if (!ok) break;
             tc_fence_after();
-            mma_acc_tmemA<D>(tmem + 384u, tmem, ring_mn + so(mo), n > 0);  // dV += P^T dO
+            mma_acc_tmemA<D, kColW>(tmem + 384u, tmem, ring_mn + so(mo), n > 0);  // dV += P^T dO
             mma_commit_warp(&bars[EMPTY + mo % kRingKV]);
             if (n + 1 < n_steps) {  // S^T(n+1) over P^T(n): issued after the product that reads it
                 ok = full(mq + 2);
@@ -308,10 +311,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
             ok = wait_phase_warp(&bars[DS_READY], n & 1, sh);
             if (!ok) break;
             tc_fence_after();
-            mma_acc_smemA<D>(tmem + 256u, ds_a, ring_mn + so(mq), n > 0);  // dK += dS^T Q
-            mma_commit_warp(&bars[DS_EMPTY]);
+            mma_acc_tmemA<D, kColW>(tmem + 256u, tmem + 128u, ring_mn + so(mq), n > 0);  // dK += dS^T Q
             mma_commit_warp(&bars[EMPTY + mq % kRingKV]);
-            if (n + 1 < n_steps) {  // dP^T(n+1): the row warps have read dP^T(n)
+            if (n + 1 < n_steps) {  // dP^T(n+1) over dS^T(n): issued after the product that reads it
                 ok = full(mo + 2);
                 if (!ok) break;
                 tc_fence_after();
@@ -322,27 +324,33 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
         mma_commit_warp(&bars[FINAL]);
         drain_phase(&bars[FINAL], 0);
     } else {
-        // row warps: thread = key row, warp half = 64 query columns
-        const int sub = warp & 3, half = warp >> 2;
+        // row warps: thread = key row; warp group cg owns query columns [cg*kColW, +kColW)
+        const int sub = warp & 3, cg = warp >> 2;
         const int row = sub * 32 + lane, key = k0 + row;
         const uint32_t lane_off = (uint32_t)(sub * 32) << 16;
-        const uint32_t tS = tmem + lane_off + half * 64, tdP = tmem + 128u + lane_off + half * 64;
-        uint8_t* ds_row = smem + L::offDS + half * kSlab + row * 128;
+        const uint32_t tS = tmem + lane_off + cg * kColW, tdP = tmem + 128u + lane_off + cg * kColW;
         const float sc = p.scale_log2;
+        auto stat_off = [&](int n) {  // offset of step n's first row statistic of this warp
+            return ((size_t)bb * p.hq + step_head(n)) * p.s_pad + step_qt(n) * 128 + cg * kColW;
+        };
         bool ok = true;
         for (int n = 0; n < n_steps; ++n) {
-            const int hh = step_head(n), qt = step_qt(n);
-            const int qb = qt * 128 + half * 64;  // first query column of this warp
-            const size_t vbase = ((size_t)bb * p.hq + hh) * p.s_pad + qb;
+            const int qt = step_qt(n);
+            const int qb = qt * 128 + cg * kColW;  // first query column of this warp
+            const size_t vbase = stat_off(n);
             const float4* l4 = reinterpret_cast<const float4*>(p.lse2[rank] + vbase);
             const float4* d4 = reinterpret_cast<const float4*>(p.dsum[rank] + vbase);
+            if (n + 1 < n_steps && lane < 2 * kChunks) {  // next step's statistics: one 128-byte line per lane
+                const size_t nb = stat_off(n + 1) + (lane % kChunks) * 32;
+                prefetch_l1(lane < kChunks ? p.lse2[rank] + nb : p.dsum[rank] + nb);
+            }
             const bool diag = p.causal && qt == kt;
-            float pf[64];
+            float pf[kColW];
             ok = wait_phase_warp(&bars[S_FULL], n & 1, sh);
             if (!ok) break;
             tc_fence_after();
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
+            for (int c = 0; c < kChunks; ++c) {
                 uint32_t sv[32];
                 float lv[32];
                 tmem_ld32(tS + c * 32, sv);
@@ -378,11 +386,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
             if (lane == 0) mbar_arrive(&bars[P_READY]);
 
             ok = wait_phase_warp(&bars[DP_FULL], n & 1, sh);
-            if (ok && n > 0) ok = wait_phase_warp(&bars[DS_EMPTY], (n - 1) & 1, sh);
             if (!ok) break;
             tc_fence_after();
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
+            for (int c = 0; c < kChunks; ++c) {
                 uint32_t dv[32];
                 float dl[32];
                 tmem_ld32(tdP + c * 32, dv);
@@ -402,26 +409,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
                     fadd2(t0, t1, __uint_as_float(dv[e]), __uint_as_float(dv[e + 1]), -dl[e], -dl[e + 1]);
                     pk[e >> 1] = pack_bf16x2(pf[c * 32 + e] * t0, pf[c * 32 + e + 1] * t1);
                 }
-                // dS^T row into the K-major 128-byte-swizzled operand tile (slab = this half)
-#pragma unroll
-                for (int q8 = 0; q8 < 4; ++q8) {
-                    const int chunk = c * 4 + q8;  // 16-byte chunk (8 queries) within the 64-query row
-                    *reinterpret_cast<uint4*>(ds_row + ((chunk ^ (row & 7)) << 4)) =
-                        make_uint4(pk[q8 * 4 + 0], pk[q8 * 4 + 1], pk[q8 * 4 + 2], pk[q8 * 4 + 3]);
-                }
+                tmem_st16(tdP + c * 16, pk);  // dS^T over dP^T columns this warp has already read
             }
-            fence_proxy_async_smem();  // generic-proxy stores -> visible to the tensor pipe
+            tmem_wait_st();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars[DS_READY]);
         }
         if (ok) ok = wait_phase_warp(&bars[FINAL], 0, sh);
-        if (ok) {
+        constexpr int kEpi = D / kColGroups >= 32 ? D / kColGroups : 32;  // accumulator columns per warp
+        if (ok && cg * kEpi < D) {
             tc_fence_after();
             const bool kok = key < p.s;
-            const size_t off = (((size_t)bb * p.s + (kok ? key : 0)) * p.hkv + kvh) * (size_t)D * 2 + half * D;
-            store_row_bf16<D / 2>(tmem + 256u + lane_off + half * (D / 2), p.dk[rank] + off, p.scale, kok);
-            store_row_bf16<D / 2>(tmem + 384u + lane_off + half * (D / 2), p.dv[rank] + off, 1.0f, kok);
+            const size_t off = (((size_t)bb * p.s + (kok ? key : 0)) * p.hkv + kvh) * (size_t)D * 2 + cg * kEpi * 2;
+            store_row_bf16<kEpi>(tmem + 256u + lane_off + cg * kEpi, p.dk[rank] + off, p.scale, kok);
+            store_row_bf16<kEpi>(tmem + 384u + lane_off + cg * kEpi, p.dv[rank] + off, 1.0f, kok);
         }
     }
     tc_fence_before();
@@ -436,9 +438,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
 // Block -> (rank, batch, query head, query tile), query tile fastest, last tile first;
 // query heads sharing a K/V head are adjacent.  Tensor memory: S/dS buffer 0 0..127 |
 // dP 128..255 | dQ 256.. | S/dS buffer 1 384..511.
-template <int D>
-__global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_constant__ BwdParams p) {
-    using L = BwdSmem<D, kRingQ, false>;
+template <int D, int RW>
+__global__ void __launch_bounds__(RowCfg<RW>::kThreads, 1) bwd_dq_kernel(const __grid_constant__ BwdParams p) {
+    using C = RowCfg<RW>;
+    constexpr int kBwdRowWarps = C::kRows, kBwdProducer = C::kProducer, kBwdMma = C::kMma;
+    constexpr int kColGroups = C::kColGroups, kColW = C::kColW, kChunks = C::kChunks;
+    using L = BwdSmem<D, kRingQ>;
     constexpr uint32_t kSlab = 128 * 128;
     enum {
         FIX = 0, FULL = 1, EMPTY = FULL + kRingQ, S_FULL = EMPTY + kRingQ, DP_FULL = S_FULL + 2, DS_READY, FINAL,
@@ -463,7 +468,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
     const int q0 = qt * 128;
     const int n_steps = p.causal ? qt + 1 : p.n_tiles;  // key tiles 0 .. n_steps-1
 
-    if (!bwd_setup(bars, NBARS, DS_READY, DS_READY + 1, sh)) return;
+    if (!bwd_setup(bars, NBARS, DS_READY, DS_READY + 1, kBwdRowWarps, kBwdMma, sh)) return;
     const uint32_t tmem = sh->tmem_base;
     auto sbuf = [tmem](int n) { return tmem + ((n & 1) ? 384u : 0u); };
 
@@ -533,7 +538,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
             ok = wait_phase_warp(&bars[DS_READY], n & 1, sh);
             if (!ok) break;
             tc_fence_after();
-            mma_acc_tmemA<D>(tmem + 256u, sbuf(n), ring_mn + so(2 * n), n > 0);  // dQ += dS K
+            mma_acc_tmemA<D, kColW>(tmem + 256u, sbuf(n), ring_mn + so(2 * n), n > 0);  // dQ += dS K
             mma_commit_warp(&bars[EMPTY + (2 * n) % kRingQ]);
             if (n + 1 < n_steps) {  // the row warps have read dP(n)
                 ok = full(2 * n + 3);
@@ -551,8 +556,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
         mma_commit_warp(&bars[FINAL]);
         drain_phase(&bars[FINAL], 0);
     } else {
-        // row warps: thread = query row, warp half = 64 key columns
-        const int sub = warp & 3, half = warp >> 2;
+        // row warps: thread = query row; warp group cg owns key columns [cg*kColW, +kColW)
+        const int sub = warp & 3, cg = warp >> 2;
         const int row = sub * 32 + lane, qrow = q0 + row;
         const uint32_t lane_off = (uint32_t)(sub * 32) << 16;
         const size_t vi = ((size_t)bb * p.hq + hh) * p.s_pad + qrow;  // qrow < s_pad always
@@ -562,18 +567,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
         const int lim = p.causal ? min(p.s, qrow + 1) : p.s;  // keys < lim are visible
         bool ok = true;
         for (int n = 0; n < n_steps; ++n) {
-            const uint32_t tS = sbuf(n) + lane_off + half * 64;
-            const uint32_t tdP = tmem + 128u + lane_off + half * 64;
-            const int kb = n * 128 + half * 64;  // first key column of this warp
+            const uint32_t tS = sbuf(n) + lane_off + cg * kColW;
+            const uint32_t tdP = tmem + 128u + lane_off + cg * kColW;
+            const int kb = n * 128 + cg * kColW;  // first key column of this warp
             // masked: the causal diagonal tile, and keys past the end (zero rows; kept out of
             // the product so that no inf/nan can reach it)
-            const bool mask = (p.causal && n == qt) || kb + 64 > p.s;
-            float pf[64];
+            const bool mask = (p.causal && n == qt) || kb + kColW > p.s;
+            float pf[kColW];
             ok = wait_phase_warp(&bars[S_FULL + (n & 1)], (n >> 1) & 1, sh);
             if (!ok) break;
             tc_fence_after();
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
+            for (int c = 0; c < kChunks; ++c) {
                 uint32_t sv[32];
                 tmem_ld32(tS + c * 32, sv);
                 tmem_wait_ld();
@@ -595,7 +600,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
             if (!ok) break;
             tc_fence_after();
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
+            for (int c = 0; c < kChunks; ++c) {
                 uint32_t dv[32];
                 tmem_ld32(tdP + c * 32, dv);
                 tmem_wait_ld();
@@ -614,11 +619,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
             if (lane == 0) mbar_arrive(&bars[DS_READY]);
         }
         if (ok) ok = wait_phase_warp(&bars[FINAL], 0, sh);
-        if (ok) {
+        constexpr int kEpi = D / kColGroups >= 32 ? D / kColGroups : 32;  // accumulator columns per warp
+        if (ok && cg * kEpi < D) {
             tc_fence_after();
             const bool qok = qrow < p.s;
-            const size_t off = (((size_t)bb * p.s + (qok ? qrow : 0)) * p.hq + hh) * (size_t)D * 2 + half * D;
-            store_row_bf16<D / 2>(tmem + 256u + lane_off + half * (D / 2), p.dq[rank] + off, p.scale, qok);
+            const size_t off = (((size_t)bb * p.s + (qok ? qrow : 0)) * p.hq + hh) * (size_t)D * 2 + cg * kEpi * 2;
+            store_row_bf16<kEpi>(tmem + 256u + lane_off + cg * kEpi, p.dq[rank] + off, p.scale, qok);
         }
     }
     tc_fence_before();
@@ -632,18 +638,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
 // ------------------------------------------------------------------ host side
 template <int D>
 cudaError_t launch_bwd_d(const BwdParams& prm, int nranks, cudaStream_t stream) {
-    using LK = BwdSmem<D, kRingKV, true>;
-    using LQ = BwdSmem<D, kRingQ, false>;
-    cudaError_t e =
-        cudaFuncSetAttribute(bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)LK::kAlloc);
+    using LK = BwdSmem<D, kRingKV>;
+    using LQ = BwdSmem<D, kRingQ>;
+    cudaError_t e = cudaFuncSetAttribute(bwd_dkdv_kernel<D, kRowsKV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)LK::kAlloc);
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)LQ::kAlloc);
+        e = cudaFuncSetAttribute(bwd_dq_kernel<D, kRowsQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)LQ::kAlloc);
     if (e != cudaSuccess) return e;
     const long long gk = (long long)nranks * prm.b * prm.hkv * prm.n_tiles;
     const long long gq = (long long)nranks * prm.b * prm.hq * prm.n_tiles;
-    bwd_dkdv_kernel<D><<<(unsigned)gk, kBwdThreads, LK::kAlloc, stream>>>(prm);
+    bwd_dkdv_kernel<D, kRowsKV><<<(unsigned)gk, RowCfg<kRowsKV>::kThreads, LK::kAlloc, stream>>>(prm);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    bwd_dq_kernel<D><<<(unsigned)gq, kBwdThreads, LQ::kAlloc, stream>>>(prm);
+    bwd_dq_kernel<D, kRowsQ><<<(unsigned)gq, RowCfg<kRowsQ>::kThreads, LQ::kAlloc, stream>>>(prm);
     return cudaGetLastError();
 }

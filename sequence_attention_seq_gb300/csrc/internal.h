@@ -16,7 +16,9 @@ constexpr int kMaxRanks = 64;  // largest P any entry point accepts
 struct PermuteTensor {
     const void* src[kMaxRanks];
     void* dst[kMaxRanks];
-    int h;  // heads of this tensor in seq layout (h_q for Q/O, h_kv for K/V)
+    int h;     // heads of this tensor in seq layout (h_q for Q/O, h_kv for K/V)
+    int hsub;  // heads per rank moved by this call (0: all h/P); the head-layout side holds hsub heads
+    int hoff;  // first moved head within each rank's group of h/P heads
 };
 
 // direction: 0 = seq -> head (all-to-all #1), 1 = head -> seq (all-to-all #2); 1 to 4 tensors.

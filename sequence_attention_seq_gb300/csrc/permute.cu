@@ -7,7 +7,9 @@
 //     head[r][bb][j*S + t][hh][:] == seq[j][bb][t][r*H + hh][:]     (S = s/P, H = h/P)
 // For every (rank r, source rank j, batch bb) the head-layout side is one contiguous slab
 // of S rows of H*d elements, and the seq-layout side is S runs of H*d elements with a
-// pitch of h*d elements.  The kernel streams those slabs with 16-byte (or narrower)
+// pitch of h*d elements.  A call may also move only heads [hoff, hoff+hsub) of every
+// rank's group (the head-layout side then holds hsub heads): the chunked, overlapped
+// forward exchanges one head group at a time.  The kernel streams those slabs with 16-byte (or narrower)
 // vector loads and stores: the contiguous side is fully coalesced, the strided side moves
 // whole runs (>= 128 bytes for every supported bf16/fp32 shape with d >= 64).
 #include "device_common.cuh"
@@ -22,7 +24,9 @@ constexpr int kUnroll = 4;
 struct PermuteJob {
     const uint8_t* src[kMaxRanks];
     uint8_t* dst[kMaxRanks];
-    uint64_t run_bytes;   // H*d*e: one contiguous run on the seq-layout side
+    uint64_t run_bytes;   // hsub*d*e: one contiguous run on the seq-layout side (H*d*e for a whole group)
+    uint64_t rank_bytes;  // H*d*e: distance between consecutive ranks' head groups in a seq-layout row
+    uint64_t head_off;    // hoff*d*e: first moved head inside a rank's group
     uint64_t row_pitch;   // h*d*e: seq-layout row pitch
     uint32_t slab_vecs;   // S*run_bytes / VEC
     FastDiv run_vecs;     // run_bytes / VEC
@@ -71,7 +75,7 @@ __global__ void __launch_bounds__(kThreads) permute_kernel(const __grid_constant
         const uint32_t bb = rest / P;
         const PermuteJob& J = p.job[t];
         const uint64_t off_contig = ((uint64_t)bb * p.s + (uint64_t)j * p.S) * J.run_bytes;
-        const uint64_t off_strided = (uint64_t)bb * p.S * J.row_pitch + (uint64_t)r * J.run_bytes;
+        const uint64_t off_strided = (uint64_t)bb * p.S * J.row_pitch + (uint64_t)r * J.rank_bytes + J.head_off;
         const uint8_t* src = DIR == 0 ? J.src[j] + off_strided : J.src[r] + off_contig;
         uint8_t* dst = DIR == 0 ? J.dst[r] + off_contig : J.dst[j] + off_strided;
         const uint32_t n = J.slab_vecs;
@@ -138,11 +142,14 @@ cudaError_t launch_permute(int direction, int P, int b, int s, int d, int elem_b
     prm.S = (uint32_t)(s / P);
     prm.s = (uint32_t)s;
     prm.units = (uint32_t)P * (uint32_t)P * (uint32_t)b;
-    // widest vector that divides every run (all pointers are 16-byte aligned by contract)
+    // widest vector that divides every run and offset (all pointers are 16-byte aligned by contract)
+    auto hsub = [&](int t) { return tensors[t].hsub > 0 ? tensors[t].hsub : tensors[t].h / P; };
     int vec = 16;
     for (int t = 0; t < ntensors; ++t) {
-        const uint64_t run = (uint64_t)(tensors[t].h / P) * d * elem_bytes;
-        while (vec > 1 && run % vec) vec >>= 1;
+        const uint64_t unit = (uint64_t)d * elem_bytes;
+        const uint64_t sizes[3] = {hsub(t) * unit, (uint64_t)(tensors[t].h / P) * unit, (uint64_t)tensors[t].hoff * unit};
+        for (uint64_t x : sizes)
+            while (vec > 1 && x % vec) vec >>= 1;
     }
     uint32_t max_slab = 0;
     for (int t = 0; t < ntensors; ++t) {
@@ -151,7 +158,9 @@ cudaError_t launch_permute(int direction, int P, int b, int s, int d, int elem_b
             J.src[r] = static_cast<const uint8_t*>(tensors[t].src[r]);
             J.dst[r] = static_cast<uint8_t*>(tensors[t].dst[r]);
         }
-        J.run_bytes = (uint64_t)(tensors[t].h / P) * d * elem_bytes;
+        J.run_bytes = (uint64_t)hsub(t) * d * elem_bytes;
+        J.rank_bytes = (uint64_t)(tensors[t].h / P) * d * elem_bytes;
+        J.head_off = (uint64_t)tensors[t].hoff * d * elem_bytes;
         J.row_pitch = (uint64_t)tensors[t].h * d * elem_bytes;
         J.slab_vecs = (uint32_t)((uint64_t)prm.S * J.run_bytes / vec);
         J.run_vecs = make_fastdiv((uint32_t)(J.run_bytes / vec));
