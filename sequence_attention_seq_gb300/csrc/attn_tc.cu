@@ -77,6 +77,7 @@ struct TcParams {
     int b;
     int nranks;        // rank groups in this launch (fused: 1)
     int n_items;       // query-tile pairs in this launch: nranks * b * heads * n_pairs
+    int band_units;    // causal: (rank, batch, K/V head) units per band (see decode_item)
     int causal;
     float scale_log2;  // log2(e) / sqrt(d)
 };
@@ -164,10 +165,12 @@ __device__ __forceinline__ TileCoord tile_coord(const TcParams& p, int rank, int
 }
 
 // Work item w (a query-tile pair) -> coordinates.  Every role of a CTA walks the same
-// sequence.  Causal: the pair index is slowest and descending, so items are globally
-// sorted heaviest first and the snake assignment balances the CTAs.  Non-causal (all items
-// equal): the pairs of one head are adjacent, so concurrent CTAs share K/V in L2.  In both,
-// the query heads that share a K/V head are adjacent.
+// sequence.  Causal: the (rank, batch, K/V head) units form bands of band_units units whose
+// K and V fit in L2 together; bands run one after another, and inside a band the pair
+// index is slowest and descending, so the band's items are sorted heaviest first and the
+// snake assignment balances the CTAs while all of them stream the same few heads' K/V.
+// Non-causal (all items equal): the pairs of one head are adjacent, so concurrent CTAs
+// share K/V in L2.  In both, the query heads that share a K/V head are adjacent.
 struct Item {
     int rank, bb, kvh, head, qt0, n0, n1;
 };
@@ -179,12 +182,18 @@ __device__ __forceinline__ Item decode_item(const TcParams& p, int w) {
     w /= p.g;
     int pair;
     if (p.causal) {
-        it.kvh = w % kv_heads;
-        w /= kv_heads;
-        it.bb = w % p.b;
-        w /= p.b;
-        it.rank = w % p.nranks;
-        pair = p.n_pairs - 1 - w / p.nranks;
+        const int units = p.nranks * p.b * kv_heads;
+        const int per_band = p.band_units * p.n_pairs;
+        const int band = w / per_band;
+        const int base = band * p.band_units;
+        const int in_band = units - base < p.band_units ? units - base : p.band_units;
+        const int r = w - band * per_band;
+        int u = base + r % in_band;
+        pair = p.n_pairs - 1 - r / in_band;
+        it.kvh = u % kv_heads;
+        u /= kv_heads;
+        it.bb = u % p.b;
+        it.rank = u / p.b;
     } else {
         pair = w % p.n_pairs;
         w /= p.n_pairs;
@@ -566,6 +575,22 @@ bool make_map(CUtensorMap* m, const void* base, int b, int rows, int heads, int 
     return r == CUDA_SUCCESS;
 }
 
+// Causal band size.  When the K and V of every (rank, batch, K/V head) unit of the launch
+// fit in L2 together, one band: the global heaviest-first order balances best.  Otherwise
+// as many units as keep their K and V within about a third of the 129 MB L2 (at least one),
+// so that all CTAs stream the same few heads' K/V and L2 serves the re-reads.
+constexpr double kL2Bytes = 129.0 * 1024 * 1024;
+constexpr double kBandBytes = 48.0 * 1024 * 1024;
+
+int band_units_for(int s, int d, int units) {
+    const double kv_bytes = 2.0 * s * d * 2;  // K and V of one unit, bf16
+    if (kv_bytes * units <= kL2Bytes) return units;
+    int bu = (int)(kBandBytes / kv_bytes);
+    if (bu < 1) bu = 1;
+    if (bu > units) bu = units;
+    return bu;
+}
+
 template <int D>
 cudaError_t launch_d(TcParams& prm, long long n_items, cudaStream_t stream) {
     const uint32_t smem = Smem<D>::kAlloc;
@@ -620,6 +645,7 @@ cudaError_t launch_attention_tc(int P, int b, int s, int h_q, int h_kv, int d, i
         }
         if (err == cudaSuccess) {
             const long long n_items = (long long)b * h_q * prm->n_pairs;
+            prm->band_units = band_units_for(s, d, b * h_kv);
             err = d == 64 ? launch_d<64>(*prm, n_items, stream) : launch_d<128>(*prm, n_items, stream);
         }
     } else {
@@ -640,6 +666,7 @@ cudaError_t launch_attention_tc(int P, int b, int s, int h_q, int h_kv, int d, i
             }
             if (err != cudaSuccess) break;
             const long long n_items = (long long)nr * b * Hq * prm->n_pairs;
+            prm->band_units = band_units_for(s, d, nr * b * Hk);
             err = d == 64 ? launch_d<64>(*prm, n_items, stream) : launch_d<128>(*prm, n_items, stream);
         }
     }
