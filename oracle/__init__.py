@@ -1,4 +1,5 @@
-"""CPU oracle for the Ulysses DistributedAttention forward and backward -- TEST INFRASTRUCTURE ONLY.
+"""CPU oracle for the Ulysses DistributedAttention forward and backward, and the two-level
+Ulysses x Ring forward -- TEST INFRASTRUCTURE ONLY.
 
 Only ``tests/``, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline leg import
 this package.  The product path (``sequence_attention_seq_gb300``) never does, and this
@@ -60,6 +61,9 @@ def _load():
             lib.orc_attention_lse.restype = i
             lib.orc_attention_bwd.argtypes = [i, i, i, i, i, i, i, vp, vp, vp, vp, vp, vp, vp]
             lib.orc_attention_bwd.restype = i
+            lib.orc_usp_fwd.argtypes = [i, i, i, i, i, i, i, i, i, ctypes.POINTER(vp), ctypes.POINTER(vp),
+                                        ctypes.POINTER(vp), ctypes.POINTER(vp)]
+            lib.orc_usp_fwd.restype = i
             _lib = lib
     return _lib
 
@@ -185,3 +189,28 @@ def dist_attn_bwd(q_seq, k_seq, v_seq, do_seq, causal):
     do_head = seq2head(do_seq)
     grads = [attention_bwd(q, k, v, g, causal) for q, k, v, g in zip(q_head, k_head, v_head, do_head)]
     return (head2seq([x[0] for x in grads]), head2seq([x[1] for x in grads]), head2seq([x[2] for x in grads]))
+
+
+def usp_fwd(q_seq, k_seq, v_seq, causal, Pu, Pr):
+    """The two-level (Ulysses inside groups of Pu ranks, ring across Pr groups) forward over
+    P = Pu*Pr seq-partitioned ranks, rank j = g*Pu + u; returns P float64 [b, s/P, h_q, d]."""
+    P = len(q_seq)
+    if P != Pu * Pr:
+        raise ValueError("len(q_seq) must be Pu * Pr")
+    qs, ks, vs = [_cpu(x) for x in q_seq], [_cpu(x) for x in k_seq], [_cpu(x) for x in v_seq]
+    if not (qs[0].dtype == ks[0].dtype == vs[0].dtype):
+        raise ValueError("q, k, v must share a dtype")
+    b, S, hq, d = qs[0].shape
+    out = [torch.empty((b, S, hq, d), dtype=torch.float64) for _ in range(P)]
+    _check(_load().orc_usp_fwd(Pu, Pr, b, S * P, hq, ks[0].shape[2], d, int(bool(causal)), DTYPE_CODE[qs[0].dtype],
+                               _ptrs(qs), _ptrs(ks), _ptrs(vs), _ptrs(out)), "usp_fwd")
+    return out
+
+
+def usp_group_exchange(x_seq, Pu):
+    """Step 1 of the two-level forward alone: all-to-all #1 inside every group of Pu
+    consecutive ranks; returns per-rank head-layout tensors [b, s/Pr, h/Pu, d]."""
+    out = []
+    for g in range(len(x_seq) // Pu):
+        out += seq2head(list(x_seq[g * Pu:(g + 1) * Pu]))
+    return out

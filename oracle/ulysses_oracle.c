@@ -378,3 +378,124 @@ int orc_attention_bwd(int b, int s, int hq, int hkv, int d, int causal, int dtyp
     free(o);
     return ORC_OK;
 }
+
+/* ------------------------------------------------- Ulysses x Ring (USP, a2a + p2p) */
+
+/* n separately allocated buffers of `bytes` each (NULL if any allocation fails). */
+static u8** alloc_bufs(int n, size_t bytes) {
+    u8** c = (u8**)calloc((size_t)n, sizeof(u8*));
+    if (!c) return NULL;
+    for (int i = 0; i < n; ++i) {
+        c[i] = (u8*)malloc(bytes ? bytes : 1);
+        if (!c[i]) {
+            for (int k = 0; k < i; ++k) free(c[k]);
+            free(c);
+            return NULL;
+        }
+    }
+    return c;
+}
+
+static void free_bufs(u8** c, int n) {
+    for (int i = 0; i < n; ++i) free(c[i]);
+    free(c);
+}
+
+/*
+ * The two-level forward: P = Pu * Pr ranks, rank j = g*Pu + u holds tokens
+ * [j*s/P, (j+1)*s/P) of every head ("长上下文训练中的 SP 与 CP", section "组合与配置：区分算法
+ * 组合和并行维度", subsection "Ulysses + Ring：组合两种 Attention 路线": 256K tokens over
+ * Ulysses degree 4 x Ring degree 2; "02 · DeepSpeed-Ulysses", section 4 "a2a+p2p 分层 CP":
+ * inner a2a, outer p2p ring, the product of the two sizes is the CP size).
+ *  1. Inside ring group g (ranks g*Pu .. g*Pu+Pu-1, which together hold the contiguous
+ *     segment g of L = s/Pr tokens) all-to-all #1: rank (g, u) gets all L tokens of the
+ *     segment for heads [u*hq/Pu, (u+1)*hq/Pu) (and the matching K/V heads).
+ *  2. Ring across the Pr groups among the ranks with the same u: rank (g, u) keeps its Q
+ *     and processes the K/V segments in the order g, g-1, ..., g-Pr+1 (mod Pr), the blocks
+ *     arriving from the neighbour ("Ring Attention：Q 留在本地，KV 沿环传递", the four-rank
+ *     example).  Each query row keeps the online-softmax state (m, l, A), starting at
+ *     (-inf, 0, 0); a block of scores S raises m to m' = max(m, rowmax S), rescales
+ *     l and A by exp(m - m'), adds sum exp(S - m') and sum exp(S - m') v; at the end
+ *     O = A / l (same section, online-softmax paragraph).  Causal, on global positions:
+ *     blocks after the query segment are skipped, in the query's own segment only keys
+ *     at or before the query count (a lower-triangular block), earlier blocks count in
+ *     full (same section, causal paragraph).
+ *  3. Inside the group, all-to-all #2 back to the sequence split.
+ * Inputs: P pointers to [b][s/P][h][d] of `dtype`; out: P pointers to double [b][s/P][hq][d].
+ */
+int orc_usp_fwd(int Pu, int Pr, int b, int s, int hq, int hkv, int d, int causal, int dtype,
+                const void* const* q_seq, const void* const* k_seq, const void* const* v_seq, double* const* out) {
+    if (Pu < 1 || Pr < 1 || b < 1 || s < 1 || d < 1 || hq < 1 || hkv < 1) return ORC_BAD_ARG;
+    const int P = Pu * Pr;
+    if (s % P || hq % Pu || hkv % Pu || hq % hkv) return ORC_BAD_ARG;
+    const int e = dtype == 0 ? 4 : (dtype == 1 ? 2 : 8);
+    const int L = s / Pr, Hq = hq / Pu, Hk = hkv / Pu, g_q = hq / hkv;
+    const size_t qh_bytes = (size_t)b * L * Hq * d * e, kh_bytes = (size_t)b * L * Hk * d * e;
+    u8** qh = alloc_bufs(P, qh_bytes);
+    u8** kh = alloc_bufs(P, kh_bytes);
+    u8** vh = alloc_bufs(P, kh_bytes);
+    u8** oh = alloc_bufs(P, (size_t)b * L * Hq * d * sizeof(double));
+    double* A = (double*)malloc(sizeof(double) * d);
+    double* sc = (double*)malloc(sizeof(double) * L);
+    int rc = ORC_OK;
+    if (!qh || !kh || !vh || !oh || !A || !sc) rc = ORC_NO_MEMORY;
+    /* 1. all-to-all #1 inside every ring group */
+    for (int g = 0; g < Pr && rc == ORC_OK; ++g) {
+        rc = orc_seq2head(Pu, b, L, hq, d, e, q_seq + g * Pu, (void* const*)(qh + g * Pu));
+        if (rc == ORC_OK) rc = orc_seq2head(Pu, b, L, hkv, d, e, k_seq + g * Pu, (void* const*)(kh + g * Pu));
+        if (rc == ORC_OK) rc = orc_seq2head(Pu, b, L, hkv, d, e, v_seq + g * Pu, (void* const*)(vh + g * Pu));
+    }
+    /* 2. the ring, per rank (g, u), query row by query row */
+    const double scale = 1.0 / sqrt((double)d);
+    for (int g = 0; g < Pr && rc == ORC_OK; ++g)
+        for (int u = 0; u < Pu; ++u) {
+            const int me = g * Pu + u;
+            for (int bb = 0; bb < b; ++bb)
+                for (int hh = 0; hh < Hq; ++hh)
+                    for (int i = 0; i < L; ++i) {
+                        const size_t qo = (((size_t)bb * L + i) * Hq + hh) * d;
+                        double m = -INFINITY, l = 0.0;
+                        for (int c = 0; c < d; ++c) A[c] = 0.0;
+                        for (int t = 0; t < Pr; ++t) {
+                            const int src = ((g - t) % Pr + Pr) % Pr; /* block received at step t */
+                            if (causal && src > g) continue;       /* after the query segment */
+                            const int nk = (causal && src == g) ? i + 1 : L;
+                            const u8* kb = kh[src * Pu + u];
+                            const u8* vb = vh[src * Pu + u];
+                            double bmax = -INFINITY;
+                            for (int j = 0; j < nk; ++j) {
+                                const size_t ko = (((size_t)bb * L + j) * Hk + hh / g_q) * d;
+                                double acc = 0.0;
+                                for (int c = 0; c < d; ++c)
+                                    acc += load_elem(qh[me], qo + c, dtype) * load_elem(kb, ko + c, dtype);
+                                sc[j] = acc * scale;
+                                if (sc[j] > bmax) bmax = sc[j];
+                            }
+                            const double mn = bmax > m ? bmax : m;
+                            const double f = exp(m - mn); /* 0 while nothing was seen */
+                            l *= f;
+                            for (int c = 0; c < d; ++c) A[c] *= f;
+                            for (int j = 0; j < nk; ++j) {
+                                const double p = exp(sc[j] - mn);
+                                const size_t vo = (((size_t)bb * L + j) * Hk + hh / g_q) * d;
+                                l += p;
+                                for (int c = 0; c < d; ++c) A[c] += p * load_elem(vb, vo + c, dtype);
+                            }
+                            m = mn;
+                        }
+                        double* o = (double*)oh[me] + qo;
+                        for (int c = 0; c < d; ++c) o[c] = l > 0.0 ? A[c] / l : 0.0;
+                    }
+        }
+    /* 3. all-to-all #2 inside every ring group */
+    for (int g = 0; g < Pr && rc == ORC_OK; ++g)
+        rc = orc_head2seq(Pu, b, L, hq, d, (int)sizeof(double), (const void* const*)(oh + g * Pu),
+                          (void* const*)(out + g * Pu));
+    free(A);
+    free(sc);
+    if (qh) free_bufs(qh, P);
+    if (kh) free_bufs(kh, P);
+    if (vh) free_bufs(vh, P);
+    if (oh) free_bufs(oh, P);
+    return rc;
+}
