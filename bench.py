@@ -41,6 +41,8 @@ WORKLOADS = {
                 name="GQA causal: P=8 b=1 s=32768 h_q=32 h_kv=8 d=128 bf16, unfused + fused forward"),
     "long": dict(P=8, b=1, s=131072, h_q=64, h_kv=64, d=128, dtype="bf16", masks=(True,),
                  name="Long-sequence causal: P=8 b=1 s=131072 h=64 d=128 bf16, unfused + fused forward"),
+    "usp": dict(P=8, Pu=4, Pr=2, b=1, s=262144, h_q=16, h_kv=16, d=128, dtype="bf16", masks=(True,),
+                name="Ulysses x Ring causal: 256K tokens, Ulysses 4 x Ring 2 (P=8), b=1 h=16 d=128 bf16"),
     "tiny": dict(P=2, b=1, s=64, h_q=4, h_kv=4, d=16, dtype="fp32", masks=(False,),
                  name="Tiny exactness case: P=2 b=1 s=64 h=4 d=16 fp32, non-causal, unfused forward"),
 }
@@ -515,6 +517,55 @@ def run_overlap(args):
                       "steps": args.steps, "results": rows, "clocks": clk}))
 
 
+def run_usp(args):
+    """The two-level (Ulysses x Ring) forward against the plain Ulysses forward (unfused and
+    fused) over the same ranks, each call bracketed by CUDA events."""
+    import torch
+
+    import sequence_attention_seq_gb300 as uly
+    from sequence_attention_seq_gb300 import build as uly_build
+    from sequence_attention_seq_gb300.inputs import seq_shards_qkv
+
+    uly_build.build()
+    w = WORKLOADS["usp"]
+    P, Pu, Pr, b, s, hq, hkv, d = w["P"], w["Pu"], w["Pr"], w["b"], w["s"], w["h_q"], w["h_kv"], w["d"]
+    qs, ks, vs = seq_shards_qkv(P, b, s, hq, hkv, d, torch.bfloat16, seed=0, device="cuda")
+    out = [torch.empty_like(q) for q in qs]
+    ws_u = torch.empty(uly.ulysses_usp_workspace_bytes(Pu, Pr, b, s, hq, hkv, d, torch.bfloat16),
+                       dtype=torch.uint8, device="cuda")
+    ws_d = torch.empty(uly.ulysses_dist_attn_workspace_bytes(P, b, s, hq, hkv, d, torch.bfloat16, False),
+                       dtype=torch.uint8, device="cuda")
+    fl = attn_flops(b, s, hq, d, True)
+    calls = {
+        "usp_4x2": lambda: uly.ulysses_usp_attn_fwd(qs, ks, vs, True, Pu, Pr, out_seq=out, workspace=ws_u),
+        "ulysses_unfused_p8": lambda: uly.ulysses_dist_attn_fwd(qs, ks, vs, True, fused=False, out_seq=out,
+                                                                workspace=ws_d),
+        "ulysses_fused_p8": lambda: uly.ulysses_dist_attn_fwd(qs, ks, vs, True, fused=True, out_seq=out),
+    }
+    rows = {}
+    clocks = ClockSampler(0)
+    clocks.start()
+    time.sleep(0.3)
+    for name, fn in calls.items():
+        for _ in range(max(3, args.warmup)):
+            fn()
+        torch.cuda.synchronize()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        for e0, e1 in evs:
+            e0.record()
+            fn()
+            e1.record()
+        torch.cuda.synchronize()
+        ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in evs)
+        rows[name] = {"ms": ms, "tflops": fl / (ms * 1e-3) / 1e12}
+    if uly.ulysses_device_status(clear=True) != 0:
+        raise RuntimeError("a kernel's bounded wait gave up")
+    clk = clocks.stop()
+    print(json.dumps({"metric": "two-level Ulysses x Ring forward vs plain Ulysses over the same 8 ranks",
+                      "unit": "TFLOP/s (algorithmic attention flops / whole forward time)", "workload": w["name"],
+                      "steps": args.steps, "results": rows, "clocks": clk}))
+
+
 # -------------------------------------------------------------------------- main
 def main():
     ap = argparse.ArgumentParser()
@@ -528,6 +579,8 @@ def main():
                     help="measure the exchanges over the permute-only sweep instead of the forward")
     ap.add_argument("--backward", action="store_true",
                     help="measure the attention backward (local and distributed) instead of the forward")
+    ap.add_argument("--usp", action="store_true",
+                    help="measure the two-level Ulysses x Ring forward on its 256K-token workload")
     ap.add_argument("--overlap", action="store_true",
                     help="measure the unfused forward against the overlapped (chunked) forward")
     args = ap.parse_args()
@@ -537,6 +590,10 @@ def main():
     if args.overlap:
         if rank == 0:
             run_overlap(args)
+        return
+    if args.usp:
+        if rank == 0:
+            run_usp(args)
         return
     if args.backward:
         if rank == 0:

@@ -153,6 +153,36 @@ uly_status ulysses_dist_attn_fwd_overlap(int P, int b, int s, int h_q, int h_kv,
                                          cudaStream_t stream, cudaStream_t side_stream);
 
 /*
+ * The two-level forward, Ulysses inside groups and a ring across them ("长上下文训练中的
+ * SP 与 CP", section "组合与配置：区分算法组合和并行维度", subsection "Ulysses + Ring：组合两种
+ * Attention 路线": 256K tokens on 8 devices as Ulysses degree 4 x Ring degree 2;
+ * "02 · DeepSpeed-Ulysses", section 4 "a2a+p2p 分层 CP").  P = Pu * Pr ranks; rank
+ * j = g*Pu + u holds tokens [j*s/P, (j+1)*s/P) of every head, so ring group g (ranks
+ * g*Pu .. g*Pu+Pu-1) holds the contiguous segment g of s/Pr tokens.
+ *  1. all-to-all #1 inside every group: rank (g, u) gets segment g's tokens of heads
+ *     [u*h/Pu, (u+1)*h/Pu) (query and K/V heads alike);
+ *  2. every rank's queries attend over the whole sequence, taking the K/V of segment g'
+ *     from rank (g', u) -- the blocks a ring across the groups would pass to it
+ *     ("Ring Attention：Q 留在本地，KV 沿环传递") -- merged by the online softmax of the
+ *     attention kernel, with the causal mask on global positions;
+ *  3. all-to-all #2 inside every group.
+ * On one GPU the ring's transfers are reads of the other ranks' buffers (no copy).
+ *   q_seq / o_seq: P pointers to [b][s/P][h_q][d]; k_seq / v_seq: [b][s/P][h_kv][d].
+ * Sizes: Pu, Pr >= 1, Pu*Pr <= 64, s % (Pu*Pr) == 0, h_q % Pu == 0, h_kv % Pu == 0,
+ * h_q % h_kv == 0, else ULY_ERR_INVALID_ARG.  Kernel: ULY_BF16, d in {64, 128},
+ * Pu*Pr <= 16 and (s/Pr) % 128 == 0, else ULY_ERR_UNSUPPORTED.  The result equals
+ * ulysses_dist_attn_fwd over the same P ranks bit for bit.  workspace: 256-byte aligned,
+ * at least ulysses_usp_workspace_bytes(...) bytes (every rank's group head-layout Q, K,
+ * V, O).  Five kinds of launches: Pr exchanges in, one attention, Pr exchanges out.
+ */
+size_t ulysses_usp_workspace_bytes(int Pu, int Pr, int b, int s, int h_q, int h_kv, int d, uly_dtype dtype);
+uly_status ulysses_usp_attn_fwd(int Pu, int Pr, int b, int s, int h_q, int h_kv, int d, uly_dtype dtype,
+                                int causal,
+                                const void* const* q_seq, const void* const* k_seq,
+                                const void* const* v_seq, void* const* o_seq,
+                                void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * The unfused forward without any allocation by the caller or the library.  The paper has
  * no counterpart: this exists for callers that cannot call cudaMalloc -- for example an
  * application whose memory pool already holds all the device memory it may use, or a

@@ -24,7 +24,7 @@ __all__ = [
     "ulysses_status_string", "EXPORTED_SYMBOLS", "ulysses_dist_attn_fwd_noalloc", "NOALLOC_SCRATCH_BYTES",
     "ulysses_local_attention_fwd_lse", "ulysses_dist_attn_fwd_lse", "ulysses_attn_bwd_workspace_bytes",
     "ulysses_local_attention_bwd", "ulysses_dist_attn_bwd", "ulysses_dist_attn_overlap_workspace_bytes",
-    "ulysses_dist_attn_fwd_overlap",
+    "ulysses_dist_attn_fwd_overlap", "ulysses_usp_workspace_bytes", "ulysses_usp_attn_fwd",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -40,6 +40,7 @@ EXPORTED_SYMBOLS = (
     "ulysses_status_string", "ulysses_dist_attn_fwd_noalloc", "ulysses_local_attention_fwd_lse",
     "ulysses_dist_attn_fwd_lse", "ulysses_attn_bwd_workspace_bytes", "ulysses_local_attention_bwd",
     "ulysses_dist_attn_bwd", "ulysses_dist_attn_overlap_workspace_bytes", "ulysses_dist_attn_fwd_overlap",
+    "ulysses_usp_workspace_bytes", "ulysses_usp_attn_fwd",
 )
 
 _lock = threading.Lock()
@@ -95,6 +96,10 @@ def load_library():
         lib.ulysses_dist_attn_overlap_workspace_bytes.restype = sz
         lib.ulysses_dist_attn_fwd_overlap.argtypes = [i, i, i, i, i, i, i, i, pp, pp, pp, pp, vp, sz, i, vp, vp]
         lib.ulysses_dist_attn_fwd_overlap.restype = i
+        lib.ulysses_usp_workspace_bytes.argtypes = [i, i, i, i, i, i, i, i]
+        lib.ulysses_usp_workspace_bytes.restype = sz
+        lib.ulysses_usp_attn_fwd.argtypes = [i, i, i, i, i, i, i, i, i, pp, pp, pp, pp, vp, sz, vp]
+        lib.ulysses_usp_attn_fwd.restype = i
         lib.ulysses_device_status.argtypes = [i]
         lib.ulysses_device_status.restype = i
         lib.ulysses_status_string.argtypes = [i]
@@ -381,4 +386,34 @@ def ulysses_dist_attn_fwd_overlap(q_seq, k_seq, v_seq, causal, n_chunks=2, out_s
         P, b, s, hq, hkv, d, _dtype_code(q0), int(bool(causal)), _ptr_array(q_seq), _ptr_array(k_seq),
         _ptr_array(v_seq), _ptr_array(out_seq), workspace.data_ptr(), workspace.numel() * workspace.element_size(),
         int(n_chunks), _stream(stream), ctypes.c_void_p(side.cuda_stream)), "ulysses_dist_attn_fwd_overlap")
+    return out_seq
+
+
+# ------------------------------------------------------------------ Ulysses x Ring forward
+def ulysses_usp_workspace_bytes(Pu, Pr, b, s, h_q, h_kv, d, dtype):
+    return int(load_library().ulysses_usp_workspace_bytes(Pu, Pr, b, s, h_q, h_kv, d, _DTYPES[dtype]))
+
+
+def ulysses_usp_attn_fwd(q_seq, k_seq, v_seq, causal, Pu, Pr, out_seq=None, workspace=None, stream=None):
+    """The two-level forward over P = Pu*Pr seq-partitioned ranks (rank j = g*Pu + u):
+    all-to-all inside groups of Pu ranks, attention with the ring groups' K/V blocks,
+    all-to-all back.  Returns P tensors [b, s/P, h_q, d]."""
+    q0 = _same(q_seq, "q_seq")
+    k0 = _same(k_seq, "k_seq")
+    _same(v_seq, "v_seq")
+    P = len(q_seq)
+    if P != Pu * Pr:
+        raise ValueError(f"{P} ranks given for Pu={Pu} x Pr={Pr}")
+    b, S, hq, d = q0.shape
+    hkv = k0.shape[2]
+    s = S * P
+    if out_seq is None:
+        out_seq = [torch.empty_like(q) for q in q_seq]
+    if workspace is None:
+        need = ulysses_usp_workspace_bytes(Pu, Pr, b, s, hq, hkv, d, q0.dtype)
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q0.device)
+    _check(load_library().ulysses_usp_attn_fwd(
+        Pu, Pr, b, s, hq, hkv, d, _dtype_code(q0), int(bool(causal)), _ptr_array(q_seq), _ptr_array(k_seq),
+        _ptr_array(v_seq), _ptr_array(out_seq), workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+        _stream(stream)), "ulysses_usp_attn_fwd")
     return out_seq

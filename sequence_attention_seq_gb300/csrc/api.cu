@@ -606,6 +606,87 @@ uly_status ulysses_dist_attn_fwd_overlap(int P, int b, int s, int h_q, int h_kv,
     return ULY_OK;
 }
 
+size_t ulysses_usp_workspace_bytes(int Pu, int Pr, int b, int s, int h_q, int h_kv, int d, uly_dtype dtype) {
+    if (Pu < 1 || Pr < 1 || Pu * Pr > kMaxRanks || s % (Pu * Pr)) return 0;
+    if (check_attention_shape(Pu, b, s / Pr, h_q, h_kv, d, dtype) == ULY_ERR_INVALID_ARG) return 0;
+    const int e = elem_bytes(dtype), L = s / Pr;
+    const uint64_t qb = round256((uint64_t)b * L * (h_q / Pu) * d * e);
+    const uint64_t kb = round256((uint64_t)b * L * (h_kv / Pu) * d * e);
+    return (size_t)((uint64_t)Pu * Pr * (2 * qb + 2 * kb));
+}
+
+uly_status ulysses_usp_attn_fwd(int Pu, int Pr, int b, int s, int h_q, int h_kv, int d, uly_dtype dtype, int causal,
+                                const void* const* q_seq, const void* const* k_seq, const void* const* v_seq,
+                                void* const* o_seq, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    if (Pu < 1 || Pr < 1 || Pu * Pr > kMaxRanks || s < 1 || s % (Pu * Pr)) return ULY_ERR_INVALID_ARG;
+    const int P = Pu * Pr, L = s / Pr, S = s / P;
+    // heads split over the Ulysses degree only; the exchanges run inside each group of Pu ranks
+    uly_status st = check_attention_shape(Pu, b, L, h_q, h_kv, d, dtype);
+    if (st != ULY_OK) return st;
+    st = check_exchange_shape(Pu, b, L, h_q, d, dtype);
+    if (st != ULY_OK) return st;
+    st = check_exchange_shape(Pu, b, L, h_kv, d, dtype);
+    if (st != ULY_OK) return st;
+    if ((long long)b * h_q * ((s + 127) / 128) > 0x7fffffffLL) return ULY_ERR_INVALID_ARG;
+    if (dtype != ULY_BF16 || P > 16 || L % 128 != 0) return ULY_ERR_UNSUPPORTED;
+    const uint64_t qsb = (uint64_t)b * S * h_q * d * 2, ksb = (uint64_t)b * S * h_kv * d * 2;
+    std::vector<Range> rq, rk, rv, ro;
+    if (!collect(q_seq, P, qsb, rq) || !collect(k_seq, P, ksb, rk) || !collect(v_seq, P, ksb, rv) ||
+        !collect(reinterpret_cast<const void* const*>(o_seq), P, qsb, ro))
+        return ULY_ERR_INVALID_ARG;
+    if (overlaps(ro, rq) || overlaps(ro, rk) || overlaps(ro, rv) || self_overlap(ro)) return ULY_ERR_INVALID_ARG;
+    const size_t need = ulysses_usp_workspace_bytes(Pu, Pr, b, s, h_q, h_kv, d, dtype);
+    if (!workspace_ok(workspace, workspace_bytes, need)) return ULY_ERR_INVALID_ARG;
+    std::vector<Range> rw{{reinterpret_cast<uintptr_t>(workspace), reinterpret_cast<uintptr_t>(workspace) + need}};
+    if (overlaps(rw, rq) || overlaps(rw, rk) || overlaps(rw, rv) || overlaps(rw, ro)) return ULY_ERR_INVALID_ARG;
+
+    // workspace: per rank [Q | K | V | O] in head layout of its group: [b][s/Pr][h/Pu][d]
+    const Carve ws(workspace, {(uint64_t)b * L * (h_q / Pu) * d * 2, (uint64_t)b * L * (h_kv / Pu) * d * 2,
+                               (uint64_t)b * L * (h_kv / Pu) * d * 2, (uint64_t)b * L * (h_q / Pu) * d * 2});
+    uly::PermuteTensor* t = new uly::PermuteTensor[3];
+    cudaError_t ce = cudaSuccess;
+    // (1) all-to-all #1 inside every ring group of Pu consecutive ranks
+    for (int g = 0; g < Pr && ce == cudaSuccess; ++g) {
+        memset(t, 0, 3 * sizeof(uly::PermuteTensor));
+        const void* const* src[3] = {q_seq, k_seq, v_seq};
+        for (int k = 0; k < 3; ++k) {
+            for (int u = 0; u < Pu; ++u) {
+                t[k].src[u] = src[k][g * Pu + u];
+                t[k].dst[u] = ws.at(g * Pu + u, k);
+            }
+            t[k].h = k == 0 ? h_q : h_kv;
+        }
+        ce = uly::launch_permute(0, Pu, b, L, d, 2, t, 3, stream);
+    }
+    // (2) attention over the whole sequence: the ring's K/V blocks are read from the buffers
+    //     of the ranks that hold them
+    uly::AttnPtrs* head = new uly::AttnPtrs;
+    memset(head, 0, sizeof(uly::AttnPtrs));
+    for (int j = 0; j < P; ++j) {
+        head->q[j] = ws.at(j, 0);
+        head->k[j] = ws.at(j, 1);
+        head->v[j] = ws.at(j, 2);
+        head->o[j] = ws.at(j, 3);
+    }
+    int unsupported = 0;
+    if (ce == cudaSuccess) ce = uly::launch_attention_tc_usp(Pu, Pr, b, s, h_q, h_kv, d, causal, *head, stream,
+                                                             &unsupported);
+    delete head;
+    // (3) all-to-all #2 inside every ring group
+    for (int g = 0; g < Pr && ce == cudaSuccess && !unsupported; ++g) {
+        memset(t, 0, sizeof(uly::PermuteTensor));
+        for (int u = 0; u < Pu; ++u) {
+            t[0].src[u] = ws.at(g * Pu + u, 3);
+            t[0].dst[u] = o_seq[g * Pu + u];
+        }
+        t[0].h = h_q;
+        ce = uly::launch_permute(1, Pu, b, L, d, 2, t, 1, stream);
+    }
+    delete[] t;
+    if (unsupported) return ULY_ERR_UNSUPPORTED;
+    return ce == cudaSuccess ? ULY_OK : ULY_ERR_CUDA;
+}
+
 uly_status ulysses_device_status(int clear) {
     unsigned int v = 0;
     if (uly::read_device_error(&v, clear) != cudaSuccess) return ULY_ERR_CUDA;

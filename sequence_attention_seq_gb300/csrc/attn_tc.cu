@@ -69,7 +69,8 @@ struct TcParams {
     uint8_t* optr[kMaxMaps];  // output buffers (same indexing as the maps): [b][rows][heads][d] bf16
     float* lse[kMaxMaps];     // optional per-row log-sum-exp (natural log), [b][heads][rows]; unfused only
     int s;             // sequence length
-    int rows_per_map;  // tokens held by one map: s/P when fused, s otherwise
+    int rows_per_map;  // tokens held by one map: s/P when fused, s/Pr for the two-level forward, s otherwise
+    int map_stride;    // map index step from one token block to the next (Pu for the two-level forward, else 1)
     int n_qtiles;      // ceil(s / BM)
     int n_pairs;       // ceil(n_qtiles / 2)
     int heads;         // query heads per map group: h_q (fused) or h_q/P (per rank)
@@ -157,9 +158,14 @@ struct TileCoord {
     int row;  // token coordinate inside that map
 };
 
+// Token t0 of the global sequence, for the unit `rank` of a work item: the map (buffer)
+// holding it and its row there.  Unfused: map = rank, row = t0.  Fused: rank = 0 and the
+// map is the seq-layout rank t0 / (s/P).  Two-level (Ulysses x Ring): rank = u and the map
+// is ring group t0 / (s/Pr)'s rank u, i.e. the K/V blocks of the other ring groups are read
+// where those ranks hold them.
 __device__ __forceinline__ TileCoord tile_coord(const TcParams& p, int rank, int t0) {
     TileCoord c;
-    c.map = rank + t0 / p.rows_per_map;
+    c.map = rank + (t0 / p.rows_per_map) * p.map_stride;
     c.row = t0 % p.rows_per_map;
     return c;
 }
@@ -624,6 +630,7 @@ cudaError_t launch_attention_tc(int P, int b, int s, int h_q, int h_kv, int d, i
     TcParams* prm = new TcParams;
     memset(prm, 0, sizeof(TcParams));
     prm->s = s;
+    prm->map_stride = 1;
     prm->n_qtiles = (s + BM - 1) / BM;
     prm->n_pairs = (prm->n_qtiles + 1) / 2;
     prm->g = h_q / h_kv;
@@ -669,6 +676,44 @@ cudaError_t launch_attention_tc(int P, int b, int s, int h_q, int h_kv, int d, i
             prm->band_units = band_units_for(s, d, nr * b * Hk);
             err = d == 64 ? launch_d<64>(*prm, n_items, stream) : launch_d<128>(*prm, n_items, stream);
         }
+    }
+    delete prm;
+    return err;
+}
+
+cudaError_t launch_attention_tc_usp(int Pu, int Pr, int b, int s, int h_q, int h_kv, int d, int causal,
+                                    const AttnPtrs& head, cudaStream_t stream, int* unsupported) {
+    *unsupported = 0;
+    const int P = Pu * Pr, L = s / Pr;
+    if (!tc_attention_supported(d) || P > kMaxMaps || L % BM != 0) {
+        *unsupported = 1;
+        return cudaSuccess;
+    }
+    const int Hq = h_q / Pu, Hk = h_kv / Pu;
+    TcParams* prm = new TcParams;
+    memset(prm, 0, sizeof(TcParams));
+    prm->s = s;
+    prm->rows_per_map = L;
+    prm->map_stride = Pu;
+    prm->n_qtiles = s / BM;
+    prm->n_pairs = (prm->n_qtiles + 1) / 2;
+    prm->heads = Hq;
+    prm->g = Hq / Hk;
+    prm->b = b;
+    prm->nranks = Pu;
+    prm->causal = causal ? 1 : 0;
+    prm->scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)d));
+    cudaError_t err = cudaSuccess;
+    for (int j = 0; j < P && err == cudaSuccess; ++j) {
+        if (!make_map(&prm->mq[j], head.q[j], b, L, Hq, d, BM) || !make_map(&prm->mk[j], head.k[j], b, L, Hk, d, BN) ||
+            !make_map(&prm->mv[j], head.v[j], b, L, Hk, d, BN))
+            err = cudaErrorInvalidValue;
+        prm->optr[j] = static_cast<uint8_t*>(head.o[j]);
+    }
+    if (err == cudaSuccess) {
+        const long long n_items = (long long)Pu * b * Hq * prm->n_pairs;
+        prm->band_units = band_units_for(s, d, Pu * b * Hk);
+        err = d == 64 ? launch_d<64>(*prm, n_items, stream) : launch_d<128>(*prm, n_items, stream);
     }
     delete prm;
     return err;

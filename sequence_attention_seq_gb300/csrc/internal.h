@@ -45,6 +45,13 @@ int tc_attention_supported(int d);
 cudaError_t launch_attention_tc(int P, int b, int s, int h_q, int h_kv, int d, int causal, int fused,
                                 const AttnPtrs& ptrs, cudaStream_t stream, int* unsupported);
 
+// Two-level (Ulysses x Ring) attention: P = Pu*Pr head-layout buffers, buffer g*Pu + u
+// holding ring group g's s/Pr tokens of heads [u*h/Pu, (u+1)*h/Pu); every query attends
+// over the whole sequence, reading the K/V blocks of the other groups from their buffers.
+// Needs P <= 16 and (s/Pr) % 128 == 0 (else *unsupported = 1).
+cudaError_t launch_attention_tc_usp(int Pu, int Pr, int b, int s, int h_q, int h_kv, int d, int causal,
+                                    const AttnPtrs& head, cudaStream_t stream, int* unsupported);
+
 // Backward of the bf16 tensor-core attention (head layout per rank).  O and dO for the
 // row sums D are read from `o_rows` / `do_rows` in head layout, or in seq layout when
 // od_seq_layout != 0 (then indexed by seq rank j, not by head rank r).
