@@ -476,6 +476,9 @@ def run_backward(args):
             "dist_bwd": lambda: uly.ulysses_dist_attn_bwd(qs, ks, vs, o, dos, lse, causal, grads=grads_s,
                                                           workspace=ws_d),
         }
+        if P <= 16 and (s // P) % 128 == 0:  # the exchanges folded into the kernels' tile addressing
+            calls["dist_bwd_fused"] = lambda: uly.ulysses_dist_attn_bwd(qs, ks, vs, o, dos, lse, causal,
+                                                                        grads=grads_s, workspace=ws_l, fused=True)
         fl = 2.5 * attn_flops(b, s, hq, d, causal)
         for name, fn in calls.items():
             for _ in range(max(3, args.warmup)):

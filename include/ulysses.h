@@ -239,24 +239,25 @@ uly_status ulysses_local_attention_fwd_lse(int P, int b, int s, int h_q, int h_k
                                            float* const* lse, cudaStream_t stream);
 
 /*
- * ulysses_dist_attn_fwd (fused == 0, same workspace) plus the log-sum-exp of every head
- * rank's rows: lse[r] is indexed in head layout ([b][h_q/P][s], all s tokens of rank r's
- * heads), which is what ulysses_dist_attn_bwd takes back.
+ * ulysses_dist_attn_fwd (same workspace, same fused / unfused rules and bits) plus the
+ * log-sum-exp of every head rank's rows: lse[r] is indexed in head layout ([b][h_q/P][s],
+ * all s tokens of rank r's heads), which is what ulysses_dist_attn_bwd takes back.
  */
 uly_status ulysses_dist_attn_fwd_lse(int P, int b, int s, int h_q, int h_kv, int d, uly_dtype dtype,
                                      int causal,
                                      const void* const* q_seq, const void* const* k_seq,
                                      const void* const* v_seq, void* const* o_seq, float* const* lse,
-                                     void* workspace, size_t workspace_bytes, cudaStream_t stream);
+                                     void* workspace, size_t workspace_bytes, int fused,
+                                     cudaStream_t stream);
 
 /*
  * Bytes of workspace the backward needs: for every rank two fp32 row arrays
- * [b][h_q/P][ceil(s/128)*128] (L in base 2 and D), and, when dist != 0, the head-layout
- * copies of Q, K, V, dO, dQ, dK and dV; each array 256-byte aligned.  0 for arguments
- * that are invalid or unsupported.
+ * [b][h_q/P][ceil(s/128)*128] (L in base 2 and D), and, when dist != 0 and fused == 0,
+ * the head-layout copies of Q, K, V, dO, dQ, dK and dV; each array 256-byte aligned.
+ * 0 for arguments that are invalid or unsupported.
  */
 size_t ulysses_attn_bwd_workspace_bytes(int P, int b, int s, int h_q, int h_kv, int d, uly_dtype dtype,
-                                        int dist);
+                                        int dist, int fused);
 
 /*
  * Backward of ulysses_local_attention, head layout in and out.
@@ -265,7 +266,7 @@ size_t ulysses_attn_bwd_workspace_bytes(int P, int b, int s, int h_q, int h_kv, 
  *   lse: from ulysses_local_attention_fwd_lse on the same q, k (and causal flag).
  * Four launches: row statistics, dK/dV, dQ (one pair per 16 ranks).  Outputs must not
  * overlap each other, any input or the workspace (256-byte aligned, at least
- * ulysses_attn_bwd_workspace_bytes(..., dist = 0) bytes, owned by the caller).
+ * ulysses_attn_bwd_workspace_bytes(..., dist = 0, fused = 0) bytes, owned by the caller).
  */
 uly_status ulysses_local_attention_bwd(int P, int b, int s, int h_q, int h_kv, int d, uly_dtype dtype,
                                        int causal,
@@ -276,21 +277,26 @@ uly_status ulysses_local_attention_bwd(int P, int b, int s, int h_q, int h_kv, i
                                        void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
- * The whole DistributedAttention backward, seq layout in and out:
- *   all-to-all #1 on Q, K, V and dO (one launch), D from the seq-layout O and dO, the
- *   local backward of every rank, all-to-all #2 on dQ, dK and dV (one launch).
+ * The whole DistributedAttention backward, seq layout in and out.
+ * fused == 0: all-to-all #1 on Q, K, V and dO (one launch), D from the seq-layout O and
+ *   dO, the local backward of every rank, all-to-all #2 on dQ, dK and dV (one launch).
+ * fused != 0: D and the statistics, then the dK/dV and dQ kernels read their Q/K/V/dO
+ *   tiles straight from the seq-layout buffers and write dQ/dK/dV rows straight into the
+ *   seq-layout outputs, so no head-layout copy exists (the backward of the fused
+ *   forward).  Needs P <= 16 and (s/P) % 128 == 0, else ULY_ERR_UNSUPPORTED.  Both paths
+ *   give the same bits.
  *   q_seq, o_seq, do_seq, dq_seq: P pointers to [b][s/P][h_q][d];
  *   k_seq, v_seq, dk_seq, dv_seq: P pointers to [b][s/P][h_kv][d];
  *   lse: from ulysses_dist_attn_fwd_lse (head-layout indexed).
- * workspace: 256-byte aligned, at least ulysses_attn_bwd_workspace_bytes(..., dist = 1)
- * bytes.  Size and overlap rules as ulysses_local_attention_bwd plus the exchange rules.
+ * workspace: 256-byte aligned, at least ulysses_attn_bwd_workspace_bytes(..., dist = 1,
+ * fused) bytes.  Size and overlap rules as ulysses_local_attention_bwd plus the exchange rules.
  */
 uly_status ulysses_dist_attn_bwd(int P, int b, int s, int h_q, int h_kv, int d, uly_dtype dtype, int causal,
                                  const void* const* q_seq, const void* const* k_seq,
                                  const void* const* v_seq, const void* const* o_seq,
                                  const void* const* do_seq, const float* const* lse,
                                  void* const* dq_seq, void* const* dk_seq, void* const* dv_seq,
-                                 void* workspace, size_t workspace_bytes, cudaStream_t stream);
+                                 void* workspace, size_t workspace_bytes, int fused, cudaStream_t stream);
 
 /*
  * Reads (and, if clear != 0, resets) the library's device-side error word after

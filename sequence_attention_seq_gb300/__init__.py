@@ -84,14 +84,16 @@ def load_library():
         lib.ulysses_dist_attn_fwd_noalloc.restype = i
         lib.ulysses_local_attention_fwd_lse.argtypes = [i, i, i, i, i, i, i, i, pp, pp, pp, pp, pp, vp]
         lib.ulysses_local_attention_fwd_lse.restype = i
-        lib.ulysses_dist_attn_fwd_lse.argtypes = [i, i, i, i, i, i, i, i, pp, pp, pp, pp, pp, vp, sz, vp]
+        lib.ulysses_dist_attn_fwd_lse.argtypes = [i, i, i, i, i, i, i, i, pp, pp, pp, pp, pp, vp, sz, i, vp]
         lib.ulysses_dist_attn_fwd_lse.restype = i
-        lib.ulysses_attn_bwd_workspace_bytes.argtypes = [i, i, i, i, i, i, i, i]
+        lib.ulysses_attn_bwd_workspace_bytes.argtypes = [i, i, i, i, i, i, i, i, i]
         lib.ulysses_attn_bwd_workspace_bytes.restype = sz
-        for name in ("ulysses_local_attention_bwd", "ulysses_dist_attn_bwd"):
-            f = getattr(lib, name)
-            f.argtypes = [i, i, i, i, i, i, i, i, pp, pp, pp, pp, pp, pp, pp, pp, pp, vp, sz, vp]
-            f.restype = i
+        lib.ulysses_local_attention_bwd.argtypes = [i, i, i, i, i, i, i, i, pp, pp, pp, pp, pp, pp, pp, pp, pp, vp,
+                                                    sz, vp]
+        lib.ulysses_local_attention_bwd.restype = i
+        lib.ulysses_dist_attn_bwd.argtypes = [i, i, i, i, i, i, i, i, pp, pp, pp, pp, pp, pp, pp, pp, pp, vp, sz, i,
+                                              vp]
+        lib.ulysses_dist_attn_bwd.restype = i
         lib.ulysses_dist_attn_overlap_workspace_bytes.argtypes = [i, i, i, i, i, i, i, i]
         lib.ulysses_dist_attn_overlap_workspace_bytes.restype = sz
         lib.ulysses_dist_attn_fwd_overlap.argtypes = [i, i, i, i, i, i, i, i, pp, pp, pp, pp, vp, sz, i, vp, vp]
@@ -279,9 +281,10 @@ def ulysses_local_attention_fwd_lse(q_head, k_head, v_head, causal, out_head=Non
     return out_head, lse
 
 
-def ulysses_dist_attn_fwd_lse(q_seq, k_seq, v_seq, causal, out_seq=None, lse=None, workspace=None, stream=None):
-    """The unfused forward plus the log-sum-exp of every head rank's rows: returns (o_seq, lse)
-    with lse P fp32 tensors [b, h_q/P, s] indexed like the head layout."""
+def ulysses_dist_attn_fwd_lse(q_seq, k_seq, v_seq, causal, fused=False, out_seq=None, lse=None, workspace=None,
+                              stream=None):
+    """The forward plus the log-sum-exp of every head rank's rows: returns (o_seq, lse) with
+    lse P fp32 tensors [b, h_q/P, s] indexed like the head layout."""
     q0 = _same(q_seq, "q_seq")
     k0 = _same(k_seq, "k_seq")
     _same(v_seq, "v_seq")
@@ -293,22 +296,24 @@ def ulysses_dist_attn_fwd_lse(q_seq, k_seq, v_seq, causal, out_seq=None, lse=Non
         out_seq = [torch.empty_like(q) for q in q_seq]
     if lse is None:
         lse = [torch.empty((b, hq // P, s), dtype=torch.float32, device=q0.device) for _ in range(P)]
-    need = ulysses_dist_attn_workspace_bytes(P, b, s, hq, hkv, d, q0.dtype, False)
-    if workspace is None:
-        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q0.device)
+    need = ulysses_dist_attn_workspace_bytes(P, b, s, hq, hkv, d, q0.dtype, fused)
+    if workspace is None and need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q0.device)
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_len = workspace.numel() * workspace.element_size() if workspace is not None else 0
     _check(load_library().ulysses_dist_attn_fwd_lse(
         P, b, s, hq, hkv, d, _dtype_code(q0), int(bool(causal)), _ptr_array(q_seq), _ptr_array(k_seq),
-        _ptr_array(v_seq), _ptr_array(out_seq), _ptr_array(lse), workspace.data_ptr(),
-        workspace.numel() * workspace.element_size(), _stream(stream)), "ulysses_dist_attn_fwd_lse")
+        _ptr_array(v_seq), _ptr_array(out_seq), _ptr_array(lse), ws_ptr, ws_len, int(bool(fused)), _stream(stream)),
+        "ulysses_dist_attn_fwd_lse")
     return out_seq, lse
 
 
-def ulysses_attn_bwd_workspace_bytes(P, b, s, h_q, h_kv, d, dtype, dist):
+def ulysses_attn_bwd_workspace_bytes(P, b, s, h_q, h_kv, d, dtype, dist, fused=False):
     return int(load_library().ulysses_attn_bwd_workspace_bytes(P, b, s, h_q, h_kv, d, _DTYPES[dtype],
-                                                               int(bool(dist))))
+                                                               int(bool(dist)), int(bool(fused))))
 
 
-def _bwd_call(name, dist, q, k, v, o, do, lse, causal, grads, workspace, stream):
+def _bwd_call(name, dist, q, k, v, o, do, lse, causal, grads, workspace, stream, fused=False):
     q0 = _same(q, "q")
     k0 = _same(k, "k")
     _same(v, "v")
@@ -324,14 +329,16 @@ def _bwd_call(name, dist, q, k, v, o, do, lse, causal, grads, workspace, stream)
         hq, hkv = Hq * P, k0.shape[2] * P
     if grads is None:
         grads = ([torch.empty_like(x) for x in q], [torch.empty_like(x) for x in k], [torch.empty_like(x) for x in v])
-    need = ulysses_attn_bwd_workspace_bytes(P, b, s, hq, hkv, d, q0.dtype, dist)
+    need = ulysses_attn_bwd_workspace_bytes(P, b, s, hq, hkv, d, q0.dtype, dist, fused)
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q0.device)
     dq, dk, dv = grads
-    _check(getattr(load_library(), name)(
-        P, b, s, hq, hkv, d, _dtype_code(q0), int(bool(causal)), _ptr_array(q), _ptr_array(k), _ptr_array(v),
-        _ptr_array(o), _ptr_array(do), _ptr_array(lse), _ptr_array(dq), _ptr_array(dk), _ptr_array(dv),
-        workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream(stream)), name)
+    args = [P, b, s, hq, hkv, d, _dtype_code(q0), int(bool(causal)), _ptr_array(q), _ptr_array(k), _ptr_array(v),
+            _ptr_array(o), _ptr_array(do), _ptr_array(lse), _ptr_array(dq), _ptr_array(dk), _ptr_array(dv),
+            workspace.data_ptr(), workspace.numel() * workspace.element_size()]
+    if dist:
+        args.append(int(bool(fused)))
+    _check(getattr(load_library(), name)(*args, _stream(stream)), name)
     return dq, dk, dv
 
 
@@ -342,10 +349,12 @@ def ulysses_local_attention_bwd(q_head, k_head, v_head, o_head, do_head, lse, ca
                      grads, workspace, stream)
 
 
-def ulysses_dist_attn_bwd(q_seq, k_seq, v_seq, o_seq, do_seq, lse, causal, grads=None, workspace=None, stream=None):
-    """The DistributedAttention backward, seq layout in and out: returns (dq, dk, dv) seq layout."""
+def ulysses_dist_attn_bwd(q_seq, k_seq, v_seq, o_seq, do_seq, lse, causal, grads=None, workspace=None, stream=None,
+                          fused=False):
+    """The DistributedAttention backward, seq layout in and out: returns (dq, dk, dv) seq layout.
+    fused=True folds both exchanges into the kernels' tile addressing (same bits)."""
     return _bwd_call("ulysses_dist_attn_bwd", True, q_seq, k_seq, v_seq, o_seq, do_seq, lse, causal, grads,
-                     workspace, stream)
+                     workspace, stream, fused)
 
 
 # ------------------------------------------------------------------------- overlapped forward

@@ -177,21 +177,21 @@ struct Carve {
 };
 
 // Workspace of the backward: per rank the two fp32 row arrays (lse2, D), and for the
-// distributed backward the head-layout Q, K, V, dO, dQ, dK, dV.
+// unfused distributed backward the head-layout Q, K, V, dO, dQ, dK, dV.
 std::vector<uint64_t> bwd_sizes(int P, int b, int s, int hq, int hkv, int d, int dist) {
     const uint64_t ra = row_array_bytes(P, b, s, hq);
     std::vector<uint64_t> v{ra, ra};
-    if (dist) {
+    if (dist == 1) {
         const uint64_t qb = (uint64_t)b * s * (hq / P) * d * 2, kb = (uint64_t)b * s * (hkv / P) * d * 2;
         for (uint64_t x : {qb, kb, kb, qb, qb, kb, kb}) v.push_back(x);
     }
     return v;
 }
 
-uly_status run_backward(int P, int b, int s, int hq, int hkv, int d, int causal, int od_seq,
+uly_status run_backward(int P, int b, int s, int hq, int hkv, int d, int causal, int fused,
                         const uly::BwdPtrs& ptrs, cudaStream_t stream) {
     int unsupported = 0;
-    cudaError_t e = uly::launch_attention_bwd_tc(P, b, s, hq, hkv, d, causal, od_seq, ptrs, stream, &unsupported);
+    cudaError_t e = uly::launch_attention_bwd_tc(P, b, s, hq, hkv, d, causal, fused, ptrs, stream, &unsupported);
     if (unsupported) return ULY_ERR_UNSUPPORTED;
     return e == cudaSuccess ? ULY_OK : ULY_ERR_CUDA;
 }
@@ -227,7 +227,7 @@ uly_status dist_attn_fwd(int P, int b, int s, int h_q, int h_kv, int d, uly_dtyp
     if (overlaps(ro, rq) || overlaps(ro, rk) || overlaps(ro, rv) || self_overlap(ro)) return ULY_ERR_INVALID_ARG;
     std::vector<Range> rl;
     if (lse) {
-        if (fused || !collect_f(lse, P, (uint64_t)b * (h_q / P) * s * 4, rl)) return ULY_ERR_INVALID_ARG;
+        if (!collect_f(lse, P, (uint64_t)b * (h_q / P) * s * 4, rl)) return ULY_ERR_INVALID_ARG;
         if (self_overlap(rl) || overlaps(rl, rq) || overlaps(rl, rk) || overlaps(rl, rv) || overlaps(rl, ro))
             return ULY_ERR_INVALID_ARG;
     }
@@ -241,6 +241,7 @@ uly_status dist_attn_fwd(int P, int b, int s, int h_q, int h_kv, int d, uly_dtyp
             ptrs.k[r] = k_seq[r];
             ptrs.v[r] = v_seq[r];
             ptrs.o[r] = o_seq[r];
+            ptrs.lse[r] = lse ? lse[r] : nullptr;
         }
         return run_attention(P, b, s, h_q, h_kv, d, dtype, causal, 1, ptrs, stream);
     }
@@ -340,21 +341,22 @@ uly_status ulysses_dist_attn_fwd(int P, int b, int s, int h_q, int h_kv, int d, 
 uly_status ulysses_dist_attn_fwd_lse(int P, int b, int s, int h_q, int h_kv, int d, uly_dtype dtype, int causal,
                                      const void* const* q_seq, const void* const* k_seq, const void* const* v_seq,
                                      void* const* o_seq, float* const* lse, void* workspace, size_t workspace_bytes,
-                                     cudaStream_t stream) {
+                                     int fused, cudaStream_t stream) {
     uly_status st = check_train_shape(P, b, s, h_q, h_kv, d, dtype);
     if (st != ULY_OK) return st;
     if (!lse) return ULY_ERR_INVALID_ARG;
     return dist_attn_fwd(P, b, s, h_q, h_kv, d, dtype, causal, q_seq, k_seq, v_seq, o_seq, lse, workspace,
-                         workspace_bytes, 0, stream);
+                         workspace_bytes, fused, stream);
 }
 
-size_t ulysses_attn_bwd_workspace_bytes(int P, int b, int s, int h_q, int h_kv, int d, uly_dtype dtype, int dist) {
+size_t ulysses_attn_bwd_workspace_bytes(int P, int b, int s, int h_q, int h_kv, int d, uly_dtype dtype, int dist,
+                                        int fused) {
     if (check_train_shape(P, b, s, h_q, h_kv, d, dtype) != ULY_OK) return 0;
     if (dist && (check_exchange_shape(P, b, s, h_q, d, dtype) != ULY_OK ||
                  check_exchange_shape(P, b, s, h_kv, d, dtype) != ULY_OK))
         return 0;
     uint64_t per_rank = 0;
-    for (uint64_t x : bwd_sizes(P, b, s, h_q, h_kv, d, dist)) per_rank += round256(x);
+    for (uint64_t x : bwd_sizes(P, b, s, h_q, h_kv, d, dist && !fused ? 1 : 0)) per_rank += round256(x);
     return (size_t)(per_rank * P);
 }
 
@@ -379,7 +381,7 @@ uly_status ulysses_local_attention_bwd(int P, int b, int s, int h_q, int h_kv, i
     outs.insert(outs.end(), rdk.begin(), rdk.end());
     outs.insert(outs.end(), rdv.begin(), rdv.end());
     if (self_overlap(outs) || overlaps(outs, in)) return ULY_ERR_INVALID_ARG;
-    const size_t need = ulysses_attn_bwd_workspace_bytes(P, b, s, h_q, h_kv, d, dtype, 0);
+    const size_t need = ulysses_attn_bwd_workspace_bytes(P, b, s, h_q, h_kv, d, dtype, 0, 0);
     if (!workspace_ok(workspace, workspace_bytes, need)) return ULY_ERR_INVALID_ARG;
     std::vector<Range> rw{{reinterpret_cast<uintptr_t>(workspace), reinterpret_cast<uintptr_t>(workspace) + need}};
     if (overlaps(rw, in) || overlaps(rw, outs)) return ULY_ERR_INVALID_ARG;
@@ -400,6 +402,7 @@ uly_status ulysses_local_attention_bwd(int P, int b, int s, int h_q, int h_kv, i
         p->lse2[r] = static_cast<float*>(ws.at(r, 0));
         p->dsum[r] = static_cast<float*>(ws.at(r, 1));
     }
+    p->od_seq_layout = 0;
     st = run_backward(P, b, s, h_q, h_kv, d, causal, 0, *p, stream);
     delete p;
     return st;
@@ -409,7 +412,7 @@ uly_status ulysses_dist_attn_bwd(int P, int b, int s, int h_q, int h_kv, int d, 
                                  const void* const* q_seq, const void* const* k_seq, const void* const* v_seq,
                                  const void* const* o_seq, const void* const* do_seq, const float* const* lse,
                                  void* const* dq_seq, void* const* dk_seq, void* const* dv_seq, void* workspace,
-                                 size_t workspace_bytes, cudaStream_t stream) {
+                                 size_t workspace_bytes, int fused, cudaStream_t stream) {
     uly_status st = check_train_shape(P, b, s, h_q, h_kv, d, dtype);
     if (st != ULY_OK) return st;
     st = check_exchange_shape(P, b, s, h_q, d, dtype);
@@ -430,10 +433,36 @@ uly_status ulysses_dist_attn_bwd(int P, int b, int s, int h_q, int h_kv, int d, 
     outs.insert(outs.end(), rdk.begin(), rdk.end());
     outs.insert(outs.end(), rdv.begin(), rdv.end());
     if (self_overlap(outs) || overlaps(outs, in)) return ULY_ERR_INVALID_ARG;
-    const size_t need = ulysses_attn_bwd_workspace_bytes(P, b, s, h_q, h_kv, d, dtype, 1);
+    if (fused && (P > 16 || S % 128 != 0)) return ULY_ERR_UNSUPPORTED;
+    const size_t need = ulysses_attn_bwd_workspace_bytes(P, b, s, h_q, h_kv, d, dtype, 1, fused);
     if (!workspace_ok(workspace, workspace_bytes, need)) return ULY_ERR_INVALID_ARG;
     std::vector<Range> rw{{reinterpret_cast<uintptr_t>(workspace), reinterpret_cast<uintptr_t>(workspace) + need}};
     if (overlaps(rw, in) || overlaps(rw, outs)) return ULY_ERR_INVALID_ARG;
+    if (fused) {
+        // one launch chain: statistics, then the two kernels read Q/K/V/dO from the seq-layout
+        // buffers and write dQ/dK/dV into them through their tile addressing
+        const Carve ws(workspace, bwd_sizes(P, b, s, h_q, h_kv, d, 0));
+        uly::BwdPtrs* p = new uly::BwdPtrs;
+        memset(p, 0, sizeof(uly::BwdPtrs));
+        for (int r = 0; r < P; ++r) {
+            p->q[r] = q_seq[r];
+            p->k[r] = k_seq[r];
+            p->v[r] = v_seq[r];
+            p->dout[r] = do_seq[r];
+            p->o_rows[r] = o_seq[r];
+            p->do_rows[r] = do_seq[r];
+            p->lse[r] = lse[r];
+            p->dq[r] = dq_seq[r];
+            p->dk[r] = dk_seq[r];
+            p->dv[r] = dv_seq[r];
+            p->lse2[r] = static_cast<float*>(ws.at(r, 0));
+            p->dsum[r] = static_cast<float*>(ws.at(r, 1));
+        }
+        p->od_seq_layout = 1;
+        st = run_backward(P, b, s, h_q, h_kv, d, causal, 1, *p, stream);
+        delete p;
+        return st;
+    }
     const Carve ws(workspace, bwd_sizes(P, b, s, h_q, h_kv, d, 1));
     enum { LSE2, DSUM, QH, KH, VH, DOH, DQH, DKH, DVH };
     // (1) all-to-all #1 on Q, K, V and dO (the backward of all-to-all #2 is all-to-all #1)
@@ -468,7 +497,8 @@ uly_status ulysses_dist_attn_bwd(int P, int b, int s, int h_q, int h_kv, int d, 
         p->lse2[r] = static_cast<float*>(ws.at(r, LSE2));
         p->dsum[r] = static_cast<float*>(ws.at(r, DSUM));
     }
-    st = run_backward(P, b, s, h_q, h_kv, d, causal, 1, *p, stream);
+    p->od_seq_layout = 1;
+    st = run_backward(P, b, s, h_q, h_kv, d, causal, 0, *p, stream);
     delete p;
     if (st != ULY_OK) return st;
     // (3) all-to-all #2 on dQ, dK, dV (the backward of all-to-all #1)

@@ -52,17 +52,38 @@ constexpr int kRowsQ = 8;    // dQ kernel: 8 and 16 measure the same; 8 needs fe
 constexpr int kRingKV = 5;   // dK/dV kernel: Q/dO ring slots
 constexpr int kRingQ = 5;    // dQ kernel: K/V ring slots
 
+// Maps and gradient buffers are indexed like the forward's: token t of the sequence, for
+// the unit `rank` of a CTA, lives in buffer rank + t / rows_per_map at row t % rows_per_map.
+// Unfused: one buffer per head rank (rows_per_map = s, hq/hkv = that rank's heads).  Fused:
+// one buffer per seq rank (rows_per_map = s/P, hq/hkv = all heads, rank = 0), so the
+// exchanges happen in the tile addressing.  The row statistics always live per head rank:
+// head h of a CTA belongs to head rank rank + h / hq_rank, local head h % hq_rank.
 struct BwdParams {
     CUtensorMap mq[kMaxMaps], mk[kMaxMaps], mv[kMaxMaps], mdo[kMaxMaps];
-    uint8_t* dq[kMaxMaps];        // [b][s][hq][d] bf16 (head layout of the rank)
-    uint8_t* dk[kMaxMaps];        // [b][s][hkv][d] bf16
+    uint8_t* dq[kMaxMaps];        // [b][rows][hq][d] bf16
+    uint8_t* dk[kMaxMaps];        // [b][rows][hkv][d] bf16
     uint8_t* dv[kMaxMaps];
-    const float* lse2[kMaxMaps];  // [b][hq][s_pad]: log-sum-exp in base-2 units (+inf on padding)
-    const float* dsum[kMaxMaps];  // [b][hq][s_pad]: D (0 on padding)
+    const float* lse2[kMaxMaps];  // per head rank [b][hq_rank][s_pad]: log-sum-exp, base-2 units (+inf on padding)
+    const float* dsum[kMaxMaps];  // per head rank [b][hq_rank][s_pad]: D (0 on padding)
     int s, s_pad, n_tiles, hq, hkv, g, b, causal;
+    int rows_per_map;             // s (unfused) or s/P (fused)
+    int hq_rank;                  // query heads per head rank
     float scale_log2;             // log2(e)/sqrt(d)
     float scale;                  // 1/sqrt(d)
 };
+
+struct BwdTok {
+    int map, row;
+};
+__device__ __forceinline__ BwdTok bwd_tok(const BwdParams& p, int rank, int t0) {
+    return BwdTok{rank + t0 / p.rows_per_map, t0 % p.rows_per_map};
+}
+
+// Row statistics of (batch bb, query head h of the CTA's unit `rank`), from query q0 on.
+__device__ __forceinline__ size_t bwd_stat_off(const BwdParams& p, int bb, int h, int q0) {
+    return ((size_t)bb * p.hq_rank + h % p.hq_rank) * p.s_pad + q0;
+}
+__device__ __forceinline__ int bwd_stat_rank(const BwdParams& p, int rank, int h) { return rank + h / p.hq_rank; }
 
 // ------------------------------------------------------------------------- prep
 struct PrepParams {
@@ -245,14 +266,13 @@ __global__ void __launch_bounds__(RowCfg<RW>::kThreads, 1) bwd_dkdv_kernel(const
     const uint32_t tmem = sh->tmem_base;
 
     if (warp == kBwdProducer) {
-        const CUtensorMap* mq = &p.mq[rank];
-        const CUtensorMap* mdo = &p.mdo[rank];
-        // the fixed tiles: K (A) and V (B) of this key tile; map_of gives Q then dO per step
+        // the fixed tiles: K (A) and V (B) of this key tile; then Q and dO per step
+        const BwdTok kp = bwd_tok(p, rank, k0);
         mbar_arrive_expect_tx_warp(&bars[FIX], 2 * L::kTile);
 #pragma unroll
         for (int c = 0; c < D / 64; ++c) {
-            tma_load_4d_warp(sbase + L::offFixA + c * kSlab, &p.mk[rank], &bars[FIX], c * 64, kvh, k0, bb);
-            tma_load_4d_warp(sbase + L::offFixB + c * kSlab, &p.mv[rank], &bars[FIX], c * 64, kvh, k0, bb);
+            tma_load_4d_warp(sbase + L::offFixA + c * kSlab, &p.mk[kp.map], &bars[FIX], c * 64, kvh, kp.row, bb);
+            tma_load_4d_warp(sbase + L::offFixB + c * kSlab, &p.mv[kp.map], &bars[FIX], c * 64, kvh, kp.row, bb);
         }
         int issued = 0;
         bool ok = true;
@@ -261,11 +281,12 @@ __global__ void __launch_bounds__(RowCfg<RW>::kThreads, 1) bwd_dkdv_kernel(const
             ok = wait_phase_warp(&bars[EMPTY + slot], ((m / kRingKV) & 1) ^ 1, sh);
             if (!ok) break;
             const int n = m >> 1;
+            const BwdTok qp = bwd_tok(p, rank, step_qt(n) * 128);
             mbar_arrive_expect_tx_warp(&bars[FULL + slot], L::kTile);
 #pragma unroll
             for (int c = 0; c < D / 64; ++c)
-                tma_load_4d_warp(sbase + L::offRing + slot * L::kTile + c * kSlab, (m & 1) ? mdo : mq,
-                                 &bars[FULL + slot], c * 64, step_head(n), step_qt(n) * 128, bb);
+                tma_load_4d_warp(sbase + L::offRing + slot * L::kTile + c * kSlab, (m & 1) ? &p.mdo[qp.map] : &p.mq[qp.map],
+                                 &bars[FULL + slot], c * 64, step_head(n), qp.row, bb);
             ++issued;
         }
         if (!ok) {
@@ -331,18 +352,20 @@ __global__ void __launch_bounds__(RowCfg<RW>::kThreads, 1) bwd_dkdv_kernel(const
         const uint32_t tS = tmem + lane_off + cg * kColW, tdP = tmem + 128u + lane_off + cg * kColW;
         const float sc = p.scale_log2;
         auto stat_off = [&](int n) {  // offset of step n's first row statistic of this warp
-            return ((size_t)bb * p.hq + step_head(n)) * p.s_pad + step_qt(n) * 128 + cg * kColW;
+            return bwd_stat_off(p, bb, step_head(n), step_qt(n) * 128 + cg * kColW);
         };
         bool ok = true;
         for (int n = 0; n < n_steps; ++n) {
             const int qt = step_qt(n);
             const int qb = qt * 128 + cg * kColW;  // first query column of this warp
             const size_t vbase = stat_off(n);
-            const float4* l4 = reinterpret_cast<const float4*>(p.lse2[rank] + vbase);
-            const float4* d4 = reinterpret_cast<const float4*>(p.dsum[rank] + vbase);
+            const int sr = bwd_stat_rank(p, rank, step_head(n));
+            const float4* l4 = reinterpret_cast<const float4*>(p.lse2[sr] + vbase);
+            const float4* d4 = reinterpret_cast<const float4*>(p.dsum[sr] + vbase);
             if (n + 1 < n_steps && lane < 2 * kChunks) {  // next step's statistics: one 128-byte line per lane
                 const size_t nb = stat_off(n + 1) + (lane % kChunks) * 32;
-                prefetch_l1(lane < kChunks ? p.lse2[rank] + nb : p.dsum[rank] + nb);
+                const int nr = bwd_stat_rank(p, rank, step_head(n + 1));
+                prefetch_l1(lane < kChunks ? p.lse2[nr] + nb : p.dsum[nr] + nb);
             }
             const bool diag = p.causal && qt == kt;
             float pf[kColW];
@@ -421,9 +444,11 @@ __global__ void __launch_bounds__(RowCfg<RW>::kThreads, 1) bwd_dkdv_kernel(const
         if (ok && cg * kEpi < D) {
             tc_fence_after();
             const bool kok = key < p.s;
-            const size_t off = (((size_t)bb * p.s + (kok ? key : 0)) * p.hkv + kvh) * (size_t)D * 2 + cg * kEpi * 2;
-            store_row_bf16<kEpi>(tmem + 256u + lane_off + cg * kEpi, p.dk[rank] + off, p.scale, kok);
-            store_row_bf16<kEpi>(tmem + 384u + lane_off + cg * kEpi, p.dv[rank] + off, 1.0f, kok);
+            const BwdTok kt_ = bwd_tok(p, rank, kok ? key : k0);
+            const size_t off =
+                (((size_t)bb * p.rows_per_map + kt_.row) * p.hkv + kvh) * (size_t)D * 2 + cg * kEpi * 2;
+            store_row_bf16<kEpi>(tmem + 256u + lane_off + cg * kEpi, p.dk[kt_.map] + off, p.scale, kok);
+            store_row_bf16<kEpi>(tmem + 384u + lane_off + cg * kEpi, p.dv[kt_.map] + off, 1.0f, kok);
         }
     }
     tc_fence_before();
@@ -473,13 +498,12 @@ __global__ void __launch_bounds__(RowCfg<RW>::kThreads, 1) bwd_dq_kernel(const _
     auto sbuf = [tmem](int n) { return tmem + ((n & 1) ? 384u : 0u); };
 
     if (warp == kBwdProducer) {
-        const CUtensorMap* mk = &p.mk[rank];
-        const CUtensorMap* mv = &p.mv[rank];
+        const BwdTok qp = bwd_tok(p, rank, q0);
         mbar_arrive_expect_tx_warp(&bars[FIX], 2 * L::kTile);
 #pragma unroll
         for (int c = 0; c < D / 64; ++c) {
-            tma_load_4d_warp(sbase + L::offFixA + c * kSlab, &p.mq[rank], &bars[FIX], c * 64, hh, q0, bb);
-            tma_load_4d_warp(sbase + L::offFixB + c * kSlab, &p.mdo[rank], &bars[FIX], c * 64, hh, q0, bb);
+            tma_load_4d_warp(sbase + L::offFixA + c * kSlab, &p.mq[qp.map], &bars[FIX], c * 64, hh, qp.row, bb);
+            tma_load_4d_warp(sbase + L::offFixB + c * kSlab, &p.mdo[qp.map], &bars[FIX], c * 64, hh, qp.row, bb);
         }
         int issued = 0;
         bool ok = true;
@@ -487,11 +511,12 @@ __global__ void __launch_bounds__(RowCfg<RW>::kThreads, 1) bwd_dq_kernel(const _
             const int slot = m % kRingQ;
             ok = wait_phase_warp(&bars[EMPTY + slot], ((m / kRingQ) & 1) ^ 1, sh);
             if (!ok) break;
+            const BwdTok kp = bwd_tok(p, rank, (m >> 1) * 128);
             mbar_arrive_expect_tx_warp(&bars[FULL + slot], L::kTile);
 #pragma unroll
             for (int c = 0; c < D / 64; ++c)
-                tma_load_4d_warp(sbase + L::offRing + slot * L::kTile + c * kSlab, (m & 1) ? mv : mk,
-                                 &bars[FULL + slot], c * 64, kvh, (m >> 1) * 128, bb);
+                tma_load_4d_warp(sbase + L::offRing + slot * L::kTile + c * kSlab, (m & 1) ? &p.mv[kp.map] : &p.mk[kp.map],
+                                 &bars[FULL + slot], c * 64, kvh, kp.row, bb);
             ++issued;
         }
         if (!ok) {
@@ -560,9 +585,10 @@ __global__ void __launch_bounds__(RowCfg<RW>::kThreads, 1) bwd_dq_kernel(const _
         const int sub = warp & 3, cg = warp >> 2;
         const int row = sub * 32 + lane, qrow = q0 + row;
         const uint32_t lane_off = (uint32_t)(sub * 32) << 16;
-        const size_t vi = ((size_t)bb * p.hq + hh) * p.s_pad + qrow;  // qrow < s_pad always
-        const float neg_l = -p.lse2[rank][vi];
-        const float neg_d = -p.dsum[rank][vi];
+        const size_t vi = bwd_stat_off(p, bb, hh, qrow);  // qrow < s_pad always
+        const int sr = bwd_stat_rank(p, rank, hh);
+        const float neg_l = -p.lse2[sr][vi];
+        const float neg_d = -p.dsum[sr][vi];
         const float sc = p.scale_log2;
         const int lim = p.causal ? min(p.s, qrow + 1) : p.s;  // keys < lim are visible
         bool ok = true;
@@ -623,8 +649,10 @@ __global__ void __launch_bounds__(RowCfg<RW>::kThreads, 1) bwd_dq_kernel(const _
         if (ok && cg * kEpi < D) {
             tc_fence_after();
             const bool qok = qrow < p.s;
-            const size_t off = (((size_t)bb * p.s + (qok ? qrow : 0)) * p.hq + hh) * (size_t)D * 2 + cg * kEpi * 2;
-            store_row_bf16<kEpi>(tmem + 256u + lane_off + cg * kEpi, p.dq[rank] + off, p.scale, qok);
+            const BwdTok qt_ = bwd_tok(p, rank, qok ? qrow : q0);
+            const size_t off =
+                (((size_t)bb * p.rows_per_map + qt_.row) * p.hq + hh) * (size_t)D * 2 + cg * kEpi * 2;
+            store_row_bf16<kEpi>(tmem + 256u + lane_off + cg * kEpi, p.dq[qt_.map] + off, p.scale, qok);
         }
     }
     tc_fence_before();

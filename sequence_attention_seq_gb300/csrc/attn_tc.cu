@@ -67,7 +67,8 @@ struct TcParams {
     CUtensorMap mk[kMaxMaps];
     CUtensorMap mv[kMaxMaps];
     uint8_t* optr[kMaxMaps];  // output buffers (same indexing as the maps): [b][rows][heads][d] bf16
-    float* lse[kMaxMaps];     // optional per-row log-sum-exp (natural log), [b][heads][rows]; unfused only
+    float* lse[kMaxMaps];     // optional per-row log-sum-exp (natural log), per head rank [b][lse_heads][s]
+    int lse_heads;            // query heads per head rank: the heads of one lse array
     int s;             // sequence length
     int rows_per_map;  // tokens held by one map: s/P when fused, s/Pr for the two-level forward, s otherwise
     int map_stride;    // map index step from one token block to the next (Pu for the two-level forward, else 1)
@@ -530,8 +531,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
                     if (row_ok) *reinterpret_cast<uint4*>(orow + (c * 32 + q4 * 8) * 2) = v;
                 }
             }
-            if (p.lse[oc.map] && row_ok)  // log-sum-exp of the scaled scores, natural log
-                p.lse[oc.map][((size_t)it.bb * p.heads + it.head) * p.rows_per_map + oc.row + row] =
+            // log-sum-exp of the scaled scores, natural log, in the head rank's [b][h/P][s] array:
+            // unfused, the item's rank is the head rank; fused, the head is global
+            const int lr = it.rank + it.head / p.lse_heads, lh = it.head % p.lse_heads;
+            if (p.lse[lr] && row_ok)
+                p.lse[lr][((size_t)it.bb * p.lse_heads + lh) * p.s + qrow] =
                     (m_ref + log2f(l_sum)) * 0.6931471805599453f;
             tc_fence_before();
             __syncwarp();
@@ -623,7 +627,7 @@ cudaError_t launch_attention_tc(int P, int b, int s, int h_q, int h_kv, int d, i
                                 const AttnPtrs& ptrs, cudaStream_t stream, int* unsupported) {
     *unsupported = 0;
     const bool want_lse = ptrs.lse[0] != nullptr;
-    if (!tc_attention_supported(d) || (fused && (P > kMaxMaps || (s / P) % BM != 0 || want_lse))) {
+    if (!tc_attention_supported(d) || (fused && (P > kMaxMaps || (s / P) % BM != 0))) {
         *unsupported = 1;
         return cudaSuccess;
     }
@@ -642,6 +646,7 @@ cudaError_t launch_attention_tc(int P, int b, int s, int h_q, int h_kv, int d, i
         const int S = s / P;
         prm->rows_per_map = S;
         prm->heads = h_q;
+        prm->lse_heads = h_q / P;  // the statistics go to the head ranks' arrays
         prm->nranks = 1;
         for (int j = 0; j < P && err == cudaSuccess; ++j) {
             if (!make_map(&prm->mq[j], ptrs.q[j], b, S, h_q, d, BM) ||
@@ -649,6 +654,7 @@ cudaError_t launch_attention_tc(int P, int b, int s, int h_q, int h_kv, int d, i
                 !make_map(&prm->mv[j], ptrs.v[j], b, S, h_kv, d, BN))
                 err = cudaErrorInvalidValue;
             prm->optr[j] = static_cast<uint8_t*>(ptrs.o[j]);
+            prm->lse[j] = want_lse ? ptrs.lse[j] : nullptr;
         }
         if (err == cudaSuccess) {
             const long long n_items = (long long)b * h_q * prm->n_pairs;
@@ -659,6 +665,7 @@ cudaError_t launch_attention_tc(int P, int b, int s, int h_q, int h_kv, int d, i
         const int Hq = h_q / P, Hk = h_kv / P;
         prm->rows_per_map = s;
         prm->heads = Hq;
+        prm->lse_heads = Hq;
         for (int r0 = 0; r0 < P && err == cudaSuccess; r0 += kMaxMaps) {
             const int nr = (P - r0) < kMaxMaps ? (P - r0) : kMaxMaps;
             prm->nranks = nr;
@@ -698,6 +705,7 @@ cudaError_t launch_attention_tc_usp(int Pu, int Pr, int b, int s, int h_q, int h
     prm->n_qtiles = s / BM;
     prm->n_pairs = (prm->n_qtiles + 1) / 2;
     prm->heads = Hq;
+    prm->lse_heads = Hq;  // no statistics are written by this launch
     prm->g = Hq / Hk;
     prm->b = b;
     prm->nranks = Pu;
@@ -719,10 +727,10 @@ cudaError_t launch_attention_tc_usp(int Pu, int Pr, int b, int s, int h_q, int h
     return err;
 }
 
-cudaError_t launch_attention_bwd_tc(int P, int b, int s, int h_q, int h_kv, int d, int causal, int od_seq_layout,
+cudaError_t launch_attention_bwd_tc(int P, int b, int s, int h_q, int h_kv, int d, int causal, int fused,
                                     const BwdPtrs& ptrs, cudaStream_t stream, int* unsupported) {
     *unsupported = 0;
-    if (!tc_attention_supported(d)) {
+    if (!tc_attention_supported(d) || (fused && (P > kMaxMaps || (s / P) % 128 != 0))) {
         *unsupported = 1;
         return cudaSuccess;
     }
@@ -745,7 +753,7 @@ cudaError_t launch_attention_bwd_tc(int P, int b, int s, int h_q, int h_kv, int 
     pp->d = d;
     pp->S = s / P;
     pp->hq_total = h_q;
-    pp->seq_layout = od_seq_layout ? 1 : 0;
+    pp->seq_layout = ptrs.od_seq_layout ? 1 : 0;
     pp->lanes_log2 = d == 64 ? 3 : 4;
     pp->rows = (long long)P * b * Hq * pp->s_pad;
     const long long threads = pp->rows << pp->lanes_log2;
@@ -753,36 +761,59 @@ cudaError_t launch_attention_bwd_tc(int P, int b, int s, int h_q, int h_kv, int 
     delete pp;
     cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess) return err;
-    // (2) dK/dV and dQ, up to kMaxMaps ranks per launch pair
+    // (2) dK/dV and dQ: one launch pair over seq-layout buffers (fused), else up to kMaxMaps
+    //     head ranks per launch pair
     BwdParams* prm = new BwdParams;
     memset(prm, 0, sizeof(BwdParams));
     prm->s = s;
     prm->s_pad = n_tiles * 128;
     prm->n_tiles = n_tiles;
-    prm->hq = Hq;
-    prm->hkv = Hk;
-    prm->g = Hq / Hk;
+    prm->g = h_q / h_kv;
     prm->b = b;
     prm->causal = causal ? 1 : 0;
+    prm->hq_rank = Hq;
     prm->scale = (float)(1.0 / std::sqrt((double)d));
     prm->scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)d));
-    for (int r0 = 0; r0 < P && err == cudaSuccess; r0 += kMaxMaps) {
-        const int nr = (P - r0) < kMaxMaps ? (P - r0) : kMaxMaps;
-        for (int i = 0; i < nr && err == cudaSuccess; ++i) {
-            const int r = r0 + i;
-            if (!make_map(&prm->mq[i], ptrs.q[r], b, s, Hq, d, 128) ||
-                !make_map(&prm->mk[i], ptrs.k[r], b, s, Hk, d, 128) ||
-                !make_map(&prm->mv[i], ptrs.v[r], b, s, Hk, d, 128) ||
-                !make_map(&prm->mdo[i], ptrs.dout[r], b, s, Hq, d, 128))
+    if (fused) {
+        const int S = s / P;
+        prm->rows_per_map = S;
+        prm->hq = h_q;
+        prm->hkv = h_kv;
+        for (int j = 0; j < P && err == cudaSuccess; ++j) {
+            if (!make_map(&prm->mq[j], ptrs.q[j], b, S, h_q, d, 128) ||
+                !make_map(&prm->mk[j], ptrs.k[j], b, S, h_kv, d, 128) ||
+                !make_map(&prm->mv[j], ptrs.v[j], b, S, h_kv, d, 128) ||
+                !make_map(&prm->mdo[j], ptrs.dout[j], b, S, h_q, d, 128))
                 err = cudaErrorInvalidValue;
-            prm->dq[i] = static_cast<uint8_t*>(ptrs.dq[r]);
-            prm->dk[i] = static_cast<uint8_t*>(ptrs.dk[r]);
-            prm->dv[i] = static_cast<uint8_t*>(ptrs.dv[r]);
-            prm->lse2[i] = ptrs.lse2[r];
-            prm->dsum[i] = ptrs.dsum[r];
+            prm->dq[j] = static_cast<uint8_t*>(ptrs.dq[j]);
+            prm->dk[j] = static_cast<uint8_t*>(ptrs.dk[j]);
+            prm->dv[j] = static_cast<uint8_t*>(ptrs.dv[j]);
+            prm->lse2[j] = ptrs.lse2[j];  // head rank j's statistics
+            prm->dsum[j] = ptrs.dsum[j];
         }
-        if (err != cudaSuccess) break;
-        err = d == 64 ? launch_bwd_d<64>(*prm, nr, stream) : launch_bwd_d<128>(*prm, nr, stream);
+        if (err == cudaSuccess) err = d == 64 ? launch_bwd_d<64>(*prm, 1, stream) : launch_bwd_d<128>(*prm, 1, stream);
+    } else {
+        prm->rows_per_map = s;
+        prm->hq = Hq;
+        prm->hkv = Hk;
+        for (int r0 = 0; r0 < P && err == cudaSuccess; r0 += kMaxMaps) {
+            const int nr = (P - r0) < kMaxMaps ? (P - r0) : kMaxMaps;
+            for (int i = 0; i < nr && err == cudaSuccess; ++i) {
+                const int r = r0 + i;
+                if (!make_map(&prm->mq[i], ptrs.q[r], b, s, Hq, d, 128) ||
+                    !make_map(&prm->mk[i], ptrs.k[r], b, s, Hk, d, 128) ||
+                    !make_map(&prm->mv[i], ptrs.v[r], b, s, Hk, d, 128) ||
+                    !make_map(&prm->mdo[i], ptrs.dout[r], b, s, Hq, d, 128))
+                    err = cudaErrorInvalidValue;
+                prm->dq[i] = static_cast<uint8_t*>(ptrs.dq[r]);
+                prm->dk[i] = static_cast<uint8_t*>(ptrs.dk[r]);
+                prm->dv[i] = static_cast<uint8_t*>(ptrs.dv[r]);
+                prm->lse2[i] = ptrs.lse2[r];
+                prm->dsum[i] = ptrs.dsum[r];
+            }
+            if (err != cudaSuccess) break;
+            err = d == 64 ? launch_bwd_d<64>(*prm, nr, stream) : launch_bwd_d<128>(*prm, nr, stream);
+        }
     }
     delete prm;
     return err;

@@ -52,10 +52,15 @@ cudaError_t launch_attention_tc(int P, int b, int s, int h_q, int h_kv, int d, i
 cudaError_t launch_attention_tc_usp(int Pu, int Pr, int b, int s, int h_q, int h_kv, int d, int causal,
                                     const AttnPtrs& head, cudaStream_t stream, int* unsupported);
 
-// Backward of the bf16 tensor-core attention (head layout per rank).  O and dO for the
-// row sums D are read from `o_rows` / `do_rows` in head layout, or in seq layout when
-// od_seq_layout != 0 (then indexed by seq rank j, not by head rank r).
+// Backward of the bf16 tensor-core attention.  fused == 0: q/k/v/dout/dq/dk/dv are the
+// head-layout buffers of every head rank.  fused != 0: they are the seq-layout buffers of
+// every seq rank, and the kernels gather/scatter through their tile addressing (needs
+// P <= 16 and (s/P) % 128 == 0, else *unsupported = 1).  O and dO for the row sums D are
+// read from `o_rows` / `do_rows` in head layout, or in seq layout when od_seq_layout != 0
+// (then indexed by seq rank j, not by head rank r).  The statistics (lse, lse2, dsum)
+// are always per head rank.
 struct BwdPtrs {
+    int od_seq_layout;
     const void* q[kMaxRanks];
     const void* k[kMaxRanks];
     const void* v[kMaxRanks];
@@ -69,7 +74,7 @@ struct BwdPtrs {
     float* lse2[kMaxRanks];       // scratch [b][h_q/P][s_pad], s_pad = ceil(s/128)*128
     float* dsum[kMaxRanks];       // scratch, same shape
 };
-cudaError_t launch_attention_bwd_tc(int P, int b, int s, int h_q, int h_kv, int d, int causal, int od_seq_layout,
+cudaError_t launch_attention_bwd_tc(int P, int b, int s, int h_q, int h_kv, int d, int causal, int fused,
                                     const BwdPtrs& ptrs, cudaStream_t stream, int* unsupported);
 
 // Device error word of the tensor-core kernels (bounded waits that gave up).

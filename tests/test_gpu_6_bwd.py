@@ -196,3 +196,45 @@ def test_backward_argument_errors():
     assert e.value.status == 1
     torch.cuda.synchronize()
     device_ok()
+
+
+@pytest.mark.parametrize("P,b,s,hq,hkv,d,causal", [
+    (2, 1, 256, 4, 2, 64, True), (4, 2, 512, 8, 8, 128, False), (8, 1, 1024, 16, 8, 128, True),
+    (4, 1, 2048, 8, 4, 128, True)])
+def test_fused_training_path_matches_unfused(P, b, s, hq, hkv, d, causal):
+    """The fused forward's statistics and the fused backward (exchanges in the tile
+    addressing) give the same bits as the unfused path, and match the oracle."""
+    need_gpu()
+    q, k, v = global_qkv(b, s, hq, hkv, d, torch.bfloat16, seed=P * 3 + s)
+    do = global_grad(b, s, hq, d, torch.bfloat16, seed=P * 3 + s + 1)
+    qs, ks, vs, dos = (shard_seq(x, P) for x in (q, k, v, do))
+    qd, kd, vd, dod = _cuda(qs), _cuda(ks), _cuda(vs), _cuda(dos)
+    o_u, lse_u = uly.ulysses_dist_attn_fwd_lse(qd, kd, vd, causal, fused=False)
+    o_f, lse_f = uly.ulysses_dist_attn_fwd_lse(qd, kd, vd, causal, fused=True)
+    g_u = uly.ulysses_dist_attn_bwd(qd, kd, vd, o_u, dod, lse_u, causal, fused=False)
+    g_f = uly.ulysses_dist_attn_bwd(qd, kd, vd, o_f, dod, lse_f, causal, fused=True)
+    torch.cuda.synchronize()
+    device_ok()
+    for j in range(P):
+        assert bits_equal(o_f[j], o_u[j]) and bits_equal(lse_f[j], lse_u[j]), f"forward rank {j}"
+        for x, y in zip(g_f, g_u):
+            assert bits_equal(x[j], y[j]), f"backward rank {j}"
+    if s <= 1024:
+        wq, wk, wv = oracle.dist_attn_bwd(qs, ks, vs, dos, causal)
+        for j in range(P):
+            assert_close_grad(g_f[0][j], wq[j], f"dq rank {j}")
+            assert_close_grad(g_f[1][j], wk[j], f"dk rank {j}")
+            assert_close_grad(g_f[2][j], wv[j], f"dv rank {j}")
+
+
+def test_fused_backward_declines_ragged_ranks():
+    need_gpu()
+    P, b, s, hq, hkv, d = 2, 1, 200, 4, 4, 128
+    q, k, v = global_qkv(b, s, hq, hkv, d, torch.bfloat16, seed=11)
+    qd, kd, vd = (_cuda(shard_seq(x, P)) for x in (q, k, v))
+    o, lse = uly.ulysses_dist_attn_fwd_lse(qd, kd, vd, True)
+    with pytest.raises(uly.UlyssesError) as e:
+        uly.ulysses_dist_attn_bwd(qd, kd, vd, o, o, lse, True, fused=True)
+    assert e.value.status == 2
+    torch.cuda.synchronize()
+    device_ok()
