@@ -64,6 +64,8 @@ def _load():
             lib.orc_usp_fwd.argtypes = [i, i, i, i, i, i, i, i, i, ctypes.POINTER(vp), ctypes.POINTER(vp),
                                         ctypes.POINTER(vp), ctypes.POINTER(vp)]
             lib.orc_usp_fwd.restype = i
+            lib.orc_attention_bwd_rows.argtypes = [i, i, i, i, i, i, i, vp, vp, vp, vp, i, vp, i, vp, vp, vp, vp]
+            lib.orc_attention_bwd_rows.restype = i
             _lib = lib
     return _lib
 
@@ -214,3 +216,19 @@ def usp_group_exchange(x_seq, Pu):
     for g in range(len(x_seq) // Pu):
         out += seq2head(list(x_seq[g * Pu:(g + 1) * Pu]))
     return out
+
+
+def attention_bwd_rows(q, k, v, dout, causal, q_samples, k_samples):
+    """Selected gradient rows of one rank's local attention (head layout):
+    q_samples = [(b, i, head), ...] -> dq rows; k_samples = [(b, j, kv_head), ...] -> dk, dv
+    rows (summed over the query heads of the group).  Returns float64 (dq [nq, d], dk, dv [nk, d])."""
+    q, k, v, dout = _cpu(q), _cpu(k), _cpu(v), _cpu(dout)
+    b, s, hq, d = q.shape
+    qa = np.ascontiguousarray(np.asarray(q_samples, dtype=np.int32).reshape(-1, 3))
+    ka = np.ascontiguousarray(np.asarray(k_samples, dtype=np.int32).reshape(-1, 3))
+    dq = np.zeros((qa.shape[0], d)); dk = np.zeros((ka.shape[0], d)); dv = np.zeros((ka.shape[0], d))
+    _check(_load().orc_attention_bwd_rows(b, s, hq, k.shape[2], d, int(bool(causal)), DTYPE_CODE[q.dtype],
+                                          q.data_ptr(), k.data_ptr(), v.data_ptr(), dout.data_ptr(),
+                                          qa.shape[0], qa.ctypes.data, ka.shape[0], ka.ctypes.data,
+                                          dq.ctypes.data, dk.ctypes.data, dv.ctypes.data), "attention_bwd_rows")
+    return torch.from_numpy(dq), torch.from_numpy(dk), torch.from_numpy(dv)

@@ -499,3 +499,122 @@ int orc_usp_fwd(int Pu, int Pr, int b, int s, int hq, int hkv, int d, int causal
     if (oh) free_bufs(oh, P);
     return rc;
 }
+
+/* --------------------------------------------------------- sampled gradient rows */
+
+/*
+ * Selected rows of the local attention gradient, for sizes whose full evaluation is out
+ * of reach.  The definitions are those of orc_attention_bwd, evaluated per row:
+ *   dQ_i = sum_j P_ij (dP_ij - D_i) k_j / sqrt(d)            (query row i of head hh)
+ *   dV_j = sum_hh sum_i P_ij dO_i,  dK_j = sum_hh sum_i P_ij (dP_ij - D_i) q_i / sqrt(d)
+ * with P_ij = exp(q_i.k_j/sqrt(d) - L_i), L_i the row's log-sum-exp, D_i = dO_i . O_i
+ * (O the exact output) and, for key rows, the sum over the query heads hh that read
+ * K/V head kvh.  One pass over a (batch, query head) computes L_i and D_i of every row.
+ * qs[3n..3n+2] = (bb, i, hh) for dq row n; ks[3n..3n+2] = (bb, j, kvh) for dk/dv row n.
+ * Head layout inputs as orc_attention_bwd; outputs double [n][d].
+ */
+int orc_attention_bwd_rows(int b, int s, int hq, int hkv, int d, int causal, int dtype,
+                           const void* q, const void* k, const void* v, const void* dout,
+                           int nq, const int* qs, int nk, const int* ks,
+                           double* dq, double* dk, double* dv) {
+    if (b < 1 || s < 1 || hq < 1 || hkv < 1 || d < 1 || hq % hkv) return ORC_BAD_ARG;
+    const int g = hq / hkv;
+    const double scale = 1.0 / sqrt((double)d);
+    double* L = (double*)malloc(sizeof(double) * s);
+    double* D = (double*)malloc(sizeof(double) * s);
+    double* sc = (double*)malloc(sizeof(double) * s);
+    double* o = (double*)malloc(sizeof(double) * d);
+    if (!L || !D || !sc || !o) {
+        free(L); free(D); free(sc); free(o);
+        return ORC_NO_MEMORY;
+    }
+#define QI(bb, i, hh, c) load_elem(q, ((((size_t)(bb) * s + (i)) * hq + (hh)) * d + (c)), dtype)
+#define DOI(bb, i, hh, c) load_elem(dout, ((((size_t)(bb) * s + (i)) * hq + (hh)) * d + (c)), dtype)
+#define KJ(bb, j, kh, c) load_elem(k, ((((size_t)(bb) * s + (j)) * hkv + (kh)) * d + (c)), dtype)
+#define VJ(bb, j, kh, c) load_elem(v, ((((size_t)(bb) * s + (j)) * hkv + (kh)) * d + (c)), dtype)
+    /* the (batch, query head) pairs any request needs */
+    for (int n = 0; n < nq + nk; ++n) {
+        const int* smp = n < nq ? qs + 3 * n : ks + 3 * (n - nq);
+        if (smp[0] < 0 || smp[0] >= b || smp[1] < 0 || smp[1] >= s || smp[2] < 0 ||
+            smp[2] >= (n < nq ? hq : hkv)) {
+            free(L); free(D); free(sc); free(o);
+            return ORC_BAD_ARG;
+        }
+    }
+    for (int n = 0; n < nq; ++n)
+        for (int c = 0; c < d; ++c) dq[(size_t)n * d + c] = 0.0;
+    for (int n = 0; n < nk; ++n)
+        for (int c = 0; c < d; ++c) dk[(size_t)n * d + c] = dv[(size_t)n * d + c] = 0.0;
+    for (int bb = 0; bb < b; ++bb)
+        for (int hh = 0; hh < hq; ++hh) {
+            const int kh = hh / g;
+            int needed = 0;
+            for (int n = 0; n < nq; ++n) needed |= qs[3 * n] == bb && qs[3 * n + 2] == hh;
+            for (int n = 0; n < nk; ++n) needed |= ks[3 * n] == bb && ks[3 * n + 2] == kh;
+            if (!needed) continue;
+            /* L_i and D_i of every query row of this (batch, head) */
+            for (int i = 0; i < s; ++i) {
+                const int nv = causal ? i + 1 : s;
+                double m = -INFINITY;
+                for (int j = 0; j < nv; ++j) {
+                    double acc = 0.0;
+                    for (int c = 0; c < d; ++c) acc += QI(bb, i, hh, c) * KJ(bb, j, kh, c);
+                    sc[j] = acc * scale;
+                    if (sc[j] > m) m = sc[j];
+                }
+                double l = 0.0;
+                for (int j = 0; j < nv; ++j) l += exp(sc[j] - m);
+                L[i] = m + log(l);
+                for (int c = 0; c < d; ++c) o[c] = 0.0;
+                for (int j = 0; j < nv; ++j) {
+                    const double w = exp(sc[j] - L[i]);
+                    for (int c = 0; c < d; ++c) o[c] += w * VJ(bb, j, kh, c);
+                }
+                double dd = 0.0;
+                for (int c = 0; c < d; ++c) dd += DOI(bb, i, hh, c) * o[c];
+                D[i] = dd;
+            }
+            /* requested query rows of this head */
+            for (int n = 0; n < nq; ++n) {
+                if (qs[3 * n] != bb || qs[3 * n + 2] != hh) continue;
+                const int i = qs[3 * n + 1], nv = causal ? i + 1 : s;
+                for (int j = 0; j < nv; ++j) {
+                    double sij = 0.0, dpij = 0.0;
+                    for (int c = 0; c < d; ++c) {
+                        sij += QI(bb, i, hh, c) * KJ(bb, j, kh, c);
+                        dpij += DOI(bb, i, hh, c) * VJ(bb, j, kh, c);
+                    }
+                    const double pij = exp(sij * scale - L[i]);
+                    const double ds = pij * (dpij - D[i]);
+                    for (int c = 0; c < d; ++c) dq[(size_t)n * d + c] += ds * KJ(bb, j, kh, c) * scale;
+                }
+            }
+            /* requested key rows of this head's K/V head: this head's share */
+            for (int n = 0; n < nk; ++n) {
+                if (ks[3 * n] != bb || ks[3 * n + 2] != kh) continue;
+                const int j = ks[3 * n + 1];
+                for (int i = causal ? j : 0; i < s; ++i) {
+                    double sij = 0.0, dpij = 0.0;
+                    for (int c = 0; c < d; ++c) {
+                        sij += QI(bb, i, hh, c) * KJ(bb, j, kh, c);
+                        dpij += DOI(bb, i, hh, c) * VJ(bb, j, kh, c);
+                    }
+                    const double pij = exp(sij * scale - L[i]);
+                    const double ds = pij * (dpij - D[i]);
+                    for (int c = 0; c < d; ++c) {
+                        dv[(size_t)n * d + c] += pij * DOI(bb, i, hh, c);
+                        dk[(size_t)n * d + c] += ds * QI(bb, i, hh, c) * scale;
+                    }
+                }
+            }
+        }
+#undef QI
+#undef DOI
+#undef KJ
+#undef VJ
+    free(L);
+    free(D);
+    free(sc);
+    free(o);
+    return ORC_OK;
+}

@@ -99,3 +99,23 @@ def test_dist_backward_equals_single_device(P, b, s, hq, hkv, d, causal):
     assert torch.allclose(torch.cat(dq, 1), rq, atol=1e-9, rtol=0)
     assert torch.allclose(torch.cat(dk, 1), rk, atol=1e-9, rtol=0)
     assert torch.allclose(torch.cat(dv, 1), rv, atol=1e-9, rtol=0)
+
+
+@pytest.mark.parametrize("b,s,hq,hkv,d,causal", [(2, 13, 4, 2, 8, True), (1, 11, 2, 2, 6, False),
+                                                 (1, 16, 4, 1, 5, True)])
+def test_backward_rows_vs_autograd(b, s, hq, hkv, d, causal):
+    """The per-row gradient evaluation against float64 autograd, rows and heads spread out."""
+    gen = torch.Generator().manual_seed(s + 100 * d)
+    q = torch.randn(b, s, hq, d, generator=gen, dtype=torch.float64)
+    k = torch.randn(b, s, hkv, d, generator=gen, dtype=torch.float64)
+    v = torch.randn(b, s, hkv, d, generator=gen, dtype=torch.float64)
+    do = torch.randn(b, s, hq, d, generator=gen, dtype=torch.float64)
+    rq, rk, rv = _autograd(q, k, v, do, causal)
+    qsm = [(bb, i, hh) for bb in range(b) for i in (0, s // 2, s - 1) for hh in (0, hq - 1)]
+    ksm = [(bb, j, kh) for bb in range(b) for j in (0, s // 3, s - 1) for kh in range(hkv)]
+    dq, dk, dv = oracle.attention_bwd_rows(q, k, v, do, causal, qsm, ksm)
+    for n, (bb, i, hh) in enumerate(qsm):
+        assert torch.allclose(dq[n], rq[bb, i, hh], atol=1e-11, rtol=0)
+    for n, (bb, j, kh) in enumerate(ksm):
+        assert torch.allclose(dk[n], rk[bb, j, kh], atol=1e-11, rtol=0)
+        assert torch.allclose(dv[n], rv[bb, j, kh], atol=1e-11, rtol=0)
