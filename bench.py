@@ -519,7 +519,8 @@ def run_overlap(args):
     out = [torch.empty_like(q) for q in qs]
     ws = torch.empty(max(1, uly.ulysses_dist_attn_workspace_bytes(P, b, s, hq, hkv, d, dt, False)),
                      dtype=torch.uint8, device="cuda")
-    chunks = [c for c in (2, 4, 8) if (hkv // P) % c == 0]
+    Hq, Hk = hq // P, hkv // P
+    chunks = [c for c in (2, 4, 8) if Hq % c == 0 and (Hk % c == 0 or c % Hk == 0)]
     wso = {c: torch.empty(uly.ulysses_dist_attn_overlap_workspace_bytes(P, b, s, hq, hkv, d, dt, c),
                           dtype=torch.uint8, device="cuda") for c in chunks}
     rows = {}

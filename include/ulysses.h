@@ -138,7 +138,10 @@ uly_status ulysses_dist_attn_fwd(int P, int b, int s, int h_q, int h_kv, int d, 
  * everything before the call returns control of the results to it; `side_stream` first
  * waits for the work already on `stream`.  side_stream may equal stream (no overlap).
  * Arguments and results as ulysses_dist_attn_fwd with fused == 0 -- the same bits --
- * plus: 1 <= n_chunks <= 64 and (h_kv/P) % n_chunks == 0, else ULY_ERR_INVALID_ARG;
+ * plus: 1 <= n_chunks <= 64 and (h_q/P) % n_chunks == 0, and either (h_kv/P) % n_chunks
+ * == 0 (every chunk has its own K/V heads) or n_chunks % (h_kv/P) == 0 (grouped heads:
+ * n_chunks/(h_kv/P) consecutive chunks share one K/V head, exchanged with the first of
+ * them), else ULY_ERR_INVALID_ARG;
  * workspace: 256-byte aligned, at least ulysses_dist_attn_overlap_workspace_bytes(...)
  * bytes (the chunks' head-layout Q, K, V, O).  The call creates and destroys CUDA events
  * (host objects) for the cross-stream ordering; it allocates no device memory.

@@ -518,14 +518,46 @@ uly_status ulysses_dist_attn_bwd(int P, int b, int s, int h_q, int h_kv, int d, 
     return ce == cudaSuccess ? ULY_OK : ULY_ERR_CUDA;
 }
 
+// Head groups of the overlapped forward.  Chunk c holds local query heads
+// [c*Hc, (c+1)*Hc).  When n_chunks divides the local K/V heads, chunk c has its own K/V
+// heads [c*Hkc, (c+1)*Hkc).  When n_chunks is a multiple of them instead (grouped heads with
+// few K/V heads per rank), n_chunks/Hk consecutive chunks share one K/V head, exchanged
+// with the first of them.
+struct OverlapPlan {
+    int nc, Hc, Hkc, kv_groups, chunks_per_kv;
+    bool valid;
+    int kv_of(int c) const { return c / chunks_per_kv; }
+    bool new_kv(int c) const { return c % chunks_per_kv == 0; }
+};
+
+OverlapPlan overlap_plan(int P, int h_q, int h_kv, int n_chunks) {
+    OverlapPlan pl{n_chunks, 0, 0, 0, 1, false};
+    const int Hq = h_q / P, Hk = h_kv / P;
+    if (n_chunks < 1 || n_chunks > kMaxChunks || Hq % n_chunks) return pl;
+    pl.Hc = Hq / n_chunks;
+    if (Hk % n_chunks == 0) {
+        pl.Hkc = Hk / n_chunks;
+        pl.kv_groups = n_chunks;
+    } else if (n_chunks % Hk == 0) {
+        pl.Hkc = 1;
+        pl.kv_groups = Hk;
+        pl.chunks_per_kv = n_chunks / Hk;
+    } else {
+        return pl;
+    }
+    pl.valid = true;
+    return pl;
+}
+
 size_t ulysses_dist_attn_overlap_workspace_bytes(int P, int b, int s, int h_q, int h_kv, int d, uly_dtype dtype,
                                                  int n_chunks) {
     if (check_attention_shape(P, b, s, h_q, h_kv, d, dtype) == ULY_ERR_INVALID_ARG) return 0;
-    if (s % P || n_chunks < 1 || n_chunks > kMaxChunks || (h_kv / P) % n_chunks) return 0;
+    const OverlapPlan pl = overlap_plan(P, h_q, h_kv, n_chunks);
+    if (s % P || !pl.valid) return 0;
     const int e = elem_bytes(dtype);
-    const uint64_t qb = round256((uint64_t)b * s * (h_q / P / n_chunks) * d * e);
-    const uint64_t kb = round256((uint64_t)b * s * (h_kv / P / n_chunks) * d * e);
-    return (size_t)((uint64_t)n_chunks * P * (2 * qb + 2 * kb));
+    const uint64_t qb = round256((uint64_t)b * s * pl.Hc * d * e);
+    const uint64_t kb = round256((uint64_t)b * s * pl.Hkc * d * e);
+    return (size_t)((uint64_t)P * (2 * qb * pl.nc + 2 * kb * pl.kv_groups));
 }
 
 uly_status ulysses_dist_attn_fwd_overlap(int P, int b, int s, int h_q, int h_kv, int d, uly_dtype dtype, int causal,
@@ -539,7 +571,8 @@ uly_status ulysses_dist_attn_fwd_overlap(int P, int b, int s, int h_q, int h_kv,
     if (st != ULY_OK) return st;
     st = check_exchange_shape(P, b, s, h_kv, d, dtype);
     if (st != ULY_OK) return st;
-    if (n_chunks < 1 || n_chunks > kMaxChunks || (h_kv / P) % n_chunks) return ULY_ERR_INVALID_ARG;
+    const OverlapPlan pl = overlap_plan(P, h_q, h_kv, n_chunks);
+    if (!pl.valid) return ULY_ERR_INVALID_ARG;
     const int e = elem_bytes(dtype);
     const int S = s / P;
     const uint64_t qsb = (uint64_t)b * S * h_q * d * e, ksb = (uint64_t)b * S * h_kv * d * e;
@@ -553,11 +586,15 @@ uly_status ulysses_dist_attn_fwd_overlap(int P, int b, int s, int h_q, int h_kv,
     std::vector<Range> rw{{reinterpret_cast<uintptr_t>(workspace), reinterpret_cast<uintptr_t>(workspace) + need}};
     if (overlaps(rw, rq) || overlaps(rw, rk) || overlaps(rw, rv) || overlaps(rw, ro)) return ULY_ERR_INVALID_ARG;
 
-    // workspace: chunk-major, then per rank [Q | K | V | O] of the chunk's heads in head layout
-    const int nc = n_chunks, Hc = h_q / P / nc, Hkc = h_kv / P / nc;
-    const Carve ws(workspace, {(uint64_t)b * s * Hc * d * e, (uint64_t)b * s * Hkc * d * e,
-                               (uint64_t)b * s * Hkc * d * e, (uint64_t)b * s * Hc * d * e});
-    auto buf = [&](int c, int r, int k) { return ws.at(c * P + r, k); };
+    // workspace: [chunk][rank] head-layout Q and O of the chunk's query heads, then
+    // [K/V group][rank] head-layout K and V
+    const int nc = pl.nc, Hc = pl.Hc, Hkc = pl.Hkc;
+    const Carve wq(workspace, {(uint64_t)b * s * Hc * d * e, (uint64_t)b * s * Hc * d * e});
+    const Carve wkv(static_cast<uint8_t*>(workspace) + wq.per_rank * nc * P,
+                    {(uint64_t)b * s * Hkc * d * e, (uint64_t)b * s * Hkc * d * e});
+    auto buf = [&](int c, int r, int k) {  // k: 0 Q, 1 K, 2 V, 3 O
+        return k == 0 || k == 3 ? wq.at(c * P + r, k == 0 ? 0 : 1) : wkv.at(pl.kv_of(c) * P + r, k - 1);
+    };
 
     std::vector<cudaEvent_t> ev;
     auto cleanup = [&]() {
@@ -576,19 +613,20 @@ uly_status ulysses_dist_attn_fwd_overlap(int P, int b, int s, int h_q, int h_kv,
     auto ev_attn = [&](int c) { return ev[2 + nc + c]; };
 
     uly::PermuteTensor* t = new uly::PermuteTensor[3];
-    auto exchange_in = [&](int c) {  // all-to-all #1 for chunk c's heads of Q, K and V (side stream)
-        memset(t, 0, 3 * sizeof(uly::PermuteTensor));
+    auto exchange_in = [&](int c) {  // all-to-all #1 for chunk c's query heads, and its K/V heads
+        memset(t, 0, 3 * sizeof(uly::PermuteTensor));  // unless an earlier chunk exchanged them
         const void* const* src[3] = {q_seq, k_seq, v_seq};
-        for (int k = 0; k < 3; ++k) {
+        const int nt = pl.new_kv(c) ? 3 : 1;
+        for (int k = 0; k < nt; ++k) {
             for (int r = 0; r < P; ++r) {
                 t[k].src[r] = src[k][r];
                 t[k].dst[r] = buf(c, r, k);
             }
             t[k].h = k == 0 ? h_q : h_kv;
             t[k].hsub = k == 0 ? Hc : Hkc;
-            t[k].hoff = c * t[k].hsub;
+            t[k].hoff = k == 0 ? c * Hc : pl.kv_of(c) * Hkc;
         }
-        return uly::launch_permute(0, P, b, s, d, e, t, 3, side_stream);
+        return uly::launch_permute(0, P, b, s, d, e, t, nt, side_stream);
     };
     auto exchange_out = [&](int c) {  // all-to-all #2 for chunk c's output heads (side stream)
         memset(t, 0, sizeof(uly::PermuteTensor));

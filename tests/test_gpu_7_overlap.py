@@ -20,6 +20,9 @@ CASES = [
     (2, 1, 200, 4, 4, 128, torch.bfloat16, True, 1),   # one chunk
     (4, 2, 4096, 32, 32, 128, torch.bfloat16, True, 8),
     (4, 2, 4096, 32, 32, 128, torch.bfloat16, False, 4),
+    (2, 1, 512, 8, 2, 128, torch.bfloat16, True, 4),     # one K/V head per rank shared by 4 chunks
+    (2, 1, 512, 8, 4, 64, torch.bfloat16, False, 4),     # two K/V heads per rank, 2 chunks each
+    (8, 1, 32768, 32, 8, 128, torch.bfloat16, True, 4),  # the GQA workload
 ]
 
 
@@ -58,7 +61,7 @@ def test_overlap_argument_errors():
     need_gpu()
     qs, ks, vs = seq_shards_qkv(2, 1, 256, 8, 8, 128, torch.bfloat16, seed=1)
     qd, kd, vd = [t.cuda() for t in qs], [t.cuda() for t in ks], [t.cuda() for t in vs]
-    for bad in (0, 3, 65):  # h_kv/P = 4: 3 does not divide it
+    for bad in (0, 3, 8, 65):  # 4 local query heads: 3 and 8 do not divide them
         with pytest.raises(uly.UlyssesError) as e:
             uly.ulysses_dist_attn_fwd_overlap(qd, kd, vd, True, n_chunks=bad,
                                               workspace=torch.empty(1 << 20, dtype=torch.uint8, device="cuda"))
