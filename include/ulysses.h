@@ -186,6 +186,41 @@ uly_status ulysses_usp_attn_fwd(int Pu, int Pr, int b, int s, int h_q, int h_kv,
                                 void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * Training on the two-level layout (the backward of the pipeline above: each exchange's
+ * backward is the opposite exchange, "DeepSpeed-Ulysses 深度解析", section "核心设计", and
+ * the attention's backward is the ordinary one, "02 · DeepSpeed-Ulysses", section 5).
+ *
+ * ulysses_usp_attn_fwd_lse: ulysses_usp_attn_fwd that also saves the softmax statistics:
+ *   lse: Pu pointers, lse[u] = fp32 [b][h_q/Pu][s], the natural-log log-sum-exp of the
+ *   scaled scores of every query row of heads [u*h_q/Pu, (u+1)*h_q/Pu), all s positions
+ *   (the rows of every ring group's rank u).  Needs ULY_BF16 (else ULY_ERR_UNSUPPORTED) and
+ *   lse non-null, not overlapping any other argument (else ULY_ERR_INVALID_ARG).
+ * ulysses_usp_attn_bwd: dQ, dK, dV in the seq layout of the inputs, from Q, K, V, the
+ *   forward's O, the gradient dO (all seq layout, P = Pu*Pr pointers each) and the lse of
+ *   ulysses_usp_attn_fwd_lse:
+ *     1. all-to-all #1 on Q, K, V and dO inside every ring group;
+ *     2. the attention backward of every Ulysses unit over the whole sequence, reading and
+ *        writing each tile in the buffer of the ring group that holds its tokens;
+ *     3. all-to-all #2 on dQ, dK, dV inside every ring group.
+ *   Same sizes and kernel limits as ulysses_usp_attn_fwd, bf16 only.  dq/dk/dv must not
+ *   overlap each other or any input.  The results equal ulysses_dist_attn_bwd over the same
+ *   P ranks bit for bit (where that call accepts the shape: h_kv % P == 0).  workspace:
+ *   256-byte aligned, at least ulysses_usp_bwd_workspace_bytes(...) bytes (every rank's group
+ *   head-layout Q, K, V, dO, dQ, dK, dV and, per Ulysses unit, two fp32 row arrays); it
+ *   returns 0 for shapes the call rejects.
+ */
+uly_status ulysses_usp_attn_fwd_lse(int Pu, int Pr, int b, int s, int h_q, int h_kv, int d, uly_dtype dtype,
+                                    int causal, const void* const* q_seq, const void* const* k_seq,
+                                    const void* const* v_seq, void* const* o_seq, float* const* lse,
+                                    void* workspace, size_t workspace_bytes, cudaStream_t stream);
+size_t ulysses_usp_bwd_workspace_bytes(int Pu, int Pr, int b, int s, int h_q, int h_kv, int d, uly_dtype dtype);
+uly_status ulysses_usp_attn_bwd(int Pu, int Pr, int b, int s, int h_q, int h_kv, int d, uly_dtype dtype,
+                                int causal, const void* const* q_seq, const void* const* k_seq,
+                                const void* const* v_seq, const void* const* o_seq, const void* const* do_seq,
+                                const float* const* lse, void* const* dq_seq, void* const* dk_seq,
+                                void* const* dv_seq, void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * The unfused forward without any allocation by the caller or the library.  The paper has
  * no counterpart: this exists for callers that cannot call cudaMalloc -- for example an
  * application whose memory pool already holds all the device memory it may use, or a

@@ -25,6 +25,7 @@ __all__ = [
     "ulysses_local_attention_fwd_lse", "ulysses_dist_attn_fwd_lse", "ulysses_attn_bwd_workspace_bytes",
     "ulysses_local_attention_bwd", "ulysses_dist_attn_bwd", "ulysses_dist_attn_overlap_workspace_bytes",
     "ulysses_dist_attn_fwd_overlap", "ulysses_usp_workspace_bytes", "ulysses_usp_attn_fwd",
+    "ulysses_usp_attn_fwd_lse", "ulysses_usp_bwd_workspace_bytes", "ulysses_usp_attn_bwd",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -40,7 +41,8 @@ EXPORTED_SYMBOLS = (
     "ulysses_status_string", "ulysses_dist_attn_fwd_noalloc", "ulysses_local_attention_fwd_lse",
     "ulysses_dist_attn_fwd_lse", "ulysses_attn_bwd_workspace_bytes", "ulysses_local_attention_bwd",
     "ulysses_dist_attn_bwd", "ulysses_dist_attn_overlap_workspace_bytes", "ulysses_dist_attn_fwd_overlap",
-    "ulysses_usp_workspace_bytes", "ulysses_usp_attn_fwd",
+    "ulysses_usp_workspace_bytes", "ulysses_usp_attn_fwd", "ulysses_usp_attn_fwd_lse",
+    "ulysses_usp_bwd_workspace_bytes", "ulysses_usp_attn_bwd",
 )
 
 _lock = threading.Lock()
@@ -102,6 +104,13 @@ def load_library():
         lib.ulysses_usp_workspace_bytes.restype = sz
         lib.ulysses_usp_attn_fwd.argtypes = [i, i, i, i, i, i, i, i, i, pp, pp, pp, pp, vp, sz, vp]
         lib.ulysses_usp_attn_fwd.restype = i
+        lib.ulysses_usp_attn_fwd_lse.argtypes = [i, i, i, i, i, i, i, i, i, pp, pp, pp, pp, pp, vp, sz, vp]
+        lib.ulysses_usp_attn_fwd_lse.restype = i
+        lib.ulysses_usp_bwd_workspace_bytes.argtypes = [i, i, i, i, i, i, i, i]
+        lib.ulysses_usp_bwd_workspace_bytes.restype = sz
+        lib.ulysses_usp_attn_bwd.argtypes = [i, i, i, i, i, i, i, i, i, pp, pp, pp, pp, pp, pp, pp, pp, pp, vp, sz,
+                                             vp]
+        lib.ulysses_usp_attn_bwd.restype = i
         lib.ulysses_device_status.argtypes = [i]
         lib.ulysses_device_status.restype = i
         lib.ulysses_status_string.argtypes = [i]
@@ -426,3 +435,66 @@ def ulysses_usp_attn_fwd(q_seq, k_seq, v_seq, causal, Pu, Pr, out_seq=None, work
         _ptr_array(v_seq), _ptr_array(out_seq), workspace.data_ptr(), workspace.numel() * workspace.element_size(),
         _stream(stream)), "ulysses_usp_attn_fwd")
     return out_seq
+
+
+def ulysses_usp_attn_fwd_lse(q_seq, k_seq, v_seq, causal, Pu, Pr, out_seq=None, lse=None, workspace=None,
+                             stream=None):
+    """The two-level forward plus its softmax statistics: returns (o_seq, lse) with lse Pu
+    fp32 tensors [b, h_q/Pu, s] (Ulysses unit u's heads, every position)."""
+    q0 = _same(q_seq, "q_seq")
+    k0 = _same(k_seq, "k_seq")
+    _same(v_seq, "v_seq")
+    P = len(q_seq)
+    if P != Pu * Pr:
+        raise ValueError(f"{P} ranks given for Pu={Pu} x Pr={Pr}")
+    b, S, hq, d = q0.shape
+    hkv = k0.shape[2]
+    s = S * P
+    if out_seq is None:
+        out_seq = [torch.empty_like(q) for q in q_seq]
+    if lse is None:
+        lse = [torch.empty((b, hq // Pu, s), dtype=torch.float32, device=q0.device) for _ in range(Pu)]
+    if len(lse) != Pu:
+        raise ValueError(f"{len(lse)} statistics arrays given for Pu={Pu}")
+    if workspace is None:
+        need = ulysses_usp_workspace_bytes(Pu, Pr, b, s, hq, hkv, d, q0.dtype)
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q0.device)
+    _check(load_library().ulysses_usp_attn_fwd_lse(
+        Pu, Pr, b, s, hq, hkv, d, _dtype_code(q0), int(bool(causal)), _ptr_array(q_seq), _ptr_array(k_seq),
+        _ptr_array(v_seq), _ptr_array(out_seq), _ptr_array(lse), workspace.data_ptr(),
+        workspace.numel() * workspace.element_size(), _stream(stream)), "ulysses_usp_attn_fwd_lse")
+    return out_seq, lse
+
+
+def ulysses_usp_bwd_workspace_bytes(Pu, Pr, b, s, h_q, h_kv, d, dtype):
+    return int(load_library().ulysses_usp_bwd_workspace_bytes(Pu, Pr, b, s, h_q, h_kv, d, _DTYPES[dtype]))
+
+
+def ulysses_usp_attn_bwd(q_seq, k_seq, v_seq, o_seq, do_seq, lse, causal, Pu, Pr, grads=None, workspace=None,
+                         stream=None):
+    """Backward of the two-level forward, seq layout in and out: returns (dq, dk, dv)."""
+    q0 = _same(q_seq, "q_seq")
+    k0 = _same(k_seq, "k_seq")
+    _same(v_seq, "v_seq")
+    _same(o_seq, "o_seq")
+    _same(do_seq, "do_seq")
+    _same(lse, "lse")
+    P = len(q_seq)
+    if P != Pu * Pr or len(lse) != Pu:
+        raise ValueError(f"{P} ranks and {len(lse)} statistics arrays given for Pu={Pu} x Pr={Pr}")
+    b, S, hq, d = q0.shape
+    hkv = k0.shape[2]
+    s = S * P
+    if grads is None:
+        grads = ([torch.empty_like(x) for x in q_seq], [torch.empty_like(x) for x in k_seq],
+                 [torch.empty_like(x) for x in v_seq])
+    if workspace is None:
+        need = ulysses_usp_bwd_workspace_bytes(Pu, Pr, b, s, hq, hkv, d, q0.dtype)
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q0.device)
+    dq, dk, dv = grads
+    _check(load_library().ulysses_usp_attn_bwd(
+        Pu, Pr, b, s, hq, hkv, d, _dtype_code(q0), int(bool(causal)), _ptr_array(q_seq), _ptr_array(k_seq),
+        _ptr_array(v_seq), _ptr_array(o_seq), _ptr_array(do_seq), _ptr_array(lse), _ptr_array(dq), _ptr_array(dk),
+        _ptr_array(dv), workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream(stream)),
+        "ulysses_usp_attn_bwd")
+    return dq, dk, dv

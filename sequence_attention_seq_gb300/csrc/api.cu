@@ -683,9 +683,16 @@ size_t ulysses_usp_workspace_bytes(int Pu, int Pr, int b, int s, int h_q, int h_
     return (size_t)((uint64_t)Pu * Pr * (2 * qb + 2 * kb));
 }
 
-uly_status ulysses_usp_attn_fwd(int Pu, int Pr, int b, int s, int h_q, int h_kv, int d, uly_dtype dtype, int causal,
-                                const void* const* q_seq, const void* const* k_seq, const void* const* v_seq,
-                                void* const* o_seq, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// The two-level forward; lse (optional) receives, per Ulysses unit u < Pu, the log-sum-exp
+// of its heads' rows over the whole sequence.
+uly_status usp_attn_fwd(int Pu, int Pr, int b, int s, int h_q, int h_kv, int d, uly_dtype dtype, int causal,
+                        const void* const* q_seq, const void* const* k_seq, const void* const* v_seq,
+                        void* const* o_seq, float* const* lse, void* workspace, size_t workspace_bytes,
+                        cudaStream_t stream) {
     if (Pu < 1 || Pr < 1 || Pu * Pr > kMaxRanks || s < 1 || s % (Pu * Pr)) return ULY_ERR_INVALID_ARG;
     const int P = Pu * Pr, L = s / Pr, S = s / P;
     // heads split over the Ulysses degree only; the exchanges run inside each group of Pu ranks
@@ -703,10 +710,17 @@ uly_status ulysses_usp_attn_fwd(int Pu, int Pr, int b, int s, int h_q, int h_kv,
         !collect(reinterpret_cast<const void* const*>(o_seq), P, qsb, ro))
         return ULY_ERR_INVALID_ARG;
     if (overlaps(ro, rq) || overlaps(ro, rk) || overlaps(ro, rv) || self_overlap(ro)) return ULY_ERR_INVALID_ARG;
+    std::vector<Range> rl;
+    if (lse) {
+        if (!collect_f(lse, Pu, (uint64_t)b * (h_q / Pu) * s * 4, rl)) return ULY_ERR_INVALID_ARG;
+        if (self_overlap(rl) || overlaps(rl, rq) || overlaps(rl, rk) || overlaps(rl, rv) || overlaps(rl, ro))
+            return ULY_ERR_INVALID_ARG;
+    }
     const size_t need = ulysses_usp_workspace_bytes(Pu, Pr, b, s, h_q, h_kv, d, dtype);
     if (!workspace_ok(workspace, workspace_bytes, need)) return ULY_ERR_INVALID_ARG;
     std::vector<Range> rw{{reinterpret_cast<uintptr_t>(workspace), reinterpret_cast<uintptr_t>(workspace) + need}};
-    if (overlaps(rw, rq) || overlaps(rw, rk) || overlaps(rw, rv) || overlaps(rw, ro)) return ULY_ERR_INVALID_ARG;
+    if (overlaps(rw, rq) || overlaps(rw, rk) || overlaps(rw, rv) || overlaps(rw, ro) || overlaps(rw, rl))
+        return ULY_ERR_INVALID_ARG;
 
     // workspace: per rank [Q | K | V | O] in head layout of its group: [b][s/Pr][h/Pu][d]
     const Carve ws(workspace, {(uint64_t)b * L * (h_q / Pu) * d * 2, (uint64_t)b * L * (h_kv / Pu) * d * 2,
@@ -736,6 +750,7 @@ uly_status ulysses_usp_attn_fwd(int Pu, int Pr, int b, int s, int h_q, int h_kv,
         head->v[j] = ws.at(j, 2);
         head->o[j] = ws.at(j, 3);
     }
+    for (int u = 0; u < Pu && lse; ++u) head->lse[u] = lse[u];
     int unsupported = 0;
     if (ce == cudaSuccess) ce = uly::launch_attention_tc_usp(Pu, Pr, b, s, h_q, h_kv, d, causal, *head, stream,
                                                              &unsupported);
@@ -752,6 +767,138 @@ uly_status ulysses_usp_attn_fwd(int Pu, int Pr, int b, int s, int h_q, int h_kv,
     }
     delete[] t;
     if (unsupported) return ULY_ERR_UNSUPPORTED;
+    return ce == cudaSuccess ? ULY_OK : ULY_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+uly_status ulysses_usp_attn_fwd(int Pu, int Pr, int b, int s, int h_q, int h_kv, int d, uly_dtype dtype, int causal,
+                                const void* const* q_seq, const void* const* k_seq, const void* const* v_seq,
+                                void* const* o_seq, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    return usp_attn_fwd(Pu, Pr, b, s, h_q, h_kv, d, dtype, causal, q_seq, k_seq, v_seq, o_seq, nullptr, workspace,
+                        workspace_bytes, stream);
+}
+
+uly_status ulysses_usp_attn_fwd_lse(int Pu, int Pr, int b, int s, int h_q, int h_kv, int d, uly_dtype dtype,
+                                    int causal, const void* const* q_seq, const void* const* k_seq,
+                                    const void* const* v_seq, void* const* o_seq, float* const* lse,
+                                    void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    if (!lse) return ULY_ERR_INVALID_ARG;
+    if (dtype != ULY_BF16) return ULY_ERR_UNSUPPORTED;
+    return usp_attn_fwd(Pu, Pr, b, s, h_q, h_kv, d, dtype, causal, q_seq, k_seq, v_seq, o_seq, lse, workspace,
+                        workspace_bytes, stream);
+}
+
+// Workspace of the two-level backward: per rank the group head-layout Q, K, V, dO, dQ, dK, dV
+// ([b][s/Pr][h/Pu][d]), then per Ulysses unit the two fp32 row arrays over all s rows.
+size_t ulysses_usp_bwd_workspace_bytes(int Pu, int Pr, int b, int s, int h_q, int h_kv, int d, uly_dtype dtype) {
+    if (ulysses_usp_workspace_bytes(Pu, Pr, b, s, h_q, h_kv, d, dtype) == 0 || dtype != ULY_BF16) return 0;
+    const int L = s / Pr;
+    const uint64_t qb = round256((uint64_t)b * L * (h_q / Pu) * d * 2);
+    const uint64_t kb = round256((uint64_t)b * L * (h_kv / Pu) * d * 2);
+    const uint64_t ra = row_array_bytes(Pu, b, s, h_q);
+    return (size_t)((uint64_t)Pu * Pr * (4 * qb + 3 * kb) + (uint64_t)Pu * 2 * ra);
+}
+
+uly_status ulysses_usp_attn_bwd(int Pu, int Pr, int b, int s, int h_q, int h_kv, int d, uly_dtype dtype, int causal,
+                                const void* const* q_seq, const void* const* k_seq, const void* const* v_seq,
+                                const void* const* o_seq, const void* const* do_seq, const float* const* lse,
+                                void* const* dq_seq, void* const* dk_seq, void* const* dv_seq, void* workspace,
+                                size_t workspace_bytes, cudaStream_t stream) {
+    if (Pu < 1 || Pr < 1 || Pu * Pr > kMaxRanks || s < 1 || s % (Pu * Pr)) return ULY_ERR_INVALID_ARG;
+    const int P = Pu * Pr, L = s / Pr, S = s / P;
+    uly_status st = check_train_shape(Pu, b, L, h_q, h_kv, d, dtype);
+    if (st != ULY_OK) return st;
+    st = check_exchange_shape(Pu, b, L, h_q, d, dtype);
+    if (st != ULY_OK) return st;
+    st = check_exchange_shape(Pu, b, L, h_kv, d, dtype);
+    if (st != ULY_OK) return st;
+    if ((long long)b * h_q * ((s + 127) / 128) > 0x7fffffffLL) return ULY_ERR_INVALID_ARG;
+    if (P > 16 || L % 128 != 0) return ULY_ERR_UNSUPPORTED;
+    const uint64_t qsb = (uint64_t)b * S * h_q * d * 2, ksb = (uint64_t)b * S * h_kv * d * 2;
+    std::vector<Range> in, rdq, rdk, rdv;
+    if (!collect(q_seq, P, qsb, in) || !collect(k_seq, P, ksb, in) || !collect(v_seq, P, ksb, in) ||
+        !collect(o_seq, P, qsb, in) || !collect(do_seq, P, qsb, in) ||
+        !collect_f(lse, Pu, (uint64_t)b * (h_q / Pu) * s * 4, in) ||
+        !collect(reinterpret_cast<const void* const*>(dq_seq), P, qsb, rdq) ||
+        !collect(reinterpret_cast<const void* const*>(dk_seq), P, ksb, rdk) ||
+        !collect(reinterpret_cast<const void* const*>(dv_seq), P, ksb, rdv))
+        return ULY_ERR_INVALID_ARG;
+    std::vector<Range> outs(rdq);
+    outs.insert(outs.end(), rdk.begin(), rdk.end());
+    outs.insert(outs.end(), rdv.begin(), rdv.end());
+    if (self_overlap(outs) || overlaps(outs, in)) return ULY_ERR_INVALID_ARG;
+    const size_t need = ulysses_usp_bwd_workspace_bytes(Pu, Pr, b, s, h_q, h_kv, d, dtype);
+    if (!workspace_ok(workspace, workspace_bytes, need)) return ULY_ERR_INVALID_ARG;
+    std::vector<Range> rw{{reinterpret_cast<uintptr_t>(workspace), reinterpret_cast<uintptr_t>(workspace) + need}};
+    if (overlaps(rw, in) || overlaps(rw, outs)) return ULY_ERR_INVALID_ARG;
+
+    const uint64_t qb = (uint64_t)b * L * (h_q / Pu) * d * 2, kb = (uint64_t)b * L * (h_kv / Pu) * d * 2;
+    enum { QH, KH, VH, DOH, DQH, DKH, DVH };
+    const Carve ws(workspace, {qb, kb, kb, qb, qb, kb, kb});
+    const uint64_t ra = row_array_bytes(Pu, b, s, h_q);
+    const Carve wr(static_cast<uint8_t*>(workspace) + ws.per_rank * P, {ra, ra});
+    // (1) all-to-all #1 on Q, K, V and dO inside every ring group
+    uly::PermuteTensor* t = new uly::PermuteTensor[4];
+    cudaError_t ce = cudaSuccess;
+    const void* const* srcs[4] = {q_seq, k_seq, v_seq, do_seq};
+    const int dsts[4] = {QH, KH, VH, DOH};
+    for (int g = 0; g < Pr && ce == cudaSuccess; ++g) {
+        memset(t, 0, 4 * sizeof(uly::PermuteTensor));
+        for (int k = 0; k < 4; ++k) {
+            for (int u = 0; u < Pu; ++u) {
+                t[k].src[u] = srcs[k][g * Pu + u];
+                t[k].dst[u] = ws.at(g * Pu + u, dsts[k]);
+            }
+            t[k].h = (k == 1 || k == 2) ? h_kv : h_q;
+        }
+        ce = uly::launch_permute(0, Pu, b, L, d, 2, t, 4, stream);
+    }
+    delete[] t;
+    if (ce != cudaSuccess) return ULY_ERR_CUDA;
+    // (2) the attention backward over the whole sequence (statistics from the seq-layout O, dO)
+    uly::BwdPtrs* p = new uly::BwdPtrs;
+    memset(p, 0, sizeof(uly::BwdPtrs));
+    for (int j = 0; j < P; ++j) {
+        p->q[j] = ws.at(j, QH);
+        p->k[j] = ws.at(j, KH);
+        p->v[j] = ws.at(j, VH);
+        p->dout[j] = ws.at(j, DOH);
+        p->o_rows[j] = o_seq[j];
+        p->do_rows[j] = do_seq[j];
+        p->dq[j] = ws.at(j, DQH);
+        p->dk[j] = ws.at(j, DKH);
+        p->dv[j] = ws.at(j, DVH);
+    }
+    for (int u = 0; u < Pu; ++u) {
+        p->lse[u] = lse[u];
+        p->lse2[u] = static_cast<float*>(wr.at(u, 0));
+        p->dsum[u] = static_cast<float*>(wr.at(u, 1));
+    }
+    p->od_seq_layout = 1;
+    int unsupported = 0;
+    ce = uly::launch_attention_bwd_tc_usp(Pu, Pr, b, s, h_q, h_kv, d, causal, *p, stream, &unsupported);
+    delete p;
+    if (unsupported) return ULY_ERR_UNSUPPORTED;
+    if (ce != cudaSuccess) return ULY_ERR_CUDA;
+    // (3) all-to-all #2 on dQ, dK, dV inside every ring group
+    t = new uly::PermuteTensor[3];
+    void* const* dsts2[3] = {dq_seq, dk_seq, dv_seq};
+    const int srcs2[3] = {DQH, DKH, DVH};
+    for (int g = 0; g < Pr && ce == cudaSuccess; ++g) {
+        memset(t, 0, 3 * sizeof(uly::PermuteTensor));
+        for (int k = 0; k < 3; ++k) {
+            for (int u = 0; u < Pu; ++u) {
+                t[k].src[u] = ws.at(g * Pu + u, srcs2[k]);
+                t[k].dst[u] = dsts2[k][g * Pu + u];
+            }
+            t[k].h = k == 0 ? h_q : h_kv;
+        }
+        ce = uly::launch_permute(1, Pu, b, L, d, 2, t, 3, stream);
+    }
+    delete[] t;
     return ce == cudaSuccess ? ULY_OK : ULY_ERR_CUDA;
 }
 

@@ -53,7 +53,9 @@ constexpr int kRingKV = 5;   // dK/dV kernel: Q/dO ring slots
 constexpr int kRingQ = 5;    // dQ kernel: K/V ring slots
 
 // Maps and gradient buffers are indexed like the forward's: token t of the sequence, for
-// the unit `rank` of a CTA, lives in buffer rank + t / rows_per_map at row t % rows_per_map.
+// the unit `rank` of a CTA, lives in buffer rank + (t / rows_per_map) * map_stride at row
+// t % rows_per_map.  Two-level (Ulysses x Ring): unit u of a Ulysses group, buffers of ring
+// group t / (s/Pr)'s rank u (rows_per_map = s/Pr, map_stride = Pu).
 // Unfused: one buffer per head rank (rows_per_map = s, hq/hkv = that rank's heads).  Fused:
 // one buffer per seq rank (rows_per_map = s/P, hq/hkv = all heads, rank = 0), so the
 // exchanges happen in the tile addressing.  The row statistics always live per head rank:
@@ -66,7 +68,8 @@ struct BwdParams {
     const float* lse2[kMaxMaps];  // per head rank [b][hq_rank][s_pad]: log-sum-exp, base-2 units (+inf on padding)
     const float* dsum[kMaxMaps];  // per head rank [b][hq_rank][s_pad]: D (0 on padding)
     int s, s_pad, n_tiles, hq, hkv, g, b, causal;
-    int rows_per_map;             // s (unfused) or s/P (fused)
+    int rows_per_map;             // s (unfused), s/P (fused) or s/Pr (two-level)
+    int map_stride;               // map step from one token block to the next (Pu two-level, else 1)
     int hq_rank;                  // query heads per head rank
     float scale_log2;             // log2(e)/sqrt(d)
     float scale;                  // 1/sqrt(d)
@@ -76,7 +79,7 @@ struct BwdTok {
     int map, row;
 };
 __device__ __forceinline__ BwdTok bwd_tok(const BwdParams& p, int rank, int t0) {
-    return BwdTok{rank + t0 / p.rows_per_map, t0 % p.rows_per_map};
+    return BwdTok{rank + (t0 / p.rows_per_map) * p.map_stride, t0 % p.rows_per_map};
 }
 
 // Row statistics of (batch bb, query head h of the CTA's unit `rank`), from query q0 on.

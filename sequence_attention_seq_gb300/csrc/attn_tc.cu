@@ -705,7 +705,7 @@ cudaError_t launch_attention_tc_usp(int Pu, int Pr, int b, int s, int h_q, int h
     prm->n_qtiles = s / BM;
     prm->n_pairs = (prm->n_qtiles + 1) / 2;
     prm->heads = Hq;
-    prm->lse_heads = Hq;  // no statistics are written by this launch
+    prm->lse_heads = Hq;  // statistics (if asked for) per Ulysses unit over all s rows
     prm->g = Hq / Hk;
     prm->b = b;
     prm->nranks = Pu;
@@ -718,6 +718,7 @@ cudaError_t launch_attention_tc_usp(int Pu, int Pr, int b, int s, int h_q, int h
             err = cudaErrorInvalidValue;
         prm->optr[j] = static_cast<uint8_t*>(head.o[j]);
     }
+    for (int u = 0; u < Pu; ++u) prm->lse[u] = head.lse[u];  // unit u's rows of every ring group
     if (err == cudaSuccess) {
         const long long n_items = (long long)Pu * b * Hq * prm->n_pairs;
         prm->band_units = band_units_for(s, d, Pu * b * Hk);
@@ -726,6 +727,45 @@ cudaError_t launch_attention_tc_usp(int Pu, int Pr, int b, int s, int h_q, int h
     delete prm;
     return err;
 }
+
+namespace {
+
+// Row statistics for the backward: D and the base-2 log-sum-exp of every query row, into
+// per-head-rank arrays (n_head_ranks of them, h_q / n_head_ranks heads each), all in one grid.
+// O and dO are read in head layout (one buffer per head rank) or in seq layout (n_seq_ranks
+// buffers of s / n_seq_ranks tokens, all heads).
+cudaError_t launch_bwd_prep(int n_head_ranks, int n_seq_ranks, int b, int s, int h_q, int d, const BwdPtrs& ptrs,
+                            cudaStream_t stream) {
+    const int n_tiles = (s + 127) / 128;
+    PrepParams* pp = new PrepParams;
+    memset(pp, 0, sizeof(PrepParams));
+    const int nb = ptrs.od_seq_layout ? n_seq_ranks : n_head_ranks;
+    for (int r = 0; r < nb; ++r) {
+        pp->o[r] = static_cast<const uint8_t*>(ptrs.o_rows[r]);
+        pp->dout[r] = static_cast<const uint8_t*>(ptrs.do_rows[r]);
+    }
+    for (int r = 0; r < n_head_ranks; ++r) {
+        pp->lse[r] = ptrs.lse[r];
+        pp->lse2[r] = ptrs.lse2[r];
+        pp->dsum[r] = ptrs.dsum[r];
+    }
+    pp->b = b;
+    pp->s = s;
+    pp->s_pad = n_tiles * 128;
+    pp->Hq = h_q / n_head_ranks;
+    pp->d = d;
+    pp->S = s / n_seq_ranks;
+    pp->hq_total = h_q;
+    pp->seq_layout = ptrs.od_seq_layout ? 1 : 0;
+    pp->lanes_log2 = d == 64 ? 3 : 4;
+    pp->rows = (long long)n_head_ranks * b * pp->Hq * pp->s_pad;
+    const long long threads = pp->rows << pp->lanes_log2;
+    bwd_prep_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, stream>>>(*pp);
+    delete pp;
+    return cudaGetLastError();
+}
+
+}  // namespace
 
 cudaError_t launch_attention_bwd_tc(int P, int b, int s, int h_q, int h_kv, int d, int causal, int fused,
                                     const BwdPtrs& ptrs, cudaStream_t stream, int* unsupported) {
@@ -737,29 +777,7 @@ cudaError_t launch_attention_bwd_tc(int P, int b, int s, int h_q, int h_kv, int 
     const int Hq = h_q / P, Hk = h_kv / P;
     const int n_tiles = (s + 127) / 128;
     // (1) row sums D and base-2 log-sum-exp, all ranks in one grid
-    PrepParams* pp = new PrepParams;
-    memset(pp, 0, sizeof(PrepParams));
-    for (int r = 0; r < P; ++r) {
-        pp->o[r] = static_cast<const uint8_t*>(ptrs.o_rows[r]);
-        pp->dout[r] = static_cast<const uint8_t*>(ptrs.do_rows[r]);
-        pp->lse[r] = ptrs.lse[r];
-        pp->lse2[r] = ptrs.lse2[r];
-        pp->dsum[r] = ptrs.dsum[r];
-    }
-    pp->b = b;
-    pp->s = s;
-    pp->s_pad = n_tiles * 128;
-    pp->Hq = Hq;
-    pp->d = d;
-    pp->S = s / P;
-    pp->hq_total = h_q;
-    pp->seq_layout = ptrs.od_seq_layout ? 1 : 0;
-    pp->lanes_log2 = d == 64 ? 3 : 4;
-    pp->rows = (long long)P * b * Hq * pp->s_pad;
-    const long long threads = pp->rows << pp->lanes_log2;
-    bwd_prep_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, stream>>>(*pp);
-    delete pp;
-    cudaError_t err = cudaGetLastError();
+    cudaError_t err = launch_bwd_prep(P, P, b, s, h_q, d, ptrs, stream);
     if (err != cudaSuccess) return err;
     // (2) dK/dV and dQ: one launch pair over seq-layout buffers (fused), else up to kMaxMaps
     //     head ranks per launch pair
@@ -772,6 +790,7 @@ cudaError_t launch_attention_bwd_tc(int P, int b, int s, int h_q, int h_kv, int 
     prm->b = b;
     prm->causal = causal ? 1 : 0;
     prm->hq_rank = Hq;
+    prm->map_stride = 1;
     prm->scale = (float)(1.0 / std::sqrt((double)d));
     prm->scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)d));
     if (fused) {
@@ -815,6 +834,54 @@ cudaError_t launch_attention_bwd_tc(int P, int b, int s, int h_q, int h_kv, int 
             err = d == 64 ? launch_bwd_d<64>(*prm, nr, stream) : launch_bwd_d<128>(*prm, nr, stream);
         }
     }
+    delete prm;
+    return err;
+}
+
+cudaError_t launch_attention_bwd_tc_usp(int Pu, int Pr, int b, int s, int h_q, int h_kv, int d, int causal,
+                                        const BwdPtrs& ptrs, cudaStream_t stream, int* unsupported) {
+    *unsupported = 0;
+    const int P = Pu * Pr, L = s / Pr;
+    if (!tc_attention_supported(d) || P > kMaxMaps || L % 128 != 0) {
+        *unsupported = 1;
+        return cudaSuccess;
+    }
+    const int Hq = h_q / Pu, Hk = h_kv / Pu;
+    const int n_tiles = (s + 127) / 128;
+    // (1) statistics per Ulysses unit (Pu head ranks over all s rows), O and dO in seq layout
+    cudaError_t err = launch_bwd_prep(Pu, P, b, s, h_q, d, ptrs, stream);
+    if (err != cudaSuccess) return err;
+    // (2) dK/dV and dQ over the Pu units, every tile read from (written to) the buffer of the
+    //     ring group that holds its tokens: the forward's two-level tile addressing
+    BwdParams* prm = new BwdParams;
+    memset(prm, 0, sizeof(BwdParams));
+    prm->s = s;
+    prm->s_pad = n_tiles * 128;
+    prm->n_tiles = n_tiles;
+    prm->g = h_q / h_kv;
+    prm->b = b;
+    prm->causal = causal ? 1 : 0;
+    prm->hq_rank = Hq;
+    prm->hq = Hq;
+    prm->hkv = Hk;
+    prm->rows_per_map = L;
+    prm->map_stride = Pu;
+    prm->scale = (float)(1.0 / std::sqrt((double)d));
+    prm->scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)d));
+    for (int j = 0; j < P && err == cudaSuccess; ++j) {
+        if (!make_map(&prm->mq[j], ptrs.q[j], b, L, Hq, d, 128) || !make_map(&prm->mk[j], ptrs.k[j], b, L, Hk, d, 128) ||
+            !make_map(&prm->mv[j], ptrs.v[j], b, L, Hk, d, 128) ||
+            !make_map(&prm->mdo[j], ptrs.dout[j], b, L, Hq, d, 128))
+            err = cudaErrorInvalidValue;
+        prm->dq[j] = static_cast<uint8_t*>(ptrs.dq[j]);
+        prm->dk[j] = static_cast<uint8_t*>(ptrs.dk[j]);
+        prm->dv[j] = static_cast<uint8_t*>(ptrs.dv[j]);
+    }
+    for (int u = 0; u < Pu; ++u) {
+        prm->lse2[u] = ptrs.lse2[u];
+        prm->dsum[u] = ptrs.dsum[u];
+    }
+    if (err == cudaSuccess) err = d == 64 ? launch_bwd_d<64>(*prm, Pu, stream) : launch_bwd_d<128>(*prm, Pu, stream);
     delete prm;
     return err;
 }

@@ -76,6 +76,11 @@ struct BwdPtrs {
 };
 cudaError_t launch_attention_bwd_tc(int P, int b, int s, int h_q, int h_kv, int d, int causal, int fused,
                                     const BwdPtrs& ptrs, cudaStream_t stream, int* unsupported);
+// Backward of the two-level forward: q/k/v/dout/dq/dk/dv are the P = Pu*Pr ranks' buffers in
+// the group head layout [b][s/Pr][h/Pu][d]; o_rows/do_rows the seq-layout O and dO
+// (od_seq_layout must be 1); lse/lse2/dsum one array per Ulysses unit u < Pu over all s rows.
+cudaError_t launch_attention_bwd_tc_usp(int Pu, int Pr, int b, int s, int h_q, int h_kv, int d, int causal,
+                                        const BwdPtrs& ptrs, cudaStream_t stream, int* unsupported);
 
 // Device error word of the tensor-core kernels (bounded waits that gave up).
 cudaError_t read_device_error(unsigned int* value, int clear);
