@@ -558,7 +558,8 @@ def run_overlap(args):
 
 def run_usp(args):
     """The two-level (Ulysses x Ring) forward against the plain Ulysses forward (unfused and
-    fused) over the same ranks, each call bracketed by CUDA events."""
+    fused) over the same ranks, each call bracketed by CUDA events; with --backward, the two
+    paths' backward instead."""
     import torch
 
     import sequence_attention_seq_gb300 as uly
@@ -581,6 +582,27 @@ def run_usp(args):
                                                                 workspace=ws_d),
         "ulysses_fused_p8": lambda: uly.ulysses_dist_attn_fwd(qs, ks, vs, True, fused=True, out_seq=out),
     }
+    flops = {name: fl for name in calls}
+    if args.backward:  # training: the backward of each path (2.5x the forward's algorithmic FLOPs)
+        from sequence_attention_seq_gb300.inputs import global_grad, shard_seq
+
+        del ws_d
+        dos = shard_seq(global_grad(b, s, hq, d, torch.bfloat16, seed=1, device="cuda"), P)
+        o_u, lse_u = uly.ulysses_usp_attn_fwd_lse(qs, ks, vs, True, Pu, Pr)
+        o_p, lse_p = uly.ulysses_dist_attn_fwd_lse(qs, ks, vs, True, fused=True)
+        grads = ([torch.empty_like(x) for x in qs], [torch.empty_like(x) for x in ks],
+                 [torch.empty_like(x) for x in vs])
+        ws_ub = torch.empty(uly.ulysses_usp_bwd_workspace_bytes(Pu, Pr, b, s, hq, hkv, d, torch.bfloat16),
+                            dtype=torch.uint8, device="cuda")
+        ws_pb = torch.empty(max(1, uly.ulysses_attn_bwd_workspace_bytes(P, b, s, hq, hkv, d, torch.bfloat16, True,
+                                                                        True)), dtype=torch.uint8, device="cuda")
+        calls = {
+            "usp_4x2_bwd": lambda: uly.ulysses_usp_attn_bwd(qs, ks, vs, o_u, dos, lse_u, True, Pu, Pr, grads=grads,
+                                                            workspace=ws_ub),
+            "ulysses_fused_p8_bwd": lambda: uly.ulysses_dist_attn_bwd(qs, ks, vs, o_p, dos, lse_p, True,
+                                                                      grads=grads, workspace=ws_pb, fused=True),
+        }
+        flops = {name: 2.5 * fl for name in calls}
     rows = {}
     clocks = ClockSampler(0)
     clocks.start()
@@ -596,12 +618,13 @@ def run_usp(args):
             e1.record()
         torch.cuda.synchronize()
         ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in evs)
-        rows[name] = {"ms": ms, "tflops": fl / (ms * 1e-3) / 1e12}
+        rows[name] = {"ms": ms, "tflops": flops[name] / (ms * 1e-3) / 1e12}
     if uly.ulysses_device_status(clear=True) != 0:
         raise RuntimeError("a kernel's bounded wait gave up")
     clk = clocks.stop()
-    print(json.dumps({"metric": "two-level Ulysses x Ring forward vs plain Ulysses over the same 8 ranks",
-                      "unit": "TFLOP/s (algorithmic attention flops / whole forward time)", "workload": w["name"],
+    what = "backward" if args.backward else "forward"
+    print(json.dumps({"metric": f"two-level Ulysses x Ring {what} vs plain Ulysses over the same 8 ranks",
+                      "unit": f"TFLOP/s (algorithmic attention flops / whole {what} time)", "workload": w["name"],
                       "steps": args.steps, "results": rows, "clocks": clk}))
 
 
