@@ -337,6 +337,16 @@ uly_status ulysses_dist_attn_bwd(int P, int b, int s, int h_q, int h_kv, int d, 
                                  void* workspace, size_t workspace_bytes, int fused, cudaStream_t stream);
 
 /*
+ * Self-test of the failure path: enqueues one CTA that waits, with the same bounded wait the
+ * kernels use, on a barrier that nothing completes; after limit_ns nanoseconds
+ * (1e3 .. 1e10, else ULY_ERR_INVALID_ARG) it gives up, sets the timeout bit of the device
+ * error word and returns, leaving the context usable.  ulysses_device_status then reports
+ * ULY_ERR_TIMEOUT.  Until that status is read with clear != 0, every kernel of this library
+ * that starts sees the error word and exits at once.
+ */
+uly_status ulysses_wait_selftest(unsigned long long limit_ns, cudaStream_t stream);
+
+/*
  * Reads (and, if clear != 0, resets) the library's device-side error word after
  * synchronising the current device.  Returns ULY_ERR_TIMEOUT if a kernel's bounded wait
  * gave up since the last reset (that kernel then wrote no output), ULY_ERR_CUDA if the

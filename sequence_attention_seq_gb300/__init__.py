@@ -26,6 +26,7 @@ __all__ = [
     "ulysses_local_attention_bwd", "ulysses_dist_attn_bwd", "ulysses_dist_attn_overlap_workspace_bytes",
     "ulysses_dist_attn_fwd_overlap", "ulysses_usp_workspace_bytes", "ulysses_usp_attn_fwd",
     "ulysses_usp_attn_fwd_lse", "ulysses_usp_bwd_workspace_bytes", "ulysses_usp_attn_bwd",
+    "ulysses_wait_selftest",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -42,7 +43,7 @@ EXPORTED_SYMBOLS = (
     "ulysses_dist_attn_fwd_lse", "ulysses_attn_bwd_workspace_bytes", "ulysses_local_attention_bwd",
     "ulysses_dist_attn_bwd", "ulysses_dist_attn_overlap_workspace_bytes", "ulysses_dist_attn_fwd_overlap",
     "ulysses_usp_workspace_bytes", "ulysses_usp_attn_fwd", "ulysses_usp_attn_fwd_lse",
-    "ulysses_usp_bwd_workspace_bytes", "ulysses_usp_attn_bwd",
+    "ulysses_usp_bwd_workspace_bytes", "ulysses_usp_attn_bwd", "ulysses_wait_selftest",
 )
 
 _lock = threading.Lock()
@@ -111,6 +112,8 @@ def load_library():
         lib.ulysses_usp_attn_bwd.argtypes = [i, i, i, i, i, i, i, i, i, pp, pp, pp, pp, pp, pp, pp, pp, pp, vp, sz,
                                              vp]
         lib.ulysses_usp_attn_bwd.restype = i
+        lib.ulysses_wait_selftest.argtypes = [ctypes.c_ulonglong, vp]
+        lib.ulysses_wait_selftest.restype = i
         lib.ulysses_device_status.argtypes = [i]
         lib.ulysses_device_status.restype = i
         lib.ulysses_status_string.argtypes = [i]
@@ -498,3 +501,9 @@ def ulysses_usp_attn_bwd(q_seq, k_seq, v_seq, o_seq, do_seq, lse, causal, Pu, Pr
         _ptr_array(dv), workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream(stream)),
         "ulysses_usp_attn_bwd")
     return dq, dk, dv
+
+
+def ulysses_wait_selftest(limit_ns=50_000_000, stream=None):
+    """Enqueue one CTA whose bounded wait on a barrier that nothing completes gives up after
+    limit_ns; ulysses_device_status() then reports the timeout (read it with clear=True)."""
+    _check(load_library().ulysses_wait_selftest(int(limit_ns), _stream(stream)), "ulysses_wait_selftest")

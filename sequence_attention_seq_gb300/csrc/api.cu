@@ -902,6 +902,11 @@ uly_status ulysses_usp_attn_bwd(int Pu, int Pr, int b, int s, int h_q, int h_kv,
     return ce == cudaSuccess ? ULY_OK : ULY_ERR_CUDA;
 }
 
+uly_status ulysses_wait_selftest(unsigned long long limit_ns, cudaStream_t stream) {
+    if (limit_ns < 1000ull || limit_ns > 10000000000ull) return ULY_ERR_INVALID_ARG;
+    return uly::launch_wait_selftest(limit_ns, stream) == cudaSuccess ? ULY_OK : ULY_ERR_CUDA;
+}
+
 uly_status ulysses_device_status(int clear) {
     unsigned int v = 0;
     if (uly::read_device_error(&v, clear) != cudaSuccess) return ULY_ERR_CUDA;

@@ -121,7 +121,8 @@ __device__ __forceinline__ bool error_word_set() {
 
 // Bounded wait on an mbarrier phase.  Returns false (and raises the CTA abort flag) when
 // the time limit passes, the CTA is aborting, or another CTA reported an error.
-__device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, Shared* sh) {
+__device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, Shared* sh,
+                                           uint64_t limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     for (uint32_t it = 1;; ++it) {
@@ -132,13 +133,29 @@ __device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, Share
                 sh->abort = 1;
                 return false;
             }
-            if (global_timer_ns() - t0 > kWaitLimitNs) {
+            if (global_timer_ns() - t0 > limit_ns) {
                 atomicOr(&g_uly_error_word, kErrTimeout);
                 sh->abort = 1;
                 return false;
             }
         }
     }
+}
+
+// Self-test of the wait above: one warp waits on a barrier that nothing ever completes, with
+// the given limit, exactly as the attention kernels' waits do; the wait gives up, raises the
+// timeout bit of the device error word and the kernel returns.
+__global__ void wait_selftest_kernel(uint64_t limit_ns) {
+    __shared__ uint64_t bar;
+    __shared__ Shared sh;
+    if (threadIdx.x == 0) {
+        sh.abort = 0;
+        mbar_init(&bar, 1);
+        fence_mbarrier_init();
+    }
+    __syncthreads();
+    wait_phase(&bar, 0, &sh, limit_ns);  // no arrival: phase 0 never completes
+    __syncthreads();
 }
 
 // Warp-uniform version for warps whose next step is a .sync.aligned tcgen05 collective.
@@ -884,6 +901,11 @@ cudaError_t launch_attention_bwd_tc_usp(int Pu, int Pr, int b, int s, int h_q, i
     if (err == cudaSuccess) err = d == 64 ? launch_bwd_d<64>(*prm, Pu, stream) : launch_bwd_d<128>(*prm, Pu, stream);
     delete prm;
     return err;
+}
+
+cudaError_t launch_wait_selftest(uint64_t limit_ns, cudaStream_t stream) {
+    wait_selftest_kernel<<<1, 32, 0, stream>>>(limit_ns);
+    return cudaGetLastError();
 }
 
 cudaError_t read_device_error(unsigned int* value, int clear) {

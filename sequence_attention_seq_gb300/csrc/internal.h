@@ -83,6 +83,9 @@ cudaError_t launch_attention_bwd_tc_usp(int Pu, int Pr, int b, int s, int h_q, i
                                         const BwdPtrs& ptrs, cudaStream_t stream, int* unsupported);
 
 // Device error word of the tensor-core kernels (bounded waits that gave up).
+// One CTA whose bounded wait on a barrier that never completes gives up after limit_ns and
+// sets the timeout bit of the device error word (the failure path, exercised without a fault).
+cudaError_t launch_wait_selftest(uint64_t limit_ns, cudaStream_t stream);
 cudaError_t read_device_error(unsigned int* value, int clear);
 
 }  // namespace uly
