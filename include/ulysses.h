@@ -81,10 +81,17 @@ uly_status ulysses_a2a_head2seq(int P, int b, int s, int h, int d, uly_dtype dty
  * causal != 0 masks keys j > i (global positions: after all-to-all #1 the local token
  * index is the global one -- "长上下文训练中的 SP 与 CP", section on Ring Attention,
  * causal paragraph).  The scale is fixed at 1/sqrt(d).
- * Sizes: P, b, s >= 1; h_q % P == 0, h_kv % P == 0, h_q % h_kv == 0 (grouped K/V heads:
- * rank r's query heads read only its own K/V heads -- "02 · DeepSpeed-Ulysses", section 3).
+ * Sizes: P, b, s >= 1; h_q % P == 0, h_q % h_kv == 0 (grouped K/V heads: rank r's query
+ * heads read only the K/V heads it holds -- "02 · DeepSpeed-Ulysses", section 3), and
+ * either h_kv % P == 0 (every rank holds h_kv/P K/V heads) or P % h_kv == 0 (fewer K/V
+ * heads than ranks: each K/V head is replicated on the rep = P/h_kv ranks whose query
+ * heads use it, rank r holding head r/rep -- "DeepSpeed-Ulysses 深度解析", sections
+ * "两行代码替换注意力" (num_kv_heads) and "构建序列并行通信组" (head counts and the
+ * degree divide each other, one way or the other); "长上下文训练中的 SP 与 CP", section on
+ * Ulysses (replicating K/V lifts the divisibility rule at the cost of memory and traffic)).
+ * Else ULY_ERR_INVALID_ARG.  Below, Hk = h_kv/P, or 1 when replicated.
  * q_head / o_head: P pointers to [b][s][h_q/P][d]; k_head / v_head: P pointers to
- * [b][s][h_kv/P][d].
+ * [b][s][Hk][d].
  * Kernels: ULY_BF16 with d in {64, 128} (tcgen05 tensor cores, fp32 accumulation, the
  * softmax weights rounded to bf16 before the P.V product, output rounded to nearest even);
  * ULY_FP32 with d % 4 == 0 and d <= 256 (fp32 FMA, no tensor cores).  Other combinations
@@ -108,7 +115,9 @@ size_t ulysses_dist_attn_workspace_bytes(int P, int b, int s, int h_q, int h_kv,
  * The whole DistributedAttention forward ("DeepSpeed-Ulysses 深度解析", steps 3-5):
  * all-to-all #1 on Q, K and V, local attention on every rank, all-to-all #2 on the output.
  *   q_seq / o_seq: P pointers to [b][s/P][h_q][d]; k_seq / v_seq: P pointers to
- *   [b][s/P][h_kv][d].  Size rules as ulysses_local_attention.
+ *   [b][s/P][h_kv][d].  Size rules as ulysses_local_attention.  With replicated K/V
+ *   heads all-to-all #1 sends K/V head r/rep to rank r (a broadcast of every head to its
+ *   rep ranks).
  * fused == 0: three launches (one for the Q, K and V exchanges, one attention, one
  *   output exchange) through `workspace` (device memory, 256-byte aligned, at least
  *   ulysses_dist_attn_workspace_bytes(...) bytes, owned by the caller).
@@ -141,7 +150,7 @@ uly_status ulysses_dist_attn_fwd(int P, int b, int s, int h_q, int h_kv, int d, 
  * plus: 1 <= n_chunks <= 64 and (h_q/P) % n_chunks == 0, and either (h_kv/P) % n_chunks
  * == 0 (every chunk has its own K/V heads) or n_chunks % (h_kv/P) == 0 (grouped heads:
  * n_chunks/(h_kv/P) consecutive chunks share one K/V head, exchanged with the first of
- * them), else ULY_ERR_INVALID_ARG;
+ * them), and h_kv % P == 0 (no replicated K/V heads), else ULY_ERR_INVALID_ARG;
  * workspace: 256-byte aligned, at least ulysses_dist_attn_overlap_workspace_bytes(...)
  * bytes (the chunks' head-layout Q, K, V, O).  The call creates and destroys CUDA events
  * (host objects) for the cross-stream ordering; it allocates no device memory.
@@ -204,7 +213,8 @@ uly_status ulysses_usp_attn_fwd(int Pu, int Pr, int b, int s, int h_q, int h_kv,
  *     3. all-to-all #2 on dQ, dK, dV inside every ring group.
  *   Same sizes and kernel limits as ulysses_usp_attn_fwd, bf16 only.  dq/dk/dv must not
  *   overlap each other or any input.  The results equal ulysses_dist_attn_bwd over the same
- *   P ranks bit for bit (where that call accepts the shape: h_kv % P == 0).  workspace:
+ *   P ranks bit for bit where h_kv % P == 0 (with replicated K/V heads the plain call's
+ *   dK/dV come from another summation order).  workspace:
  *   256-byte aligned, at least ulysses_usp_bwd_workspace_bytes(...) bytes (every rank's group
  *   head-layout Q, K, V, dO, dQ, dK, dV and, per Ulysses unit, two fp32 row arrays); it
  *   returns 0 for shapes the call rejects.
@@ -300,7 +310,9 @@ size_t ulysses_attn_bwd_workspace_bytes(int P, int b, int s, int h_q, int h_kv, 
 /*
  * Backward of ulysses_local_attention, head layout in and out.
  *   q_head, o_head, do_head, dq_head: P pointers to [b][s][h_q/P][d];
- *   k_head, v_head, dk_head, dv_head: P pointers to [b][s][h_kv/P][d];
+ *   k_head, v_head, dk_head, dv_head: P pointers to [b][s][Hk][d] (Hk as in
+ *   ulysses_local_attention; with replicated K/V heads dk_head / dv_head hold each
+ *   rank's share only, the gradient of its own query heads);
  *   lse: from ulysses_local_attention_fwd_lse on the same q, k (and causal flag).
  * Four launches: row statistics, dK/dV, dQ (one pair per 16 ranks).  Outputs must not
  * overlap each other, any input or the workspace (256-byte aligned, at least
@@ -326,6 +338,11 @@ uly_status ulysses_local_attention_bwd(int P, int b, int s, int h_q, int h_kv, i
  *   q_seq, o_seq, do_seq, dq_seq: P pointers to [b][s/P][h_q][d];
  *   k_seq, v_seq, dk_seq, dv_seq: P pointers to [b][s/P][h_kv][d];
  *   lse: from ulysses_dist_attn_fwd_lse (head-layout indexed).
+ * Replicated K/V heads (P % h_kv == 0, h_kv < P): dK and dV of head h are the sum of
+ *   the shares of its rep ranks.  fused == 0 writes the shares in fp32 and adds them in
+ *   a fixed order before one rounding to bf16 (the reverse of the broadcast); fused != 0
+ *   needs no sum, since its dK/dV kernel owns every global K/V head and reads all of that
+ *   head's query heads.
  * workspace: 256-byte aligned, at least ulysses_attn_bwd_workspace_bytes(..., dist = 1,
  * fused) bytes.  Size and overlap rules as ulysses_local_attention_bwd plus the exchange rules.
  */

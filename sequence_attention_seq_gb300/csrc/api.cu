@@ -63,9 +63,22 @@ uly_status check_exchange_shape(int P, int b, int s, int h, int d, uly_dtype dt)
     return ULY_OK;
 }
 
+// The K/V exchange of the attention pipeline: split (P | h_kv) or replicated (h_kv | P, one
+// head per rank).
+uly_status check_kv_exchange_shape(int P, int b, int s, int h_kv, int d, uly_dtype dt) {
+    if (h_kv < 1 || h_kv >= P || P % h_kv) return check_exchange_shape(P, b, s, h_kv, d, dt);
+    return check_exchange_shape(P, b, s, P, d, dt);  // one head per rank, like P heads split P ways
+}
+
+// K/V heads either split over the ranks (P | h_kv) or, with fewer K/V heads than ranks,
+// replicated on P / h_kv ranks each (h_kv | P): the head counts must be multiples of one
+// another ("DeepSpeed-Ulysses 深度解析", API section, num_kv_heads; "02 · DeepSpeed-Ulysses",
+// section 3: replicating K/V lifts the divisibility limit at a cost in memory and traffic).
+uly_status check_kv_exchange_shape(int P, int b, int s, int h_kv, int d, uly_dtype dt);
+
 uly_status check_attention_shape(int P, int b, int s, int hq, int hkv, int d, uly_dtype dt) {
     if (P < 1 || P > kMaxRanks || b < 1 || s < 1 || hq < 1 || hkv < 1 || d < 1) return ULY_ERR_INVALID_ARG;
-    if (hq % P || hkv % P || hq % hkv) return ULY_ERR_INVALID_ARG;
+    if (hq % P || hq % hkv || (hkv % P && P % hkv)) return ULY_ERR_INVALID_ARG;
     if (!elem_bytes(dt)) return ULY_ERR_INVALID_ARG;
     if ((long long)b * P > 65535 || hq / P > 65535) return ULY_ERR_INVALID_ARG;
     if ((long long)b * hq * ((s + 127) / 128) > 0x7fffffffLL) return ULY_ERR_INVALID_ARG;
@@ -138,7 +151,8 @@ uly_status local_attention(int P, int b, int s, int h_q, int h_kv, int d, uly_dt
     uly_status st = check_attention_shape(P, b, s, h_q, h_kv, d, dtype);
     if (st != ULY_OK) return st;
     const int e = elem_bytes(dtype);
-    const uint64_t qb = (uint64_t)b * s * (h_q / P) * d * e, kb = (uint64_t)b * s * (h_kv / P) * d * e;
+    const uint64_t qb = (uint64_t)b * s * (h_q / P) * d * e,
+                   kb = (uint64_t)b * s * uly::kv_heads_per_rank(P, h_kv) * d * e;
     std::vector<Range> rq, rk, rv, ro, rl;
     if (!collect(q_head, P, qb, rq) || !collect(k_head, P, kb, rk) || !collect(v_head, P, kb, rv) ||
         !collect(reinterpret_cast<const void* const*>(o_head), P, qb, ro))
@@ -182,8 +196,11 @@ std::vector<uint64_t> bwd_sizes(int P, int b, int s, int hq, int hkv, int d, int
     const uint64_t ra = row_array_bytes(P, b, s, hq);
     std::vector<uint64_t> v{ra, ra};
     if (dist == 1) {
-        const uint64_t qb = (uint64_t)b * s * (hq / P) * d * 2, kb = (uint64_t)b * s * (hkv / P) * d * 2;
-        for (uint64_t x : {qb, kb, kb, qb, qb, kb, kb}) v.push_back(x);
+        const uint64_t qb = (uint64_t)b * s * (hq / P) * d * 2,
+                       kb = (uint64_t)b * s * uly::kv_heads_per_rank(P, hkv) * d * 2;
+        // replicated K/V heads: each rank's dK/dV is an fp32 partial sum
+        const uint64_t gb = uly::kv_replication(P, hkv) > 1 ? 2 * kb : kb;
+        for (uint64_t x : {qb, kb, kb, qb, qb, gb, gb}) v.push_back(x);
     }
     return v;
 }
@@ -202,7 +219,7 @@ size_t dist_workspace_bytes(int P, int b, int s, int h_q, int h_kv, int d, uly_d
     if (fused) return 0;
     const int e = elem_bytes(dtype);
     const uint64_t qb = round256((uint64_t)b * s * (h_q / P) * d * e);
-    const uint64_t kb = round256((uint64_t)b * s * (h_kv / P) * d * e);
+    const uint64_t kb = round256((uint64_t)b * s * uly::kv_heads_per_rank(P, h_kv) * d * e);
     return (size_t)((uint64_t)P * (2 * qb + 2 * kb));
 }
 
@@ -215,7 +232,7 @@ uly_status dist_attn_fwd(int P, int b, int s, int h_q, int h_kv, int d, uly_dtyp
     if (st != ULY_OK) return st;
     st = check_exchange_shape(P, b, s, h_q, d, dtype);
     if (st != ULY_OK) return st;
-    st = check_exchange_shape(P, b, s, h_kv, d, dtype);
+    st = check_kv_exchange_shape(P, b, s, h_kv, d, dtype);
     if (st != ULY_OK) return st;
     const int e = elem_bytes(dtype);
     const int S = s / P;
@@ -255,7 +272,7 @@ uly_status dist_attn_fwd(int P, int b, int s, int h_q, int h_kv, int d, uly_dtyp
 
     // workspace: per rank [Q_head | K_head | V_head | O_head], each 256-byte aligned
     const uint64_t qhb = round256((uint64_t)b * s * (h_q / P) * d * e);
-    const uint64_t khb = round256((uint64_t)b * s * (h_kv / P) * d * e);
+    const uint64_t khb = round256((uint64_t)b * s * uly::kv_heads_per_rank(P, h_kv) * d * e);
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     uly::AttnPtrs head;
     memset(&head, 0, sizeof(head));
@@ -281,6 +298,7 @@ uly_status dist_attn_fwd(int P, int b, int s, int h_q, int h_kv, int d, uly_dtyp
     t[0].h = h_q;
     t[1].h = h_kv;
     t[2].h = h_kv;
+    t[1].rep = t[2].rep = uly::kv_replication(P, h_kv);  // fewer K/V heads than ranks: copies
     if (uly::launch_permute(0, P, b, s, d, e, t, 3, stream) != cudaSuccess) return ULY_ERR_CUDA;
     // (2) local attention of every rank
     st = run_attention(P, b, s, h_q, h_kv, d, dtype, causal, 0, head, stream);
@@ -353,7 +371,7 @@ size_t ulysses_attn_bwd_workspace_bytes(int P, int b, int s, int h_q, int h_kv, 
                                         int fused) {
     if (check_train_shape(P, b, s, h_q, h_kv, d, dtype) != ULY_OK) return 0;
     if (dist && (check_exchange_shape(P, b, s, h_q, d, dtype) != ULY_OK ||
-                 check_exchange_shape(P, b, s, h_kv, d, dtype) != ULY_OK))
+                 check_kv_exchange_shape(P, b, s, h_kv, d, dtype) != ULY_OK))
         return 0;
     uint64_t per_rank = 0;
     for (uint64_t x : bwd_sizes(P, b, s, h_q, h_kv, d, dist && !fused ? 1 : 0)) per_rank += round256(x);
@@ -368,7 +386,8 @@ uly_status ulysses_local_attention_bwd(int P, int b, int s, int h_q, int h_kv, i
                                        size_t workspace_bytes, cudaStream_t stream) {
     uly_status st = check_train_shape(P, b, s, h_q, h_kv, d, dtype);
     if (st != ULY_OK) return st;
-    const uint64_t qb = (uint64_t)b * s * (h_q / P) * d * 2, kb = (uint64_t)b * s * (h_kv / P) * d * 2;
+    const uint64_t qb = (uint64_t)b * s * (h_q / P) * d * 2,
+                   kb = (uint64_t)b * s * uly::kv_heads_per_rank(P, h_kv) * d * 2;
     std::vector<Range> in, rdq, rdk, rdv;
     if (!collect(q_head, P, qb, in) || !collect(k_head, P, kb, in) || !collect(v_head, P, kb, in) ||
         !collect(o_head, P, qb, in) || !collect(do_head, P, qb, in) ||
@@ -417,7 +436,7 @@ uly_status ulysses_dist_attn_bwd(int P, int b, int s, int h_q, int h_kv, int d, 
     if (st != ULY_OK) return st;
     st = check_exchange_shape(P, b, s, h_q, d, dtype);
     if (st != ULY_OK) return st;
-    st = check_exchange_shape(P, b, s, h_kv, d, dtype);
+    st = check_kv_exchange_shape(P, b, s, h_kv, d, dtype);
     if (st != ULY_OK) return st;
     const int S = s / P;
     const uint64_t qsb = (uint64_t)b * S * h_q * d * 2, ksb = (uint64_t)b * S * h_kv * d * 2;
@@ -476,6 +495,7 @@ uly_status ulysses_dist_attn_bwd(int P, int b, int s, int h_q, int h_kv, int d, 
             t[k].dst[r] = ws.at(r, dsts[k]);
         }
         t[k].h = (k == 1 || k == 2) ? h_kv : h_q;
+        if (k == 1 || k == 2) t[k].rep = uly::kv_replication(P, h_kv);
     }
     cudaError_t ce = uly::launch_permute(0, P, b, s, d, 2, t, 4, stream);
     delete[] t;
@@ -498,10 +518,15 @@ uly_status ulysses_dist_attn_bwd(int P, int b, int s, int h_q, int h_kv, int d, 
         p->dsum[r] = static_cast<float*>(ws.at(r, DSUM));
     }
     p->od_seq_layout = 1;
+    p->kv_grad_f32 = uly::kv_replication(P, h_kv) > 1 ? 1 : 0;
     st = run_backward(P, b, s, h_q, h_kv, d, causal, 0, *p, stream);
     delete p;
     if (st != ULY_OK) return st;
-    // (3) all-to-all #2 on dQ, dK, dV (the backward of all-to-all #1)
+    // (3) all-to-all #2 on dQ, dK, dV (the backward of all-to-all #1).  Replicated K/V heads:
+    //     every replica holds the gradient from its own query heads, and the backward of the
+    //     copy is their sum
+    const int kv_rep = uly::kv_replication(P, h_kv);
+    const int n_plain = kv_rep > 1 ? 1 : 3;
     t = new uly::PermuteTensor[3];
     memset(t, 0, 3 * sizeof(uly::PermuteTensor));
     void* const* dsts2[3] = {dq_seq, dk_seq, dv_seq};
@@ -513,7 +538,9 @@ uly_status ulysses_dist_attn_bwd(int P, int b, int s, int h_q, int h_kv, int d, 
         }
         t[k].h = k == 0 ? h_q : h_kv;
     }
-    ce = uly::launch_permute(1, P, b, s, d, 2, t, 3, stream);
+    ce = uly::launch_permute(1, P, b, s, d, 2, t, n_plain, stream);
+    for (int k = 1; k < 3 && kv_rep > 1 && ce == cudaSuccess; ++k)
+        ce = uly::launch_kv_grad_sum(P, kv_rep, b, s, h_kv, d, t[k].src, t[k].dst, stream);
     delete[] t;
     return ce == cudaSuccess ? ULY_OK : ULY_ERR_CUDA;
 }
@@ -533,7 +560,7 @@ struct OverlapPlan {
 OverlapPlan overlap_plan(int P, int h_q, int h_kv, int n_chunks) {
     OverlapPlan pl{n_chunks, 0, 0, 0, 1, false};
     const int Hq = h_q / P, Hk = h_kv / P;
-    if (n_chunks < 1 || n_chunks > kMaxChunks || Hq % n_chunks) return pl;
+    if (Hk < 1 || n_chunks < 1 || n_chunks > kMaxChunks || Hq % n_chunks) return pl;  // no replicated K/V
     pl.Hc = Hq / n_chunks;
     if (Hk % n_chunks == 0) {
         pl.Hkc = Hk / n_chunks;
@@ -675,7 +702,7 @@ uly_status ulysses_dist_attn_fwd_overlap(int P, int b, int s, int h_q, int h_kv,
 }
 
 size_t ulysses_usp_workspace_bytes(int Pu, int Pr, int b, int s, int h_q, int h_kv, int d, uly_dtype dtype) {
-    if (Pu < 1 || Pr < 1 || Pu * Pr > kMaxRanks || s % (Pu * Pr)) return 0;
+    if (Pu < 1 || Pr < 1 || Pu * Pr > kMaxRanks || s % (Pu * Pr) || h_kv < 1 || h_kv % Pu) return 0;
     if (check_attention_shape(Pu, b, s / Pr, h_q, h_kv, d, dtype) == ULY_ERR_INVALID_ARG) return 0;
     const int e = elem_bytes(dtype), L = s / Pr;
     const uint64_t qb = round256((uint64_t)b * L * (h_q / Pu) * d * e);

@@ -63,7 +63,7 @@ constexpr int kRingQ = 5;    // dQ kernel: K/V ring slots
 struct BwdParams {
     CUtensorMap mq[kMaxMaps], mk[kMaxMaps], mv[kMaxMaps], mdo[kMaxMaps];
     uint8_t* dq[kMaxMaps];        // [b][rows][hq][d] bf16
-    uint8_t* dk[kMaxMaps];        // [b][rows][hkv][d] bf16
+    uint8_t* dk[kMaxMaps];        // [b][rows][hkv][d] bf16 (fp32 with kv_grad_f32)
     uint8_t* dv[kMaxMaps];
     const float* lse2[kMaxMaps];  // per head rank [b][hq_rank][s_pad]: log-sum-exp, base-2 units (+inf on padding)
     const float* dsum[kMaxMaps];  // per head rank [b][hq_rank][s_pad]: D (0 on padding)
@@ -73,6 +73,7 @@ struct BwdParams {
     int hq_rank;                  // query heads per head rank
     float scale_log2;             // log2(e)/sqrt(d)
     float scale;                  // 1/sqrt(d)
+    int kv_grad_f32;              // host: launch the dK/dV kernel that stores fp32 partial sums
 };
 
 struct BwdTok {
@@ -185,6 +186,26 @@ __device__ __forceinline__ void store_row_bf16(uint32_t taddr, uint8_t* dst, flo
     }
 }
 
+// As store_row_bf16, in fp32 (a partial sum that is added to others before rounding).
+template <int NC>
+__device__ __forceinline__ void store_row_f32(uint32_t taddr, uint8_t* dst, float mul, bool ok) {
+#pragma unroll
+    for (int c = 0; c < NC / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld32(taddr + c * 32, r);
+        tmem_wait_ld();
+#pragma unroll
+        for (int q4 = 0; q4 < 8; ++q4) {
+            float4 v;
+            v.x = __uint_as_float(r[q4 * 4 + 0]) * mul;
+            v.y = __uint_as_float(r[q4 * 4 + 1]) * mul;
+            v.z = __uint_as_float(r[q4 * 4 + 2]) * mul;
+            v.w = __uint_as_float(r[q4 * 4 + 3]) * mul;
+            if (ok) *reinterpret_cast<float4*>(dst + (c * 32 + q4 * 4) * 4) = v;
+        }
+    }
+}
+
 // Initialises the barriers (those in [rows_from, rows_to) count one arrival per row warp)
 // and allocates tensor memory; false when the CTA must leave at once.
 __device__ __forceinline__ bool bwd_setup(uint64_t* bars, int nbars, int rows_from, int rows_to, int row_warps,
@@ -232,7 +253,8 @@ __device__ __forceinline__ void mma_acc_tmemA(uint32_t acc, uint32_t a_tmem, uin
 // ------------------------------------------------------------------ dK / dV
 // Block -> (rank, batch, K/V head, key tile), key tile fastest and ascending.
 // Tensor memory: S^T (then P^T) 0..127 | dP^T (then dS^T) 128..255 | dK 256.. | dV 384..
-template <int D, int RW>
+// F32: dk/dv receive fp32 partial sums (a replicated K/V head's share from this rank).
+template <int D, int RW, bool F32>
 __global__ void __launch_bounds__(RowCfg<RW>::kThreads, 1) bwd_dkdv_kernel(const __grid_constant__ BwdParams p) {
     using C = RowCfg<RW>;
     constexpr int kBwdRowWarps = C::kRows, kBwdProducer = C::kProducer, kBwdMma = C::kMma;
@@ -448,10 +470,16 @@ __global__ void __launch_bounds__(RowCfg<RW>::kThreads, 1) bwd_dkdv_kernel(const
             tc_fence_after();
             const bool kok = key < p.s;
             const BwdTok kt_ = bwd_tok(p, rank, kok ? key : k0);
+            constexpr size_t kEl = F32 ? 4 : 2;  // bytes per stored element
             const size_t off =
-                (((size_t)bb * p.rows_per_map + kt_.row) * p.hkv + kvh) * (size_t)D * 2 + cg * kEpi * 2;
-            store_row_bf16<kEpi>(tmem + 256u + lane_off + cg * kEpi, p.dk[kt_.map] + off, p.scale, kok);
-            store_row_bf16<kEpi>(tmem + 384u + lane_off + cg * kEpi, p.dv[kt_.map] + off, 1.0f, kok);
+                (((size_t)bb * p.rows_per_map + kt_.row) * p.hkv + kvh) * (size_t)D * kEl + cg * kEpi * kEl;
+            if constexpr (F32) {
+                store_row_f32<kEpi>(tmem + 256u + lane_off + cg * kEpi, p.dk[kt_.map] + off, p.scale, kok);
+                store_row_f32<kEpi>(tmem + 384u + lane_off + cg * kEpi, p.dv[kt_.map] + off, 1.0f, kok);
+            } else {
+                store_row_bf16<kEpi>(tmem + 256u + lane_off + cg * kEpi, p.dk[kt_.map] + off, p.scale, kok);
+                store_row_bf16<kEpi>(tmem + 384u + lane_off + cg * kEpi, p.dv[kt_.map] + off, 1.0f, kok);
+            }
         }
     }
     tc_fence_before();
@@ -671,15 +699,15 @@ template <int D>
 cudaError_t launch_bwd_d(const BwdParams& prm, int nranks, cudaStream_t stream) {
     using LK = BwdSmem<D, kRingKV>;
     using LQ = BwdSmem<D, kRingQ>;
-    cudaError_t e = cudaFuncSetAttribute(bwd_dkdv_kernel<D, kRowsKV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)LK::kAlloc);
+    auto* dkdv = prm.kv_grad_f32 ? bwd_dkdv_kernel<D, kRowsKV, true> : bwd_dkdv_kernel<D, kRowsKV, false>;
+    cudaError_t e = cudaFuncSetAttribute(dkdv, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)LK::kAlloc);
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(bwd_dq_kernel<D, kRowsQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)LQ::kAlloc);
     if (e != cudaSuccess) return e;
     const long long gk = (long long)nranks * prm.b * prm.hkv * prm.n_tiles;
     const long long gq = (long long)nranks * prm.b * prm.hq * prm.n_tiles;
-    bwd_dkdv_kernel<D, kRowsKV><<<(unsigned)gk, RowCfg<kRowsKV>::kThreads, LK::kAlloc, stream>>>(prm);
+    dkdv<<<(unsigned)gk, RowCfg<kRowsKV>::kThreads, LK::kAlloc, stream>>>(prm);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     bwd_dq_kernel<D, kRowsQ><<<(unsigned)gq, RowCfg<kRowsQ>::kThreads, LQ::kAlloc, stream>>>(prm);

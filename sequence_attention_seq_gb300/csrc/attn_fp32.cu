@@ -151,8 +151,8 @@ cudaError_t launch_attention_fp32(int P, int b, int s, int h_q, int h_kv, int d,
     prm.b = b;
     prm.s = s;
     prm.Hq = h_q / P;
-    prm.Hk = h_kv / P;
-    prm.g = h_q / h_kv;
+    prm.Hk = kv_heads_per_rank(P, h_kv);
+    prm.g = prm.Hq / prm.Hk;  // within a rank (its K/V heads may be replicas shared with other ranks)
     prm.d = d;
     prm.causal = causal ? 1 : 0;
     prm.scale = 1.0f / sqrtf((float)d);

@@ -679,9 +679,10 @@ cudaError_t launch_attention_tc(int P, int b, int s, int h_q, int h_kv, int d, i
             err = d == 64 ? launch_d<64>(*prm, n_items, stream) : launch_d<128>(*prm, n_items, stream);
         }
     } else {
-        const int Hq = h_q / P, Hk = h_kv / P;
+        const int Hq = h_q / P, Hk = kv_heads_per_rank(P, h_kv);
         prm->rows_per_map = s;
         prm->heads = Hq;
+        prm->g = Hq / Hk;  // within a rank (its K/V heads may be replicas shared with other ranks)
         prm->lse_heads = Hq;
         for (int r0 = 0; r0 < P && err == cudaSuccess; r0 += kMaxMaps) {
             const int nr = (P - r0) < kMaxMaps ? (P - r0) : kMaxMaps;
@@ -791,7 +792,7 @@ cudaError_t launch_attention_bwd_tc(int P, int b, int s, int h_q, int h_kv, int 
         *unsupported = 1;
         return cudaSuccess;
     }
-    const int Hq = h_q / P, Hk = h_kv / P;
+    const int Hq = h_q / P, Hk = kv_heads_per_rank(P, h_kv);
     const int n_tiles = (s + 127) / 128;
     // (1) row sums D and base-2 log-sum-exp, all ranks in one grid
     cudaError_t err = launch_bwd_prep(P, P, b, s, h_q, d, ptrs, stream);
@@ -832,6 +833,8 @@ cudaError_t launch_attention_bwd_tc(int P, int b, int s, int h_q, int h_kv, int 
         prm->rows_per_map = s;
         prm->hq = Hq;
         prm->hkv = Hk;
+        prm->g = Hq / Hk;  // within a rank (its K/V heads may be replicas shared with other ranks)
+        prm->kv_grad_f32 = ptrs.kv_grad_f32;
         for (int r0 = 0; r0 < P && err == cudaSuccess; r0 += kMaxMaps) {
             const int nr = (P - r0) < kMaxMaps ? (P - r0) : kMaxMaps;
             for (int i = 0; i < nr && err == cudaSuccess; ++i) {

@@ -19,11 +19,25 @@ struct PermuteTensor {
     int h;     // heads of this tensor in seq layout (h_q for Q/O, h_kv for K/V)
     int hsub;  // heads per rank moved by this call (0: all h/P); the head-layout side holds hsub heads
     int hoff;  // first moved head within each rank's group of h/P heads
+    int rep;   // > 1: K/V heads replicated (h < P, P % h == 0): rank r receives head r / rep only
+               // (direction 0 only)
 };
+
+// K/V heads per rank, and how many ranks share each K/V head.  With fewer K/V heads than
+// ranks (P a multiple of h_kv), each K/V head is replicated on P / h_kv consecutive ranks,
+// one head per rank: rank r's query heads are exactly the ones that use K/V head r / rep.
+inline int kv_heads_per_rank(int P, int h_kv) { return h_kv >= P ? h_kv / P : 1; }
+inline int kv_replication(int P, int h_kv) { return h_kv >= P ? 1 : P / h_kv; }
 
 // direction: 0 = seq -> head (all-to-all #1), 1 = head -> seq (all-to-all #2); 1 to 4 tensors.
 cudaError_t launch_permute(int direction, int P, int b, int s, int d, int elem_bytes, const PermuteTensor* tensors,
                            int ntensors, cudaStream_t stream);
+
+// The backward of the replicating exchange: gradients of K/V heads replicated on `rep` ranks.
+// src[r]: rank r's fp32 head-layout partial gradient [b][s][1][d] (from its own query heads);
+// dst[j]: bf16 seq layout [b][s/P][h_kv][d] = the sum over the rep replicas, rounded once.
+cudaError_t launch_kv_grad_sum(int P, int rep, int b, int s, int h_kv, int d, const void* const* src,
+                               void* const* dst, cudaStream_t stream);
 
 // ----------------------------------------------------------------- fp32 attention
 struct AttnPtrs {
@@ -73,6 +87,7 @@ struct BwdPtrs {
     void* dv[kMaxRanks];
     float* lse2[kMaxRanks];       // scratch [b][h_q/P][s_pad], s_pad = ceil(s/128)*128
     float* dsum[kMaxRanks];       // scratch, same shape
+    int kv_grad_f32;              // unfused only: dk/dv receive fp32 partial sums (replicated K/V heads)
 };
 cudaError_t launch_attention_bwd_tc(int P, int b, int s, int h_q, int h_kv, int d, int causal, int fused,
                                     const BwdPtrs& ptrs, cudaStream_t stream, int* unsupported);

@@ -12,6 +12,9 @@
 // forward exchanges one head group at a time.  The kernel streams those slabs with 16-byte (or narrower)
 // vector loads and stores: the contiguous side is fully coalesced, the strided side moves
 // whole runs (>= 128 bytes for every supported bf16/fp32 shape with d >= 64).
+#include <cstring>
+#include <cuda_bf16.h>
+
 #include "device_common.cuh"
 #include "internal.h"
 
@@ -28,6 +31,7 @@ struct PermuteJob {
     uint64_t rank_bytes;  // H*d*e: distance between consecutive ranks' head groups in a seq-layout row
     uint64_t head_off;    // hoff*d*e: first moved head inside a rank's group
     uint64_t row_pitch;   // h*d*e: seq-layout row pitch
+    uint32_t rep;         // ranks sharing one head group (replicated K/V heads), else 1
     uint32_t slab_vecs;   // S*run_bytes / VEC
     FastDiv run_vecs;     // run_bytes / VEC
 };
@@ -75,7 +79,8 @@ __global__ void __launch_bounds__(kThreads) permute_kernel(const __grid_constant
         const uint32_t bb = rest / P;
         const PermuteJob& J = p.job[t];
         const uint64_t off_contig = ((uint64_t)bb * p.s + (uint64_t)j * p.S) * J.run_bytes;
-        const uint64_t off_strided = (uint64_t)bb * p.S * J.row_pitch + (uint64_t)r * J.rank_bytes + J.head_off;
+        const uint64_t off_strided =
+            (uint64_t)bb * p.S * J.row_pitch + (uint64_t)(r / J.rep) * J.rank_bytes + J.head_off;
         const uint8_t* src = DIR == 0 ? J.src[j] + off_strided : J.src[r] + off_contig;
         uint8_t* dst = DIR == 0 ? J.dst[r] + off_contig : J.dst[j] + off_strided;
         const uint32_t n = J.slab_vecs;
@@ -128,6 +133,8 @@ cudaError_t launch_vec(int direction, const PermuteParams& prm, uint32_t max_sla
 cudaError_t launch_permute(int direction, int P, int b, int s, int d, int elem_bytes, const PermuteTensor* tensors,
                            int ntensors, cudaStream_t stream) {
     if (ntensors < 1 || ntensors > 4) return cudaErrorInvalidValue;
+    for (int t = 0; t < ntensors; ++t)  // replication only broadcasts (the reverse sums: launch_kv_grad_sum)
+        if (tensors[t].rep > 1 && (direction != 0 || tensors[t].h * tensors[t].rep != P)) return cudaErrorInvalidValue;
     if ((uint64_t)ntensors * P * P * b > 0xffffffffull) {  // one launch per tensor keeps the slab index in 32 bits
         for (int t = 0; t < ntensors; ++t) {
             const cudaError_t e = launch_permute(direction, P, b, s, d, elem_bytes, tensors + t, 1, stream);
@@ -143,11 +150,12 @@ cudaError_t launch_permute(int direction, int P, int b, int s, int d, int elem_b
     prm.s = (uint32_t)s;
     prm.units = (uint32_t)P * (uint32_t)P * (uint32_t)b;
     // widest vector that divides every run and offset (all pointers are 16-byte aligned by contract)
-    auto hsub = [&](int t) { return tensors[t].hsub > 0 ? tensors[t].hsub : tensors[t].h / P; };
+    auto per_rank = [&](int t) { return tensors[t].rep > 1 ? 1 : tensors[t].h / P; };  // heads of a rank's group
+    auto hsub = [&](int t) { return tensors[t].hsub > 0 ? tensors[t].hsub : per_rank(t); };
     int vec = 16;
     for (int t = 0; t < ntensors; ++t) {
         const uint64_t unit = (uint64_t)d * elem_bytes;
-        const uint64_t sizes[3] = {hsub(t) * unit, (uint64_t)(tensors[t].h / P) * unit, (uint64_t)tensors[t].hoff * unit};
+        const uint64_t sizes[3] = {hsub(t) * unit, (uint64_t)per_rank(t) * unit, (uint64_t)tensors[t].hoff * unit};
         for (uint64_t x : sizes)
             while (vec > 1 && x % vec) vec >>= 1;
     }
@@ -159,7 +167,8 @@ cudaError_t launch_permute(int direction, int P, int b, int s, int d, int elem_b
             J.dst[r] = static_cast<uint8_t*>(tensors[t].dst[r]);
         }
         J.run_bytes = (uint64_t)hsub(t) * d * elem_bytes;
-        J.rank_bytes = (uint64_t)(tensors[t].h / P) * d * elem_bytes;
+        J.rank_bytes = (uint64_t)per_rank(t) * d * elem_bytes;
+        J.rep = tensors[t].rep > 1 ? (uint32_t)tensors[t].rep : 1u;
         J.head_off = (uint64_t)tensors[t].hoff * d * elem_bytes;
         J.row_pitch = (uint64_t)tensors[t].h * d * elem_bytes;
         J.slab_vecs = (uint32_t)((uint64_t)prm.S * J.run_bytes / vec);
@@ -174,6 +183,82 @@ cudaError_t launch_permute(int direction, int P, int b, int s, int d, int elem_b
         case 2: return launch_vec<2>(direction, prm, max_slab, stream);
         default: return launch_vec<1>(direction, prm, max_slab, stream);
     }
+}
+
+namespace {
+
+struct KvGradSumParams {
+    const uint8_t* src[kMaxRanks];
+    uint8_t* dst[kMaxRanks];
+    uint64_t n_vec;  // P * b * (s/P) * h_kv * (d/8) output vectors of 8 bf16
+    uint32_t rep, b, s, S, hkv, dvec;
+};
+
+// One thread per 8 output elements: the rep replicas' fp32 partial gradients, summed.
+__global__ void __launch_bounds__(256) kv_grad_sum_kernel(const __grid_constant__ KvGradSumParams p) {
+    for (uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i < p.n_vec;
+         i += (uint64_t)gridDim.x * blockDim.x) {
+        uint64_t r = i;
+        const uint32_t v = (uint32_t)(r % p.dvec);
+        r /= p.dvec;
+        const uint32_t h = (uint32_t)(r % p.hkv);
+        r /= p.hkv;
+        const uint32_t t = (uint32_t)(r % p.S);
+        r /= p.S;
+        const uint32_t bb = (uint32_t)(r % p.b);
+        const uint32_t j = (uint32_t)(r / p.b);
+        // fp32 head layout of replica rank h*rep + k: [b][s][1][d]; token j*S + t
+        const uint64_t src_off = (((uint64_t)bb * p.s + (uint64_t)j * p.S + t) * p.dvec + v) * 32;
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        for (uint32_t k = 0; k < p.rep; ++k) {
+            const float4* x = reinterpret_cast<const float4*>(p.src[h * p.rep + k] + src_off);
+            const float4 a = __ldcs(x), c = __ldcs(x + 1);
+            acc[0] += a.x;
+            acc[1] += a.y;
+            acc[2] += a.z;
+            acc[3] += a.w;
+            acc[4] += c.x;
+            acc[5] += c.y;
+            acc[6] += c.z;
+            acc[7] += c.w;
+        }
+        uint4 out;
+        __nv_bfloat162* o2 = reinterpret_cast<__nv_bfloat162*>(&out);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o2[e] = __floats2bfloat162_rn(acc[2 * e], acc[2 * e + 1]);
+        // seq layout of rank j: [b][s/P][h_kv][d]
+        const uint64_t dst_off = ((((uint64_t)bb * p.S + t) * p.hkv + h) * p.dvec + v) * 16;
+        *reinterpret_cast<uint4*>(p.dst[j] + dst_off) = out;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_kv_grad_sum(int P, int rep, int b, int s, int h_kv, int d, const void* const* src,
+                               void* const* dst, cudaStream_t stream) {
+    if (rep < 1 || h_kv * rep != P || d % 8 || s % P) return cudaErrorInvalidValue;
+    KvGradSumParams prm;
+    memset(&prm, 0, sizeof(prm));
+    for (int r = 0; r < P; ++r) {
+        prm.src[r] = static_cast<const uint8_t*>(src[r]);
+        prm.dst[r] = static_cast<uint8_t*>(dst[r]);
+    }
+    prm.rep = (uint32_t)rep;
+    prm.b = (uint32_t)b;
+    prm.s = (uint32_t)s;
+    prm.S = (uint32_t)(s / P);
+    prm.hkv = (uint32_t)h_kv;
+    prm.dvec = (uint32_t)(d / 8);
+    prm.n_vec = (uint64_t)P * b * prm.S * h_kv * prm.dvec;
+    if (prm.n_vec == 0) return cudaSuccess;
+    int dev = 0, sms = 152;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    uint64_t blocks = (prm.n_vec + 255) / 256;
+    const uint64_t cap = (uint64_t)sms * 8;
+    if (blocks > cap) blocks = cap;
+    kv_grad_sum_kernel<<<(unsigned)blocks, 256, 0, stream>>>(prm);
+    return cudaGetLastError();
 }
 
 }  // namespace uly

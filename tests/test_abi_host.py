@@ -66,8 +66,10 @@ def test_attention_argument_errors(lib):
     f = lib.ulysses_local_attention
     q, k, v, o = _arr(A), _arr(B), _arr(C), _arr(D)
     assert f(1, 1, 64, 4, 3, 16, FP32, 0, q, k, v, o, None) == INVALID        # h_q % h_kv
-    assert f(2, 1, 64, 4, 1, 16, FP32, 0, _arr(A, A + 0x1000000), _arr(B, B + 0x1000000),
-             _arr(C, C + 0x1000000), _arr(D, D + 0x1000000), None) == INVALID  # h_kv % P
+    four = (_arr(A, A + 0x1000000, A + 0x2000000, A + 0x3000000), _arr(B, B + 0x1000000, B + 0x2000000, B + 0x3000000),
+            _arr(C, C + 0x1000000, C + 0x2000000, C + 0x3000000), _arr(D, D + 0x1000000, D + 0x2000000, D + 0x3000000))
+    # K/V heads and ranks must be multiples of one another (split or replicated): 6 and 4 are not
+    assert f(4, 1, 64, 12, 6, 16, FP32, 0, *four, None) == INVALID
     assert f(1, 1, 64, 4, 4, 96, BF16, 0, q, k, v, o, None) == UNSUPPORTED    # bf16 needs d in {64,128}
     assert f(1, 1, 64, 4, 4, 6, FP32, 0, q, k, v, o, None) == UNSUPPORTED     # fp32 needs d % 4 == 0
     assert f(1, 1, 64, 4, 4, 260, FP32, 0, q, k, v, o, None) == UNSUPPORTED   # fp32 needs d <= 256
@@ -102,3 +104,15 @@ def test_status_strings(lib):
     for code, name in enumerate(["ULY_OK", "ULY_ERR_INVALID_ARG", "ULY_ERR_UNSUPPORTED", "ULY_ERR_CUDA",
                                  "ULY_ERR_TIMEOUT"]):
         assert uly.ulysses_status_string(code) == name
+
+
+def test_replicated_kv_workspace(lib):
+    """Fewer K/V heads than ranks (h_kv | P): each rank holds one K/V head in head layout."""
+    ws = lib.ulysses_dist_attn_workspace_bytes
+    P, b, s, hq, d = 4, 1, 512, 8, 128
+    r = lambda x: (x + 255) // 256 * 256
+    qb, kb = r(b * s * (hq // P) * d * 2), r(b * s * 1 * d * 2)
+    for hkv in (1, 2):
+        assert ws(P, b, s, hq, hkv, d, BF16, 0) == P * (2 * qb + 2 * kb)
+        assert ws(P, b, s, hq, hkv, d, BF16, 1) == 0          # fused: no workspace
+    assert ws(P, b, s, 12, 6, d, BF16, 0) == 0               # 6 and 4: neither divides the other
