@@ -455,7 +455,8 @@ __global__ void __launch_bounds__(RowCfg<RW>::kThreads, 1) bwd_dkdv_kernel(const
                 for (int e = 0; e < 32; e += 2) {
                     float t0, t1;
                     fadd2(t0, t1, __uint_as_float(dv[e]), __uint_as_float(dv[e + 1]), -dl[e], -dl[e + 1]);
-                    pk[e >> 1] = pack_bf16x2(pf[c * 32 + e] * t0, pf[c * 32 + e + 1] * t1);
+                    fmul2(t0, t1, pf[c * 32 + e], pf[c * 32 + e + 1], t0, t1);
+                    pk[e >> 1] = pack_bf16x2(t0, t1);
                 }
                 tmem_st16(tdP + c * 16, pk);  // dS^T over dP^T columns this warp has already read
             }
@@ -634,15 +635,16 @@ __global__ void __launch_bounds__(RowCfg<RW>::kThreads, 1) bwd_dq_kernel(const _
             ok = wait_phase_warp(&bars[S_FULL + (n & 1)], (n >> 1) & 1, sh);
             if (!ok) break;
             tc_fence_after();
+            uint32_t sv[kChunks][32];  // every chunk's load in flight before one wait
+#pragma unroll
+            for (int c = 0; c < kChunks; ++c) tmem_ld32(tS + c * 32, sv[c]);
+            tmem_wait_ld();
 #pragma unroll
             for (int c = 0; c < kChunks; ++c) {
-                uint32_t sv[32];
-                tmem_ld32(tS + c * 32, sv);
-                tmem_wait_ld();
 #pragma unroll
                 for (int e = 0; e < 32; e += 2) {
                     float a0, a1;
-                    ffma2(a0, a1, __uint_as_float(sv[e]), __uint_as_float(sv[e + 1]), sc, sc, neg_l, neg_l);
+                    ffma2(a0, a1, __uint_as_float(sv[c][e]), __uint_as_float(sv[c][e + 1]), sc, sc, neg_l, neg_l);
                     float p0 = ex2_approx(a0), p1 = ex2_approx(a1);
                     if (mask) {
                         const int key = kb + c * 32 + e;
@@ -656,17 +658,19 @@ __global__ void __launch_bounds__(RowCfg<RW>::kThreads, 1) bwd_dq_kernel(const _
             ok = wait_phase_warp(&bars[DP_FULL], n & 1, sh);
             if (!ok) break;
             tc_fence_after();
+            uint32_t dv[kChunks][32];
+#pragma unroll
+            for (int c = 0; c < kChunks; ++c) tmem_ld32(tdP + c * 32, dv[c]);
+            tmem_wait_ld();
 #pragma unroll
             for (int c = 0; c < kChunks; ++c) {
-                uint32_t dv[32];
-                tmem_ld32(tdP + c * 32, dv);
-                tmem_wait_ld();
                 uint32_t pk[16];
 #pragma unroll
                 for (int e = 0; e < 32; e += 2) {
                     float t0, t1;
-                    fadd2(t0, t1, __uint_as_float(dv[e]), __uint_as_float(dv[e + 1]), neg_d, neg_d);
-                    pk[e >> 1] = pack_bf16x2(pf[c * 32 + e] * t0, pf[c * 32 + e + 1] * t1);
+                    fadd2(t0, t1, __uint_as_float(dv[c][e]), __uint_as_float(dv[c][e + 1]), neg_d, neg_d);
+                    fmul2(t0, t1, pf[c * 32 + e], pf[c * 32 + e + 1], t0, t1);
+                    pk[e >> 1] = pack_bf16x2(t0, t1);
                 }
                 tmem_st16(tS + c * 16, pk);  // dS over S columns this warp has already read
             }
