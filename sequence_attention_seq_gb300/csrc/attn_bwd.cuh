@@ -74,6 +74,9 @@ struct BwdParams {
     float scale_log2;             // log2(e)/sqrt(d)
     float scale;                  // 1/sqrt(d)
     int kv_grad_f32;              // host: launch the dK/dV kernel that stores fp32 partial sums
+    int n_units;                  // dK/dV work: (rank, batch, K/V head) units of the launch
+    int kv_items;                 // n_units * n_tiles
+    int band_units;               // causal: units per band (see kv_item)
 };
 
 struct BwdTok {
@@ -251,7 +254,53 @@ __device__ __forceinline__ void mma_acc_tmemA(uint32_t acc, uint32_t a_tmem, uin
 }
 
 // ------------------------------------------------------------------ dK / dV
-// Block -> (rank, batch, K/V head, key tile), key tile fastest and ascending.
+// Work item = (rank, batch, K/V head, 128-key tile); a unit = (rank, batch, K/V head).
+// Non-causal (all items equal): the key tiles of a unit are adjacent, so the CTAs working
+// at the same time stream the same Q/dO tiles and L2 serves the re-reads.  Causal (key tile
+// kt has g*(n_tiles-kt) steps): the units form bands of band_units units, and inside a band
+// the key tile is slowest and ascending, so the items run heaviest first.  band_units = 1
+// gives the unit-major order, key tile ascending.
+struct KvItem {
+    int rank, bb, kvh, kt;
+};
+
+__device__ __forceinline__ KvItem kv_item(const BwdParams& p, int w) {
+    int u, kt;
+    if (p.causal) {
+        const int per_band = p.band_units * p.n_tiles;
+        const int band = w / per_band, base = band * p.band_units;
+        const int in_band = p.n_units - base < p.band_units ? p.n_units - base : p.band_units;
+        const int r = w - band * per_band;
+        u = base + r % in_band;
+        kt = r / in_band;
+    } else {
+        u = w / p.n_tiles;
+        kt = w % p.n_tiles;
+    }
+    KvItem it;
+    it.kvh = u % p.hkv;
+    u /= p.hkv;
+    it.bb = u % p.b;
+    it.rank = u / p.b;
+    it.kt = kt;
+    return it;
+}
+
+// The k-th item of this CTA: rounds of gridDim.x items, alternating direction (snake), so a
+// heaviest-first order spreads evenly over the CTAs; -1 when the CTA has no k-th item.
+__device__ __forceinline__ int bwd_item_index(int n_items, int k) {
+    const int G = gridDim.x, c = blockIdx.x;
+    const int w = k * G + ((k & 1) ? G - 1 - c : c);
+    return w < n_items ? w : -1;
+}
+
+// Persistent (grid below the item count): each CTA walks its items; every role walks the
+// same sequence, and the barrier phases run on across items.  With one CTA per item the
+// loop runs once.  At an item boundary the producer loads the next K/V
+// as soon as the last S^T and dP^T products have read the current ones, and the MMA warp
+// issues the next item's first S^T and dP^T right after the last dK product, so both run
+// while the row warps store dK and dV.  The next item's first dV product (which overwrites
+// the accumulator) waits for P-ready, which every row warp signals only after its epilogue.
 // Tensor memory: S^T (then P^T) 0..127 | dP^T (then dS^T) 128..255 | dK 256.. | dV 384..
 // F32: dk/dv receive fp32 partial sums (a replicated K/V head's share from this rank).
 template <int D, int RW, bool F32>
@@ -262,8 +311,8 @@ __global__ void __launch_bounds__(RowCfg<RW>::kThreads, 1) bwd_dkdv_kernel(const
     using L = BwdSmem<D, kRingKV>;
     constexpr uint32_t kSlab = 128 * 128;
     enum {
-        FIX = 0, FULL = 1, EMPTY = FULL + kRingKV, S_FULL = EMPTY + kRingKV, DP_FULL, P_READY, DS_READY, FINAL,
-        NBARS
+        FIX = 0, FIX_EMPTY, FULL, EMPTY = FULL + kRingKV, S_FULL = EMPTY + kRingKV, DP_FULL, P_READY, DS_READY, FINAL,
+        MMA_DONE, NBARS
     };
     static_assert(NBARS <= (int)L::kBarSlots, "barrier slots");
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -273,214 +322,253 @@ __global__ void __launch_bounds__(RowCfg<RW>::kThreads, 1) bwd_dkdv_kernel(const
     const uint32_t sbase = smem_addr(smem);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    int bid = blockIdx.x;
-    const int kt = bid % p.n_tiles;
-    bid /= p.n_tiles;
-    const int kvh = bid % p.hkv;
-    bid /= p.hkv;
-    const int bb = bid % p.b;
-    const int rank = bid / p.b;
-    const int k0 = kt * 128;
-    const int n_steps = p.g * (p.n_tiles - (p.causal ? kt : 0));  // (query tile, head) pairs
-    // step n: query tile n_tiles-1 - n/g of query head kvh*g + n%g
+    // step n of an item: query tile n_tiles-1 - n/g of query head kvh*g + n%g
     const int g = p.g, n_tiles = p.n_tiles;
-    auto step_head = [kvh, g](int n) { return kvh * g + n % g; };
+    auto item_steps = [&p, g, n_tiles](const KvItem& it) { return g * (n_tiles - (p.causal ? it.kt : 0)); };
     auto step_qt = [n_tiles, g](int n) { return n_tiles - 1 - n / g; };
 
     if (!bwd_setup(bars, NBARS, P_READY, DS_READY + 1, kBwdRowWarps, kBwdMma, sh)) return;
     const uint32_t tmem = sh->tmem_base;
 
     if (warp == kBwdProducer) {
-        // the fixed tiles: K (A) and V (B) of this key tile; then Q and dO per step
-        const BwdTok kp = bwd_tok(p, rank, k0);
-        mbar_arrive_expect_tx_warp(&bars[FIX], 2 * L::kTile);
-#pragma unroll
-        for (int c = 0; c < D / 64; ++c) {
-            tma_load_4d_warp(sbase + L::offFixA + c * kSlab, &p.mk[kp.map], &bars[FIX], c * 64, kvh, kp.row, bb);
-            tma_load_4d_warp(sbase + L::offFixB + c * kSlab, &p.mv[kp.map], &bars[FIX], c * 64, kvh, kp.row, bb);
-        }
-        int issued = 0;
+        // per item: the fixed tiles K (A) and V (B) of its key tile, then Q and dO per step
+        int issued = 0, fix_loads = 0;  // ring loads and fixed-tile loads issued so far
         bool ok = true;
-        for (int m = 0; m < 2 * n_steps; ++m) {
-            const int slot = m % kRingKV;
-            ok = wait_phase_warp(&bars[EMPTY + slot], ((m / kRingKV) & 1) ^ 1, sh);
-            if (!ok) break;
-            const int n = m >> 1;
-            const BwdTok qp = bwd_tok(p, rank, step_qt(n) * 128);
-            mbar_arrive_expect_tx_warp(&bars[FULL + slot], L::kTile);
+        for (int k = 0; ok; ++k) {
+            const int w = bwd_item_index(p.kv_items, k);
+            if (w < 0) break;
+            const KvItem it = kv_item(p, w);
+            const int n_steps = item_steps(it);
+            if (k > 0) {  // the previous item's last S^T and dP^T have read K and V
+                ok = wait_phase_warp(&bars[FIX_EMPTY], (k - 1) & 1, sh);
+                if (!ok) break;
+            }
+            const BwdTok kp = bwd_tok(p, it.rank, it.kt * 128);
+            mbar_arrive_expect_tx_warp(&bars[FIX], 2 * L::kTile);
 #pragma unroll
-            for (int c = 0; c < D / 64; ++c)
-                tma_load_4d_warp(sbase + L::offRing + slot * L::kTile + c * kSlab, (m & 1) ? &p.mdo[qp.map] : &p.mq[qp.map],
-                                 &bars[FULL + slot], c * 64, step_head(n), qp.row, bb);
-            ++issued;
+            for (int c = 0; c < D / 64; ++c) {
+                tma_load_4d_warp(sbase + L::offFixA + c * kSlab, &p.mk[kp.map], &bars[FIX], c * 64, it.kvh, kp.row,
+                                 it.bb);
+                tma_load_4d_warp(sbase + L::offFixB + c * kSlab, &p.mv[kp.map], &bars[FIX], c * 64, it.kvh, kp.row,
+                                 it.bb);
+            }
+            ++fix_loads;
+            for (int m = 0; m < 2 * n_steps; ++m) {
+                const int slot = issued % kRingKV;
+                ok = wait_phase_warp(&bars[EMPTY + slot], ((issued / kRingKV) & 1) ^ 1, sh);
+                if (!ok) break;
+                const int n = m >> 1;
+                const BwdTok qp = bwd_tok(p, it.rank, step_qt(n) * 128);
+                mbar_arrive_expect_tx_warp(&bars[FULL + slot], L::kTile);
+#pragma unroll
+                for (int c = 0; c < D / 64; ++c)
+                    tma_load_4d_warp(sbase + L::offRing + slot * L::kTile + c * kSlab,
+                                     (m & 1) ? &p.mdo[qp.map] : &p.mq[qp.map], &bars[FULL + slot], c * 64,
+                                     it.kvh * g + n % g, qp.row, it.bb);
+                ++issued;
+            }
         }
-        if (!ok) {
+        if (!ok) {  // let the copies in flight land before the CTA leaves
             for (int slot = 0; slot < kRingKV; ++slot) {
                 const int cnt = (issued - slot + kRingKV - 1) / kRingKV;
                 if (cnt > 0) drain_phase(&bars[FULL + slot], (cnt - 1) & 1);
             }
-            drain_phase(&bars[FIX], 0);
+            if (fix_loads > 0) drain_phase(&bars[FIX], (fix_loads - 1) & 1);
         }
     } else if (warp == kBwdMma) {
         const uint64_t dk_a = smem_desc_sw128(sbase + L::offFixA, 16, 1024);        // K
         const uint64_t dv_a = smem_desc_sw128(sbase + L::offFixB, 16, 1024);        // V
         const uint64_t ring_k = smem_desc_sw128(sbase + L::offRing, 16, 1024);      // Q / dO, K-major
         const uint64_t ring_mn = smem_desc_sw128(sbase + L::offRing, kSlab, 1024);  // Q / dO, MN-major
-        auto so = [](int m) { return (uint64_t)(((m % kRingKV) * L::kTile) >> 4); };
-        auto full = [&](int m) { return wait_phase_warp(&bars[FULL + m % kRingKV], (m / kRingKV) & 1, sh); };
-        bool ok = wait_phase_warp(&bars[FIX], 0, sh) && full(0);
-        if (ok) {
-            tc_fence_after();
-            mma_kmajor<D>(tmem, dk_a, ring_k + so(0));  // S^T(0)
-            mma_commit_warp(&bars[S_FULL]);
-            ok = full(1);
-        }
-        if (ok) {
-            tc_fence_after();
-            mma_kmajor<D>(tmem + 128u, dv_a, ring_k + so(1));  // dP^T(0)
-            mma_commit_warp(&bars[DP_FULL]);
-        }
-        for (int n = 0; n < n_steps && ok; ++n) {
-            const int mq = 2 * n, mo = 2 * n + 1;
-            ok = wait_phase_warp(&bars[P_READY], n & 1, sh);
-            if (!ok) break;
-            tc_fence_after();
-            mma_acc_tmemA<D, kColW>(tmem + 384u, tmem, ring_mn + so(mo), n > 0);  // dV += P^T dO
-            mma_commit_warp(&bars[EMPTY + mo % kRingKV]);
-            if (n + 1 < n_steps) {  // S^T(n+1) over P^T(n): issued after the product that reads it
-                ok = full(mq + 2);
-                if (!ok) break;
+        int m0 = 0;  // ring position of the current item's first Q tile
+        int gs = 0;  // steps of the earlier items (the per-step barriers' phases run on)
+        bool ok = true;
+        for (int k = 0; ok; ++k) {
+            const int w = bwd_item_index(p.kv_items, k);
+            if (w < 0) break;
+            const int n_steps = item_steps(kv_item(p, w));
+            auto so = [m0](int m) { return (uint64_t)((((m0 + m) % kRingKV) * L::kTile) >> 4); };
+            auto full = [&](int m) {
+                return wait_phase_warp(&bars[FULL + (m0 + m) % kRingKV], ((m0 + m) / kRingKV) & 1, sh);
+            };
+            auto release = [&](int m) { mma_commit_warp(&bars[EMPTY + (m0 + m) % kRingKV]); };
+            ok = wait_phase_warp(&bars[FIX], k & 1, sh) && full(0);
+            if (ok) {
                 tc_fence_after();
-                mma_kmajor<D>(tmem, dk_a, ring_k + so(mq + 2));
+                mma_kmajor<D>(tmem, dk_a, ring_k + so(0));  // S^T(0)
                 mma_commit_warp(&bars[S_FULL]);
+                ok = full(1);
             }
-            ok = wait_phase_warp(&bars[DS_READY], n & 1, sh);
-            if (!ok) break;
-            tc_fence_after();
-            mma_acc_tmemA<D, kColW>(tmem + 256u, tmem + 128u, ring_mn + so(mq), n > 0);  // dK += dS^T Q
-            mma_commit_warp(&bars[EMPTY + mq % kRingKV]);
-            if (n + 1 < n_steps) {  // dP^T(n+1) over dS^T(n): issued after the product that reads it
-                ok = full(mo + 2);
+            if (ok) {
+                tc_fence_after();
+                mma_kmajor<D>(tmem + 128u, dv_a, ring_k + so(1));  // dP^T(0)
+                mma_commit_warp(&bars[DP_FULL]);
+                if (n_steps == 1) mma_commit_warp(&bars[FIX_EMPTY]);  // K and V read for the last time
+            }
+            for (int n = 0; n < n_steps && ok; ++n) {
+                const int mq = 2 * n, mo = 2 * n + 1;
+                ok = wait_phase_warp(&bars[P_READY], (gs + n) & 1, sh);
                 if (!ok) break;
                 tc_fence_after();
-                mma_kmajor<D>(tmem + 128u, dv_a, ring_k + so(mo + 2));
-                mma_commit_warp(&bars[DP_FULL]);
+                mma_acc_tmemA<D, kColW>(tmem + 384u, tmem, ring_mn + so(mo), n > 0);  // dV += P^T dO
+                release(mo);
+                if (n + 1 < n_steps) {  // S^T(n+1) over P^T(n): issued after the product that reads it
+                    ok = full(mq + 2);
+                    if (!ok) break;
+                    tc_fence_after();
+                    mma_kmajor<D>(tmem, dk_a, ring_k + so(mq + 2));
+                    mma_commit_warp(&bars[S_FULL]);
+                }
+                ok = wait_phase_warp(&bars[DS_READY], (gs + n) & 1, sh);
+                if (!ok) break;
+                tc_fence_after();
+                mma_acc_tmemA<D, kColW>(tmem + 256u, tmem + 128u, ring_mn + so(mq), n > 0);  // dK += dS^T Q
+                release(mq);
+                if (n + 1 < n_steps) {  // dP^T(n+1) over dS^T(n): issued after the product that reads it
+                    ok = full(mo + 2);
+                    if (!ok) break;
+                    tc_fence_after();
+                    mma_kmajor<D>(tmem + 128u, dv_a, ring_k + so(mo + 2));
+                    mma_commit_warp(&bars[DP_FULL]);
+                    if (n + 2 == n_steps) mma_commit_warp(&bars[FIX_EMPTY]);
+                }
             }
+            if (!ok) break;
+            mma_commit_warp(&bars[FINAL]);  // dK and dV of this item are complete
+            gs += n_steps;
+            m0 += 2 * n_steps;
         }
-        mma_commit_warp(&bars[FINAL]);
-        drain_phase(&bars[FINAL], 0);
+        // every MMA issued above completes before tensor memory is released
+        mma_commit_warp(&bars[MMA_DONE]);
+        drain_phase(&bars[MMA_DONE], 0);
     } else {
         // row warps: thread = key row; warp group cg owns query columns [cg*kColW, +kColW)
         const int sub = warp & 3, cg = warp >> 2;
-        const int row = sub * 32 + lane, key = k0 + row;
+        const int row = sub * 32 + lane;
         const uint32_t lane_off = (uint32_t)(sub * 32) << 16;
         const uint32_t tS = tmem + lane_off + cg * kColW, tdP = tmem + 128u + lane_off + cg * kColW;
         const float sc = p.scale_log2;
-        auto stat_off = [&](int n) {  // offset of step n's first row statistic of this warp
-            return bwd_stat_off(p, bb, step_head(n), step_qt(n) * 128 + cg * kColW);
-        };
+        int gs = 0;
         bool ok = true;
-        for (int n = 0; n < n_steps; ++n) {
-            const int qt = step_qt(n);
-            const int qb = qt * 128 + cg * kColW;  // first query column of this warp
-            const size_t vbase = stat_off(n);
-            const int sr = bwd_stat_rank(p, rank, step_head(n));
-            const float4* l4 = reinterpret_cast<const float4*>(p.lse2[sr] + vbase);
-            const float4* d4 = reinterpret_cast<const float4*>(p.dsum[sr] + vbase);
-            if (n + 1 < n_steps && lane < 2 * kChunks) {  // next step's statistics: one 128-byte line per lane
-                const size_t nb = stat_off(n + 1) + (lane % kChunks) * 32;
-                const int nr = bwd_stat_rank(p, rank, step_head(n + 1));
-                prefetch_l1(lane < kChunks ? p.lse2[nr] + nb : p.dsum[nr] + nb);
-            }
-            const bool diag = p.causal && qt == kt;
-            float pf[kColW];
-            ok = wait_phase_warp(&bars[S_FULL], n & 1, sh);
-            if (!ok) break;
-            tc_fence_after();
-#pragma unroll
-            for (int c = 0; c < kChunks; ++c) {
-                uint32_t sv[32];
-                float lv[32];
-                tmem_ld32(tS + c * 32, sv);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const float4 x = __ldg(l4 + c * 8 + i);
-                    lv[4 * i] = x.x;
-                    lv[4 * i + 1] = x.y;
-                    lv[4 * i + 2] = x.z;
-                    lv[4 * i + 3] = x.w;
+        for (int k = 0; ok; ++k) {
+            const int w = bwd_item_index(p.kv_items, k);
+            if (w < 0) break;
+            const KvItem it = kv_item(p, w);
+            const int n_steps = item_steps(it);
+            const int kt = it.kt;
+            const int k0 = kt * 128, key = k0 + row;
+            const int head0 = it.kvh * g;                  // first query head of the step sequence
+            const int bh0 = it.bb * p.hq_rank;             // batch offset of the statistic rows
+            auto step_head = [head0, g](int n) { return head0 + n % g; };
+            auto stat_off = [&](int n) {  // offset of step n's first row statistic of this warp
+                return ((size_t)bh0 + step_head(n) % p.hq_rank) * p.s_pad + step_qt(n) * 128 + cg * kColW;
+            };
+            const int rank = it.rank;
+            for (int n = 0; n < n_steps; ++n) {
+                const int qt = step_qt(n);
+                const int qb = qt * 128 + cg * kColW;  // first query column of this warp
+                const size_t vbase = stat_off(n);
+                const int sr = bwd_stat_rank(p, rank, step_head(n));
+                const float4* l4 = reinterpret_cast<const float4*>(p.lse2[sr] + vbase);
+                const float4* d4 = reinterpret_cast<const float4*>(p.dsum[sr] + vbase);
+                if (n + 1 < n_steps && lane < 2 * kChunks) {  // next step's statistics: one 128-byte line per lane
+                    const size_t nb = stat_off(n + 1) + (lane % kChunks) * 32;
+                    const int nr = bwd_stat_rank(p, rank, step_head(n + 1));
+                    prefetch_l1(lane < kChunks ? p.lse2[nr] + nb : p.dsum[nr] + nb);
                 }
-                tmem_wait_ld();
-                uint32_t pk[16];
+                const bool diag = p.causal && qt == kt;
+                float pf[kColW];
+                ok = wait_phase_warp(&bars[S_FULL], (gs + n) & 1, sh);
+                if (!ok) break;
+                tc_fence_after();
 #pragma unroll
-                for (int e = 0; e < 32; e += 2) {
-                    float a0, a1;
-                    ffma2(a0, a1, __uint_as_float(sv[e]), __uint_as_float(sv[e + 1]), sc, sc, -lv[e], -lv[e + 1]);
-                    float p0 = ex2_approx(a0), p1 = ex2_approx(a1);
-                    if (diag) {
-                        const int q = qb + c * 32 + e;
-                        p0 = key <= q ? p0 : 0.f;
-                        p1 = key <= q + 1 ? p1 : 0.f;
+                for (int c = 0; c < kChunks; ++c) {
+                    uint32_t sv[32];
+                    float lv[32];
+                    tmem_ld32(tS + c * 32, sv);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const float4 x = __ldg(l4 + c * 8 + i);
+                        lv[4 * i] = x.x;
+                        lv[4 * i + 1] = x.y;
+                        lv[4 * i + 2] = x.z;
+                        lv[4 * i + 3] = x.w;
                     }
-                    pf[c * 32 + e] = p0;
-                    pf[c * 32 + e + 1] = p1;
-                    pk[e >> 1] = pack_bf16x2(p0, p1);
+                    tmem_wait_ld();
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int e = 0; e < 32; e += 2) {
+                        float a0, a1;
+                        ffma2(a0, a1, __uint_as_float(sv[e]), __uint_as_float(sv[e + 1]), sc, sc, -lv[e], -lv[e + 1]);
+                        float p0 = ex2_approx(a0), p1 = ex2_approx(a1);
+                        if (diag) {
+                            const int q = qb + c * 32 + e;
+                            p0 = key <= q ? p0 : 0.f;
+                            p1 = key <= q + 1 ? p1 : 0.f;
+                        }
+                        pf[c * 32 + e] = p0;
+                        pf[c * 32 + e + 1] = p1;
+                        pk[e >> 1] = pack_bf16x2(p0, p1);
+                    }
+                    tmem_st16(tS + c * 16, pk);  // P^T over S^T columns this warp has already read
                 }
-                tmem_st16(tS + c * 16, pk);  // P^T over S^T columns this warp has already read
-            }
-            tmem_wait_st();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars[P_READY]);
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars[P_READY]);
 
-            ok = wait_phase_warp(&bars[DP_FULL], n & 1, sh);
+                ok = wait_phase_warp(&bars[DP_FULL], (gs + n) & 1, sh);
+                if (!ok) break;
+                tc_fence_after();
+#pragma unroll
+                for (int c = 0; c < kChunks; ++c) {
+                    uint32_t dv[32];
+                    float dl[32];
+                    tmem_ld32(tdP + c * 32, dv);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const float4 x = __ldg(d4 + c * 8 + i);
+                        dl[4 * i] = x.x;
+                        dl[4 * i + 1] = x.y;
+                        dl[4 * i + 2] = x.z;
+                        dl[4 * i + 3] = x.w;
+                    }
+                    tmem_wait_ld();
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int e = 0; e < 32; e += 2) {
+                        float t0, t1;
+                        fadd2(t0, t1, __uint_as_float(dv[e]), __uint_as_float(dv[e + 1]), -dl[e], -dl[e + 1]);
+                        fmul2(t0, t1, pf[c * 32 + e], pf[c * 32 + e + 1], t0, t1);
+                        pk[e >> 1] = pack_bf16x2(t0, t1);
+                    }
+                    tmem_st16(tdP + c * 16, pk);  // dS^T over dP^T columns this warp has already read
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars[DS_READY]);
+            }
+            if (ok) ok = wait_phase_warp(&bars[FINAL], k & 1, sh);
             if (!ok) break;
-            tc_fence_after();
-#pragma unroll
-            for (int c = 0; c < kChunks; ++c) {
-                uint32_t dv[32];
-                float dl[32];
-                tmem_ld32(tdP + c * 32, dv);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const float4 x = __ldg(d4 + c * 8 + i);
-                    dl[4 * i] = x.x;
-                    dl[4 * i + 1] = x.y;
-                    dl[4 * i + 2] = x.z;
-                    dl[4 * i + 3] = x.w;
+            constexpr int kEpi = D / kColGroups >= 32 ? D / kColGroups : 32;  // accumulator columns per warp
+            if (cg * kEpi < D) {
+                tc_fence_after();
+                const bool kok = key < p.s;
+                const BwdTok kt_ = bwd_tok(p, rank, kok ? key : k0);
+                constexpr size_t kEl = F32 ? 4 : 2;  // bytes per stored element
+                const KvItem e_it = kv_item(p, w);
+                const size_t off = (((size_t)e_it.bb * p.rows_per_map + kt_.row) * p.hkv + e_it.kvh) * (size_t)D * kEl +
+                                   cg * kEpi * kEl;
+                if constexpr (F32) {
+                    store_row_f32<kEpi>(tmem + 256u + lane_off + cg * kEpi, p.dk[kt_.map] + off, p.scale, kok);
+                    store_row_f32<kEpi>(tmem + 384u + lane_off + cg * kEpi, p.dv[kt_.map] + off, 1.0f, kok);
+                } else {
+                    store_row_bf16<kEpi>(tmem + 256u + lane_off + cg * kEpi, p.dk[kt_.map] + off, p.scale, kok);
+                    store_row_bf16<kEpi>(tmem + 384u + lane_off + cg * kEpi, p.dv[kt_.map] + off, 1.0f, kok);
                 }
-                tmem_wait_ld();
-                uint32_t pk[16];
-#pragma unroll
-                for (int e = 0; e < 32; e += 2) {
-                    float t0, t1;
-                    fadd2(t0, t1, __uint_as_float(dv[e]), __uint_as_float(dv[e + 1]), -dl[e], -dl[e + 1]);
-                    fmul2(t0, t1, pf[c * 32 + e], pf[c * 32 + e + 1], t0, t1);
-                    pk[e >> 1] = pack_bf16x2(t0, t1);
-                }
-                tmem_st16(tdP + c * 16, pk);  // dS^T over dP^T columns this warp has already read
             }
-            tmem_wait_st();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars[DS_READY]);
-        }
-        if (ok) ok = wait_phase_warp(&bars[FINAL], 0, sh);
-        constexpr int kEpi = D / kColGroups >= 32 ? D / kColGroups : 32;  // accumulator columns per warp
-        if (ok && cg * kEpi < D) {
-            tc_fence_after();
-            const bool kok = key < p.s;
-            const BwdTok kt_ = bwd_tok(p, rank, kok ? key : k0);
-            constexpr size_t kEl = F32 ? 4 : 2;  // bytes per stored element
-            const size_t off =
-                (((size_t)bb * p.rows_per_map + kt_.row) * p.hkv + kvh) * (size_t)D * kEl + cg * kEpi * kEl;
-            if constexpr (F32) {
-                store_row_f32<kEpi>(tmem + 256u + lane_off + cg * kEpi, p.dk[kt_.map] + off, p.scale, kok);
-                store_row_f32<kEpi>(tmem + 384u + lane_off + cg * kEpi, p.dv[kt_.map] + off, 1.0f, kok);
-            } else {
-                store_row_bf16<kEpi>(tmem + 256u + lane_off + cg * kEpi, p.dk[kt_.map] + off, p.scale, kok);
-                store_row_bf16<kEpi>(tmem + 384u + lane_off + cg * kEpi, p.dv[kt_.map] + off, 1.0f, kok);
-            }
+            gs += n_steps;
         }
     }
     tc_fence_before();
@@ -699,17 +787,43 @@ __global__ void __launch_bounds__(RowCfg<RW>::kThreads, 1) bwd_dq_kernel(const _
 }
 
 // ------------------------------------------------------------------ host side
+// Causal band of the dK/dV items: all units when their Q and dO fit in L2 together, else as
+// many as keep them within the band budget (at least one).
+inline int bwd_band_units(int s_pad, int d, int g, int units) {
+    const double qdo_bytes = 2.0 * g * s_pad * d * 2;  // Q and dO of one unit's query heads, bf16
+    if (qdo_bytes * units <= kL2Bytes) return units;
+    int bu = (int)(kBandBytes / qdo_bytes);
+    if (bu < 1) bu = 1;
+    if (bu > units) bu = units;
+    return bu;
+}
+
 template <int D>
-cudaError_t launch_bwd_d(const BwdParams& prm, int nranks, cudaStream_t stream) {
+cudaError_t launch_bwd_d(const BwdParams& prm_in, int nranks, cudaStream_t stream) {
     using LK = BwdSmem<D, kRingKV>;
     using LQ = BwdSmem<D, kRingQ>;
+    BwdParams prm = prm_in;
+    prm.n_units = nranks * prm.b * prm.hkv;
+    prm.kv_items = prm.n_units * prm.n_tiles;
+    prm.band_units = bwd_band_units(prm.s_pad, D, prm.g, prm.n_units);
+    // Persistent when every CTA's share is balanced by the static order: items all equal
+    // (non-causal), or one band heaviest first.  Causal work in several bands runs one item
+    // per CTA in unit-major order instead (band_units = 1), so the hardware's block scheduler
+    // balances the unequal items as they finish.
+    const bool persistent = !prm.causal || prm.band_units == prm.n_units;
+    if (!persistent) prm.band_units = 1;
     auto* dkdv = prm.kv_grad_f32 ? bwd_dkdv_kernel<D, kRowsKV, true> : bwd_dkdv_kernel<D, kRowsKV, false>;
     cudaError_t e = cudaFuncSetAttribute(dkdv, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)LK::kAlloc);
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(bwd_dq_kernel<D, kRowsQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)LQ::kAlloc);
     if (e != cudaSuccess) return e;
-    const long long gk = (long long)nranks * prm.b * prm.hkv * prm.n_tiles;
+    int dev = 0, sms = 0;
+    e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    // dK/dV: one CTA per SM when persistent (each CTA fills an SM: shared memory and all TMEM)
+    const long long gk = persistent && prm.kv_items > sms ? sms : prm.kv_items;
     const long long gq = (long long)nranks * prm.b * prm.hq * prm.n_tiles;
     dkdv<<<(unsigned)gk, RowCfg<kRowsKV>::kThreads, LK::kAlloc, stream>>>(prm);
     e = cudaGetLastError();
