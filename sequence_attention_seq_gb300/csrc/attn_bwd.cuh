@@ -77,6 +77,9 @@ struct BwdParams {
     int n_units;                  // dK/dV work: (rank, batch, K/V head) units of the launch
     int kv_items;                 // n_units * n_tiles
     int band_units;               // causal: units per band (see kv_item)
+    int n_units_q;                // dQ work: (rank, batch, query head) units of the launch
+    int q_items;                  // n_units_q * n_tiles
+    int band_units_q;             // causal: units per band (see q_item)
 };
 
 struct BwdTok {
@@ -286,11 +289,14 @@ __device__ __forceinline__ KvItem kv_item(const BwdParams& p, int w) {
     return it;
 }
 
-// The k-th item of this CTA: rounds of gridDim.x items, alternating direction (snake), so a
-// heaviest-first order spreads evenly over the CTAs; -1 when the CTA has no k-th item.
+// The k-th item of this CTA.  PERSIST: rounds of gridDim.x items, alternating direction
+// (snake), so a heaviest-first order spreads evenly over the CTAs.  Else one item per CTA
+// (the loops that call this run once, and their running counters fold to constants).
+// -1 when the CTA has no k-th item.
+template <bool PERSIST>
 __device__ __forceinline__ int bwd_item_index(int n_items, int k) {
     const int G = gridDim.x, c = blockIdx.x;
-    const int w = k * G + ((k & 1) ? G - 1 - c : c);
+    const int w = PERSIST ? k * G + ((k & 1) ? G - 1 - c : c) : (k == 0 ? c : n_items);
     return w < n_items ? w : -1;
 }
 
@@ -303,7 +309,7 @@ __device__ __forceinline__ int bwd_item_index(int n_items, int k) {
 // the accumulator) waits for P-ready, which every row warp signals only after its epilogue.
 // Tensor memory: S^T (then P^T) 0..127 | dP^T (then dS^T) 128..255 | dK 256.. | dV 384..
 // F32: dk/dv receive fp32 partial sums (a replicated K/V head's share from this rank).
-template <int D, int RW, bool F32>
+template <int D, int RW, bool F32, bool PERSIST>
 __global__ void __launch_bounds__(RowCfg<RW>::kThreads, 1) bwd_dkdv_kernel(const __grid_constant__ BwdParams p) {
     using C = RowCfg<RW>;
     constexpr int kBwdRowWarps = C::kRows, kBwdProducer = C::kProducer, kBwdMma = C::kMma;
@@ -334,8 +340,8 @@ __global__ void __launch_bounds__(RowCfg<RW>::kThreads, 1) bwd_dkdv_kernel(const
         // per item: the fixed tiles K (A) and V (B) of its key tile, then Q and dO per step
         int issued = 0, fix_loads = 0;  // ring loads and fixed-tile loads issued so far
         bool ok = true;
-        for (int k = 0; ok; ++k) {
-            const int w = bwd_item_index(p.kv_items, k);
+        for (int k = 0; ok && (PERSIST || k == 0); ++k) {
+            const int w = bwd_item_index<PERSIST>(p.kv_items, k);
             if (w < 0) break;
             const KvItem it = kv_item(p, w);
             const int n_steps = item_steps(it);
@@ -383,8 +389,8 @@ __global__ void __launch_bounds__(RowCfg<RW>::kThreads, 1) bwd_dkdv_kernel(const
         int m0 = 0;  // ring position of the current item's first Q tile
         int gs = 0;  // steps of the earlier items (the per-step barriers' phases run on)
         bool ok = true;
-        for (int k = 0; ok; ++k) {
-            const int w = bwd_item_index(p.kv_items, k);
+        for (int k = 0; ok && (PERSIST || k == 0); ++k) {
+            const int w = bwd_item_index<PERSIST>(p.kv_items, k);
             if (w < 0) break;
             const int n_steps = item_steps(kv_item(p, w));
             auto so = [m0](int m) { return (uint64_t)((((m0 + m) % kRingKV) * L::kTile) >> 4); };
@@ -450,8 +456,8 @@ __global__ void __launch_bounds__(RowCfg<RW>::kThreads, 1) bwd_dkdv_kernel(const
         const float sc = p.scale_log2;
         int gs = 0;
         bool ok = true;
-        for (int k = 0; ok; ++k) {
-            const int w = bwd_item_index(p.kv_items, k);
+        for (int k = 0; ok && (PERSIST || k == 0); ++k) {
+            const int w = bwd_item_index<PERSIST>(p.kv_items, k);
             if (w < 0) break;
             const KvItem it = kv_item(p, w);
             const int n_steps = item_steps(it);
@@ -580,10 +586,45 @@ __global__ void __launch_bounds__(RowCfg<RW>::kThreads, 1) bwd_dkdv_kernel(const
 }
 
 // ----------------------------------------------------------------------- dQ
-// Block -> (rank, batch, query head, query tile), query tile fastest, last tile first;
-// query heads sharing a K/V head are adjacent.  Tensor memory: S/dS buffer 0 0..127 |
-// dP 128..255 | dQ 256.. | S/dS buffer 1 384..511.
-template <int D, int RW>
+// Work item = (rank, batch, query head, 128-query tile); a unit = (rank, batch, query head).
+// The query tiles of a unit run last tile first (the heaviest first under the causal mask).
+// Non-causal: a unit's tiles are adjacent.  Causal: bands of band_units_q units with the
+// query tile slowest inside a band (band_units_q = 1: unit-major).  Query heads sharing a
+// K/V head are adjacent units.
+struct QItem {
+    int rank, bb, hh, qt;
+};
+
+__device__ __forceinline__ QItem q_item(const BwdParams& p, int w) {
+    int u, r;
+    if (p.causal) {
+        const int per_band = p.band_units_q * p.n_tiles;
+        const int band = w / per_band, base = band * p.band_units_q;
+        const int in_band = p.n_units_q - base < p.band_units_q ? p.n_units_q - base : p.band_units_q;
+        const int i = w - band * per_band;
+        u = base + i % in_band;
+        r = i / in_band;
+    } else {
+        u = w / p.n_tiles;
+        r = w % p.n_tiles;
+    }
+    QItem it;
+    it.qt = p.n_tiles - 1 - r;
+    it.hh = u % p.hq;
+    u /= p.hq;
+    it.bb = u % p.b;
+    it.rank = u / p.b;
+    return it;
+}
+
+// Persistent as the dK/dV kernel: each CTA walks its items (once when the grid has one CTA
+// per item) with the barrier phases running on across items.  The producer loads the next
+// Q and dO as soon as the item's last S and dP have read the current ones; the next item's
+// first S, dP and second S follow the last dQ product and run while the row warps store
+// dQ; the next item's first dQ product (which overwrites the accumulator) waits for
+// dS-ready, which every row warp signals only after its epilogue.
+// Tensor memory: S/dS buffer 0 0..127 | dP 128..255 | dQ 256.. | S/dS buffer 1 384..511.
+template <int D, int RW, bool PERSIST>
 __global__ void __launch_bounds__(RowCfg<RW>::kThreads, 1) bwd_dq_kernel(const __grid_constant__ BwdParams p) {
     using C = RowCfg<RW>;
     constexpr int kBwdRowWarps = C::kRows, kBwdProducer = C::kProducer, kBwdMma = C::kMma;
@@ -591,8 +632,8 @@ __global__ void __launch_bounds__(RowCfg<RW>::kThreads, 1) bwd_dq_kernel(const _
     using L = BwdSmem<D, kRingQ>;
     constexpr uint32_t kSlab = 128 * 128;
     enum {
-        FIX = 0, FULL = 1, EMPTY = FULL + kRingQ, S_FULL = EMPTY + kRingQ, DP_FULL = S_FULL + 2, DS_READY, FINAL,
-        NBARS
+        FIX = 0, FIX_EMPTY, FULL, EMPTY = FULL + kRingQ, S_FULL = EMPTY + kRingQ, DP_FULL = S_FULL + 2, DS_READY,
+        FINAL, MMA_DONE, NBARS
     };
     static_assert(NBARS <= (int)L::kBarSlots, "barrier slots");
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -601,181 +642,213 @@ __global__ void __launch_bounds__(RowCfg<RW>::kThreads, 1) bwd_dq_kernel(const _
     Shared* sh = reinterpret_cast<Shared*>(smem + L::offBar + L::kBarSlots * 8);
     const uint32_t sbase = smem_addr(smem);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-    int bid = blockIdx.x;
-    const int qt = p.n_tiles - 1 - bid % p.n_tiles;
-    bid /= p.n_tiles;
-    const int hh = bid % p.hq;
-    bid /= p.hq;
-    const int bb = bid % p.b;
-    const int rank = bid / p.b;
-    const int kvh = hh / p.g;
-    const int q0 = qt * 128;
-    const int n_steps = p.causal ? qt + 1 : p.n_tiles;  // key tiles 0 .. n_steps-1
+    auto item_steps = [&p](const QItem& it) { return p.causal ? it.qt + 1 : p.n_tiles; };  // key tiles
 
     if (!bwd_setup(bars, NBARS, DS_READY, DS_READY + 1, kBwdRowWarps, kBwdMma, sh)) return;
     const uint32_t tmem = sh->tmem_base;
-    auto sbuf = [tmem](int n) { return tmem + ((n & 1) ? 384u : 0u); };
+    auto sbuf = [tmem](int gn) { return tmem + ((gn & 1) ? 384u : 0u); };  // by global step
 
     if (warp == kBwdProducer) {
-        const BwdTok qp = bwd_tok(p, rank, q0);
-        mbar_arrive_expect_tx_warp(&bars[FIX], 2 * L::kTile);
-#pragma unroll
-        for (int c = 0; c < D / 64; ++c) {
-            tma_load_4d_warp(sbase + L::offFixA + c * kSlab, &p.mq[qp.map], &bars[FIX], c * 64, hh, qp.row, bb);
-            tma_load_4d_warp(sbase + L::offFixB + c * kSlab, &p.mdo[qp.map], &bars[FIX], c * 64, hh, qp.row, bb);
-        }
-        int issued = 0;
+        // per item: the fixed tiles Q (A) and dO (B) of its query tile, then K_n and V_n
+        int issued = 0, fix_loads = 0;
         bool ok = true;
-        for (int m = 0; m < 2 * n_steps; ++m) {  // K_n, then V_n
-            const int slot = m % kRingQ;
-            ok = wait_phase_warp(&bars[EMPTY + slot], ((m / kRingQ) & 1) ^ 1, sh);
-            if (!ok) break;
-            const BwdTok kp = bwd_tok(p, rank, (m >> 1) * 128);
-            mbar_arrive_expect_tx_warp(&bars[FULL + slot], L::kTile);
+        for (int k = 0; ok && (PERSIST || k == 0); ++k) {
+            const int w = bwd_item_index<PERSIST>(p.q_items, k);
+            if (w < 0) break;
+            const QItem it = q_item(p, w);
+            const int n_steps = item_steps(it), kvh = it.hh / p.g;
+            if (k > 0) {  // the previous item's last S and dP have read Q and dO
+                ok = wait_phase_warp(&bars[FIX_EMPTY], (k - 1) & 1, sh);
+                if (!ok) break;
+            }
+            const BwdTok qp = bwd_tok(p, it.rank, it.qt * 128);
+            mbar_arrive_expect_tx_warp(&bars[FIX], 2 * L::kTile);
 #pragma unroll
-            for (int c = 0; c < D / 64; ++c)
-                tma_load_4d_warp(sbase + L::offRing + slot * L::kTile + c * kSlab, (m & 1) ? &p.mv[kp.map] : &p.mk[kp.map],
-                                 &bars[FULL + slot], c * 64, kvh, kp.row, bb);
-            ++issued;
+            for (int c = 0; c < D / 64; ++c) {
+                tma_load_4d_warp(sbase + L::offFixA + c * kSlab, &p.mq[qp.map], &bars[FIX], c * 64, it.hh, qp.row,
+                                 it.bb);
+                tma_load_4d_warp(sbase + L::offFixB + c * kSlab, &p.mdo[qp.map], &bars[FIX], c * 64, it.hh, qp.row,
+                                 it.bb);
+            }
+            ++fix_loads;
+            for (int m = 0; m < 2 * n_steps; ++m) {  // K_n, then V_n
+                const int slot = issued % kRingQ;
+                ok = wait_phase_warp(&bars[EMPTY + slot], ((issued / kRingQ) & 1) ^ 1, sh);
+                if (!ok) break;
+                const BwdTok kp = bwd_tok(p, it.rank, (m >> 1) * 128);
+                mbar_arrive_expect_tx_warp(&bars[FULL + slot], L::kTile);
+#pragma unroll
+                for (int c = 0; c < D / 64; ++c)
+                    tma_load_4d_warp(sbase + L::offRing + slot * L::kTile + c * kSlab,
+                                     (m & 1) ? &p.mv[kp.map] : &p.mk[kp.map], &bars[FULL + slot], c * 64, kvh, kp.row,
+                                     it.bb);
+                ++issued;
+            }
         }
-        if (!ok) {
+        if (!ok) {  // let the copies in flight land before the CTA leaves
             for (int slot = 0; slot < kRingQ; ++slot) {
                 const int cnt = (issued - slot + kRingQ - 1) / kRingQ;
                 if (cnt > 0) drain_phase(&bars[FULL + slot], (cnt - 1) & 1);
             }
-            drain_phase(&bars[FIX], 0);
+            if (fix_loads > 0) drain_phase(&bars[FIX], (fix_loads - 1) & 1);
         }
     } else if (warp == kBwdMma) {
         const uint64_t q_a = smem_desc_sw128(sbase + L::offFixA, 16, 1024);         // Q
         const uint64_t do_a = smem_desc_sw128(sbase + L::offFixB, 16, 1024);        // dO
         const uint64_t ring_k = smem_desc_sw128(sbase + L::offRing, 16, 1024);      // K / V, K-major
         const uint64_t ring_mn = smem_desc_sw128(sbase + L::offRing, kSlab, 1024);  // K, MN-major
-        auto so = [](int m) { return (uint64_t)(((m % kRingQ) * L::kTile) >> 4); };
-        auto full = [&](int m) { return wait_phase_warp(&bars[FULL + m % kRingQ], (m / kRingQ) & 1, sh); };
-        auto issue_s = [&](int n) {  // S(n) = Q K_n^T into buffer n % 2
-            mma_kmajor<D>(sbuf(n), q_a, ring_k + so(2 * n));
-            mma_commit_warp(&bars[S_FULL + (n & 1)]);
-        };
-        auto issue_dp = [&](int n) {  // dP(n) = dO V_n^T; V_n is not read after this
-            mma_kmajor<D>(tmem + 128u, do_a, ring_k + so(2 * n + 1));
-            mma_commit_warp(&bars[DP_FULL]);
-            mma_commit_warp(&bars[EMPTY + (2 * n + 1) % kRingQ]);
-        };
-        bool ok = wait_phase_warp(&bars[FIX], 0, sh) && full(0);
-        if (ok) {
-            tc_fence_after();
-            issue_s(0);
-            ok = full(1);
-        }
-        if (ok) {
-            tc_fence_after();
-            issue_dp(0);
-            if (n_steps > 1) {
-                ok = full(2);
-                if (ok) {
-                    tc_fence_after();
-                    issue_s(1);
+        int m0 = 0;  // ring position of the current item's K_0
+        int gs = 0;  // steps of the earlier items (buffers and per-step phases run on)
+        bool ok = true;
+        for (int k = 0; ok && (PERSIST || k == 0); ++k) {
+            const int w = bwd_item_index<PERSIST>(p.q_items, k);
+            if (w < 0) break;
+            const int n_steps = item_steps(q_item(p, w));
+            auto so = [m0](int m) { return (uint64_t)((((m0 + m) % kRingQ) * L::kTile) >> 4); };
+            auto full = [&](int m) {
+                return wait_phase_warp(&bars[FULL + (m0 + m) % kRingQ], ((m0 + m) / kRingQ) & 1, sh);
+            };
+            auto issue_s = [&](int n) {  // S(n) = Q K_n^T into the buffer of global step gs+n
+                mma_kmajor<D>(sbuf(gs + n), q_a, ring_k + so(2 * n));
+                mma_commit_warp(&bars[S_FULL + ((gs + n) & 1)]);
+            };
+            auto issue_dp = [&](int n) {  // dP(n) = dO V_n^T; V_n is not read after this
+                mma_kmajor<D>(tmem + 128u, do_a, ring_k + so(2 * n + 1));
+                mma_commit_warp(&bars[DP_FULL]);
+                mma_commit_warp(&bars[EMPTY + (m0 + 2 * n + 1) % kRingQ]);
+                if (n + 1 == n_steps) mma_commit_warp(&bars[FIX_EMPTY]);  // Q and dO read for the last time
+            };
+            ok = wait_phase_warp(&bars[FIX], k & 1, sh) && full(0);
+            if (ok) {
+                tc_fence_after();
+                issue_s(0);
+                ok = full(1);
+            }
+            if (ok) {
+                tc_fence_after();
+                issue_dp(0);
+                if (n_steps > 1) {
+                    ok = full(2);
+                    if (ok) {
+                        tc_fence_after();
+                        issue_s(1);
+                    }
                 }
             }
-        }
-        for (int n = 0; n < n_steps && ok; ++n) {
-            ok = wait_phase_warp(&bars[DS_READY], n & 1, sh);
+            for (int n = 0; n < n_steps && ok; ++n) {
+                ok = wait_phase_warp(&bars[DS_READY], (gs + n) & 1, sh);
+                if (!ok) break;
+                tc_fence_after();
+                mma_acc_tmemA<D, kColW>(tmem + 256u, sbuf(gs + n), ring_mn + so(2 * n), n > 0);  // dQ += dS K
+                mma_commit_warp(&bars[EMPTY + (m0 + 2 * n) % kRingQ]);
+                if (n + 1 < n_steps) {  // the row warps have read dP(n)
+                    ok = full(2 * n + 3);
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_dp(n + 1);
+                }
+                if (n + 2 < n_steps) {  // dS(n)'s buffer: dS(n) is read by the product issued above
+                    ok = full(2 * n + 4);
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_s(n + 2);
+                }
+            }
             if (!ok) break;
-            tc_fence_after();
-            mma_acc_tmemA<D, kColW>(tmem + 256u, sbuf(n), ring_mn + so(2 * n), n > 0);  // dQ += dS K
-            mma_commit_warp(&bars[EMPTY + (2 * n) % kRingQ]);
-            if (n + 1 < n_steps) {  // the row warps have read dP(n)
-                ok = full(2 * n + 3);
-                if (!ok) break;
-                tc_fence_after();
-                issue_dp(n + 1);
-            }
-            if (n + 2 < n_steps) {  // buffer n % 2: dS(n) is read by the product issued above
-                ok = full(2 * n + 4);
-                if (!ok) break;
-                tc_fence_after();
-                issue_s(n + 2);
-            }
+            mma_commit_warp(&bars[FINAL]);  // dQ of this item is complete
+            gs += n_steps;
+            m0 += 2 * n_steps;
         }
-        mma_commit_warp(&bars[FINAL]);
-        drain_phase(&bars[FINAL], 0);
+        // every MMA issued above completes before tensor memory is released
+        mma_commit_warp(&bars[MMA_DONE]);
+        drain_phase(&bars[MMA_DONE], 0);
     } else {
         // row warps: thread = query row; warp group cg owns key columns [cg*kColW, +kColW)
         const int sub = warp & 3, cg = warp >> 2;
-        const int row = sub * 32 + lane, qrow = q0 + row;
+        const int row = sub * 32 + lane;
         const uint32_t lane_off = (uint32_t)(sub * 32) << 16;
-        const size_t vi = bwd_stat_off(p, bb, hh, qrow);  // qrow < s_pad always
-        const int sr = bwd_stat_rank(p, rank, hh);
-        const float neg_l = -p.lse2[sr][vi];
-        const float neg_d = -p.dsum[sr][vi];
         const float sc = p.scale_log2;
-        const int lim = p.causal ? min(p.s, qrow + 1) : p.s;  // keys < lim are visible
+        const uint32_t tdP = tmem + 128u + lane_off + cg * kColW;
+        int gs = 0;
         bool ok = true;
-        for (int n = 0; n < n_steps; ++n) {
-            const uint32_t tS = sbuf(n) + lane_off + cg * kColW;
-            const uint32_t tdP = tmem + 128u + lane_off + cg * kColW;
-            const int kb = n * 128 + cg * kColW;  // first key column of this warp
-            // masked: the causal diagonal tile, and keys past the end (zero rows; kept out of
-            // the product so that no inf/nan can reach it)
-            const bool mask = (p.causal && n == qt) || kb + kColW > p.s;
-            float pf[kColW];
-            ok = wait_phase_warp(&bars[S_FULL + (n & 1)], (n >> 1) & 1, sh);
-            if (!ok) break;
-            tc_fence_after();
-            uint32_t sv[kChunks][32];  // every chunk's load in flight before one wait
+        for (int k = 0; ok && (PERSIST || k == 0); ++k) {
+            const int w = bwd_item_index<PERSIST>(p.q_items, k);
+            if (w < 0) break;
+            const QItem it = q_item(p, w);
+            const int n_steps = item_steps(it);
+            const int qt = it.qt, q0 = qt * 128, qrow = q0 + row;
+            const size_t vi = bwd_stat_off(p, it.bb, it.hh, qrow);  // qrow < s_pad always
+            const int sr = bwd_stat_rank(p, it.rank, it.hh);
+            const float neg_l = -p.lse2[sr][vi];
+            const float neg_d = -p.dsum[sr][vi];
+            const int lim = p.causal ? min(p.s, qrow + 1) : p.s;  // keys < lim are visible
+            for (int n = 0; n < n_steps; ++n) {
+                const int gn = gs + n;
+                const uint32_t tS = sbuf(gn) + lane_off + cg * kColW;
+                const int kb = n * 128 + cg * kColW;  // first key column of this warp
+                // masked: the causal diagonal tile, and keys past the end (zero rows; kept out of
+                // the product so that no inf/nan can reach it)
+                const bool mask = (p.causal && n == qt) || kb + kColW > p.s;
+                float pf[kColW];
+                ok = wait_phase_warp(&bars[S_FULL + (gn & 1)], (gn >> 1) & 1, sh);
+                if (!ok) break;
+                tc_fence_after();
+                uint32_t sv[kChunks][32];  // every chunk's load in flight before one wait
 #pragma unroll
-            for (int c = 0; c < kChunks; ++c) tmem_ld32(tS + c * 32, sv[c]);
-            tmem_wait_ld();
+                for (int c = 0; c < kChunks; ++c) tmem_ld32(tS + c * 32, sv[c]);
+                tmem_wait_ld();
 #pragma unroll
-            for (int c = 0; c < kChunks; ++c) {
+                for (int c = 0; c < kChunks; ++c) {
 #pragma unroll
-                for (int e = 0; e < 32; e += 2) {
-                    float a0, a1;
-                    ffma2(a0, a1, __uint_as_float(sv[c][e]), __uint_as_float(sv[c][e + 1]), sc, sc, neg_l, neg_l);
-                    float p0 = ex2_approx(a0), p1 = ex2_approx(a1);
-                    if (mask) {
-                        const int key = kb + c * 32 + e;
-                        p0 = key < lim ? p0 : 0.f;
-                        p1 = key + 1 < lim ? p1 : 0.f;
+                    for (int e = 0; e < 32; e += 2) {
+                        float a0, a1;
+                        ffma2(a0, a1, __uint_as_float(sv[c][e]), __uint_as_float(sv[c][e + 1]), sc, sc, neg_l, neg_l);
+                        float p0 = ex2_approx(a0), p1 = ex2_approx(a1);
+                        if (mask) {
+                            const int key = kb + c * 32 + e;
+                            p0 = key < lim ? p0 : 0.f;
+                            p1 = key + 1 < lim ? p1 : 0.f;
+                        }
+                        pf[c * 32 + e] = p0;
+                        pf[c * 32 + e + 1] = p1;
                     }
-                    pf[c * 32 + e] = p0;
-                    pf[c * 32 + e + 1] = p1;
                 }
+                ok = wait_phase_warp(&bars[DP_FULL], gn & 1, sh);
+                if (!ok) break;
+                tc_fence_after();
+                uint32_t dv[kChunks][32];
+#pragma unroll
+                for (int c = 0; c < kChunks; ++c) tmem_ld32(tdP + c * 32, dv[c]);
+                tmem_wait_ld();
+#pragma unroll
+                for (int c = 0; c < kChunks; ++c) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int e = 0; e < 32; e += 2) {
+                        float t0, t1;
+                        fadd2(t0, t1, __uint_as_float(dv[c][e]), __uint_as_float(dv[c][e + 1]), neg_d, neg_d);
+                        fmul2(t0, t1, pf[c * 32 + e], pf[c * 32 + e + 1], t0, t1);
+                        pk[e >> 1] = pack_bf16x2(t0, t1);
+                    }
+                    tmem_st16(tS + c * 16, pk);  // dS over S columns this warp has already read
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars[DS_READY]);
             }
-            ok = wait_phase_warp(&bars[DP_FULL], n & 1, sh);
+            if (ok) ok = wait_phase_warp(&bars[FINAL], k & 1, sh);
             if (!ok) break;
-            tc_fence_after();
-            uint32_t dv[kChunks][32];
-#pragma unroll
-            for (int c = 0; c < kChunks; ++c) tmem_ld32(tdP + c * 32, dv[c]);
-            tmem_wait_ld();
-#pragma unroll
-            for (int c = 0; c < kChunks; ++c) {
-                uint32_t pk[16];
-#pragma unroll
-                for (int e = 0; e < 32; e += 2) {
-                    float t0, t1;
-                    fadd2(t0, t1, __uint_as_float(dv[c][e]), __uint_as_float(dv[c][e + 1]), neg_d, neg_d);
-                    fmul2(t0, t1, pf[c * 32 + e], pf[c * 32 + e + 1], t0, t1);
-                    pk[e >> 1] = pack_bf16x2(t0, t1);
-                }
-                tmem_st16(tS + c * 16, pk);  // dS over S columns this warp has already read
+            constexpr int kEpi = D / kColGroups >= 32 ? D / kColGroups : 32;  // accumulator columns per warp
+            if (cg * kEpi < D) {
+                tc_fence_after();
+                const bool qok = qrow < p.s;
+                const BwdTok qt_ = bwd_tok(p, it.rank, qok ? qrow : q0);
+                const size_t off =
+                    (((size_t)it.bb * p.rows_per_map + qt_.row) * p.hq + it.hh) * (size_t)D * 2 + cg * kEpi * 2;
+                store_row_bf16<kEpi>(tmem + 256u + lane_off + cg * kEpi, p.dq[qt_.map] + off, p.scale, qok);
             }
-            tmem_wait_st();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars[DS_READY]);
-        }
-        if (ok) ok = wait_phase_warp(&bars[FINAL], 0, sh);
-        constexpr int kEpi = D / kColGroups >= 32 ? D / kColGroups : 32;  // accumulator columns per warp
-        if (ok && cg * kEpi < D) {
-            tc_fence_after();
-            const bool qok = qrow < p.s;
-            const BwdTok qt_ = bwd_tok(p, rank, qok ? qrow : q0);
-            const size_t off =
-                (((size_t)bb * p.rows_per_map + qt_.row) * p.hq + hh) * (size_t)D * 2 + cg * kEpi * 2;
-            store_row_bf16<kEpi>(tmem + 256u + lane_off + cg * kEpi, p.dq[qt_.map] + off, p.scale, qok);
+            gs += n_steps;
         }
     }
     tc_fence_before();
@@ -798,6 +871,17 @@ inline int bwd_band_units(int s_pad, int d, int g, int units) {
     return bu;
 }
 
+// Causal band of the dQ items, by the K and V they stream: the query heads of a band share
+// the K/V heads whose tiles fit in L2 together (all units when everything fits).
+inline int bwd_band_units_q(int s_pad, int d, int g, int units) {
+    const double kv_bytes = 2.0 * s_pad * d * 2;  // K and V of one K/V head, bf16
+    if (kv_bytes * units / g <= kL2Bytes) return units;
+    int bu = (int)(kBandBytes / kv_bytes) * g;
+    if (bu < 1) bu = 1;
+    if (bu > units) bu = units;
+    return bu;
+}
+
 template <int D>
 cudaError_t launch_bwd_d(const BwdParams& prm_in, int nranks, cudaStream_t stream) {
     using LK = BwdSmem<D, kRingKV>;
@@ -806,17 +890,27 @@ cudaError_t launch_bwd_d(const BwdParams& prm_in, int nranks, cudaStream_t strea
     prm.n_units = nranks * prm.b * prm.hkv;
     prm.kv_items = prm.n_units * prm.n_tiles;
     prm.band_units = bwd_band_units(prm.s_pad, D, prm.g, prm.n_units);
-    // Persistent when every CTA's share is balanced by the static order: items all equal
-    // (non-causal), or one band heaviest first.  Causal work in several bands runs one item
-    // per CTA in unit-major order instead (band_units = 1), so the hardware's block scheduler
-    // balances the unequal items as they finish.
-    const bool persistent = !prm.causal || prm.band_units == prm.n_units;
+    // Persistent when the static order balances the CTAs and the items are short enough for
+    // their fixed cost (about 8k cycles of set-up and epilogue against 2-3k per step) to
+    // matter: items all equal (non-causal), or causal in one band heaviest first with at most
+    // 64 tiles (33 steps per item on average).  Other causal work runs one item per CTA in
+    // unit-major order (band_units = 1): the hardware's block scheduler balances the unequal
+    // items as they finish, and the CTAs running at once share the same heads' tiles in L2.
+    const bool short_causal = prm.n_tiles <= 64;
+    const bool persistent = !prm.causal || (short_causal && prm.band_units == prm.n_units);
     if (!persistent) prm.band_units = 1;
-    auto* dkdv = prm.kv_grad_f32 ? bwd_dkdv_kernel<D, kRowsKV, true> : bwd_dkdv_kernel<D, kRowsKV, false>;
+    prm.n_units_q = nranks * prm.b * prm.hq;
+    prm.q_items = prm.n_units_q * prm.n_tiles;
+    prm.band_units_q = bwd_band_units_q(prm.s_pad, D, prm.g, prm.n_units_q);
+    const bool persistent_q = !prm.causal || (short_causal && prm.band_units_q == prm.n_units_q);
+    if (!persistent_q) prm.band_units_q = 1;
+    auto* dkdv = prm.kv_grad_f32 ? (persistent ? bwd_dkdv_kernel<D, kRowsKV, true, true>
+                                               : bwd_dkdv_kernel<D, kRowsKV, true, false>)
+                                 : (persistent ? bwd_dkdv_kernel<D, kRowsKV, false, true>
+                                               : bwd_dkdv_kernel<D, kRowsKV, false, false>);
+    auto* dq = persistent_q ? bwd_dq_kernel<D, kRowsQ, true> : bwd_dq_kernel<D, kRowsQ, false>;
     cudaError_t e = cudaFuncSetAttribute(dkdv, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)LK::kAlloc);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(bwd_dq_kernel<D, kRowsQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)LQ::kAlloc);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(dq, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)LQ::kAlloc);
     if (e != cudaSuccess) return e;
     int dev = 0, sms = 0;
     e = cudaGetDevice(&dev);
@@ -824,10 +918,10 @@ cudaError_t launch_bwd_d(const BwdParams& prm_in, int nranks, cudaStream_t strea
     if (e != cudaSuccess) return e;
     // dK/dV: one CTA per SM when persistent (each CTA fills an SM: shared memory and all TMEM)
     const long long gk = persistent && prm.kv_items > sms ? sms : prm.kv_items;
-    const long long gq = (long long)nranks * prm.b * prm.hq * prm.n_tiles;
+    const long long gq = persistent_q && prm.q_items > sms ? sms : prm.q_items;
     dkdv<<<(unsigned)gk, RowCfg<kRowsKV>::kThreads, LK::kAlloc, stream>>>(prm);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    bwd_dq_kernel<D, kRowsQ><<<(unsigned)gq, RowCfg<kRowsQ>::kThreads, LQ::kAlloc, stream>>>(prm);
+    dq<<<(unsigned)gq, RowCfg<kRowsQ>::kThreads, LQ::kAlloc, stream>>>(prm);
     return cudaGetLastError();
 }
