@@ -10,8 +10,8 @@ value   = algorithmic attention FLOP of the step / step time (TFLOP/s), whole jo
 roofline = the attention kernel against the measured bf16 tensor peak.
 e2e     = the same metric with host buffers: per step the pinned-host Q/K/V go to the
           device, the forward runs through the public API, the outputs come back; the
-          copies run on two copy streams with double-buffered device tensors, so step k+1's
-          inputs and step k's outputs move while the next step computes.
+          copies run on two copy streams with three device buffer sets, so the next steps'
+          inputs and the previous steps' outputs move while a step computes.
 cpu_baseline / --impl reference = the fp64 CPU oracle on a bounded sample of the workload.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
@@ -243,39 +243,41 @@ def run_gpu(args, rank, world):
 
     # end to end through the public API with pinned host buffers.  Every step copies its
     # inputs host -> device and every output device -> host inside the timed region; the
-    # copies run on their own streams with double-buffered device tensors, so step k+1's
-    # inputs and step k-1's outputs move while step k computes (as a training loop
-    # prefetches its next batch).
+    # copies run on their own streams with NBUF device buffer sets, so the next steps' inputs
+    # and the previous steps' outputs move while a step computes (as a training loop
+    # prefetches its next batches).  The host link carries both directions at once, and with
+    # three sets it always has a copy queued (two sets left it idle between steps).
     host_q = [t.cpu().pin_memory() for t in qs]
     host_k = [t.cpu().pin_memory() for t in ks]
     host_v = [t.cpu().pin_memory() for t in vs]
     fused_modes = (False, True) if fused_ok else (False,)
     variants = [(c, f) for c in w["masks"] for f in fused_modes]
     host_o = [[torch.empty((b, S, hq, d), dtype=dt).pin_memory() for _ in range(P)] for _ in variants]
-    dev_in = [[[torch.empty_like(t) for t in src] for src in (qs, ks, vs)] for _ in range(2)]
+    NBUF = 3
+    dev_in = [[[torch.empty_like(t) for t in src] for src in (qs, ks, vs)] for _ in range(NBUF)]
     dev_out = [[[torch.empty((b, S, hq, d), dtype=dt, device=dev) for _ in range(P)] for _ in variants]
-               for _ in range(2)]
+               for _ in range(NBUF)]
     h2d = sum(t.numel() * esz for t in host_q + host_k + host_v)
     d2h = sum(t.numel() * esz for ho in host_o for t in ho)
     ws = [torch.empty(uly.ulysses_dist_attn_workspace_bytes(P, b, s, hq, hkv, d, dt, False),
-                      dtype=torch.uint8, device=dev) for _ in range(2)]
+                      dtype=torch.uint8, device=dev) for _ in range(NBUF)]
     s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
-    ev_in = [torch.cuda.Event() for _ in range(2)]       # inputs of buffer i have landed
-    ev_done = [torch.cuda.Event() for _ in range(2)]     # compute on buffer i has finished
-    ev_copied = [torch.cuda.Event() for _ in range(2)]   # outputs of buffer i are on the host
+    ev_in = [torch.cuda.Event() for _ in range(NBUF)]       # inputs of buffer i have landed
+    ev_done = [torch.cuda.Event() for _ in range(NBUF)]     # compute on buffer i has finished
+    ev_copied = [torch.cuda.Event() for _ in range(NBUF)]   # outputs of buffer i are on the host
 
     def upload(k):
-        i = k % 2
-        s_in.wait_event(ev_done[i])  # step k-2 has finished reading these inputs
+        i = k % NBUF
+        s_in.wait_event(ev_done[i])  # step k-NBUF has finished reading these inputs
         with torch.cuda.stream(s_in):
             for src, dst in zip(host_q + host_k + host_v, [t for grp in dev_in[i] for t in grp]):
                 dst.copy_(src, non_blocking=True)
         ev_in[i].record(s_in)
 
     def compute_and_download(k):
-        i = k % 2
+        i = k % NBUF
         stream.wait_event(ev_in[i])
-        stream.wait_event(ev_copied[i])  # step k-2's outputs have left these buffers
+        stream.wait_event(ev_copied[i])  # step k-NBUF's outputs have left these buffers
         q_i, k_i, v_i = dev_in[i]
         for n, (causal, fused) in enumerate(variants):
             uly.ulysses_dist_attn_fwd(q_i, k_i, v_i, causal, fused=fused, out_seq=dev_out[i][n],
@@ -289,13 +291,14 @@ def run_gpu(args, rank, world):
         ev_copied[i].record(s_out)
 
     def run_e2e(n_steps):
-        for i in range(2):  # nothing is pending on either buffer
+        for i in range(NBUF):  # nothing is pending on any buffer
             ev_done[i].record(stream)
             ev_copied[i].record(stream)
-        upload(0)
+        for k in range(min(NBUF - 1, n_steps)):
+            upload(k)
         for k in range(n_steps):
-            if k + 1 < n_steps:
-                upload(k + 1)
+            if k + NBUF - 1 < n_steps:
+                upload(k + NBUF - 1)
             compute_and_download(k)
         stream.wait_stream(s_out)  # the last outputs are on the host before the clock stops
 
