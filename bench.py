@@ -363,15 +363,24 @@ def cpu_baseline_obj(smp):
                        f"({smp['perm_gbs']:.2f} GB/s); single thread of {os.cpu_count()} host cores")}
 
 
+KERNEL_REGION_END = b"// ---------------------------------------------------------------- host side"
+
+
 def kernel_source_digest():
-    """Digest of the attention kernel's sources (the traffic figure belongs to one version)."""
+    """Digest of the forward attention kernel's source: attn_tc.cu up to its host-side
+    section (the kernel and its device helpers) and device_common.cuh.  The traffic figure
+    belongs to one version of that code; launchers and the backward do not change it."""
     import hashlib
 
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "sequence_attention_seq_gb300", "csrc")
-    for name in ("attn_tc.cu", "device_common.cuh"):
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(f.read())
+    with open(os.path.join(csrc, "attn_tc.cu"), "rb") as f:
+        text = f.read()
+    if KERNEL_REGION_END not in text:
+        return None
+    h.update(text.split(KERNEL_REGION_END)[0])
+    with open(os.path.join(csrc, "device_common.cuh"), "rb") as f:
+        h.update(f.read())
     return h.hexdigest()
 
 

@@ -102,7 +102,7 @@ struct PrepParams {
     const float* lse[kMaxRanks];  // [b][Hq][s], natural log
     float* lse2[kMaxRanks];
     float* dsum[kMaxRanks];
-    long long rows;               // P * b * Hq * s_pad
+    int units;                    // P * b * Hq (rank, batch, head) units
     int b, s, s_pad, Hq, d, S, hq_total, seq_layout;
     int lanes_log2;               // log2(d / 8): lanes per row
 };
@@ -110,51 +110,65 @@ struct PrepParams {
 // d/8 lanes per (rank, batch, head, token) row, 16 bytes each.  O and dO are read in the
 // layout the caller holds them in: head layout of rank r, or (seq_layout) the seq layout,
 // where head-layout row (r, hh, t) is row t % S of rank t / S at head r*Hq + hh.
+constexpr int kPrepRows = 4;  // rows per lane group: their loads are all in flight at once
+
+// grid.y walks the (rank, batch, head) units, so their coordinates are decoded once per
+// block; grid.x covers the token rows of a unit, kPrepRows per lane group (rows t, t + G, ...).
 __global__ void __launch_bounds__(256) bwd_prep_kernel(const __grid_constant__ PrepParams p) {
-    const long long gt = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-    const long long row = gt >> p.lanes_log2;
-    const int sub = (int)(gt & ((1 << p.lanes_log2) - 1));
-    const bool valid = row < p.rows;
-    const long long rr = valid ? row : 0;
-    const int t = (int)(rr % p.s_pad);
-    long long r1 = rr / p.s_pad;
-    const int hh = (int)(r1 % p.Hq);
-    r1 /= p.Hq;
-    const int bb = (int)(r1 % p.b);
-    const int r = (int)(r1 / p.b);
-    float acc = 0.f;
-    if (valid && t < p.s) {
-        size_t off;
-        const uint8_t *o, *g;
-        if (p.seq_layout) {
-            const int j = t / p.S;
-            off = (((size_t)bb * p.S + (t - j * p.S)) * p.hq_total + (size_t)r * p.Hq + hh) * (size_t)p.d * 2;
-            o = p.o[j];
-            g = p.dout[j];
-        } else {
-            off = (((size_t)bb * p.s + t) * p.Hq + hh) * (size_t)p.d * 2;
-            o = p.o[r];
-            g = p.dout[r];
-        }
-        const uint4 a = *reinterpret_cast<const uint4*>(o + off + sub * 16);
-        const uint4 c = *reinterpret_cast<const uint4*>(g + off + sub * 16);
-        const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
-        const __nv_bfloat162* c2 = reinterpret_cast<const __nv_bfloat162*>(&c);
+    const int lanes_log2 = p.lanes_log2;
+    const int sub = (int)(threadIdx.x & ((1u << lanes_log2) - 1));
+    const int per_block = 256 >> lanes_log2;  // lane groups per block
+    const int G = (int)gridDim.x * per_block;
+    const int grp = (int)blockIdx.x * per_block + (int)(threadIdx.x >> lanes_log2);
+    for (int u = blockIdx.y; u < p.units; u += gridDim.y) {  // block-uniform: every shuffle has the whole warp
+        const int hh = u % p.Hq, r1 = u / p.Hq;
+        const int bb = r1 % p.b, r = r1 / p.b;
+        uint4 a[kPrepRows], c[kPrepRows];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const float2 fa = __bfloat1622float2(a2[e]), fc = __bfloat1622float2(c2[e]);
-            acc = fmaf(fa.x, fc.x, fmaf(fa.y, fc.y, acc));
+        for (int k = 0; k < kPrepRows; ++k) {
+            const int t = grp + k * G;
+            a[k] = make_uint4(0, 0, 0, 0);
+            c[k] = make_uint4(0, 0, 0, 0);
+            if (t < p.s) {
+                size_t off;
+                const uint8_t *o, *gp;
+                if (p.seq_layout) {
+                    const int j = t / p.S;
+                    off = (((size_t)bb * p.S + (t - j * p.S)) * p.hq_total + (size_t)r * p.Hq + hh) * (size_t)p.d * 2;
+                    o = p.o[j];
+                    gp = p.dout[j];
+                } else {
+                    off = (((size_t)bb * p.s + t) * p.Hq + hh) * (size_t)p.d * 2;
+                    o = p.o[r];
+                    gp = p.dout[r];
+                }
+                a[k] = *reinterpret_cast<const uint4*>(o + off + sub * 16);
+                c[k] = *reinterpret_cast<const uint4*>(gp + off + sub * 16);
+            }
         }
-    }
-    for (int o = 1 << (p.lanes_log2 - 1); o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-    if (valid && sub == 0) {
-        const size_t vi = ((size_t)bb * p.Hq + hh) * p.s_pad + t;
-        if (t < p.s) {
-            p.dsum[r][vi] = acc;
-            p.lse2[r][vi] = p.lse[r][((size_t)bb * p.Hq + hh) * p.s + t] * 1.4426950408889634f;
-        } else {
-            p.dsum[r][vi] = 0.f;
-            p.lse2[r][vi] = INFINITY;
+        const size_t vbase = ((size_t)bb * p.Hq + hh) * p.s_pad;
+        const size_t lbase = ((size_t)bb * p.Hq + hh) * p.s;
+#pragma unroll
+        for (int k = 0; k < kPrepRows; ++k) {
+            const int t = grp + k * G;
+            const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a[k]);
+            const __nv_bfloat162* c2 = reinterpret_cast<const __nv_bfloat162*>(&c[k]);
+            float acc = 0.f;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 fa = __bfloat1622float2(a2[e]), fc = __bfloat1622float2(c2[e]);
+                acc = fmaf(fa.x, fc.x, fmaf(fa.y, fc.y, acc));
+            }
+            for (int o = 1 << (lanes_log2 - 1); o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+            if (t < p.s_pad && sub == 0) {
+                if (t < p.s) {
+                    p.dsum[r][vbase + t] = acc;
+                    p.lse2[r][vbase + t] = p.lse[r][lbase + t] * 1.4426950408889634f;
+                } else {
+                    p.dsum[r][vbase + t] = 0.f;
+                    p.lse2[r][vbase + t] = INFINITY;
+                }
+            }
         }
     }
 }

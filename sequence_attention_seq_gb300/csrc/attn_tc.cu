@@ -776,9 +776,12 @@ cudaError_t launch_bwd_prep(int n_head_ranks, int n_seq_ranks, int b, int s, int
     pp->hq_total = h_q;
     pp->seq_layout = ptrs.od_seq_layout ? 1 : 0;
     pp->lanes_log2 = d == 64 ? 3 : 4;
-    pp->rows = (long long)n_head_ranks * b * pp->Hq * pp->s_pad;
-    const long long threads = pp->rows << pp->lanes_log2;
-    bwd_prep_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, stream>>>(*pp);
+    pp->units = n_head_ranks * b * pp->Hq;
+    // x: the s_pad rows of a unit, kPrepRows per lane group; y: the units
+    const int per_block = 256 >> pp->lanes_log2;
+    const int gx = (pp->s_pad + per_block * kPrepRows - 1) / (per_block * kPrepRows);
+    const int gy = pp->units < 65535 ? pp->units : 65535;
+    bwd_prep_kernel<<<dim3((unsigned)gx, (unsigned)gy, 1), 256, 0, stream>>>(*pp);
     delete pp;
     return cudaGetLastError();
 }
