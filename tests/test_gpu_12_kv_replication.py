@@ -57,7 +57,9 @@ def test_replicated_kv_forward_fp32():
 
 
 @pytest.mark.parametrize("P,b,s,hq,hkv,d,causal", [(4, 1, 512, 8, 2, 128, True), (4, 1, 512, 4, 1, 64, False),
-                                                     (8, 1, 1024, 8, 1, 128, True)])
+                                                     (8, 1, 1024, 8, 1, 128, True),
+                                                     # 192 dK/dV items: several per CTA of the persistent kernel
+                                                     (8, 8, 384, 16, 2, 64, True)])
 @pytest.mark.parametrize("fused", [False, True])
 def test_replicated_kv_training(P, b, s, hq, hkv, d, causal, fused):
     need_gpu()
