@@ -63,6 +63,8 @@ def test_replicated_kv_forward_fp32():
 @pytest.mark.parametrize("fused", [False, True])
 def test_replicated_kv_training(P, b, s, hq, hkv, d, causal, fused):
     need_gpu()
+    if fused and (s // P) % 128:
+        pytest.skip("the fused kernels need s/P to be a multiple of 128")
     q, k, v, (qs, ks, vs) = _inputs(P, b, s, hq, hkv, d, torch.bfloat16, seed=21 + s)
     do = global_grad(b, s, hq, d, torch.bfloat16, seed=22 + s)
     qd, kd, vd = ([t.cuda() for t in x] for x in (qs, ks, vs))
