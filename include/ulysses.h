@@ -150,7 +150,8 @@ uly_status ulysses_dist_attn_fwd(int P, int b, int s, int h_q, int h_kv, int d, 
  * plus: 1 <= n_chunks <= 64 and (h_q/P) % n_chunks == 0, and either (h_kv/P) % n_chunks
  * == 0 (every chunk has its own K/V heads) or n_chunks % (h_kv/P) == 0 (grouped heads:
  * n_chunks/(h_kv/P) consecutive chunks share one K/V head, exchanged with the first of
- * them), and h_kv % P == 0 (no replicated K/V heads), else ULY_ERR_INVALID_ARG;
+ * them), else ULY_ERR_INVALID_ARG.  Replicated K/V heads (P % h_kv == 0) leave every rank
+ * one K/V head, which all chunks share (exchanged, as a broadcast, with chunk 0);
  * workspace: 256-byte aligned, at least ulysses_dist_attn_overlap_workspace_bytes(...)
  * bytes (the chunks' head-layout Q, K, V, O).  The call creates and destroys CUDA events
  * (host objects) for the cross-stream ordering; it allocates no device memory.

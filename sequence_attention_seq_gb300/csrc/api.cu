@@ -559,8 +559,9 @@ struct OverlapPlan {
 
 OverlapPlan overlap_plan(int P, int h_q, int h_kv, int n_chunks) {
     OverlapPlan pl{n_chunks, 0, 0, 0, 1, false};
-    const int Hq = h_q / P, Hk = h_kv / P;
-    if (Hk < 1 || n_chunks < 1 || n_chunks > kMaxChunks || Hq % n_chunks) return pl;  // no replicated K/V
+    // replicated K/V heads (P a multiple of h_kv): one K/V head per rank, shared by every chunk
+    const int Hq = h_q / P, Hk = uly::kv_heads_per_rank(P, h_kv);
+    if (n_chunks < 1 || n_chunks > kMaxChunks || Hq % n_chunks) return pl;
     pl.Hc = Hq / n_chunks;
     if (Hk % n_chunks == 0) {
         pl.Hkc = Hk / n_chunks;
@@ -596,7 +597,7 @@ uly_status ulysses_dist_attn_fwd_overlap(int P, int b, int s, int h_q, int h_kv,
     if (st != ULY_OK) return st;
     st = check_exchange_shape(P, b, s, h_q, d, dtype);
     if (st != ULY_OK) return st;
-    st = check_exchange_shape(P, b, s, h_kv, d, dtype);
+    st = check_kv_exchange_shape(P, b, s, h_kv, d, dtype);
     if (st != ULY_OK) return st;
     const OverlapPlan pl = overlap_plan(P, h_q, h_kv, n_chunks);
     if (!pl.valid) return ULY_ERR_INVALID_ARG;
@@ -652,6 +653,7 @@ uly_status ulysses_dist_attn_fwd_overlap(int P, int b, int s, int h_q, int h_kv,
             t[k].h = k == 0 ? h_q : h_kv;
             t[k].hsub = k == 0 ? Hc : Hkc;
             t[k].hoff = k == 0 ? c * Hc : pl.kv_of(c) * Hkc;
+            if (k > 0) t[k].rep = uly::kv_replication(P, h_kv);
         }
         return uly::launch_permute(0, P, b, s, d, e, t, nt, side_stream);
     };

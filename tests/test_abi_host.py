@@ -116,3 +116,17 @@ def test_replicated_kv_workspace(lib):
         assert ws(P, b, s, hq, hkv, d, BF16, 0) == P * (2 * qb + 2 * kb)
         assert ws(P, b, s, hq, hkv, d, BF16, 1) == 0          # fused: no workspace
     assert ws(P, b, s, 12, 6, d, BF16, 0) == 0               # 6 and 4: neither divides the other
+
+
+def test_replicated_kv_overlap_workspace(lib):
+    """The overlapped forward with fewer K/V heads than ranks: all chunks share each rank's
+    one K/V head, so the workspace holds one K/V group next to every chunk's Q and O."""
+    ws = lib.ulysses_dist_attn_overlap_workspace_bytes
+    P, b, s, hq, d = 4, 1, 512, 8, 128
+    r = lambda x: (x + 255) // 256 * 256
+    for hkv in (1, 2):
+        for nc in (1, 2):
+            qb, kb = r(b * s * (hq // P // nc) * d * 2), r(b * s * 1 * d * 2)
+            assert ws(P, b, s, hq, hkv, d, BF16, nc) == P * (2 * qb * nc + 2 * kb)
+    assert ws(P, b, s, hq, 1, d, BF16, 4) == 0   # 2 query heads per rank do not split into 4 chunks
+    assert ws(P, b, s, 12, 6, d, BF16, 1) == 0   # 6 and 4: neither divides the other

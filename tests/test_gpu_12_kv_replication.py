@@ -1,8 +1,8 @@
 """Fewer K/V heads than ranks (P a multiple of h_kv, e.g. one K/V head for all ranks): every
 K/V head is replicated on the P/h_kv ranks whose query heads use it.  The forward (unfused,
 fused, fp32) and the training path against the oracle's attention on the global tensors,
-which is what replicated Ulysses must compute; fused and unfused forwards bit for bit; the
-unfused backward sums the replicas' dK/dV."""
+which is what replicated Ulysses must compute; fused, unfused and overlapped forwards bit
+for bit; the unfused backward sums the replicas' dK/dV."""
 import pytest
 import torch
 
@@ -83,13 +83,19 @@ def test_replicated_kv_training(P, b, s, hq, hkv, d, causal, fused):
             assert_close_grad(got[j], want[j], f"{name} rank {j}")
 
 
-def test_replicated_kv_limits():
+@pytest.mark.parametrize("P,b,s,hq,hkv,d,causal,n_chunks", [(4, 1, 512, 8, 2, 128, True, 2),
+                                                              (4, 2, 512, 8, 1, 64, False, 4),
+                                                              (8, 1, 1024, 16, 2, 128, True, 2),
+                                                              (2, 1, 384, 4, 1, 128, True, 1)])
+def test_replicated_kv_overlap(P, b, s, hq, hkv, d, causal, n_chunks):
+    # the overlapped forward: every chunk shares the rank's one K/V head; same bits as the
+    # unfused forward
     need_gpu()
-    # the overlapped forward splits K/V heads into groups: it needs P | h_kv
-    _, _, _, (qs, ks, vs) = _inputs(4, 1, 512, 8, 2, 128, torch.bfloat16, seed=5)
+    _, _, _, (qs, ks, vs) = _inputs(P, b, s, hq, hkv, d, torch.bfloat16, seed=5 + n_chunks)
     qd, kd, vd = ([t.cuda() for t in x] for x in (qs, ks, vs))
-    with pytest.raises(uly.UlyssesError) as e:
-        uly.ulysses_dist_attn_fwd_overlap(qd, kd, vd, True, n_chunks=2)
-    assert e.value.status == uly.ULY_ERR_INVALID_ARG
+    over = uly.ulysses_dist_attn_fwd_overlap(qd, kd, vd, causal, n_chunks=n_chunks)
+    plain = uly.ulysses_dist_attn_fwd(qd, kd, vd, causal, fused=False)
     torch.cuda.synchronize()
     device_ok()
+    for j in range(P):
+        assert bits_equal(over[j], plain[j]), f"rank {j}: overlapped != unfused"
