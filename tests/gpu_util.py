@@ -48,6 +48,24 @@ def assert_close_grad(got, ref, what=""):
     return err.max().item(), err.mean().item()
 
 
+# Norm-wise bound: max error <= 2^-6 max|ref| and mean error <= 2^-8 mean|ref|.  Used where
+# the element-wise bound above does not apply:
+# - saturated softmax inputs, where dS = P (dP - D) is a small difference of large terms;
+# - K/V heads shared by more than 4 query heads, where each dK/dV element sums many
+#   bf16-rounded dS (or P) terms of both signs.  Their rounding error scales with the sum
+#   of the terms' magnitudes, not with the (partly cancelled) result, so a few elements
+#   exceed the element-wise bound.  A float64 emulation of the kernel's roundings gives the
+#   same excess: 8 query heads per K/V head, 384 keys, ratio 1.01.
+def assert_normwise_grad(got, ref, what=""):
+    g = got.detach().to("cpu", torch.float64)
+    r = ref.to(torch.float64)
+    assert g.shape == r.shape, (g.shape, r.shape)
+    assert torch.isfinite(g).all(), f"{what}: non-finite gradient"
+    err = (g - r).abs()
+    assert err.max().item() <= 2.0 ** -6 * r.abs().max().item(), f"{what}: max-abs {err.max().item():.3e}"
+    assert err.mean().item() <= 2.0 ** -8 * r.abs().mean().item(), f"{what}: mean-abs {err.mean().item():.3e}"
+
+
 def bits_equal(a, b):
     return torch.equal(a.contiguous().view(torch.uint8), b.contiguous().view(torch.uint8))
 

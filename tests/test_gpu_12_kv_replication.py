@@ -8,7 +8,7 @@ import torch
 
 import oracle
 import sequence_attention_seq_gb300 as uly
-from gpu_util import assert_close, assert_close_grad, bits_equal, device_ok, need_gpu
+from gpu_util import assert_close, assert_close_grad, assert_normwise_grad, bits_equal, device_ok, need_gpu
 from sequence_attention_seq_gb300.inputs import global_grad, global_qkv, shard_seq
 
 pytestmark = pytest.mark.gpu
@@ -79,8 +79,10 @@ def test_replicated_kv_training(P, b, s, hq, hkv, d, causal, fused):
     gq, gk, gv = oracle.attention_bwd(q, k, v, do, causal)
     for name, got, ref in (("dq", dq, gq), ("dk", dk, gk), ("dv", dv, gv)):
         want = shard_seq(ref, P)
+        # dK/dV of a K/V head shared by more than 4 query heads: norm-wise (see gpu_util)
+        check = assert_normwise_grad if name != "dq" and hq // hkv > 4 else assert_close_grad
         for j in range(P):
-            assert_close_grad(got[j], want[j], f"{name} rank {j}")
+            check(got[j], want[j], f"{name} rank {j}")
 
 
 @pytest.mark.parametrize("P,b,s,hq,hkv,d,causal,n_chunks", [(4, 1, 512, 8, 2, 128, True, 2),
