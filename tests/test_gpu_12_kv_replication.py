@@ -86,7 +86,7 @@ def test_replicated_kv_training(P, b, s, hq, hkv, d, causal, fused):
 
 
 @pytest.mark.parametrize("P,b,s,hq,hkv,d,causal,n_chunks", [(4, 1, 512, 8, 2, 128, True, 2),
-                                                              (4, 2, 512, 8, 1, 64, False, 4),
+                                                              (4, 2, 512, 16, 1, 64, False, 4),
                                                               (8, 1, 1024, 16, 2, 128, True, 2),
                                                               (2, 1, 384, 4, 1, 128, True, 1)])
 def test_replicated_kv_overlap(P, b, s, hq, hkv, d, causal, n_chunks):
