@@ -181,8 +181,10 @@ uly_status ulysses_dist_attn_fwd_overlap(int P, int b, int s, int h_q, int h_kv,
  *  3. all-to-all #2 inside every group.
  * On one GPU the ring's transfers are reads of the other ranks' buffers (no copy).
  *   q_seq / o_seq: P pointers to [b][s/P][h_q][d]; k_seq / v_seq: [b][s/P][h_kv][d].
- * Sizes: Pu, Pr >= 1, Pu*Pr <= 64, s % (Pu*Pr) == 0, h_q % Pu == 0, h_kv % Pu == 0,
- * h_q % h_kv == 0, else ULY_ERR_INVALID_ARG.  Kernel: ULY_BF16, d in {64, 128},
+ * Sizes: Pu, Pr >= 1, Pu*Pr <= 64, s % (Pu*Pr) == 0, h_q % Pu == 0, h_q % h_kv == 0, and
+ * h_kv % Pu == 0 or Pu % h_kv == 0 (fewer K/V heads than Ulysses ranks: each K/V head is
+ * replicated on the Pu/h_kv ranks of every group whose query heads use it, as in
+ * ulysses_local_attention with P = Pu), else ULY_ERR_INVALID_ARG.  Kernel: ULY_BF16, d in {64, 128},
  * Pu*Pr <= 16 and (s/Pr) % 128 == 0, else ULY_ERR_UNSUPPORTED.  The result equals
  * ulysses_dist_attn_fwd over the same P ranks bit for bit.  workspace: 256-byte aligned,
  * at least ulysses_usp_workspace_bytes(...) bytes (every rank's group head-layout Q, K,

@@ -704,11 +704,11 @@ uly_status ulysses_dist_attn_fwd_overlap(int P, int b, int s, int h_q, int h_kv,
 }
 
 size_t ulysses_usp_workspace_bytes(int Pu, int Pr, int b, int s, int h_q, int h_kv, int d, uly_dtype dtype) {
-    if (Pu < 1 || Pr < 1 || Pu * Pr > kMaxRanks || s % (Pu * Pr) || h_kv < 1 || h_kv % Pu) return 0;
+    if (Pu < 1 || Pr < 1 || Pu * Pr > kMaxRanks || s % (Pu * Pr) || h_kv < 1) return 0;
     if (check_attention_shape(Pu, b, s / Pr, h_q, h_kv, d, dtype) == ULY_ERR_INVALID_ARG) return 0;
     const int e = elem_bytes(dtype), L = s / Pr;
     const uint64_t qb = round256((uint64_t)b * L * (h_q / Pu) * d * e);
-    const uint64_t kb = round256((uint64_t)b * L * (h_kv / Pu) * d * e);
+    const uint64_t kb = round256((uint64_t)b * L * uly::kv_heads_per_rank(Pu, h_kv) * d * e);
     return (size_t)((uint64_t)Pu * Pr * (2 * qb + 2 * kb));
 }
 
@@ -729,10 +729,11 @@ uly_status usp_attn_fwd(int Pu, int Pr, int b, int s, int h_q, int h_kv, int d, 
     if (st != ULY_OK) return st;
     st = check_exchange_shape(Pu, b, L, h_q, d, dtype);
     if (st != ULY_OK) return st;
-    st = check_exchange_shape(Pu, b, L, h_kv, d, dtype);
+    st = check_kv_exchange_shape(Pu, b, L, h_kv, d, dtype);
     if (st != ULY_OK) return st;
     if ((long long)b * h_q * ((s + 127) / 128) > 0x7fffffffLL) return ULY_ERR_INVALID_ARG;
     if (dtype != ULY_BF16 || P > 16 || L % 128 != 0) return ULY_ERR_UNSUPPORTED;
+    const int Hk = uly::kv_heads_per_rank(Pu, h_kv), kv_rep = uly::kv_replication(Pu, h_kv);
     const uint64_t qsb = (uint64_t)b * S * h_q * d * 2, ksb = (uint64_t)b * S * h_kv * d * 2;
     std::vector<Range> rq, rk, rv, ro;
     if (!collect(q_seq, P, qsb, rq) || !collect(k_seq, P, ksb, rk) || !collect(v_seq, P, ksb, rv) ||
@@ -752,8 +753,8 @@ uly_status usp_attn_fwd(int Pu, int Pr, int b, int s, int h_q, int h_kv, int d, 
         return ULY_ERR_INVALID_ARG;
 
     // workspace: per rank [Q | K | V | O] in head layout of its group: [b][s/Pr][h/Pu][d]
-    const Carve ws(workspace, {(uint64_t)b * L * (h_q / Pu) * d * 2, (uint64_t)b * L * (h_kv / Pu) * d * 2,
-                               (uint64_t)b * L * (h_kv / Pu) * d * 2, (uint64_t)b * L * (h_q / Pu) * d * 2});
+    const Carve ws(workspace, {(uint64_t)b * L * (h_q / Pu) * d * 2, (uint64_t)b * L * Hk * d * 2,
+                               (uint64_t)b * L * Hk * d * 2, (uint64_t)b * L * (h_q / Pu) * d * 2});
     uly::PermuteTensor* t = new uly::PermuteTensor[3];
     cudaError_t ce = cudaSuccess;
     // (1) all-to-all #1 inside every ring group of Pu consecutive ranks
@@ -766,6 +767,7 @@ uly_status usp_attn_fwd(int Pu, int Pr, int b, int s, int h_q, int h_kv, int d, 
                 t[k].dst[u] = ws.at(g * Pu + u, k);
             }
             t[k].h = k == 0 ? h_q : h_kv;
+            if (k > 0) t[k].rep = kv_rep;  // replicated K/V heads: a broadcast inside the group
         }
         ce = uly::launch_permute(0, Pu, b, L, d, 2, t, 3, stream);
     }
@@ -826,9 +828,11 @@ size_t ulysses_usp_bwd_workspace_bytes(int Pu, int Pr, int b, int s, int h_q, in
     if (ulysses_usp_workspace_bytes(Pu, Pr, b, s, h_q, h_kv, d, dtype) == 0 || dtype != ULY_BF16) return 0;
     const int L = s / Pr;
     const uint64_t qb = round256((uint64_t)b * L * (h_q / Pu) * d * 2);
-    const uint64_t kb = round256((uint64_t)b * L * (h_kv / Pu) * d * 2);
+    const uint64_t kb = round256((uint64_t)b * L * uly::kv_heads_per_rank(Pu, h_kv) * d * 2);
+    // replicated K/V heads: the dK/dV slots hold every replica's fp32 share until they are summed
+    const uint64_t gb = uly::kv_replication(Pu, h_kv) > 1 ? 2 * kb : kb;
     const uint64_t ra = row_array_bytes(Pu, b, s, h_q);
-    return (size_t)((uint64_t)Pu * Pr * (4 * qb + 3 * kb) + (uint64_t)Pu * 2 * ra);
+    return (size_t)((uint64_t)Pu * Pr * (4 * qb + kb + 2 * gb) + (uint64_t)Pu * 2 * ra);
 }
 
 uly_status ulysses_usp_attn_bwd(int Pu, int Pr, int b, int s, int h_q, int h_kv, int d, uly_dtype dtype, int causal,
@@ -842,10 +846,11 @@ uly_status ulysses_usp_attn_bwd(int Pu, int Pr, int b, int s, int h_q, int h_kv,
     if (st != ULY_OK) return st;
     st = check_exchange_shape(Pu, b, L, h_q, d, dtype);
     if (st != ULY_OK) return st;
-    st = check_exchange_shape(Pu, b, L, h_kv, d, dtype);
+    st = check_kv_exchange_shape(Pu, b, L, h_kv, d, dtype);
     if (st != ULY_OK) return st;
     if ((long long)b * h_q * ((s + 127) / 128) > 0x7fffffffLL) return ULY_ERR_INVALID_ARG;
     if (P > 16 || L % 128 != 0) return ULY_ERR_UNSUPPORTED;
+    const int Hk = uly::kv_heads_per_rank(Pu, h_kv), kv_rep = uly::kv_replication(Pu, h_kv);
     const uint64_t qsb = (uint64_t)b * S * h_q * d * 2, ksb = (uint64_t)b * S * h_kv * d * 2;
     std::vector<Range> in, rdq, rdk, rdv;
     if (!collect(q_seq, P, qsb, in) || !collect(k_seq, P, ksb, in) || !collect(v_seq, P, ksb, in) ||
@@ -864,9 +869,10 @@ uly_status ulysses_usp_attn_bwd(int Pu, int Pr, int b, int s, int h_q, int h_kv,
     std::vector<Range> rw{{reinterpret_cast<uintptr_t>(workspace), reinterpret_cast<uintptr_t>(workspace) + need}};
     if (overlaps(rw, in) || overlaps(rw, outs)) return ULY_ERR_INVALID_ARG;
 
-    const uint64_t qb = (uint64_t)b * L * (h_q / Pu) * d * 2, kb = (uint64_t)b * L * (h_kv / Pu) * d * 2;
+    const uint64_t qb = (uint64_t)b * L * (h_q / Pu) * d * 2, kb = (uint64_t)b * L * Hk * d * 2;
+    const uint64_t gb = kv_rep > 1 ? 2 * kb : kb;  // fp32 shares of replicated K/V heads
     enum { QH, KH, VH, DOH, DQH, DKH, DVH };
-    const Carve ws(workspace, {qb, kb, kb, qb, qb, kb, kb});
+    const Carve ws(workspace, {qb, kb, kb, qb, qb, gb, gb});
     const uint64_t ra = row_array_bytes(Pu, b, s, h_q);
     const Carve wr(static_cast<uint8_t*>(workspace) + ws.per_rank * P, {ra, ra});
     // (1) all-to-all #1 on Q, K, V and dO inside every ring group
@@ -882,6 +888,7 @@ uly_status ulysses_usp_attn_bwd(int Pu, int Pr, int b, int s, int h_q, int h_kv,
                 t[k].dst[u] = ws.at(g * Pu + u, dsts[k]);
             }
             t[k].h = (k == 1 || k == 2) ? h_kv : h_q;
+            if (k == 1 || k == 2) t[k].rep = kv_rep;
         }
         ce = uly::launch_permute(0, Pu, b, L, d, 2, t, 4, stream);
     }
@@ -907,12 +914,16 @@ uly_status ulysses_usp_attn_bwd(int Pu, int Pr, int b, int s, int h_q, int h_kv,
         p->dsum[u] = static_cast<float*>(wr.at(u, 1));
     }
     p->od_seq_layout = 1;
+    p->kv_grad_f32 = kv_rep > 1 ? 1 : 0;
     int unsupported = 0;
     ce = uly::launch_attention_bwd_tc_usp(Pu, Pr, b, s, h_q, h_kv, d, causal, *p, stream, &unsupported);
     delete p;
     if (unsupported) return ULY_ERR_UNSUPPORTED;
     if (ce != cudaSuccess) return ULY_ERR_CUDA;
-    // (3) all-to-all #2 on dQ, dK, dV inside every ring group
+    // (3) all-to-all #2 on dQ, dK, dV inside every ring group.  Replicated K/V heads: the
+    //     group's replicas of a head hold the gradients from their own query heads, and the
+    //     backward of the broadcast is their sum
+    const int n_plain = kv_rep > 1 ? 1 : 3;
     t = new uly::PermuteTensor[3];
     void* const* dsts2[3] = {dq_seq, dk_seq, dv_seq};
     const int srcs2[3] = {DQH, DKH, DVH};
@@ -925,7 +936,9 @@ uly_status ulysses_usp_attn_bwd(int Pu, int Pr, int b, int s, int h_q, int h_kv,
             }
             t[k].h = k == 0 ? h_q : h_kv;
         }
-        ce = uly::launch_permute(1, Pu, b, L, d, 2, t, 3, stream);
+        ce = uly::launch_permute(1, Pu, b, L, d, 2, t, n_plain, stream);
+        for (int k = 1; k < 3 && kv_rep > 1 && ce == cudaSuccess; ++k)
+            ce = uly::launch_kv_grad_sum(Pu, kv_rep, b, L, h_kv, d, t[k].src, t[k].dst, stream);
     }
     delete[] t;
     return ce == cudaSuccess ? ULY_OK : ULY_ERR_CUDA;

@@ -714,7 +714,7 @@ cudaError_t launch_attention_tc_usp(int Pu, int Pr, int b, int s, int h_q, int h
         *unsupported = 1;
         return cudaSuccess;
     }
-    const int Hq = h_q / Pu, Hk = h_kv / Pu;
+    const int Hq = h_q / Pu, Hk = kv_heads_per_rank(Pu, h_kv);  // 1: a replicated K/V head
     TcParams* prm = new TcParams;
     memset(prm, 0, sizeof(TcParams));
     prm->s = s;
@@ -869,7 +869,7 @@ cudaError_t launch_attention_bwd_tc_usp(int Pu, int Pr, int b, int s, int h_q, i
         *unsupported = 1;
         return cudaSuccess;
     }
-    const int Hq = h_q / Pu, Hk = h_kv / Pu;
+    const int Hq = h_q / Pu, Hk = kv_heads_per_rank(Pu, h_kv);  // 1: a replicated K/V head
     const int n_tiles = (s + 127) / 128;
     // (1) statistics per Ulysses unit (Pu head ranks over all s rows), O and dO in seq layout
     cudaError_t err = launch_bwd_prep(Pu, P, b, s, h_q, d, ptrs, stream);
@@ -881,7 +881,7 @@ cudaError_t launch_attention_bwd_tc_usp(int Pu, int Pr, int b, int s, int h_q, i
     prm->s = s;
     prm->s_pad = n_tiles * 128;
     prm->n_tiles = n_tiles;
-    prm->g = h_q / h_kv;
+    prm->g = Hq / Hk;  // within a unit
     prm->b = b;
     prm->causal = causal ? 1 : 0;
     prm->hq_rank = Hq;
@@ -889,6 +889,7 @@ cudaError_t launch_attention_bwd_tc_usp(int Pu, int Pr, int b, int s, int h_q, i
     prm->hkv = Hk;
     prm->rows_per_map = L;
     prm->map_stride = Pu;
+    prm->kv_grad_f32 = ptrs.kv_grad_f32;
     prm->scale = (float)(1.0 / std::sqrt((double)d));
     prm->scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)d));
     for (int j = 0; j < P && err == cudaSuccess; ++j) {

@@ -130,3 +130,18 @@ def test_replicated_kv_overlap_workspace(lib):
             assert ws(P, b, s, hq, hkv, d, BF16, nc) == P * (2 * qb * nc + 2 * kb)
     assert ws(P, b, s, hq, 1, d, BF16, 4) == 0   # 2 query heads per rank do not split into 4 chunks
     assert ws(P, b, s, 12, 6, d, BF16, 1) == 0   # 6 and 4: neither divides the other
+
+
+def test_replicated_kv_two_level_workspace(lib):
+    """The two-level layout with fewer K/V heads than Ulysses ranks: one K/V head per rank of
+    a group; the backward keeps fp32 dK/dV shares (twice the bf16 size) until they are summed."""
+    fw, bw = lib.ulysses_usp_workspace_bytes, lib.ulysses_usp_bwd_workspace_bytes
+    Pu, Pr, b, s, hq, d = 4, 2, 1, 1024, 8, 128
+    r = lambda x: (x + 255) // 256 * 256
+    L = s // Pr
+    qb, kb = r(b * L * (hq // Pu) * d * 2), r(b * L * 1 * d * 2)
+    ra = r(b * (hq // Pu) * ((s + 127) // 128 * 128) * 4)
+    for hkv in (1, 2):
+        assert fw(Pu, Pr, b, s, hq, hkv, d, BF16) == Pu * Pr * (2 * qb + 2 * kb)
+        assert bw(Pu, Pr, b, s, hq, hkv, d, BF16) == Pu * Pr * (4 * qb + kb + 4 * kb) + Pu * 2 * ra
+    assert fw(Pu, Pr, b, s, 12, 3, d, BF16) == 0   # 3 and 4: neither divides the other

@@ -101,3 +101,42 @@ def test_replicated_kv_overlap(P, b, s, hq, hkv, d, causal, n_chunks):
     device_ok()
     for j in range(P):
         assert bits_equal(over[j], plain[j]), f"rank {j}: overlapped != unfused"
+
+
+USP_CASES = [
+    # Pu, Pr, b, s, hq, hkv, d, causal: fewer K/V heads than Ulysses ranks in every group
+    (4, 2, 1, 1024, 8, 2, 128, True),    # each K/V head on 2 ranks of a group
+    (4, 2, 1, 1024, 4, 1, 64, False),    # one K/V head for the whole group
+    (2, 2, 2, 512, 4, 1, 128, True),
+]
+
+
+@pytest.mark.parametrize("Pu,Pr,b,s,hq,hkv,d,causal", USP_CASES)
+def test_replicated_kv_two_level(Pu, Pr, b, s, hq, hkv, d, causal):
+    # the two-level layout with replicated K/V heads: forward against the oracle's attention
+    # on the global tensors and bit for bit against plain Ulysses over the same ranks (which
+    # replicates too); the training path against the oracle's attention backward
+    need_gpu()
+    P = Pu * Pr
+    q, k, v, (qs, ks, vs) = _inputs(P, b, s, hq, hkv, d, torch.bfloat16, seed=41 + s + Pu)
+    do = global_grad(b, s, hq, d, torch.bfloat16, seed=42 + s + Pu)
+    qd, kd, vd = ([t.cuda() for t in x] for x in (qs, ks, vs))
+    dod = [t.cuda() for t in shard_seq(do, P)]
+    out = uly.ulysses_usp_attn_fwd(qd, kd, vd, causal, Pu, Pr)
+    # plain Ulysses over all P ranks needs P | h_q (the two-level split only Pu | h_q)
+    plain = uly.ulysses_dist_attn_fwd(qd, kd, vd, causal, fused=False) if hq % P == 0 else None
+    o, lse = uly.ulysses_usp_attn_fwd_lse(qd, kd, vd, causal, Pu, Pr)
+    dq, dk, dv = uly.ulysses_usp_attn_bwd(qd, kd, vd, o, dod, lse, causal, Pu, Pr)
+    torch.cuda.synchronize()
+    device_ok()
+    want = shard_seq(oracle.attention(q, k, v, causal), P)
+    for j in range(P):
+        assert_close(out[j], want[j], torch.bfloat16, f"rank {j}")
+        if plain is not None:
+            assert bits_equal(out[j], plain[j]), f"rank {j}: two-level != plain Ulysses"
+        assert bits_equal(o[j], out[j]), f"rank {j}: the statistics store changed the output"
+    gq, gk, gv = oracle.attention_bwd(q, k, v, do, causal)
+    for name, got, ref in (("dq", dq, gq), ("dk", dk, gk), ("dv", dv, gv)):
+        want = shard_seq(ref, P)
+        for j in range(P):
+            assert_close_grad(got[j], want[j], f"{name} rank {j}")
