@@ -145,3 +145,14 @@ def test_replicated_kv_two_level_workspace(lib):
         assert fw(Pu, Pr, b, s, hq, hkv, d, BF16) == Pu * Pr * (2 * qb + 2 * kb)
         assert bw(Pu, Pr, b, s, hq, hkv, d, BF16) == Pu * Pr * (4 * qb + kb + 4 * kb) + Pu * 2 * ra
     assert fw(Pu, Pr, b, s, 12, 3, d, BF16) == 0   # 3 and 4: neither divides the other
+
+
+def test_two_level_kv_head_rule(lib):
+    """The two-level forward checks the K/V-head rule with the Ulysses degree Pu in place of P,
+    before anything is enqueued: 3 K/V heads and Pu = 4 divide neither way."""
+    f = lib.ulysses_usp_attn_fwd
+    arr = lambda base: _arr(*[base + i * 0x1000000 for i in range(4)])
+    q, k, v, o = arr(A), arr(B), arr(C), arr(D)
+    assert f(4, 1, 1, 512, 12, 3, 128, BF16, 1, q, k, v, o, None, 0, None) == INVALID
+    assert f(4, 1, 1, 512, 12, 5, 128, BF16, 1, q, k, v, o, None, 0, None) == INVALID   # h_q % h_kv
+    assert f(4, 1, 1, 512, 6, 2, 128, BF16, 1, q, k, v, o, None, 0, None) == INVALID    # h_q % Pu
