@@ -1,20 +1,26 @@
 """Benchmark of the Ulysses DistributedAttention forward on GB300.
 
-One step = one pass of the whole hot path over the DiT-like workload (P=4 virtual ranks,
-b=2, s=4096, h=32, d=128, bf16 N(0,1)), for both the non-causal and the causal mask:
+The default line is the Long-sequence causal workload (P=8 virtual ranks, b=1, s=131072,
+h=64, d=128, bf16 N(0,1)).  One step = one pass of the whole hot path over it:
     all-to-all #1 on Q, K, V  ->  local attention  ->  all-to-all #2 on O   (unfused)
-    the fused kernel (exchanges folded into the attention tiles)             (fused)
+    the fused kernel (both exchanges folded into the attention tiles)         (fused)
 Every kernel launch is bracketed by CUDA events on the launching stream.
 
-value   = algorithmic attention FLOP of the step / step time (TFLOP/s), whole job.
-roofline = the attention kernel against the measured bf16 tensor peak.
-e2e     = the same metric with host buffers: per step the pinned-host Q/K/V go to the
-          device, the forward runs through the public API, the outputs come back; the
-          copies run on two copy streams with three device buffer sets, so the next steps'
-          inputs and the previous steps' outputs move while a step computes.
-cpu_baseline / --impl reference = the fp64 CPU oracle on a bounded sample of the workload.
+value    = algorithmic attention FLOP of the step / step time (TFLOP/s), whole job.
+roofline = the fused attention launch against the measured bf16 tensor peak (burst, and
+           the sustained figure beside it); the unfused attention launch is reported too.
+permute  = the exchanges of the step (2 GiB tensors, far beyond L2) against the measured
+           HBM copy rate.
+e2e      = the fused forward through the public API with host buffers: per step the
+           pinned-host Q/K/V go to the device, the call runs, the output comes back; the
+           copies run on two copy streams with three device buffer sets, so the next steps'
+           inputs and the previous steps' outputs move while a step computes.
+extra    = the DiT-like and GQA workloads, each in a timed region of its own after the
+           main one (attention launches and exchanges).
+cpu_baseline / --impl reference = the fp64 CPU oracle on a bounded sample of the workload
+           (exact output rows, extrapolated to a rate).
 
-Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference] [--workload W]
 Multi-GPU (torchrun): every rank runs an independent replica (the path needs no exchange
 between GPUs on this single-GPU emulation); value sums ranks over the slowest rank's time.
 """
@@ -34,22 +40,23 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "Ulysses attn fwd TFLOP/s + a2a permute GB/s, as fraction of GB300 roofline"
-# The default line is the DiT-like workload; the others are the named configurations,
-# measured on request (--workload).
 WORKLOADS = {
+    "long": dict(P=8, b=1, s=131072, h_q=64, h_kv=64, d=128, dtype="bf16", masks=(True,),
+                 name="Long-sequence causal: P=8 b=1 s=131072 h=64 d=128 bf16, unfused + fused forward"),
     "dit": dict(P=4, b=2, s=4096, h_q=32, h_kv=32, d=128, dtype="bf16", masks=(False, True),
                 name="DiT-like MHA: P=4 b=2 s=4096 h=32 d=128 bf16, non-causal + causal, unfused + fused forward"),
     "gqa": dict(P=8, b=1, s=32768, h_q=32, h_kv=8, d=128, dtype="bf16", masks=(True,),
                 name="GQA causal: P=8 b=1 s=32768 h_q=32 h_kv=8 d=128 bf16, unfused + fused forward"),
-    "long": dict(P=8, b=1, s=131072, h_q=64, h_kv=64, d=128, dtype="bf16", masks=(True,),
-                 name="Long-sequence causal: P=8 b=1 s=131072 h=64 d=128 bf16, unfused + fused forward"),
     "usp": dict(P=8, Pu=4, Pr=2, b=1, s=262144, h_q=16, h_kv=16, d=128, dtype="bf16", masks=(True,),
                 name="Ulysses x Ring causal: 256K tokens, Ulysses 4 x Ring 2 (P=8), b=1 h=16 d=128 bf16"),
     "tiny": dict(P=2, b=1, s=64, h_q=4, h_kv=4, d=16, dtype="fp32", masks=(False,),
                  name="Tiny exactness case: P=2 b=1 s=64 h=4 d=16 fp32, non-causal, unfused forward"),
 }
-WORKLOAD = WORKLOADS["dit"]
-WORKLOAD_NAME = WORKLOAD["name"]
+DEFAULT_WORKLOAD = "long"
+# timed steps when --steps is not given: a multi-second timed region for every workload
+DEFAULT_STEPS = {"long": 20, "gqa": 100, "dit": 2000, "usp": 10, "tiny": 400}
+# the other named workloads, measured after the main line's timed region: (workload, steps)
+EXTRAS = {"long": (("dit", 1000), ("gqa", 60))}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -134,42 +141,33 @@ class ClockSampler:
 
         sm = [num(r[1]) for r in rows if num(r[1]) is not None]
         mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        pw = [num(r[3]) for r in rows if num(r[3]) is not None]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[k] for r in rows for k in range(4) if r[5 + k].lower().startswith("active")})
+        capped = sum(1 for r in rows if r[8].lower().startswith("active"))
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": reasons, "samples": len(rows)}
+                "sm_mhz_min": min(sm) if sm else None, "power_w_median": statistics.median(pw) if pw else None,
+                "reasons": reasons, "samples": len(rows), "samples_sw_power_cap": capped}
 
 
 # ------------------------------------------------------------------------- GPU arm
-def run_gpu(args, rank, world):
-    import torch
-
-    import sequence_attention_seq_gb300 as uly
-    from sequence_attention_seq_gb300 import build as uly_build
+def forward_ops(uly, torch, w, dev, seed):
+    """The launches of one step of workload w, (label, kind, bytes moved, flops, callable),
+    one kernel launch each, plus the seq-layout inputs."""
     from sequence_attention_seq_gb300.inputs import seq_shards_qkv
 
-    if rank == 0 or not os.path.exists(uly.library_path()):
-        uly_build.build()
-    if world > 1:
-        torch.distributed.barrier()
-    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
-    torch.cuda.set_device(dev)
-    w = WORKLOADS[args.workload]
     P, b, s, hq, hkv, d = w["P"], w["b"], w["s"], w["h_q"], w["h_kv"], w["d"]
     S = s // P
     dt = torch.bfloat16 if w["dtype"] == "bf16" else torch.float32
     esz = 2 if dt == torch.bfloat16 else 4
     fused_ok = dt == torch.bfloat16 and S % 128 == 0 and P <= 16
-    qs, ks, vs = seq_shards_qkv(P, b, s, hq, hkv, d, dt, seed=rank, device=str(dev))
+    qs, ks, vs = seq_shards_qkv(P, b, s, hq, hkv, d, dt, seed=seed, device=str(dev))
     q_head = [torch.empty((b, s, hq // P, d), dtype=dt, device=dev) for _ in range(P)]
     k_head = [torch.empty((b, s, hkv // P, d), dtype=dt, device=dev) for _ in range(P)]
     v_head = [torch.empty((b, s, hkv // P, d), dtype=dt, device=dev) for _ in range(P)]
     o_head = [torch.empty((b, s, hq // P, d), dtype=dt, device=dev) for _ in range(P)]
     o_seq = [torch.empty((b, S, hq, d), dtype=dt, device=dev) for _ in range(P)]
     o_fused = [torch.empty((b, S, hq, d), dtype=dt, device=dev) for _ in range(P)]
-    stream = torch.cuda.current_stream(dev)
-
-    # (label, kind, bytes moved, flops, callable); one kernel launch each
     tensor_bytes = b * s * hq * d * esz
     kv_bytes = b * s * hkv * d * esz
     ops = []
@@ -177,18 +175,22 @@ def run_gpu(args, rank, world):
         fl = attn_flops(b, s, hq, d, causal)
         tag = "causal" if causal else "noncausal"
         ops += [
-            (f"a2a_seq2head_q", "permute", 2 * tensor_bytes, 0, lambda: uly.ulysses_a2a_seq2head(qs, q_head)),
-            (f"a2a_seq2head_k", "permute", 2 * kv_bytes, 0, lambda: uly.ulysses_a2a_seq2head(ks, k_head)),
-            (f"a2a_seq2head_v", "permute", 2 * kv_bytes, 0, lambda: uly.ulysses_a2a_seq2head(vs, v_head)),
+            ("a2a_seq2head_q", "permute", 2 * tensor_bytes, 0, lambda: uly.ulysses_a2a_seq2head(qs, q_head)),
+            ("a2a_seq2head_k", "permute", 2 * kv_bytes, 0, lambda: uly.ulysses_a2a_seq2head(ks, k_head)),
+            ("a2a_seq2head_v", "permute", 2 * kv_bytes, 0, lambda: uly.ulysses_a2a_seq2head(vs, v_head)),
             (f"attn_{tag}", "attention", 0, fl,
              (lambda c=causal: uly.ulysses_local_attention(q_head, k_head, v_head, c, o_head))),
-            (f"a2a_head2seq_o", "permute", 2 * tensor_bytes, 0, lambda: uly.ulysses_a2a_head2seq(o_head, o_seq)),
+            ("a2a_head2seq_o", "permute", 2 * tensor_bytes, 0, lambda: uly.ulysses_a2a_head2seq(o_head, o_seq)),
         ]
         if fused_ok:
             ops.append((f"fused_{tag}", "fused", 0, fl,
                         (lambda c=causal: uly.ulysses_dist_attn_fwd(qs, ks, vs, c, fused=True, out_seq=o_fused))))
-    step_flops = sum(op[3] for op in ops)
+    return ops, (qs, ks, vs), fused_ok
 
+
+def time_ops(torch, uly, ops, steps, warmup, dev, stream, clocks=None, world=1):
+    """W untimed steps, then exactly K timed steps bracketed by a barrier and a device
+    synchronisation on both sides; every launch between CUDA events on its stream."""
     def step(events=None):
         for n, op in enumerate(ops):
             if events is not None:
@@ -197,80 +199,94 @@ def run_gpu(args, rank, world):
             if events is not None:
                 events[n][1].record(stream)
 
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         step()
     torch.cuda.synchronize(dev)
     if uly.ulysses_device_status(clear=True) != 0:
         raise RuntimeError("a kernel's bounded wait gave up during warm-up")
-
     ev = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)] for _ in ops]
-          for _ in range(args.steps)]
+          for _ in range(steps)]
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    clocks = ClockSampler(dev.index if dev.index is not None else 0)
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize(dev)
-    clocks.start()
-    time.sleep(0.3)  # let the sampler come up before the timed region
+    if clocks is not None:
+        clocks.start()
+        time.sleep(0.3)  # let the sampler come up before the timed region
     t_start.record(stream)
-    for k in range(args.steps):
+    for k in range(steps):
         step(ev[k])
     t_end.record(stream)
     torch.cuda.synchronize(dev)
-    clk = clocks.stop()
+    clk = clocks.stop() if clocks is not None else None
     if world > 1:
         torch.distributed.barrier()
-    total_ms = t_start.elapsed_time(t_end)
     if uly.ulysses_device_status(clear=True) != 0:
         raise RuntimeError("a kernel's bounded wait gave up during the timed steps")
-
     per_op = {}
     for n, op in enumerate(ops):
-        per_op.setdefault(op[0], []).extend(ev[k][n][0].elapsed_time(ev[k][n][1]) for k in range(args.steps))
+        per_op.setdefault(op[0], []).extend(ev[k][n][0].elapsed_time(ev[k][n][1]) for k in range(steps))
+    return t_start.elapsed_time(t_end), per_op, clk
 
-    # attention kernel (fused launches carry the whole forward in one launch)
-    attn_launch_ms, attn_launch_flops = [], []
-    for n, op in enumerate(ops):
-        if op[1] in ("attention", "fused"):
-            for k in range(args.steps):
-                attn_launch_ms.append(ev[k][n][0].elapsed_time(ev[k][n][1]))
-                attn_launch_flops.append(op[3])
-    attn_tflops = sum(attn_launch_flops) / (sum(attn_launch_ms) * 1e-3) / 1e12
-    perm_ms = [ev[k][n][0].elapsed_time(ev[k][n][1]) for n, op in enumerate(ops) if op[1] == "permute"
-               for k in range(args.steps)]
-    perm_bytes = [op[2] for op in ops if op[1] == "permute"] * args.steps
-    perm_gbs = sum(perm_bytes) / (sum(perm_ms) * 1e-3) / 1e9
 
-    # end to end through the public API with pinned host buffers.  Every step copies its
-    # inputs host -> device and every output device -> host inside the timed region; the
-    # copies run on their own streams with NBUF device buffer sets, so the next steps' inputs
-    # and the previous steps' outputs move while a step computes (as a training loop
-    # prefetches its next batches).  The host link carries both directions at once, and with
-    # three sets it always has a copy queued (two sets left it idle between steps).
-    host_q = [t.cpu().pin_memory() for t in qs]
-    host_k = [t.cpu().pin_memory() for t in ks]
-    host_v = [t.cpu().pin_memory() for t in vs]
-    fused_modes = (False, True) if fused_ok else (False,)
-    variants = [(c, f) for c in w["masks"] for f in fused_modes]
-    host_o = [[torch.empty((b, S, hq, d), dtype=dt).pin_memory() for _ in range(P)] for _ in variants]
+def summarize(ops, per_op, steps, peaks):
+    """Per-kind rates from the per-launch event times: attention and fused launches in
+    TFLOP/s against the bf16 peak, exchanges in GB/s against the copy bandwidth."""
+    out = {}
+    labels = {}
+    for op in ops:
+        labels.setdefault(op[1], {}).setdefault(op[0], 0)
+    for kind in ("attention", "fused"):
+        sel = [op for op in ops if op[1] == kind]
+        if not sel:
+            continue
+        ms = sum(sum(per_op[lab]) for lab in labels[kind]) / steps
+        tf = sum(op[3] for op in sel) / (ms * 1e-3) / 1e12
+        out[kind] = {"tflops": tf, "frac": tf / peaks["bf16_tflops"], "ms_per_step": ms,
+                     "per_launch_ms": {lab: statistics.mean(per_op[lab]) for lab in labels[kind]}}
+    if "permute" in labels:
+        ms = sum(sum(per_op[lab]) for lab in labels["permute"]) / steps
+        nbytes = sum(op[2] for op in ops if op[1] == "permute")
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        out["permute"] = {"gbs": gbs, "frac": gbs / peaks["hbm_gbs"], "bytes_per_step": nbytes,
+                          "ms_per_step": ms}
+    return out
+
+
+def run_e2e(torch, uly, w, ins, dev, stream, steps, warmup):
+    """The fused forward (unfused where fused does not apply) end to end through the public
+    API: every step copies its inputs host -> device from pinned memory and its output
+    device -> host, inside the timed region.  The copies run on their own streams with
+    NBUF device buffer sets, so the next steps' inputs and the previous steps' outputs move
+    while a step computes (as a training loop prefetches its next batches); the host link
+    carries both directions at once, and with three sets it always has a copy queued."""
+    P, b, s, hq, hkv, d = w["P"], w["b"], w["s"], w["h_q"], w["h_kv"], w["d"]
+    S = s // P
+    qs, ks, vs = ins
+    dt = qs[0].dtype
+    esz = qs[0].element_size()
+    fused = dt == torch.bfloat16 and S % 128 == 0 and P <= 16
+    causal = w["masks"][-1]
+    host_in = [[t.cpu().pin_memory() for t in src] for src in (qs, ks, vs)]
+    host_o = [torch.empty((b, S, hq, d), dtype=dt).pin_memory() for _ in range(P)]
     NBUF = 3
     dev_in = [[[torch.empty_like(t) for t in src] for src in (qs, ks, vs)] for _ in range(NBUF)]
-    dev_out = [[[torch.empty((b, S, hq, d), dtype=dt, device=dev) for _ in range(P)] for _ in variants]
-               for _ in range(NBUF)]
-    h2d = sum(t.numel() * esz for t in host_q + host_k + host_v)
-    d2h = sum(t.numel() * esz for ho in host_o for t in ho)
-    ws = [torch.empty(uly.ulysses_dist_attn_workspace_bytes(P, b, s, hq, hkv, d, dt, False),
-                      dtype=torch.uint8, device=dev) for _ in range(NBUF)]
+    dev_out = [[torch.empty((b, S, hq, d), dtype=dt, device=dev) for _ in range(P)] for _ in range(NBUF)]
+    ws = None if fused else [torch.empty(uly.ulysses_dist_attn_workspace_bytes(P, b, s, hq, hkv, d, dt, False),
+                                         dtype=torch.uint8, device=dev) for _ in range(NBUF)]
+    h2d = sum(t.numel() * esz for grp in host_in for t in grp)
+    d2h = sum(t.numel() * esz for t in host_o)
     s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
     ev_in = [torch.cuda.Event() for _ in range(NBUF)]       # inputs of buffer i have landed
     ev_done = [torch.cuda.Event() for _ in range(NBUF)]     # compute on buffer i has finished
     ev_copied = [torch.cuda.Event() for _ in range(NBUF)]   # outputs of buffer i are on the host
+    flat_host = [t for grp in host_in for t in grp]
 
     def upload(k):
         i = k % NBUF
         s_in.wait_event(ev_done[i])  # step k-NBUF has finished reading these inputs
         with torch.cuda.stream(s_in):
-            for src, dst in zip(host_q + host_k + host_v, [t for grp in dev_in[i] for t in grp]):
+            for src, dst in zip(flat_host, [t for grp in dev_in[i] for t in grp]):
                 dst.copy_(src, non_blocking=True)
         ev_in[i].record(s_in)
 
@@ -279,18 +295,16 @@ def run_gpu(args, rank, world):
         stream.wait_event(ev_in[i])
         stream.wait_event(ev_copied[i])  # step k-NBUF's outputs have left these buffers
         q_i, k_i, v_i = dev_in[i]
-        for n, (causal, fused) in enumerate(variants):
-            uly.ulysses_dist_attn_fwd(q_i, k_i, v_i, causal, fused=fused, out_seq=dev_out[i][n],
-                                      workspace=None if fused else ws[i], stream=stream)
+        uly.ulysses_dist_attn_fwd(q_i, k_i, v_i, causal, fused=fused, out_seq=dev_out[i],
+                                  workspace=None if fused else ws[i], stream=stream)
         ev_done[i].record(stream)
         s_out.wait_event(ev_done[i])
         with torch.cuda.stream(s_out):
-            for n in range(len(variants)):
-                for o, ho in zip(dev_out[i][n], host_o[n]):
-                    ho.copy_(o, non_blocking=True)
+            for o, ho in zip(dev_out[i], host_o):
+                ho.copy_(o, non_blocking=True)
         ev_copied[i].record(s_out)
 
-    def run_e2e(n_steps):
+    def run(n_steps):
         for i in range(NBUF):  # nothing is pending on any buffer
             ev_done[i].record(stream)
             ev_copied[i].record(stream)
@@ -302,48 +316,90 @@ def run_gpu(args, rank, world):
             compute_and_download(k)
         stream.wait_stream(s_out)  # the last outputs are on the host before the clock stops
 
-    run_e2e(max(1, args.warmup))
+    run(max(1, warmup))
     torch.cuda.synchronize(dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    run_e2e(args.steps)
+    run(steps)
     e1.record(stream)
     torch.cuda.synchronize(dev)
-    e2e_ms = e0.elapsed_time(e1)
+    if uly.ulysses_device_status(clear=True) != 0:
+        raise RuntimeError("a kernel's bounded wait gave up during the end-to-end steps")
+    fl = attn_flops(b, s, hq, d, causal)
+    del dev_in, dev_out, ws
+    return dict(e2e_ms=e0.elapsed_time(e1), step_flops=fl, h2d=h2d, d2h=d2h, host_in=host_in,
+                call="ulysses_dist_attn_fwd(fused=%d, causal=%d)" % (int(fused), int(causal)))
 
-    res = dict(total_ms=total_ms, e2e_ms=e2e_ms, attn_tflops=attn_tflops, perm_gbs=perm_gbs, clocks=clk,
-               per_op={k: statistics.mean(v) for k, v in per_op.items()}, step_flops=step_flops,
-               attn_launch_ms=statistics.mean(attn_launch_ms), h2d=h2d, d2h=d2h,
-               n_launches=len(ops) * args.steps)
+
+def run_gpu(args, rank, world):
+    import torch
+
+    import sequence_attention_seq_gb300 as uly
+    from sequence_attention_seq_gb300 import build as uly_build
+
+    if rank == 0 or not os.path.exists(uly.library_path()):
+        uly_build.build()
+    if world > 1:
+        torch.distributed.barrier()
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    peaks, _ = load_peaks()
+    w = WORKLOADS[args.workload]
+    ops, ins, fused_ok = forward_ops(uly, torch, w, dev, seed=rank)
+    clocks = ClockSampler(dev.index if dev.index is not None else 0)
+    total_ms, per_op, clk = time_ops(torch, uly, ops, args.steps, args.warmup, dev, stream, clocks, world)
+    res = dict(total_ms=total_ms, clocks=clk, per_op={k: statistics.mean(v) for k, v in per_op.items()},
+               step_flops=sum(op[3] for op in ops), n_launches=len(ops) * args.steps,
+               summary=summarize(ops, per_op, args.steps, peaks), fused_ok=fused_ok)
+    del ops
+    e2e = run_e2e(torch, uly, w, ins, dev, stream, args.steps, args.warmup)
+    res["e2e"] = e2e
+    del ins
+    torch.cuda.empty_cache()
+    res["extra"] = {}
+    if not args.no_extras:
+        for name, steps in EXTRAS.get(args.workload, ()):
+            wx = WORKLOADS[name]
+            ops_x, ins_x, _ = forward_ops(uly, torch, wx, dev, seed=rank)
+            ms_x, per_x, clk_x = time_ops(torch, uly, ops_x, steps, max(3, args.warmup), dev, stream,
+                                          ClockSampler(dev.index if dev.index is not None else 0), world)
+            sm = summarize(ops_x, per_x, steps, peaks)
+            sm.update({"workload": wx["name"], "steps": steps, "ms_per_step": ms_x / steps,
+                       "per_launch_ms": {k: statistics.mean(v) for k, v in per_x.items()}, "clocks": clk_x})
+            if name == "dit":
+                sm["permute"]["note"] = ("64 MiB tensors, smaller than the 129 MB L2: the output exchange reads O "
+                                         "just written by attention, partly from L2")
+            res["extra"][name] = sm
+            del ops_x, ins_x
+            torch.cuda.empty_cache()
     return res
 
 
 # -------------------------------------------------------------------- CPU oracle
-def oracle_sample(budget_s=12.0, seed=0):
-    """Times the fp64 oracle on a bounded sample of the workload: the exchanges at full size
-    and sampled attention rows (each row exact), until the time budget is spent."""
+def oracle_sample(w, ins, budget_s=12.0, seed=0, with_exchange=True):
+    """Times the fp64 oracle on a bounded sample of workload w (seq-layout CPU inputs
+    `ins`): one exchange at full size (Q, seq->head) and exact attention output rows drawn
+    at random, until the time budget is spent.  Returns the rates (attention: algorithmic
+    FLOP of the rows computed / their time)."""
     import random
 
-    import torch
-
     import oracle
-    from sequence_attention_seq_gb300.inputs import seq_shards_qkv
 
-    w = WORKLOAD
-    P, b, s, hq, hkv, d = w["P"], w["b"], w["s"], w["h_q"], w["h_kv"], w["d"]
-    qs, ks, vs = seq_shards_qkv(P, b, s, hq, hkv, d, torch.bfloat16, seed=seed)
-    t0 = time.perf_counter()
-    q_head = oracle.seq2head(qs)
-    oracle.seq2head(ks)
-    oracle.seq2head(vs)
-    oracle.head2seq(q_head)
-    t_perm = time.perf_counter() - t0
-    perm_bytes = 2 * 4 * b * s * hq * d * 2
-    rng = random.Random(seed)
-    flops, rows, t_attn = 0, 0, 0.0
+    qs, ks, vs = ins
+    P, b, s, hq, d = w["P"], w["b"], w["s"], w["h_q"], w["d"]
     S = s // P
+    t_perm, perm_bytes = None, 2 * b * s * hq * d * qs[0].element_size()
+    if with_exchange:
+        t0 = time.perf_counter()
+        oracle.seq2head(qs)
+        t_perm = time.perf_counter() - t0
+    rng = random.Random(seed)
+    flops, rows, t_attn, k = 0, 0, 0.0, 0
+    masks = w["masks"]
     while t_attn < budget_s:
-        causal = rows % 2 == 1
+        causal = masks[k % len(masks)]
+        k += 1
         smp = [(rng.randrange(P), rng.randrange(b), rng.randrange(S), rng.randrange(hq)) for _ in range(8)]
         t1 = time.perf_counter()
         oracle.dist_attn_rows(qs, ks, vs, causal, smp)
@@ -352,15 +408,17 @@ def oracle_sample(budget_s=12.0, seed=0):
             keys = (j * S + t + 1) if causal else s
             flops += 4 * d * keys
         rows += len(smp)
-    return dict(tflops=flops / t_attn / 1e12, rows=rows, t_attn=t_attn, perm_gbs=perm_bytes / t_perm / 1e9,
-                t_perm=t_perm)
+    return dict(tflops=flops / t_attn / 1e12, rows=rows, t_attn=t_attn,
+                perm_gbs=(perm_bytes / t_perm / 1e9) if t_perm else None, t_perm=t_perm)
 
 
-def cpu_baseline_obj(smp):
+def cpu_baseline_obj(w, smp):
+    ex = (f", plus the Q exchange (seq->head) at full size ({smp['perm_gbs']:.2f} GB/s)"
+          if smp["perm_gbs"] else "")
     return {"value": smp["tflops"], "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
-            "sample": (f"{smp['rows']} attention rows (exact fp64, mixed causal/non-causal) of the DiT workload in "
-                       f"{smp['t_attn']:.1f} s, plus the four exchanges at full size "
-                       f"({smp['perm_gbs']:.2f} GB/s); single thread of {os.cpu_count()} host cores")}
+            "sample": (f"{smp['rows']} exact fp64 attention output rows of the workload ({w['name']}), random "
+                       f"(rank, batch, token, head), in {smp['t_attn']:.1f} s, rate extrapolated from them{ex}; "
+                       f"single thread of {os.cpu_count()} host cores")}
 
 
 KERNEL_REGION_END = b"// ---------------------------------------------------------------- host side"
@@ -644,11 +702,13 @@ def run_usp(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default: a multi-second timed region for the chosen workload)")
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", default="dit", choices=sorted(WORKLOADS))
+    ap.add_argument("--no-extras", action="store_true", help="skip the extra workloads after the main line")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
     ap.add_argument("--permute-sweep", action="store_true",
                     help="measure the exchanges over the permute-only sweep instead of the forward")
     ap.add_argument("--backward", action="store_true",
@@ -658,6 +718,8 @@ def main():
     ap.add_argument("--overlap", action="store_true",
                     help="measure the unfused forward against the overlapped (chunked) forward")
     args = ap.parse_args()
+    if args.steps is None:
+        args.steps = DEFAULT_STEPS[args.workload]
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -681,24 +743,33 @@ def main():
     esz = 2 if w["dtype"] == "bf16" else 4
     io_bytes = (2 * w["h_q"] + 2 * w["h_kv"]) * w["b"] * w["s"] * w["d"] * esz
     config = {"workload": w["name"], "P": w["P"], "b": w["b"], "s": w["s"], "h_q": w["h_q"], "h_kv": w["h_kv"],
-              "d": w["d"], "l2": (f"inputs larger than L2 (Q+K+V+O = {io_bytes / 2**20:.0f} MiB > 129 MB); no flush"
-                                  if io_bytes > 129e6 else "inputs smaller than L2: latency-bound exactness case")}
+              "d": w["d"], "causal": list(w["masks"]),
+              "l2": (f"inputs larger than L2 (Q+K+V+O = {io_bytes / 2**20:.0f} MiB > 129 MB); no flush"
+                     if io_bytes > 129e6 else "inputs smaller than L2: latency-bound exactness case")}
 
     if args.impl == "reference":
         if rank != 0:
             return
+        import torch
+
+        from sequence_attention_seq_gb300.inputs import seq_shards_qkv
+
+        dt = torch.bfloat16 if w["dtype"] == "bf16" else torch.float32
+        ins = seq_shards_qkv(w["P"], w["b"], w["s"], w["h_q"], w["h_kv"], w["d"], dt, seed=0)
         steps = []
         for k in range(args.warmup + args.steps):
-            smp = oracle_sample(budget_s=2.0, seed=k)
+            smp = oracle_sample(w, ins, budget_s=2.0, seed=k, with_exchange=False)
             if k >= args.warmup:
                 steps.append(smp)
         v = sum(x["tflops"] for x in steps) / len(steps)
+        rows = sum(x["rows"] for x in steps)
         line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "TFLOP/s", "n_gpus": args.gpus,
                 "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "dtype": "f64",
-                "data": "synthetic", "config": config,
+                "data": "synthetic (seeded N(0,1), CPU generator)", "config": config,
                 "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
-                                 "sample": "per step: the four exchanges at full size and ~2 s of exact fp64 "
-                                           "attention rows of the DiT workload, single thread"},
+                                 "sample": (f"per step ~2 s of exact fp64 attention output rows of the workload "
+                                            f"({rows} rows over {args.steps} steps), rate extrapolated from them; "
+                                            f"single thread of {os.cpu_count()} host cores")},
                 "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
         print(json.dumps(line))
         return
@@ -708,43 +779,60 @@ def main():
     if world > 1:
         torch.distributed.init_process_group("nccl")
     res = run_gpu(args, rank, world)
-    total_ms, e2e_ms = reduce_max_over_ranks([res["total_ms"], res["e2e_ms"]], device="cuda")
+    total_ms, e2e_ms = reduce_max_over_ranks([res["total_ms"], res["e2e"]["e2e_ms"]], device="cuda")
     if rank != 0:
         torch.distributed.destroy_process_group()
         return
     peaks, peak_src = load_peaks()
+    summ = res["summary"]
     if w["dtype"] == "bf16":
-        kernel, bound, peak, peak_note = "attn_tc_kernel<%d> (all attention launches of the step)" % w["d"], \
-            "tensor", peaks["bf16_tflops"], f"{peak_src} (bf16 dense, burst)"
+        main_kind = "fused" if "fused" in summ else "attention"
+        kernel = ("attn_tc_kernel<%d>, fused launch (both exchanges in its tile addressing)" % w["d"]
+                  if main_kind == "fused" else "attn_tc_kernel<%d>, unfused launch (head layout)" % w["d"])
+        bound, peak, peak_note = "tensor", peaks["bf16_tflops"], f"{peak_src} (bf16 dense, burst)"
     else:  # fp32 FMA attention: plain ALU peak, 152 SMs x 128 FMA lanes x 2 flop x max SM clock
-        kernel, bound = "attn_fp32_kernel (all attention launches of the step)", "alu"
+        main_kind = "attention"
+        kernel, bound = "attn_fp32_kernel (attention launches of the step)", "alu"
         peak = 152 * 128 * 2 * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
         peak_note = "derived: 152 SMs x 128 fp32 FMA/clk x 2 flop x 2070 MHz"
-    traffic = measured_traffic(args.workload)
+    achieved = summ[main_kind]["tflops"]
+    traffic = measured_traffic(args.workload) if main_kind == "fused" else None
     value = job_throughput(res["step_flops"] * args.steps, world, total_ms) / 1e12
-    e2e_value = job_throughput(res["step_flops"] * args.steps, world, e2e_ms) / 1e12
+    e2e = res["e2e"]
+    e2e_value = job_throughput(e2e["step_flops"] * args.steps, world, e2e_ms) / 1e12
     cpu = None
-    if not args.no_cpu_baseline and world == 1 and args.workload == "dit":
-        cpu = cpu_baseline_obj(oracle_sample(budget_s=12.0))
+    if not args.no_cpu_baseline and world == 1:
+        cpu = cpu_baseline_obj(w, oracle_sample(w, e2e["host_in"], budget_s=12.0))
+    extra = {}
+    for name, sm in res["extra"].items():
+        ent = {"workload": sm["workload"], "steps": sm["steps"], "ms_per_step": sm["ms_per_step"],
+               "per_launch_ms": sm["per_launch_ms"], "clocks": sm["clocks"]}
+        for kind in ("fused", "attention", "permute"):
+            if kind in sm:
+                ent[kind] = sm[kind]
+        extra[name] = ent
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": w["dtype"], "data": f"synthetic (seeded N(0,1) {w['dtype']})",
+        "vs_baseline": None, "dtype": w["dtype"], "data": f"synthetic (seeded N(0,1) {w['dtype']}, CUDA generator)",
         "config": config,
-        "roofline": {"kernel": kernel, "bound": bound,
-                     "achieved": res["attn_tflops"], "peak": peak, "unit": "TFLOP/s",
-                     "frac": res["attn_tflops"] / peak,
-                     "frac_of_sustained": (res["attn_tflops"] / peaks["bf16_tflops_sustained"]
-                                           if bound == "tensor" else None),
-                     "peak_source": peak_note, "traffic": traffic},
-        "permute": {"achieved": res["perm_gbs"], "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                    "frac": res["perm_gbs"] / peaks["hbm_gbs"], "bytes": "read+write of all ranks' data"},
+        "roofline": {"kernel": kernel, "bound": bound, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak,
+                     "frac_of_sustained": (achieved / peaks["bf16_tflops_sustained"] if bound == "tensor" else None),
+                     "peak_source": peak_note, "traffic": traffic,
+                     "flops_per_launch": attn_flops(w["b"], w["s"], w["h_q"], w["d"], w["masks"][-1]),
+                     "launch_ms": summ[main_kind]["ms_per_step"] / max(1, len(w["masks"]))},
+        "attention_unfused": summ.get("attention") if main_kind == "fused" else None,
+        "permute": ({"achieved": summ["permute"]["gbs"], "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": summ["permute"]["frac"], "bytes_per_step": summ["permute"]["bytes_per_step"],
+                     "bytes": "read+write of all ranks' data"} if "permute" in summ else None),
         "per_launch_ms": res["per_op"],
-        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": res["h2d"],
-                "d2h_bytes_per_step": res["d2h"]},
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": e2e["h2d"],
+                "d2h_bytes_per_step": e2e["d2h"], "call": e2e["call"]},
         "gpu_launches": res["n_launches"] * world,
         "clocks": res["clocks"],
         "cpu_baseline": cpu,
+        "extra": extra,
     }
     print(json.dumps(line))
     if world > 1:
