@@ -243,10 +243,20 @@ uly_status ulysses_usp_attn_bwd(int Pu, int Pr, int b, int s, int h_q, int h_kv,
  * device memory inside the library, which every GPU that loads the library holds until
  * the process exits.  Calls needing more scratch than that
  * (ulysses_dist_attn_workspace_bytes(..., fused = 0) > ULYSSES_NOALLOC_SCRATCH_BYTES)
- * return ULY_ERR_INVALID_ARG without enqueuing work.  The first call on a device looks up
- * the array's device address (make it before any stream capture begins).  Every call
- * shares the array: calls whose work overlaps on the GPU (e.g. on two streams) race and
- * must be serialised by the caller.  Nothing is allocated, on the host or the device.
+ * return ULY_ERR_INVALID_ARG without enqueuing work.
+ * Set-up: the first call in each CUDA context of a device looks up the array's device
+ * address (make it before any stream capture begins).  Under CUDA's lazy module loading
+ * (the default) that lookup also loads the module holding the array and reserves its
+ * memory, so the first call returns ULY_ERR_CUDA if the device has less than
+ * ULYSSES_NOALLOC_SCRATCH_BYTES free; make it early.  The address is cached per context,
+ * so a cudaDeviceReset (which gives the device a new context and a new array) is handled
+ * by a fresh lookup on the next call.
+ * Every call shares the array and finds the previous call's contents there; the forward
+ * writes each scratch byte before reading it, so nothing needs clearing.  Calls whose work
+ * overlaps on the GPU (e.g. on two streams) race on it and must be serialised by the caller.
+ * No cudaMalloc, cudaFree or other allocating routine is called, and the library's own code
+ * makes no host heap allocation on this path (the CUDA runtime's internal bookkeeping is
+ * outside its control).
  */
 #define ULYSSES_NOALLOC_SCRATCH_BYTES (64ull << 20)
 uly_status ulysses_dist_attn_fwd_noalloc(int P, int b, int s, int h_q, int h_kv, int d, uly_dtype dtype,

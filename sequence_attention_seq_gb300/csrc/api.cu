@@ -1,11 +1,11 @@
 // C ABI of the Ulysses forward (declared in include/ulysses.h): argument validation, the
 // composition of the three stages, and dispatch to the kernels.  Nothing here allocates
-// device memory; every argument error is reported before any work is enqueued.
-#include <algorithm>
+// device memory, and nothing allocates on the host heap either: argument records live on
+// the stack and the overlap checks use fixed-capacity range sets.  Every argument error is
+// reported before any work is enqueued.
 #include <cstdint>
 #include <cstring>
-#include <utility>
-#include <vector>
+#include <initializer_list>
 
 #include "../../include/ulysses.h"
 #include "internal.h"
@@ -23,30 +23,57 @@ struct Range {
     uintptr_t lo, hi;  // [lo, hi)
 };
 
+// A fixed-capacity set of byte ranges (at most six per-rank buffer lists of kMaxRanks).
+struct RangeSet {
+    static constexpr int kCap = 6 * kMaxRanks;
+    Range v[kCap];
+    int n = 0;
+    bool push(Range r) {
+        if (n >= kCap) return false;
+        v[n++] = r;
+        return true;
+    }
+    bool append(const RangeSet& o) {
+        for (int i = 0; i < o.n; ++i)
+            if (!push(o.v[i])) return false;
+        return true;
+    }
+};
+
+RangeSet one_range(const void* p, uint64_t bytes) {
+    RangeSet r;
+    r.push({reinterpret_cast<uintptr_t>(p), reinterpret_cast<uintptr_t>(p) + (uintptr_t)bytes});
+    return r;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Non-null, 16-byte aligned pointers; collects their byte ranges.
-bool collect(const void* const* ptrs, int P, uint64_t bytes, std::vector<Range>& out) {
+bool collect(const void* const* ptrs, int P, uint64_t bytes, RangeSet& out) {
     if (!ptrs) return false;
     for (int i = 0; i < P; ++i) {
         if (!ptrs[i] || !aligned16(ptrs[i])) return false;
         const uintptr_t lo = reinterpret_cast<uintptr_t>(ptrs[i]);
-        out.push_back({lo, lo + (uintptr_t)bytes});
+        if (!out.push({lo, lo + (uintptr_t)bytes})) return false;
     }
     return true;
 }
 
-bool overlaps(const std::vector<Range>& a, const std::vector<Range>& b) {
-    for (const Range& x : a)
-        for (const Range& y : b)
+bool overlaps(const RangeSet& a, const RangeSet& b) {
+    for (int i = 0; i < a.n; ++i)
+        for (int k = 0; k < b.n; ++k) {
+            const Range& x = a.v[i];
+            const Range& y = b.v[k];
             if (x.lo < y.hi && y.lo < x.hi && x.hi > x.lo && y.hi > y.lo) return true;
+        }
     return false;
 }
 
-bool self_overlap(const std::vector<Range>& a) {
-    for (size_t i = 0; i < a.size(); ++i)
-        for (size_t k = i + 1; k < a.size(); ++k)
-            if (a[i].lo < a[k].hi && a[k].lo < a[i].hi && a[i].hi > a[i].lo && a[k].hi > a[k].lo) return true;
+bool self_overlap(const RangeSet& a) {
+    for (int i = 0; i < a.n; ++i)
+        for (int k = i + 1; k < a.n; ++k)
+            if (a.v[i].lo < a.v[k].hi && a.v[k].lo < a.v[i].hi && a.v[i].hi > a.v[i].lo && a.v[k].hi > a.v[k].lo)
+                return true;
     return false;
 }
 
@@ -102,7 +129,7 @@ uint64_t row_array_bytes(int P, int b, int s, int hq) {
     return round256((uint64_t)b * (hq / P) * (((uint64_t)s + 127) / 128 * 128) * 4);
 }
 
-bool collect_f(const float* const* ptrs, int P, uint64_t bytes, std::vector<Range>& out) {
+bool collect_f(const float* const* ptrs, int P, uint64_t bytes, RangeSet& out) {
     return collect(reinterpret_cast<const void* const*>(ptrs), P, bytes, out);
 }
 
@@ -115,7 +142,7 @@ uly_status exchange(int direction, int P, int b, int s, int h, int d, uly_dtype 
     uly_status st = check_exchange_shape(P, b, s, h, d, dt);
     if (st != ULY_OK) return st;
     const uint64_t bytes = (uint64_t)b * (s / P) * h * d * elem_bytes(dt);  // equal on both sides
-    std::vector<Range> ri, ro;
+    RangeSet ri, ro;
     if (!collect(in, P, bytes, ri) || !collect(reinterpret_cast<const void* const*>(out), P, bytes, ro))
         return ULY_ERR_INVALID_ARG;
     if (overlaps(ri, ro) || self_overlap(ro)) return ULY_ERR_INVALID_ARG;
@@ -153,7 +180,7 @@ uly_status local_attention(int P, int b, int s, int h_q, int h_kv, int d, uly_dt
     const int e = elem_bytes(dtype);
     const uint64_t qb = (uint64_t)b * s * (h_q / P) * d * e,
                    kb = (uint64_t)b * s * uly::kv_heads_per_rank(P, h_kv) * d * e;
-    std::vector<Range> rq, rk, rv, ro, rl;
+    RangeSet rq, rk, rv, ro, rl;
     if (!collect(q_head, P, qb, rq) || !collect(k_head, P, kb, rk) || !collect(v_head, P, kb, rv) ||
         !collect(reinterpret_cast<const void* const*>(o_head), P, qb, ro))
         return ULY_ERR_INVALID_ARG;
@@ -177,14 +204,27 @@ uly_status local_attention(int P, int b, int s, int h_q, int h_kv, int d, uly_dt
 
 // Pointers of one head-layout scratch set inside a workspace: per rank, in this order,
 // the arrays whose per-rank sizes are listed in `sizes` (each 256-byte aligned).
+struct SizeList {
+    static constexpr int kCap = 16;
+    uint64_t v[kCap];
+    int n = 0;
+    SizeList() = default;
+    SizeList(std::initializer_list<uint64_t> xs) {
+        for (uint64_t x : xs) push(x);
+    }
+    void push(uint64_t x) {
+        if (n < kCap) v[n++] = x;
+    }
+};
+
 struct Carve {
     uint8_t* base;
     uint64_t per_rank;
-    std::vector<uint64_t> offs;
-    Carve(void* ws, const std::vector<uint64_t>& sizes) : base(static_cast<uint8_t*>(ws)), per_rank(0) {
-        for (uint64_t x : sizes) {
-            offs.push_back(per_rank);
-            per_rank += round256(x);
+    uint64_t offs[SizeList::kCap];
+    Carve(void* ws, const SizeList& sizes) : base(static_cast<uint8_t*>(ws)), per_rank(0) {
+        for (int i = 0; i < sizes.n; ++i) {
+            offs[i] = per_rank;
+            per_rank += round256(sizes.v[i]);
         }
     }
     void* at(int r, int k) const { return base + (uint64_t)r * per_rank + offs[k]; }
@@ -192,15 +232,15 @@ struct Carve {
 
 // Workspace of the backward: per rank the two fp32 row arrays (lse2, D), and for the
 // unfused distributed backward the head-layout Q, K, V, dO, dQ, dK, dV.
-std::vector<uint64_t> bwd_sizes(int P, int b, int s, int hq, int hkv, int d, int dist) {
+SizeList bwd_sizes(int P, int b, int s, int hq, int hkv, int d, int dist) {
     const uint64_t ra = row_array_bytes(P, b, s, hq);
-    std::vector<uint64_t> v{ra, ra};
+    SizeList v{ra, ra};
     if (dist == 1) {
         const uint64_t qb = (uint64_t)b * s * (hq / P) * d * 2,
                        kb = (uint64_t)b * s * uly::kv_heads_per_rank(P, hkv) * d * 2;
         // replicated K/V heads: each rank's dK/dV is an fp32 partial sum
         const uint64_t gb = uly::kv_replication(P, hkv) > 1 ? 2 * kb : kb;
-        for (uint64_t x : {qb, kb, kb, qb, qb, gb, gb}) v.push_back(x);
+        for (uint64_t x : {qb, kb, kb, qb, qb, gb, gb}) v.push(x);
     }
     return v;
 }
@@ -237,12 +277,12 @@ uly_status dist_attn_fwd(int P, int b, int s, int h_q, int h_kv, int d, uly_dtyp
     const int e = elem_bytes(dtype);
     const int S = s / P;
     const uint64_t qsb = (uint64_t)b * S * h_q * d * e, ksb = (uint64_t)b * S * h_kv * d * e;
-    std::vector<Range> rq, rk, rv, ro;
+    RangeSet rq, rk, rv, ro;
     if (!collect(q_seq, P, qsb, rq) || !collect(k_seq, P, ksb, rk) || !collect(v_seq, P, ksb, rv) ||
         !collect(reinterpret_cast<const void* const*>(o_seq), P, qsb, ro))
         return ULY_ERR_INVALID_ARG;
     if (overlaps(ro, rq) || overlaps(ro, rk) || overlaps(ro, rv) || self_overlap(ro)) return ULY_ERR_INVALID_ARG;
-    std::vector<Range> rl;
+    RangeSet rl;
     if (lse) {
         if (!collect_f(lse, P, (uint64_t)b * (h_q / P) * s * 4, rl)) return ULY_ERR_INVALID_ARG;
         if (self_overlap(rl) || overlaps(rl, rq) || overlaps(rl, rk) || overlaps(rl, rv) || overlaps(rl, ro))
@@ -266,7 +306,7 @@ uly_status dist_attn_fwd(int P, int b, int s, int h_q, int h_kv, int d, uly_dtyp
     const size_t need = dist_workspace_bytes(P, b, s, h_q, h_kv, d, dtype, 0);
     if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < need)
         return ULY_ERR_INVALID_ARG;
-    std::vector<Range> rw{{reinterpret_cast<uintptr_t>(workspace), reinterpret_cast<uintptr_t>(workspace) + need}};
+    const RangeSet rw = one_range(workspace, need);
     if (overlaps(rw, rq) || overlaps(rw, rk) || overlaps(rw, rv) || overlaps(rw, ro) || overlaps(rw, rl))
         return ULY_ERR_INVALID_ARG;
 
@@ -374,7 +414,8 @@ size_t ulysses_attn_bwd_workspace_bytes(int P, int b, int s, int h_q, int h_kv, 
                  check_kv_exchange_shape(P, b, s, h_kv, d, dtype) != ULY_OK))
         return 0;
     uint64_t per_rank = 0;
-    for (uint64_t x : bwd_sizes(P, b, s, h_q, h_kv, d, dist && !fused ? 1 : 0)) per_rank += round256(x);
+    const SizeList sizes = bwd_sizes(P, b, s, h_q, h_kv, d, dist && !fused ? 1 : 0);
+    for (int i = 0; i < sizes.n; ++i) per_rank += round256(sizes.v[i]);
     return (size_t)(per_rank * P);
 }
 
@@ -388,7 +429,7 @@ uly_status ulysses_local_attention_bwd(int P, int b, int s, int h_q, int h_kv, i
     if (st != ULY_OK) return st;
     const uint64_t qb = (uint64_t)b * s * (h_q / P) * d * 2,
                    kb = (uint64_t)b * s * uly::kv_heads_per_rank(P, h_kv) * d * 2;
-    std::vector<Range> in, rdq, rdk, rdv;
+    RangeSet in, rdq, rdk, rdv;
     if (!collect(q_head, P, qb, in) || !collect(k_head, P, kb, in) || !collect(v_head, P, kb, in) ||
         !collect(o_head, P, qb, in) || !collect(do_head, P, qb, in) ||
         !collect_f(lse, P, (uint64_t)b * (h_q / P) * s * 4, in) ||
@@ -396,16 +437,16 @@ uly_status ulysses_local_attention_bwd(int P, int b, int s, int h_q, int h_kv, i
         !collect(reinterpret_cast<const void* const*>(dk_head), P, kb, rdk) ||
         !collect(reinterpret_cast<const void* const*>(dv_head), P, kb, rdv))
         return ULY_ERR_INVALID_ARG;
-    std::vector<Range> outs(rdq);
-    outs.insert(outs.end(), rdk.begin(), rdk.end());
-    outs.insert(outs.end(), rdv.begin(), rdv.end());
+    RangeSet outs;
+    if (!outs.append(rdq) || !outs.append(rdk) || !outs.append(rdv)) return ULY_ERR_INVALID_ARG;
     if (self_overlap(outs) || overlaps(outs, in)) return ULY_ERR_INVALID_ARG;
     const size_t need = ulysses_attn_bwd_workspace_bytes(P, b, s, h_q, h_kv, d, dtype, 0, 0);
     if (!workspace_ok(workspace, workspace_bytes, need)) return ULY_ERR_INVALID_ARG;
-    std::vector<Range> rw{{reinterpret_cast<uintptr_t>(workspace), reinterpret_cast<uintptr_t>(workspace) + need}};
+    const RangeSet rw = one_range(workspace, need);
     if (overlaps(rw, in) || overlaps(rw, outs)) return ULY_ERR_INVALID_ARG;
     const Carve ws(workspace, bwd_sizes(P, b, s, h_q, h_kv, d, 0));
-    uly::BwdPtrs* p = new uly::BwdPtrs;
+    uly::BwdPtrs p_rec;
+    uly::BwdPtrs* p = &p_rec;
     memset(p, 0, sizeof(uly::BwdPtrs));
     for (int r = 0; r < P; ++r) {
         p->q[r] = q_head[r];
@@ -423,7 +464,6 @@ uly_status ulysses_local_attention_bwd(int P, int b, int s, int h_q, int h_kv, i
     }
     p->od_seq_layout = 0;
     st = run_backward(P, b, s, h_q, h_kv, d, causal, 0, *p, stream);
-    delete p;
     return st;
 }
 
@@ -440,7 +480,7 @@ uly_status ulysses_dist_attn_bwd(int P, int b, int s, int h_q, int h_kv, int d, 
     if (st != ULY_OK) return st;
     const int S = s / P;
     const uint64_t qsb = (uint64_t)b * S * h_q * d * 2, ksb = (uint64_t)b * S * h_kv * d * 2;
-    std::vector<Range> in, rdq, rdk, rdv;
+    RangeSet in, rdq, rdk, rdv;
     if (!collect(q_seq, P, qsb, in) || !collect(k_seq, P, ksb, in) || !collect(v_seq, P, ksb, in) ||
         !collect(o_seq, P, qsb, in) || !collect(do_seq, P, qsb, in) ||
         !collect_f(lse, P, (uint64_t)b * (h_q / P) * s * 4, in) ||
@@ -448,20 +488,20 @@ uly_status ulysses_dist_attn_bwd(int P, int b, int s, int h_q, int h_kv, int d, 
         !collect(reinterpret_cast<const void* const*>(dk_seq), P, ksb, rdk) ||
         !collect(reinterpret_cast<const void* const*>(dv_seq), P, ksb, rdv))
         return ULY_ERR_INVALID_ARG;
-    std::vector<Range> outs(rdq);
-    outs.insert(outs.end(), rdk.begin(), rdk.end());
-    outs.insert(outs.end(), rdv.begin(), rdv.end());
+    RangeSet outs;
+    if (!outs.append(rdq) || !outs.append(rdk) || !outs.append(rdv)) return ULY_ERR_INVALID_ARG;
     if (self_overlap(outs) || overlaps(outs, in)) return ULY_ERR_INVALID_ARG;
     if (fused && (P > 16 || S % 128 != 0)) return ULY_ERR_UNSUPPORTED;
     const size_t need = ulysses_attn_bwd_workspace_bytes(P, b, s, h_q, h_kv, d, dtype, 1, fused);
     if (!workspace_ok(workspace, workspace_bytes, need)) return ULY_ERR_INVALID_ARG;
-    std::vector<Range> rw{{reinterpret_cast<uintptr_t>(workspace), reinterpret_cast<uintptr_t>(workspace) + need}};
+    const RangeSet rw = one_range(workspace, need);
     if (overlaps(rw, in) || overlaps(rw, outs)) return ULY_ERR_INVALID_ARG;
     if (fused) {
         // one launch chain: statistics, then the two kernels read Q/K/V/dO from the seq-layout
         // buffers and write dQ/dK/dV into them through their tile addressing
         const Carve ws(workspace, bwd_sizes(P, b, s, h_q, h_kv, d, 0));
-        uly::BwdPtrs* p = new uly::BwdPtrs;
+        uly::BwdPtrs p_rec;
+    uly::BwdPtrs* p = &p_rec;
         memset(p, 0, sizeof(uly::BwdPtrs));
         for (int r = 0; r < P; ++r) {
             p->q[r] = q_seq[r];
@@ -479,13 +519,13 @@ uly_status ulysses_dist_attn_bwd(int P, int b, int s, int h_q, int h_kv, int d, 
         }
         p->od_seq_layout = 1;
         st = run_backward(P, b, s, h_q, h_kv, d, causal, 1, *p, stream);
-        delete p;
         return st;
     }
     const Carve ws(workspace, bwd_sizes(P, b, s, h_q, h_kv, d, 1));
     enum { LSE2, DSUM, QH, KH, VH, DOH, DQH, DKH, DVH };
     // (1) all-to-all #1 on Q, K, V and dO (the backward of all-to-all #2 is all-to-all #1)
-    uly::PermuteTensor* t = new uly::PermuteTensor[4];
+    uly::PermuteTensor t_rec[4];
+    uly::PermuteTensor* t = t_rec;
     memset(t, 0, 4 * sizeof(uly::PermuteTensor));
     const void* const* srcs[4] = {q_seq, k_seq, v_seq, do_seq};
     const int dsts[4] = {QH, KH, VH, DOH};
@@ -498,10 +538,10 @@ uly_status ulysses_dist_attn_bwd(int P, int b, int s, int h_q, int h_kv, int d, 
         if (k == 1 || k == 2) t[k].rep = uly::kv_replication(P, h_kv);
     }
     cudaError_t ce = uly::launch_permute(0, P, b, s, d, 2, t, 4, stream);
-    delete[] t;
     if (ce != cudaSuccess) return ULY_ERR_CUDA;
     // (2) local backward of every rank; D straight from the seq-layout O and dO
-    uly::BwdPtrs* p = new uly::BwdPtrs;
+    uly::BwdPtrs p_rec;
+    uly::BwdPtrs* p = &p_rec;
     memset(p, 0, sizeof(uly::BwdPtrs));
     for (int r = 0; r < P; ++r) {
         p->q[r] = ws.at(r, QH);
@@ -520,14 +560,12 @@ uly_status ulysses_dist_attn_bwd(int P, int b, int s, int h_q, int h_kv, int d, 
     p->od_seq_layout = 1;
     p->kv_grad_f32 = uly::kv_replication(P, h_kv) > 1 ? 1 : 0;
     st = run_backward(P, b, s, h_q, h_kv, d, causal, 0, *p, stream);
-    delete p;
     if (st != ULY_OK) return st;
     // (3) all-to-all #2 on dQ, dK, dV (the backward of all-to-all #1).  Replicated K/V heads:
     //     every replica holds the gradient from its own query heads, and the backward of the
     //     copy is their sum
     const int kv_rep = uly::kv_replication(P, h_kv);
     const int n_plain = kv_rep > 1 ? 1 : 3;
-    t = new uly::PermuteTensor[3];
     memset(t, 0, 3 * sizeof(uly::PermuteTensor));
     void* const* dsts2[3] = {dq_seq, dk_seq, dv_seq};
     const int srcs2[3] = {DQH, DKH, DVH};
@@ -541,7 +579,6 @@ uly_status ulysses_dist_attn_bwd(int P, int b, int s, int h_q, int h_kv, int d, 
     ce = uly::launch_permute(1, P, b, s, d, 2, t, n_plain, stream);
     for (int k = 1; k < 3 && kv_rep > 1 && ce == cudaSuccess; ++k)
         ce = uly::launch_kv_grad_sum(P, kv_rep, b, s, h_kv, d, t[k].src, t[k].dst, stream);
-    delete[] t;
     return ce == cudaSuccess ? ULY_OK : ULY_ERR_CUDA;
 }
 
@@ -604,14 +641,14 @@ uly_status ulysses_dist_attn_fwd_overlap(int P, int b, int s, int h_q, int h_kv,
     const int e = elem_bytes(dtype);
     const int S = s / P;
     const uint64_t qsb = (uint64_t)b * S * h_q * d * e, ksb = (uint64_t)b * S * h_kv * d * e;
-    std::vector<Range> rq, rk, rv, ro;
+    RangeSet rq, rk, rv, ro;
     if (!collect(q_seq, P, qsb, rq) || !collect(k_seq, P, ksb, rk) || !collect(v_seq, P, ksb, rv) ||
         !collect(reinterpret_cast<const void* const*>(o_seq), P, qsb, ro))
         return ULY_ERR_INVALID_ARG;
     if (overlaps(ro, rq) || overlaps(ro, rk) || overlaps(ro, rv) || self_overlap(ro)) return ULY_ERR_INVALID_ARG;
     const size_t need = ulysses_dist_attn_overlap_workspace_bytes(P, b, s, h_q, h_kv, d, dtype, n_chunks);
     if (!workspace_ok(workspace, workspace_bytes, need)) return ULY_ERR_INVALID_ARG;
-    std::vector<Range> rw{{reinterpret_cast<uintptr_t>(workspace), reinterpret_cast<uintptr_t>(workspace) + need}};
+    const RangeSet rw = one_range(workspace, need);
     if (overlaps(rw, rq) || overlaps(rw, rk) || overlaps(rw, rv) || overlaps(rw, ro)) return ULY_ERR_INVALID_ARG;
 
     // workspace: [chunk][rank] head-layout Q and O of the chunk's query heads, then
@@ -624,23 +661,24 @@ uly_status ulysses_dist_attn_fwd_overlap(int P, int b, int s, int h_q, int h_kv,
         return k == 0 || k == 3 ? wq.at(c * P + r, k == 0 ? 0 : 1) : wkv.at(pl.kv_of(c) * P + r, k - 1);
     };
 
-    std::vector<cudaEvent_t> ev;
+    cudaEvent_t ev[2 * kMaxChunks + 2];
+    int n_ev = 0;
     auto cleanup = [&]() {
-        for (cudaEvent_t x : ev) cudaEventDestroy(x);
+        for (int i = 0; i < n_ev; ++i) cudaEventDestroy(ev[i]);
     };
     for (int i = 0; i < 2 * nc + 2; ++i) {
-        cudaEvent_t x;
-        if (cudaEventCreateWithFlags(&x, cudaEventDisableTiming) != cudaSuccess) {
+        if (cudaEventCreateWithFlags(&ev[n_ev], cudaEventDisableTiming) != cudaSuccess) {
             cleanup();
             return ULY_ERR_CUDA;
         }
-        ev.push_back(x);
+        ++n_ev;
     }
     cudaEvent_t ev_start = ev[0], ev_done = ev[1];
     auto ev_in = [&](int c) { return ev[2 + c]; };
     auto ev_attn = [&](int c) { return ev[2 + nc + c]; };
 
-    uly::PermuteTensor* t = new uly::PermuteTensor[3];
+    uly::PermuteTensor t_rec[3];
+    uly::PermuteTensor* t = t_rec;
     auto exchange_in = [&](int c) {  // all-to-all #1 for chunk c's query heads, and its K/V heads
         memset(t, 0, 3 * sizeof(uly::PermuteTensor));  // unless an earlier chunk exchanged them
         const void* const* src[3] = {q_seq, k_seq, v_seq};
@@ -668,7 +706,8 @@ uly_status ulysses_dist_attn_fwd_overlap(int P, int b, int s, int h_q, int h_kv,
         t[0].hoff = c * Hc;
         return uly::launch_permute(1, P, b, s, d, e, t, 1, side_stream);
     };
-    uly::AttnPtrs* head = new uly::AttnPtrs;
+    uly::AttnPtrs head_rec;
+    uly::AttnPtrs* head = &head_rec;
     bool ok = cudaEventRecord(ev_start, stream) == cudaSuccess &&
               cudaStreamWaitEvent(side_stream, ev_start, 0) == cudaSuccess;
     for (int c = 0; c < 2 && c < nc && ok; ++c)
@@ -696,8 +735,6 @@ uly_status ulysses_dist_attn_fwd_overlap(int P, int b, int s, int h_q, int h_kv,
     }
     ok = ok && cudaEventRecord(ev_done, side_stream) == cudaSuccess &&
          cudaStreamWaitEvent(stream, ev_done, 0) == cudaSuccess;
-    delete head;
-    delete[] t;
     cleanup();  // destroying a recorded event is legal: its resources go once the work completes
     if (!ok) return st != ULY_OK ? st : ULY_ERR_CUDA;
     return ULY_OK;
@@ -735,12 +772,12 @@ uly_status usp_attn_fwd(int Pu, int Pr, int b, int s, int h_q, int h_kv, int d, 
     if (dtype != ULY_BF16 || P > 16 || L % 128 != 0) return ULY_ERR_UNSUPPORTED;
     const int Hk = uly::kv_heads_per_rank(Pu, h_kv), kv_rep = uly::kv_replication(Pu, h_kv);
     const uint64_t qsb = (uint64_t)b * S * h_q * d * 2, ksb = (uint64_t)b * S * h_kv * d * 2;
-    std::vector<Range> rq, rk, rv, ro;
+    RangeSet rq, rk, rv, ro;
     if (!collect(q_seq, P, qsb, rq) || !collect(k_seq, P, ksb, rk) || !collect(v_seq, P, ksb, rv) ||
         !collect(reinterpret_cast<const void* const*>(o_seq), P, qsb, ro))
         return ULY_ERR_INVALID_ARG;
     if (overlaps(ro, rq) || overlaps(ro, rk) || overlaps(ro, rv) || self_overlap(ro)) return ULY_ERR_INVALID_ARG;
-    std::vector<Range> rl;
+    RangeSet rl;
     if (lse) {
         if (!collect_f(lse, Pu, (uint64_t)b * (h_q / Pu) * s * 4, rl)) return ULY_ERR_INVALID_ARG;
         if (self_overlap(rl) || overlaps(rl, rq) || overlaps(rl, rk) || overlaps(rl, rv) || overlaps(rl, ro))
@@ -748,14 +785,15 @@ uly_status usp_attn_fwd(int Pu, int Pr, int b, int s, int h_q, int h_kv, int d, 
     }
     const size_t need = ulysses_usp_workspace_bytes(Pu, Pr, b, s, h_q, h_kv, d, dtype);
     if (!workspace_ok(workspace, workspace_bytes, need)) return ULY_ERR_INVALID_ARG;
-    std::vector<Range> rw{{reinterpret_cast<uintptr_t>(workspace), reinterpret_cast<uintptr_t>(workspace) + need}};
+    const RangeSet rw = one_range(workspace, need);
     if (overlaps(rw, rq) || overlaps(rw, rk) || overlaps(rw, rv) || overlaps(rw, ro) || overlaps(rw, rl))
         return ULY_ERR_INVALID_ARG;
 
     // workspace: per rank [Q | K | V | O] in head layout of its group: [b][s/Pr][h/Pu][d]
     const Carve ws(workspace, {(uint64_t)b * L * (h_q / Pu) * d * 2, (uint64_t)b * L * Hk * d * 2,
                                (uint64_t)b * L * Hk * d * 2, (uint64_t)b * L * (h_q / Pu) * d * 2});
-    uly::PermuteTensor* t = new uly::PermuteTensor[3];
+    uly::PermuteTensor t_rec[3];
+    uly::PermuteTensor* t = t_rec;
     cudaError_t ce = cudaSuccess;
     // (1) all-to-all #1 inside every ring group of Pu consecutive ranks
     for (int g = 0; g < Pr && ce == cudaSuccess; ++g) {
@@ -773,7 +811,8 @@ uly_status usp_attn_fwd(int Pu, int Pr, int b, int s, int h_q, int h_kv, int d, 
     }
     // (2) attention over the whole sequence: the ring's K/V blocks are read from the buffers
     //     of the ranks that hold them
-    uly::AttnPtrs* head = new uly::AttnPtrs;
+    uly::AttnPtrs head_rec;
+    uly::AttnPtrs* head = &head_rec;
     memset(head, 0, sizeof(uly::AttnPtrs));
     for (int j = 0; j < P; ++j) {
         head->q[j] = ws.at(j, 0);
@@ -785,7 +824,6 @@ uly_status usp_attn_fwd(int Pu, int Pr, int b, int s, int h_q, int h_kv, int d, 
     int unsupported = 0;
     if (ce == cudaSuccess) ce = uly::launch_attention_tc_usp(Pu, Pr, b, s, h_q, h_kv, d, causal, *head, stream,
                                                              &unsupported);
-    delete head;
     // (3) all-to-all #2 inside every ring group
     for (int g = 0; g < Pr && ce == cudaSuccess && !unsupported; ++g) {
         memset(t, 0, sizeof(uly::PermuteTensor));
@@ -796,7 +834,6 @@ uly_status usp_attn_fwd(int Pu, int Pr, int b, int s, int h_q, int h_kv, int d, 
         t[0].h = h_q;
         ce = uly::launch_permute(1, Pu, b, L, d, 2, t, 1, stream);
     }
-    delete[] t;
     if (unsupported) return ULY_ERR_UNSUPPORTED;
     return ce == cudaSuccess ? ULY_OK : ULY_ERR_CUDA;
 }
@@ -852,7 +889,7 @@ uly_status ulysses_usp_attn_bwd(int Pu, int Pr, int b, int s, int h_q, int h_kv,
     if (P > 16 || L % 128 != 0) return ULY_ERR_UNSUPPORTED;
     const int Hk = uly::kv_heads_per_rank(Pu, h_kv), kv_rep = uly::kv_replication(Pu, h_kv);
     const uint64_t qsb = (uint64_t)b * S * h_q * d * 2, ksb = (uint64_t)b * S * h_kv * d * 2;
-    std::vector<Range> in, rdq, rdk, rdv;
+    RangeSet in, rdq, rdk, rdv;
     if (!collect(q_seq, P, qsb, in) || !collect(k_seq, P, ksb, in) || !collect(v_seq, P, ksb, in) ||
         !collect(o_seq, P, qsb, in) || !collect(do_seq, P, qsb, in) ||
         !collect_f(lse, Pu, (uint64_t)b * (h_q / Pu) * s * 4, in) ||
@@ -860,13 +897,12 @@ uly_status ulysses_usp_attn_bwd(int Pu, int Pr, int b, int s, int h_q, int h_kv,
         !collect(reinterpret_cast<const void* const*>(dk_seq), P, ksb, rdk) ||
         !collect(reinterpret_cast<const void* const*>(dv_seq), P, ksb, rdv))
         return ULY_ERR_INVALID_ARG;
-    std::vector<Range> outs(rdq);
-    outs.insert(outs.end(), rdk.begin(), rdk.end());
-    outs.insert(outs.end(), rdv.begin(), rdv.end());
+    RangeSet outs;
+    if (!outs.append(rdq) || !outs.append(rdk) || !outs.append(rdv)) return ULY_ERR_INVALID_ARG;
     if (self_overlap(outs) || overlaps(outs, in)) return ULY_ERR_INVALID_ARG;
     const size_t need = ulysses_usp_bwd_workspace_bytes(Pu, Pr, b, s, h_q, h_kv, d, dtype);
     if (!workspace_ok(workspace, workspace_bytes, need)) return ULY_ERR_INVALID_ARG;
-    std::vector<Range> rw{{reinterpret_cast<uintptr_t>(workspace), reinterpret_cast<uintptr_t>(workspace) + need}};
+    const RangeSet rw = one_range(workspace, need);
     if (overlaps(rw, in) || overlaps(rw, outs)) return ULY_ERR_INVALID_ARG;
 
     const uint64_t qb = (uint64_t)b * L * (h_q / Pu) * d * 2, kb = (uint64_t)b * L * Hk * d * 2;
@@ -876,7 +912,8 @@ uly_status ulysses_usp_attn_bwd(int Pu, int Pr, int b, int s, int h_q, int h_kv,
     const uint64_t ra = row_array_bytes(Pu, b, s, h_q);
     const Carve wr(static_cast<uint8_t*>(workspace) + ws.per_rank * P, {ra, ra});
     // (1) all-to-all #1 on Q, K, V and dO inside every ring group
-    uly::PermuteTensor* t = new uly::PermuteTensor[4];
+    uly::PermuteTensor t_rec[4];
+    uly::PermuteTensor* t = t_rec;
     cudaError_t ce = cudaSuccess;
     const void* const* srcs[4] = {q_seq, k_seq, v_seq, do_seq};
     const int dsts[4] = {QH, KH, VH, DOH};
@@ -892,10 +929,10 @@ uly_status ulysses_usp_attn_bwd(int Pu, int Pr, int b, int s, int h_q, int h_kv,
         }
         ce = uly::launch_permute(0, Pu, b, L, d, 2, t, 4, stream);
     }
-    delete[] t;
     if (ce != cudaSuccess) return ULY_ERR_CUDA;
     // (2) the attention backward over the whole sequence (statistics from the seq-layout O, dO)
-    uly::BwdPtrs* p = new uly::BwdPtrs;
+    uly::BwdPtrs p_rec;
+    uly::BwdPtrs* p = &p_rec;
     memset(p, 0, sizeof(uly::BwdPtrs));
     for (int j = 0; j < P; ++j) {
         p->q[j] = ws.at(j, QH);
@@ -917,14 +954,12 @@ uly_status ulysses_usp_attn_bwd(int Pu, int Pr, int b, int s, int h_q, int h_kv,
     p->kv_grad_f32 = kv_rep > 1 ? 1 : 0;
     int unsupported = 0;
     ce = uly::launch_attention_bwd_tc_usp(Pu, Pr, b, s, h_q, h_kv, d, causal, *p, stream, &unsupported);
-    delete p;
     if (unsupported) return ULY_ERR_UNSUPPORTED;
     if (ce != cudaSuccess) return ULY_ERR_CUDA;
     // (3) all-to-all #2 on dQ, dK, dV inside every ring group.  Replicated K/V heads: the
     //     group's replicas of a head hold the gradients from their own query heads, and the
     //     backward of the broadcast is their sum
     const int n_plain = kv_rep > 1 ? 1 : 3;
-    t = new uly::PermuteTensor[3];
     void* const* dsts2[3] = {dq_seq, dk_seq, dv_seq};
     const int srcs2[3] = {DQH, DKH, DVH};
     for (int g = 0; g < Pr && ce == cudaSuccess; ++g) {
@@ -940,7 +975,6 @@ uly_status ulysses_usp_attn_bwd(int Pu, int Pr, int b, int s, int h_q, int h_kv,
         for (int k = 1; k < 3 && kv_rep > 1 && ce == cudaSuccess; ++k)
             ce = uly::launch_kv_grad_sum(Pu, kv_rep, b, L, h_kv, d, t[k].src, t[k].dst, stream);
     }
-    delete[] t;
     return ce == cudaSuccess ? ULY_OK : ULY_ERR_CUDA;
 }
 

@@ -648,7 +648,8 @@ cudaError_t launch_attention_tc(int P, int b, int s, int h_q, int h_kv, int d, i
         *unsupported = 1;
         return cudaSuccess;
     }
-    TcParams* prm = new TcParams;
+    TcParams prm_rec;
+    TcParams* prm = &prm_rec;
     memset(prm, 0, sizeof(TcParams));
     prm->s = s;
     prm->map_stride = 1;
@@ -702,7 +703,6 @@ cudaError_t launch_attention_tc(int P, int b, int s, int h_q, int h_kv, int d, i
             err = d == 64 ? launch_d<64>(*prm, n_items, stream) : launch_d<128>(*prm, n_items, stream);
         }
     }
-    delete prm;
     return err;
 }
 
@@ -715,7 +715,8 @@ cudaError_t launch_attention_tc_usp(int Pu, int Pr, int b, int s, int h_q, int h
         return cudaSuccess;
     }
     const int Hq = h_q / Pu, Hk = kv_heads_per_rank(Pu, h_kv);  // 1: a replicated K/V head
-    TcParams* prm = new TcParams;
+    TcParams prm_rec;
+    TcParams* prm = &prm_rec;
     memset(prm, 0, sizeof(TcParams));
     prm->s = s;
     prm->rows_per_map = L;
@@ -742,7 +743,6 @@ cudaError_t launch_attention_tc_usp(int Pu, int Pr, int b, int s, int h_q, int h
         prm->band_units = band_units_for(s, d, Pu * b * Hk);
         err = d == 64 ? launch_d<64>(*prm, n_items, stream) : launch_d<128>(*prm, n_items, stream);
     }
-    delete prm;
     return err;
 }
 
@@ -755,7 +755,8 @@ namespace {
 cudaError_t launch_bwd_prep(int n_head_ranks, int n_seq_ranks, int b, int s, int h_q, int d, const BwdPtrs& ptrs,
                             cudaStream_t stream) {
     const int n_tiles = (s + 127) / 128;
-    PrepParams* pp = new PrepParams;
+    PrepParams pp_rec;
+    PrepParams* pp = &pp_rec;
     memset(pp, 0, sizeof(PrepParams));
     const int nb = ptrs.od_seq_layout ? n_seq_ranks : n_head_ranks;
     for (int r = 0; r < nb; ++r) {
@@ -782,7 +783,6 @@ cudaError_t launch_bwd_prep(int n_head_ranks, int n_seq_ranks, int b, int s, int
     const int gx = (pp->s_pad + per_block * kPrepRows - 1) / (per_block * kPrepRows);
     const int gy = pp->units < 65535 ? pp->units : 65535;
     bwd_prep_kernel<<<dim3((unsigned)gx, (unsigned)gy, 1), 256, 0, stream>>>(*pp);
-    delete pp;
     return cudaGetLastError();
 }
 
@@ -802,7 +802,8 @@ cudaError_t launch_attention_bwd_tc(int P, int b, int s, int h_q, int h_kv, int 
     if (err != cudaSuccess) return err;
     // (2) dK/dV and dQ: one launch pair over seq-layout buffers (fused), else up to kMaxMaps
     //     head ranks per launch pair
-    BwdParams* prm = new BwdParams;
+    BwdParams prm_rec;
+    BwdParams* prm = &prm_rec;
     memset(prm, 0, sizeof(BwdParams));
     prm->s = s;
     prm->s_pad = n_tiles * 128;
@@ -857,7 +858,6 @@ cudaError_t launch_attention_bwd_tc(int P, int b, int s, int h_q, int h_kv, int 
             err = d == 64 ? launch_bwd_d<64>(*prm, nr, stream) : launch_bwd_d<128>(*prm, nr, stream);
         }
     }
-    delete prm;
     return err;
 }
 
@@ -876,7 +876,8 @@ cudaError_t launch_attention_bwd_tc_usp(int Pu, int Pr, int b, int s, int h_q, i
     if (err != cudaSuccess) return err;
     // (2) dK/dV and dQ over the Pu units, every tile read from (written to) the buffer of the
     //     ring group that holds its tokens: the forward's two-level tile addressing
-    BwdParams* prm = new BwdParams;
+    BwdParams prm_rec;
+    BwdParams* prm = &prm_rec;
     memset(prm, 0, sizeof(BwdParams));
     prm->s = s;
     prm->s_pad = n_tiles * 128;
@@ -906,7 +907,6 @@ cudaError_t launch_attention_bwd_tc_usp(int Pu, int Pr, int b, int s, int h_q, i
         prm->dsum[u] = ptrs.dsum[u];
     }
     if (err == cudaSuccess) err = d == 64 ? launch_bwd_d<64>(*prm, Pu, stream) : launch_bwd_d<128>(*prm, Pu, stream);
-    delete prm;
     return err;
 }
 

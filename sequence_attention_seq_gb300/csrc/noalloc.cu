@@ -18,8 +18,19 @@
 // In host code `g_noalloc_scratch` is only a host-side stand-in for the device array, not
 // a device address; passing it to a kernel would fault or, where the GPU can reach host
 // memory, silently use the wrong memory.  The real address comes from
-// cudaGetSymbolAddress, taken once per device with that device current, on the first call
-// made on that device; make that first call before any stream capture begins.
+// cudaGetSymbolAddress, taken once per device (once per CUDA context of that device) with
+// that device current, on the first call made there; make that first call before any
+// stream capture begins.  The address is cached together with the identifier of the
+// context it belongs to: after cudaDeviceReset the device gets a new primary context (with
+// a new copy of the array), and the next call looks the address up again.  With CUDA's
+// lazy module loading (the default) the first lookup is also when the module holding the
+// array is loaded and its memory reserved, so that first call fails with ULY_ERR_CUDA if
+// the device has less than kNoAllocScratchBytes free.
+//
+// Nothing on this path allocates: no cudaMalloc or cudaFree, and no host heap allocation
+// in this library's code (the argument records and overlap checks live on the stack).
+#include <cuda.h>
+
 #include <mutex>
 
 #include "../../include/ulysses.h"
@@ -32,23 +43,59 @@ constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
-std::mutex g_scratch_mu;
-void* g_scratch_addr[kMaxDevices] = {};
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
 
-// Device address of the scratch array on the current device (set-up on first use).
+template <typename Fn>
+Fn driver_fn(const char* name) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion(name, &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+        return nullptr;
+    return reinterpret_cast<Fn>(f);
+}
+
+// Identifier of the calling thread's current context (0 if there is none yet).
+bool current_context_id(unsigned long long* id) {
+    static CtxGetCurrentFn get_current = driver_fn<CtxGetCurrentFn>("cuCtxGetCurrent");
+    static CtxGetIdFn get_id = driver_fn<CtxGetIdFn>("cuCtxGetId");
+    if (!get_current || !get_id) return false;
+    CUcontext ctx = nullptr;
+    if (get_current(&ctx) != CUDA_SUCCESS) return false;
+    *id = 0;
+    return !ctx || get_id(ctx, id) == CUDA_SUCCESS;
+}
+
+struct CachedAddress {
+    unsigned long long ctx_id;  // context the address belongs to (0: none cached)
+    void* addr;
+};
+
+std::mutex g_scratch_mu;
+CachedAddress g_scratch_addr[kMaxDevices] = {};
+
+// Device address of the scratch array in the current device's context (set-up on first
+// use in each context).
 cudaError_t scratch_address(void** out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (dev >= 0 && dev < kMaxDevices && g_scratch_addr[dev]) {
-        *out = g_scratch_addr[dev];
+    unsigned long long id = 0;
+    if (!current_context_id(&id)) return cudaErrorNotSupported;
+    CachedAddress& c = g_scratch_addr[dev];
+    if (id != 0 && c.ctx_id == id && c.addr) {
+        *out = c.addr;
         return cudaSuccess;
     }
     void* ptr = nullptr;
-    e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+    e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);  // initialises the context if needed
     if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < kMaxDevices) g_scratch_addr[dev] = ptr;
+    if (!current_context_id(&id) || id == 0) return cudaErrorNotSupported;
+    c.ctx_id = id;
+    c.addr = ptr;
     *out = ptr;
     return cudaSuccess;
 }
