@@ -1,6 +1,9 @@
 """The measured attention workloads at their full sizes, in the launch configuration the
 benchmark times: sampled output rows against the oracle's per-row evaluation (exact per
-row), and fused == unfused bit for bit over every output element."""
+row), and fused == unfused bit for bit over every output element.  Every query head is
+sampled at least once; Long's causal items run in bands of one head each, and its samples
+include every sampled head's first and last query tile (the last and the first item of
+that head's band)."""
 import random
 
 import pytest
@@ -15,9 +18,9 @@ pytestmark = pytest.mark.gpu
 
 CONFIGS = {
     # name: (P, b, s, hq, hkv, d, causal list, rows sampled)
-    "dit_mha": (4, 2, 4096, 32, 32, 128, (False, True), 48),
-    "gqa_causal": (8, 1, 32768, 32, 8, 128, (True,), 24),
-    "long_causal": (8, 1, 131072, 64, 64, 128, (True,), 12),
+    "dit_mha": (4, 2, 4096, 32, 32, 128, (False, True), 64),
+    "gqa_causal": (8, 1, 32768, 32, 8, 128, (True,), 128),
+    "long_causal": (8, 1, 131072, 64, 64, 128, (True,), 96),
 }
 
 
@@ -25,6 +28,11 @@ def _samples(P, b, S, hq, n, seed):
     rng = random.Random(seed)
     picks = set()
     edges = [0, 1, 127, 128, S // 2, S - 129, S - 1]
+    for h in range(hq):  # every head once, at a random token
+        picks.add((rng.randrange(P), rng.randrange(b), rng.randrange(S), h))
+    for h in rng.sample(range(hq), min(8, hq)):  # first and last query tile of some heads
+        picks.add((0, rng.randrange(b), rng.randrange(128), h))
+        picks.add((P - 1, rng.randrange(b), S - 1 - rng.randrange(128), h))
     while len(picks) < n:
         j = rng.randrange(P)
         t = rng.choice(edges) if rng.random() < 0.5 else rng.randrange(S)
