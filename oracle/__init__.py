@@ -66,6 +66,8 @@ def _load():
             lib.orc_usp_fwd.restype = i
             lib.orc_attention_bwd_rows.argtypes = [i, i, i, i, i, i, i, vp, vp, vp, vp, i, vp, i, vp, vp, vp, vp]
             lib.orc_attention_bwd_rows.restype = i
+            lib.orc_attention_bwd_magnitudes.argtypes = [i, i, i, i, i, i, i, vp, vp, vp, vp, vp, vp, vp]
+            lib.orc_attention_bwd_magnitudes.restype = i
             _lib = lib
     return _lib
 
@@ -181,6 +183,26 @@ def attention_bwd(q, k, v, dout, causal):
                                      k.data_ptr(), v.data_ptr(), dout.data_ptr(), dq.data_ptr(), dk.data_ptr(),
                                      dv.data_ptr()), "attention_bwd")
     return dq, dk, dv
+
+
+def attention_bwd_magnitudes(q, k, v, dout, causal):
+    """Per gradient element of one rank's local attention backward (head layout), the sum
+    of the absolute values of its terms, with every dS_ij widened by P_ij E_i (the
+    sensitivity of dS_ij to an output O known only to rounding accuracy): the magnitudes
+    (mq, mk, mv), float64, that bound the effect of rounding the terms."""
+    q, k, v, dout = _cpu(q), _cpu(k), _cpu(v), _cpu(dout)
+    if not (q.dtype == k.dtype == v.dtype == dout.dtype):
+        raise ValueError("q, k, v, dout must share a dtype")
+    b, s, hq, d = q.shape
+    hkv = k.shape[2]
+    mq = torch.empty((b, s, hq, d), dtype=torch.float64)
+    mk = torch.empty((b, s, hkv, d), dtype=torch.float64)
+    mv = torch.empty((b, s, hkv, d), dtype=torch.float64)
+    _check(_load().orc_attention_bwd_magnitudes(b, s, hq, hkv, d, int(bool(causal)), DTYPE_CODE[q.dtype],
+                                                q.data_ptr(), k.data_ptr(), v.data_ptr(), dout.data_ptr(),
+                                                mq.data_ptr(), mk.data_ptr(), mv.data_ptr()),
+           "attention_bwd_magnitudes")
+    return mq, mk, mv
 
 
 def dist_attn_bwd(q_seq, k_seq, v_seq, do_seq, causal):

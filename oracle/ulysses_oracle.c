@@ -618,3 +618,88 @@ int orc_attention_bwd_rows(int b, int s, int hq, int hkv, int d, int causal, int
     free(o);
     return ORC_OK;
 }
+
+/* ------------------------------------------------- magnitudes of the gradient terms */
+
+/*
+ * For every gradient element of the local attention backward, the sum of the absolute
+ * values of the terms that orc_attention_bwd adds up for it -- the quantity that bounds
+ * the effect of rounding those terms (each term rounded with relative error u moves the
+ * sum by at most u times this magnitude; the textbook error bound of a sum of rounded
+ * products).  With P_ij, dP_ij = dO_i . v_j, D_i = dO_i . O_i and dS_ij = P_ij (dP_ij - D_i)
+ * as in orc_attention_bwd ("02 · DeepSpeed-Ulysses", section 5: the ordinary attention
+ * backward), and
+ *   E_i = sum_c |dO_ic| (|O_ic| + sum_j P_ij |v_jc|),
+ * the bound on |D_i - D~_i| in units of u when every O_ic is known only to within
+ * u (|O_ic| + sum_j P_ij |v_jc|) -- an output formed from rounded weights P_ij and then
+ * rounded itself:
+ *   mq_ic = sum_j (|dS_ij| + P_ij E_i) |k_jc| / sqrt(d)
+ *   mk_jc = sum_hh sum_i (|dS_ij| + P_ij E_i) |q_ic| / sqrt(d)
+ *   mv_jc = sum_hh sum_i P_ij |dO_ic|
+ * (grouped heads: key rows sum over the query heads hh that read K/V head kvh, exactly as
+ * the gradients do).  Same layouts and arguments as orc_attention_bwd.
+ */
+int orc_attention_bwd_magnitudes(int b, int s, int hq, int hkv, int d, int causal, int dtype,
+                                 const void* q, const void* k, const void* v, const void* dout,
+                                 double* mq, double* mk, double* mv) {
+    if (b < 0 || s < 0 || hq < 1 || hkv < 1 || d < 1 || hq % hkv) return ORC_BAD_ARG;
+    int g = hq / hkv;
+    double scale = 1.0 / sqrt((double)d);
+    size_t nq = (size_t)b * s * hq * d, nk = (size_t)b * s * hkv * d;
+    for (size_t x = 0; x < nq; ++x) mq[x] = 0.0;
+    for (size_t x = 0; x < nk; ++x) { mk[x] = 0.0; mv[x] = 0.0; }
+    double* p = (double*)malloc(sizeof(double) * (s ? s : 1));
+    double* o = (double*)malloc(sizeof(double) * (d ? d : 1));
+    double* oa = (double*)malloc(sizeof(double) * (d ? d : 1));
+    if (!p || !o || !oa) { free(p); free(o); free(oa); return ORC_NO_MEMORY; }
+    for (int bb = 0; bb < b; ++bb)
+        for (int hh = 0; hh < hq; ++hh) {
+            int kh = hh / g;
+            for (int i = 0; i < s; ++i) {
+                int n = causal ? i + 1 : s;
+                size_t qo = (((size_t)bb * s + i) * hq + hh) * d;
+                double m = -INFINITY;
+                for (int j = 0; j < n; ++j) {
+                    size_t ko = (((size_t)bb * s + j) * hkv + kh) * d;
+                    double acc = 0.0;
+                    for (int c = 0; c < d; ++c) acc += load_elem(q, qo + c, dtype) * load_elem(k, ko + c, dtype);
+                    p[j] = acc * scale;
+                    if (p[j] > m) m = p[j];
+                }
+                double l = 0.0;
+                for (int j = 0; j < n; ++j) { p[j] = exp(p[j] - m); l += p[j]; }
+                for (int j = 0; j < n; ++j) p[j] /= l;
+                /* O_i and sum_j P_ij |v_j| */
+                for (int c = 0; c < d; ++c) { o[c] = 0.0; oa[c] = 0.0; }
+                for (int j = 0; j < n; ++j) {
+                    size_t vo = (((size_t)bb * s + j) * hkv + kh) * d;
+                    for (int c = 0; c < d; ++c) {
+                        double vv = load_elem(v, vo + c, dtype);
+                        o[c] += p[j] * vv;
+                        oa[c] += p[j] * fabs(vv);
+                    }
+                }
+                double Di = 0.0, Ei = 0.0;
+                for (int c = 0; c < d; ++c) {
+                    double g_c = load_elem(dout, qo + c, dtype);
+                    Di += g_c * o[c];
+                    Ei += fabs(g_c) * (fabs(o[c]) + oa[c]);
+                }
+                for (int j = 0; j < n; ++j) {
+                    size_t ko = (((size_t)bb * s + j) * hkv + kh) * d;
+                    double dp = 0.0;
+                    for (int c = 0; c < d; ++c) dp += load_elem(dout, qo + c, dtype) * load_elem(v, ko + c, dtype);
+                    double w = fabs(p[j] * (dp - Di)) + p[j] * Ei;
+                    for (int c = 0; c < d; ++c) {
+                        mv[ko + c] += p[j] * fabs(load_elem(dout, qo + c, dtype));
+                        mq[qo + c] += w * fabs(load_elem(k, ko + c, dtype)) * scale;
+                        mk[ko + c] += w * fabs(load_elem(q, qo + c, dtype)) * scale;
+                    }
+                }
+            }
+        }
+    free(p);
+    free(o);
+    free(oa);
+    return ORC_OK;
+}

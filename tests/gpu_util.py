@@ -48,22 +48,30 @@ def assert_close_grad(got, ref, what=""):
     return err.max().item(), err.mean().item()
 
 
-# Norm-wise bound: max error <= 2^-6 max|ref| and mean error <= 2^-8 mean|ref|.  Used where
-# the element-wise bound above does not apply:
+# Element-wise bound scaled by the magnitude of each gradient element's terms
+# (oracle.attention_bwd_magnitudes): |err| <= 1.5e-2 + 2^-7 |ref| + 2^-8 m.  Each term of a
+# gradient sum is rounded to bf16 (P and dS before their tile products; D is formed from
+# the bf16 output O), so the error of the sum is at most 2^-8 times the sum of the terms'
+# magnitudes -- the textbook bound for a sum of rounded products.  Used where the bound above
+# does not apply:
 # - saturated softmax inputs, where dS = P (dP - D) is a small difference of large terms;
 # - K/V heads shared by more than 4 query heads, where each dK/dV element sums many
-#   bf16-rounded dS (or P) terms of both signs.  Their rounding error scales with the sum
-#   of the terms' magnitudes, not with the (partly cancelled) result, so a few elements
-#   exceed the element-wise bound.  A float64 emulation of the kernel's roundings gives the
-#   same excess: 8 query heads per K/V head, 384 keys, ratio 1.01.
-def assert_normwise_grad(got, ref, what=""):
+#   bf16-rounded dS (or P) terms of both signs, whose rounding error scales with the sum of
+#   their magnitudes, not with the (partly cancelled) result.
+# An emulation of the kernel's roundings in float64 meets it with ratio <= 0.28 on both.
+def assert_grad_within_rounding(got, ref, mag, what="", mean_tol=None):
     g = got.detach().to("cpu", torch.float64)
     r = ref.to(torch.float64)
-    assert g.shape == r.shape, (g.shape, r.shape)
+    m = mag.to(torch.float64)
+    assert g.shape == r.shape == m.shape, (g.shape, r.shape, m.shape)
     assert torch.isfinite(g).all(), f"{what}: non-finite gradient"
     err = (g - r).abs()
-    assert err.max().item() <= 2.0 ** -6 * r.abs().max().item(), f"{what}: max-abs {err.max().item():.3e}"
-    assert err.mean().item() <= 2.0 ** -8 * r.abs().mean().item(), f"{what}: mean-abs {err.mean().item():.3e}"
+    bound = GRAD_ATOL + GRAD_RTOL * r.abs() + 2.0 ** -8 * m
+    worst = (err / bound).max().item()
+    assert worst <= 1.0, f"{what}: error {err.max().item():.3e} exceeds the bound (ratio {worst:.2f})"
+    if mean_tol is not None:
+        assert err.mean().item() <= mean_tol, f"{what}: mean-abs {err.mean().item():.3e} > {mean_tol}"
+    return worst
 
 
 def bits_equal(a, b):

@@ -8,7 +8,8 @@ import torch
 
 import oracle
 import sequence_attention_seq_gb300 as uly
-from gpu_util import assert_close, assert_close_grad, assert_normwise_grad, bits_equal, device_ok, need_gpu
+from gpu_util import (GRAD_MEAN, assert_close, assert_close_grad, assert_grad_within_rounding, bits_equal,
+                      device_ok, need_gpu)
 from sequence_attention_seq_gb300.inputs import global_grad, global_qkv, shard_seq
 
 pytestmark = pytest.mark.gpu
@@ -77,12 +78,17 @@ def test_replicated_kv_training(P, b, s, hq, hkv, d, causal, fused):
     err = (torch.cat([x.cpu().double() for x in lse], dim=1) - oracle.attention_lse(q, k, causal)).abs().max().item()
     assert err <= 2e-4, f"lse max-abs {err:.3e}"
     gq, gk, gv = oracle.attention_bwd(q, k, v, do, causal)
-    for name, got, ref in (("dq", dq, gq), ("dk", dk, gk), ("dv", dv, gv)):
+    mags = oracle.attention_bwd_magnitudes(q, k, v, do, causal) if hq // hkv > 4 else None
+    for n, (name, got, ref) in enumerate((("dq", dq, gq), ("dk", dk, gk), ("dv", dv, gv))):
         want = shard_seq(ref, P)
-        # dK/dV of a K/V head shared by more than 4 query heads: norm-wise (see gpu_util)
-        check = assert_normwise_grad if name != "dq" and hq // hkv > 4 else assert_close_grad
         for j in range(P):
-            check(got[j], want[j], f"{name} rank {j}")
+            if name != "dq" and mags is not None:
+                # dK/dV of a K/V head shared by more than 4 query heads: the bound scales with
+                # the magnitude of the summed terms (see gpu_util)
+                assert_grad_within_rounding(got[j], want[j], shard_seq(mags[n], P)[j], f"{name} rank {j}",
+                                            mean_tol=GRAD_MEAN)
+            else:
+                assert_close_grad(got[j], want[j], f"{name} rank {j}")
 
 
 @pytest.mark.parametrize("P,b,s,hq,hkv,d,causal,n_chunks", [(4, 1, 512, 8, 2, 128, True, 2),

@@ -7,7 +7,7 @@ import torch
 
 import oracle
 import sequence_attention_seq_gb300 as uly
-from gpu_util import assert_close_grad, assert_normwise_grad, bits_equal, device_ok, need_gpu
+from gpu_util import assert_close_grad, assert_grad_within_rounding, bits_equal, device_ok, need_gpu
 from sequence_attention_seq_gb300.inputs import global_grad, global_qkv, shard_seq
 
 pytestmark = pytest.mark.gpu
@@ -88,9 +88,11 @@ def test_backward_score_spike():
         dq, dk, dv = uly.ulysses_local_attention_bwd([q.cuda()], [k.cuda()], [v.cuda()], o, [do.cuda()], lse, causal)
         torch.cuda.synchronize()
         wq, wk, wv = oracle.attention_bwd(q, k, v, do, causal)
-        assert_normwise_grad(dq[0], wq, f"dq causal={causal}")
-        assert_normwise_grad(dk[0], wk, f"dk causal={causal}")
-        assert_normwise_grad(dv[0], wv, f"dv causal={causal}")
+        mq, mk, mv = oracle.attention_bwd_magnitudes(q, k, v, do, causal)
+        for name, got, ref, mag in (("dq", dq[0], wq, mq), ("dk", dk[0], wk, mk), ("dv", dv[0], wv, mv)):
+            # keys scaled up to 4x are not N(0,1): the mean bound scales with the terms too
+            assert_grad_within_rounding(got, ref, mag, f"{name} causal={causal}",
+                                        mean_tol=2.0 ** -8 * (ref.abs() + mag).mean().item())
     device_ok()
 
 

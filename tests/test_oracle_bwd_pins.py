@@ -119,3 +119,84 @@ def test_backward_rows_vs_autograd(b, s, hq, hkv, d, causal):
     for n, (bb, j, kh) in enumerate(ksm):
         assert torch.allclose(dk[n], rk[bb, j, kh], atol=1e-11, rtol=0)
         assert torch.allclose(dv[n], rv[bb, j, kh], atol=1e-11, rtol=0)
+
+
+# ---------------------------------------------------------------- term magnitudes
+# oracle.attention_bwd_magnitudes: per gradient element, the sum of the absolute values of
+# its terms (dS_ij widened by P_ij E_i), the quantity a rounding-error bound scales with.
+
+def _autograd_scores(q, k, v, do, causal):
+    """P and dS = dL/dS of one head, from float64 autograd through softmax (a library
+    routine); q, do [s, d], k, v [s, d]."""
+    d = q.shape[-1]
+    sc = (q.double() @ k.double().T / d ** 0.5).detach().requires_grad_()
+    if causal:
+        mask = torch.ones(sc.shape, dtype=torch.bool).tril()
+        p = torch.softmax(sc.masked_fill(~mask, float("-inf")), dim=-1)
+    else:
+        p = torch.softmax(sc, dim=-1)
+    o = p @ v.double()
+    (o * do.double()).sum().backward()
+    return p.detach(), sc.grad, o.detach()
+
+
+@pytest.mark.parametrize("b,s,hq,hkv,d,causal", [(1, 9, 2, 2, 4, False), (2, 13, 4, 2, 8, True),
+                                                 (1, 16, 4, 1, 5, True)])
+def test_magnitudes_vs_autograd_scores(b, s, hq, hkv, d, causal):
+    gen = torch.Generator().manual_seed(41 + s)
+    q = torch.randn(b, s, hq, d, generator=gen, dtype=torch.float64)
+    k = torch.randn(b, s, hkv, d, generator=gen, dtype=torch.float64)
+    v = torch.randn(b, s, hkv, d, generator=gen, dtype=torch.float64)
+    do = torch.randn(b, s, hq, d, generator=gen, dtype=torch.float64)
+    mq, mk, mv = oracle.attention_bwd_magnitudes(q, k, v, do, causal)
+    g = hq // hkv
+    wk = torch.zeros_like(mk)
+    wv = torch.zeros_like(mv)
+    for bb in range(b):
+        for hh in range(hq):
+            kh = hh // g
+            p, ds, o = _autograd_scores(q[bb, :, hh], k[bb, :, kh], v[bb, :, kh], do[bb, :, hh], causal)
+            e = (do[bb, :, hh].abs() * (o.abs() + p @ v[bb, :, kh].abs())).sum(-1, keepdim=True)
+            w = ds.abs() + p * e
+            want_q = w @ k[bb, :, kh].abs() / d ** 0.5
+            assert torch.allclose(mq[bb, :, hh], want_q, atol=1e-10, rtol=1e-10)
+            wk[bb, :, kh] += w.T @ q[bb, :, hh].abs() / d ** 0.5
+            wv[bb, :, kh] += p.T @ do[bb, :, hh].abs()
+    assert torch.allclose(mk, wk, atol=1e-10, rtol=1e-10)
+    assert torch.allclose(mv, wv, atol=1e-10, rtol=1e-10)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_magnitudes_bound_the_gradients(causal):
+    """Triangle inequality: each magnitude is at least the gradient it belongs to."""
+    gen = torch.Generator().manual_seed(5)
+    b, s, hq, hkv, d = 2, 11, 4, 2, 6
+    q, k, v = (torch.randn(b, s, h, d, generator=gen, dtype=torch.float64) for h in (hq, hkv, hkv))
+    do = torch.randn(b, s, hq, d, generator=gen, dtype=torch.float64)
+    dq, dk, dv = oracle.attention_bwd(q, k, v, do, causal)
+    mq, mk, mv = oracle.attention_bwd_magnitudes(q, k, v, do, causal)
+    for grad, mag in ((dq, mq), (dk, mk), (dv, mv)):
+        assert (mag >= grad.abs() - 1e-12).all()
+
+
+def test_magnitudes_closed_forms():
+    gen = torch.Generator().manual_seed(9)
+    d = 7
+    # one token: P = 1, dS = dO.v - dO.O = 0, E = 2 sum_c |dO_c||v_c|
+    q, k, v, do = (torch.randn(1, 1, 1, d, generator=gen, dtype=torch.float64) for _ in range(4))
+    mq, mk, mv = oracle.attention_bwd_magnitudes(q, k, v, do, False)
+    e = 2 * (do.abs() * v.abs()).sum()
+    assert torch.allclose(mv, do.abs(), atol=1e-14)
+    assert torch.allclose(mq, e * k.abs() / d ** 0.5, atol=1e-13)
+    assert torch.allclose(mk, e * q.abs() / d ** 0.5, atol=1e-13)
+    # non-negative dO: every dV term is non-negative, so the magnitude is dV itself
+    s = 10
+    q, k, v = (torch.randn(1, s, 2, d, generator=gen, dtype=torch.float64) for _ in range(3))
+    do = torch.randn(1, s, 2, d, generator=gen, dtype=torch.float64).abs()
+    for causal in (False, True):
+        _, _, dv = oracle.attention_bwd(q, k, v, do, causal)
+        _, _, mv = oracle.attention_bwd_magnitudes(q, k, v, do, causal)
+        assert torch.allclose(mv, dv, atol=1e-12)
+    # zero values: O = 0, dP = 0, so dS = 0 and E = 0
+    mq, mk, _ = oracle.attention_bwd_magnitudes(q, k, torch.zeros_like(v), do, True)
+    assert mq.abs().max().item() == 0.0 and mk.abs().max().item() == 0.0
