@@ -28,7 +28,9 @@
 // overlap window costs more than the pipe drain between PV_k(j) and S_k(j+1) it avoids).
 // The reference maximum m is only raised when a row maximum exceeds it by more than 8
 // (a factor 256), so O is rarely rescaled; P entries stay below 256, exact enough in
-// bf16, and the final O / l is unchanged mathematically.
+// bf16, and the final O / l is unchanged mathematically.  After a row's first key tile
+// the maximum itself is rarely needed: the row's terms are formed against m first, and a
+// sum of at most 256 shows that none exceeds 2^8.
 //
 // Fused mode ("DeepSpeed-Ulysses 深度解析", steps 3 and 5; "02 · DeepSpeed-Ulysses",
 // section 3, where the exchanges "can be merged"): the tiles of tokens [t0, t0+128) come
@@ -248,36 +250,34 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&v);
 }
 
-// Row maximum of the 128 score columns; columns >= lim are masked when MASK.
-template <bool MASK>
-__device__ __forceinline__ float row_max(const uint32_t (&r)[BN], int lim, float m) {
-    float acc[4] = {m, -INFINITY, -INFINITY, -INFINITY};
+// Columns >= lim of a score row -> -inf (diagonal and ragged tiles only).
+__device__ __forceinline__ void mask_row(uint32_t (&r)[BN], int lim) {
+#pragma unroll
+    for (int e = 0; e < BN; ++e)
+        if (e >= lim) r[e] = 0xff800000u;
+}
+
+// Row maximum of the 128 score columns.
+__device__ __forceinline__ float row_max(const uint32_t (&r)[BN]) {
+    float acc[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
     for (int e = 0; e < BN; e += 8) {
         float x[8];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            x[u] = __uint_as_float(r[e + u]);
-            if (MASK) x[u] = e + u < lim ? x[u] : -INFINITY;
-        }
+        for (int u = 0; u < 8; ++u) x[u] = __uint_as_float(r[e + u]);
         acc[(e >> 3) & 3] = fmax3(acc[(e >> 3) & 3], fmax3(x[0], x[1], x[2]), fmax3(x[3], x[4], fmax3(x[5], x[6], x[7])));
     }
     return fmax3(acc[0], acc[1], fmax3(acc[2], acc[3], -INFINITY));
 }
 
-// P = exp2(S*scale - m) for columns [32c, 32c+32), packed into 16 bf16 pairs; returns their sum.
-template <bool MASK>
-__device__ __forceinline__ float chunk_exp(const uint32_t (&r)[BN], int c, int lim, float scale, float neg_m,
-                                           uint32_t (&pk)[16]) {
+// P = exp2(S*scale - m) for columns [32c, 32c+32), packed into 16 bf16 pairs at pk[0..15];
+// returns their sum.
+__device__ __forceinline__ float chunk_exp(const uint32_t (&r)[BN], int c, float scale, float neg_m, uint32_t* pk) {
     float s0 = 0.f, s1 = 0.f;
 #pragma unroll
     for (int e = 0; e < 32; e += 2) {
         const int col = c * 32 + e;
-        float x0 = __uint_as_float(r[col]), x1 = __uint_as_float(r[col + 1]);
-        if (MASK) {
-            x0 = col < lim ? x0 : -INFINITY;
-            x1 = col + 1 < lim ? x1 : -INFINITY;
-        }
+        const float x0 = __uint_as_float(r[col]), x1 = __uint_as_float(r[col + 1]);
         float a0, a1;
         ffma2(a0, a1, x0, x1, scale, scale, neg_m, neg_m);  // S*scale - m for two columns at once
         const float e0 = ex2_approx(a0);
@@ -485,23 +485,47 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
                 const int k0 = j * BN;
                 const bool need_mask = (p.causal && k0 + BN - 1 > q0) || k0 + BN > p.s;
                 const int lim = min(p.s - k0, p.causal ? qrow - k0 + 1 : BN);  // visible columns of this row
-                // the whole S row in one tensor-memory load, its maximum, then the exponentials
+                // The whole S row in one tensor-memory load, then the exponentials.  The first key
+                // tile of a row sets the reference m from the row maximum.  Later tiles first form
+                // their terms against the current reference, in registers: a row whose terms sum
+                // to at most 256 has no term above 2^8, so its maximum exceeds m by at most 8 and
+                // m stands (the rule above).  Only when some row's sum is larger does the warp
+                // reload S (nothing has been stored over it yet) and take the maximum; rows whose
+                // maximum exceeds m by more than 8 raise m, and the terms are formed again.
                 uint32_t sr[BN];
                 tmem_ld128(tS, sr);
                 tmem_wait_ld();
-                const float mx =
-                    need_mask ? row_max<true>(sr, lim, -INFINITY) : row_max<false>(sr, lim, -INFINITY);
-                const float mx2 = mx * scale;
-                float m_new = (j == 0 || mx2 > m_ref + 8.0f) ? mx2 : m_ref;
-                if (m_new == -INFINITY) m_new = 0.f;  // a row with nothing visible yet (padding rows only)
-                float rsum = 0.f;
+                if (need_mask) mask_row(sr, lim);
+                float m_new = m_ref, rsum = 0.f;
+                do {
+                    if (j > 0) {
+                        uint32_t pk[BN / 2];
 #pragma unroll
-                for (int c = 0; c < BN / 32; ++c) {
-                    uint32_t pk[16];
-                    rsum += need_mask ? chunk_exp<true>(sr, c, lim, scale, -m_new, pk)
-                                      : chunk_exp<false>(sr, c, lim, scale, -m_new, pk);
-                    tmem_st16(tS + c * 16, pk);
-                }
+                        for (int c = 0; c < BN / 32; ++c) rsum += chunk_exp(sr, c, scale, -m_ref, pk + 16 * c);
+                        const bool big = !(rsum <= 256.0f);  // also for an infinite sum
+                        if (!__any_sync(0xffffffffu, big)) {
+#pragma unroll
+                            for (int c = 0; c < BN / 32; ++c)
+                                tmem_st16(tS + c * 16, *reinterpret_cast<const uint32_t(*)[16]>(pk + 16 * c));
+                            break;
+                        }
+                        tmem_ld128(tS, sr);
+                        tmem_wait_ld();
+                        if (need_mask) mask_row(sr, lim);
+                        const float mx2 = row_max(sr) * scale;
+                        if (big && mx2 > m_ref + 8.0f) m_new = mx2;
+                    } else {
+                        m_new = row_max(sr) * scale;
+                        if (m_new == -INFINITY) m_new = 0.f;  // a row with nothing visible yet (padding rows only)
+                    }
+                    rsum = 0.f;
+#pragma unroll
+                    for (int c = 0; c < BN / 32; ++c) {
+                        uint32_t pk[16];
+                        rsum += chunk_exp(sr, c, scale, -m_new, pk);
+                        tmem_st16(tS + c * 16, pk);
+                    }
+                } while (0);
                 const float alpha = (j == 0) ? 0.f : ex2_approx(m_ref - m_new);
                 // O_t already holds P_t(j-1) V_{j-1} (S_t(j) was issued after it): rescale in place
                 if (j > 0 && __any_sync(0xffffffffu, m_new != m_ref)) {
