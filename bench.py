@@ -457,7 +457,9 @@ def measured_traffic(workload):
 
 
 def run_permute_sweep(args):
-    """Exchange bandwidth over bf16 [P][1, s/P, 64, 128] with uniform random bits."""
+    """Exchange bandwidth over bf16 [P][1, s/P, 64, 128] with uniform random bits: the
+    kernels alone (20 calls replayed from a CUDA graph) and through the public call with
+    its host work (20 calls back to back), each between CUDA events."""
     import torch
 
     import sequence_attention_seq_gb300 as uly
@@ -468,38 +470,62 @@ def run_permute_sweep(args):
     peaks, _ = load_peaks()
     h, d = 64, 128
     rows = []
-    for s in (8192, 32768, 131072, 262144):
-        for P in (2, 4, 8, 16, 32, 64):
-            xs = [random_bits((1, s // P, h, d), torch.bfloat16, seed=j, device="cuda") for j in range(P)]
-            hd = [torch.empty((1, s, h // P, d), dtype=torch.bfloat16, device="cuda") for _ in range(P)]
-            back = [torch.empty_like(x) for x in xs]
-            nbytes = 2 * s * h * d * 2
-            res = {}
-            for name, fn in (("seq2head", lambda: uly.ulysses_a2a_seq2head(xs, hd)),
-                             ("head2seq", lambda: uly.ulysses_a2a_head2seq(hd, back))):
-                for _ in range(max(3, args.warmup)):
-                    fn()
-                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                reps = 20
-                torch.cuda.synchronize()
-                e0.record()
+    shapes = [(s, P) for s in (8192, 32768, 131072, 262144) for P in (2, 4, 8, 16, 32, 64)]
+    if args.sweep_only:
+        shapes = [tuple(int(x) for x in item.split(",")) for item in args.sweep_only]
+    clocks = ClockSampler(0)
+    clocks.start()
+    time.sleep(0.3)
+    for s, P in shapes:
+        xs = [random_bits((1, s // P, h, d), torch.bfloat16, seed=j, device="cuda") for j in range(P)]
+        hd = [torch.empty((1, s, h // P, d), dtype=torch.bfloat16, device="cuda") for _ in range(P)]
+        back = [torch.empty_like(x) for x in xs]
+        nbytes = 2 * s * h * d * 2
+        res = {}
+        for name, fn in (("seq2head", lambda: uly.ulysses_a2a_seq2head(xs, hd)),
+                         ("head2seq", lambda: uly.ulysses_a2a_head2seq(hd, back))):
+            for _ in range(max(3, args.warmup)):
+                fn()
+            reps = 20
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            # kernels alone: the reps captured in a CUDA graph and replayed, so the host's
+            # per-call argument handling (P pointers per side) is out of the timed region
+            side = torch.cuda.Stream()
+            side.wait_stream(torch.cuda.current_stream())
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=side):
                 for _ in range(reps):
                     fn()
-                e1.record()
-                torch.cuda.synchronize()
-                res[name] = nbytes / (e0.elapsed_time(e1) / reps * 1e-3) / 1e9
-            exact = all(torch.equal(a.view(torch.int16), c.view(torch.int16)) for a, c in zip(xs, back))
-            row = {"s": s, "P": P, "run_bytes": h // P * d * 2, "seq2head_gbs": res["seq2head"],
-                   "head2seq_gbs": res["head2seq"], "round_trip_bit_exact": exact}
-            rows.append(row)
-            print(json.dumps(row))
-            del xs, hd, back
-            torch.cuda.empty_cache()
+            graph.replay()
+            torch.cuda.synchronize()
+            e0.record()
+            graph.replay()
+            e1.record()
+            torch.cuda.synchronize()
+            res[name] = nbytes / (e0.elapsed_time(e1) / reps * 1e-3) / 1e9
+            # and through the public call, host work included
+            e0.record()
+            for _ in range(reps):
+                fn()
+            e1.record()
+            torch.cuda.synchronize()
+            res[name + "_eager"] = nbytes / (e0.elapsed_time(e1) / reps * 1e-3) / 1e9
+            del graph
+        exact = all(torch.equal(a.view(torch.int16), c.view(torch.int16)) for a, c in zip(xs, back))
+        row = {"s": s, "P": P, "run_bytes": h // P * d * 2, "seq2head_gbs": res["seq2head"],
+               "head2seq_gbs": res["head2seq"], "seq2head_gbs_eager": res["seq2head_eager"],
+               "head2seq_gbs_eager": res["head2seq_eager"], "round_trip_bit_exact": exact}
+        rows.append(row)
+        print(json.dumps(row))
+        del xs, hd, back
+        torch.cuda.empty_cache()
+    clk = clocks.stop()
     allv = [r[k] for r in rows for k in ("seq2head_gbs", "head2seq_gbs")]
     print(json.dumps({"metric": "a2a permute GB/s (read+write), bf16 [P][1,s/P,64,128] sweep", "unit": "GB/s",
                       "min": min(allv), "median": statistics.median(allv), "max": max(allv),
                       "peak": peaks["hbm_gbs"], "median_frac": statistics.median(allv) / peaks["hbm_gbs"],
-                      "all_bit_exact": all(r["round_trip_bit_exact"] for r in rows)}))
+                      "min_frac": min(allv) / peaks["hbm_gbs"],
+                      "all_bit_exact": all(r["round_trip_bit_exact"] for r in rows), "clocks": clk}))
 
 
 def run_backward(args):
@@ -711,6 +737,8 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
     ap.add_argument("--permute-sweep", action="store_true",
                     help="measure the exchanges over the permute-only sweep instead of the forward")
+    ap.add_argument("--sweep-only", nargs="*", metavar="S,P",
+                    help="with --permute-sweep: only these (sequence length, ranks) shapes")
     ap.add_argument("--backward", action="store_true",
                     help="measure the attention backward (local and distributed) instead of the forward")
     ap.add_argument("--usp", action="store_true",
