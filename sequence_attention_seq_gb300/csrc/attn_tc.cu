@@ -659,127 +659,8 @@ cudaError_t launch_d(TcParams& prm, long long n_items, cudaStream_t stream) {
 }
 
 #include "attn_bwd.cuh"
-#include "permute_tma.cuh"
-
-// 4-D map over a seq-layout buffer seen as [b][S][row_bytes / inner][inner] 32-bit words;
-// box = (inner, run / inner, R rows, 1 batch), no swizzle.
-bool make_perm_map(CUtensorMap* m, const void* base, int b, int S, uint64_t row_bytes, uint32_t inner, uint32_t run,
-                   uint32_t R) {
-    EncodeTiledFn enc = encode_fn();
-    if (!enc) return false;
-    cuuint64_t dims[4] = {inner / 4, row_bytes / inner, (cuuint64_t)S, (cuuint64_t)b};
-    cuuint64_t strides[3] = {inner, row_bytes, (cuuint64_t)S * row_bytes};
-    cuuint32_t box[4] = {inner / 4, run / inner, R, 1};
-    cuuint32_t estr[4] = {1, 1, 1, 1};
-    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, const_cast<void*>(base), dims, strides, box, estr,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
-}
-
-uint64_t gcd_u64(uint64_t a, uint64_t b) {
-    while (b) {
-        const uint64_t t = a % b;
-        a = b;
-        b = t;
-    }
-    return a;
-}
-
-// Geometry of one tensor's exchange for the TMA path; false if the path does not take it.
-struct PermGeom {
-    uint64_t run, rank_bytes, head_off, row, inner;
-};
-
-bool perm_geometry(const PermuteTensor& T, int P, int d, int elem_bytes, PermGeom* g) {
-    const int per_rank = T.rep > 1 ? 1 : T.h / P;
-    const int hsub = T.hsub > 0 ? T.hsub : per_rank;
-    const uint64_t unit = (uint64_t)d * elem_bytes;
-    g->run = hsub * unit;
-    g->rank_bytes = per_rank * unit;
-    g->head_off = (uint64_t)T.hoff * unit;
-    g->row = (uint64_t)T.h * unit;
-    if (g->run == 0 || g->row == 0) return false;
-    uint64_t inner = gcd_u64(gcd_u64(g->run, g->rank_bytes), g->row);
-    if (g->head_off) inner = gcd_u64(inner, g->head_off);
-    while (inner > 1024 && inner % 32 == 0) inner /= 2;
-    g->inner = inner;
-    return inner % 16 == 0 && inner <= 1024 && g->run / inner <= 256 && g->run <= kPermStageBytes;
-}
 
 }  // namespace
-
-cudaError_t launch_permute_tma(int direction, int P, int b, int s, int d, int elem_bytes, const PermuteTensor* tensors,
-                               int ntensors, cudaStream_t stream, int* eligible) {
-    *eligible = 0;
-    if (ntensors < 1 || ntensors > 4 || P < 1 || s % P) return cudaSuccess;
-    PermGeom geo[4];
-    for (int t = 0; t < ntensors; ++t)
-        if (!perm_geometry(tensors[t], P, d, elem_bytes, &geo[t])) return cudaSuccess;
-    const int S = s / P;
-    if (ntensors * P > kPermMaxMaps) {  // more maps than one launch's parameters hold: one launch per tensor
-        for (int t = 0; t < ntensors; ++t) {
-            int ok = 0;
-            const cudaError_t e = launch_permute_tma(direction, P, b, s, d, elem_bytes, tensors + t, 1, stream, &ok);
-            if (e != cudaSuccess) return e;
-            if (!ok) return cudaErrorInvalidValue;  // cannot happen: every tensor was checked above
-        }
-        *eligible = 1;
-        return cudaSuccess;
-    }
-    TmaPermParams prm_rec;
-    TmaPermParams* prm = &prm_rec;
-    memset(prm, 0, sizeof(TmaPermParams));
-    prm->ntensors = (uint32_t)ntensors;
-    prm->P = (uint32_t)P;
-    prm->S = (uint32_t)S;
-    prm->s = (uint64_t)s;
-    uint64_t chunks = 0;
-    for (int t = 0; t < ntensors; ++t) {
-        const PermuteTensor& T = tensors[t];
-        const PermGeom& g = geo[t];
-        TmaPermJob& J = prm->job[t];
-        J.map0 = (uint32_t)(t * P);
-        J.run = (uint32_t)g.run;
-        J.col0 = (uint32_t)(g.head_off / g.inner);
-        J.rank_cols = (uint32_t)(g.rank_bytes / g.inner);
-        J.rep = T.rep > 1 ? (uint32_t)T.rep : 1u;
-        uint32_t R = kPermStageBytes / (uint32_t)g.run;
-        if (R > 256) R = 256;
-        if (R > (uint32_t)S) R = (uint32_t)S;
-        J.R = R;
-        J.n_rb = (uint32_t)((S + R - 1) / R);
-        J.box_bytes = R * (uint32_t)g.run;
-        chunks += (uint64_t)P * P * b * J.n_rb;
-        J.chunk_end = chunks;
-        for (int r = 0; r < P; ++r) {
-            const void* seq = direction == 0 ? T.src[r] : T.dst[r];
-            void* head = direction == 0 ? T.dst[r] : const_cast<void*>(T.src[r]);
-            if (!make_perm_map(&prm->maps[J.map0 + r], seq, b, S, g.row, (uint32_t)g.inner, (uint32_t)g.run, R))
-                return cudaErrorInvalidValue;
-            prm->contig[J.map0 + r] = static_cast<uint8_t*>(head);
-        }
-    }
-    prm->n_chunks = chunks;
-    *eligible = 1;
-    if (chunks == 0) return cudaSuccess;
-    const uint32_t smem = kPermStages * kPermStageBytes + 1024;
-    cudaError_t e = direction == 0
-                        ? cudaFuncSetAttribute(permute_tma_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)
-                        : cudaFuncSetAttribute(permute_tma_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    int dev = 0, sms = 0;
-    e = cudaGetDevice(&dev);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return e;
-    const uint64_t slots = (uint64_t)sms * kPermCtasPerSm;
-    const uint64_t grid = chunks < slots ? chunks : slots;
-    if (direction == 0)
-        permute_tma_kernel<0><<<(unsigned)grid, 32, smem, stream>>>(*prm);
-    else
-        permute_tma_kernel<1><<<(unsigned)grid, 32, smem, stream>>>(*prm);
-    return cudaGetLastError();
-}
 
 int tc_attention_supported(int d) { return d == 64 || d == 128; }
 

@@ -33,12 +33,6 @@ inline int kv_replication(int P, int h_kv) { return h_kv >= P ? 1 : P / h_kv; }
 cudaError_t launch_permute(int direction, int P, int b, int s, int d, int elem_bytes, const PermuteTensor* tensors,
                            int ntensors, cudaStream_t stream);
 
-// The same exchange with the seq-layout side moved by TMA tensor copies (whole runs per
-// box) and the head-layout side by bulk copies.  *eligible = 0 (nothing enqueued) for
-// shapes it does not take: a run that is not a multiple of 16 bytes or exceeds one box.
-cudaError_t launch_permute_tma(int direction, int P, int b, int s, int d, int elem_bytes, const PermuteTensor* tensors,
-                               int ntensors, cudaStream_t stream, int* eligible);
-
 // The backward of the replicating exchange: gradients of K/V heads replicated on `rep` ranks.
 // src[r]: rank r's fp32 head-layout partial gradient [b][s][1][d] (from its own query heads);
 // dst[j]: bf16 seq layout [b][s/P][h_kv][d] = the sum over the rep replicas, rounded once.

@@ -9,10 +9,11 @@
 // of S rows of H*d elements, and the seq-layout side is S runs of H*d elements with a
 // pitch of h*d elements.  A call may also move only heads [hoff, hoff+hsub) of every
 // rank's group (the head-layout side then holds hsub heads): the chunked, overlapped
-// forward exchanges one head group at a time.  Shapes whose runs are 16-byte multiples of
-// at most 32 KB go to the TMA kernel (permute_tma.cuh); the kernel here covers the rest,
-// streaming the slabs with 16-byte (or narrower) vector loads and stores: the contiguous
-// side is fully coalesced, the strided side moves whole runs.
+// forward exchanges one head group at a time.  The kernel streams those slabs with 16-byte
+// (or narrower) vector loads and stores: the contiguous side is fully coalesced, the
+// strided side moves whole runs.  On GB300 it runs at the device's copy bandwidth; a
+// version that moved whole runs as TMA tensor-map boxes measured 1.5-7% slower on every
+// shape of the exchange sweep and is not used.
 #include <cstring>
 #include <cuda_bf16.h>
 
@@ -24,7 +25,6 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kUnroll = 4;
-constexpr bool kPermuteUseTma = false;
 
 struct PermuteJob {
     const uint8_t* src[kMaxRanks];
@@ -143,13 +143,6 @@ cudaError_t launch_permute(int direction, int P, int b, int s, int d, int elem_b
             if (e != cudaSuccess) return e;
         }
         return cudaSuccess;
-    }
-    // whole runs by TMA boxes where the shapes allow it (16-byte multiples up to 32 KB),
-    // else the vector kernel below
-    if (kPermuteUseTma) {
-        int tma = 0;
-        const cudaError_t te = launch_permute_tma(direction, P, b, s, d, elem_bytes, tensors, ntensors, stream, &tma);
-        if (te != cudaSuccess || tma) return te;
     }
     PermuteParams prm;
     memset(&prm, 0, sizeof(prm));
