@@ -123,8 +123,8 @@ size_t ulysses_dist_attn_workspace_bytes(int P, int b, int s, int h_q, int h_kv,
  *   ulysses_dist_attn_workspace_bytes(...) bytes, owned by the caller).
  * fused != 0: one launch; the attention kernel reads its Q/K/V tiles straight from the
  *   seq-layout buffers and stores its output tiles straight into o_seq, so no
- *   head-layout copy exists.  Needs ULY_BF16, d in {64, 128}, P <= 16 and
- *   (s/P) % 128 == 0, else ULY_ERR_UNSUPPORTED.  workspace may be NULL.
+ *   head-layout copy exists.  Needs ULY_BF16, d in {64, 128} and (s/P) % 128 == 0, else
+ *   ULY_ERR_UNSUPPORTED (any P up to 64).  workspace may be NULL.
  * Both paths give the same bits for the same inputs.
  */
 uly_status ulysses_dist_attn_fwd(int P, int b, int s, int h_q, int h_kv, int d, uly_dtype dtype,
@@ -185,7 +185,7 @@ uly_status ulysses_dist_attn_fwd_overlap(int P, int b, int s, int h_q, int h_kv,
  * h_kv % Pu == 0 or Pu % h_kv == 0 (fewer K/V heads than Ulysses ranks: each K/V head is
  * replicated on the Pu/h_kv ranks of every group whose query heads use it, as in
  * ulysses_local_attention with P = Pu), else ULY_ERR_INVALID_ARG.  Kernel: ULY_BF16, d in {64, 128},
- * Pu*Pr <= 16 and (s/Pr) % 128 == 0, else ULY_ERR_UNSUPPORTED.  The result equals
+ * and (s/Pr) % 128 == 0, else ULY_ERR_UNSUPPORTED.  The result equals
  * ulysses_dist_attn_fwd over the same P ranks bit for bit.  workspace: 256-byte aligned,
  * at least ulysses_usp_workspace_bytes(...) bytes (every rank's group head-layout Q, K,
  * V, O).  Five kinds of launches: Pr exchanges in, one attention, Pr exchanges out.
@@ -214,7 +214,8 @@ uly_status ulysses_usp_attn_fwd(int Pu, int Pr, int b, int s, int h_q, int h_kv,
  *     2. the attention backward of every Ulysses unit over the whole sequence, reading and
  *        writing each tile in the buffer of the ring group that holds its tokens;
  *     3. all-to-all #2 on dQ, dK, dV inside every ring group.
- *   Same sizes and kernel limits as ulysses_usp_attn_fwd, bf16 only.  dq/dk/dv must not
+ *   Same sizes and kernel limits as ulysses_usp_attn_fwd, bf16 only, and Pu*Pr <= 16 (else
+ *   ULY_ERR_UNSUPPORTED).  dq/dk/dv must not
  *   overlap each other or any input.  The results equal ulysses_dist_attn_bwd over the same
  *   P ranks bit for bit where h_kv % P == 0 (with replicated K/V heads the plain call's
  *   dK/dV come from another summation order).  workspace:

@@ -769,7 +769,7 @@ uly_status usp_attn_fwd(int Pu, int Pr, int b, int s, int h_q, int h_kv, int d, 
     st = check_kv_exchange_shape(Pu, b, L, h_kv, d, dtype);
     if (st != ULY_OK) return st;
     if ((long long)b * h_q * ((s + 127) / 128) > 0x7fffffffLL) return ULY_ERR_INVALID_ARG;
-    if (dtype != ULY_BF16 || P > 16 || L % 128 != 0) return ULY_ERR_UNSUPPORTED;
+    if (dtype != ULY_BF16 || L % 128 != 0) return ULY_ERR_UNSUPPORTED;
     const int Hk = uly::kv_heads_per_rank(Pu, h_kv), kv_rep = uly::kv_replication(Pu, h_kv);
     const uint64_t qsb = (uint64_t)b * S * h_q * d * 2, ksb = (uint64_t)b * S * h_kv * d * 2;
     RangeSet rq, rk, rv, ro;

@@ -59,17 +59,22 @@ constexpr int kSlots = 4; // K/V ring slots
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kThreads = 320;
-constexpr int kMaxMaps = 16;
+constexpr int kMaxMaps = 16;      // maps per launch: unfused rank groups, the backward
+constexpr int kMaxMapsWide = 64;  // fused and two-level forwards over more than kMaxMaps ranks
 constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far beyond any legitimate wait
 constexpr unsigned int kErrTimeout = 1u;
 
-struct TcParams {
-    CUtensorMap mq[kMaxMaps];
-    CUtensorMap mk[kMaxMaps];
-    CUtensorMap mv[kMaxMaps];
-    uint8_t* optr[kMaxMaps];  // output buffers (same indexing as the maps): [b][rows][heads][d] bf16
-    float* lse[kMaxMaps];     // optional per-row log-sum-exp (natural log), per head rank [b][lse_heads][s]
+// NM maps of each kind: kMaxMaps, or kMaxMapsWide for more ranks (about 25 KB of kernel
+// parameters, so the common launches keep the small block).
+template <int NM>
+struct TcParamsT {
+    static constexpr int kMaps = NM;
+    CUtensorMap mq[NM];
+    CUtensorMap mk[NM];
+    CUtensorMap mv[NM];
+    uint8_t* optr[NM];  // output buffers (same indexing as the maps): [b][rows][heads][d] bf16
+    float* lse[NM];     // optional per-row log-sum-exp (natural log), per head rank [b][lse_heads][s]
     int lse_heads;            // query heads per head rank: the heads of one lse array
     int s;             // sequence length
     int rows_per_map;  // tokens held by one map: s/P when fused, s/Pr for the two-level forward, s otherwise
@@ -85,6 +90,7 @@ struct TcParams {
     int causal;
     float scale_log2;  // log2(e) / sqrt(d)
 };
+using TcParams = TcParamsT<kMaxMaps>;
 
 template <int D>
 struct Smem {
@@ -183,7 +189,8 @@ struct TileCoord {
 // map is the seq-layout rank t0 / (s/P).  Two-level (Ulysses x Ring): rank = u and the map
 // is ring group t0 / (s/Pr)'s rank u, i.e. the K/V blocks of the other ring groups are read
 // where those ranks hold them.
-__device__ __forceinline__ TileCoord tile_coord(const TcParams& p, int rank, int t0) {
+template <class PR>
+__device__ __forceinline__ TileCoord tile_coord(const PR& p, int rank, int t0) {
     TileCoord c;
     c.map = rank + (t0 / p.rows_per_map) * p.map_stride;
     c.row = t0 % p.rows_per_map;
@@ -201,7 +208,8 @@ struct Item {
     int rank, bb, kvh, head, qt0, n0, n1;
 };
 
-__device__ __forceinline__ Item decode_item(const TcParams& p, int w) {
+template <class PR>
+__device__ __forceinline__ Item decode_item(const PR& p, int w) {
     Item it;
     const int kv_heads = p.heads / p.g;
     const int hg = w % p.g;
@@ -239,7 +247,8 @@ __device__ __forceinline__ Item decode_item(const TcParams& p, int w) {
 
 // The k-th item of CTA c: rounds of gridDim.x items, alternating direction (snake), so
 // the heavy-first order spreads evenly; -1 when the CTA has no k-th item.
-__device__ __forceinline__ int item_index(const TcParams& p, int k) {
+template <class PR>
+__device__ __forceinline__ int item_index(const PR& p, int k) {
     const int G = gridDim.x, c = blockIdx.x;
     const int w = k * G + ((k & 1) ? G - 1 - c : c);
     return w < p.n_items ? w : -1;
@@ -288,8 +297,8 @@ __device__ __forceinline__ float chunk_exp(const uint32_t (&r)[BN], int c, float
     return s0 + s1;
 }
 
-template <int D>
-__global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_constant__ TcParams p) {
+template <int D, int NM>
+__global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_constant__ TcParamsT<NM> p) {
     using L = Smem<D>;
     constexpr int KSTEPS_QK = D / 16;  // MMA K-steps for S = Q K^T
     constexpr int KSTEPS_PV = BN / 16; // MMA K-steps for O += P V
@@ -642,10 +651,11 @@ int band_units_for(int s, int d, int units) {
     return bu;
 }
 
-template <int D>
-cudaError_t launch_d(TcParams& prm, long long n_items, cudaStream_t stream) {
+template <int D, int NM>
+cudaError_t launch_d(TcParamsT<NM>& prm, long long n_items, cudaStream_t stream) {
     const uint32_t smem = Smem<D>::kAlloc;
-    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e =
+        cudaFuncSetAttribute(attn_tc_kernel<D, NM>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     int dev = 0, sms = 0;
     e = cudaGetDevice(&dev);
@@ -654,7 +664,7 @@ cudaError_t launch_d(TcParams& prm, long long n_items, cudaStream_t stream) {
     // persistent: one CTA per SM walks the items (each CTA fills an SM: smem and all TMEM)
     prm.n_items = (int)n_items;
     const long long grid = n_items < sms ? n_items : sms;
-    attn_tc_kernel<D><<<(unsigned)grid, kThreads, smem, stream>>>(prm);
+    attn_tc_kernel<D, NM><<<(unsigned)grid, kThreads, smem, stream>>>(prm);
     return cudaGetLastError();
 }
 
@@ -664,68 +674,112 @@ cudaError_t launch_d(TcParams& prm, long long n_items, cudaStream_t stream) {
 
 int tc_attention_supported(int d) { return d == 64 || d == 128; }
 
-cudaError_t launch_attention_tc(int P, int b, int s, int h_q, int h_kv, int d, int causal, int fused,
-                                const AttnPtrs& ptrs, cudaStream_t stream, int* unsupported) {
-    *unsupported = 0;
-    const bool want_lse = ptrs.lse[0] != nullptr;
-    if (!tc_attention_supported(d) || (fused && (P > kMaxMaps || (s / P) % BM != 0))) {
-        *unsupported = 1;
-        return cudaSuccess;
-    }
-    TcParams prm_rec;
-    TcParams* prm = &prm_rec;
-    memset(prm, 0, sizeof(TcParams));
+namespace {
+
+template <class PR>
+void fill_common(PR* prm, int s, int b, int g, int causal, int d) {
+    memset(prm, 0, sizeof(PR));
     prm->s = s;
     prm->map_stride = 1;
     prm->n_qtiles = (s + BM - 1) / BM;
     prm->n_pairs = (prm->n_qtiles + 1) / 2;
-    prm->g = h_q / h_kv;
+    prm->g = g;
     prm->b = b;
     prm->causal = causal ? 1 : 0;
     prm->scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)d));
+}
+
+template <class PR>
+cudaError_t launch_any_d(PR& prm, int d, long long n_items, cudaStream_t stream) {
+    return d == 64 ? launch_d<64>(prm, n_items, stream) : launch_d<128>(prm, n_items, stream);
+}
+
+// The fused forward: one map per seq-layout rank buffer (NM >= P).
+template <int NM>
+cudaError_t launch_fused_fwd(int P, int b, int s, int h_q, int h_kv, int d, int causal, const AttnPtrs& ptrs,
+                             bool want_lse, cudaStream_t stream) {
+    TcParamsT<NM> prm_rec;
+    TcParamsT<NM>* prm = &prm_rec;
+    fill_common(prm, s, b, h_q / h_kv, causal, d);
+    const int S = s / P;
+    prm->rows_per_map = S;
+    prm->heads = h_q;
+    prm->lse_heads = h_q / P;  // the statistics go to the head ranks' arrays
+    prm->nranks = 1;
+    for (int j = 0; j < P; ++j) {
+        if (!make_map(&prm->mq[j], ptrs.q[j], b, S, h_q, d, BM) || !make_map(&prm->mk[j], ptrs.k[j], b, S, h_kv, d, BN) ||
+            !make_map(&prm->mv[j], ptrs.v[j], b, S, h_kv, d, BN))
+            return cudaErrorInvalidValue;
+        prm->optr[j] = static_cast<uint8_t*>(ptrs.o[j]);
+        prm->lse[j] = want_lse ? ptrs.lse[j] : nullptr;
+    }
+    const long long n_items = (long long)b * h_q * prm->n_pairs;
+    prm->band_units = band_units_for(s, d, b * h_kv);
+    return launch_any_d(*prm, d, n_items, stream);
+}
+
+// The two-level forward: one map per rank's group head-layout buffer (NM >= Pu * Pr).
+template <int NM>
+cudaError_t launch_usp_fwd(int Pu, int Pr, int b, int s, int h_q, int h_kv, int d, int causal, const AttnPtrs& head,
+                           cudaStream_t stream) {
+    const int P = Pu * Pr, L = s / Pr;
+    const int Hq = h_q / Pu, Hk = kv_heads_per_rank(Pu, h_kv);  // 1: a replicated K/V head
+    TcParamsT<NM> prm_rec;
+    TcParamsT<NM>* prm = &prm_rec;
+    fill_common(prm, s, b, Hq / Hk, causal, d);
+    prm->rows_per_map = L;
+    prm->map_stride = Pu;
+    prm->heads = Hq;
+    prm->lse_heads = Hq;  // statistics (if asked for) per Ulysses unit over all s rows
+    prm->nranks = Pu;
+    for (int j = 0; j < P; ++j) {
+        if (!make_map(&prm->mq[j], head.q[j], b, L, Hq, d, BM) || !make_map(&prm->mk[j], head.k[j], b, L, Hk, d, BN) ||
+            !make_map(&prm->mv[j], head.v[j], b, L, Hk, d, BN))
+            return cudaErrorInvalidValue;
+        prm->optr[j] = static_cast<uint8_t*>(head.o[j]);
+    }
+    for (int u = 0; u < Pu; ++u) prm->lse[u] = head.lse[u];  // unit u's rows of every ring group
+    const long long n_items = (long long)Pu * b * Hq * prm->n_pairs;
+    prm->band_units = band_units_for(s, d, Pu * b * Hk);
+    return launch_any_d(*prm, d, n_items, stream);
+}
+
+}  // namespace
+
+cudaError_t launch_attention_tc(int P, int b, int s, int h_q, int h_kv, int d, int causal, int fused,
+                                const AttnPtrs& ptrs, cudaStream_t stream, int* unsupported) {
+    *unsupported = 0;
+    const bool want_lse = ptrs.lse[0] != nullptr;
+    if (!tc_attention_supported(d) || (fused && (P > kMaxMapsWide || (s / P) % BM != 0))) {
+        *unsupported = 1;
+        return cudaSuccess;
+    }
+    if (fused)
+        return P <= kMaxMaps ? launch_fused_fwd<kMaxMaps>(P, b, s, h_q, h_kv, d, causal, ptrs, want_lse, stream)
+                             : launch_fused_fwd<kMaxMapsWide>(P, b, s, h_q, h_kv, d, causal, ptrs, want_lse, stream);
+    // unfused: the head ranks in groups of up to kMaxMaps per launch
+    TcParams prm_rec;
+    TcParams* prm = &prm_rec;
+    const int Hq = h_q / P, Hk = kv_heads_per_rank(P, h_kv);
+    fill_common(prm, s, b, Hq / Hk, causal, d);  // g within a rank (its K/V heads may be shared replicas)
+    prm->rows_per_map = s;
+    prm->heads = Hq;
+    prm->lse_heads = Hq;
     cudaError_t err = cudaSuccess;
-    if (fused) {
-        const int S = s / P;
-        prm->rows_per_map = S;
-        prm->heads = h_q;
-        prm->lse_heads = h_q / P;  // the statistics go to the head ranks' arrays
-        prm->nranks = 1;
-        for (int j = 0; j < P && err == cudaSuccess; ++j) {
-            if (!make_map(&prm->mq[j], ptrs.q[j], b, S, h_q, d, BM) ||
-                !make_map(&prm->mk[j], ptrs.k[j], b, S, h_kv, d, BN) ||
-                !make_map(&prm->mv[j], ptrs.v[j], b, S, h_kv, d, BN))
-                err = cudaErrorInvalidValue;
-            prm->optr[j] = static_cast<uint8_t*>(ptrs.o[j]);
-            prm->lse[j] = want_lse ? ptrs.lse[j] : nullptr;
+    for (int r0 = 0; r0 < P && err == cudaSuccess; r0 += kMaxMaps) {
+        const int nr = (P - r0) < kMaxMaps ? (P - r0) : kMaxMaps;
+        prm->nranks = nr;
+        for (int i = 0; i < nr; ++i) {
+            const int r = r0 + i;
+            if (!make_map(&prm->mq[i], ptrs.q[r], b, s, Hq, d, BM) || !make_map(&prm->mk[i], ptrs.k[r], b, s, Hk, d, BN) ||
+                !make_map(&prm->mv[i], ptrs.v[r], b, s, Hk, d, BN))
+                return cudaErrorInvalidValue;
+            prm->optr[i] = static_cast<uint8_t*>(ptrs.o[r]);
+            prm->lse[i] = want_lse ? ptrs.lse[r] : nullptr;
         }
-        if (err == cudaSuccess) {
-            const long long n_items = (long long)b * h_q * prm->n_pairs;
-            prm->band_units = band_units_for(s, d, b * h_kv);
-            err = d == 64 ? launch_d<64>(*prm, n_items, stream) : launch_d<128>(*prm, n_items, stream);
-        }
-    } else {
-        const int Hq = h_q / P, Hk = kv_heads_per_rank(P, h_kv);
-        prm->rows_per_map = s;
-        prm->heads = Hq;
-        prm->g = Hq / Hk;  // within a rank (its K/V heads may be replicas shared with other ranks)
-        prm->lse_heads = Hq;
-        for (int r0 = 0; r0 < P && err == cudaSuccess; r0 += kMaxMaps) {
-            const int nr = (P - r0) < kMaxMaps ? (P - r0) : kMaxMaps;
-            prm->nranks = nr;
-            for (int i = 0; i < nr && err == cudaSuccess; ++i) {
-                const int r = r0 + i;
-                if (!make_map(&prm->mq[i], ptrs.q[r], b, s, Hq, d, BM) ||
-                    !make_map(&prm->mk[i], ptrs.k[r], b, s, Hk, d, BN) ||
-                    !make_map(&prm->mv[i], ptrs.v[r], b, s, Hk, d, BN))
-                    err = cudaErrorInvalidValue;
-                prm->optr[i] = static_cast<uint8_t*>(ptrs.o[r]);
-                prm->lse[i] = want_lse ? ptrs.lse[r] : nullptr;
-            }
-            if (err != cudaSuccess) break;
-            const long long n_items = (long long)nr * b * Hq * prm->n_pairs;
-            prm->band_units = band_units_for(s, d, nr * b * Hk);
-            err = d == 64 ? launch_d<64>(*prm, n_items, stream) : launch_d<128>(*prm, n_items, stream);
-        }
+        const long long n_items = (long long)nr * b * Hq * prm->n_pairs;
+        prm->band_units = band_units_for(s, d, nr * b * Hk);
+        err = launch_any_d(*prm, d, n_items, stream);
     }
     return err;
 }
@@ -734,40 +788,12 @@ cudaError_t launch_attention_tc_usp(int Pu, int Pr, int b, int s, int h_q, int h
                                     const AttnPtrs& head, cudaStream_t stream, int* unsupported) {
     *unsupported = 0;
     const int P = Pu * Pr, L = s / Pr;
-    if (!tc_attention_supported(d) || P > kMaxMaps || L % BM != 0) {
+    if (!tc_attention_supported(d) || P > kMaxMapsWide || L % BM != 0) {
         *unsupported = 1;
         return cudaSuccess;
     }
-    const int Hq = h_q / Pu, Hk = kv_heads_per_rank(Pu, h_kv);  // 1: a replicated K/V head
-    TcParams prm_rec;
-    TcParams* prm = &prm_rec;
-    memset(prm, 0, sizeof(TcParams));
-    prm->s = s;
-    prm->rows_per_map = L;
-    prm->map_stride = Pu;
-    prm->n_qtiles = s / BM;
-    prm->n_pairs = (prm->n_qtiles + 1) / 2;
-    prm->heads = Hq;
-    prm->lse_heads = Hq;  // statistics (if asked for) per Ulysses unit over all s rows
-    prm->g = Hq / Hk;
-    prm->b = b;
-    prm->nranks = Pu;
-    prm->causal = causal ? 1 : 0;
-    prm->scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)d));
-    cudaError_t err = cudaSuccess;
-    for (int j = 0; j < P && err == cudaSuccess; ++j) {
-        if (!make_map(&prm->mq[j], head.q[j], b, L, Hq, d, BM) || !make_map(&prm->mk[j], head.k[j], b, L, Hk, d, BN) ||
-            !make_map(&prm->mv[j], head.v[j], b, L, Hk, d, BN))
-            err = cudaErrorInvalidValue;
-        prm->optr[j] = static_cast<uint8_t*>(head.o[j]);
-    }
-    for (int u = 0; u < Pu; ++u) prm->lse[u] = head.lse[u];  // unit u's rows of every ring group
-    if (err == cudaSuccess) {
-        const long long n_items = (long long)Pu * b * Hq * prm->n_pairs;
-        prm->band_units = band_units_for(s, d, Pu * b * Hk);
-        err = d == 64 ? launch_d<64>(*prm, n_items, stream) : launch_d<128>(*prm, n_items, stream);
-    }
-    return err;
+    return P <= kMaxMaps ? launch_usp_fwd<kMaxMaps>(Pu, Pr, b, s, h_q, h_kv, d, causal, head, stream)
+                         : launch_usp_fwd<kMaxMapsWide>(Pu, Pr, b, s, h_q, h_kv, d, causal, head, stream);
 }
 
 namespace {

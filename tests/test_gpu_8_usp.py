@@ -22,6 +22,7 @@ CASES = [
     (2, 2, 1, 768, 2, 2, 128, False),
     (4, 2, 1, 1024, 8, 8, 128, True),    # P | h_kv: also bitwise against plain Ulysses
     (2, 2, 2, 512, 8, 4, 64, False),
+    (4, 8, 1, 2048, 4, 4, 64, True),     # 32 ranks: the wide parameter block
 ]
 
 
