@@ -319,15 +319,19 @@ def run_e2e(torch, uly, w, ins, dev, stream, steps, warmup):
     run(max(1, warmup))
     torch.cuda.synchronize(dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(dev.index if dev.index is not None else 0)
+    clocks.start()
+    time.sleep(0.3)
     e0.record(stream)
     run(steps)
     e1.record(stream)
     torch.cuda.synchronize(dev)
+    clk = clocks.stop()
     if uly.ulysses_device_status(clear=True) != 0:
         raise RuntimeError("a kernel's bounded wait gave up during the end-to-end steps")
     fl = attn_flops(b, s, hq, d, causal)
     del dev_in, dev_out, ws
-    return dict(e2e_ms=e0.elapsed_time(e1), step_flops=fl, h2d=h2d, d2h=d2h, host_in=host_in,
+    return dict(e2e_ms=e0.elapsed_time(e1), step_flops=fl, h2d=h2d, d2h=d2h, host_in=host_in, clocks=clk,
                 call="ulysses_dist_attn_fwd(fused=%d, causal=%d)" % (int(fused), int(causal)))
 
 
@@ -572,7 +576,7 @@ def run_backward(args):
             "dist_bwd": lambda: uly.ulysses_dist_attn_bwd(qs, ks, vs, o, dos, lse, causal, grads=grads_s,
                                                           workspace=ws_d),
         }
-        if P <= 16 and (s // P) % 128 == 0:  # the exchanges folded into the kernels' tile addressing
+        if P <= 48 and (s // P) % 128 == 0:  # the exchanges folded into the kernels' tile addressing
             calls["dist_bwd_fused"] = lambda: uly.ulysses_dist_attn_bwd(qs, ks, vs, o, dos, lse, causal,
                                                                         grads=grads_s, workspace=ws_l, fused=True)
         fl = 2.5 * attn_flops(b, s, hq, d, causal)
@@ -856,7 +860,8 @@ def main():
                      "bytes": "read+write of all ranks' data"} if "permute" in summ else None),
         "per_launch_ms": res["per_op"],
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": e2e["h2d"],
-                "d2h_bytes_per_step": e2e["d2h"], "call": e2e["call"]},
+                "d2h_bytes_per_step": e2e["d2h"], "call": e2e["call"], "ms_per_step": e2e_ms / args.steps,
+                "clocks": e2e["clocks"]},
         "gpu_launches": res["n_launches"] * world,
         "clocks": res["clocks"],
         "cpu_baseline": cpu,

@@ -214,7 +214,7 @@ uly_status ulysses_usp_attn_fwd(int Pu, int Pr, int b, int s, int h_q, int h_kv,
  *     2. the attention backward of every Ulysses unit over the whole sequence, reading and
  *        writing each tile in the buffer of the ring group that holds its tokens;
  *     3. all-to-all #2 on dQ, dK, dV inside every ring group.
- *   Same sizes and kernel limits as ulysses_usp_attn_fwd, bf16 only, and Pu*Pr <= 16 (else
+ *   Same sizes and kernel limits as ulysses_usp_attn_fwd, bf16 only, and Pu*Pr <= 48 (else
  *   ULY_ERR_UNSUPPORTED).  dq/dk/dv must not
  *   overlap each other or any input.  The results equal ulysses_dist_attn_bwd over the same
  *   P ranks bit for bit where h_kv % P == 0 (with replicated K/V heads the plain call's
@@ -347,7 +347,7 @@ uly_status ulysses_local_attention_bwd(int P, int b, int s, int h_q, int h_kv, i
  * fused != 0: D and the statistics, then the dK/dV and dQ kernels read their Q/K/V/dO
  *   tiles straight from the seq-layout buffers and write dQ/dK/dV rows straight into the
  *   seq-layout outputs, so no head-layout copy exists (the backward of the fused
- *   forward).  Needs P <= 16 and (s/P) % 128 == 0, else ULY_ERR_UNSUPPORTED.  Both paths
+ *   forward).  Needs P <= 48 and (s/P) % 128 == 0, else ULY_ERR_UNSUPPORTED.  Both paths
  *   give the same bits.
  *   q_seq, o_seq, do_seq, dq_seq: P pointers to [b][s/P][h_q][d];
  *   k_seq, v_seq, dk_seq, dv_seq: P pointers to [b][s/P][h_kv][d];

@@ -491,7 +491,7 @@ uly_status ulysses_dist_attn_bwd(int P, int b, int s, int h_q, int h_kv, int d, 
     RangeSet outs;
     if (!outs.append(rdq) || !outs.append(rdk) || !outs.append(rdv)) return ULY_ERR_INVALID_ARG;
     if (self_overlap(outs) || overlaps(outs, in)) return ULY_ERR_INVALID_ARG;
-    if (fused && (P > 16 || S % 128 != 0)) return ULY_ERR_UNSUPPORTED;
+    if (fused && (P > 48 || S % 128 != 0)) return ULY_ERR_UNSUPPORTED;
     const size_t need = ulysses_attn_bwd_workspace_bytes(P, b, s, h_q, h_kv, d, dtype, 1, fused);
     if (!workspace_ok(workspace, workspace_bytes, need)) return ULY_ERR_INVALID_ARG;
     const RangeSet rw = one_range(workspace, need);
@@ -886,7 +886,7 @@ uly_status ulysses_usp_attn_bwd(int Pu, int Pr, int b, int s, int h_q, int h_kv,
     st = check_kv_exchange_shape(Pu, b, L, h_kv, d, dtype);
     if (st != ULY_OK) return st;
     if ((long long)b * h_q * ((s + 127) / 128) > 0x7fffffffLL) return ULY_ERR_INVALID_ARG;
-    if (P > 16 || L % 128 != 0) return ULY_ERR_UNSUPPORTED;
+    if (P > 48 || L % 128 != 0) return ULY_ERR_UNSUPPORTED;
     const int Hk = uly::kv_heads_per_rank(Pu, h_kv), kv_rep = uly::kv_replication(Pu, h_kv);
     const uint64_t qsb = (uint64_t)b * S * h_q * d * 2, ksb = (uint64_t)b * S * h_kv * d * 2;
     RangeSet in, rdq, rdk, rdv;

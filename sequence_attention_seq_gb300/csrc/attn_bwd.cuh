@@ -60,13 +60,17 @@ constexpr int kRingQ = 5;    // dQ kernel: K/V ring slots
 // one buffer per seq rank (rows_per_map = s/P, hq/hkv = all heads, rank = 0), so the
 // exchanges happen in the tile addressing.  The row statistics always live per head rank:
 // head h of a CTA belongs to head rank rank + h / hq_rank, local head h % hq_rank.
-struct BwdParams {
-    CUtensorMap mq[kMaxMaps], mk[kMaxMaps], mv[kMaxMaps], mdo[kMaxMaps];
-    uint8_t* dq[kMaxMaps];        // [b][rows][hq][d] bf16
-    uint8_t* dk[kMaxMaps];        // [b][rows][hkv][d] bf16 (fp32 with kv_grad_f32)
-    uint8_t* dv[kMaxMaps];
-    const float* lse2[kMaxMaps];  // per head rank [b][hq_rank][s_pad]: log-sum-exp, base-2 units (+inf on padding)
-    const float* dsum[kMaxMaps];  // per head rank [b][hq_rank][s_pad]: D (0 on padding)
+// NM maps of each kind: kMaxMaps, or kMaxMapsBwdWide for fused or two-level calls over
+// more rank buffers (four maps per rank: at most 48 ranks fit the 32 KB parameter limit).
+template <int NM>
+struct BwdParamsT {
+    static constexpr int kMaps = NM;
+    CUtensorMap mq[NM], mk[NM], mv[NM], mdo[NM];
+    uint8_t* dq[NM];        // [b][rows][hq][d] bf16
+    uint8_t* dk[NM];        // [b][rows][hkv][d] bf16 (fp32 with kv_grad_f32)
+    uint8_t* dv[NM];
+    const float* lse2[NM];  // per head rank [b][hq_rank][s_pad]: log-sum-exp, base-2 units (+inf on padding)
+    const float* dsum[NM];  // per head rank [b][hq_rank][s_pad]: D (0 on padding)
     int s, s_pad, n_tiles, hq, hkv, g, b, causal;
     int rows_per_map;             // s (unfused), s/P (fused) or s/Pr (two-level)
     int map_stride;               // map step from one token block to the next (Pu two-level, else 1)
@@ -81,19 +85,23 @@ struct BwdParams {
     int q_items;                  // n_units_q * n_tiles
     int band_units_q;             // causal: units per band (see q_item)
 };
+using BwdParams = BwdParamsT<kMaxMaps>;
 
 struct BwdTok {
     int map, row;
 };
-__device__ __forceinline__ BwdTok bwd_tok(const BwdParams& p, int rank, int t0) {
+template <class PR>
+__device__ __forceinline__ BwdTok bwd_tok(const PR& p, int rank, int t0) {
     return BwdTok{rank + (t0 / p.rows_per_map) * p.map_stride, t0 % p.rows_per_map};
 }
 
 // Row statistics of (batch bb, query head h of the CTA's unit `rank`), from query q0 on.
-__device__ __forceinline__ size_t bwd_stat_off(const BwdParams& p, int bb, int h, int q0) {
+template <class PR>
+__device__ __forceinline__ size_t bwd_stat_off(const PR& p, int bb, int h, int q0) {
     return ((size_t)bb * p.hq_rank + h % p.hq_rank) * p.s_pad + q0;
 }
-__device__ __forceinline__ int bwd_stat_rank(const BwdParams& p, int rank, int h) { return rank + h / p.hq_rank; }
+template <class PR>
+__device__ __forceinline__ int bwd_stat_rank(const PR& p, int rank, int h) { return rank + h / p.hq_rank; }
 
 // ------------------------------------------------------------------------- prep
 struct PrepParams {
@@ -281,7 +289,8 @@ struct KvItem {
     int rank, bb, kvh, kt;
 };
 
-__device__ __forceinline__ KvItem kv_item(const BwdParams& p, int w) {
+template <class PR>
+__device__ __forceinline__ KvItem kv_item(const PR& p, int w) {
     int u, kt;
     if (p.causal) {
         const int per_band = p.band_units * p.n_tiles;
@@ -323,8 +332,8 @@ __device__ __forceinline__ int bwd_item_index(int n_items, int k) {
 // the accumulator) waits for P-ready, which every row warp signals only after its epilogue.
 // Tensor memory: S^T (then P^T) 0..127 | dP^T (then dS^T) 128..255 | dK 256.. | dV 384..
 // F32: dk/dv receive fp32 partial sums (a replicated K/V head's share from this rank).
-template <int D, int RW, bool F32, bool PERSIST>
-__global__ void __launch_bounds__(RowCfg<RW>::kThreads, 1) bwd_dkdv_kernel(const __grid_constant__ BwdParams p) {
+template <int D, int RW, bool F32, bool PERSIST, int NM>
+__global__ void __launch_bounds__(RowCfg<RW>::kThreads, 1) bwd_dkdv_kernel(const __grid_constant__ BwdParamsT<NM> p) {
     using C = RowCfg<RW>;
     constexpr int kBwdRowWarps = C::kRows, kBwdProducer = C::kProducer, kBwdMma = C::kMma;
     constexpr int kColGroups = C::kColGroups, kColW = C::kColW, kChunks = C::kChunks;
@@ -609,7 +618,8 @@ struct QItem {
     int rank, bb, hh, qt;
 };
 
-__device__ __forceinline__ QItem q_item(const BwdParams& p, int w) {
+template <class PR>
+__device__ __forceinline__ QItem q_item(const PR& p, int w) {
     int u, r;
     if (p.causal) {
         const int per_band = p.band_units_q * p.n_tiles;
@@ -638,8 +648,8 @@ __device__ __forceinline__ QItem q_item(const BwdParams& p, int w) {
 // dQ; the next item's first dQ product (which overwrites the accumulator) waits for
 // dS-ready, which every row warp signals only after its epilogue.
 // Tensor memory: S/dS buffer 0 0..127 | dP 128..255 | dQ 256.. | S/dS buffer 1 384..511.
-template <int D, int RW, bool PERSIST>
-__global__ void __launch_bounds__(RowCfg<RW>::kThreads, 1) bwd_dq_kernel(const __grid_constant__ BwdParams p) {
+template <int D, int RW, bool PERSIST, int NM>
+__global__ void __launch_bounds__(RowCfg<RW>::kThreads, 1) bwd_dq_kernel(const __grid_constant__ BwdParamsT<NM> p) {
     using C = RowCfg<RW>;
     constexpr int kBwdRowWarps = C::kRows, kBwdProducer = C::kProducer, kBwdMma = C::kMma;
     constexpr int kColGroups = C::kColGroups, kColW = C::kColW, kChunks = C::kChunks;
@@ -896,11 +906,11 @@ inline int bwd_band_units_q(int s_pad, int d, int g, int units) {
     return bu;
 }
 
-template <int D>
-cudaError_t launch_bwd_d(const BwdParams& prm_in, int nranks, cudaStream_t stream) {
+template <int D, int NM>
+cudaError_t launch_bwd_d(const BwdParamsT<NM>& prm_in, int nranks, cudaStream_t stream) {
     using LK = BwdSmem<D, kRingKV>;
     using LQ = BwdSmem<D, kRingQ>;
-    BwdParams prm = prm_in;
+    BwdParamsT<NM> prm = prm_in;
     prm.n_units = nranks * prm.b * prm.hkv;
     prm.kv_items = prm.n_units * prm.n_tiles;
     prm.band_units = bwd_band_units(prm.s_pad, D, prm.g, prm.n_units);
@@ -918,11 +928,11 @@ cudaError_t launch_bwd_d(const BwdParams& prm_in, int nranks, cudaStream_t strea
     prm.band_units_q = bwd_band_units_q(prm.s_pad, D, prm.g, prm.n_units_q);
     const bool persistent_q = !prm.causal || (short_causal && prm.band_units_q == prm.n_units_q);
     if (!persistent_q) prm.band_units_q = 1;
-    auto* dkdv = prm.kv_grad_f32 ? (persistent ? bwd_dkdv_kernel<D, kRowsKV, true, true>
-                                               : bwd_dkdv_kernel<D, kRowsKV, true, false>)
-                                 : (persistent ? bwd_dkdv_kernel<D, kRowsKV, false, true>
-                                               : bwd_dkdv_kernel<D, kRowsKV, false, false>);
-    auto* dq = persistent_q ? bwd_dq_kernel<D, kRowsQ, true> : bwd_dq_kernel<D, kRowsQ, false>;
+    auto* dkdv = prm.kv_grad_f32 ? (persistent ? bwd_dkdv_kernel<D, kRowsKV, true, true, NM>
+                                               : bwd_dkdv_kernel<D, kRowsKV, true, false, NM>)
+                                 : (persistent ? bwd_dkdv_kernel<D, kRowsKV, false, true, NM>
+                                               : bwd_dkdv_kernel<D, kRowsKV, false, false, NM>);
+    auto* dq = persistent_q ? bwd_dq_kernel<D, kRowsQ, true, NM> : bwd_dq_kernel<D, kRowsQ, false, NM>;
     cudaError_t e = cudaFuncSetAttribute(dkdv, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)LK::kAlloc);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(dq, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)LQ::kAlloc);
     if (e != cudaSuccess) return e;

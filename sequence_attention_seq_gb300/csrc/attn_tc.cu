@@ -61,6 +61,7 @@ constexpr int kMmaWarp = 9;
 constexpr int kThreads = 320;
 constexpr int kMaxMaps = 16;      // maps per launch: unfused rank groups, the backward
 constexpr int kMaxMapsWide = 64;  // fused and two-level forwards over more than kMaxMaps ranks
+constexpr int kMaxMapsBwdWide = 48;  // fused and two-level backwards (four maps per rank)
 constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far beyond any legitimate wait
 constexpr unsigned int kErrTimeout = 1u;
@@ -838,116 +839,75 @@ cudaError_t launch_bwd_prep(int n_head_ranks, int n_seq_ranks, int b, int s, int
 
 }  // namespace
 
-cudaError_t launch_attention_bwd_tc(int P, int b, int s, int h_q, int h_kv, int d, int causal, int fused,
-                                    const BwdPtrs& ptrs, cudaStream_t stream, int* unsupported) {
-    *unsupported = 0;
-    if (!tc_attention_supported(d) || (fused && (P > kMaxMaps || (s / P) % 128 != 0))) {
-        *unsupported = 1;
-        return cudaSuccess;
-    }
-    const int Hq = h_q / P, Hk = kv_heads_per_rank(P, h_kv);
+namespace {
+
+template <class PR>
+void fill_bwd_common(PR* prm, int s, int b, int causal, int d) {
+    memset(prm, 0, sizeof(PR));
     const int n_tiles = (s + 127) / 128;
-    // (1) row sums D and base-2 log-sum-exp, all ranks in one grid
-    cudaError_t err = launch_bwd_prep(P, P, b, s, h_q, d, ptrs, stream);
-    if (err != cudaSuccess) return err;
-    // (2) dK/dV and dQ: one launch pair over seq-layout buffers (fused), else up to kMaxMaps
-    //     head ranks per launch pair
-    BwdParams prm_rec;
-    BwdParams* prm = &prm_rec;
-    memset(prm, 0, sizeof(BwdParams));
     prm->s = s;
     prm->s_pad = n_tiles * 128;
     prm->n_tiles = n_tiles;
-    prm->g = h_q / h_kv;
     prm->b = b;
     prm->causal = causal ? 1 : 0;
-    prm->hq_rank = Hq;
     prm->map_stride = 1;
     prm->scale = (float)(1.0 / std::sqrt((double)d));
     prm->scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)d));
-    if (fused) {
-        const int S = s / P;
-        prm->rows_per_map = S;
-        prm->hq = h_q;
-        prm->hkv = h_kv;
-        for (int j = 0; j < P && err == cudaSuccess; ++j) {
-            if (!make_map(&prm->mq[j], ptrs.q[j], b, S, h_q, d, 128) ||
-                !make_map(&prm->mk[j], ptrs.k[j], b, S, h_kv, d, 128) ||
-                !make_map(&prm->mv[j], ptrs.v[j], b, S, h_kv, d, 128) ||
-                !make_map(&prm->mdo[j], ptrs.dout[j], b, S, h_q, d, 128))
-                err = cudaErrorInvalidValue;
-            prm->dq[j] = static_cast<uint8_t*>(ptrs.dq[j]);
-            prm->dk[j] = static_cast<uint8_t*>(ptrs.dk[j]);
-            prm->dv[j] = static_cast<uint8_t*>(ptrs.dv[j]);
-            prm->lse2[j] = ptrs.lse2[j];  // head rank j's statistics
-            prm->dsum[j] = ptrs.dsum[j];
-        }
-        if (err == cudaSuccess) err = d == 64 ? launch_bwd_d<64>(*prm, 1, stream) : launch_bwd_d<128>(*prm, 1, stream);
-    } else {
-        prm->rows_per_map = s;
-        prm->hq = Hq;
-        prm->hkv = Hk;
-        prm->g = Hq / Hk;  // within a rank (its K/V heads may be replicas shared with other ranks)
-        prm->kv_grad_f32 = ptrs.kv_grad_f32;
-        for (int r0 = 0; r0 < P && err == cudaSuccess; r0 += kMaxMaps) {
-            const int nr = (P - r0) < kMaxMaps ? (P - r0) : kMaxMaps;
-            for (int i = 0; i < nr && err == cudaSuccess; ++i) {
-                const int r = r0 + i;
-                if (!make_map(&prm->mq[i], ptrs.q[r], b, s, Hq, d, 128) ||
-                    !make_map(&prm->mk[i], ptrs.k[r], b, s, Hk, d, 128) ||
-                    !make_map(&prm->mv[i], ptrs.v[r], b, s, Hk, d, 128) ||
-                    !make_map(&prm->mdo[i], ptrs.dout[r], b, s, Hq, d, 128))
-                    err = cudaErrorInvalidValue;
-                prm->dq[i] = static_cast<uint8_t*>(ptrs.dq[r]);
-                prm->dk[i] = static_cast<uint8_t*>(ptrs.dk[r]);
-                prm->dv[i] = static_cast<uint8_t*>(ptrs.dv[r]);
-                prm->lse2[i] = ptrs.lse2[r];
-                prm->dsum[i] = ptrs.dsum[r];
-            }
-            if (err != cudaSuccess) break;
-            err = d == 64 ? launch_bwd_d<64>(*prm, nr, stream) : launch_bwd_d<128>(*prm, nr, stream);
-        }
-    }
-    return err;
 }
 
-cudaError_t launch_attention_bwd_tc_usp(int Pu, int Pr, int b, int s, int h_q, int h_kv, int d, int causal,
-                                        const BwdPtrs& ptrs, cudaStream_t stream, int* unsupported) {
-    *unsupported = 0;
-    const int P = Pu * Pr, L = s / Pr;
-    if (!tc_attention_supported(d) || P > kMaxMaps || L % 128 != 0) {
-        *unsupported = 1;
-        return cudaSuccess;
+template <class PR>
+cudaError_t launch_bwd_any_d(const PR& prm, int d, int nranks, cudaStream_t stream) {
+    return d == 64 ? launch_bwd_d<64>(prm, nranks, stream) : launch_bwd_d<128>(prm, nranks, stream);
+}
+
+// dK/dV and dQ over the seq-layout buffers: one map per rank buffer and kind (NM >= P).
+template <int NM>
+cudaError_t launch_fused_bwd(int P, int b, int s, int h_q, int h_kv, int d, int causal, const BwdPtrs& ptrs,
+                             cudaStream_t stream) {
+    BwdParamsT<NM> prm_rec;
+    BwdParamsT<NM>* prm = &prm_rec;
+    fill_bwd_common(prm, s, b, causal, d);
+    const int S = s / P;
+    prm->g = h_q / h_kv;
+    prm->hq_rank = h_q / P;
+    prm->rows_per_map = S;
+    prm->hq = h_q;
+    prm->hkv = h_kv;
+    for (int j = 0; j < P; ++j) {
+        if (!make_map(&prm->mq[j], ptrs.q[j], b, S, h_q, d, 128) || !make_map(&prm->mk[j], ptrs.k[j], b, S, h_kv, d, 128) ||
+            !make_map(&prm->mv[j], ptrs.v[j], b, S, h_kv, d, 128) ||
+            !make_map(&prm->mdo[j], ptrs.dout[j], b, S, h_q, d, 128))
+            return cudaErrorInvalidValue;
+        prm->dq[j] = static_cast<uint8_t*>(ptrs.dq[j]);
+        prm->dk[j] = static_cast<uint8_t*>(ptrs.dk[j]);
+        prm->dv[j] = static_cast<uint8_t*>(ptrs.dv[j]);
+        prm->lse2[j] = ptrs.lse2[j];  // head rank j's statistics
+        prm->dsum[j] = ptrs.dsum[j];
     }
+    return launch_bwd_any_d(*prm, d, 1, stream);
+}
+
+// The two-level backward's dK/dV and dQ over the Pu units: one map per rank buffer and kind.
+template <int NM>
+cudaError_t launch_usp_bwd(int Pu, int Pr, int b, int s, int h_q, int h_kv, int d, int causal, const BwdPtrs& ptrs,
+                           cudaStream_t stream) {
+    const int P = Pu * Pr, L = s / Pr;
     const int Hq = h_q / Pu, Hk = kv_heads_per_rank(Pu, h_kv);  // 1: a replicated K/V head
-    const int n_tiles = (s + 127) / 128;
-    // (1) statistics per Ulysses unit (Pu head ranks over all s rows), O and dO in seq layout
-    cudaError_t err = launch_bwd_prep(Pu, P, b, s, h_q, d, ptrs, stream);
-    if (err != cudaSuccess) return err;
-    // (2) dK/dV and dQ over the Pu units, every tile read from (written to) the buffer of the
-    //     ring group that holds its tokens: the forward's two-level tile addressing
-    BwdParams prm_rec;
-    BwdParams* prm = &prm_rec;
-    memset(prm, 0, sizeof(BwdParams));
-    prm->s = s;
-    prm->s_pad = n_tiles * 128;
-    prm->n_tiles = n_tiles;
+    BwdParamsT<NM> prm_rec;
+    BwdParamsT<NM>* prm = &prm_rec;
+    fill_bwd_common(prm, s, b, causal, d);
     prm->g = Hq / Hk;  // within a unit
-    prm->b = b;
-    prm->causal = causal ? 1 : 0;
     prm->hq_rank = Hq;
     prm->hq = Hq;
     prm->hkv = Hk;
     prm->rows_per_map = L;
     prm->map_stride = Pu;
     prm->kv_grad_f32 = ptrs.kv_grad_f32;
-    prm->scale = (float)(1.0 / std::sqrt((double)d));
-    prm->scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)d));
-    for (int j = 0; j < P && err == cudaSuccess; ++j) {
+    for (int j = 0; j < P; ++j) {
         if (!make_map(&prm->mq[j], ptrs.q[j], b, L, Hq, d, 128) || !make_map(&prm->mk[j], ptrs.k[j], b, L, Hk, d, 128) ||
             !make_map(&prm->mv[j], ptrs.v[j], b, L, Hk, d, 128) ||
             !make_map(&prm->mdo[j], ptrs.dout[j], b, L, Hq, d, 128))
-            err = cudaErrorInvalidValue;
+            return cudaErrorInvalidValue;
         prm->dq[j] = static_cast<uint8_t*>(ptrs.dq[j]);
         prm->dk[j] = static_cast<uint8_t*>(ptrs.dk[j]);
         prm->dv[j] = static_cast<uint8_t*>(ptrs.dv[j]);
@@ -956,8 +916,70 @@ cudaError_t launch_attention_bwd_tc_usp(int Pu, int Pr, int b, int s, int h_q, i
         prm->lse2[u] = ptrs.lse2[u];
         prm->dsum[u] = ptrs.dsum[u];
     }
-    if (err == cudaSuccess) err = d == 64 ? launch_bwd_d<64>(*prm, Pu, stream) : launch_bwd_d<128>(*prm, Pu, stream);
+    return launch_bwd_any_d(*prm, d, Pu, stream);
+}
+
+}  // namespace
+
+cudaError_t launch_attention_bwd_tc(int P, int b, int s, int h_q, int h_kv, int d, int causal, int fused,
+                                    const BwdPtrs& ptrs, cudaStream_t stream, int* unsupported) {
+    *unsupported = 0;
+    if (!tc_attention_supported(d) || (fused && (P > kMaxMapsBwdWide || (s / P) % 128 != 0))) {
+        *unsupported = 1;
+        return cudaSuccess;
+    }
+    // (1) row sums D and base-2 log-sum-exp, all ranks in one grid
+    cudaError_t err = launch_bwd_prep(P, P, b, s, h_q, d, ptrs, stream);
+    if (err != cudaSuccess) return err;
+    // (2) dK/dV and dQ: one launch pair over seq-layout buffers (fused), else up to kMaxMaps
+    //     head ranks per launch pair
+    if (fused)
+        return P <= kMaxMaps ? launch_fused_bwd<kMaxMaps>(P, b, s, h_q, h_kv, d, causal, ptrs, stream)
+                             : launch_fused_bwd<kMaxMapsBwdWide>(P, b, s, h_q, h_kv, d, causal, ptrs, stream);
+    const int Hq = h_q / P, Hk = kv_heads_per_rank(P, h_kv);
+    BwdParams prm_rec;
+    BwdParams* prm = &prm_rec;
+    fill_bwd_common(prm, s, b, causal, d);
+    prm->hq_rank = Hq;
+    prm->rows_per_map = s;
+    prm->hq = Hq;
+    prm->hkv = Hk;
+    prm->g = Hq / Hk;  // within a rank (its K/V heads may be replicas shared with other ranks)
+    prm->kv_grad_f32 = ptrs.kv_grad_f32;
+    for (int r0 = 0; r0 < P && err == cudaSuccess; r0 += kMaxMaps) {
+        const int nr = (P - r0) < kMaxMaps ? (P - r0) : kMaxMaps;
+        for (int i = 0; i < nr; ++i) {
+            const int r = r0 + i;
+            if (!make_map(&prm->mq[i], ptrs.q[r], b, s, Hq, d, 128) || !make_map(&prm->mk[i], ptrs.k[r], b, s, Hk, d, 128) ||
+                !make_map(&prm->mv[i], ptrs.v[r], b, s, Hk, d, 128) ||
+                !make_map(&prm->mdo[i], ptrs.dout[r], b, s, Hq, d, 128))
+                return cudaErrorInvalidValue;
+            prm->dq[i] = static_cast<uint8_t*>(ptrs.dq[r]);
+            prm->dk[i] = static_cast<uint8_t*>(ptrs.dk[r]);
+            prm->dv[i] = static_cast<uint8_t*>(ptrs.dv[r]);
+            prm->lse2[i] = ptrs.lse2[r];
+            prm->dsum[i] = ptrs.dsum[r];
+        }
+        err = launch_bwd_any_d(*prm, d, nr, stream);
+    }
     return err;
+}
+
+cudaError_t launch_attention_bwd_tc_usp(int Pu, int Pr, int b, int s, int h_q, int h_kv, int d, int causal,
+                                        const BwdPtrs& ptrs, cudaStream_t stream, int* unsupported) {
+    *unsupported = 0;
+    const int P = Pu * Pr, L = s / Pr;
+    if (!tc_attention_supported(d) || P > kMaxMapsBwdWide || L % 128 != 0) {
+        *unsupported = 1;
+        return cudaSuccess;
+    }
+    // (1) statistics per Ulysses unit (Pu head ranks over all s rows), O and dO in seq layout
+    cudaError_t err = launch_bwd_prep(Pu, P, b, s, h_q, d, ptrs, stream);
+    if (err != cudaSuccess) return err;
+    // (2) dK/dV and dQ over the Pu units, every tile read from (written to) the buffer of the
+    //     ring group that holds its tokens: the forward's two-level tile addressing
+    return P <= kMaxMaps ? launch_usp_bwd<kMaxMaps>(Pu, Pr, b, s, h_q, h_kv, d, causal, ptrs, stream)
+                         : launch_usp_bwd<kMaxMapsBwdWide>(Pu, Pr, b, s, h_q, h_kv, d, causal, ptrs, stream);
 }
 
 cudaError_t launch_wait_selftest(uint64_t limit_ns, cudaStream_t stream) {

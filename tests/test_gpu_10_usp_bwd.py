@@ -20,6 +20,7 @@ CASES = [
     (1, 2, 1, 256, 2, 1, 128, True),     # ring only
     (4, 1, 1, 512, 8, 4, 64, True),      # Ulysses only
     (4, 2, 1, 1024, 8, 8, 128, False),   # P | h_kv
+    (4, 8, 1, 1024, 4, 4, 64, True),     # 32 rank buffers: the wide parameter block
 ]
 
 
