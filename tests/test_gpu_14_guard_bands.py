@@ -2,7 +2,8 @@
 larger buffer whose margins hold a known byte pattern, and the margins must come back
 unchanged.  This catches a kernel writing past the end (or before the start) of what it
 owns, in the cases most likely to do so: ragged last tiles, head sub-ranges, the
-replicated-K/V partial sums and the two-level layout.  The results themselves are
+replicated-K/V partial sums, the two-level layout and the fused paths over more rank
+buffers than the small parameter block holds.  The results themselves are
 checked elsewhere; here only that nothing else was touched."""
 import pytest
 import torch
@@ -54,6 +55,7 @@ def _seq(P, b, s, hq, hkv, d, dt, seed):
     (4, 2, 512, 8, 8, 64, torch.bfloat16),
     (4, 1, 512, 8, 2, 128, torch.bfloat16),   # replicated K/V heads (h_kv < P)
     (2, 1, 96, 4, 4, 32, torch.float32),      # the fp32 kernel
+    (32, 1, 4096, 32, 32, 64, torch.bfloat16),  # fused over 32 rank buffers: the wide parameter block
 ])
 def test_forward_paths_stay_inside(P, b, s, hq, hkv, d, dt):
     need_gpu()
@@ -82,6 +84,7 @@ def test_forward_paths_stay_inside(P, b, s, hq, hkv, d, dt):
     (4, 2, 512, 8, 8, 64, True),
     (4, 1, 512, 8, 2, 128, False),    # replicated K/V: fp32 partial sums in the workspace
     (4, 8, 320, 32, 16, 64, False),   # several work items per CTA
+    (24, 1, 3072, 24, 24, 64, True),  # fused over 24 rank buffers: the wide parameter block
 ])
 def test_backward_stays_inside(P, b, s, hq, hkv, d, fused):
     need_gpu()
