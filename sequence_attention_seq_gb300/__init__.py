@@ -26,7 +26,7 @@ __all__ = [
     "ulysses_local_attention_bwd", "ulysses_dist_attn_bwd", "ulysses_dist_attn_overlap_workspace_bytes",
     "ulysses_dist_attn_fwd_overlap", "ulysses_usp_workspace_bytes", "ulysses_usp_attn_fwd",
     "ulysses_usp_attn_fwd_lse", "ulysses_usp_bwd_workspace_bytes", "ulysses_usp_attn_bwd",
-    "ulysses_wait_selftest",
+    "ulysses_wait_selftest", "ulysses_a2a_pack", "ulysses_a2a_unpack",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -44,6 +44,7 @@ EXPORTED_SYMBOLS = (
     "ulysses_dist_attn_bwd", "ulysses_dist_attn_overlap_workspace_bytes", "ulysses_dist_attn_fwd_overlap",
     "ulysses_usp_workspace_bytes", "ulysses_usp_attn_fwd", "ulysses_usp_attn_fwd_lse",
     "ulysses_usp_bwd_workspace_bytes", "ulysses_usp_attn_bwd", "ulysses_wait_selftest",
+    "ulysses_a2a_pack", "ulysses_a2a_unpack",
 )
 
 _lock = threading.Lock()
@@ -112,6 +113,10 @@ def load_library():
         lib.ulysses_usp_attn_bwd.argtypes = [i, i, i, i, i, i, i, i, i, pp, pp, pp, pp, pp, pp, pp, pp, pp, vp, sz,
                                              vp]
         lib.ulysses_usp_attn_bwd.restype = i
+        for name in ("ulysses_a2a_pack", "ulysses_a2a_unpack"):
+            f = getattr(lib, name)
+            f.argtypes = [i, i, i, i, i, i, i, vp, vp, vp]
+            f.restype = i
         lib.ulysses_wait_selftest.argtypes = [ctypes.c_ulonglong, vp]
         lib.ulysses_wait_selftest.restype = i
         lib.ulysses_device_status.argtypes = [i]
@@ -158,11 +163,14 @@ def _dtype_code(t):
 
 def _same(tensors, what):
     t0 = tensors[0]
+    if not t0.is_cuda:
+        raise ValueError(f"{what}: tensors must live on a CUDA device")
+    # one pass of cheap attribute reads: with 64 ranks a call checks 128 tensors
+    shape, dtype, dev = t0.shape, t0.dtype, t0.get_device()
     for t in tensors:
-        if t.shape != t0.shape or t.dtype != t0.dtype or t.device != t0.device or not t.is_contiguous():
+        if t.shape != shape or t.dtype is not dtype or t.get_device() != dev or not t.is_cuda \
+                or not t.is_contiguous():
             raise ValueError(f"{what}: every rank needs a contiguous tensor of one shape, dtype and device")
-        if t.device.type != "cuda":
-            raise ValueError(f"{what}: tensors must live on a CUDA device")
     return t0
 
 
@@ -190,6 +198,44 @@ def ulysses_a2a_head2seq(in_head, out_seq=None, stream=None):
     _check(load_library().ulysses_a2a_head2seq(P, b, s, H * P, d, _dtype_code(t0), _ptr_array(in_head),
                                                _ptr_array(out_seq), _stream(stream)), "ulysses_a2a_head2seq")
     return out_seq
+
+
+def ulysses_a2a_pack(local, direction, P, out=None, stream=None):
+    """One rank's send blocks for an all-to-all with P processes: direction 0 takes this
+    rank's seq shard [b, s/P, h, d], direction 1 its head shard [b, s, h/P, d]; returns
+    [P, b, s/P, h/P, d] (block i goes to rank i)."""
+    _same([local], "local")
+    if direction == 0:
+        b, S, h, d = local.shape
+        s = S * P
+    elif direction == 1:
+        b, s, H, d = local.shape
+        S, h = s // P, H * P
+    else:
+        raise ValueError("direction must be 0 (seq -> head) or 1 (head -> seq)")
+    if out is None:
+        out = torch.empty((P, b, S, h // P, d), dtype=local.dtype, device=local.device)
+    _same([out], "out")
+    _check(load_library().ulysses_a2a_pack(direction, P, b, s, h, d, _dtype_code(local), local.data_ptr(),
+                                           out.data_ptr(), _stream(stream)), "ulysses_a2a_pack")
+    return out
+
+
+def ulysses_a2a_unpack(recv, direction, out=None, stream=None):
+    """This rank's layout after an all-to-all with P processes: recv [P, b, s/P, h/P, d]
+    (block j came from rank j) -> direction 0: the head shard [b, s, h/P, d]; direction 1:
+    the seq shard [b, s/P, h, d]."""
+    _same([recv], "recv")
+    P, b, S, H, d = recv.shape
+    if direction not in (0, 1):
+        raise ValueError("direction must be 0 (seq -> head) or 1 (head -> seq)")
+    shape = (b, S * P, H, d) if direction == 0 else (b, S, H * P, d)
+    if out is None:
+        out = torch.empty(shape, dtype=recv.dtype, device=recv.device)
+    _same([out], "out")
+    _check(load_library().ulysses_a2a_unpack(direction, P, b, S * P, H * P, d, _dtype_code(recv), recv.data_ptr(),
+                                             out.data_ptr(), _stream(stream)), "ulysses_a2a_unpack")
+    return out
 
 
 def ulysses_local_attention(q_head, k_head, v_head, causal, out_head=None, stream=None):
