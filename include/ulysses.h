@@ -74,6 +74,36 @@ uly_status ulysses_a2a_head2seq(int P, int b, int s, int h, int d, uly_dtype dty
                                 cudaStream_t stream);
 
 /*
+ * The local halves of one rank's all-to-all when the P ranks are P processes on P GPUs
+ * (one rank per process, the exchange itself a collective between them): "DeepSpeed-Ulysses
+ * 深度解析", section "构建序列并行通信组" (DistributedAttention over a sequence-parallel
+ * process group) and "大模型分布式训练通信原语及其应用", section 5 "AllToAll（全交换）"
+ * (every rank cuts its input into P parts, sends part i to rank i, and lays the parts it
+ * receives out in sending-rank order).  With S = s/P and H = h/P, every send and receive
+ * buffer is P contiguous blocks [P][b][S][H][d] -- block i of the send buffer goes to rank i,
+ * block j of the receive buffer came from rank j -- so an equal-split all-to-all (NCCL
+ * ncclSend/ncclRecv pairs, or torch.distributed.all_to_all_single) moves them:
+ *   ulysses_a2a_pack(0, ...):   local = this rank's seq shard [b][S][h][d];
+ *                               send block r = heads [r*H, (r+1)*H) of every token.
+ *   ulysses_a2a_unpack(0, ...): recv block j = tokens [j*S, (j+1)*S) of this rank's heads;
+ *                               local = this rank's head shard [b][s][H][d].
+ *   ulysses_a2a_pack(1, ...):   local = this rank's head shard [b][s][H][d];
+ *                               send block j = tokens [j*S, (j+1)*S).
+ *   ulysses_a2a_unpack(1, ...): recv block r = heads [r*H, (r+1)*H) of this rank's tokens;
+ *                               local = this rank's seq shard [b][S][h][d].
+ * pack(0), the collective and unpack(0) together give this rank's part of
+ * ulysses_a2a_seq2head; pack(1), the collective and unpack(1) its part of
+ * ulysses_a2a_head2seq.  Both sides hold b*S*h*d elements.  Sizes as the exchanges above.
+ * direction not 0 or 1, a null or misaligned pointer, or overlapping in/out buffers give
+ * ULY_ERR_INVALID_ARG.  Bit copies.  Device pointers, owned by the caller; enqueued on stream.
+ */
+uly_status ulysses_a2a_pack(int direction, int P, int b, int s, int h, int d, uly_dtype dtype,
+                            const void* local, void* send, cudaStream_t stream);
+uly_status ulysses_a2a_unpack(int direction, int P, int b, int s, int h, int d, uly_dtype dtype,
+                              const void* recv, void* local, cudaStream_t stream);
+
+
+/*
  * Local attention of every rank, head layout in and out ("DeepSpeed-Ulysses 深度解析",
  * step 4: softmax(Q K^T / sqrt(d)) V per local head over the full sequence).
  *   o_head[r][bb][i][hh][:] = sum_j softmax_j(q.k_j / sqrt(d)) v_j

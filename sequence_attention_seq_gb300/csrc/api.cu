@@ -368,6 +368,42 @@ uly_status ulysses_a2a_head2seq(int P, int b, int s, int h, int d, uly_dtype dty
     return exchange(1, P, b, s, h, d, dtype, in_head, out_seq, stream);
 }
 
+// The local halves of one rank's exchange with other GPUs: the send blocks before the
+// collective and the layout after it, each one block transpose.
+static uly_status a2a_local(int pack, int direction, int P, int b, int s, int h, int d, uly_dtype dtype,
+                            const void* in, void* out, cudaStream_t stream) {
+    uly_status st = check_exchange_shape(P, b, s, h, d, dtype);
+    if (st != ULY_OK) return st;
+    if (direction != 0 && direction != 1) return ULY_ERR_INVALID_ARG;
+    const uint64_t e = (uint64_t)elem_bytes(dtype), S = (uint64_t)(s / P), H = (uint64_t)(h / P);
+    const uint64_t bytes = (uint64_t)b * S * h * d * e;  // one rank's share, on either side
+    RangeSet ri, ro;
+    if (!collect(&in, 1, bytes, ri) || !collect(const_cast<const void* const*>(&out), 1, bytes, ro) || overlaps(ri, ro))
+        return ULY_ERR_INVALID_ARG;
+    const uint64_t head_run = H * d * e, block_run = S * H * d * e;
+    uint64_t A, C, run;
+    if (direction == 0 && pack) {         // seq shard [b*S][P][H*d] -> blocks [P][b*S][H*d]
+        A = (uint64_t)b * S, C = P, run = head_run;
+    } else if (direction == 0) {          // received blocks [P][b][S*H*d] -> head shard [b][P][S*H*d]
+        A = P, C = b, run = block_run;
+    } else if (pack) {                    // head shard [b][P][S*H*d] -> blocks [P][b][S*H*d]
+        A = b, C = P, run = block_run;
+    } else {                              // received blocks [P][b*S][H*d] -> seq shard [b*S][P][H*d]
+        A = P, C = (uint64_t)b * S, run = head_run;
+    }
+    return uly::launch_block_transpose(A, C, run, in, out, stream) == cudaSuccess ? ULY_OK : ULY_ERR_CUDA;
+}
+
+uly_status ulysses_a2a_pack(int direction, int P, int b, int s, int h, int d, uly_dtype dtype, const void* local,
+                            void* send, cudaStream_t stream) {
+    return a2a_local(1, direction, P, b, s, h, d, dtype, local, send, stream);
+}
+
+uly_status ulysses_a2a_unpack(int direction, int P, int b, int s, int h, int d, uly_dtype dtype, const void* recv,
+                              void* local, cudaStream_t stream) {
+    return a2a_local(0, direction, P, b, s, h, d, dtype, recv, local, stream);
+}
+
 uly_status ulysses_local_attention(int P, int b, int s, int h_q, int h_kv, int d, uly_dtype dtype, int causal,
                                    const void* const* q_head, const void* const* k_head, const void* const* v_head,
                                    void* const* o_head, cudaStream_t stream) {

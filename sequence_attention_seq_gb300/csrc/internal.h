@@ -33,6 +33,11 @@ inline int kv_replication(int P, int h_kv) { return h_kv >= P ? 1 : P / h_kv; }
 cudaError_t launch_permute(int direction, int P, int b, int s, int d, int elem_bytes, const PermuteTensor* tensors,
                            int ntensors, cudaStream_t stream);
 
+// out[c][a] = in[a][c] for A x C runs of run_bytes each: the local halves of one rank's
+// all-to-all with other GPUs (the send blocks before the collective, the layout after it).
+cudaError_t launch_block_transpose(uint64_t A, uint64_t C, uint64_t run_bytes, const void* in, void* out,
+                                   cudaStream_t stream);
+
 // The backward of the replicating exchange: gradients of K/V heads replicated on `rep` ranks.
 // src[r]: rank r's fp32 head-layout partial gradient [b][s][1][d] (from its own query heads);
 // dst[j]: bf16 seq layout [b][s/P][h_kv][d] = the sum over the rep replicas, rounded once.

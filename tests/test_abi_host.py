@@ -156,3 +156,15 @@ def test_two_level_kv_head_rule(lib):
     assert f(4, 1, 1, 512, 12, 3, 128, BF16, 1, q, k, v, o, None, 0, None) == INVALID
     assert f(4, 1, 1, 512, 12, 5, 128, BF16, 1, q, k, v, o, None, 0, None) == INVALID   # h_q % h_kv
     assert f(4, 1, 1, 512, 6, 2, 128, BF16, 1, q, k, v, o, None, 0, None) == INVALID    # h_q % Pu
+
+
+def test_pack_unpack_argument_errors(lib):
+    # validation fails before any CUDA call: fake, never dereferenced addresses
+    for f in (lib.ulysses_a2a_pack, lib.ulysses_a2a_unpack):
+        assert f(2, 2, 1, 64, 4, 16, FP32, A, B, None) == INVALID       # direction not 0 or 1
+        assert f(0, 2, 1, 63, 4, 16, FP32, A, B, None) == INVALID       # s % P
+        assert f(1, 2, 1, 64, 3, 16, FP32, A, B, None) == INVALID       # h % P
+        assert f(0, 2, 1, 64, 4, 16, FP32, 0, B, None) == INVALID       # null
+        assert f(0, 2, 1, 64, 4, 16, FP32, A + 4, B, None) == INVALID   # misaligned
+        assert f(0, 2, 1, 64, 4, 16, FP32, A, A + 1024, None) == INVALID  # out overlaps in (4 KB each side)
+        assert f(0, 65, 1, 65, 65, 16, FP32, A, B, None) == INVALID     # P > 64
