@@ -20,9 +20,11 @@ from __future__ import annotations
 import torch
 import torch.distributed as dist
 
-from . import ulysses_a2a_pack, ulysses_a2a_unpack, ulysses_local_attention
+from . import (ulysses_a2a_pack, ulysses_a2a_unpack, ulysses_local_attention, ulysses_local_attention_bwd,
+               ulysses_local_attention_fwd_lse)
 
-__all__ = ["exchange", "ulysses_dist_attn_fwd_multi"]
+__all__ = ["exchange", "ulysses_dist_attn_fwd_multi", "ulysses_dist_attn_fwd_lse_multi",
+           "ulysses_dist_attn_bwd_multi"]
 
 
 def exchange(x, direction, group=None, stream=None):
@@ -45,3 +47,25 @@ def ulysses_dist_attn_fwd_multi(q, k, v, causal, group=None):
     qh, kh, vh = (exchange(x, 0, group) for x in (q, k, v))
     (oh,) = ulysses_local_attention([qh], [kh], [vh], causal)
     return exchange(oh, 1, group)
+
+
+def ulysses_dist_attn_fwd_lse_multi(q, k, v, causal, group=None):
+    """The forward for training: returns (o [b, s/P, h_q, d], saved), saved holding what the
+    backward needs -- this rank's head shards of Q, K, V and O and the natural-log
+    log-sum-exp [b, h_q/P, s] of its heads' rows."""
+    P = dist.get_world_size(group)
+    if q.shape[2] % P or k.shape[2] % P:
+        raise ValueError(f"h_q={q.shape[2]} and h_kv={k.shape[2]} must be multiples of the {P} ranks")
+    qh, kh, vh = (exchange(x, 0, group) for x in (q, k, v))
+    (oh,), (lse,) = ulysses_local_attention_fwd_lse([qh], [kh], [vh], causal)
+    return exchange(oh, 1, group), (qh, kh, vh, oh, lse)
+
+
+def ulysses_dist_attn_bwd_multi(do, saved, causal, group=None):
+    """The backward ("02 · DeepSpeed-Ulysses", section 5: the backward of all-to-all #2 is
+    all-to-all #1 and the reverse): dO [b, s/P, h_q, d] of this rank's tokens and the saved
+    forward state -> (dq, dk, dv) in this rank's seq layout."""
+    qh, kh, vh, oh, lse = saved
+    doh = exchange(do, 0, group)
+    (dqh,), (dkh,), (dvh,) = ulysses_local_attention_bwd([qh], [kh], [vh], [oh], [doh], [lse], causal)
+    return tuple(exchange(g, 1, group) for g in (dqh, dkh, dvh))

@@ -7,8 +7,9 @@
     all-to-all would (block r of rank j's send buffer becomes block j of rank r's receive
     buffer), every rank unpacks: the result equals ulysses_a2a_seq2head (and, back,
     ulysses_a2a_head2seq) bit for bit.
-(3) The forward over a process group of one rank (the only group one GPU can form) runs
-    the whole multi-process path and equals the single-process forward bit for bit."""
+(3) The forward, and the training forward and backward, over a process group of one rank
+    (the only group one GPU can form) run the whole multi-process path and equal the
+    single-process calls bit for bit."""
 
 import pytest
 import torch
@@ -71,7 +72,9 @@ def test_multi_process_forward_on_one_rank():
 
     import torch.distributed as dist
 
-    from sequence_attention_seq_gb300.multi import ulysses_dist_attn_fwd_multi
+    from sequence_attention_seq_gb300.inputs import global_grad
+    from sequence_attention_seq_gb300.multi import (ulysses_dist_attn_bwd_multi, ulysses_dist_attn_fwd_lse_multi,
+                                                    ulysses_dist_attn_fwd_multi)
 
     with socket.socket() as sk:
         sk.bind(("127.0.0.1", 0))
@@ -85,6 +88,16 @@ def test_multi_process_forward_on_one_rank():
             want = uly.ulysses_dist_attn_fwd(qs, ks, vs, causal)[0]
             torch.cuda.synchronize()
             assert bits_equal(got, want), f"causal={causal}"
+            # training: forward with statistics, then the backward through both exchanges
+            do = global_grad(2, 384, 4, 128, torch.bfloat16, seed=5, device="cuda")
+            o_m, saved = ulysses_dist_attn_fwd_lse_multi(qs[0], ks[0], vs[0], causal)
+            g_m = ulysses_dist_attn_bwd_multi(do, saved, causal)
+            o_s, lse_s = uly.ulysses_dist_attn_fwd_lse(qs, ks, vs, causal)
+            g_s = uly.ulysses_dist_attn_bwd(qs, ks, vs, o_s, [do], lse_s, causal)
+            torch.cuda.synchronize()
+            assert bits_equal(o_m, o_s[0]) and bits_equal(saved[4], lse_s[0])
+            for name, a, c in zip(("dq", "dk", "dv"), g_m, g_s):
+                assert bits_equal(a, c[0]), f"{name} causal={causal}"
     finally:
         dist.destroy_process_group()
     device_ok()
