@@ -21,6 +21,7 @@ cpu_baseline / --impl reference = the fp64 CPU oracle on a bounded sample of the
            (exact output rows, extrapolated to a rate).
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference] [--workload W]
+       python bench.py --permute-sweep | --exchange-kernels | --backward | --overlap | --usp
 Multi-GPU (torchrun): every rank runs an independent replica (the path needs no exchange
 between GPUs on this single-GPU emulation); value sums ranks over the slowest rank's time.
 """
@@ -532,6 +533,80 @@ def run_permute_sweep(args):
                       "all_bit_exact": all(r["round_trip_bit_exact"] for r in rows), "clocks": clk}))
 
 
+def run_exchange_kernels(args):
+    """The per-process halves of the exchange across GPUs (ulysses_a2a_pack before the
+    process-group all-to-all, ulysses_a2a_unpack after it) for one rank's bf16 shard
+    [1, s/P, 64, 128] (direction 0) or [1, s, 64/P, 128] (direction 1), kernels alone: 20
+    calls replayed from a CUDA graph between CUDA events.  Each call reads and writes the
+    shard once.  unpack(pack(x, 0), 1) == x and unpack(pack(y, 1), 0) == y are checked."""
+    import torch
+
+    import sequence_attention_seq_gb300 as uly
+    from sequence_attention_seq_gb300 import build as uly_build
+    from sequence_attention_seq_gb300.inputs import random_bits
+
+    uly_build.build()
+    peaks, _ = load_peaks()
+    h, d, reps = 64, 128, 20
+    shapes = [(s, P) for s in (131072, 262144) for P in (2, 4, 8, 16, 32, 64)]
+    if args.sweep_only:
+        shapes = [tuple(int(x) for x in item.split(",")) for item in args.sweep_only]
+    clocks = ClockSampler(0)
+    clocks.start()
+    time.sleep(0.3)
+    rows = []
+    for s, P in shapes:
+        S = s // P
+        seq = random_bits((1, S, h, d), torch.bfloat16, seed=s + P, device="cuda")
+        head = random_bits((1, s, h // P, d), torch.bfloat16, seed=s + P + 1, device="cuda")
+        send0 = torch.empty((P, 1, S, h // P, d), dtype=torch.bfloat16, device="cuda")
+        send1 = torch.empty_like(send0)
+        seq_back, head_back = torch.empty_like(seq), torch.empty_like(head)
+        nbytes = 2 * seq.numel() * 2
+        ops = (("pack_seq2head", lambda: uly.ulysses_a2a_pack(seq, 0, P, out=send0)),
+               ("unpack_seq2head", lambda: uly.ulysses_a2a_unpack(send1, 0, out=head_back)),
+               ("pack_head2seq", lambda: uly.ulysses_a2a_pack(head, 1, P, out=send1)),
+               ("unpack_head2seq", lambda: uly.ulysses_a2a_unpack(send0, 1, out=seq_back)))
+        row = {"s": s, "P": P, "shard_mib": seq.numel() * 2 / 2**20, "run_bytes": h // P * d * 2}
+        for name, fn in ops:
+            for _ in range(max(3, args.warmup)):
+                fn()
+            side = torch.cuda.Stream()
+            side.wait_stream(torch.cuda.current_stream())
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=side):
+                for _ in range(reps):
+                    fn()
+            graph.replay()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            graph.replay()
+            e1.record()
+            torch.cuda.synchronize()
+            row[name + "_gbs"] = nbytes / (e0.elapsed_time(e1) / reps * 1e-3) / 1e9
+            del graph
+        uly.ulysses_a2a_pack(seq, 0, P, out=send0)
+        uly.ulysses_a2a_unpack(send0, 1, out=seq_back)
+        uly.ulysses_a2a_pack(head, 1, P, out=send1)
+        uly.ulysses_a2a_unpack(send1, 0, out=head_back)
+        torch.cuda.synchronize()
+        row["round_trips_bit_exact"] = bool(torch.equal(seq.view(torch.int16), seq_back.view(torch.int16))
+                                            and torch.equal(head.view(torch.int16), head_back.view(torch.int16)))
+        rows.append(row)
+        print(json.dumps(row))
+        del seq, head, send0, send1, seq_back, head_back
+        torch.cuda.empty_cache()
+    clk = clocks.stop()
+    allv = [r[k + "_gbs"] for r in rows for k, _ in (("pack_seq2head", 0), ("unpack_seq2head", 0),
+                                                      ("pack_head2seq", 0), ("unpack_head2seq", 0))]
+    print(json.dumps({"metric": "per-process exchange kernels GB/s (read+write), one rank's bf16 shard",
+                      "unit": "GB/s", "min": min(allv), "median": statistics.median(allv), "max": max(allv),
+                      "peak": peaks["hbm_gbs"], "median_frac": statistics.median(allv) / peaks["hbm_gbs"],
+                      "min_frac": min(allv) / peaks["hbm_gbs"],
+                      "all_bit_exact": all(r["round_trips_bit_exact"] for r in rows), "clocks": clk}))
+
+
 def run_backward(args):
     """Backward of the Ulysses attention (not part of the default line): per mask, the local
     backward alone (row statistics + dK/dV + dQ kernels, head layout) and the whole
@@ -741,8 +816,10 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
     ap.add_argument("--permute-sweep", action="store_true",
                     help="measure the exchanges over the permute-only sweep instead of the forward")
+    ap.add_argument("--exchange-kernels", action="store_true",
+                    help="measure the per-process pack and unpack kernels of the exchange across GPUs")
     ap.add_argument("--sweep-only", nargs="*", metavar="S,P",
-                    help="with --permute-sweep: only these (sequence length, ranks) shapes")
+                    help="with --permute-sweep or --exchange-kernels: only these (sequence length, ranks) shapes")
     ap.add_argument("--backward", action="store_true",
                     help="measure the attention backward (local and distributed) instead of the forward")
     ap.add_argument("--usp", action="store_true",
@@ -770,6 +847,10 @@ def main():
     if args.permute_sweep:
         if rank == 0:
             run_permute_sweep(args)
+        return
+    if args.exchange_kernels:
+        if rank == 0:
+            run_exchange_kernels(args)
         return
     w = WORKLOADS[args.workload]
     esz = 2 if w["dtype"] == "bf16" else 4

@@ -93,7 +93,10 @@ uly_status ulysses_a2a_head2seq(int P, int b, int s, int h, int d, uly_dtype dty
  *                               local = this rank's seq shard [b][S][h][d].
  * pack(0), the collective and unpack(0) together give this rank's part of
  * ulysses_a2a_seq2head; pack(1), the collective and unpack(1) its part of
- * ulysses_a2a_head2seq.  Both sides hold b*S*h*d elements.  Sizes as the exchanges above.
+ * ulysses_a2a_head2seq.  Both sides hold b*S*h*d elements.  Sizes as the exchanges above;
+ * besides, the largest contiguous piece a call writes (b*S*H*d elements for pack(0),
+ * s*H*d for unpack(0), b*S*H*d for pack(1)) must fit in 2^31 - 1 copy vectors (16 bytes each
+ * when the rows and pointers are 16-byte aligned, else 8, 4, 2 or 1).  A larger piece,
  * direction not 0 or 1, a null or misaligned pointer, or overlapping in/out buffers give
  * ULY_ERR_INVALID_ARG.  Bit copies.  Device pointers, owned by the caller; enqueued on stream.
  */

@@ -161,17 +161,60 @@ def _dtype_code(t):
     return _DTYPES[t.dtype]
 
 
-def _same(tensors, what):
+def _same(tensors, what, n=None, shape=None, like=None, dtype=None):
+    """Checks a per-rank list of tensors and returns its first: n tensors (when n is given),
+    each contiguous, on one CUDA device, of one shape and dtype.  The shape is `shape` when
+    given, else the first tensor's; dtype and device are `like`'s when given (dtype may be
+    overridden), else the first tensor's.  The library only sees pointers and sizes, so a
+    list that is too short or a tensor of the wrong size must be stopped here."""
+    if n is not None and len(tensors) != n:
+        raise ValueError(f"{what}: {len(tensors)} tensors given for {n} ranks")
+    if len(tensors) == 0:
+        raise ValueError(f"{what}: no tensors given")
     t0 = tensors[0]
     if not t0.is_cuda:
         raise ValueError(f"{what}: tensors must live on a CUDA device")
-    # one pass of cheap attribute reads: with 64 ranks a call checks 128 tensors
-    shape, dtype, dev = t0.shape, t0.dtype, t0.get_device()
+    # one pass of cheap attribute reads: with 64 ranks a call checks several hundred tensors
+    ref = t0 if like is None else like
+    want_shape = t0.shape if shape is None else torch.Size(shape)
+    want_dtype = ref.dtype if dtype is None else dtype
+    dev = ref.get_device()
     for t in tensors:
-        if t.shape != shape or t.dtype is not dtype or t.get_device() != dev or not t.is_cuda \
+        if t.shape != want_shape or t.dtype is not want_dtype or t.get_device() != dev or not t.is_cuda \
                 or not t.is_contiguous():
-            raise ValueError(f"{what}: every rank needs a contiguous tensor of one shape, dtype and device")
+            raise ValueError(f"{what}: every rank needs a contiguous {want_dtype} tensor of shape "
+                             f"{tuple(want_shape)} on cuda:{dev}")
     return t0
+
+
+def _workspace(workspace, like, what="workspace"):
+    """(pointer, bytes) of a caller's workspace: a contiguous tensor on `like`'s device."""
+    if workspace is None:
+        return None, 0
+    if not workspace.is_cuda or workspace.get_device() != like.get_device() or not workspace.is_contiguous():
+        raise ValueError(f"{what}: a contiguous tensor on cuda:{like.get_device()} is needed")
+    return workspace.data_ptr(), workspace.numel() * workspace.element_size()
+
+
+def _kv_heads(tensors, what):
+    """The head count (dimension 2) of a per-rank list of [b, tokens, heads, d] tensors."""
+    if len(tensors) == 0 or tensors[0].dim() != 4:
+        raise ValueError(f"{what}: per-rank tensors [b, tokens, heads, d] are needed")
+    return tensors[0].shape[2]
+
+
+def _seq_qkv(q_seq, k_seq, v_seq):
+    """Checks seq-layout Q [b, s/P, h_q, d] and K, V [b, s/P, h_kv, d] of P ranks; returns
+    (first Q tensor, P, b, s, h_q, h_kv, d)."""
+    q0 = _same(q_seq, "q_seq")
+    if q0.dim() != 4:
+        raise ValueError("q_seq: per-rank tensors [b, s/P, h_q, d] are needed")
+    P = len(q_seq)
+    b, S, hq, d = q0.shape
+    hkv = _kv_heads(k_seq, "k_seq")
+    _same(k_seq, "k_seq", P, (b, S, hkv, d), q0)
+    _same(v_seq, "v_seq", P, (b, S, hkv, d), q0)
+    return q0, P, b, S * P, hq, hkv, d
 
 
 def ulysses_a2a_seq2head(in_seq, out_head=None, stream=None):
@@ -181,7 +224,7 @@ def ulysses_a2a_seq2head(in_seq, out_head=None, stream=None):
     b, S, h, d = t0.shape
     if out_head is None:
         out_head = [torch.empty((b, S * P, h // P, d), dtype=t0.dtype, device=t0.device) for _ in range(P)]
-    _same(out_head, "out_head")
+    _same(out_head, "out_head", P, (b, S * P, h // P, d), t0)
     _check(load_library().ulysses_a2a_seq2head(P, b, S * P, h, d, _dtype_code(t0), _ptr_array(in_seq),
                                                _ptr_array(out_head), _stream(stream)), "ulysses_a2a_seq2head")
     return out_head
@@ -194,7 +237,7 @@ def ulysses_a2a_head2seq(in_head, out_seq=None, stream=None):
     b, s, H, d = t0.shape
     if out_seq is None:
         out_seq = [torch.empty((b, s // P, H * P, d), dtype=t0.dtype, device=t0.device) for _ in range(P)]
-    _same(out_seq, "out_seq")
+    _same(out_seq, "out_seq", P, (b, s // P, H * P, d), t0)
     _check(load_library().ulysses_a2a_head2seq(P, b, s, H * P, d, _dtype_code(t0), _ptr_array(in_head),
                                                _ptr_array(out_seq), _stream(stream)), "ulysses_a2a_head2seq")
     return out_seq
@@ -215,7 +258,7 @@ def ulysses_a2a_pack(local, direction, P, out=None, stream=None):
         raise ValueError("direction must be 0 (seq -> head) or 1 (head -> seq)")
     if out is None:
         out = torch.empty((P, b, S, h // P, d), dtype=local.dtype, device=local.device)
-    _same([out], "out")
+    _same([out], "out", 1, (P, b, S, h // P, d), local)
     _check(load_library().ulysses_a2a_pack(direction, P, b, s, h, d, _dtype_code(local), local.data_ptr(),
                                            out.data_ptr(), _stream(stream)), "ulysses_a2a_pack")
     return out
@@ -232,7 +275,7 @@ def ulysses_a2a_unpack(recv, direction, out=None, stream=None):
     shape = (b, S * P, H, d) if direction == 0 else (b, S, H * P, d)
     if out is None:
         out = torch.empty(shape, dtype=recv.dtype, device=recv.device)
-    _same([out], "out")
+    _same([out], "out", 1, shape, recv)
     _check(load_library().ulysses_a2a_unpack(direction, P, b, S * P, H * P, d, _dtype_code(recv), recv.data_ptr(),
                                              out.data_ptr(), _stream(stream)), "ulysses_a2a_unpack")
     return out
@@ -241,13 +284,14 @@ def ulysses_a2a_unpack(recv, direction, out=None, stream=None):
 def ulysses_local_attention(q_head, k_head, v_head, causal, out_head=None, stream=None):
     """Attention of every rank in head layout: softmax(Q K^T / sqrt(d)) V per local head."""
     q0 = _same(q_head, "q_head")
-    k0 = _same(k_head, "k_head")
-    _same(v_head, "v_head")
     P = len(q_head)
     b, s, Hq, d = q0.shape
-    Hk = k0.shape[2]
+    Hk = _kv_heads(k_head, "k_head")
+    _same(k_head, "k_head", P, (b, s, Hk, d), q0)
+    _same(v_head, "v_head", P, (b, s, Hk, d), q0)
     if out_head is None:
         out_head = [torch.empty_like(q) for q in q_head]
+    _same(out_head, "out_head", P, q0.shape, q0)
     _check(load_library().ulysses_local_attention(
         P, b, s, Hq * P, Hk * P, d, _dtype_code(q0), int(bool(causal)), _ptr_array(q_head), _ptr_array(k_head),
         _ptr_array(v_head), _ptr_array(out_head), _stream(stream)), "ulysses_local_attention")
@@ -264,20 +308,14 @@ def ulysses_dist_attn_fwd(q_seq, k_seq, v_seq, causal, fused=False, out_seq=None
     q_seq / k_seq / v_seq: P tensors [b, s/P, heads, d]; returns P tensors [b, s/P, h_q, d].
     ``workspace`` (a uint8 CUDA tensor) is allocated when not given and fused is False.
     """
-    q0 = _same(q_seq, "q_seq")
-    k0 = _same(k_seq, "k_seq")
-    _same(v_seq, "v_seq")
-    P = len(q_seq)
-    b, S, hq, d = q0.shape
-    hkv = k0.shape[2]
-    s = S * P
+    q0, P, b, s, hq, hkv, d = _seq_qkv(q_seq, k_seq, v_seq)
     if out_seq is None:
         out_seq = [torch.empty_like(q) for q in q_seq]
+    _same(out_seq, "out_seq", P, q0.shape, q0)
     need = ulysses_dist_attn_workspace_bytes(P, b, s, hq, hkv, d, q0.dtype, fused)
     if workspace is None and need:
         workspace = torch.empty(need, dtype=torch.uint8, device=q0.device)
-    ws_ptr = workspace.data_ptr() if workspace is not None else None
-    ws_len = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    ws_ptr, ws_len = _workspace(workspace, q0)
     _check(load_library().ulysses_dist_attn_fwd(
         P, b, s, hq, hkv, d, _dtype_code(q0), int(bool(causal)), _ptr_array(q_seq), _ptr_array(k_seq),
         _ptr_array(v_seq), _ptr_array(out_seq), ws_ptr, ws_len, int(bool(fused)), _stream(stream)),
@@ -302,14 +340,10 @@ def ulysses_dist_attn_fwd_noalloc(q_seq, k_seq, v_seq, causal, out_seq, stream=N
     Calls that would need more than NOALLOC_SCRATCH_BYTES of scratch raise.  Calls that
     overlap on the GPU share the scratch and race; serialise them.
     """
-    q0 = _same(q_seq, "q_seq")
-    k0 = _same(k_seq, "k_seq")
-    _same(v_seq, "v_seq")
-    _same(out_seq, "out_seq")
-    P = len(q_seq)
-    b, S, hq, d = q0.shape
+    q0, P, b, s, hq, hkv, d = _seq_qkv(q_seq, k_seq, v_seq)
+    _same(out_seq, "out_seq", P, q0.shape, q0)
     _check(load_library().ulysses_dist_attn_fwd_noalloc(
-        P, b, S * P, hq, k0.shape[2], d, _dtype_code(q0), int(bool(causal)), _ptr_array(q_seq), _ptr_array(k_seq),
+        P, b, s, hq, hkv, d, _dtype_code(q0), int(bool(causal)), _ptr_array(q_seq), _ptr_array(k_seq),
         _ptr_array(v_seq), _ptr_array(out_seq), _stream(stream)), "ulysses_dist_attn_fwd_noalloc")
     return out_seq
 
@@ -324,16 +358,19 @@ def ulysses_local_attention_fwd_lse(q_head, k_head, v_head, causal, out_head=Non
     """ulysses_local_attention plus the per-row log-sum-exp: returns (o_head, lse), lse being
     P fp32 tensors [b, h_q/P, s] (natural log of the sum of exp of the scaled scores)."""
     q0 = _same(q_head, "q_head")
-    k0 = _same(k_head, "k_head")
-    _same(v_head, "v_head")
     P = len(q_head)
     b, s, Hq, d = q0.shape
+    Hk = _kv_heads(k_head, "k_head")
+    _same(k_head, "k_head", P, (b, s, Hk, d), q0)
+    _same(v_head, "v_head", P, (b, s, Hk, d), q0)
     if out_head is None:
         out_head = [torch.empty_like(q) for q in q_head]
+    _same(out_head, "out_head", P, q0.shape, q0)
     if lse is None:
         lse = [_rows_like(q0.shape, q0.device) for _ in range(P)]
+    _same(lse, "lse", P, (b, Hq, s), q0, torch.float32)
     _check(load_library().ulysses_local_attention_fwd_lse(
-        P, b, s, Hq * P, k0.shape[2] * P, d, _dtype_code(q0), int(bool(causal)), _ptr_array(q_head),
+        P, b, s, Hq * P, Hk * P, d, _dtype_code(q0), int(bool(causal)), _ptr_array(q_head),
         _ptr_array(k_head), _ptr_array(v_head), _ptr_array(out_head), _ptr_array(lse), _stream(stream)),
         "ulysses_local_attention_fwd_lse")
     return out_head, lse
@@ -343,22 +380,17 @@ def ulysses_dist_attn_fwd_lse(q_seq, k_seq, v_seq, causal, fused=False, out_seq=
                               stream=None):
     """The forward plus the log-sum-exp of every head rank's rows: returns (o_seq, lse) with
     lse P fp32 tensors [b, h_q/P, s] indexed like the head layout."""
-    q0 = _same(q_seq, "q_seq")
-    k0 = _same(k_seq, "k_seq")
-    _same(v_seq, "v_seq")
-    P = len(q_seq)
-    b, S, hq, d = q0.shape
-    hkv = k0.shape[2]
-    s = S * P
+    q0, P, b, s, hq, hkv, d = _seq_qkv(q_seq, k_seq, v_seq)
     if out_seq is None:
         out_seq = [torch.empty_like(q) for q in q_seq]
+    _same(out_seq, "out_seq", P, q0.shape, q0)
     if lse is None:
         lse = [torch.empty((b, hq // P, s), dtype=torch.float32, device=q0.device) for _ in range(P)]
+    _same(lse, "lse", P, (b, hq // P, s), q0, torch.float32)
     need = ulysses_dist_attn_workspace_bytes(P, b, s, hq, hkv, d, q0.dtype, fused)
     if workspace is None and need:
         workspace = torch.empty(need, dtype=torch.uint8, device=q0.device)
-    ws_ptr = workspace.data_ptr() if workspace is not None else None
-    ws_len = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    ws_ptr, ws_len = _workspace(workspace, q0)
     _check(load_library().ulysses_dist_attn_fwd_lse(
         P, b, s, hq, hkv, d, _dtype_code(q0), int(bool(causal)), _ptr_array(q_seq), _ptr_array(k_seq),
         _ptr_array(v_seq), _ptr_array(out_seq), _ptr_array(lse), ws_ptr, ws_len, int(bool(fused)), _stream(stream)),
@@ -373,27 +405,31 @@ def ulysses_attn_bwd_workspace_bytes(P, b, s, h_q, h_kv, d, dtype, dist, fused=F
 
 def _bwd_call(name, dist, q, k, v, o, do, lse, causal, grads, workspace, stream, fused=False):
     q0 = _same(q, "q")
-    k0 = _same(k, "k")
-    _same(v, "v")
-    _same(o, "o")
-    _same(do, "do")
-    _same(lse, "lse")
     P = len(q)
+    b, T, Hq, d = q0.shape  # T tokens (s/P seq layout, s head layout), Hq heads of the layout
+    Hk = _kv_heads(k, "k")
+    _same(k, "k", P, (b, T, Hk, d), q0)
+    _same(v, "v", P, (b, T, Hk, d), q0)
+    _same(o, "o", P, q0.shape, q0)
+    _same(do, "do", P, q0.shape, q0)
     if dist:
-        b, S, hq, d = q0.shape
-        s, hkv = S * P, k0.shape[2]
+        s, hq, hkv = T * P, Hq, Hk
     else:
-        b, s, Hq, d = q0.shape
-        hq, hkv = Hq * P, k0.shape[2] * P
+        s, hq, hkv = T, Hq * P, Hk * P
+    _same(lse, "lse", P, (b, hq // P, s), q0, torch.float32)
     if grads is None:
         grads = ([torch.empty_like(x) for x in q], [torch.empty_like(x) for x in k], [torch.empty_like(x) for x in v])
+    dq, dk, dv = grads
+    _same(dq, "dq", P, q0.shape, q0)
+    _same(dk, "dk", P, (b, T, Hk, d), q0)
+    _same(dv, "dv", P, (b, T, Hk, d), q0)
     need = ulysses_attn_bwd_workspace_bytes(P, b, s, hq, hkv, d, q0.dtype, dist, fused)
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q0.device)
-    dq, dk, dv = grads
+    ws_ptr, ws_len = _workspace(workspace, q0)
     args = [P, b, s, hq, hkv, d, _dtype_code(q0), int(bool(causal)), _ptr_array(q), _ptr_array(k), _ptr_array(v),
             _ptr_array(o), _ptr_array(do), _ptr_array(lse), _ptr_array(dq), _ptr_array(dk), _ptr_array(dv),
-            workspace.data_ptr(), workspace.numel() * workspace.element_size()]
+            ws_ptr, ws_len]
     if dist:
         args.append(int(bool(fused)))
     _check(getattr(load_library(), name)(*args, _stream(stream)), name)
@@ -436,22 +472,18 @@ def ulysses_dist_attn_fwd_overlap(q_seq, k_seq, v_seq, causal, n_chunks=2, out_s
                                   stream=None, side_stream=None):
     """The unfused forward with the exchanges of one head group overlapped with the attention
     of the next (n_chunks head groups); same results, bit for bit, as ulysses_dist_attn_fwd."""
-    q0 = _same(q_seq, "q_seq")
-    k0 = _same(k_seq, "k_seq")
-    _same(v_seq, "v_seq")
-    P = len(q_seq)
-    b, S, hq, d = q0.shape
-    hkv = k0.shape[2]
-    s = S * P
+    q0, P, b, s, hq, hkv, d = _seq_qkv(q_seq, k_seq, v_seq)
     if out_seq is None:
         out_seq = [torch.empty_like(q) for q in q_seq]
+    _same(out_seq, "out_seq", P, q0.shape, q0)
     if workspace is None:
         need = ulysses_dist_attn_overlap_workspace_bytes(P, b, s, hq, hkv, d, q0.dtype, n_chunks)
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q0.device)
+    ws_ptr, ws_len = _workspace(workspace, q0)
     side = side_stream if side_stream is not None else _side_stream(q0.device)
     _check(load_library().ulysses_dist_attn_fwd_overlap(
         P, b, s, hq, hkv, d, _dtype_code(q0), int(bool(causal)), _ptr_array(q_seq), _ptr_array(k_seq),
-        _ptr_array(v_seq), _ptr_array(out_seq), workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+        _ptr_array(v_seq), _ptr_array(out_seq), ws_ptr, ws_len,
         int(n_chunks), _stream(stream), ctypes.c_void_p(side.cuda_stream)), "ulysses_dist_attn_fwd_overlap")
     return out_seq
 
@@ -465,24 +497,19 @@ def ulysses_usp_attn_fwd(q_seq, k_seq, v_seq, causal, Pu, Pr, out_seq=None, work
     """The two-level forward over P = Pu*Pr seq-partitioned ranks (rank j = g*Pu + u):
     all-to-all inside groups of Pu ranks, attention with the ring groups' K/V blocks,
     all-to-all back.  Returns P tensors [b, s/P, h_q, d]."""
-    q0 = _same(q_seq, "q_seq")
-    k0 = _same(k_seq, "k_seq")
-    _same(v_seq, "v_seq")
-    P = len(q_seq)
+    q0, P, b, s, hq, hkv, d = _seq_qkv(q_seq, k_seq, v_seq)
     if P != Pu * Pr:
         raise ValueError(f"{P} ranks given for Pu={Pu} x Pr={Pr}")
-    b, S, hq, d = q0.shape
-    hkv = k0.shape[2]
-    s = S * P
     if out_seq is None:
         out_seq = [torch.empty_like(q) for q in q_seq]
+    _same(out_seq, "out_seq", P, q0.shape, q0)
     if workspace is None:
         need = ulysses_usp_workspace_bytes(Pu, Pr, b, s, hq, hkv, d, q0.dtype)
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q0.device)
+    ws_ptr, ws_len = _workspace(workspace, q0)
     _check(load_library().ulysses_usp_attn_fwd(
         Pu, Pr, b, s, hq, hkv, d, _dtype_code(q0), int(bool(causal)), _ptr_array(q_seq), _ptr_array(k_seq),
-        _ptr_array(v_seq), _ptr_array(out_seq), workspace.data_ptr(), workspace.numel() * workspace.element_size(),
-        _stream(stream)), "ulysses_usp_attn_fwd")
+        _ptr_array(v_seq), _ptr_array(out_seq), ws_ptr, ws_len, _stream(stream)), "ulysses_usp_attn_fwd")
     return out_seq
 
 
@@ -490,28 +517,23 @@ def ulysses_usp_attn_fwd_lse(q_seq, k_seq, v_seq, causal, Pu, Pr, out_seq=None, 
                              stream=None):
     """The two-level forward plus its softmax statistics: returns (o_seq, lse) with lse Pu
     fp32 tensors [b, h_q/Pu, s] (Ulysses unit u's heads, every position)."""
-    q0 = _same(q_seq, "q_seq")
-    k0 = _same(k_seq, "k_seq")
-    _same(v_seq, "v_seq")
-    P = len(q_seq)
+    q0, P, b, s, hq, hkv, d = _seq_qkv(q_seq, k_seq, v_seq)
     if P != Pu * Pr:
         raise ValueError(f"{P} ranks given for Pu={Pu} x Pr={Pr}")
-    b, S, hq, d = q0.shape
-    hkv = k0.shape[2]
-    s = S * P
     if out_seq is None:
         out_seq = [torch.empty_like(q) for q in q_seq]
+    _same(out_seq, "out_seq", P, q0.shape, q0)
     if lse is None:
         lse = [torch.empty((b, hq // Pu, s), dtype=torch.float32, device=q0.device) for _ in range(Pu)]
-    if len(lse) != Pu:
-        raise ValueError(f"{len(lse)} statistics arrays given for Pu={Pu}")
+    _same(lse, "lse", Pu, (b, hq // Pu, s), q0, torch.float32)
     if workspace is None:
         need = ulysses_usp_workspace_bytes(Pu, Pr, b, s, hq, hkv, d, q0.dtype)
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q0.device)
+    ws_ptr, ws_len = _workspace(workspace, q0)
     _check(load_library().ulysses_usp_attn_fwd_lse(
         Pu, Pr, b, s, hq, hkv, d, _dtype_code(q0), int(bool(causal)), _ptr_array(q_seq), _ptr_array(k_seq),
-        _ptr_array(v_seq), _ptr_array(out_seq), _ptr_array(lse), workspace.data_ptr(),
-        workspace.numel() * workspace.element_size(), _stream(stream)), "ulysses_usp_attn_fwd_lse")
+        _ptr_array(v_seq), _ptr_array(out_seq), _ptr_array(lse), ws_ptr, ws_len, _stream(stream)),
+        "ulysses_usp_attn_fwd_lse")
     return out_seq, lse
 
 
@@ -522,30 +544,27 @@ def ulysses_usp_bwd_workspace_bytes(Pu, Pr, b, s, h_q, h_kv, d, dtype):
 def ulysses_usp_attn_bwd(q_seq, k_seq, v_seq, o_seq, do_seq, lse, causal, Pu, Pr, grads=None, workspace=None,
                          stream=None):
     """Backward of the two-level forward, seq layout in and out: returns (dq, dk, dv)."""
-    q0 = _same(q_seq, "q_seq")
-    k0 = _same(k_seq, "k_seq")
-    _same(v_seq, "v_seq")
-    _same(o_seq, "o_seq")
-    _same(do_seq, "do_seq")
-    _same(lse, "lse")
-    P = len(q_seq)
-    if P != Pu * Pr or len(lse) != Pu:
-        raise ValueError(f"{P} ranks and {len(lse)} statistics arrays given for Pu={Pu} x Pr={Pr}")
-    b, S, hq, d = q0.shape
-    hkv = k0.shape[2]
-    s = S * P
+    q0, P, b, s, hq, hkv, d = _seq_qkv(q_seq, k_seq, v_seq)
+    if P != Pu * Pr:
+        raise ValueError(f"{P} ranks given for Pu={Pu} x Pr={Pr}")
+    _same(o_seq, "o_seq", P, q0.shape, q0)
+    _same(do_seq, "do_seq", P, q0.shape, q0)
+    _same(lse, "lse", Pu, (b, hq // Pu, s), q0, torch.float32)
     if grads is None:
         grads = ([torch.empty_like(x) for x in q_seq], [torch.empty_like(x) for x in k_seq],
                  [torch.empty_like(x) for x in v_seq])
+    dq, dk, dv = grads
+    _same(dq, "dq", P, q0.shape, q0)
+    _same(dk, "dk", P, k_seq[0].shape, q0)
+    _same(dv, "dv", P, k_seq[0].shape, q0)
     if workspace is None:
         need = ulysses_usp_bwd_workspace_bytes(Pu, Pr, b, s, hq, hkv, d, q0.dtype)
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q0.device)
-    dq, dk, dv = grads
+    ws_ptr, ws_len = _workspace(workspace, q0)
     _check(load_library().ulysses_usp_attn_bwd(
         Pu, Pr, b, s, hq, hkv, d, _dtype_code(q0), int(bool(causal)), _ptr_array(q_seq), _ptr_array(k_seq),
         _ptr_array(v_seq), _ptr_array(o_seq), _ptr_array(do_seq), _ptr_array(lse), _ptr_array(dq), _ptr_array(dk),
-        _ptr_array(dv), workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream(stream)),
-        "ulysses_usp_attn_bwd")
+        _ptr_array(dv), ws_ptr, ws_len, _stream(stream)), "ulysses_usp_attn_bwd")
     return dq, dk, dv
 
 

@@ -391,6 +391,7 @@ static uly_status a2a_local(int pack, int direction, int P, int b, int s, int h,
     } else {                              // received blocks [P][b*S][H*d] -> seq shard [b*S][P][H*d]
         A = P, C = (uint64_t)b * S, run = head_run;
     }
+    if (!uly::block_transpose_fits(A, C, run, in, out)) return ULY_ERR_INVALID_ARG;
     return uly::launch_block_transpose(A, C, run, in, out, stream) == cudaSuccess ? ULY_OK : ULY_ERR_CUDA;
 }
 

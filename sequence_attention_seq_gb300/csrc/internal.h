@@ -35,6 +35,9 @@ cudaError_t launch_permute(int direction, int P, int b, int s, int d, int elem_b
 
 // out[c][a] = in[a][c] for A x C runs of run_bytes each: the local halves of one rank's
 // all-to-all with other GPUs (the send blocks before the collective, the layout after it).
+// block_transpose_fits: false when a slab (A runs) would exceed the kernel's 32-bit vector
+// index (2^31 - 1 vectors of up to 16 bytes); launch_block_transpose then refuses the copy.
+bool block_transpose_fits(uint64_t A, uint64_t C, uint64_t run_bytes, const void* in, const void* out);
 cudaError_t launch_block_transpose(uint64_t A, uint64_t C, uint64_t run_bytes, const void* in, void* out,
                                    cudaStream_t stream);
 

@@ -266,35 +266,42 @@ cudaError_t launch_kv_grad_sum(int P, int rep, int b, int s, int h_kv, int d, co
 namespace {
 
 // out[c][a] = in[a][c] for runs of run_bytes (a < A, c < C): the local halves of one rank's
-// all-to-all with other GPUs (see launch_block_transpose).  grid.y walks the (a, c) runs,
-// grid.x the vectors inside a run.
+// all-to-all with other GPUs (see launch_block_transpose).  Slab c = the A runs that land
+// contiguously at out[c][0..A); they lie C runs apart in `in`.  grid.y walks the slabs,
+// grid.x the vectors of a slab (read strided, written contiguously), as permute_kernel
+// does, so small runs (a few KB) still give every thread four vectors in flight.
 struct BlockTransposeParams {
     const uint8_t* in;
     uint8_t* out;
-    uint64_t run_bytes;
-    uint32_t A, C, run_vecs;
+    uint64_t run_bytes;   // bytes of one run
+    uint64_t in_pitch;    // C * run_bytes: from in[a][c] to in[a+1][c]
+    uint64_t slab_bytes;  // A * run_bytes
+    uint32_t C;
+    uint32_t slab_vecs;   // A * run_bytes / VEC
+    FastDiv run_vecs;     // run_bytes / VEC
 };
 
 template <int VEC>
 __global__ void __launch_bounds__(kThreads) block_transpose_kernel(const __grid_constant__ BlockTransposeParams p) {
     using V = typename VecT<VEC>::T;
-    const uint64_t runs = (uint64_t)p.A * p.C;
-    for (uint64_t y = blockIdx.y; y < runs; y += gridDim.y) {
-        const uint64_t a = y / p.C, c = y - a * p.C;
-        const uint8_t* src = p.in + y * p.run_bytes;              // in[a][c]
-        uint8_t* dst = p.out + (c * p.A + a) * p.run_bytes;       // out[c][a]
-        for (uint32_t i0 = blockIdx.x * (kThreads * kUnroll) + threadIdx.x; i0 < p.run_vecs;
+    for (uint32_t c = blockIdx.y; c < p.C; c += gridDim.y) {
+        const uint8_t* src = p.in + (uint64_t)c * p.run_bytes;  // in[0][c]
+        uint8_t* dst = p.out + (uint64_t)c * p.slab_bytes;      // out[c][0]
+        const uint32_t n = p.slab_vecs;
+        for (uint32_t i0 = blockIdx.x * (kThreads * kUnroll) + threadIdx.x; i0 < n;
              i0 += gridDim.x * (kThreads * kUnroll)) {
             V val[kUnroll];
 #pragma unroll
             for (int k = 0; k < kUnroll; ++k) {
                 const uint32_t i = i0 + k * kThreads;
-                if (i < p.run_vecs) val[k] = load_stream<V>(src + (uint64_t)i * VEC);
+                const uint32_t a = fdiv(i, p.run_vecs);
+                const uint32_t col = i - a * p.run_vecs.d;
+                if (i < n) val[k] = load_stream<V>(src + (uint64_t)a * p.in_pitch + (uint64_t)col * VEC);
             }
 #pragma unroll
             for (int k = 0; k < kUnroll; ++k) {
                 const uint32_t i = i0 + k * kThreads;
-                if (i < p.run_vecs) *reinterpret_cast<V*>(dst + (uint64_t)i * VEC) = val[k];
+                if (i < n) *reinterpret_cast<V*>(dst + (uint64_t)i * VEC) = val[k];
             }
         }
     }
@@ -302,14 +309,13 @@ __global__ void __launch_bounds__(kThreads) block_transpose_kernel(const __grid_
 
 template <int VEC>
 cudaError_t launch_bt(const BlockTransposeParams& prm, cudaStream_t stream) {
-    const uint64_t runs = (uint64_t)prm.A * prm.C;
-    const uint32_t grid_y = runs < 65535u ? (uint32_t)runs : 65535u;
+    const uint32_t grid_y = prm.C < 65535u ? prm.C : 65535u;
     int dev = 0, sms = 152;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const uint64_t per_run = (prm.run_vecs + (uint64_t)kThreads * kUnroll - 1) / ((uint64_t)kThreads * kUnroll);
+    const uint64_t per_slab = (prm.slab_vecs + (uint64_t)kThreads * kUnroll - 1) / ((uint64_t)kThreads * kUnroll);
     uint64_t gx = ((uint64_t)sms * 8 + grid_y - 1) / grid_y;  // one wave of 8 blocks per SM
-    if (gx > per_run) gx = per_run;
+    if (gx > per_slab) gx = per_slab;
     if (gx < 1) gx = 1;
     if (gx > 65535) gx = 65535;
     block_transpose_kernel<VEC><<<dim3((unsigned)gx, grid_y, 1), kThreads, 0, stream>>>(prm);
@@ -318,21 +324,35 @@ cudaError_t launch_bt(const BlockTransposeParams& prm, cudaStream_t stream) {
 
 }  // namespace
 
-cudaError_t launch_block_transpose(uint64_t A, uint64_t C, uint64_t run_bytes, const void* in, void* out,
-                                   cudaStream_t stream) {
-    if (A == 0 || C == 0 || run_bytes == 0) return cudaSuccess;
-    if (A > 0xffffffffull || C > 0xffffffffull) return cudaErrorInvalidValue;
+static int block_transpose_vec(uint64_t run_bytes, const void* in, const void* out) {
     int vec = 16;
     while (vec > 1 && (run_bytes % vec || (reinterpret_cast<uintptr_t>(in) | reinterpret_cast<uintptr_t>(out)) % vec))
         vec >>= 1;
-    if (run_bytes / vec > 0xffffffffull) return cudaErrorInvalidValue;
+    return vec;
+}
+
+// A slab's vector index is 32-bit: at most 2^31 - 1 vectors, so that the grid-stride steps
+// past the end never wrap.
+bool block_transpose_fits(uint64_t A, uint64_t C, uint64_t run_bytes, const void* in, const void* out) {
+    if (A == 0 || C == 0 || run_bytes == 0) return true;
+    const uint64_t rv = run_bytes / block_transpose_vec(run_bytes, in, out);
+    return C <= 0xffffffffull && rv <= 0x7fffffffull && A <= 0x7fffffffull / rv;
+}
+
+cudaError_t launch_block_transpose(uint64_t A, uint64_t C, uint64_t run_bytes, const void* in, void* out,
+                                   cudaStream_t stream) {
+    if (A == 0 || C == 0 || run_bytes == 0) return cudaSuccess;
+    if (!block_transpose_fits(A, C, run_bytes, in, out)) return cudaErrorInvalidValue;
+    const int vec = block_transpose_vec(run_bytes, in, out);
     BlockTransposeParams prm;
     prm.in = static_cast<const uint8_t*>(in);
     prm.out = static_cast<uint8_t*>(out);
     prm.run_bytes = run_bytes;
-    prm.A = (uint32_t)A;
+    prm.in_pitch = C * run_bytes;
+    prm.slab_bytes = A * run_bytes;
     prm.C = (uint32_t)C;
-    prm.run_vecs = (uint32_t)(run_bytes / vec);
+    prm.slab_vecs = (uint32_t)(A * (run_bytes / vec));
+    prm.run_vecs = make_fastdiv((uint32_t)(run_bytes / vec));
     switch (vec) {
         case 16: return launch_bt<16>(prm, stream);
         case 8: return launch_bt<8>(prm, stream);

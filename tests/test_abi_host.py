@@ -168,3 +168,7 @@ def test_pack_unpack_argument_errors(lib):
         assert f(0, 2, 1, 64, 4, 16, FP32, A + 4, B, None) == INVALID   # misaligned
         assert f(0, 2, 1, 64, 4, 16, FP32, A, A + 1024, None) == INVALID  # out overlaps in (4 KB each side)
         assert f(0, 65, 1, 65, 65, 16, FP32, A, B, None) == INVALID     # P > 64
+    # unpack(0) writes one piece of s*H*d elements: 2^26 tokens x 1 head x 256 fp32 is 2^32
+    # 16-byte vectors, past the copy kernel's 32-bit index (the per-rank exchange checks pass)
+    far_in, far_out = 1 << 48, 1 << 49  # 64 GiB each side: far apart so that they do not overlap
+    assert lib.ulysses_a2a_unpack(0, 64, 1, 1 << 26, 64, 256, FP32, far_in, far_out, None) == INVALID
