@@ -381,7 +381,7 @@ uly_status ulysses_local_attention_bwd(int P, int b, int s, int h_q, int h_kv, i
  *   tiles straight from the seq-layout buffers and write dQ/dK/dV rows straight into the
  *   seq-layout outputs, so no head-layout copy exists (the backward of the fused
  *   forward).  Needs P <= 48 and (s/P) % 128 == 0, else ULY_ERR_UNSUPPORTED.  Both paths
- *   give the same bits.
+ *   give the same bits where h_kv % P == 0 (for replicated K/V heads, see below).
  *   q_seq, o_seq, do_seq, dq_seq: P pointers to [b][s/P][h_q][d];
  *   k_seq, v_seq, dk_seq, dv_seq: P pointers to [b][s/P][h_kv][d];
  *   lse: from ulysses_dist_attn_fwd_lse (head-layout indexed).
@@ -389,7 +389,8 @@ uly_status ulysses_local_attention_bwd(int P, int b, int s, int h_q, int h_kv, i
  *   the shares of its rep ranks.  fused == 0 writes the shares in fp32 and adds them in
  *   a fixed order before one rounding to bf16 (the reverse of the broadcast); fused != 0
  *   needs no sum, since its dK/dV kernel owns every global K/V head and reads all of that
- *   head's query heads.
+ *   head's query heads.  The two orders of summation round differently, so there dK and
+ *   dV of the two paths may differ in the last bits (dQ and the forward do not).
  * workspace: 256-byte aligned, at least ulysses_attn_bwd_workspace_bytes(..., dist = 1,
  * fused) bytes.  Size and overlap rules as ulysses_local_attention_bwd plus the exchange rules.
  */
