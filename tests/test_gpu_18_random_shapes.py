@@ -121,3 +121,109 @@ def test_the_draw_covers_the_shape_classes():
     assert any(hkv < P for P, _, _, _, hkv, *_ in cases)
     assert any(hq > hkv for _, _, _, hq, hkv, *_ in cases)
     assert any(c for *_, c in cases) and any(not c for *_, c in cases)
+
+
+def _fp32_cases(seed, n):
+    rng = random.Random(seed)
+    out = []
+    while len(out) < n:
+        P = rng.choice([1, 2, 3, 4])
+        hkv = P * rng.choice([1, 2])
+        hq = hkv * rng.choice([1, 2])
+        d = 4 * rng.randint(1, 64)            # any multiple of 4 up to 256
+        s = P * rng.randint(1, 160 // P)
+        if hq * s * s * d <= 1 << 26:
+            out.append((P, 1, s, hq, hkv, d, rng.random() < 0.5))
+    return out
+
+
+@pytest.mark.parametrize("P,b,s,hq,hkv,d,causal", _fp32_cases(seed=77, n=10))
+def test_random_forward_fp32(P, b, s, hq, hkv, d, causal):
+    """The fp32 path (any d that is a multiple of 4) against the oracle at 1e-5."""
+    need_gpu()
+    q, k, v = global_qkv(b, s, hq, hkv, d, torch.float32, seed=s + d)
+    qs, ks, vs = shard_seq(q, P), shard_seq(k, P), shard_seq(v, P)
+    out = uly.ulysses_dist_attn_fwd([t.cuda() for t in qs], [t.cuda() for t in ks], [t.cuda() for t in vs], causal)
+    torch.cuda.synchronize()
+    device_ok()
+    want = oracle.dist_attn_fwd(qs, ks, vs, causal)
+    for j in range(P):
+        assert_close(out[j], want[j], torch.float32, f"rank {j}")
+
+
+def _overlap_cases(seed, n):
+    """Drawn FWD-style shapes with a valid head-group count for the overlapped forward."""
+    rng = random.Random(seed)
+    out = []
+    for P, b, s, hq, hkv, d, causal in _cases(seed, 4 * n, 1024, 1 << 29, 16):
+        Hq, Hk = hq // P, max(1, hkv // P)
+        chunks = [c for c in (1, 2, 3, 4, 6, 8) if Hq % c == 0 and (Hk % c == 0 or c % Hk == 0)]
+        if chunks:
+            out.append((P, b, s, hq, hkv, d, causal, rng.choice(chunks)))
+        if len(out) == n:
+            break
+    return out
+
+
+@pytest.mark.parametrize("P,b,s,hq,hkv,d,causal,n_chunks", _overlap_cases(seed=91, n=10))
+def test_random_overlap(P, b, s, hq, hkv, d, causal, n_chunks):
+    """The overlapped forward gives the unfused forward's bits for every drawn shape."""
+    need_gpu()
+    q, k, v = global_qkv(b, s, hq, hkv, d, torch.bfloat16, seed=s + n_chunks)
+    qd, kd, vd = ([t.cuda() for t in shard_seq(x, P)] for x in (q, k, v))
+    over = uly.ulysses_dist_attn_fwd_overlap(qd, kd, vd, causal, n_chunks=n_chunks)
+    plain = uly.ulysses_dist_attn_fwd(qd, kd, vd, causal, fused=False)
+    torch.cuda.synchronize()
+    device_ok()
+    for j in range(P):
+        assert bits_equal(over[j], plain[j]), f"rank {j}: overlapped != unfused"
+
+
+def _usp_cases(seed, n):
+    rng = random.Random(seed)
+    out = []
+    while len(out) < n:
+        Pu, Pr = rng.choice([1, 2, 3, 4]), rng.choice([1, 2, 3, 4])
+        P = Pu * Pr
+        d = rng.choice([64, 128])
+        if rng.random() < 0.3 and Pu > 1:
+            hkv = rng.choice([x for x in (1, 2) if Pu % x == 0 and x < Pu] or [Pu])
+            hq = Pu * rng.choice([1, 2])
+        else:
+            hkv = Pu * rng.choice([1, 2])
+            hq = hkv * rng.choice([1, 2, 4])
+        s = Pr * 128 * rng.randint(1, max(1, 768 // (128 * Pr)))  # (s/Pr) % 128 == 0
+        if s % P or hq * s * s * d > 1 << 29 or hq // hkv > 4:
+            continue
+        out.append((Pu, Pr, 1, s, hq, hkv, d, rng.random() < 0.5))
+    return out
+
+
+@pytest.mark.parametrize("Pu,Pr,b,s,hq,hkv,d,causal", _usp_cases(seed=123, n=10))
+def test_random_two_level(Pu, Pr, b, s, hq, hkv, d, causal):
+    """The two-level forward and training path: forward against the oracle's explicit ring
+    (or, with replicated K/V heads, its attention over the global tensors), bit for bit
+    against plain Ulysses where that call takes the shape; gradients against the oracle."""
+    need_gpu()
+    P = Pu * Pr
+    q, k, v = global_qkv(b, s, hq, hkv, d, torch.bfloat16, seed=s + 3 * Pu + Pr)
+    do = global_grad(b, s, hq, d, torch.bfloat16, seed=s + 1)
+    qs, ks, vs, dos = (shard_seq(x, P) for x in (q, k, v, do))
+    qd, kd, vd, dod = ([t.cuda() for t in x] for x in (qs, ks, vs, dos))
+    out = uly.ulysses_usp_attn_fwd(qd, kd, vd, causal, Pu, Pr)
+    plain = uly.ulysses_dist_attn_fwd(qd, kd, vd, causal) if hq % P == 0 and hkv % P == 0 else None
+    o, lse = uly.ulysses_usp_attn_fwd_lse(qd, kd, vd, causal, Pu, Pr)
+    grads = uly.ulysses_usp_attn_bwd(qd, kd, vd, o, dod, lse, causal, Pu, Pr)
+    torch.cuda.synchronize()
+    device_ok()
+    want = oracle.usp_fwd(qs, ks, vs, causal, Pu, Pr) if hkv % Pu == 0 else shard_seq(
+        oracle.attention(q, k, v, causal), P)
+    for j in range(P):
+        assert_close(out[j], want[j], torch.bfloat16, f"rank {j}")
+        assert bits_equal(o[j], out[j]), f"rank {j}: the forward with statistics changed the output"
+        if plain is not None:
+            assert bits_equal(out[j], plain[j]), f"rank {j}: two-level != plain Ulysses"
+    ref = [shard_seq(x, P) for x in oracle.attention_bwd(q, k, v, do, causal)]
+    for name, got, r in zip(("dq", "dk", "dv"), grads, ref):
+        for j in range(P):
+            assert_close_grad(got[j], r[j], f"{name} rank {j}")
