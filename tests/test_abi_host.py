@@ -172,3 +172,68 @@ def test_pack_unpack_argument_errors(lib):
     # 16-byte vectors, past the copy kernel's 32-bit index (the per-rank exchange checks pass)
     far_in, far_out = 1 << 48, 1 << 49  # 64 GiB each side: far apart so that they do not overlap
     assert lib.ulysses_a2a_unpack(0, 64, 1, 1 << 26, 64, 256, FP32, far_in, far_out, None) == INVALID
+
+
+def _far(kind, n):
+    """n fake, never dereferenced device addresses of one tensor kind, far from other kinds."""
+    return _arr(*[(kind << 40) + (r << 32) for r in range(n)])
+
+
+def test_empty_and_negative_sizes(lib):
+    """Every entry point rejects a zero or negative size (P, b, s, heads, d) before it touches
+    a pointer or the device; the workspace queries return 0 for them.  Each call below
+    differs from a valid configuration (P=4 or Pu=Pr=2, b=1, s=512, h_q=8, h_kv=4, d=64,
+    bf16) in one size only.  Only rejected calls are made: the addresses are fake."""
+    q, k, v, o, do, dq, dk, dv, lse = (_far(i + 1, 4) for i in range(9))
+    ws, wsn = 1 << 48, 1 << 40
+    base = [4, 1, 512, 8, 4, 64]          # P, b, s, h_q, h_kv, d
+    calls = {
+        "ulysses_local_attention": lambda a: lib.ulysses_local_attention(*a, BF16, 0, q, k, v, o, None),
+        "ulysses_dist_attn_fwd": lambda a: lib.ulysses_dist_attn_fwd(*a, BF16, 0, q, k, v, o, ws, wsn, 0, None),
+        "ulysses_dist_attn_fwd_noalloc": lambda a: lib.ulysses_dist_attn_fwd_noalloc(*a, BF16, 0, q, k, v, o, None),
+        "ulysses_local_attention_fwd_lse": lambda a: lib.ulysses_local_attention_fwd_lse(*a, BF16, 0, q, k, v, o, lse,
+                                                                                         None),
+        "ulysses_dist_attn_fwd_lse": lambda a: lib.ulysses_dist_attn_fwd_lse(*a, BF16, 0, q, k, v, o, lse, ws, wsn, 1,
+                                                                             None),
+        "ulysses_local_attention_bwd": lambda a: lib.ulysses_local_attention_bwd(*a, BF16, 0, q, k, v, o, do, lse, dq,
+                                                                                 dk, dv, ws, wsn, None),
+        "ulysses_dist_attn_bwd": lambda a: lib.ulysses_dist_attn_bwd(*a, BF16, 0, q, k, v, o, do, lse, dq, dk, dv, ws,
+                                                                     wsn, 1, None),
+        "ulysses_dist_attn_fwd_overlap": lambda a: lib.ulysses_dist_attn_fwd_overlap(*a, BF16, 0, q, k, v, o, ws, wsn,
+                                                                                     2, None, None),
+    }
+    sizes = {
+        "ulysses_dist_attn_workspace_bytes": lambda a: lib.ulysses_dist_attn_workspace_bytes(*a, BF16, 0),
+        "ulysses_attn_bwd_workspace_bytes": lambda a: lib.ulysses_attn_bwd_workspace_bytes(*a, BF16, 1, 0),
+        "ulysses_dist_attn_overlap_workspace_bytes":
+            lambda a: lib.ulysses_dist_attn_overlap_workspace_bytes(*a, BF16, 2),
+    }
+    for i in range(len(base)):
+        for bad in (0, -1):
+            a = list(base)
+            a[i] = bad
+            for name, f in calls.items():
+                assert f(a) == INVALID, f"{name} with size {i} = {bad}"
+            for name, f in sizes.items():
+                assert f(a) == 0, f"{name} with size {i} = {bad}"
+    # the exchanges and their per-process halves: P, b, s, h, d
+    ex = [2, 1, 64, 4, 16]
+    for i in range(len(ex)):
+        for bad in (0, -1):
+            a = list(ex)
+            a[i] = bad
+            for f in (lib.ulysses_a2a_seq2head, lib.ulysses_a2a_head2seq):
+                assert f(*a, FP32, q, o, None) == INVALID, f"exchange with size {i} = {bad}"
+            for f in (lib.ulysses_a2a_pack, lib.ulysses_a2a_unpack):
+                assert f(0, *a, FP32, A, B, None) == INVALID, f"pack/unpack with size {i} = {bad}"
+    # the two-level calls: Pu, Pr, b, s, h_q, h_kv, d
+    two = [2, 2, 1, 512, 8, 4, 64]
+    for i in range(len(two)):
+        for bad in (0, -1):
+            a = list(two)
+            a[i] = bad
+            assert lib.ulysses_usp_workspace_bytes(*a, BF16) == 0
+            assert lib.ulysses_usp_bwd_workspace_bytes(*a, BF16) == 0
+            assert lib.ulysses_usp_attn_fwd(*a, BF16, 0, q, k, v, o, ws, wsn, None) == INVALID
+            assert lib.ulysses_usp_attn_fwd_lse(*a, BF16, 0, q, k, v, o, lse, ws, wsn, None) == INVALID
+            assert lib.ulysses_usp_attn_bwd(*a, BF16, 0, q, k, v, o, do, lse, dq, dk, dv, ws, wsn, None) == INVALID
