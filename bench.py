@@ -16,7 +16,8 @@ e2e      = the fused forward through the public API with host buffers: per step 
            copies run on two copy streams with three device buffer sets, so the next steps'
            inputs and the previous steps' outputs move while a step computes.
 extra    = the DiT-like and GQA workloads, each in a timed region of its own after the
-           main one (attention launches and exchanges).
+           main one (attention launches and exchanges), and their training backward
+           (the fused distributed backward, per mask).
 cpu_baseline / --impl reference = the fp64 CPU oracle on a bounded sample of the workload
            (exact output rows, extrapolated to a rate).
 
@@ -58,6 +59,8 @@ DEFAULT_WORKLOAD = "long"
 DEFAULT_STEPS = {"long": 20, "gqa": 100, "dit": 2000, "usp": 10, "tiny": 400}
 # the other named workloads, measured after the main line's timed region: (workload, steps)
 EXTRAS = {"long": (("dit", 1000), ("gqa", 60))}
+# and the training backward (fused distributed backward) of these: (workload, calls per mask)
+EXTRAS_BWD = {"long": (("dit", 300), ("gqa", 30))}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -378,7 +381,53 @@ def run_gpu(args, rank, world):
             res["extra"][name] = sm
             del ops_x, ins_x
             torch.cuda.empty_cache()
+        for name, steps in EXTRAS_BWD.get(args.workload, ()):
+            res["extra"][name + "_backward"] = backward_extra(torch, uly, WORKLOADS[name], dev, steps,
+                                                              max(3, args.warmup), peaks)
+            torch.cuda.empty_cache()
     return res
+
+
+def backward_extra(torch, uly, w, dev, steps, warmup, peaks):
+    """The whole DistributedAttention backward of workload w through its fused path (both
+    exchanges in the kernels' tile addressing, as in training after the fused forward), per
+    mask: `steps` calls, each between CUDA events on the current stream.  FLOP/s count the
+    algorithmic 2.5x forward FLOPs (the five tile products S, dP, dV, dK, dQ)."""
+    from sequence_attention_seq_gb300.inputs import global_grad, seq_shards_qkv, shard_seq
+
+    P, b, s, hq, hkv, d = w["P"], w["b"], w["s"], w["h_q"], w["h_kv"], w["d"]
+    qs, ks, vs = seq_shards_qkv(P, b, s, hq, hkv, d, torch.bfloat16, seed=0, device=dev)
+    dos = shard_seq(global_grad(b, s, hq, d, torch.bfloat16, seed=1, device=dev), P)
+    grads = ([torch.empty_like(x) for x in qs], [torch.empty_like(x) for x in ks], [torch.empty_like(x) for x in vs])
+    ws = torch.empty(max(1, uly.ulysses_attn_bwd_workspace_bytes(P, b, s, hq, hkv, d, torch.bfloat16, True, True)),
+                     dtype=torch.uint8, device=dev)
+    clocks = ClockSampler(dev.index if dev.index is not None else 0)
+    out = {"workload": w["name"], "call": "ulysses_dist_attn_bwd(fused=1)", "steps": steps,
+           "flops": "algorithmic, 2.5x the forward's", "peak": peaks["bf16_tflops"]}
+    clocks.start()
+    time.sleep(0.3)
+    for causal in w["masks"]:
+        o, lse = uly.ulysses_dist_attn_fwd_lse(qs, ks, vs, causal, fused=True)
+
+        def call():
+            uly.ulysses_dist_attn_bwd(qs, ks, vs, o, dos, lse, causal, grads=grads, workspace=ws, fused=True)
+
+        for _ in range(warmup):
+            call()
+        torch.cuda.synchronize()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for e0, e1 in evs:
+            e0.record()
+            call()
+            e1.record()
+        torch.cuda.synchronize()
+        ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in evs)
+        tf = 2.5 * attn_flops(b, s, hq, d, causal) / (ms * 1e-3) / 1e12
+        out["causal" if causal else "noncausal"] = {"ms": ms, "tflops": tf, "frac": tf / peaks["bf16_tflops"]}
+    out["clocks"] = clocks.stop()
+    if uly.ulysses_device_status(clear=True) != 0:
+        raise RuntimeError("a kernel's bounded wait gave up")
+    return out
 
 
 # -------------------------------------------------------------------- CPU oracle
@@ -918,6 +967,9 @@ def main():
         cpu = cpu_baseline_obj(w, oracle_sample(w, e2e["host_in"], budget_s=12.0))
     extra = {}
     for name, sm in res["extra"].items():
+        if name.endswith("_backward"):
+            extra[name] = sm
+            continue
         ent = {"workload": sm["workload"], "steps": sm["steps"], "ms_per_step": sm["ms_per_step"],
                "per_launch_ms": sm["per_launch_ms"], "clocks": sm["clocks"]}
         for kind in ("fused", "attention", "permute"):
