@@ -268,8 +268,8 @@ uly_status ulysses_usp_attn_bwd(int Pu, int Pr, int b, int s, int h_q, int h_kv,
                                 void* const* dv_seq, void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
- * The unfused forward without any allocation by the caller or the library.  The paper has
- * no counterpart: this exists for callers that cannot call cudaMalloc -- for example an
+ * The unfused forward without any allocation by the caller or the library.  DeepSpeed-Ulysses
+ * itself has no such call: this exists for callers that cannot call cudaMalloc -- for example an
  * application whose memory pool already holds all the device memory it may use, or a
  * plugin whose host runtime gives it no allocator on its hot path.
  * Same arguments, layouts, results and errors as ulysses_dist_attn_fwd with fused == 0,
