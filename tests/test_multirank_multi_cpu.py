@@ -11,6 +11,7 @@ against) and the oracle's local attention, statistics and backward.  Each rank's
 gradients must equal the oracle's single-process Ulysses pipeline for that rank
 ("DeepSpeed-Ulysses 深度解析", section "核心设计" steps 3-5; "02 · DeepSpeed-Ulysses",
 section 5 for the backward)."""
+import datetime
 import os
 import sys
 
@@ -21,7 +22,7 @@ import torch.multiprocessing as mp
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
-def _worker(rank, world, port, shape, out):
+def _run(rank, world, port, shape):
     import torch.distributed as dist
 
     sys.path.insert(0, ROOT)
@@ -47,7 +48,7 @@ def _worker(rank, world, port, shape, out):
 
     os.environ["MASTER_ADDR"] = "127.0.0.1"
     os.environ["MASTER_PORT"] = str(port)
-    dist.init_process_group("gloo", rank=rank, world_size=world)
+    dist.init_process_group("gloo", rank=rank, world_size=world, timeout=datetime.timedelta(seconds=60))
     b, s, hq, hkv, d, causal = shape
     g = torch.Generator().manual_seed(11)
     q = torch.randn((b, s, hq, d), generator=g)
@@ -67,8 +68,16 @@ def _worker(rank, world, port, shape, out):
           "shapes": [tuple(x.shape) for x in grads] == [tuple(x.shape) for x in want_g]}
     for name, got, want in zip(("dq", "dk", "dv"), grads, want_g):
         ok[name] = torch.equal(got, want)
-    out.put((rank, ok))
     dist.destroy_process_group()
+    return ok
+
+
+def _worker(rank, world, port, shape, out):
+    # a failing rank reports at once (its peers' collectives then time out after 60 s)
+    try:
+        out.put((rank, _run(rank, world, port, shape)))
+    except Exception as e:  # noqa: BLE001
+        out.put((rank, {f"error: {e!r}": False}))
 
 
 @pytest.mark.parametrize("world,shape", [
@@ -83,7 +92,7 @@ def test_multi_process_forward_and_backward_gloo(world, shape):
     procs = [ctx.Process(target=_worker, args=(r, world, port, shape, q)) for r in range(world)]
     for p in procs:
         p.start()
-    res = sorted((q.get(timeout=300) for _ in procs), key=lambda x: x[0])
+    res = sorted((q.get(timeout=180) for _ in procs), key=lambda x: x[0])
     for p in procs:
         p.join(timeout=300)
         assert p.exitcode == 0
