@@ -33,7 +33,8 @@
 // sum of at most 256 shows that none exceeds 2^8.
 //
 // Fused mode ("DeepSpeed-Ulysses 深度解析", steps 3 and 5; "02 · DeepSpeed-Ulysses",
-// section 3, where the exchanges "can be merged"): the tiles of tokens [t0, t0+128) come
+// section 3, whose comparison table notes that the two exchanges lend themselves to being
+// combined): the tiles of tokens [t0, t0+128) come
 // straight from source rank t0 / (s/P)'s seq-layout buffer at head column gh, and the
 // output tile goes straight to that rank's seq-layout output, so the head-layout copies
 // never exist.  Requires (s/P) % 128 == 0 so no tile straddles two ranks.

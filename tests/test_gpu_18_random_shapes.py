@@ -8,7 +8,9 @@ oracle's pipeline and, where the fused kernel takes the shape ((s/P) % 128 == 0)
 forward bit for bit with the unfused one; the training cases do the same for dQ, dK and dV
 (with replicated K/V heads the two paths sum dK/dV in different orders, so there each is
 checked against the oracle instead) ("DeepSpeed-Ulysses 深度解析", section "核心设计"
-steps 3-5; "02 · DeepSpeed-Ulysses", section 5).  Sizes stay small enough for the oracle to finish each case in a few seconds."""
+steps 3-5; "02 · DeepSpeed-Ulysses", section 5).  The later tests draw fp32, overlapped and
+two-level cases the same way.  Sizes stay small enough for the oracle to finish each case
+in a few seconds."""
 import random
 
 import pytest
