@@ -478,10 +478,20 @@ def cpu_baseline_obj(w, smp):
 KERNEL_REGION_END = b"// ---------------------------------------------------------------- host side"
 
 
+def _code_only(text):
+    """C/CUDA source without its comments and blank lines: edits to comments leave it alone."""
+    import re
+
+    text = re.sub(rb"/\*.*?\*/", b"", text, flags=re.S)
+    text = re.sub(rb"//[^\n]*", b"", text)
+    return b"\n".join(line.rstrip() for line in text.split(b"\n") if line.strip())
+
+
 def kernel_source_digest():
-    """Digest of the forward attention kernel's source: attn_tc.cu up to its host-side
-    section (the kernel and its device helpers) and device_common.cuh.  The traffic figure
-    belongs to one version of that code; launchers and the backward do not change it."""
+    """Digest of the forward attention kernel's code: attn_tc.cu up to its host-side section
+    (the kernel and its device helpers) and device_common.cuh, comments removed.  The
+    traffic figure belongs to one version of that code; launchers, the backward and comment
+    edits do not change it."""
     import hashlib
 
     h = hashlib.sha256()
@@ -490,9 +500,9 @@ def kernel_source_digest():
         text = f.read()
     if KERNEL_REGION_END not in text:
         return None
-    h.update(text.split(KERNEL_REGION_END)[0])
+    h.update(_code_only(text.split(KERNEL_REGION_END)[0]))
     with open(os.path.join(csrc, "device_common.cuh"), "rb") as f:
-        h.update(f.read())
+        h.update(_code_only(f.read()))
     return h.hexdigest()
 
 
