@@ -358,6 +358,7 @@ def run_gpu(args, rank, world):
     clocks = ClockSampler(dev.index if dev.index is not None else 0)
     total_ms, per_op, clk = time_ops(torch, uly, ops, args.steps, args.warmup, dev, stream, clocks, world)
     res = dict(total_ms=total_ms, clocks=clk, per_op={k: statistics.mean(v) for k, v in per_op.items()},
+               per_op_median={k: statistics.median(v) for k, v in per_op.items()},
                step_flops=sum(op[3] for op in ops), n_launches=len(ops) * args.steps,
                summary=summarize(ops, per_op, args.steps, peaks), fused_ok=fused_ok)
     del ops
@@ -996,7 +997,8 @@ def main():
                      "frac_of_sustained": (achieved / peaks["bf16_tflops_sustained"] if bound == "tensor" else None),
                      "peak_source": peak_note, "traffic": traffic,
                      "flops_per_launch": attn_flops(w["b"], w["s"], w["h_q"], w["d"], w["masks"][-1]),
-                     "launch_ms": summ[main_kind]["ms_per_step"] / max(1, len(w["masks"]))},
+                     "launch_ms": summ[main_kind]["ms_per_step"] / max(1, len(w["masks"])),
+                     "launch_ms_median": {lab: res["per_op_median"][lab] for lab in summ[main_kind]["per_launch_ms"]}},
         "attention_unfused": summ.get("attention") if main_kind == "fused" else None,
         "permute": ({"achieved": summ["permute"]["gbs"], "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": summ["permute"]["frac"], "bytes_per_step": summ["permute"]["bytes_per_step"],
