@@ -129,10 +129,14 @@ class _KernelsMulti(torch.autograd.Function):
 
     @staticmethod
     def forward(ctx, causal, group, q, k, v):
-        from .multi import ulysses_dist_attn_fwd_lse_multi
+        from .multi import ulysses_dist_attn_fwd_lse_multi, ulysses_dist_attn_fwd_multi
 
-        o, saved = ulysses_dist_attn_fwd_lse_multi(q.contiguous(), k.contiguous(), v.contiguous(), causal, group)
         ctx.causal, ctx.group = causal, group
+        q, k, v = q.contiguous(), k.contiguous(), v.contiguous()
+        ctx.trainable = q.dtype == torch.bfloat16
+        if not ctx.trainable:  # the fp32 kernels have no backward
+            return ulysses_dist_attn_fwd_multi(q, k, v, causal, group)
+        o, saved = ulysses_dist_attn_fwd_lse_multi(q, k, v, causal, group)
         ctx.save_for_backward(*saved)
         return o
 
@@ -140,6 +144,8 @@ class _KernelsMulti(torch.autograd.Function):
     def backward(ctx, do):
         from .multi import ulysses_dist_attn_bwd_multi
 
+        if not ctx.trainable:
+            raise RuntimeError("DistributedAttention: the library's backward kernels are bf16 only")
         dq, dk, dv = ulysses_dist_attn_bwd_multi(do.contiguous(), ctx.saved_tensors, ctx.causal, ctx.group)
         return None, None, dq, dk, dv
 

@@ -142,6 +142,13 @@ def test_module_over_a_process_group_of_one_rank():
             assert bits_equal(o1, o2[0])
             for a, c in zip(g1, g2):
                 assert bits_equal(a, c)
+        # fp32: the forward only (the fp32 kernels have no backward)
+        q, k, v = global_qkv(1, 128, 2, 2, 64, torch.float32, seed=10)
+        qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+        o1 = DistributedAttention(group=dist.group.WORLD, causal=True)(qd, kd, vd)
+        o2 = uly.ulysses_dist_attn_fwd([qd], [kd], [vd], True)
+        torch.cuda.synchronize()
+        assert bits_equal(o1, o2[0])
     finally:
         dist.destroy_process_group()
     device_ok()
