@@ -9,7 +9,7 @@ import torch
 import torch.nn.functional as F
 
 import oracle
-from sequence_attention_seq_gb300.inputs import global_qkv, random_bits, shard_seq
+from sequence_attention_seq_gb300.inputs import global_qkv, shard_seq
 
 
 def _autograd(q, k, v, do, causal):
