@@ -341,6 +341,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         int n = 0;                   // ring loads issued so far (slot n % kSlots)
         int quse[2] = {0, 0};        // Q_t loads issued so far
         bool ok = true;
+        // K/V tiles are read by every item of their head: kept in L2 ahead of the Q tiles,
+        // which one item reads once
+        const uint64_t keep = l2_policy_evict_last(), once = l2_policy_evict_first();
         for (int k = 0; ok; ++k) {
             const int w = item_index(p, k);
             if (w < 0) break;
@@ -353,8 +356,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
                 mbar_arrive_expect_tx_warp(&bars[B_Q_FULL + t], L::kTile);
 #pragma unroll
                 for (int c = 0; c < D / 64; ++c)
-                    tma_load_4d_warp(sbase + L::offQ + t * L::kTile + c * kSlab, &p.mq[qc.map], &bars[B_Q_FULL + t],
-                                     c * 64, it.head, qc.row, it.bb);
+                    tma_load_4d_warp_hint(sbase + L::offQ + t * L::kTile + c * kSlab, &p.mq[qc.map],
+                                          &bars[B_Q_FULL + t], c * 64, it.head, qc.row, it.bb, once);
                 ++quse[t];
             }
             const int n_max = it.n0 > it.n1 ? it.n0 : it.n1;
@@ -367,8 +370,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
                 mbar_arrive_expect_tx_warp(&bars[B_KV_FULL + slot], L::kTile);
 #pragma unroll
                 for (int c = 0; c < D / 64; ++c)
-                    tma_load_4d_warp(sbase + L::offKV + slot * L::kTile + c * kSlab, map, &bars[B_KV_FULL + slot],
-                                     c * 64, it.kvh, kc.row, it.bb);
+                    tma_load_4d_warp_hint(sbase + L::offKV + slot * L::kTile + c * kSlab, map,
+                                          &bars[B_KV_FULL + slot], c * 64, it.kvh, kc.row, it.bb, keep);
             }
         }
         if (!ok) {  // every copy issued must land before shared memory goes away

@@ -86,6 +86,30 @@ __device__ __forceinline__ void tma_load_4d_warp(uint32_t dst_smem, const CUtens
         : "memory");
 }
 
+// As tma_load_4d_warp, with an L2 eviction-priority policy for the loaded lines (from
+// l2_policy_evict_last / l2_policy_evict_first).
+__device__ __forceinline__ void tma_load_4d_warp_hint(uint32_t dst_smem, const CUtensorMap* map, uint64_t* bar,
+                                                      int c0, int c1, int c2, int c3, uint64_t policy) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+        "@e cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4, %5}], [%6], %7;\n\t}" ::"r"(dst_smem),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_addr(bar)), "l"(policy)
+        : "memory");
+}
+
+// L2 cache policies for the hinted loads: keep the lines (evict last) or let them go first.
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
 // ------------------------------------------------------------------------------ tcgen05
 __device__ __forceinline__ void tmem_alloc(uint32_t* slot_smem, uint32_t ncols) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(slot_smem)),
